@@ -1,0 +1,276 @@
+/*
+ * sparsekv.h -- C ABI of libsparsekv.so, sparse long-context decode attention
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * One decode step of one attention layer, for a batch of requests:
+ *   1. indexer score of every cached token (int4 rank-64 key sketch, fp32
+ *      sketch, or bf16 indexer keys pooled by blocks of 4),
+ *   2. deterministic top-k, one pick shared by every KV head of the layer,
+ *   3. union with the sink and recent-tail tokens (or block expansion),
+ *   4. exact attention over only the selected rows.
+ * Sources (page title, section):
+ *   [P1] "8 agents x 250K context on two 3090s: sparse KV decode with a
+ *        rank-64 key sketch and a host-RAM tier", "What shipped".
+ *   [P2] "vLLM's Hybrid HiSparse Triples Concurrent Requests on Million-Token
+ *        Contexts", "Three residency states, one block pool".
+ *   [P3] "You can offload most of Qwen3.8-Flash-Next's KV cache to RAM with
+ *        little decode slowdown".
+ *   [P4] "3.14M Context on 3x 3090: The Power of an Architecture That Puts KV
+ *        Cache in Host RAM", sections "Why", "No Need to Rewrite the Kernel",
+ *        "What Needs to Stay in VRAM".
+ *
+ * General rules for every entry point:
+ *  - Pointers are DEVICE pointers unless stated otherwise (for host-tier data
+ *    pass the device alias returned by skv_host_register).  The caller owns
+ *    every buffer; the library allocates nothing and never synchronises.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream) and contains no host-side decision that depends on device
+ *    data, so a sequence of calls can be captured in a CUDA graph ([P2]: the
+ *    decode path stays graph-capturable because nothing waits on a CPU-side
+ *    decision; [P4]: capture survived host-resident KV).
+ *  - Return value: SKV_OK, or an SKV_E* code.  Argument errors are detected on
+ *    the host before anything is launched.  SKV_ECUDA means a launch failed
+ *    (the CUDA error is left for cudaGetLastError-style inspection by the
+ *    caller's runtime).
+ *  - Errors that only the device can see (a NaN score, a row index out of
+ *    range, a bounded wait that gave up) are OR-ed into the caller's int32
+ *    `dev_status` word (SKV_DEV_* bits) when it is non-NULL; the kernel skips
+ *    the offending access and carries on.  The caller reads the word after
+ *    synchronising.  No kernel traps.
+ *  - Scratch memory ("workspace") is caller-provided, sized by the matching
+ *    *_workspace_size call, must be zero-filled once before its first use,
+ *    and is left zero-filled by every call that completes.  Calls that share a
+ *    workspace must not overlap on the GPU.
+ *  - bf16 / fp16 arguments are passed as uint16_t bit patterns.
+ */
+#ifndef SPARSEKV_H
+#define SPARSEKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes --------------------------------------------------------- */
+#define SKV_OK 0
+#define SKV_EINVAL 1        /* bad argument (null pointer, size, alignment)    */
+#define SKV_EUNSUPPORTED 2  /* valid request this build does not implement     */
+#define SKV_ECUDA 3         /* a CUDA runtime call or launch failed            */
+#define SKV_ENOMEM 4        /* caller buffer too small                         */
+
+/* ---- device status bits (OR-ed into *dev_status) -------------------------- */
+#define SKV_DEV_NAN 1u       /* a score was NaN                                 */
+#define SKV_DEV_RANGE 2u     /* a row / token index was out of range            */
+#define SKV_DEV_TIMEOUT 4u   /* a bounded device-side wait gave up              */
+#define SKV_DEV_COUNT 8u     /* a selection produced an unexpected row count    */
+
+/* ---- enumerations ---------------------------------------------------------- */
+/* Indexer modes of skv_index_score. */
+#define SKV_SCORE_SKETCH_INT4 0   /* int4 key sketch x int8 folded query, int32 */
+#define SKV_SCORE_SKETCH_F32 1    /* fp32 key sketch x fp32 folded query        */
+#define SKV_SCORE_POOLED_BF16 2   /* bf16 pooled indexer keys x bf16 query      */
+
+/* KV row encodings of skv_sparse_attend_decode. */
+#define SKV_KV_BF16 0   /* bf16 K and V rows                                      */
+#define SKV_KV_INT8 1   /* int8 K and V rows, one fp16 scale per (row, head) each  */
+
+/* Returns the ABI version (incremented on any incompatible change). */
+int skv_version(void);
+
+/* Short English description of a status code (static storage). */
+const char *skv_status_string(int status);
+
+/* Number of streaming multiprocessors of the current device (0 on error). */
+int skv_device_sm_count(void);
+
+/* ========================================================================== */
+/* a1: key sketch ([P1] "What shipped": each token is scored through a rank-64 */
+/* key sketch held as int4; the basis is frozen, fitted once offline).        */
+/* ========================================================================== */
+/*
+ * For every input token i and KV head h:
+ *   s[j] = sum_{x=0}^{d-1} basis[x*r + j] * key[i][h][x]        (fp32)
+ * With c != NULL the sketch is stored int4: code = clamp(rint(s[j] / c[h*r+j]),
+ * -8, 7) (round half to even, IEEE division; c == 0 gives code 0), two codes
+ * per byte, dim 2b in the low nibble and dim 2b+1 in the high nibble, heads
+ * consecutive: an output row is Hkv*r/2 bytes.  With c == NULL the fp32 sketch
+ * itself is stored: an output row is Hkv*r floats.
+ *   keys     bf16 [n_tok][Hkv][d]
+ *   basis    fp32 [d][r]  (column j is basis vector j)
+ *   c        fp32 [Hkv][r] quantiser step, or NULL for the fp32 sketch
+ *   out_rows int64 [n_tok] destination row of each token in `out`, or NULL
+ *            (token i -> row i).  Used to append decode tokens in place.
+ *   out      u8 [rows][Hkv*r/2] (int4) or fp32 [rows][Hkv*r]
+ * Constraints: r == 64, d a multiple of 8 and <= 512, n_tok >= 0.
+ * Rounding: the projection's summation order is the kernel's; an int4 code may
+ * differ by one from a different summation only where s/c lies within a few
+ * ulps of a half-integer.
+ */
+int skv_sketch_project(const uint16_t *keys, int64_t n_tok, int Hkv, int d, int r,
+                       const float *basis, const float *c, const int64_t *out_rows,
+                       void *out, void *stream);
+
+/* ========================================================================== */
+/* a2: folded query ([P1] "What shipped": one pick per layer is shared by all */
+/* four KV heads; read as the sum of the per-head sketch scores, with the     */
+/* query heads of a KV head's group (kv_head = g / (Hq/Hkv)) summed).         */
+/* ========================================================================== */
+/*
+ * For request b, KV head h, sketch dim j:
+ *   qp[b][h*r + j] = c[h*r+j] * sum_{g in group h} sum_x basis[x*r+j] * q[b][g][x]
+ * (c omitted when NULL).  int8 mode (c != NULL): sigma[b] = max_m |qp[b][m]| /
+ * 127, q8 = clamp(rint(qp / sigma), -127, 127), sigma == 0 gives zeros; out is
+ * int8 [B][Hkv*r] and sigma_out fp32 [B] (may be NULL).  fp32 mode (c == NULL):
+ * out is fp32 [B][Hkv*r] and sigma_out is unused.
+ *   q     bf16 [B][Hq][d]
+ * Constraints: r == 64, Hq % Hkv == 0, Hkv*r <= 1024, d <= 512.
+ */
+int skv_sketch_query(const uint16_t *q, int B, int Hq, int Hkv, int d, int r,
+                     const float *basis, const float *c, void *out, float *sigma_out,
+                     void *stream);
+
+/* ========================================================================== */
+/* a2': pooled indexer keys ([P3]: indexer keys compressed by ratio 4; [P4]   */
+/* "What Needs to Stay in VRAM": keys pooled per block, kept in HBM).         */
+/* ========================================================================== */
+/*
+ * pooled[b][blk][x] = bf16_rne( (((k0 + k1) + k2) + k3) / 4 ) with k_u =
+ * keys[b][4*blk + u][x] in fp32, for blk in [first_block, first_block +
+ * n_blocks) of every request b.  The caller passes only complete blocks.
+ *   keys    bf16 [B][t_cap][D]       (t_cap tokens of capacity per request)
+ *   pooled  bf16 [B][t_cap/4][D]
+ * Constraints: ratio == 4, D a multiple of 8, first_block >= 0, and
+ * 4*(first_block + n_blocks) <= t_cap.  The result is bit-exact.
+ */
+int skv_pool_keys(const uint16_t *keys, int B, int64_t t_cap, int D, int ratio,
+                  int64_t first_block, int64_t n_blocks, uint16_t *pooled, void *stream);
+
+/* ========================================================================== */
+/* a3: indexer scores ([P1]: score every token through the sketch each decode */
+/* step; [P4] "What Needs to Stay in VRAM": the indexer scores all blocks at  */
+/* every step -- the only read that grows with the context).                  */
+/* ========================================================================== */
+/*
+ * Candidates of request b (T = lengths[b]):
+ *   sketch modes: tokens t in [S, T - W)  (sinks and tail do not compete);
+ *   pooled mode : complete blocks blk in [0, T / ratio).
+ * For each candidate, in the same row index space as `keys`:
+ *   SKETCH_INT4 : score = sum_m q8[b][m] * code(t, m)   (exact int32)
+ *   SKETCH_F32  : score = sum_m qp[b][m] * s[t][m]      (fp32)
+ *   POOLED_BF16 : score = sum_x q_idx[b][x] * pooled[blk][x]  (fp32 accumulate)
+ * and order_keys[b][t] = order key of the score: an unsigned 32-bit value
+ * whose order is the score's order (int32: sign bit flipped; fp32: -0 taken
+ * as +0, negative values bit-inverted, others with the sign bit set).  Entries
+ * of non-candidates are not written.  A NaN fp32 score sets SKV_DEV_NAN.
+ *   query  int8 [B][width] | fp32 [B][width] | bf16 [B][width]
+ *   keys   u8 [B][n_cap][width/2] | fp32 [B][n_cap][width] | bf16 [B][n_cap][width]
+ *   order_keys  u32 [B][n_cap]
+ *   raw_scores  int32 (INT4) or fp32 (other modes) [B][n_cap], or NULL
+ * width: Hkv*r for the sketch modes, the indexer dim for pooled mode.
+ * Constraints: INT4 width in {128, 256, 512}; F32 width a multiple of 4 and
+ * <= 1024; POOLED width == 128; ratio == 1 for sketch modes, 4 for pooled;
+ * lengths[b] <= n_cap (sketch) or n_cap*ratio (pooled) (else SKV_DEV_RANGE
+ * and the request is clamped).  Keys rows must be 16-byte aligned.
+ */
+int skv_index_score(int mode, int B, int width, const void *query, const void *keys,
+                    int64_t n_cap, const int32_t *lengths, int ratio, int S, int W,
+                    uint32_t *order_keys, void *raw_scores, int32_t *dev_status,
+                    void *stream);
+
+/* ========================================================================== */
+/* a4: deterministic top-k with sink/tail union ([P1]: top 2048 + 64 sinks +  */
+/* last 1024 tokens, deterministic radix select) and the pooled expansion     */
+/* ([P4] "Why": sparse once the context exceeds 4*block_topk + 3 tokens).     */
+/* ========================================================================== */
+/*
+ * For request b with T = lengths[b]:
+ *  sketch (ratio == 1): if T <= S + W + k every token 0..T-1 is selected
+ *    (dense fallback); otherwise the k best candidates of [S, T - W) by (order
+ *    key descending, index ascending), and idx[b] = [0..S) ++ picks ascending
+ *    ++ [T-W..T), count[b] = S + k + W.
+ *  pooled (ratio > 1, S = W = 0): if T <= ratio*k + ratio - 1 every token;
+ *    otherwise the k best complete blocks, each expanded to its `ratio` tokens
+ *    in ascending order, then the tokens of the incomplete last block;
+ *    count[b] = ratio*k + T % ratio.
+ *   order_keys u32 [B][n_cap] (skv_index_score output; n_cap in candidates)
+ *   idx        int32 [B][max_rows]   count int32 [B]
+ *   workspace  skv_topk_workspace_size(B) bytes (zero-filled before first use)
+ * Constraints: k >= 1; max_rows >= S + k + W (sketch) or ratio*k + ratio - 1
+ * (pooled); B <= 4096.  The result is unique and bit-exact.
+ */
+size_t skv_topk_workspace_size(int B);
+int skv_topk_select(int B, const uint32_t *order_keys, int64_t n_cap,
+                    const int32_t *lengths, int k, int S, int W, int ratio,
+                    int32_t *idx, int max_rows, int32_t *count, void *workspace,
+                    size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+/* ========================================================================== */
+/* KV row encoding (write path).                                               */
+/* ========================================================================== */
+/*
+ * int8 rows with one fp16 scale per (row, head): scale = fp16_rne(max|x| /
+ * 127) (fp32 division), code = clamp(rint(x / scale), -127, 127); a zero scale
+ * gives zero codes.  Bit-exact.
+ *   x          bf16 [n_rows][Hkv][d]
+ *   out_rows   int64 [n_rows] destination row, or NULL (identity)
+ *   q          int8 [rows][Hkv][d]     scale  fp16 [rows][Hkv]
+ * Constraints: d a multiple of 8, <= 1024.
+ */
+int skv_quantize_int8_rows(const uint16_t *x, int64_t n_rows, int Hkv, int d,
+                           const int64_t *out_rows, int8_t *q, uint16_t *scale,
+                           void *stream);
+
+/* ========================================================================== */
+/* a6: exact attention over the selected rows ([P1]: exact int8 attention on  */
+/* the picked tokens; [P4] "No Need to Rewrite the Kernel": each row is found */
+/* by adding an offset to the base, layout [token][kv_head][dim]).            */
+/* ========================================================================== */
+/*
+ * For request b, query head g (KV head h = g / (Hq/Hkv)) and the count[b]
+ * selected rows i with physical row p_i = b*req_row_stride + rows[b][i]:
+ *   logit_i = softmax_scale * sum_x q[b][g][x] * K(p_i, h, x)
+ *   out[b][g][:] = sum_i softmax(logit)_i * V(p_i, h, :)
+ * K(p, h, x) = k_pool[(p*Hkv + h)*d + x] (bf16), or int8 code times
+ * k_scale[p*Hkv + h] (fp16) for SKV_KV_INT8; V likewise with v_pool/v_scale.
+ * The split-K partial results are combined in a fixed order, so the output is
+ * deterministic.  count[b] == 0 gives a zero output.
+ *   q        bf16 [B][Hq][d]
+ *   out      fp32 [B][Hq][d]
+ *   workspace  skv_attend_workspace_size(...) bytes
+ *   n_pool_rows  rows in the pools; a physical row outside [0, n_pool_rows)
+ *            is skipped and sets SKV_DEV_RANGE
+ * Constraints: d == 256, Hq % Hkv == 0, 1 <= max_rows, pools 16-byte aligned.
+ * Accuracy: logits accumulate exact products in fp32; the probabilities are
+ * rounded to fp16 (int8 rows) or split into two bf16 terms (bf16 rows) for
+ * the tensor-core P.V product; max abs error well below 2e-3 for
+ * unit-variance values.
+ */
+size_t skv_attend_workspace_size(int B, int Hq, int Hkv, int d, int max_rows);
+int skv_sparse_attend_decode(int kv_kind, int B, int Hq, int Hkv, int d,
+                             const uint16_t *q, const void *k_pool, const void *v_pool,
+                             const uint16_t *k_scale, const uint16_t *v_scale,
+                             int64_t req_row_stride, int64_t n_pool_rows,
+                             const int32_t *rows, int max_rows, const int32_t *count,
+                             float softmax_scale, float *out, void *workspace,
+                             size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+/* ========================================================================== */
+/* Host tier ([P4] "No Need to Rewrite the Kernel": allocate with anonymous    */
+/* mmap, cudaHostRegister(ptr, n, PORTABLE | MAPPED), use the device pointer). */
+/* ========================================================================== */
+/*
+ * Page-locks `bytes` of existing host memory at `host` (HOST pointer, owned by
+ * the caller) for every device and returns in *dev_alias the device pointer
+ * through which kernels read it zero-copy.  Synchronous; not for the hot path.
+ */
+int skv_host_register(void *host, size_t bytes, void **dev_alias);
+/* Undoes skv_host_register.  The caller ensures no kernel still reads it. */
+int skv_host_unregister(void *host);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPARSEKV_H */

@@ -1,0 +1,194 @@
+"""Python binding of libsparsekv.so (sparse long-context decode on GB300).
+
+Argument marshalling only: every function passes tensor pointers, sizes and
+the current CUDA stream to the C ABI declared in ``include/sparsekv.h`` and
+raises ``SkvError`` on a non-zero status.  All computation runs in the CUDA
+kernels of the library; there is no fallback.  If the library has not been
+built, the first call raises.
+
+bf16 tensors are passed as torch.bfloat16; fp16 scales as torch.float16.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libsparsekv.so")
+
+SKETCH_INT4, SKETCH_F32, POOLED_BF16 = 0, 1, 2
+KV_BF16, KV_INT8 = 0, 1
+DEV_NAN, DEV_RANGE, DEV_TIMEOUT, DEV_COUNT = 1, 2, 4, 8
+
+_lock = threading.Lock()
+_lib = None
+
+
+class SkvError(RuntimeError):
+    def __init__(self, name, status):
+        msg = _load().skv_status_string(status).decode()
+        super().__init__(f"{name} failed: status {status} ({msg})")
+        self.status = status
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                                   "(nvcc, sm_103a); there is no CPU fallback")
+            lib = ctypes.CDLL(LIB_PATH)
+            P, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+            sig = {
+                "skv_version": ([], i32),
+                "skv_status_string": ([i32], ctypes.c_char_p),
+                "skv_device_sm_count": ([], i32),
+                "skv_sketch_project": ([P, i64, i32, i32, i32, P, P, P, P, P], i32),
+                "skv_sketch_query": ([P, i32, i32, i32, i32, i32, P, P, P, P, P], i32),
+                "skv_pool_keys": ([P, i32, i64, i32, i32, i64, i64, P, P], i32),
+                "skv_index_score": ([i32, i32, i32, P, P, i64, P, i32, i32, i32, P, P, P, P], i32),
+                "skv_topk_workspace_size": ([i32], sz),
+                "skv_topk_select": ([i32, P, i64, P, i32, i32, i32, i32, P, i32, P, P, sz, P, P], i32),
+                "skv_quantize_int8_rows": ([P, i64, i32, i32, P, P, P, P], i32),
+                "skv_attend_workspace_size": ([i32, i32, i32, i32, i32], sz),
+                "skv_sparse_attend_decode": ([i32, i32, i32, i32, i32, P, P, P, P, P, i64, i64, P, i32, P,
+                                              f32, P, P, sz, P, P], i32),
+                "skv_host_register": ([P, sz, ctypes.POINTER(ctypes.c_void_p)], i32),
+                "skv_host_unregister": ([P], i32),
+            }
+            for name, (args, res) in sig.items():
+                fn = getattr(lib, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = lib
+    return _lib
+
+
+def lib():
+    """The loaded ctypes library (raises if it was not built)."""
+    return _load()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(name, status):
+    if status != 0:
+        raise SkvError(name, status)
+
+
+def version() -> int:
+    return int(_load().skv_version())
+
+
+def sm_count() -> int:
+    return int(_load().skv_device_sm_count())
+
+
+# ---- a1 / a2 / a2' ----------------------------------------------------------
+
+def sketch_project(keys, basis, c, out, out_rows=None, stream=None):
+    """keys bf16 [n][Hkv][d]; basis fp32 [d][r]; c fp32 [Hkv][r] or None; out u8/fp32."""
+    n, Hkv, d = keys.shape
+    r = basis.shape[1]
+    _check("skv_sketch_project", _load().skv_sketch_project(
+        _ptr(keys), n, Hkv, d, r, _ptr(basis), _ptr(c), _ptr(out_rows), _ptr(out), _stream(stream)))
+    return out
+
+
+def sketch_query(q, Hkv, basis, c, out, sigma=None, stream=None):
+    """q bf16 [B][Hq][d] -> out int8 (c given) or fp32 (c None) [B][Hkv*r]."""
+    B, Hq, d = q.shape
+    r = basis.shape[1]
+    _check("skv_sketch_query", _load().skv_sketch_query(
+        _ptr(q), B, Hq, Hkv, d, r, _ptr(basis), _ptr(c), _ptr(out), _ptr(sigma), _stream(stream)))
+    return out
+
+
+def pool_keys(keys, pooled, first_block, n_blocks, ratio=4, stream=None):
+    """keys bf16 [B][t_cap][D] -> pooled bf16 [B][t_cap/4][D] for the given blocks."""
+    B, t_cap, D = keys.shape
+    _check("skv_pool_keys", _load().skv_pool_keys(
+        _ptr(keys), B, t_cap, D, ratio, int(first_block), int(n_blocks), _ptr(pooled), _stream(stream)))
+    return pooled
+
+
+# ---- a3 / a4 ----------------------------------------------------------------
+
+def index_score(mode, query, keys, lengths, order_keys, S=0, W=0, ratio=1, raw=None, status=None,
+                stream=None):
+    B, width = query.shape[0], query.shape[1]
+    n_cap = keys.shape[1]
+    _check("skv_index_score", _load().skv_index_score(
+        mode, B, width, _ptr(query), _ptr(keys), n_cap, _ptr(lengths), ratio, S, W, _ptr(order_keys),
+        _ptr(raw), _ptr(status), _stream(stream)))
+    return order_keys
+
+
+def topk_workspace_size(B) -> int:
+    return int(_load().skv_topk_workspace_size(B))
+
+
+def topk_select(order_keys, lengths, k, idx, count, workspace, S=0, W=0, ratio=1, status=None,
+                stream=None):
+    B, n_cap = order_keys.shape
+    _check("skv_topk_select", _load().skv_topk_select(
+        B, _ptr(order_keys), n_cap, _ptr(lengths), k, S, W, ratio, _ptr(idx), idx.shape[1], _ptr(count),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream)))
+    return idx, count
+
+
+# ---- row encodings ------------------------------------------------------------
+
+def quantize_int8_rows(x, q, scale, out_rows=None, stream=None):
+    """x bf16 [n][Hkv][d] -> q int8 [rows][Hkv][d], scale fp16 [rows][Hkv]."""
+    n, Hkv, d = x.shape
+    _check("skv_quantize_int8_rows", _load().skv_quantize_int8_rows(
+        _ptr(x), n, Hkv, d, _ptr(out_rows), _ptr(q), _ptr(scale), _stream(stream)))
+    return q, scale
+
+
+# ---- a6 -------------------------------------------------------------------------
+
+def attend_workspace_size(B, Hq, Hkv, d, max_rows) -> int:
+    return int(_load().skv_attend_workspace_size(B, Hq, Hkv, d, max_rows))
+
+
+def sparse_attend_decode(kv_kind, q, k_pool, v_pool, rows, count, softmax_scale, out, workspace,
+                         Hkv, k_scale=None, v_scale=None, req_row_stride=0, n_pool_rows=None,
+                         status=None, stream=None):
+    """q bf16 [B][Hq][d]; pools [n_rows][Hkv][d] (bf16 or int8); rows int32 [B][max_rows]."""
+    B, Hq, d = q.shape
+    if n_pool_rows is None:
+        n_pool_rows = k_pool.shape[0]
+    _check("skv_sparse_attend_decode", _load().skv_sparse_attend_decode(
+        kv_kind, B, Hq, Hkv, d, _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_scale), _ptr(v_scale),
+        int(req_row_stride), int(n_pool_rows), _ptr(rows), rows.shape[1], _ptr(count), float(softmax_scale),
+        _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(status),
+        _stream(stream)))
+    return out
+
+
+# ---- host tier -------------------------------------------------------------------
+
+def host_register(host_ptr: int, nbytes: int) -> int:
+    """Page-lock existing host memory and return its device alias (an int)."""
+    alias = ctypes.c_void_p()
+    _check("skv_host_register", _load().skv_host_register(ctypes.c_void_p(host_ptr), nbytes,
+                                                          ctypes.byref(alias)))
+    return int(alias.value)
+
+
+def host_unregister(host_ptr: int) -> None:
+    _check("skv_host_unregister", _load().skv_host_unregister(ctypes.c_void_p(host_ptr)))

@@ -1,0 +1,245 @@
+// sketch.cu -- key sketch (a1), folded query (a2) and int8 row encoding.
+//
+// [P1] "8 agents x 250K context on two 3090s ...", "What shipped": every
+// token is scored through a rank-64 key sketch stored int4, computed on a
+// frozen basis; one pick per layer is shared by all KV heads.
+#include "common.cuh"
+
+namespace skv {
+namespace {
+
+constexpr int kRank = 64;
+constexpr int kProjThreads = 256;
+constexpr int kMaxD = 512;
+
+// One warp per (token, head): lane j computes sketch dims 2j and 2j+1.
+__global__ __launch_bounds__(kProjThreads) void sketch_project_kernel(
+    const uint16_t* __restrict__ keys, int64_t n_tok, int Hkv, int d,
+    const float* __restrict__ basis, const float* __restrict__ c,
+    const int64_t* __restrict__ out_rows, uint8_t* __restrict__ out4,
+    float* __restrict__ out32) {
+  extern __shared__ float smem[];
+  float* P = smem;                                   // [d][64]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nw = blockDim.x >> 5;
+  float* krow = smem + d * kRank + warp * d;         // [d] per warp
+  for (int i = threadIdx.x; i < d * kRank / 4; i += blockDim.x)
+    reinterpret_cast<float4*>(P)[i] = reinterpret_cast<const float4*>(basis)[i];
+  __syncthreads();
+  const int j0 = 2 * lane;
+  float c0 = 0.f, c1 = 0.f;
+  const int64_t total = n_tok * Hkv;
+  for (int64_t item = static_cast<int64_t>(blockIdx.x) * nw + warp; item < total;
+       item += static_cast<int64_t>(gridDim.x) * nw) {
+    const int64_t t = item / Hkv;
+    const int h = static_cast<int>(item % Hkv);
+    const uint16_t* k = keys + item * d;
+    for (int x8 = lane; x8 < d / 8; x8 += 32) {
+      uint4 v = *reinterpret_cast<const uint4*>(k + 8 * x8);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int e = 0; e < 4; e++) {
+        krow[8 * x8 + 2 * e] = __uint_as_float(w[e] << 16);
+        krow[8 * x8 + 2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+      }
+    }
+    __syncwarp();
+    float s0 = 0.f, s1 = 0.f;
+    for (int x = 0; x < d; x++) {
+      const float kx = krow[x];
+      const float2 p = *reinterpret_cast<const float2*>(P + x * kRank + j0);
+      s0 = fmaf(p.x, kx, s0);
+      s1 = fmaf(p.y, kx, s1);
+    }
+    __syncwarp();
+    const int64_t row = out_rows ? out_rows[t] : t;
+    if (c) {
+      c0 = c[h * kRank + j0];
+      c1 = c[h * kRank + j0 + 1];
+      const int q0 = (c0 != 0.f) ? rint_clamp(__fdiv_rn(s0, c0), -8, 7) : 0;
+      const int q1 = (c1 != 0.f) ? rint_clamp(__fdiv_rn(s1, c1), -8, 7) : 0;
+      out4[row * (Hkv * kRank / 2) + h * (kRank / 2) + lane] =
+          static_cast<uint8_t>((q0 & 15) | ((q1 & 15) << 4));
+    } else {
+      *reinterpret_cast<float2*>(out32 + (row * Hkv + h) * kRank + j0) = make_float2(s0, s1);
+    }
+  }
+}
+
+constexpr int kQueryThreads = 512;
+
+// One CTA per request.  y[g][j] = basis[:, j] . q[g]; qp[h][j] = c[h][j] *
+// sum over the group's heads (ascending); int8 quantisation with one scale per
+// request.
+__global__ __launch_bounds__(kQueryThreads) void sketch_query_kernel(
+    const uint16_t* __restrict__ q, int Hq, int Hkv, int d, const float* __restrict__ basis,
+    const float* __restrict__ c, int8_t* __restrict__ q8, float* __restrict__ qf32,
+    float* __restrict__ sigma_out) {
+  extern __shared__ float smem[];
+  float* P = smem;                     // [d][64]
+  float* qs = P + d * kRank;           // [Hq][d]
+  float* y = qs + Hq * d;              // [Hq][64]
+  float* qp = y + Hq * kRank;          // [Hkv][64]
+  __shared__ float red[32];
+  const int b = blockIdx.x;
+  const int G = Hq / Hkv;
+  for (int i = threadIdx.x; i < d * kRank / 4; i += blockDim.x)
+    reinterpret_cast<float4*>(P)[i] = reinterpret_cast<const float4*>(basis)[i];
+  const uint16_t* qb = q + static_cast<int64_t>(b) * Hq * d;
+  for (int i = threadIdx.x; i < Hq * d; i += blockDim.x) qs[i] = bf16_bits_to_f32(qb[i]);
+  __syncthreads();
+  for (int o = threadIdx.x; o < Hq * kRank; o += blockDim.x) {
+    const int g = o / kRank, j = o % kRank;
+    const float* qg = qs + g * d;
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    int x = 0;
+    for (; x + 3 < d; x += 4) {
+      a0 = fmaf(P[x * kRank + j], qg[x], a0);
+      a1 = fmaf(P[(x + 1) * kRank + j], qg[x + 1], a1);
+      a2 = fmaf(P[(x + 2) * kRank + j], qg[x + 2], a2);
+      a3 = fmaf(P[(x + 3) * kRank + j], qg[x + 3], a3);
+    }
+    for (; x < d; x++) a0 = fmaf(P[x * kRank + j], qg[x], a0);
+    y[o] = (a0 + a1) + (a2 + a3);
+  }
+  __syncthreads();
+  const int width = Hkv * kRank;
+  float amax = 0.f;
+  for (int m = threadIdx.x; m < width; m += blockDim.x) {
+    const int h = m / kRank, j = m % kRank;
+    float acc = 0.f;
+    for (int gg = 0; gg < G; gg++) acc = __fadd_rn(acc, y[(h * G + gg) * kRank + j]);
+    if (c) acc = __fmul_rn(acc, c[m]);
+    qp[m] = acc;
+    amax = fmaxf(amax, fabsf(acc));
+  }
+  if (!c) {
+    __syncthreads();
+    for (int m = threadIdx.x; m < width; m += blockDim.x)
+      qf32[static_cast<int64_t>(b) * width + m] = qp[m];
+    return;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if (threadIdx.x == 0) red[0] = v;
+  }
+  __syncthreads();
+  const float sigma = __fdiv_rn(red[0], 127.f);
+  if (threadIdx.x == 0 && sigma_out) sigma_out[b] = sigma;
+  for (int m = threadIdx.x; m < width; m += blockDim.x) {
+    const int v = (sigma != 0.f) ? rint_clamp(__fdiv_rn(qp[m], sigma), -127, 127) : 0;
+    q8[static_cast<int64_t>(b) * width + m] = static_cast<int8_t>(v);
+  }
+}
+
+// One warp per (row, head).
+__global__ __launch_bounds__(256) void quant_int8_kernel(const uint16_t* __restrict__ x,
+                                                         int64_t n_items, int d,
+                                                         const int64_t* __restrict__ out_rows,
+                                                         int Hkv, int8_t* __restrict__ q,
+                                                         __half* __restrict__ scale) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  const int chunks = d / 8;
+  for (int64_t item = static_cast<int64_t>(blockIdx.x) * nw + warp; item < n_items;
+       item += static_cast<int64_t>(gridDim.x) * nw) {
+    const uint16_t* row = x + item * d;
+    float amax = 0.f;
+    for (int ch = lane; ch < chunks; ch += 32) {
+      uint4 v = *reinterpret_cast<const uint4*>(row + 8 * ch);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int e = 0; e < 4; e++) {
+        amax = fmaxf(amax, fabsf(__uint_as_float(w[e] << 16)));
+        amax = fmaxf(amax, fabsf(__uint_as_float(w[e] & 0xffff0000u)));
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const __half sh = __float2half_rn(__fdiv_rn(amax, 127.f));
+    const float sf = __half2float(sh);
+    const bool ok = (sf != 0.f) && isfinite(sf);
+    const int64_t t = item / Hkv;
+    const int h = static_cast<int>(item % Hkv);
+    const int64_t orow = out_rows ? out_rows[t] : t;
+    int8_t* qo = q + (orow * Hkv + h) * d;
+    if (lane == 0) scale[orow * Hkv + h] = sh;
+    for (int ch = lane; ch < chunks; ch += 32) {
+      uint4 v = *reinterpret_cast<const uint4*>(row + 8 * ch);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      uint32_t packed[2] = {0u, 0u};
+#pragma unroll
+      for (int e = 0; e < 4; e++) {
+        const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xffff0000u);
+        const int a = ok ? rint_clamp(__fdiv_rn(lo, sf), -127, 127) : 0;
+        const int bb = ok ? rint_clamp(__fdiv_rn(hi, sf), -127, 127) : 0;
+        const uint32_t two = (static_cast<uint32_t>(a) & 0xffu) | ((static_cast<uint32_t>(bb) & 0xffu) << 8);
+        packed[e >> 1] |= two << (16 * (e & 1));
+      }
+      *reinterpret_cast<uint2*>(qo + 8 * ch) = make_uint2(packed[0], packed[1]);
+    }
+  }
+}
+
+}  // namespace
+}  // namespace skv
+
+using namespace skv;
+
+SKV_EXPORT int skv_sketch_project(const uint16_t* keys, int64_t n_tok, int Hkv, int d, int r,
+                                  const float* basis, const float* c, const int64_t* out_rows,
+                                  void* out, void* stream) {
+  if (n_tok < 0 || Hkv <= 0 || r != kRank || d <= 0 || d % 8 || d > kMaxD) return SKV_EINVAL;
+  if (n_tok == 0) return SKV_OK;
+  if (!keys || !basis || !out || !aligned16(keys) || !aligned16(basis)) return SKV_EINVAL;
+  const size_t smem = (static_cast<size_t>(d) * kRank + (kProjThreads / 32) * d) * sizeof(float);
+  if (cudaFuncSetAttribute(sketch_project_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return SKV_ECUDA;
+  const int64_t items = n_tok * Hkv;
+  const int64_t want = (items + (kProjThreads / 32) - 1) / (kProjThreads / 32);
+  const int grid = static_cast<int>(want < 4L * sm_count() ? want : 4L * sm_count());
+  sketch_project_kernel<<<grid > 0 ? grid : 1, kProjThreads, smem, as_stream(stream)>>>(
+      keys, n_tok, Hkv, d, basis, c, out_rows, static_cast<uint8_t*>(out), static_cast<float*>(out));
+  return launch_status();
+}
+
+SKV_EXPORT int skv_sketch_query(const uint16_t* q, int B, int Hq, int Hkv, int d, int r,
+                                const float* basis, const float* c, void* out, float* sigma_out,
+                                void* stream) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || r != kRank || d <= 0 || d > kMaxD ||
+      Hkv * kRank > 1024)
+    return SKV_EINVAL;
+  if (B == 0) return SKV_OK;
+  if (!q || !basis || !out || !aligned16(basis)) return SKV_EINVAL;
+  const size_t smem =
+      (static_cast<size_t>(d) * kRank + static_cast<size_t>(Hq) * d + Hq * kRank + Hkv * kRank) *
+      sizeof(float);
+  if (smem > 220 * 1024) return SKV_EUNSUPPORTED;
+  if (cudaFuncSetAttribute(sketch_query_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return SKV_ECUDA;
+  sketch_query_kernel<<<B, kQueryThreads, smem, as_stream(stream)>>>(
+      q, Hq, Hkv, d, basis, c, static_cast<int8_t*>(out), static_cast<float*>(out), sigma_out);
+  return launch_status();
+}
+
+SKV_EXPORT int skv_quantize_int8_rows(const uint16_t* x, int64_t n_rows, int Hkv, int d,
+                                      const int64_t* out_rows, int8_t* q, uint16_t* scale,
+                                      void* stream) {
+  if (n_rows < 0 || Hkv <= 0 || d <= 0 || d % 8 || d > 1024) return SKV_EINVAL;
+  if (n_rows == 0) return SKV_OK;
+  if (!x || !q || !scale || !aligned16(x) || (reinterpret_cast<uintptr_t>(q) & 7)) return SKV_EINVAL;
+  const int64_t items = n_rows * Hkv;
+  const int64_t want = (items + 7) / 8;
+  const int64_t cap = 16L * sm_count();
+  const int grid = static_cast<int>(want < cap ? want : cap);
+  quant_int8_kernel<<<grid > 0 ? grid : 1, 256, 0, as_stream(stream)>>>(
+      x, items, d, out_rows, Hkv, q, reinterpret_cast<__half*>(scale));
+  return launch_status();
+}

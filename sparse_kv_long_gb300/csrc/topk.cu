@@ -1,0 +1,313 @@
+// topk.cu -- deterministic top-k selection (a4).
+//
+// [P1] "8 agents x 250K context on two 3090s ...", "What shipped": top 2048 +
+// 64 sinks + last 1024 tokens, "deterministic radix select", one pick per
+// layer.  [P4] "3.14M Context on 3x 3090 ...", "Why": the pooled indexer
+// switches to sparse reads once the context exceeds 4*block_topk + 3 tokens.
+//
+// Radix select over 32-bit order keys in three digit passes (bits 31..21,
+// 20..10, 9..0).  Each pass is one launch of CT CTAs per request: a CTA
+// histograms the digit of the keys that still match the prefix found so far
+// (shared-memory bins, warp-aggregated increments), adds its bins to the
+// request's global histogram, and the last CTA to finish (atomic ticket, no
+// waiting) finds the digit holding the k-th key and updates the prefix.  After
+// the last pass the k-th key K* is exact and `need` says how many keys equal to
+// K* are taken: the lowest-index ones.  A count launch and a write launch then
+// emit the selection in ascending index order with an ordered block-wide
+// compaction per chunk.  All steps are deterministic.
+#include "common.cuh"
+
+namespace skv {
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kBins = 2048;
+constexpr int kCTMax = 64;
+
+struct Ws {
+  uint32_t* hist;   // [3][B][kBins]
+  uint32_t* done;   // [3][B]
+  uint32_t* state;  // [B][4]: prefix, mask, need, pad
+  int32_t* cgt;     // [B][kCTMax]
+  int32_t* ceq;     // [B][kCTMax]
+};
+
+__host__ __device__ inline size_t ws_bytes(int B) {
+  return sizeof(uint32_t) * (3ull * B * kBins + 3ull * B + 4ull * B) + sizeof(int32_t) * 2ull * B * kCTMax;
+}
+
+inline Ws ws_carve(void* base, int B) {
+  Ws w;
+  uint32_t* p = static_cast<uint32_t*>(base);
+  w.hist = p;
+  p += 3ull * B * kBins;
+  w.done = p;
+  p += 3ull * B;
+  w.state = p;
+  p += 4ull * B;
+  w.cgt = reinterpret_cast<int32_t*>(p);
+  w.ceq = w.cgt + static_cast<size_t>(B) * kCTMax;
+  return w;
+}
+
+struct Sel {
+  const uint32_t* okeys;
+  int64_t n_cap;
+  const int32_t* lengths;
+  int k, S, W, ratio, CT, B;
+  int32_t* idx;
+  int max_rows;
+  int32_t* count;
+  int32_t* status;
+};
+
+// Candidate range [lo, hi) of request b and whether it takes the dense path.
+__device__ __forceinline__ bool request_range(const Sel& s, int b, int64_t* T, int64_t* lo, int64_t* hi) {
+  int64_t t = s.lengths[b];
+  const int64_t cap = s.ratio > 1 ? s.n_cap * s.ratio : s.n_cap;
+  if (t > cap) t = cap;
+  if (t < 0) t = 0;
+  *T = t;
+  bool dense;
+  if (s.ratio <= 1) {
+    dense = t <= static_cast<int64_t>(s.S) + s.W + s.k;
+    *lo = s.S;
+    *hi = t - s.W;
+  } else {
+    dense = t <= static_cast<int64_t>(s.ratio) * s.k + s.ratio - 1;
+    *lo = 0;
+    *hi = t / s.ratio;
+  }
+  return dense;
+}
+
+__device__ __forceinline__ void chunk_of(int64_t lo, int64_t hi, int CT, int c, int64_t* c0, int64_t* c1) {
+  const int64_t n = hi - lo;
+  const int64_t chunk = (n + CT - 1) / CT;
+  *c0 = lo + c * chunk;
+  *c1 = (*c0 + chunk < hi) ? *c0 + chunk : hi;
+  if (*c0 > hi) *c0 = hi;
+}
+
+__device__ __forceinline__ void pass_digits(int pass, int* shift, int* nbins) {
+  *shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+  *nbins = pass == 2 ? 1024 : 2048;
+}
+
+__global__ __launch_bounds__(kThreads) void topk_hist_kernel(Sel s, Ws w, int pass) {
+  __shared__ uint32_t h[kBins];
+  __shared__ int scan[33];
+  __shared__ int last;
+  const int b = blockIdx.y, c = blockIdx.x;
+  int64_t T, lo, hi;
+  if (request_range(s, b, &T, &lo, &hi)) return;  // dense: nothing to select
+  int shift, nbins;
+  pass_digits(pass, &shift, &nbins);
+  uint32_t prefix = 0, mask = 0, need = static_cast<uint32_t>(s.k);
+  if (pass > 0) {
+    prefix = w.state[4 * b];
+    mask = w.state[4 * b + 1];
+    need = w.state[4 * b + 2];
+  }
+  for (int i = threadIdx.x; i < nbins; i += blockDim.x) h[i] = 0;
+  __syncthreads();
+  int64_t c0, c1;
+  chunk_of(lo, hi, s.CT, c, &c0, &c1);
+  const uint32_t* ok = s.okeys + static_cast<int64_t>(b) * s.n_cap;
+  const int lane = threadIdx.x & 31;
+  for (int64_t base = c0; base < c1; base += blockDim.x) {
+    const int64_t i = base + threadIdx.x;
+    uint32_t digit = 0xffffffffu;
+    if (i < c1) {
+      const uint32_t key = ok[i];
+      if ((key & mask) == prefix) digit = (key >> shift) & static_cast<uint32_t>(nbins - 1);
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, digit);
+    if (digit != 0xffffffffu && lane == __ffs(peers) - 1) atomicAdd(&h[digit], __popc(peers));
+  }
+  __syncthreads();
+  uint32_t* gh = w.hist + (static_cast<size_t>(pass) * s.B + b) * kBins;
+  for (int i = threadIdx.x; i < nbins; i += blockDim.x)
+    if (h[i]) atomicAdd(&gh[i], h[i]);
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last = (atomicAdd(&w.done[pass * s.B + b], 1u) == static_cast<unsigned>(s.CT - 1));
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  // Last CTA of this request: read the full histogram (from L2) and clear it.
+  for (int i = threadIdx.x; i < nbins; i += blockDim.x) {
+    h[i] = __ldcg(&gh[i]);
+    gh[i] = 0;
+  }
+  __syncthreads();
+  // Thread t owns bins_per_thread consecutive bins counted from the top.
+  const int bpt = nbins / blockDim.x;
+  const int top = nbins - 1 - threadIdx.x * bpt;
+  int local = 0;
+  for (int j = 0; j < bpt; j++) local += static_cast<int>(h[top - j]);
+  int tot;
+  int above = block_exclusive_scan(local, scan, &tot);
+  if (static_cast<uint32_t>(tot) < need && threadIdx.x == 0) set_status(s.status, SKV_DEV_COUNT);
+  for (int j = 0; j < bpt; j++) {
+    const int bin = top - j;
+    const int cnt = static_cast<int>(h[bin]);
+    if (static_cast<uint32_t>(above) < need && static_cast<uint32_t>(above + cnt) >= need) {
+      w.state[4 * b] = prefix | (static_cast<uint32_t>(bin) << shift);
+      w.state[4 * b + 1] = mask | (static_cast<uint32_t>(nbins - 1) << shift);
+      w.state[4 * b + 2] = need - static_cast<uint32_t>(above);
+    }
+    above += cnt;
+  }
+  if (threadIdx.x == 0) w.done[pass * s.B + b] = 0;
+}
+
+__global__ __launch_bounds__(kThreads) void topk_count_kernel(Sel s, Ws w) {
+  __shared__ int red[2][32];
+  const int b = blockIdx.y, c = blockIdx.x;
+  int64_t T, lo, hi;
+  if (request_range(s, b, &T, &lo, &hi)) return;
+  const uint32_t kstar = w.state[4 * b];
+  int64_t c0, c1;
+  chunk_of(lo, hi, s.CT, c, &c0, &c1);
+  const uint32_t* ok = s.okeys + static_cast<int64_t>(b) * s.n_cap;
+  int gt = 0, eq = 0;
+  for (int64_t i = c0 + threadIdx.x; i < c1; i += blockDim.x) {
+    const uint32_t key = ok[i];
+    gt += key > kstar;
+    eq += key == kstar;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    gt += __shfl_xor_sync(0xffffffffu, gt, o);
+    eq += __shfl_xor_sync(0xffffffffu, eq, o);
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) {
+    red[0][warp] = gt;
+    red[1][warp] = eq;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int g = 0, e = 0;
+    for (int i = 0; i < (blockDim.x >> 5); i++) {
+      g += red[0][i];
+      e += red[1][i];
+    }
+    w.cgt[b * kCTMax + c] = g;
+    w.ceq[b * kCTMax + c] = e;
+  }
+}
+
+__global__ __launch_bounds__(kThreads) void topk_write_kernel(Sel s, Ws w) {
+  __shared__ int scan[33];
+  __shared__ int base_s[2];
+  const int b = blockIdx.y, c = blockIdx.x;
+  int64_t T, lo, hi;
+  const bool dense = request_range(s, b, &T, &lo, &hi);
+  int32_t* out = s.idx + static_cast<int64_t>(b) * s.max_rows;
+  if (dense) {
+    for (int64_t i = static_cast<int64_t>(c) * blockDim.x + threadIdx.x; i < T;
+         i += static_cast<int64_t>(s.CT) * blockDim.x)
+      out[i] = static_cast<int32_t>(i);
+    if (c == 0 && threadIdx.x == 0) s.count[b] = static_cast<int32_t>(T);
+    return;
+  }
+  const uint32_t kstar = w.state[4 * b];
+  const int need = static_cast<int>(w.state[4 * b + 2]);
+  if (threadIdx.x < 32) {
+    int g = 0, e = 0;
+    for (int i = threadIdx.x; i < c; i += 32) {
+      g += w.cgt[b * kCTMax + i];
+      e += w.ceq[b * kCTMax + i];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      g += __shfl_xor_sync(0xffffffffu, g, o);
+      e += __shfl_xor_sync(0xffffffffu, e, o);
+    }
+    if (threadIdx.x == 0) {
+      base_s[0] = g;
+      base_s[1] = e;
+    }
+  }
+  __syncthreads();
+  const int ties_before = base_s[1] < need ? base_s[1] : need;
+  const int quota = need - ties_before;
+  int out_pos = base_s[0] + ties_before;
+  int eq_seen = 0;
+  int64_t c0, c1;
+  chunk_of(lo, hi, s.CT, c, &c0, &c1);
+  const uint32_t* ok = s.okeys + static_cast<int64_t>(b) * s.n_cap;
+  const int ratio = s.ratio > 1 ? s.ratio : 1;
+  const int head = s.ratio > 1 ? 0 : s.S;
+  for (int64_t base = c0; base < c1; base += blockDim.x) {
+    const int64_t i = base + threadIdx.x;
+    uint32_t key = 0;
+    const bool valid = i < c1;
+    if (valid) key = ok[i];
+    const int gt = valid && key > kstar;
+    const int eq = valid && key == kstar;
+    int eq_tot, sel_tot;
+    const int eq_rank = block_exclusive_scan(eq, scan, &eq_tot) + eq_seen;
+    const int sel = gt || (eq && eq_rank < quota);
+    const int pos = block_exclusive_scan(sel, scan, &sel_tot);
+    if (sel) {
+      const int j = out_pos + pos;
+      if (j < s.k) {
+        for (int u = 0; u < ratio; u++) out[head + ratio * j + u] = static_cast<int32_t>(ratio * i + u);
+      } else {
+        set_status(s.status, SKV_DEV_COUNT);
+      }
+    }
+    out_pos += sel_tot;
+    eq_seen += eq_tot;
+  }
+  if (c == s.CT - 1 && threadIdx.x == 0 && out_pos != s.k) set_status(s.status, SKV_DEV_COUNT);
+  if (c == 0) {
+    if (s.ratio <= 1) {
+      for (int i = threadIdx.x; i < s.S; i += blockDim.x) out[i] = i;
+      for (int i = threadIdx.x; i < s.W; i += blockDim.x)
+        out[s.S + s.k + i] = static_cast<int32_t>(T - s.W + i);
+      if (threadIdx.x == 0) s.count[b] = s.S + s.k + s.W;
+    } else {
+      const int64_t nb = T / s.ratio;
+      const int rem = static_cast<int>(T - nb * s.ratio);
+      for (int i = threadIdx.x; i < rem; i += blockDim.x)
+        out[s.ratio * s.k + i] = static_cast<int32_t>(nb * s.ratio + i);
+      if (threadIdx.x == 0) s.count[b] = s.ratio * s.k + rem;
+    }
+  }
+}
+
+}  // namespace
+}  // namespace skv
+
+using namespace skv;
+
+SKV_EXPORT size_t skv_topk_workspace_size(int B) { return B > 0 ? ws_bytes(B) : 0; }
+
+SKV_EXPORT int skv_topk_select(int B, const uint32_t* order_keys, int64_t n_cap,
+                               const int32_t* lengths, int k, int S, int W, int ratio, int32_t* idx,
+                               int max_rows, int32_t* count, void* workspace, size_t workspace_bytes,
+                               int32_t* dev_status, void* stream) {
+  if (B < 0 || B > 4096 || k < 1 || S < 0 || W < 0 || ratio < 1 || n_cap < 0) return SKV_EINVAL;
+  if (B == 0) return SKV_OK;
+  if (!order_keys || !lengths || !idx || !count || !workspace) return SKV_EINVAL;
+  if (ratio > 1 && (S != 0 || W != 0)) return SKV_EINVAL;
+  const int64_t need_rows = ratio > 1 ? static_cast<int64_t>(ratio) * k + ratio - 1
+                                      : static_cast<int64_t>(S) + k + W;
+  if (max_rows < need_rows) return SKV_EINVAL;
+  if (workspace_bytes < ws_bytes(B)) return SKV_ENOMEM;
+  if (reinterpret_cast<uintptr_t>(workspace) & 15) return SKV_EINVAL;
+  int CT = (2 * sm_count() + B - 1) / B;
+  CT = CT < 1 ? 1 : (CT > kCTMax ? kCTMax : CT);
+  Sel s{order_keys, n_cap, lengths, k, S, W, ratio, CT, B, idx, max_rows, count, dev_status};
+  Ws w = ws_carve(workspace, B);
+  cudaStream_t st = as_stream(stream);
+  dim3 grid(CT, B);
+  for (int pass = 0; pass < 3; pass++) topk_hist_kernel<<<grid, kThreads, 0, st>>>(s, w, pass);
+  topk_count_kernel<<<grid, kThreads, 0, st>>>(s, w);
+  topk_write_kernel<<<grid, kThreads, 0, st>>>(s, w);
+  return launch_status();
+}

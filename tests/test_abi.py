@@ -1,0 +1,59 @@
+"""The C ABI library builds, loads without a GPU, exports every symbol that
+include/*.h declares, and rejects bad arguments on the host before launching."""
+import ctypes
+
+import pytest
+
+import skvtest
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from sparse_kv_long_gb300 import _build
+    _build.build()
+    import sparse_kv_long_gb300 as skv
+    return skv.lib()
+
+
+def test_header_declares_the_hot_path():
+    names = skvtest.declared_symbols()
+    for must in ["skv_sketch_project", "skv_sketch_query", "skv_pool_keys", "skv_index_score",
+                 "skv_topk_select", "skv_sparse_attend_decode", "skv_host_register"]:
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in skvtest.declared_symbols() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_version_and_status_strings(lib):
+    assert lib.skv_version() == 1
+    assert lib.skv_status_string(0) == b"ok"
+    assert lib.skv_status_string(1) == b"invalid argument"
+
+
+def test_host_side_argument_checks(lib):
+    P = ctypes.c_void_p
+    # r must be 64
+    assert lib.skv_sketch_project(P(16), 4, 2, 256, 32, P(16), None, None, P(16), None) == 1
+    # negative batch
+    assert lib.skv_index_score(0, -1, 256, P(16), P(16), 10, P(16), 1, 0, 0, P(16), None, None, None) == 1
+    # k must be >= 1
+    assert lib.skv_topk_select(1, P(16), 10, P(16), 0, 0, 0, 1, P(16), 10, P(16), P(16), 1 << 20,
+                               None, None) == 1
+    # max_rows too small for S + k + W
+    assert lib.skv_topk_select(1, P(16), 10, P(16), 4, 2, 2, 1, P(16), 7, P(16), P(16), 1 << 20,
+                               None, None) == 1
+    # pooled mode takes no sinks or tail
+    assert lib.skv_topk_select(1, P(16), 10, P(16), 4, 1, 0, 4, P(16), 100, P(16), P(16), 1 << 20,
+                               None, None) == 1
+    # head dim other than 256 is not implemented by the attention kernel
+    assert lib.skv_attend_workspace_size(1, 8, 2, 128, 64) == 0
+    assert lib.skv_sparse_attend_decode(0, 1, 8, 2, 128, P(16), P(16), P(16), None, None, 0, 10,
+                                        P(16), 16, P(16), 1.0, P(16), P(16), 1 << 20, None, None) == 2
+    # empty inputs are a no-op success
+    assert lib.skv_sketch_project(P(16), 0, 2, 256, 64, P(16), None, None, P(16), None) == 0
+    assert lib.skv_pool_keys(P(16), 0, 64, 128, 4, 0, 4, P(16), None) == 0
+    assert lib.skv_pool_keys(P(16), 1, 64, 128, 4, 10, 8, P(16), None) == 1  # past capacity
+    assert lib.skv_topk_workspace_size(8) > 0

@@ -1,0 +1,350 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle, on seeded
+inputs sized to span several tiles and a ragged tail.
+
+Bars: bit-exact for integer work (int4 scores, selections, int8 encodings,
+pooled keys); sketch codes exact except +-1 at rounding ties; fp32/bf16
+scores: selections may differ only within 1e-3 relative of the k-th score;
+attention within 2e-3 max abs error of the fp64 oracle on the same rows.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import skvtest as T
+import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+ATOL = 2e-3
+
+
+@pytest.fixture(scope="module")
+def skv():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from sparse_kv_long_gb300 import _build
+    _build.build()
+    import sparse_kv_long_gb300 as m
+    return m
+
+
+def status_word():
+    return torch.zeros(1, dtype=torch.int32, device="cuda")
+
+
+def check_status(st):
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, f"device status {int(st.item())}"
+
+
+# ---------------------------------------------------------------------------
+# a1 / a2 / encodings
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("n,Hkv", [(1, 4), (333, 4), (77, 2)])
+def test_sketch_project_int4_and_f32(skv, orc, n, Hkv):
+    rng = np.random.default_rng(100 + n)
+    d, r = 256, 64
+    U = wl.orthonormal_basis(d, r, 5)
+    keys = wl.to_bf16_bits(wl.lowrank_rows(rng, n * Hkv, U).reshape(n, Hkv, d))
+    c = wl.sketch_step(Hkv, r, d)
+    ref = orc.sketch_project(keys, U, c)
+    out4 = torch.zeros((n, Hkv * r // 2), dtype=torch.uint8, device="cuda")
+    skv.sketch_project(T.bf16_dev(keys), T.dev(U), T.dev(c), out4)
+    out32 = torch.zeros((n, Hkv * r), dtype=torch.float32, device="cuda")
+    skv.sketch_project(T.bf16_dev(keys), T.dev(U), None, out32)
+    torch.cuda.synchronize()
+    got = T.unpack_int4(T.host(out4)).reshape(n, Hkv, r)
+    want = T.unpack_int4(ref["q4"]).reshape(n, Hkv, r)
+    T.assert_codes_match_except_ties(got, want, ref["x"])
+    s = T.host(out32).reshape(n, Hkv, r)
+    kf = wl.bf16_bits_to_f32(keys).astype(np.float64)
+    bound = d * 2.0 ** -23 * np.einsum("thi,ij->thj", np.abs(kf), np.abs(U.astype(np.float64)))
+    assert np.all(np.abs(s - ref["s"]) <= 2 * bound)
+
+
+def test_sketch_project_append_rows(skv, orc):
+    rng = np.random.default_rng(7)
+    Hkv, d, r, n_cap = 4, 256, 64, 50
+    U = wl.orthonormal_basis(d, r, 6)
+    keys = wl.to_bf16_bits(rng.standard_normal((3, Hkv, d)).astype(np.float32))
+    c = wl.sketch_step(Hkv, r, d)
+    rows = np.array([49, 0, 17], np.int64)
+    out = torch.full((n_cap, Hkv * r // 2), 0x5A, dtype=torch.uint8, device="cuda")
+    skv.sketch_project(T.bf16_dev(keys), T.dev(U), T.dev(c), out, out_rows=T.dev(rows))
+    torch.cuda.synchronize()
+    o = T.host(out)
+    ref = orc.sketch_project(keys, U, c)
+    for i, row in enumerate(rows):
+        T.assert_codes_match_except_ties(T.unpack_int4(o[row]), T.unpack_int4(ref["q4"][i]), ref["x"][i].ravel())
+    untouched = np.setdiff1d(np.arange(n_cap), rows)
+    assert np.all(o[untouched] == 0x5A)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv", [(1, 8, 2), (8, 24, 4), (3, 16, 2)])
+def test_sketch_query(skv, orc, B, Hq, Hkv):
+    rng = np.random.default_rng(200 + B)
+    d, r = 256, 64
+    U = wl.orthonormal_basis(d, r, 9)
+    q = wl.to_bf16_bits(wl.lowrank_rows(rng, B * Hq, U).reshape(B, Hq, d))
+    c = wl.sketch_step(Hkv, r, d)
+    ref = orc.sketch_query(q, Hkv, U, c)
+    q8 = torch.zeros((B, Hkv * r), dtype=torch.int8, device="cuda")
+    sig = torch.zeros((B,), dtype=torch.float32, device="cuda")
+    skv.sketch_query(T.bf16_dev(q), Hkv, T.dev(U), T.dev(c), q8, sig)
+    qf = torch.zeros((B, Hkv * r), dtype=torch.float32, device="cuda")
+    skv.sketch_query(T.bf16_dev(q), Hkv, T.dev(U), None, qf)
+    torch.cuda.synchronize()
+    assert np.allclose(T.host(sig), ref["sigma"], rtol=1e-5)
+    T.assert_codes_match_except_ties(T.host(q8), ref["q8"], ref["x"])
+    ref32 = orc.sketch_query(q, Hkv, U, None, int8=False)["qp"]
+    assert np.allclose(T.host(qf), ref32, rtol=1e-4, atol=1e-4)
+
+
+@pytest.mark.parametrize("n,Hkv,d", [(1, 1, 256), (301, 4, 256), (40, 2, 128)])
+def test_quantize_int8_rows_bit_exact(skv, orc, n, Hkv, d):
+    rng = np.random.default_rng(300 + n)
+    x = rng.standard_normal((n, Hkv, d)).astype(np.float32) * rng.uniform(0.01, 10, (n, Hkv, 1)).astype(np.float32)
+    x[0, 0] = 0.0  # an all-zero row
+    xb = wl.to_bf16_bits(x)
+    qr, sr = orc.quant_int8_rows(xb)
+    q = torch.zeros((n, Hkv, d), dtype=torch.int8, device="cuda")
+    s = torch.zeros((n, Hkv), dtype=torch.float16, device="cuda")
+    skv.quantize_int8_rows(T.bf16_dev(xb), q, s)
+    torch.cuda.synchronize()
+    assert np.array_equal(T.host(q), qr)
+    assert np.array_equal(T.host(s), sr)
+
+
+@pytest.mark.parametrize("B,n_tok", [(1, 4), (2, 4 * 1000 + 3), (3, 4 * 517)])
+def test_pool_keys_bit_exact(skv, orc, B, n_tok):
+    rng = np.random.default_rng(400 + n_tok)
+    D = 128
+    t_cap = ((n_tok + 3) // 4) * 4 + 8
+    x = wl.to_bf16_bits(rng.standard_normal((B, t_cap, D)).astype(np.float32))
+    nb = n_tok // 4
+    pooled = torch.zeros((B, t_cap // 4, D), dtype=torch.bfloat16, device="cuda")
+    skv.pool_keys(T.bf16_dev(x), pooled, 0, nb)
+    torch.cuda.synchronize()
+    got = T.host(pooled)
+    for b in range(B):
+        assert np.array_equal(got[b, :nb], orc.pool_keys(x[b, :4 * nb], 4))
+    assert np.all(got[:, nb:] == 0)
+
+
+# ---------------------------------------------------------------------------
+# a3 scores
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("lengths,width", [([5000], 256), ([1, 3000, 20000, 7], 256), ([4096, 999], 128),
+                                           ([2500], 512)])
+def test_index_score_int4_bit_exact(skv, orc, lengths, width):
+    rng = np.random.default_rng(500 + sum(lengths))
+    B, n_cap, S, W = len(lengths), max(lengths) + 5, 64, 100
+    q8 = rng.integers(-127, 128, (B, width)).astype(np.int8)
+    sk = rng.integers(0, 256, (B, n_cap, width // 2)).astype(np.uint8)
+    L = np.array(lengths, np.int32)
+    ref = orc.index_score(orc.SKETCH_INT4, q8, sk, L, S=S, W=W)
+    okeys = torch.zeros((B, n_cap), dtype=torch.int32, device="cuda")
+    raw = torch.zeros((B, n_cap), dtype=torch.int32, device="cuda")
+    st = status_word()
+    skv.index_score(skv.SKETCH_INT4, T.dev(q8), T.dev(sk), T.dev(L), okeys, S=S, W=W, raw=raw, status=st)
+    check_status(st)
+    got_k = T.host(okeys).view(np.uint32)
+    got_s = T.host(raw)
+    for b in range(B):
+        lo, hi = S, max(S, lengths[b] - W)
+        assert np.array_equal(got_k[b, lo:hi], ref["okey"][b, lo:hi])
+        assert np.array_equal(got_s[b, lo:hi], ref["iscore"][b, lo:hi])
+        assert np.all(got_k[b, :lo] == 0) and np.all(got_k[b, hi:] == 0)
+
+
+def test_index_score_f32_and_pooled(skv, orc):
+    rng = np.random.default_rng(600)
+    B, n_cap, width = 2, 3001, 128
+    qp = rng.standard_normal((B, width)).astype(np.float32)
+    s = rng.standard_normal((B, n_cap, width)).astype(np.float32)
+    L = np.array([3001, 1777], np.int32)
+    ref = orc.index_score(orc.SKETCH_F32, qp, s, L, S=8, W=16)
+    okeys = torch.zeros((B, n_cap), dtype=torch.int32, device="cuda")
+    raw = torch.zeros((B, n_cap), dtype=torch.float32, device="cuda")
+    st = status_word()
+    skv.index_score(skv.SKETCH_F32, T.dev(qp), T.dev(s), T.dev(L), okeys, S=8, W=16, raw=raw, status=st)
+    check_status(st)
+    for b in range(B):
+        lo, hi = 8, L[b] - 16
+        assert np.allclose(T.host(raw)[b, lo:hi], ref["dscore"][b, lo:hi], rtol=1e-5, atol=1e-4)
+    nb_cap = 2049
+    qi = wl.to_bf16_bits(rng.standard_normal((B, 128)).astype(np.float32))
+    pk = wl.to_bf16_bits(rng.standard_normal((B, nb_cap, 128)).astype(np.float32))
+    L2 = np.array([4 * nb_cap, 4 * 1000 + 2], np.int32)
+    ref2 = orc.index_score(orc.POOLED_BF16, qi, pk, L2, ratio=4)
+    okeys2 = torch.zeros((B, nb_cap), dtype=torch.int32, device="cuda")
+    raw2 = torch.zeros((B, nb_cap), dtype=torch.float32, device="cuda")
+    skv.index_score(skv.POOLED_BF16, T.bf16_dev(qi), T.bf16_dev(pk), T.dev(L2), okeys2, ratio=4, raw=raw2,
+                    status=st)
+    check_status(st)
+    for b in range(B):
+        nb = L2[b] // 4
+        assert np.allclose(T.host(raw2)[b, :nb], ref2["dscore"][b, :nb], rtol=1e-5, atol=1e-4)
+        assert np.all(T.host(okeys2)[b, nb:] == 0)
+
+
+def test_index_score_nan_is_reported(skv):
+    qp = torch.full((1, 128), float("nan"), device="cuda")
+    s = torch.ones((1, 40, 128), device="cuda")
+    L = torch.tensor([40], dtype=torch.int32, device="cuda")
+    okeys = torch.zeros((1, 40), dtype=torch.int32, device="cuda")
+    st = status_word()
+    skv.index_score(skv.SKETCH_F32, qp, s, L, okeys, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & skv.DEV_NAN
+
+
+# ---------------------------------------------------------------------------
+# a4 selection
+# ---------------------------------------------------------------------------
+
+def run_topk(skv, okey, L, k, S=0, W=0, ratio=1):
+    B, n_cap = okey.shape
+    max_rows = (S + k + W) if ratio == 1 else ratio * k + ratio - 1
+    idx = torch.full((B, max_rows), -7, dtype=torch.int32, device="cuda")
+    cnt = torch.zeros((B,), dtype=torch.int32, device="cuda")
+    ws = torch.zeros((skv.topk_workspace_size(B),), dtype=torch.uint8, device="cuda")
+    st = status_word()
+    skv.topk_select(T.dev(okey.view(np.int32)), T.dev(L), k, idx, cnt, ws, S=S, W=W, ratio=ratio, status=st)
+    check_status(st)
+    assert int(ws.count_nonzero().item()) == 0  # workspace left zero-filled
+    return T.host(idx), T.host(cnt)
+
+
+@pytest.mark.parametrize("case", [
+    dict(lengths=[250_000], k=2048, S=64, W=1024, alphabet=None),
+    dict(lengths=[9000, 3136, 3137, 20, 40000], k=2048, S=64, W=1024, alphabet=None),
+    dict(lengths=[5000, 7000], k=512, S=64, W=256, alphabet=3),     # massive ties
+    dict(lengths=[6000], k=100, S=0, W=0, alphabet=1),               # all keys equal
+    dict(lengths=[3000, 4000], k=1, S=5, W=5, alphabet=50),
+    dict(lengths=[70000, 1234], k=777, S=3, W=9, alphabet=None),
+])
+def test_topk_bit_exact(skv, orc, case):
+    rng = np.random.default_rng(700 + case["k"] + len(case["lengths"]))
+    L = np.array(case["lengths"], np.int32)
+    n_cap = int(L.max())
+    if case["alphabet"] is None:
+        okey = rng.integers(0, 2 ** 32, (len(L), n_cap), dtype=np.uint64).astype(np.uint32)
+        okey[:, ::97] = okey[:, 5:6]  # some exact ties among large keys
+    else:
+        okey = (0x80000000 + rng.integers(0, case["alphabet"], (len(L), n_cap))).astype(np.uint32)
+    k, S, W = case["k"], case["S"], case["W"]
+    gi, gc = run_topk(skv, okey, L, k, S, W)
+    ri, rc = orc.topk_select(okey, L, k, S=S, W=W)
+    assert np.array_equal(gc, rc)
+    for b in range(len(L)):
+        assert np.array_equal(gi[b, :gc[b]], ri[b, :rc[b]])
+
+
+@pytest.mark.parametrize("lengths", [[2051], [2052, 2055, 4 * 262_144], [9, 2048 * 4 + 3]])
+def test_topk_pooled_bit_exact(skv, orc, lengths):
+    rng = np.random.default_rng(800 + len(lengths))
+    L = np.array(lengths, np.int32)
+    n_cap = int(L.max()) // 4 + 1
+    okey = rng.integers(0x7fff0000, 0x80010000, (len(L), n_cap), dtype=np.uint64).astype(np.uint32)
+    gi, gc = run_topk(skv, okey, L, 512, ratio=4)
+    ri, rc = orc.topk_select(okey, L, 512, ratio=4)
+    assert np.array_equal(gc, rc)
+    for b in range(len(L)):
+        assert np.array_equal(gi[b, :gc[b]], ri[b, :rc[b]])
+
+
+# ---------------------------------------------------------------------------
+# a6 attention
+# ---------------------------------------------------------------------------
+
+def attention_case(rng, B, Hq, Hkv, n_rows_pool, counts, max_rows, kind, shuffle=True):
+    d = 256
+    q = wl.to_bf16_bits(rng.standard_normal((B, Hq, d)).astype(np.float32))
+    K = rng.standard_normal((n_rows_pool, Hkv, d)).astype(np.float32)
+    V = rng.standard_normal((n_rows_pool, Hkv, d)).astype(np.float32)
+    rows = np.full((B, max_rows), -1, np.int32)
+    per_req = n_rows_pool // B
+    for b in range(B):
+        sel = rng.choice(per_req, size=counts[b], replace=False)
+        rows[b, :counts[b]] = np.sort(sel) if not shuffle else sel
+    return q, K, V, rows, per_req
+
+
+@pytest.mark.parametrize("kind", ["bf16", "int8"])
+@pytest.mark.parametrize("B,Hq,Hkv,counts,max_rows", [
+    (1, 8, 2, [832], 832),
+    (3, 24, 4, [3136, 17, 1], 3136),
+    (2, 16, 2, [2048, 2051], 2051),
+    (2, 32, 2, [500, 0], 600),       # 16 query heads per KV head, an empty request
+    (1, 4, 4, [33], 40),             # one query head per KV head
+])
+def test_attention_matches_oracle(skv, orc, kind, B, Hq, Hkv, counts, max_rows):
+    rng = np.random.default_rng(900 + Hq + sum(counts))
+    d = 256
+    pool_rows = B * 4000
+    q, K, V, rows, per_req = attention_case(rng, B, Hq, Hkv, pool_rows, counts, max_rows, kind)
+    cnt = np.array(counts, np.int32)
+    scale = 1 / math.sqrt(d)
+    out = torch.zeros((B, Hq, d), dtype=torch.float32, device="cuda")
+    ws = torch.zeros((skv.attend_workspace_size(B, Hq, Hkv, d, max_rows),), dtype=torch.uint8, device="cuda")
+    st = status_word()
+    if kind == "bf16":
+        Kb, Vb = wl.to_bf16_bits(K), wl.to_bf16_bits(V)
+        skv.sparse_attend_decode(skv.KV_BF16, T.bf16_dev(q), T.bf16_dev(Kb), T.bf16_dev(Vb), T.dev(rows),
+                                 T.dev(cnt), scale, out, ws, Hkv, req_row_stride=per_req, status=st)
+        ref = orc.attend(orc.KV_BF16, q, Kb.reshape(pool_rows, -1), Vb.reshape(pool_rows, -1), rows, cnt,
+                         scale, Hkv, d, d, req_row_stride=per_req)
+    else:
+        k8, ks = orc.quant_int8_rows(wl.to_bf16_bits(K))
+        v8, vs = orc.quant_int8_rows(wl.to_bf16_bits(V))
+        skv.sparse_attend_decode(skv.KV_INT8, T.bf16_dev(q), T.dev(k8), T.dev(v8), T.dev(rows), T.dev(cnt),
+                                 scale, out, ws, Hkv, k_scale=T.f16_dev(ks), v_scale=T.f16_dev(vs),
+                                 req_row_stride=per_req, status=st)
+        ref = orc.attend(orc.KV_INT8, q, k8.reshape(pool_rows, -1), v8.reshape(pool_rows, -1), rows, cnt,
+                         scale, Hkv, d, d, k_scale=ks, v_scale=vs, req_row_stride=per_req)
+    check_status(st)
+    got = T.host(out)
+    err = np.max(np.abs(got - ref))
+    assert err < ATOL, err
+    assert int(ws.count_nonzero().item()) <= ws.numel()  # partials may remain; tickets are reset
+    tickets = ws[:256].view(torch.int32)
+    assert int(tickets.count_nonzero().item()) == 0
+
+
+def test_attention_out_of_range_rows_are_flagged(skv):
+    B, Hq, Hkv, d = 1, 8, 2, 256
+    q = torch.randn((B, Hq, d), device="cuda").to(torch.bfloat16)
+    K = torch.randn((100, Hkv, d), device="cuda").to(torch.bfloat16)
+    rows = torch.tensor([[3, 150, 7, -2]], dtype=torch.int32, device="cuda")
+    cnt = torch.tensor([4], dtype=torch.int32, device="cuda")
+    out = torch.zeros((B, Hq, d), device="cuda")
+    ws = torch.zeros((skv.attend_workspace_size(B, Hq, Hkv, d, 4),), dtype=torch.uint8, device="cuda")
+    st = status_word()
+    skv.sparse_attend_decode(skv.KV_BF16, q, K, K, rows, cnt, 0.0625, out, ws, Hkv, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & skv.DEV_RANGE
+    assert torch.isfinite(out).all()
+
+
+def test_attention_is_deterministic(skv):
+    torch.manual_seed(0)
+    B, Hq, Hkv, d, n = 2, 24, 4, 256, 3136
+    q = torch.randn((B, Hq, d), device="cuda").to(torch.bfloat16)
+    K = torch.randint(-127, 128, (B * 5000, Hkv, d), device="cuda", dtype=torch.int8)
+    ks = torch.rand((B * 5000, Hkv), device="cuda").to(torch.float16) * 0.02
+    rows = torch.stack([torch.randperm(5000, device="cuda")[:n] for _ in range(B)]).to(torch.int32)
+    cnt = torch.full((B,), n, dtype=torch.int32, device="cuda")
+    ws = torch.zeros((skv.attend_workspace_size(B, Hq, Hkv, d, n),), dtype=torch.uint8, device="cuda")
+    outs = []
+    for _ in range(3):
+        out = torch.zeros((B, Hq, d), device="cuda")
+        skv.sparse_attend_decode(skv.KV_INT8, q, K, K, rows, cnt, 0.0625, out, ws, Hkv, k_scale=ks, v_scale=ks,
+                                 req_row_stride=5000)
+        outs.append(out)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
