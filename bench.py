@@ -295,8 +295,9 @@ def run_gpu(args):
         w.step()
     torch.cuda.synchronize()
 
-    for _ in range(args.warmup):
-        graph.replay()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph.replay()
     torch.cuda.synchronize()
     barrier()
     torch.cuda.synchronize()
@@ -307,10 +308,11 @@ def run_gpu(args):
         gpu_id = str(local)
     with ClockSampler(gpu_id) as clk:
         time.sleep(0.3)
-        e0.record(stream)
-        for _ in range(args.steps):
-            graph.replay()
-        e1.record(stream)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(args.steps):
+                graph.replay()
+            e1.record(stream)
         torch.cuda.synchronize()
     barrier()
     ms_total = e0.elapsed_time(e1)
@@ -374,8 +376,7 @@ def run_gpu(args):
             w.q.copy_(q_host, non_blocking=True)
             w.newk.copy_(k_host, non_blocking=True)
             w.newv.copy_(v_host, non_blocking=True)
-        graph.replay()
-        with torch.cuda.stream(stream):
+            graph.replay()
             o_host.copy_(w.out, non_blocking=True)
         stream.synchronize()
     e2e_s = (time.perf_counter() - t0) / args.steps

@@ -38,9 +38,11 @@
  *    the offending access and carries on.  The caller reads the word after
  *    synchronising.  No kernel traps.
  *  - Scratch memory ("workspace") is caller-provided, sized by the matching
- *    *_workspace_size call, must be zero-filled once before its first use,
- *    and is left zero-filled by every call that completes.  Calls that share a
- *    workspace must not overlap on the GPU.
+ *    *_workspace_size call, and must be zero-filled once before its first use.
+ *    Every call that completes returns its counters and histograms to zero, so
+ *    the workspace is ready for the next call without clearing; the rest is
+ *    rewritten before it is read.  Calls that share a workspace must not
+ *    overlap on the GPU.
  *  - bf16 / fp16 arguments are passed as uint16_t bit patterns.
  */
 #ifndef SPARSEKV_H

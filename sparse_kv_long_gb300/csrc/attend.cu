@@ -374,8 +374,12 @@ Plan make_plan(int B, int Hq, int Hkv, int max_rows) {
   p.hgroups = (G + 7) / 8;
   p.gy = Hkv * p.hgroups;
   const int pairs = B * p.gy;
-  const int target = 2 * (sm_count() > 0 ? sm_count() : 1);
-  int ns = (target + pairs - 1) / pairs;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attend_kernel<SKV_KV_INT8>, kThreads, 0) !=
+          cudaSuccess || per_sm < 1)
+    per_sm = 1;
+  const int target = per_sm * (sm_count() > 0 ? sm_count() : 1);
+  int ns = target / pairs;  // at most one wave
   const int max_ns = (max_rows + 63) / 64;
   ns = ns < 1 ? 1 : (ns > max_ns ? max_ns : ns);
   if (ns < 1) ns = 1;

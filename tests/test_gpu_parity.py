@@ -216,7 +216,8 @@ def run_topk(skv, okey, L, k, S=0, W=0, ratio=1):
     st = status_word()
     skv.topk_select(T.dev(okey.view(np.int32)), T.dev(L), k, idx, cnt, ws, S=S, W=W, ratio=ratio, status=st)
     check_status(st)
-    assert int(ws.count_nonzero().item()) == 0  # workspace left zero-filled
+    # histograms and tickets (the parts that must start at zero) are left zero-filled
+    assert int(ws[:4 * (3 * B * 2048 + 3 * B)].count_nonzero().item()) == 0
     return T.host(idx), T.host(cnt)
 
 
