@@ -208,6 +208,29 @@ int skv_topk_select(int B, const uint32_t *order_keys, int64_t n_cap,
                     int32_t *idx, int max_rows, int32_t *count, void *workspace,
                     size_t workspace_bytes, int32_t *dev_status, void *stream);
 
+/*
+ * skv_topk_select_noalloc -- the same selection as skv_topk_select, for
+ * callers that cannot give this library any scratch memory: for example an
+ * engine that reserves all device memory for its own KV pools before decoding
+ * starts and hands out no side buffers, or a latency-critical decode loop
+ * that must not call cudaMalloc (an allocation can synchronise the device).
+ * The pages have no counterpart of this call; it is a library convenience.
+ * Its scratch is a fixed array compiled into the library (about 0.8 MB, held
+ * by every device that loads the library until the process exits), enough for
+ * at most 32 requests: B > 32 returns SKV_ENOMEM before anything is launched.
+ * The call allocates nothing.  Its first call on a device looks up that
+ * array's device address (with the device current) and caches it, so make
+ * the first call on each device before any stream capture.  Every call reuses
+ * the same array and clears the parts that must start at zero, so two calls
+ * that overlap on the GPU (different streams, or different host threads on
+ * one device) race and give wrong results: serialise them.
+ * Arguments, results and errors are otherwise those of skv_topk_select.
+ */
+int skv_topk_select_noalloc(int B, const uint32_t *order_keys, int64_t n_cap,
+                            const int32_t *lengths, int k, int S, int W, int ratio,
+                            int32_t *idx, int max_rows, int32_t *count,
+                            int32_t *dev_status, void *stream);
+
 /* ========================================================================== */
 /* KV row encoding (write path).                                               */
 /* ========================================================================== */

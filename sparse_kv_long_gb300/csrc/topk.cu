@@ -15,6 +15,8 @@
 // K* are taken: the lowest-index ones.  A count launch and a write launch then
 // emit the selection in ascending index order with an ordered block-wide
 // compaction per chunk.  All steps are deterministic.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace skv {
@@ -305,6 +307,93 @@ SKV_EXPORT int skv_topk_select(int B, const uint32_t* order_keys, int64_t n_cap,
   Sel s{order_keys, n_cap, lengths, k, S, W, ratio, CT, B, idx, max_rows, count, dev_status};
   Ws w = ws_carve(workspace, B);
   cudaStream_t st = as_stream(stream);
+  dim3 grid(CT, B);
+  for (int pass = 0; pass < 3; pass++) topk_hist_kernel<<<grid, kThreads, 0, st>>>(s, w, pass);
+  topk_count_kernel<<<grid, kThreads, 0, st>>>(s, w);
+  topk_write_kernel<<<grid, kThreads, 0, st>>>(s, w);
+  return launch_status();
+}
+
+// ---------------------------------------------------------------------------
+// Top-k selection without caller-provided scratch.
+//
+// Some callers cannot hand this library a workspace: for example an engine
+// that reserves all device memory for its own KV pools before decoding starts
+// and gives out no side buffers, or a latency-critical decode loop that must
+// not call cudaMalloc (which can synchronise the device).  For them the
+// selection's scratch (digit histograms, tickets, per-chunk counts) lives in
+// a fixed device array compiled into the library, sized for at most
+// kNoAllocMaxB requests.  Every device that loads the library holds this
+// array until the process exits.
+// ---------------------------------------------------------------------------
+namespace skv {
+namespace {
+
+constexpr int kNoAllocMaxB = 32;
+constexpr size_t kNoAllocBytes = sizeof(uint32_t) * (3ull * kNoAllocMaxB * kBins + 3ull * kNoAllocMaxB +
+                                                     4ull * kNoAllocMaxB) +
+                                 sizeof(int32_t) * 2ull * kNoAllocMaxB * kCTMax;
+
+static __device__ __align__(256) unsigned char g_topk_scratch[kNoAllocBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of g_topk_scratch on the current device.  The host-side name
+// of the array is only a stand-in, so the address is looked up once per device
+// (with that device current) and cached.
+int scratch_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return SKV_ECUDA;
+  }
+  if (dev < 0 || dev >= kMaxDevices) return SKV_EUNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_topk_scratch);
+    if (e != cudaSuccess || !p) {
+      cudaGetLastError();
+      return SKV_ECUDA;
+    }
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return SKV_OK;
+}
+
+}  // namespace
+}  // namespace skv
+
+SKV_EXPORT int skv_topk_select_noalloc(int B, const uint32_t* order_keys, int64_t n_cap,
+                                       const int32_t* lengths, int k, int S, int W, int ratio,
+                                       int32_t* idx, int max_rows, int32_t* count, int32_t* dev_status,
+                                       void* stream) {
+  if (B < 0 || k < 1 || S < 0 || W < 0 || ratio < 1 || n_cap < 0) return SKV_EINVAL;
+  if (B > kNoAllocMaxB) return SKV_ENOMEM;  // the fixed scratch holds kNoAllocMaxB requests
+  if (B == 0) return SKV_OK;
+  if (!order_keys || !lengths || !idx || !count) return SKV_EINVAL;
+  if (ratio > 1 && (S != 0 || W != 0)) return SKV_EINVAL;
+  const int64_t need_rows = ratio > 1 ? static_cast<int64_t>(ratio) * k + ratio - 1
+                                      : static_cast<int64_t>(S) + k + W;
+  if (max_rows < need_rows) return SKV_EINVAL;
+  void* scratch = nullptr;
+  const int rc = scratch_address(&scratch);
+  if (rc != SKV_OK) return rc;
+  cudaStream_t st = as_stream(stream);
+  // The array keeps whatever the previous call left; the histograms and
+  // tickets must start at zero, so clear them (no allocation involved).
+  const size_t zero_bytes = sizeof(uint32_t) * (3ull * B * kBins + 3ull * B);
+  if (cudaMemsetAsync(scratch, 0, zero_bytes, st) != cudaSuccess) {
+    cudaGetLastError();
+    return SKV_ECUDA;
+  }
+  int CT = (2 * sm_count() + B - 1) / B;
+  CT = CT < 1 ? 1 : (CT > kCTMax ? kCTMax : CT);
+  Sel s{order_keys, n_cap, lengths, k, S, W, ratio, CT, B, idx, max_rows, count, dev_status};
+  Ws w = ws_carve(scratch, B);
   dim3 grid(CT, B);
   for (int pass = 0; pass < 3; pass++) topk_hist_kernel<<<grid, kThreads, 0, st>>>(s, w, pass);
   topk_count_kernel<<<grid, kThreads, 0, st>>>(s, w);
