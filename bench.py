@@ -40,7 +40,7 @@ W_B, W_T, W_L, W_HQ, W_HKV, W_D, W_R = 8, 250_000, 16, 24, 4, 256, 64
 W_K, W_S, W_W = 2048, 64, 1024
 MAX_ROWS = W_S + W_K + W_W
 SEED = 2
-SCAN_BYTES_PER_CAND = W_HKV * W_R // 2 + 4      # 128 B sketch row read + 4 B order key written
+SCAN_BYTES_PER_CAND = W_HKV * W_R // 2          # 128 B sketch row read (keys stay on chip)
 ATTN_BYTES_PER_ROW_HEAD = 2 * W_D + 2 * 2       # int8 K + V rows and their fp16 scales
 
 
@@ -158,7 +158,7 @@ class ClockSampler:
              "clocks_event_reasons.sw_power_cap")
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -228,14 +228,14 @@ class SketchWorkloadGPU:
         self.okeys = torch.zeros((B, T), dtype=torch.int32, device=dev)
         self.idx = torch.zeros((B, MAX_ROWS), dtype=torch.int32, device=dev)
         self.cnt = torch.zeros((B,), dtype=torch.int32, device=dev)
-        self.tws = torch.zeros((skv.topk_workspace_size(B),), dtype=torch.uint8, device=dev)
+        self.tws = torch.zeros((skv.score_select_workspace_size(B),), dtype=torch.uint8, device=dev)
         self.aws = torch.zeros((skv.attend_workspace_size(B, W_HQ, W_HKV, W_D, MAX_ROWS),), dtype=torch.uint8,
                                device=dev)
         self.out = torch.zeros((L, B, W_HQ, W_D), dtype=torch.float32, device=dev)
         self.status = torch.zeros((1,), dtype=torch.int32, device=dev)
         torch.cuda.synchronize()
 
-    KERNELS_PER_LAYER = 11  # a1 1, int8 encodings 2, a2 1, a3 1, a4 5, a6 1
+    KERNELS_PER_LAYER = 6  # a1 1, int8 encodings 2, a2 1, a3+a4 fused 1, a6 1
 
     def layer(self, l, marks=None):
         skv, st = self.skv, self.status
@@ -246,9 +246,9 @@ class SketchWorkloadGPU:
         skv.quantize_int8_rows(self.newv[l], self.v8[l], self.vs[l], out_rows=self.new_rows)
         skv.sketch_query(self.q[l], W_HKV, self.U, self.c, self.q8, self.sigma)
         ev("scan0")
-        skv.index_score(skv.SKETCH_INT4, self.q8, self.sk[l], self.lengths, self.okeys, S=W_S, W=W_W, status=st)
+        skv.score_select(skv.SKETCH_INT4, self.q8, self.sk[l], self.lengths, W_K, self.idx, self.cnt, self.tws,
+                         S=W_S, W=W_W, status=st)
         ev("scan1")
-        skv.topk_select(self.okeys, self.lengths, W_K, self.idx, self.cnt, self.tws, S=W_S, W=W_W, status=st)
         ev("attn0")
         skv.sparse_attend_decode(skv.KV_INT8, self.q[l], self.k8[l], self.v8[l], self.idx, self.cnt,
                                  1 / math.sqrt(W_D), self.out[l], self.aws, W_HKV, k_scale=self.ks[l],
@@ -394,11 +394,11 @@ def run_gpu(args):
                               f"{step_bytes / 1e9:.2f} GB read per step", layers=L),
         "tokens_per_s": tokens_per_s, "hbm_gbs": step_gbs,
         "parallelism": "replicas only" if world > 1 else "single GPU",
-        "kernel_us": {"index_score_int4": scan_us, "topk_select": topk_us, "sparse_attend_int8": attn_us},
+        "kernel_us": {"score_select_int4": scan_us, "sparse_attend_int8": attn_us},
         "roofline": {"bound": "hbm", "achieved": scan_gbs, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": scan_gbs / hbm_peak, "traffic": None, "kernel": "score_int4_kernel",
+                     "frac": scan_gbs / hbm_peak, "traffic": None, "kernel": "score_select_kernel (scan + top-k)",
                      "peak_source": peak_src, "bytes_per_launch": scan_bytes,
-                     "bytes_rule": f"{SCAN_BYTES_PER_CAND} B per candidate token x {W_B} x {n_cand}"},
+                     "bytes_rule": f"{SCAN_BYTES_PER_CAND} B sketch row per candidate token x {W_B} x {n_cand}"},
         "roofline_attend": {"bound": "hbm", "achieved": attn_gbs, "peak": hbm_peak, "unit": "GB/s",
                             "frac": attn_gbs / hbm_peak, "bytes_per_launch": attn_bytes,
                             "bytes_rule": f"{ATTN_BYTES_PER_ROW_HEAD} B per row-head x {W_B} x {MAX_ROWS} x {W_HKV}"},
@@ -414,8 +414,8 @@ def run_gpu(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)

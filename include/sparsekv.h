@@ -232,6 +232,33 @@ int skv_topk_select_noalloc(int B, const uint32_t *order_keys, int64_t n_cap,
                             int32_t *dev_status, void *stream);
 
 /* ========================================================================== */
+/* a3 + a4 fused: one launch scores the candidates and selects the top-k.      */
+/* ========================================================================== */
+/*
+ * Same result as skv_index_score followed by skv_topk_select with the same
+ * arguments (the scores are computed by the same code, so the selection is
+ * identical), in one cooperative launch: each CTA keeps its chunk's order
+ * keys on chip, the CTAs of a request agree on the radix digits through
+ * request-wide barriers, and the key range found during the scan lets the
+ * digit passes skip the bits all keys share.  `order_keys` ([B][n_cap], may be
+ * NULL) receives a copy of the keys of the candidates.
+ *   workspace  skv_score_select_workspace_size(B) bytes, zero-filled before
+ *              first use; each call returns its counters to zero.
+ * Errors: as skv_index_score and skv_topk_select; SKV_EUNSUPPORTED when B is
+ * larger than the GPU can hold one resident CTA per request for, or when a
+ * request's chunk of keys does not fit on chip (more than about 24K rows per
+ * CTA); use the two separate calls then.  A barrier wait that runs out (it
+ * cannot on a GPU running only this launch) sets SKV_DEV_TIMEOUT, after which
+ * the workspace must be zero-filled again.
+ */
+size_t skv_score_select_workspace_size(int B);
+int skv_score_select(int mode, int B, int width, const void *query, const void *keys,
+                     int64_t n_cap, const int32_t *lengths, int ratio, int k, int S, int W,
+                     int32_t *idx, int max_rows, int32_t *count, uint32_t *order_keys,
+                     void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                     void *stream);
+
+/* ========================================================================== */
 /* KV row encoding (write path).                                               */
 /* ========================================================================== */
 /*
@@ -266,7 +293,8 @@ int skv_quantize_int8_rows(const uint16_t *x, int64_t n_rows, int Hkv, int d,
  *   workspace  skv_attend_workspace_size(...) bytes
  *   n_pool_rows  rows in the pools; a physical row outside [0, n_pool_rows)
  *            is skipped and sets SKV_DEV_RANGE
- * Constraints: d == 256, Hq % Hkv == 0, 1 <= max_rows, pools 16-byte aligned.
+ * Constraints: d == 256, Hq % Hkv == 0, 1 <= max_rows <= 32768, n_pool_rows >= 1,
+ * pools, out and workspace 16-byte aligned.
  * Accuracy: logits accumulate exact products in fp32; the probabilities are
  * rounded to fp16 (int8 rows) or split into two bf16 terms (bf16 rows) for
  * the tensor-core P.V product; max abs error well below 2e-3 for

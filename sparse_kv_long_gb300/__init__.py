@@ -53,6 +53,9 @@ def _load():
                 "skv_index_score": ([i32, i32, i32, P, P, i64, P, i32, i32, i32, P, P, P, P], i32),
                 "skv_topk_workspace_size": ([i32], sz),
                 "skv_topk_select": ([i32, P, i64, P, i32, i32, i32, i32, P, i32, P, P, sz, P, P], i32),
+                "skv_score_select_workspace_size": ([i32], sz),
+                "skv_score_select": ([i32, i32, i32, P, P, i64, P, i32, i32, i32, i32, P, i32, P, P, P, sz, P, P],
+                                     i32),
                 "skv_quantize_int8_rows": ([P, i64, i32, i32, P, P, P, P], i32),
                 "skv_attend_workspace_size": ([i32, i32, i32, i32, i32], sz),
                 "skv_sparse_attend_decode": ([i32, i32, i32, i32, i32, P, P, P, P, P, i64, i64, P, i32, P,
@@ -146,6 +149,22 @@ def topk_select(order_keys, lengths, k, idx, count, workspace, S=0, W=0, ratio=1
     _check("skv_topk_select", _load().skv_topk_select(
         B, _ptr(order_keys), n_cap, _ptr(lengths), k, S, W, ratio, _ptr(idx), idx.shape[1], _ptr(count),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream)))
+    return idx, count
+
+
+def score_select_workspace_size(B) -> int:
+    return int(_load().skv_score_select_workspace_size(B))
+
+
+def score_select(mode, query, keys, lengths, k, idx, count, workspace, S=0, W=0, ratio=1, order_keys=None,
+                 status=None, stream=None):
+    """Fused a3 + a4: scores every candidate and selects as topk_select does."""
+    B, width = query.shape[0], query.shape[1]
+    n_cap = keys.shape[1]
+    _check("skv_score_select", _load().skv_score_select(
+        mode, B, width, _ptr(query), _ptr(keys), n_cap, _ptr(lengths), ratio, k, S, W, _ptr(idx), idx.shape[1],
+        _ptr(count), _ptr(order_keys), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(status), _stream(stream)))
     return idx, count
 
 

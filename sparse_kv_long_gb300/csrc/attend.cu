@@ -3,24 +3,31 @@
 // [P1] "8 agents x 250K context on two 3090s ...", "What shipped": exact int8
 // attention on the top 2048 tokens, 64 sinks and the last 1024.  [P4] "3.14M
 // Context on 3x 3090 ...", "No Need to Rewrite the Kernel": a row is found by
-// adding (token*n_kv_heads + kv_head)*head_dim to the base, so the pool may be
-// HBM or host memory mapped for the GPU.
+// adding (token*n_kv_heads + kv_head)*head_dim to the base, layout
+// [token][kv_head][dim].
 //
 // Design.  A CTA owns one (request, KV head, group of up to 8 query heads,
-// split of the selected rows); its 4 warps take 16-row tiles in turn.  Per
-// tile a warp computes S = Q K^T with m16n8k16 tensor-core MMAs (the query
+// split of the selected rows).  It first stages the split's physical row
+// numbers and (int8) scales in shared memory.  Each of its 4 warps then takes
+// 16-row tiles in turn through a private 2-stage shared-memory ring: lanes
+// 0..15 each issue two TMA bulk copies (cp.async.bulk, one K row and one V
+// row of the KV head) completing on the stage's mbarrier, so the next tile is
+// in flight while the current one is computed and no registers hold pending
+// loads.  Rows land at offsets chosen so that the fragment loads below are
+// free of shared-memory bank conflicts.
+//
+// Per tile a warp computes S = Q K^T with m16n8k16 tensor-core MMAs (query
 // heads are the M rows, padded to 16; two n8 tiles cover the 16 rows), runs
-// the online softmax on the accumulator registers, and accumulates O^T += V^T
-// P^T with the probabilities reused straight from the S accumulators as the B
-// operand.  The head dimension is permuted consistently on Q and K so that
-// each lane loads contiguous 16-byte pieces of a row; the V dimension is
-// permuted so that a lane loads 32 contiguous dims of 4 rows.  int8 codes are
-// converted to fp16 exactly (magic-number trick), and the per-row scales are
-// applied in fp32: the K scale to the logits, the V scale folded into P.
-// bf16 rows keep bf16 operands, with P split into two bf16 terms.
-// Partials (m, l, O) of the 4 warps are merged in shared memory, each CTA
-// writes one partial, and the last CTA of a (request, head group) merges all
-// splits in split order (deterministic) and writes the output.
+// the online softmax on the accumulator registers, and accumulates
+// O^T += V^T P^T with the probabilities reused from the S accumulators as the
+// B operand.  The head dimension is permuted consistently on Q and K so that a
+// lane reads contiguous 16-byte pieces of a row; the V dimension is permuted
+// so that a lane reads 32 contiguous dims of 4 rows.  int8 codes convert to
+// fp16 exactly (0x6400 magic); the K scale multiplies the logits in fp32 and
+// the V scale is folded into P.  bf16 rows keep bf16 operands with P split
+// into two bf16 terms.  The warps' partials (m, l, O) merge in shared memory,
+// each CTA writes one partial, and the last CTA of a (request, head group)
+// merges the splits in split order (deterministic) and writes the output.
 #include "common.cuh"
 
 namespace skv {
@@ -30,6 +37,33 @@ constexpr int D = 256;
 constexpr int kWarps = 4;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kPart = 16 + 8 * D;  // m[8], l[8], O[8][D] floats per partial
+constexpr int kMaxSplit = 64;
+constexpr int kMaxRowsPerSplit = 512;
+constexpr int kStages = 2;
+constexpr int kTileRows = 16;
+constexpr long kWaitLimit = 1L << 20;  // bounded mbarrier polls (~1 s with backoff)
+// Warp partials in shared memory: float (head, dim) at head*kMH + (dim/32)*33 +
+// dim%32, so the fragment-order stores of a warp hit 32 different banks.
+constexpr int kMH = 8 * 33 + 4;
+constexpr int kMW = 8 * kMH;  // floats per warp
+__device__ __forceinline__ int mix(int head, int dim) { return head * kMH + (dim >> 5) * 33 + (dim & 31); }
+
+template <int KV>
+struct Geo {
+  static constexpr int ES = KV == SKV_KV_INT8 ? 1 : 2;
+  static constexpr int RB = D * ES;                                  // bytes of one row of one head
+  static constexpr int KP = RB + 64;                                 // K row pitch in smem
+  static constexpr int VP = KV == SKV_KV_INT8 ? RB + 128 : RB + 64;  // V row pitch in smem
+  static constexpr int STAGE = kTileRows * (KP + VP);
+  static constexpr int WARP_BYTES = kStages * STAGE;
+  // Row r's V slot starts 16*h(r) bytes into its pitch so that the 8 lanes of a
+  // quarter-warp read 8 different bank groups.
+  __device__ static int voff(int r) {
+    const int q = (r >> 1) & 3;
+    const int hsh = KV == SKV_KV_INT8 ? (q == 0 ? 0 : q == 1 ? 1 : q == 2 ? 4 : 5) : q;
+    return r * VP + 16 * hsh;
+  }
+};
 
 struct AttendArgs {
   const uint16_t* q;
@@ -49,6 +83,54 @@ struct AttendArgs {
   float* out;
   int32_t* status;
 };
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for the phase `parity` of `bar`; false when it gave up.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  for (long i = 0; i < kWaitLimit; i++) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (i > 16) __nanosleep(256);
+  }
+  return false;
+}
+
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(const void* p) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(smem_u32(p)));
+  return v;
+}
 
 __device__ __forceinline__ void mma_f16(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                         uint32_t b0, uint32_t b1) {
@@ -87,14 +169,20 @@ __device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-__device__ __forceinline__ float exp2_fast(float x) { return exp2f(x); }
+__device__ __forceinline__ uint32_t word(const uint4& v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
 
 template <int KV>
 __global__ __launch_bounds__(kThreads) void attend_kernel(AttendArgs a) {
-  constexpr int ES = KV == SKV_KV_INT8 ? 1 : 2;  // bytes per element
+  using Gm = Geo<KV>;
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ uint64_t bars[kWarps][kStages];
+  __shared__ int64_t s_prow[kMaxRowsPerSplit];
+  __shared__ float s_ks[kMaxRowsPerSplit], s_vs[kMaxRowsPerSplit];
   __shared__ float sm_m[kWarps][8], sm_l[kWarps][8];
-  __shared__ float sm_o[kWarps][8][D];
   __shared__ float fin_m[8], fin_l[8];
+  __shared__ float wts[8][kMaxSplit];
   __shared__ int is_last;
 
   const int b = blockIdx.z, hy = blockIdx.y, split = blockIdx.x;
@@ -109,6 +197,32 @@ __global__ __launch_bounds__(kThreads) void attend_kernel(AttendArgs a) {
   n = n < 0 ? 0 : (n > a.max_rows ? a.max_rows : n);
   const int r0 = split * a.rows_per_split;
   const int r1 = r0 + a.rows_per_split < n ? r0 + a.rows_per_split : n;
+  const int nr = r1 > r0 ? r1 - r0 : 0;
+
+  const int64_t pitch = static_cast<int64_t>(a.Hkv) * Gm::RB;  // bytes per pool row
+  const uint8_t* kbase = a.kpool + static_cast<int64_t>(h) * Gm::RB;
+  const uint8_t* vbase = a.vpool + static_cast<int64_t>(h) * Gm::RB;
+
+  // ---- stage row numbers and scales of this split ----------------------------
+  for (int i = threadIdx.x; i < nr; i += blockDim.x) {
+    const int32_t rid = a.rows[static_cast<int64_t>(b) * a.max_rows + r0 + i];
+    const int64_t p = static_cast<int64_t>(b) * a.req_row_stride + rid;
+    int64_t pr = -1;
+    if (rid >= 0 && p >= 0 && p < a.n_pool_rows)
+      pr = p;
+    else
+      set_status(a.status, SKV_DEV_RANGE);
+    s_prow[i] = pr;
+    if (KV == SKV_KV_INT8) {
+      s_ks[i] = pr >= 0 ? __half2float(__ushort_as_half(a.kscale[pr * a.Hkv + h])) : 0.f;
+      s_vs[i] = pr >= 0 ? __half2float(__ushort_as_half(a.vscale[pr * a.Hkv + h])) : 0.f;
+    }
+  }
+  if (lane == 0) {
+    for (int s = 0; s < kStages; s++) mbar_init(&bars[warp][s], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
 
   // ---- query fragments (A operand of S = Q K^T), permuted head dim ----------
   uint32_t qa[16][2];
@@ -134,76 +248,97 @@ __global__ __launch_bounds__(kThreads) void attend_kernel(AttendArgs a) {
   for (int mt = 0; mt < 16; mt++) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
   float m_run = -INFINITY, l_part = 0.f;
 
-  const int64_t pitch = static_cast<int64_t>(a.Hkv) * D * ES;  // bytes per pool row
-  const uint8_t* kbase = a.kpool + static_cast<int64_t>(h) * D * ES;
-  const uint8_t* vbase = a.vpool + static_cast<int64_t>(h) * D * ES;
-  const int32_t* rows = a.rows + static_cast<int64_t>(b) * a.max_rows;
+  unsigned char* wbuf = smem + warp * Gm::WARP_BYTES;
+  const int ntiles = (nr + kTileRows - 1) / kTileRows;
+  int my_tiles = 0;
+  for (int t = warp; t < ntiles; t += kWarps) my_tiles++;
 
-  for (int tile = r0 + warp * 16; tile < r1; tile += 16 * kWarps) {
-    // Physical row of tile row `lane` (lanes 0..15), -1 when absent.
-    int64_t prow = -1;
-    if (lane < 16 && tile + lane < r1) {
-      const int32_t rid = rows[tile + lane];
-      const int64_t p = static_cast<int64_t>(b) * a.req_row_stride + rid;
-      if (rid >= 0 && p >= 0 && p < a.n_pool_rows) {
-        prow = p;
-      } else {
-        set_status(a.status, SKV_DEV_RANGE);
-      }
+  for (int it = 0; it < kStages && it < my_tiles; it++) {
+    // Lanes 0..15 copy row `lane` of the warp's tile `it` into stage `it`.
+    // Absent rows copy pool row 0 and are masked below.
+    unsigned char* kst = wbuf + it * Gm::STAGE;
+    unsigned char* vst = kst + kTileRows * Gm::KP;
+    uint64_t* bar = &bars[warp][it];
+    if (lane == 0) mbar_arrive_expect_tx(bar, kTileRows * 2 * Gm::RB);
+    __syncwarp();
+    if (lane < kTileRows) {
+      const int idx = (warp + kWarps * it) * kTileRows + lane;
+      int64_t pr = idx < nr ? s_prow[idx] : -1;
+      if (pr < 0) pr = 0;
+      bulk_g2s(kst + lane * Gm::KP, kbase + pr * pitch, Gm::RB, bar);
+      bulk_g2s(vst + Gm::voff(lane), vbase + pr * pitch, Gm::RB, bar);
     }
-    const int64_t pk0 = __shfl_sync(0xffffffffu, prow, g);
-    const int64_t pk1 = __shfl_sync(0xffffffffu, prow, g + 8);
-    int64_t pv[4];
-    pv[0] = __shfl_sync(0xffffffffu, prow, 2 * c);
-    pv[1] = __shfl_sync(0xffffffffu, prow, 2 * c + 1);
-    pv[2] = __shfl_sync(0xffffffffu, prow, 2 * c + 8);
-    pv[3] = __shfl_sync(0xffffffffu, prow, 2 * c + 9);
+  }
 
-    // ---- S = Q K^T ----------------------------------------------------------
+  int completed = 0;  // tiles whose copies have landed
+  for (int it = 0; it < my_tiles; it++) {
+    const int stage = it % kStages;
+    const uint32_t parity = (it / kStages) & 1;
+    if (!mbar_wait(&bars[warp][stage], parity)) {
+      set_status(a.status, SKV_DEV_TIMEOUT);
+      break;
+    }
+    completed = it + 1;
+    const unsigned char* kst = wbuf + stage * Gm::STAGE;
+    const unsigned char* vst = kst + kTileRows * Gm::KP;
+    const int tbase = (warp + kWarps * it) * kTileRows;  // index of the tile's first row in the split
+
+    // ---- S = Q K^T ------------------------------------------------------------
     float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
     if (KV == SKV_KV_INT8) {
       uint4 k0[4], k1[4];
 #pragma unroll
       for (int i = 0; i < 4; i++) {
-        k0[i] = pk0 >= 0 ? ld_nc16(kbase + pk0 * pitch + 16 * (c + 4 * i)) : make_uint4(0u, 0u, 0u, 0u);
-        k1[i] = pk1 >= 0 ? ld_nc16(kbase + pk1 * pitch + 16 * (c + 4 * i)) : make_uint4(0u, 0u, 0u, 0u);
+        k0[i] = lds128(kst + g * Gm::KP + 16 * (c + 4 * i));
+        k1[i] = lds128(kst + (g + 8) * Gm::KP + 16 * (c + 4 * i));
       }
+      float t0[4] = {0.f, 0.f, 0.f, 0.f}, t1[4] = {0.f, 0.f, 0.f, 0.f};  // second chains (odd k-steps)
 #pragma unroll
       for (int ks = 0; ks < 16; ks++) {
-        const int i = ks >> 2, wsel = ks & 3;
-        const uint32_t w0 = (wsel == 0 ? k0[i].x : wsel == 1 ? k0[i].y : wsel == 2 ? k0[i].z : k0[i].w) ^ 0x80808080u;
-        const uint32_t w1 = (wsel == 0 ? k1[i].x : wsel == 1 ? k1[i].y : wsel == 2 ? k1[i].z : k1[i].w) ^ 0x80808080u;
-        mma_f16(s0, qa[ks][0], 0u, qa[ks][1], 0u, u8pair_to_h2(w0, 0x4140), u8pair_to_h2(w0, 0x4342));
-        mma_f16(s1, qa[ks][0], 0u, qa[ks][1], 0u, u8pair_to_h2(w1, 0x4140), u8pair_to_h2(w1, 0x4342));
+        const uint32_t w0 = word(k0[ks >> 2], ks & 3) ^ 0x80808080u;
+        const uint32_t w1 = word(k1[ks >> 2], ks & 3) ^ 0x80808080u;
+        float* d0 = (ks & 1) ? t0 : s0;
+        float* d1 = (ks & 1) ? t1 : s1;
+        mma_f16(d0, qa[ks][0], 0u, qa[ks][1], 0u, u8pair_to_h2(w0, 0x4140), u8pair_to_h2(w0, 0x4342));
+        mma_f16(d1, qa[ks][0], 0u, qa[ks][1], 0u, u8pair_to_h2(w1, 0x4140), u8pair_to_h2(w1, 0x4342));
+      }
+#pragma unroll
+      for (int j = 0; j < 4; j++) {
+        s0[j] += t0[j];
+        s1[j] += t1[j];
       }
     } else {
-      uint4 k0[8], k1[8];
+      float t0[4] = {0.f, 0.f, 0.f, 0.f}, t1[4] = {0.f, 0.f, 0.f, 0.f};  // second chains (odd k-steps)
 #pragma unroll
       for (int i = 0; i < 8; i++) {
-        k0[i] = pk0 >= 0 ? ld_nc16(kbase + pk0 * pitch + 16 * (c + 4 * i)) : make_uint4(0u, 0u, 0u, 0u);
-        k1[i] = pk1 >= 0 ? ld_nc16(kbase + pk1 * pitch + 16 * (c + 4 * i)) : make_uint4(0u, 0u, 0u, 0u);
+        const uint4 ka = lds128(kst + g * Gm::KP + 16 * (c + 4 * i));
+        const uint4 kb = lds128(kst + (g + 8) * Gm::KP + 16 * (c + 4 * i));
+        mma_bf16(s0, qa[2 * i][0], 0u, qa[2 * i][1], 0u, ka.x, ka.y);
+        mma_bf16(s1, qa[2 * i][0], 0u, qa[2 * i][1], 0u, kb.x, kb.y);
+        mma_bf16(t0, qa[2 * i + 1][0], 0u, qa[2 * i + 1][1], 0u, ka.z, ka.w);
+        mma_bf16(t1, qa[2 * i + 1][0], 0u, qa[2 * i + 1][1], 0u, kb.z, kb.w);
       }
 #pragma unroll
-      for (int ks = 0; ks < 16; ks++) {
-        const int i = ks >> 1;
-        const uint32_t b0a = (ks & 1) ? k0[i].z : k0[i].x, b1a = (ks & 1) ? k0[i].w : k0[i].y;
-        const uint32_t b0b = (ks & 1) ? k1[i].z : k1[i].x, b1b = (ks & 1) ? k1[i].w : k1[i].y;
-        mma_bf16(s0, qa[ks][0], 0u, qa[ks][1], 0u, b0a, b1a);
-        mma_bf16(s1, qa[ks][0], 0u, qa[ks][1], 0u, b0b, b1b);
+      for (int j = 0; j < 4; j++) {
+        s0[j] += t0[j];
+        s1[j] += t1[j];
       }
     }
 
-    // ---- online softmax on S[head g][rows 2c, 2c+1, 2c+8, 2c+9] -------------
+    // ---- online softmax on S[head g][rows 2c, 2c+1, 2c+8, 2c+9] ---------------
+    const int rr[4] = {2 * c, 2 * c + 1, 2 * c + 8, 2 * c + 9};
     float x[4] = {s0[0], s0[1], s1[0], s1[1]};
     float vsc[4];
 #pragma unroll
     for (int i = 0; i < 4; i++) {
-      if (pv[i] >= 0) {
+      const int idx = tbase + rr[i];
+      const bool ok = idx < nr && s_prow[idx] >= 0;
+      if (ok) {
         float f = a.scale_log2;
         vsc[i] = 1.f;
         if (KV == SKV_KV_INT8) {
-          f *= __half2float(__ushort_as_half(a.kscale[pv[i] * a.Hkv + h]));
-          vsc[i] = __half2float(__ushort_as_half(a.vscale[pv[i] * a.Hkv + h]));
+          f *= s_ks[idx];
+          vsc[i] = s_vs[idx];
         }
         x[i] *= f;
       } else {
@@ -216,10 +351,10 @@ __global__ __launch_bounds__(kThreads) void attend_kernel(AttendArgs a) {
     tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
     const float m_new = fmaxf(m_run, tmax);
     const float m_use = m_new == -INFINITY ? 0.f : m_new;
-    const float alpha = exp2_fast(m_run - m_use);
+    const float alpha = exp2f(m_run - m_use);
     float p[4];
 #pragma unroll
-    for (int i = 0; i < 4; i++) p[i] = exp2_fast(x[i] - m_use);
+    for (int i = 0; i < 4; i++) p[i] = exp2f(x[i] - m_use);
     l_part = l_part * alpha + ((p[0] + p[1]) + (p[2] + p[3]));
     m_run = m_new;
     const float a_e = __shfl_sync(0xffffffffu, alpha, 8 * c);
@@ -232,61 +367,77 @@ __global__ __launch_bounds__(kThreads) void attend_kernel(AttendArgs a) {
       o[mt][3] *= a_o;
     }
 
-    // ---- O^T += V^T P^T -----------------------------------------------------
+    // ---- O^T += V^T P^T -------------------------------------------------------
     if (KV == SKV_KV_INT8) {
       const uint32_t bp0 = pack_h2(p[0] * vsc[0], p[1] * vsc[1]);
       const uint32_t bp1 = pack_h2(p[2] * vsc[2], p[3] * vsc[3]);
-      uint4 v[4][2];
 #pragma unroll
-      for (int r = 0; r < 4; r++) {
+      for (int hh = 0; hh < 2; hh++) {
+        uint4 v[4];
 #pragma unroll
-        for (int hh = 0; hh < 2; hh++)
-          v[r][hh] = pv[r] >= 0 ? ld_nc16(vbase + pv[r] * pitch + 32 * g + 16 * hh)
-                                : make_uint4(0u, 0u, 0u, 0u);
-      }
+        for (int r = 0; r < 4; r++) v[r] = lds128(vst + Gm::voff(rr[r]) + 32 * g + 16 * hh);
 #pragma unroll
-      for (int qq = 0; qq < 8; qq++) {
-        const int hh = qq >> 2, ws = qq & 3;
-        uint32_t w[4];
-#pragma unroll
-        for (int r = 0; r < 4; r++)
-          w[r] = ws == 0 ? v[r][hh].x : ws == 1 ? v[r][hh].y : ws == 2 ? v[r][hh].z : v[r][hh].w;
-        const uint32_t t01 = prmt(w[0], w[1], 0x5140) ^ 0x80808080u;  // rows 2c,2c+1: dims 4qq, 4qq+1
-        const uint32_t t23 = prmt(w[0], w[1], 0x7362) ^ 0x80808080u;  // dims 4qq+2, 4qq+3
-        const uint32_t u01 = prmt(w[2], w[3], 0x5140) ^ 0x80808080u;  // rows 2c+8, 2c+9
-        const uint32_t u23 = prmt(w[2], w[3], 0x7362) ^ 0x80808080u;
-        mma_f16(o[2 * qq], u8pair_to_h2(t01, 0x4140), u8pair_to_h2(t01, 0x4342), u8pair_to_h2(u01, 0x4140),
-                u8pair_to_h2(u01, 0x4342), bp0, bp1);
-        mma_f16(o[2 * qq + 1], u8pair_to_h2(t23, 0x4140), u8pair_to_h2(t23, 0x4342),
-                u8pair_to_h2(u23, 0x4140), u8pair_to_h2(u23, 0x4342), bp0, bp1);
+        for (int ws = 0; ws < 4; ws++) {
+          const int qq = 4 * hh + ws;  // dims 32g + 4qq .. 4qq+3
+          const uint32_t t01 = prmt(word(v[0], ws), word(v[1], ws), 0x5140) ^ 0x80808080u;
+          const uint32_t t23 = prmt(word(v[0], ws), word(v[1], ws), 0x7362) ^ 0x80808080u;
+          const uint32_t u01 = prmt(word(v[2], ws), word(v[3], ws), 0x5140) ^ 0x80808080u;
+          const uint32_t u23 = prmt(word(v[2], ws), word(v[3], ws), 0x7362) ^ 0x80808080u;
+          mma_f16(o[2 * qq], u8pair_to_h2(t01, 0x4140), u8pair_to_h2(t01, 0x4342), u8pair_to_h2(u01, 0x4140),
+                  u8pair_to_h2(u01, 0x4342), bp0, bp1);
+          mma_f16(o[2 * qq + 1], u8pair_to_h2(t23, 0x4140), u8pair_to_h2(t23, 0x4342),
+                  u8pair_to_h2(u23, 0x4140), u8pair_to_h2(u23, 0x4342), bp0, bp1);
+        }
       }
     } else {
       const uint32_t ph0 = pack_bf2(p[0], p[1]), ph1 = pack_bf2(p[2], p[3]);
-      const float r0f = p[0] - __uint_as_float(ph0 << 16), r1f = p[1] - __uint_as_float(ph0 & 0xffff0000u);
-      const float r2f = p[2] - __uint_as_float(ph1 << 16), r3f = p[3] - __uint_as_float(ph1 & 0xffff0000u);
-      const uint32_t pl0 = pack_bf2(r0f, r1f), pl1 = pack_bf2(r2f, r3f);
+      const float e0 = p[0] - __uint_as_float(ph0 << 16), e1 = p[1] - __uint_as_float(ph0 & 0xffff0000u);
+      const float e2 = p[2] - __uint_as_float(ph1 << 16), e3 = p[3] - __uint_as_float(ph1 & 0xffff0000u);
+      const uint32_t pl0 = pack_bf2(e0, e1), pl1 = pack_bf2(e2, e3);
 #pragma unroll
       for (int hh = 0; hh < 4; hh++) {  // 16-byte piece hh: dims 32g + 8hh .. +7
         uint4 v[4];
 #pragma unroll
-        for (int r = 0; r < 4; r++)
-          v[r] = pv[r] >= 0 ? ld_nc16(vbase + pv[r] * pitch + 64 * g + 16 * hh) : make_uint4(0u, 0u, 0u, 0u);
+        for (int r = 0; r < 4; r++) v[r] = lds128(vst + Gm::voff(rr[r]) + 64 * g + 16 * hh);
 #pragma unroll
         for (int ws = 0; ws < 4; ws++) {
           const int mt = 4 * hh + ws;  // dims 32g + 2mt, 32g + 2mt + 1
-          uint32_t w[4];
-#pragma unroll
-          for (int r = 0; r < 4; r++) w[r] = ws == 0 ? v[r].x : ws == 1 ? v[r].y : ws == 2 ? v[r].z : v[r].w;
-          const uint32_t a0 = prmt(w[0], w[1], 0x5410), a1 = prmt(w[0], w[1], 0x7632);
-          const uint32_t a2 = prmt(w[2], w[3], 0x5410), a3 = prmt(w[2], w[3], 0x7632);
+          const uint32_t a0 = prmt(word(v[0], ws), word(v[1], ws), 0x5410);
+          const uint32_t a1 = prmt(word(v[0], ws), word(v[1], ws), 0x7632);
+          const uint32_t a2 = prmt(word(v[2], ws), word(v[3], ws), 0x5410);
+          const uint32_t a3 = prmt(word(v[2], ws), word(v[3], ws), 0x7632);
           mma_bf16(o[mt], a0, a1, a2, a3, ph0, ph1);
           mma_bf16(o[mt], a0, a1, a2, a3, pl0, pl1);
         }
       }
     }
+    __syncwarp();
+    const int nx = it + kStages;
+    if (nx < my_tiles) {
+      // Reads of this stage are done; refill it with the warp's tile nx.
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      unsigned char* kdst = wbuf + stage * Gm::STAGE;
+      unsigned char* vdst = kdst + kTileRows * Gm::KP;
+      uint64_t* bar = &bars[warp][stage];
+      if (lane == 0) mbar_arrive_expect_tx(bar, kTileRows * 2 * Gm::RB);
+      __syncwarp();
+      if (lane < kTileRows) {
+        const int idx = (warp + kWarps * nx) * kTileRows + lane;
+        int64_t pr = idx < nr ? s_prow[idx] : -1;
+        if (pr < 0) pr = 0;
+        bulk_g2s(kdst + lane * Gm::KP, kbase + pr * pitch, Gm::RB, bar);
+        bulk_g2s(vdst + Gm::voff(lane), vbase + pr * pitch, Gm::RB, bar);
+      }
+    }
   }
+  // After a timeout, give the copies still in flight a bounded chance to land
+  // before the buffers are reused for the merge.
+  for (int it = completed; it < my_tiles && it < completed + kStages; it++)
+    mbar_wait(&bars[warp][it % kStages], (it / kStages) & 1);
 
-  // ---- merge the 4 warps ---------------------------------------------------
+  // ---- merge the 4 warps (partials staged in the ring buffers) -------------------
+  __syncthreads();
+  float* sm_o = reinterpret_cast<float*>(smem);  // [kWarps][kMW], see mix()
   float l_grp = l_part;
   l_grp += __shfl_xor_sync(0xffffffffu, l_grp, 1);
   l_grp += __shfl_xor_sync(0xffffffffu, l_grp, 2);
@@ -297,10 +448,11 @@ __global__ __launch_bounds__(kThreads) void attend_kernel(AttendArgs a) {
 #pragma unroll
   for (int mt = 0; mt < 16; mt++) {
     const int d0 = 32 * g + 2 * mt;
-    sm_o[warp][2 * c][d0] = o[mt][0];
-    sm_o[warp][2 * c + 1][d0] = o[mt][1];
-    sm_o[warp][2 * c][d0 + 1] = o[mt][2];
-    sm_o[warp][2 * c + 1][d0 + 1] = o[mt][3];
+    float* ow = sm_o + warp * kMW;
+    ow[mix(2 * c, d0)] = o[mt][0];
+    ow[mix(2 * c + 1, d0)] = o[mt][1];
+    ow[mix(2 * c, d0 + 1)] = o[mt][2];
+    ow[mix(2 * c + 1, d0 + 1)] = o[mt][3];
   }
   __syncthreads();
   const int gy = gridDim.y;
@@ -311,18 +463,18 @@ __global__ __launch_bounds__(kThreads) void attend_kernel(AttendArgs a) {
     for (int w = 0; w < kWarps; w++) M = fmaxf(M, sm_m[w][hd]);
     float L = 0.f;
     if (M != -INFINITY)
-      for (int w = 0; w < kWarps; w++) L += exp2_fast(sm_m[w][hd] - M) * sm_l[w][hd];
+      for (int w = 0; w < kWarps; w++) L += exp2f(sm_m[w][hd] - M) * sm_l[w][hd];
     fin_m[hd] = M;
     mypart[hd] = M;
     mypart[8 + hd] = L;
   }
   __syncthreads();
   for (int e = threadIdx.x; e < 8 * D; e += blockDim.x) {
-    const int hd = e / D, dd = e % D;
+    const int hd = e / D;
     const float M = fin_m[hd];
     float acc = 0.f;
     if (M != -INFINITY)
-      for (int w = 0; w < kWarps; w++) acc += exp2_fast(sm_m[w][hd] - M) * sm_o[w][hd][dd];
+      for (int w = 0; w < kWarps; w++) acc += exp2f(sm_m[w][hd] - M) * sm_o[w * kMW + mix(hd, e % D)];
     mypart[16 + e] = acc;
   }
   __threadfence();
@@ -333,34 +485,72 @@ __global__ __launch_bounds__(kThreads) void attend_kernel(AttendArgs a) {
   if (!is_last) return;
   __threadfence();
 
-  // ---- last CTA: merge the splits in split order ----------------------------
+  // ---- last CTA: merge the splits in split order ----------------------------------
+  // Weights w[h][s] = exp2(m_s - M) / L are computed once; the O partials are
+  // then read as independent 16-byte loads so their latencies overlap.
   const float* parts = a.part + (static_cast<int64_t>(b) * gy + hy) * a.nsplit * kPart;
   if (threadIdx.x < 8) {
     const int hd = threadIdx.x;
     float M = -INFINITY;
-    for (int s = 0; s < a.nsplit; s++) M = fmaxf(M, __ldcg(parts + s * kPart + hd));
+    for (int s2 = 0; s2 < a.nsplit; s2++) M = fmaxf(M, __ldcg(parts + s2 * kPart + hd));
     float L = 0.f;
-    if (M != -INFINITY)
-      for (int s = 0; s < a.nsplit; s++)
-        L += exp2_fast(__ldcg(parts + s * kPart + hd) - M) * __ldcg(parts + s * kPart + 8 + hd);
-    fin_m[hd] = M;
+    for (int s2 = 0; s2 < a.nsplit; s2++) {
+      const float wgt = M == -INFINITY ? 0.f : exp2f(__ldcg(parts + s2 * kPart + hd) - M);
+      wts[hd][s2] = wgt;
+      L += wgt * __ldcg(parts + s2 * kPart + 8 + hd);
+    }
     fin_l[hd] = L;
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < 8 * D; e += blockDim.x) {
+  for (int t = threadIdx.x; t < 8 * a.nsplit; t += blockDim.x) {
+    const int hd = t / a.nsplit, s2 = t % a.nsplit;
+    const float L = fin_l[hd];
+    wts[hd][s2] = L > 0.f ? wts[hd][s2] / L : 0.f;
+  }
+  __syncthreads();
+  for (int e4 = threadIdx.x; e4 < 8 * D / 4; e4 += blockDim.x) {
+    const int e = 4 * e4;
     const int hd = e / D, dd = e % D;
     const int hl = hg * 8 + hd;
     if (hl >= a.G) continue;
-    const float M = fin_m[hd], L = fin_l[hd];
-    float acc = 0.f;
-    if (M != -INFINITY && L > 0.f) {
-      for (int s = 0; s < a.nsplit; s++)
-        acc += exp2_fast(__ldcg(parts + s * kPart + hd) - M) * __ldcg(parts + s * kPart + 16 + e);
-      acc = acc / L;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+    for (int s2 = 0; s2 < a.nsplit; s2++) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(parts + s2 * kPart + 16 + e));
+      const float wgt = wts[hd][s2];
+      acc.x += wgt * v.x;
+      acc.y += wgt * v.y;
+      acc.z += wgt * v.z;
+      acc.w += wgt * v.w;
     }
-    a.out[(static_cast<int64_t>(b) * a.Hq + h * a.G + hl) * D + dd] = acc;
+    *reinterpret_cast<float4*>(a.out + (static_cast<int64_t>(b) * a.Hq + h * a.G + hl) * D + dd) = acc;
   }
   if (threadIdx.x == 0) a.tickets[b * gy + hy] = 0;
+}
+
+template <int KV>
+size_t dyn_smem() {
+  const size_t ring = static_cast<size_t>(kWarps) * Geo<KV>::WARP_BYTES;
+  const size_t merge = static_cast<size_t>(kWarps) * kMW * sizeof(float);
+  return ring > merge ? ring : merge;
+}
+
+template <int KV>
+int occupancy() {
+  static int cached = -1;
+  if (cached < 0) {
+    int per_sm = 0;
+    if (cudaFuncSetAttribute(attend_kernel<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(dyn_smem<KV>())) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attend_kernel<KV>, kThreads, dyn_smem<KV>()) !=
+            cudaSuccess ||
+        per_sm < 1) {
+      cudaGetLastError();
+      per_sm = 1;
+    }
+    cached = per_sm;
+  }
+  return cached;
 }
 
 struct Plan {
@@ -368,25 +558,25 @@ struct Plan {
   size_t part_bytes, ticket_bytes;
 };
 
-Plan make_plan(int B, int Hq, int Hkv, int max_rows) {
+Plan make_plan(int kv_kind, int B, int Hq, int Hkv, int max_rows) {
   Plan p;
   const int G = Hq / Hkv;
   p.hgroups = (G + 7) / 8;
   p.gy = Hkv * p.hgroups;
   const int pairs = B * p.gy;
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attend_kernel<SKV_KV_INT8>, kThreads, 0) !=
-          cudaSuccess || per_sm < 1)
-    per_sm = 1;
+  const int per_sm = kv_kind == SKV_KV_INT8 ? occupancy<SKV_KV_INT8>() : occupancy<SKV_KV_BF16>();
   const int target = per_sm * (sm_count() > 0 ? sm_count() : 1);
-  int ns = target / pairs;  // at most one wave
+  int ns = target / pairs;  // at most one wave ...
+  const int min_ns = (max_rows + kMaxRowsPerSplit - 1) / kMaxRowsPerSplit;  // ... unless splits get long
   const int max_ns = (max_rows + 63) / 64;
-  ns = ns < 1 ? 1 : (ns > max_ns ? max_ns : ns);
+  if (ns > max_ns) ns = max_ns;
+  if (ns > kMaxSplit) ns = kMaxSplit;
+  if (ns < min_ns) ns = min_ns;
   if (ns < 1) ns = 1;
   int rps = (max_rows + ns - 1) / ns;
   rps = (rps + 15) / 16 * 16;
+  if (rps > kMaxRowsPerSplit) rps = kMaxRowsPerSplit;
   ns = (max_rows + rps - 1) / rps;
-  if (ns < 1) ns = 1;
   p.nsplit = ns;
   p.rows_per_split = rps;
   p.part_bytes = static_cast<size_t>(B) * p.gy * ns * kPart * sizeof(float);
@@ -400,9 +590,14 @@ Plan make_plan(int B, int Hq, int Hkv, int max_rows) {
 using namespace skv;
 
 SKV_EXPORT size_t skv_attend_workspace_size(int B, int Hq, int Hkv, int d, int max_rows) {
-  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || d != D || max_rows < 1) return 0;
-  Plan p = make_plan(B, Hq, Hkv, max_rows);
-  return p.ticket_bytes + p.part_bytes;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || d != D || max_rows < 1 ||
+      max_rows > kMaxSplit * kMaxRowsPerSplit)
+    return 0;
+  // Sized for the larger of the two row encodings' plans.
+  Plan p8 = make_plan(SKV_KV_INT8, B, Hq, Hkv, max_rows);
+  Plan p16 = make_plan(SKV_KV_BF16, B, Hq, Hkv, max_rows);
+  const size_t s8 = p8.ticket_bytes + p8.part_bytes, s16 = p16.ticket_bytes + p16.part_bytes;
+  return s8 > s16 ? s8 : s16;
 }
 
 SKV_EXPORT int skv_sparse_attend_decode(int kv_kind, int B, int Hq, int Hkv, int d, const uint16_t* q,
@@ -416,11 +611,15 @@ SKV_EXPORT int skv_sparse_attend_decode(int kv_kind, int B, int Hq, int Hkv, int
     return SKV_EINVAL;
   if (d != D) return SKV_EUNSUPPORTED;
   if (kv_kind != SKV_KV_BF16 && kv_kind != SKV_KV_INT8) return SKV_EUNSUPPORTED;
+  if (max_rows > kMaxSplit * kMaxRowsPerSplit) return SKV_EUNSUPPORTED;
   if (B == 0) return SKV_OK;
+  if (n_pool_rows < 1) return SKV_EINVAL;
   if (!q || !k_pool || !v_pool || !rows || !count || !out || !workspace) return SKV_EINVAL;
   if (kv_kind == SKV_KV_INT8 && (!k_scale || !v_scale)) return SKV_EINVAL;
-  if (!aligned16(k_pool) || !aligned16(v_pool) || (reinterpret_cast<uintptr_t>(q) & 7)) return SKV_EINVAL;
-  Plan p = make_plan(B, Hq, Hkv, max_rows);
+  if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out) || !aligned16(workspace) ||
+      (reinterpret_cast<uintptr_t>(q) & 7))
+    return SKV_EINVAL;
+  Plan p = make_plan(kv_kind, B, Hq, Hkv, max_rows);
   if (workspace_bytes < p.ticket_bytes + p.part_bytes) return SKV_ENOMEM;
   if (p.gy > 65535) return SKV_EUNSUPPORTED;
   AttendArgs a;
@@ -448,8 +647,8 @@ SKV_EXPORT int skv_sparse_attend_decode(int kv_kind, int B, int Hq, int Hkv, int
   a.status = dev_status;
   dim3 grid(p.nsplit, p.gy, B);
   if (kv_kind == SKV_KV_INT8)
-    attend_kernel<SKV_KV_INT8><<<grid, kThreads, 0, as_stream(stream)>>>(a);
+    attend_kernel<SKV_KV_INT8><<<grid, kThreads, dyn_smem<SKV_KV_INT8>(), as_stream(stream)>>>(a);
   else
-    attend_kernel<SKV_KV_BF16><<<grid, kThreads, 0, as_stream(stream)>>>(a);
+    attend_kernel<SKV_KV_BF16><<<grid, kThreads, dyn_smem<SKV_KV_BF16>(), as_stream(stream)>>>(a);
   return launch_status();
 }

@@ -1,0 +1,598 @@
+// select.cu -- fused indexer score scan + deterministic top-k (a3 + a4).
+//
+// [P1] "8 agents x 250K context on two 3090s ...", "What shipped": every token
+// is scored through the sketch each step, the top 2048 are picked by a
+// deterministic radix select, one pick per layer, and unioned with 64 sinks
+// and the last 1024 tokens.  [P4] "3.14M Context on 3x 3090 ...", "Why": with
+// pooled keys the top blocks are expanded to tokens once the context exceeds
+// 4*block_topk + 3.
+//
+// One cooperative launch per layer-step.  The CTAs of a request split its
+// candidate rows into contiguous chunks.  Each CTA
+//   1. streams its chunk of indexer rows (the same loops, hence the same
+//      scores, as skv_index_score: coalesced 16-byte loads, eight in flight
+//      per lane) and keeps the order keys in shared memory;
+//   2. works on rel = key - base, where every candidate's rel fits in `bits`
+//      bits: int32 sketch scores are bounded (|s| < 2^20), so base is fixed;
+//      for fp32 scores the CTAs first agree on the key range (one barrier);
+//   3. radix passes over rel, top digits first: each non-final pass (<= 13
+//      bits) histograms the keys still matching the prefix, adds the bins to
+//      the request's global histogram, and after a request-wide barrier every
+//      CTA derives the same digit;
+//   4. the final pass (<= 8 bits) publishes per-CTA bins plus the count of
+//      keys above the prefix; after one barrier every CTA knows the exact k-th
+//      key K*, how many keys equal to K* are taken, and -- from the chunks
+//      before it -- where its own picks go; it writes them in ascending index
+//      order (equal keys: lowest index first).
+// int32 scores need two barriers, fp32 scores three or four.  A barrier is a
+// monotonic arrival counter (release add, acquire poll); the last CTA to
+// leave resets it.  Polls are bounded: a wait that runs out sets
+// SKV_DEV_TIMEOUT and the kernel goes on.  The cooperative launch guarantees
+// that all CTAs are resident together.
+#include "score_common.cuh"
+
+namespace skv {
+namespace {
+
+constexpr int kWarpsF = 16;
+constexpr int kThreads = 32 * kWarpsF;
+constexpr int kMaxDigit = 13;                    // bits of a non-final pass
+constexpr int kBins = 1 << kMaxDigit;
+constexpr int kLastBits = 8;                     // bits of the final pass
+constexpr int kLastBins = 1 << kLastBits;
+constexpr int kFin = 4 + kLastBins;              // per-CTA final record: above count, pad, bins
+constexpr int kCMax = 512;                       // CTAs per request
+constexpr long kSpinLimit = 1L << 21;            // bounded barrier polls (well under a second)
+constexpr size_t kKeyBudget = 96 * 1024;         // shared memory for the chunk's order keys
+constexpr uint32_t kInt4Base = 0x80000000u - (1u << 20);  // order key of score -2^20
+
+struct Ws {
+  unsigned* bar;   // [B][2]: arrivals (monotonic within a launch), exits
+  unsigned* rng;   // [B][2]: largest key, largest inverted key (= ~smallest key)
+  unsigned* hist;  // [2][B][kBins]: non-final passes
+  int* fin;        // [B][kCMax][kFin]: final pass, per CTA
+};
+
+size_t ws_bytes(int B) {
+  const size_t words = 2ull * B + 2ull * B + 2ull * B * kBins + static_cast<size_t>(B) * kCMax * kFin;
+  return (words * 4 + 255) / 256 * 256;
+}
+
+Ws ws_carve(void* base, int B) {
+  Ws w;
+  unsigned* p = static_cast<unsigned*>(base);
+  w.bar = p;
+  p += 2ull * B;
+  w.rng = p;
+  p += 2ull * B;
+  w.hist = p;
+  p += 2ull * B * kBins;
+  w.fin = reinterpret_cast<int*>(p);
+  return w;
+}
+
+struct Args {
+  int mode, width;
+  const void* query;
+  const void* keys;
+  int64_t n_cap;
+  const int32_t* lengths;
+  int ratio, k, S, W;
+  int32_t* idx;
+  int max_rows;
+  int32_t* count;
+  uint32_t* okeys;  // optional copy of the order keys
+  int32_t* status;
+  int B;
+};
+
+// Request-wide barrier: the n-th barrier of a launch waits until the
+// request's arrival counter reaches n * C.
+__device__ void req_barrier(unsigned* arrive, unsigned target, int32_t* status) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(arrive) : "memory");
+    bool ok = false;
+    for (long i = 0; i < kSpinLimit; i++) {
+      unsigned v;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(arrive) : "memory");
+      if (v >= target) {
+        ok = true;
+        break;
+      }
+      if (i > 64) __nanosleep(32);
+    }
+    if (!ok) set_status(status, SKV_DEV_TIMEOUT);
+  }
+  __syncthreads();
+}
+
+// rel >> sh, with a shift of 32 giving 0.
+__device__ __forceinline__ uint32_t top_bits(uint32_t rel, int sh) { return sh >= 32 ? 0u : rel >> sh; }
+
+// Find the digit holding the need-th largest key from bins h[0..nb) and the
+// number of keys in the bins above it.  Position r = 0, 1, ... counts bins
+// from the top (bin nb-1-r).  Warp v sums positions [v*span, (v+1)*span) with
+// lane-strided (bank-conflict-free) reads; the warp whose range holds the
+// need-th key then scans it 32 positions at a time.
+__device__ void find_digit(const uint32_t* h, int nb, uint32_t need, uint32_t* digit, uint32_t* above_out,
+                           int32_t* status) {
+  __shared__ unsigned wsum[kWarpsF];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int span = ((nb + kWarpsF - 1) / kWarpsF + 31) / 32 * 32;
+  const int r0 = warp * span;
+  unsigned sum = 0;
+  for (int r = r0 + lane; r < r0 + span && r < nb; r += 32) sum += h[nb - 1 - r];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  if (lane == 0) wsum[warp] = sum;
+  __syncthreads();
+  unsigned before = 0, total = 0;
+  for (int v = 0; v < kWarpsF; v++) {
+    if (v < warp) before += wsum[v];
+    total += wsum[v];
+  }
+  if (threadIdx.x == 0 && total < need) set_status(status, SKV_DEV_COUNT);
+  if (before < need && before + wsum[warp] >= need) {  // warp-uniform
+    unsigned run = before;
+    for (int r = r0; r < r0 + span && r < nb; r += 32) {
+      const int rr = r + lane;
+      const unsigned cnt = rr < nb && rr < r0 + span ? h[nb - 1 - rr] : 0u;
+      unsigned incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (run + incl - cnt < need && run + incl >= need) {
+        *digit = static_cast<uint32_t>(nb - 1 - rr);
+        *above_out = run + incl - cnt;
+      }
+      run += __shfl_sync(0xffffffffu, incl, 31);
+      if (run >= need) break;
+    }
+  }
+  __syncthreads();
+}
+
+template <int MODE, int LPT>
+__global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w) {
+  extern __shared__ uint32_t skey[];
+  __shared__ __align__(16) uint32_t hist[kBins];
+  __shared__ int wgt[kWarpsF], weq[kWarpsF];
+  __shared__ unsigned red_a[kWarpsF], red_b[kWarpsF];
+  __shared__ uint32_t s_digit, s_above;
+  __shared__ int s_before[2];
+
+  const int b = blockIdx.y, c = blockIdx.x, C = gridDim.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const bool pooled = MODE == SKV_SCORE_POOLED_BF16;
+  const int ratio = pooled ? a.ratio : 1;
+  int64_t T = a.lengths[b];
+  const int64_t cap = pooled ? a.n_cap * ratio : a.n_cap;
+  if (T > cap) {
+    if (threadIdx.x == 0 && c == 0) set_status(a.status, SKV_DEV_RANGE);
+    T = cap;
+  }
+  if (T < 0) T = 0;
+  int32_t* out = a.idx + static_cast<int64_t>(b) * a.max_rows;
+  const bool dense = pooled ? T <= static_cast<int64_t>(ratio) * a.k + ratio - 1
+                            : T <= static_cast<int64_t>(a.S) + a.W + a.k;
+  if (dense) {  // every token; the same decision in every CTA of the request
+    for (int64_t i = static_cast<int64_t>(c) * blockDim.x + threadIdx.x; i < T;
+         i += static_cast<int64_t>(C) * blockDim.x)
+      out[i] = static_cast<int32_t>(i);
+    if (c == 0 && threadIdx.x == 0) a.count[b] = static_cast<int32_t>(T);
+    return;
+  }
+  const int64_t lo = pooled ? 0 : a.S;
+  const int64_t hi = pooled ? T / ratio : T - a.W;
+  const int64_t chunk = (hi - lo + C - 1) / C;
+  int64_t c0 = lo + c * chunk;
+  if (c0 > hi) c0 = hi;
+  const int64_t c1 = c0 + chunk < hi ? c0 + chunk : hi;
+  const int len = static_cast<int>(c1 - c0);
+  unsigned* arrive = w.bar + 2 * b;
+  unsigned nbar = 0;
+
+  // ---- 1. scores of the chunk into shared memory -----------------------------------
+  unsigned kmax = 0u, kinv = 0u;
+  uint32_t* gk = a.okeys ? a.okeys + static_cast<int64_t>(b) * a.n_cap : nullptr;
+  auto keep = [&](int64_t t, uint32_t key) {
+    skey[t - c0] = key;
+    if (gk) gk[t] = key;
+    kmax = max(kmax, key);
+    kinv = max(kinv, ~key);
+  };
+  if (MODE == SKV_SCORE_SKETCH_INT4) {
+    constexpr int width = LPT * 32;
+    const int8_t* q8 = static_cast<const int8_t*>(a.query) + static_cast<int64_t>(b) * width;
+    const uint8_t* rows = static_cast<const uint8_t*>(a.keys) + static_cast<int64_t>(b) * a.n_cap * (width / 2);
+    auto emit = [&](int64_t t, int32_t sc) { keep(t, order_key_i32(sc)); };
+    if (LPT == 8)
+      scan_int4_rows128(q8, rows, c0, c1, warp, kWarpsF, emit);
+    else
+      scan_int4<LPT>(q8, rows, c0, c1, emit);
+  } else if (MODE == SKV_SCORE_POOLED_BF16) {
+    scan_pooled(static_cast<const uint16_t*>(a.query) + static_cast<int64_t>(b) * 128,
+                static_cast<const uint16_t*>(a.keys) + static_cast<int64_t>(b) * a.n_cap * 128, c0, c1,
+                [&](int64_t t, float sc) {
+                  if (isnan(sc)) set_status(a.status, SKV_DEV_NAN);
+                  keep(t, order_key_f32(sc));
+                });
+  } else {
+    scan_f32(static_cast<const float*>(a.query) + static_cast<int64_t>(b) * a.width,
+             static_cast<const float*>(a.keys) + static_cast<int64_t>(b) * a.n_cap * a.width, a.width, c0, c1,
+             [&](int64_t t, float sc) {
+               if (isnan(sc)) set_status(a.status, SKV_DEV_NAN);
+               keep(t, order_key_f32(sc));
+             });
+  }
+
+  // ---- 2. the range of rel = key - base ----------------------------------------------
+  uint32_t base;
+  int bits;
+  if (MODE == SKV_SCORE_SKETCH_INT4) {
+    base = kInt4Base;  // |score| < 2^20 for any int8 query and int4 codes, width <= 512
+    bits = 21;
+    __syncthreads();
+  } else {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+      kinv = max(kinv, __shfl_xor_sync(0xffffffffu, kinv, o));
+    }
+    if (lane == 0) {
+      red_a[warp] = kmax;
+      red_b[warp] = kinv;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && len > 0) {
+      unsigned m1 = 0u, m2 = 0u;
+      for (int i = 0; i < kWarpsF; i++) {
+        m1 = max(m1, red_a[i]);
+        m2 = max(m2, red_b[i]);
+      }
+      atomicMax(&w.rng[2 * b], m1);
+      atomicMax(&w.rng[2 * b + 1], m2);
+    }
+    req_barrier(arrive, ++nbar * C, a.status);
+    const unsigned gmax = __ldcg(&w.rng[2 * b]);
+    const unsigned gmin = ~__ldcg(&w.rng[2 * b + 1]);
+    base = gmin;
+    bits = gmax == gmin ? 0 : 32 - __clz(gmax - gmin);
+  }
+
+  // ---- 3. non-final radix passes ---------------------------------------------------
+  uint32_t need = static_cast<uint32_t>(a.k);
+  uint32_t P = 0;  // rel >> rem of the keys still in play
+  int rem = bits;
+  const int wlast = bits < kLastBits ? bits : kLastBits;
+  int pass = 0;
+  while (rem > wlast) {
+    const int wb = rem - wlast < kMaxDigit ? rem - wlast : kMaxDigit;
+    const int shift = rem - wb;
+    const int nb = 1 << wb;
+    for (int i = threadIdx.x; i < nb; i += blockDim.x) hist[i] = 0u;
+    __syncthreads();
+    for (int i = threadIdx.x; i < len; i += blockDim.x) {
+      const uint32_t rel = skey[i] - base;
+      if (top_bits(rel, rem) == P) atomicAdd(&hist[(rel >> shift) & static_cast<uint32_t>(nb - 1)], 1u);
+    }
+    __syncthreads();
+    unsigned* gh = w.hist + (static_cast<size_t>(pass) * a.B + b) * kBins;
+    for (int i = threadIdx.x; i < nb; i += blockDim.x)
+      if (hist[i]) atomicAdd(&gh[i], hist[i]);
+    req_barrier(arrive, ++nbar * C, a.status);
+    {  // all loads in flight together: 16-byte pieces, unrolled
+      const uint4* g4 = reinterpret_cast<const uint4*>(gh);
+      uint4* h4 = reinterpret_cast<uint4*>(hist);
+      const int n4 = nb / 4;  // nb >= 4 here: a non-final pass has at least 3 bits... or 1 bin group
+      constexpr int kPer = kBins / 4 / kThreads;
+      uint4 v[kPer];
+#pragma unroll
+      for (int j = 0; j < kPer; j++) {
+        const int i = threadIdx.x + j * kThreads;
+        v[j] = i < n4 ? __ldcg(&g4[i]) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int j = 0; j < kPer; j++) {
+        const int i = threadIdx.x + j * kThreads;
+        if (i < n4) h4[i] = v[j];
+      }
+      for (int i = 4 * n4 + threadIdx.x; i < nb; i += blockDim.x) hist[i] = __ldcg(&gh[i]);
+    }
+    __syncthreads();
+    find_digit(hist, nb, need, &s_digit, &s_above, a.status);
+    P = (P << wb) | s_digit;
+    need -= s_above;
+    rem = shift;
+    pass++;
+  }
+
+  // ---- 4. final pass: K*, ties, and this CTA's offsets ------------------------------
+  uint32_t kstar;
+  uint32_t need_eq;  // keys equal to K* that are taken (lowest index first)
+  if (wlast == 0) {  // every candidate has the same key
+    kstar = base;
+    need_eq = need;
+    if (threadIdx.x == 0) {
+      s_before[0] = 0;
+      s_before[1] = static_cast<int>(c0 - lo);
+    }
+  } else {
+    const int nbf = 1 << wlast;
+    for (int i = threadIdx.x; i < nbf; i += blockDim.x) hist[i] = 0u;
+    if (threadIdx.x == 0) s_above = 0u;
+    __syncthreads();
+    unsigned above_local = 0u;
+    for (int i = threadIdx.x; i < len; i += blockDim.x) {
+      const uint32_t rel = skey[i] - base;
+      const uint32_t t = rel >> wlast;
+      if (t == P)
+        atomicAdd(&hist[rel & static_cast<uint32_t>(nbf - 1)], 1u);
+      else if (t > P)
+        above_local++;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) above_local += __shfl_xor_sync(0xffffffffu, above_local, o);
+    if (lane == 0 && above_local) atomicAdd(&s_above, above_local);
+    __syncthreads();
+    // Record: [0] keys above the prefix, [1..3] unused, [4 + d] bin d.
+    int* myfin = w.fin + (static_cast<size_t>(b) * kCMax + c) * kFin;
+    if (threadIdx.x < 4) myfin[threadIdx.x] = threadIdx.x == 0 ? static_cast<int>(s_above) : 0;
+    for (int i = threadIdx.x; i < kLastBins; i += blockDim.x) myfin[4 + i] = i < nbf ? static_cast<int>(hist[i]) : 0;
+    req_barrier(arrive, ++nbar * C, a.status);
+    // Every record of the request, read once (16-byte loads, all in flight):
+    // the request-wide bins, and the records of the chunks before this one.
+    for (int i = threadIdx.x; i < nbf; i += blockDim.x) hist[i] = 0u;
+    __syncthreads();
+    const int4* rf4 = reinterpret_cast<const int4*>(w.fin + static_cast<size_t>(b) * kCMax * kFin);
+    constexpr int kQ = kFin / 4;  // 16-byte pieces per record
+    const int nq = C * kQ;
+    constexpr int kPerF = 8;
+    int4 rv[kPerF];
+    // pieces beyond the unrolled window are read in a second loop
+#pragma unroll
+    for (int j = 0; j < kPerF; j++) {
+      const int e = threadIdx.x + j * kThreads;
+      rv[j] = e < nq ? __ldcg(&rf4[e]) : make_int4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int j = 0; j < kPerF; j++) {
+      const int e = threadIdx.x + j * kThreads;
+      const int q = e % kQ;
+      if (e < nq && q > 0) {
+        const int d = 4 * (q - 1);
+        const int vv[4] = {rv[j].x, rv[j].y, rv[j].z, rv[j].w};
+#pragma unroll
+        for (int u = 0; u < 4; u++)
+          if (vv[u] && d + u < nbf) atomicAdd(&hist[d + u], static_cast<unsigned>(vv[u]));
+      }
+    }
+    for (int e = threadIdx.x + kPerF * kThreads; e < nq; e += blockDim.x) {
+      const int q = e % kQ;
+      if (q > 0) {
+        const int4 x = __ldcg(&rf4[e]);
+        const int d = 4 * (q - 1);
+        const int vv[4] = {x.x, x.y, x.z, x.w};
+        for (int u = 0; u < 4; u++)
+          if (vv[u] && d + u < nbf) atomicAdd(&hist[d + u], static_cast<unsigned>(vv[u]));
+      }
+    }
+    __syncthreads();
+    find_digit(hist, nbf, need, &s_digit, &s_above, a.status);
+    const uint32_t dstar = s_digit;
+    need_eq = need - s_above;
+    kstar = base + ((P << wlast) | dstar);
+    // keys of the chunks before this one: above K*, and equal to K*
+    int gb = 0, eb = 0;
+    auto tally = [&](int e, const int4& x) {
+      const int cc = e / kQ, q = e % kQ;
+      if (cc >= c) return;
+      if (q == 0) {
+        gb += x.x;
+        return;
+      }
+      const int d = 4 * (q - 1);
+      const int vv[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int u = 0; u < 4; u++) {
+        if (d + u > static_cast<int>(dstar))
+          gb += vv[u];
+        else if (d + u == static_cast<int>(dstar))
+          eb += vv[u];
+      }
+    };
+#pragma unroll
+    for (int j = 0; j < kPerF; j++) {
+      const int e = threadIdx.x + j * kThreads;
+      if (e < nq) tally(e, rv[j]);
+    }
+    for (int e = threadIdx.x + kPerF * kThreads; e < nq; e += blockDim.x) tally(e, __ldcg(&rf4[e]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      gb += __shfl_xor_sync(0xffffffffu, gb, o);
+      eb += __shfl_xor_sync(0xffffffffu, eb, o);
+    }
+    if (threadIdx.x == 0) s_before[0] = s_before[1] = 0;
+    __syncthreads();
+    if (lane == 0) {
+      atomicAdd(&s_before[0], gb);
+      atomicAdd(&s_before[1], eb);
+    }
+  }
+  // This CTA is done with everything the request's CTAs published.  The last
+  // CTA to get here clears the range cells, the non-final histograms and the
+  // counters, so the workspace is ready for the next launch.
+  __shared__ int s_last;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_last = atomicAdd(&w.bar[2 * b + 1], 1u) == static_cast<unsigned>(C - 1);
+  }
+  __syncthreads();
+  if (s_last) {
+    __threadfence();
+    for (int p = 0; p < pass; p++)
+      for (int i = threadIdx.x; i < kBins; i += blockDim.x) w.hist[(static_cast<size_t>(p) * a.B + b) * kBins + i] = 0u;
+    if (threadIdx.x == 0) {
+      w.rng[2 * b] = 0u;
+      w.rng[2 * b + 1] = 0u;
+      w.bar[2 * b] = 0u;
+      w.bar[2 * b + 1] = 0u;
+    }
+  }
+
+  // ---- 5. this CTA's picks, in ascending index order ---------------------------------
+  // Warp v owns the contiguous piece [v*sub, (v+1)*sub) of the chunk.
+  const int sub = ((len + kWarpsF - 1) / kWarpsF + 31) / 32 * 32;
+  const int p0 = warp * sub, p1 = min(len, p0 + sub);
+  int ngt = 0, neq = 0;
+  for (int i = p0 + lane; i < p1; i += 32) {
+    const uint32_t key = skey[i];
+    ngt += key > kstar;
+    neq += key == kstar;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    ngt += __shfl_xor_sync(0xffffffffu, ngt, o);
+    neq += __shfl_xor_sync(0xffffffffu, neq, o);
+  }
+  if (lane == 0) {
+    wgt[warp] = ngt;
+    weq[warp] = neq;
+  }
+  __syncthreads();
+  const int needi = static_cast<int>(need_eq);
+  int eq_run = s_before[1];  // equal keys before this warp's piece
+  int pos = s_before[0] + min(s_before[1], needi);
+  for (int v = 0; v < warp; v++) {
+    pos += wgt[v] + max(0, min(weq[v], needi - eq_run));
+    eq_run += weq[v];
+  }
+  const unsigned lt = (1u << lane) - 1u;
+  const int head = pooled ? 0 : a.S;
+  for (int bb = p0; bb < p1; bb += 32) {
+    const int i = bb + lane;
+    const uint32_t key = i < p1 ? skey[i] : 0u;
+    const bool gt = i < p1 && key > kstar;
+    const bool eq = i < p1 && key == kstar;
+    const unsigned eqb = __ballot_sync(0xffffffffu, eq);
+    const int eq_rank = eq_run + __popc(eqb & lt);
+    const bool sel = gt || (eq && eq_rank < needi);
+    const unsigned selb = __ballot_sync(0xffffffffu, sel);
+    if (sel) {
+      const int j = pos + __popc(selb & lt);
+      const int64_t t = c0 + i;
+      if (j < a.k) {
+        for (int u = 0; u < ratio; u++) out[head + ratio * j + u] = static_cast<int32_t>(ratio * t + u);
+      } else {
+        set_status(a.status, SKV_DEV_COUNT);
+      }
+    }
+    eq_run += __popc(eqb);
+    pos += __popc(selb);
+  }
+  if (c == 0) {
+    if (!pooled) {
+      for (int i = threadIdx.x; i < a.S; i += blockDim.x) out[i] = i;
+      for (int i = threadIdx.x; i < a.W; i += blockDim.x) out[a.S + a.k + i] = static_cast<int32_t>(T - a.W + i);
+      if (threadIdx.x == 0) a.count[b] = a.S + a.k + a.W;
+    } else {
+      const int64_t nbk = T / ratio;
+      const int rem_tok = static_cast<int>(T - nbk * ratio);
+      for (int i = threadIdx.x; i < rem_tok; i += blockDim.x)
+        out[ratio * a.k + i] = static_cast<int32_t>(nbk * ratio + i);
+      if (threadIdx.x == 0) a.count[b] = ratio * a.k + rem_tok;
+    }
+  }
+}
+
+template <int MODE, int LPT>
+int launch(const Args& a, Ws w, cudaStream_t st) {
+  auto kernel = score_select_kernel<MODE, LPT>;
+  static bool configured = false;
+  if (!configured) {
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kKeyBudget)) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return SKV_ECUDA;
+    }
+    configured = true;
+  }
+  // Largest grid whose CTAs are all resident at once (two per SM if they fit).
+  int C = 0;
+  size_t smem = 0;
+  for (int per_sm_try = 2; per_sm_try >= 1 && C == 0; per_sm_try--) {
+    const int c_try = per_sm_try * sm_count() / a.B;
+    if (c_try < 1) continue;
+    const int c_use = c_try > kCMax ? kCMax : c_try;
+    const size_t need = static_cast<size_t>((a.n_cap + c_use - 1) / c_use) * sizeof(uint32_t);
+    int fit = 0;
+    if (need > kKeyBudget ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, kernel, kThreads, need) != cudaSuccess) {
+      cudaGetLastError();
+      continue;
+    }
+    if (fit >= per_sm_try) {
+      C = c_use;
+      smem = need;
+    }
+  }
+  if (C < 1) return SKV_EUNSUPPORTED;  // too many requests, or a chunk too large for on-chip keys
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(C, a.B, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kernel, a, w) != cudaSuccess) {
+    cudaGetLastError();
+    return SKV_ECUDA;
+  }
+  return SKV_OK;
+}
+
+}  // namespace
+}  // namespace skv
+
+using namespace skv;
+
+SKV_EXPORT size_t skv_score_select_workspace_size(int B) { return B > 0 ? ws_bytes(B) : 0; }
+
+SKV_EXPORT int skv_score_select(int mode, int B, int width, const void* query, const void* keys, int64_t n_cap,
+                                const int32_t* lengths, int ratio, int k, int S, int W, int32_t* idx,
+                                int max_rows, int32_t* count, uint32_t* order_keys, void* workspace,
+                                size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  if (B < 0 || B > 65535 || n_cap < 0 || k < 1 || S < 0 || W < 0 || ratio < 1) return SKV_EINVAL;
+  if (B == 0) return SKV_OK;
+  if (!query || !keys || !lengths || !idx || !count || !workspace) return SKV_EINVAL;
+  if (!aligned16(keys) || !aligned16(query) || !aligned16(workspace)) return SKV_EINVAL;
+  if (workspace_bytes < ws_bytes(B)) return SKV_ENOMEM;
+  const bool pooled = mode == SKV_SCORE_POOLED_BF16;
+  if (pooled ? (ratio != 4 || width != 128 || S != 0 || W != 0) : ratio != 1) return SKV_EINVAL;
+  const int64_t need_rows = pooled ? static_cast<int64_t>(ratio) * k + ratio - 1 : static_cast<int64_t>(S) + k + W;
+  if (max_rows < need_rows) return SKV_EINVAL;
+  Args a{mode, width, query, keys, n_cap, lengths, ratio, k, S, W, idx, max_rows, count, order_keys, dev_status, B};
+  Ws w = ws_carve(workspace, B);
+  cudaStream_t st = as_stream(stream);
+  switch (mode) {
+    case SKV_SCORE_SKETCH_INT4:
+      if (width == 128) return launch<SKV_SCORE_SKETCH_INT4, 4>(a, w, st);
+      if (width == 256) return launch<SKV_SCORE_SKETCH_INT4, 8>(a, w, st);
+      if (width == 512) return launch<SKV_SCORE_SKETCH_INT4, 16>(a, w, st);
+      return SKV_EUNSUPPORTED;
+    case SKV_SCORE_SKETCH_F32:
+      if (width <= 0 || width % 4 || width > 1024) return SKV_EINVAL;
+      return launch<SKV_SCORE_SKETCH_F32, 32>(a, w, st);
+    case SKV_SCORE_POOLED_BF16:
+      return launch<SKV_SCORE_POOLED_BF16, 16>(a, w, st);
+    default:
+      return SKV_EINVAL;
+  }
+}

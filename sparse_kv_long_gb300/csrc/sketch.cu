@@ -66,49 +66,46 @@ __global__ __launch_bounds__(kProjThreads) void sketch_project_kernel(
   }
 }
 
-constexpr int kQueryThreads = 512;
+constexpr int kQueryThreads = 256;
 
-// One CTA per request.  y[g][j] = basis[:, j] . q[g]; qp[h][j] = c[h][j] *
-// sum over the group's heads (ascending); int8 quantisation with one scale per
-// request.
+// One CTA per request.  The group's query heads are summed first (fp32, head
+// order), then projected once per KV head: qp[h][j] = c[h][j] * sum_x
+// basis[x][j] * Qsum_h[x] -- the same linear map as projecting each head and
+// summing, with six times fewer multiply-adds for groups of six.  int8
+// quantisation with one scale per request follows.
 __global__ __launch_bounds__(kQueryThreads) void sketch_query_kernel(
     const uint16_t* __restrict__ q, int Hq, int Hkv, int d, const float* __restrict__ basis,
     const float* __restrict__ c, int8_t* __restrict__ q8, float* __restrict__ qf32,
     float* __restrict__ sigma_out) {
   extern __shared__ float smem[];
-  float* P = smem;                     // [d][64]
-  float* qs = P + d * kRank;           // [Hq][d]
-  float* y = qs + Hq * d;              // [Hq][64]
-  float* qp = y + Hq * kRank;          // [Hkv][64]
+  float* qs = smem;                    // [Hkv][d] group sums
+  float* qp = qs + Hkv * d;            // [Hkv][64]
   __shared__ float red[32];
   const int b = blockIdx.x;
   const int G = Hq / Hkv;
-  for (int i = threadIdx.x; i < d * kRank / 4; i += blockDim.x)
-    reinterpret_cast<float4*>(P)[i] = reinterpret_cast<const float4*>(basis)[i];
   const uint16_t* qb = q + static_cast<int64_t>(b) * Hq * d;
-  for (int i = threadIdx.x; i < Hq * d; i += blockDim.x) qs[i] = bf16_bits_to_f32(qb[i]);
-  __syncthreads();
-  for (int o = threadIdx.x; o < Hq * kRank; o += blockDim.x) {
-    const int g = o / kRank, j = o % kRank;
-    const float* qg = qs + g * d;
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-    int x = 0;
-    for (; x + 3 < d; x += 4) {
-      a0 = fmaf(P[x * kRank + j], qg[x], a0);
-      a1 = fmaf(P[(x + 1) * kRank + j], qg[x + 1], a1);
-      a2 = fmaf(P[(x + 2) * kRank + j], qg[x + 2], a2);
-      a3 = fmaf(P[(x + 3) * kRank + j], qg[x + 3], a3);
-    }
-    for (; x < d; x++) a0 = fmaf(P[x * kRank + j], qg[x], a0);
-    y[o] = (a0 + a1) + (a2 + a3);
+  for (int i = threadIdx.x; i < Hkv * d; i += blockDim.x) {
+    const int h = i / d, x = i % d;
+    float acc = 0.f;
+    for (int gg = 0; gg < G; gg++) acc = __fadd_rn(acc, bf16_bits_to_f32(qb[(h * G + gg) * d + x]));
+    qs[i] = acc;
   }
   __syncthreads();
   const int width = Hkv * kRank;
   float amax = 0.f;
   for (int m = threadIdx.x; m < width; m += blockDim.x) {
     const int h = m / kRank, j = m % kRank;
-    float acc = 0.f;
-    for (int gg = 0; gg < G; gg++) acc = __fadd_rn(acc, y[(h * G + gg) * kRank + j]);
+    const float* qh = qs + h * d;
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    int x = 0;
+    for (; x + 3 < d; x += 4) {
+      a0 = fmaf(__ldg(basis + x * kRank + j), qh[x], a0);
+      a1 = fmaf(__ldg(basis + (x + 1) * kRank + j), qh[x + 1], a1);
+      a2 = fmaf(__ldg(basis + (x + 2) * kRank + j), qh[x + 2], a2);
+      a3 = fmaf(__ldg(basis + (x + 3) * kRank + j), qh[x + 3], a3);
+    }
+    for (; x < d; x++) a0 = fmaf(__ldg(basis + x * kRank + j), qh[x], a0);
+    float acc = (a0 + a1) + (a2 + a3);
     if (c) acc = __fmul_rn(acc, c[m]);
     qp[m] = acc;
     amax = fmaxf(amax, fabsf(acc));
@@ -217,9 +214,7 @@ SKV_EXPORT int skv_sketch_query(const uint16_t* q, int B, int Hq, int Hkv, int d
     return SKV_EINVAL;
   if (B == 0) return SKV_OK;
   if (!q || !basis || !out || !aligned16(basis)) return SKV_EINVAL;
-  const size_t smem =
-      (static_cast<size_t>(d) * kRank + static_cast<size_t>(Hq) * d + Hq * kRank + Hkv * kRank) *
-      sizeof(float);
+  const size_t smem = (static_cast<size_t>(Hkv) * d + Hkv * kRank) * sizeof(float);
   if (smem > 220 * 1024) return SKV_EUNSUPPORTED;
   if (cudaFuncSetAttribute(sketch_query_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)

@@ -349,3 +349,100 @@ def test_attention_is_deterministic(skv):
         outs.append(out)
     torch.cuda.synchronize()
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
+
+
+# ---------------------------------------------------------------------------
+# a3 + a4 fused (one cooperative launch)
+# ---------------------------------------------------------------------------
+
+def run_fused(skv, mode, query, keys, L, k, S=0, W=0, ratio=1, want_keys=True):
+    B, n_cap = keys.shape[0], keys.shape[1]
+    max_rows = (S + k + W) if ratio == 1 else ratio * k + ratio - 1
+    idx = torch.full((B, max_rows), -7, dtype=torch.int32, device="cuda")
+    cnt = torch.zeros((B,), dtype=torch.int32, device="cuda")
+    okeys = torch.zeros((B, n_cap), dtype=torch.int32, device="cuda") if want_keys else None
+    ws = torch.zeros((skv.score_select_workspace_size(B),), dtype=torch.uint8, device="cuda")
+    st = status_word()
+    for _ in range(2):  # the workspace must be reusable without clearing
+        skv.score_select(mode, query, keys, T.dev(L), k, idx, cnt, ws, S=S, W=W, ratio=ratio, order_keys=okeys,
+                         status=st)
+    check_status(st)
+    return T.host(idx), T.host(cnt), (T.host(okeys).view(np.uint32) if want_keys else None)
+
+
+@pytest.mark.parametrize("lengths,width,k,S,W", [
+    ([250_000, 250_000], 256, 2048, 64, 1024),
+    ([9000, 3136, 3137, 20, 40000, 70001, 5000, 1], 256, 2048, 64, 1024),
+    ([4096, 999], 128, 512, 64, 256),
+    ([2500, 7000, 12000], 512, 100, 8, 16),
+])
+def test_score_select_int4_bit_exact(skv, orc, lengths, width, k, S, W):
+    rng = np.random.default_rng(1000 + sum(lengths))
+    B, n_cap = len(lengths), max(lengths)
+    q8 = rng.integers(-127, 128, (B, width)).astype(np.int8)
+    sk = rng.integers(0, 256, (B, n_cap, width // 2)).astype(np.uint8)
+    L = np.array(lengths, np.int32)
+    ref = orc.index_score(orc.SKETCH_INT4, q8, sk, L, S=S, W=W)
+    ri, rc = orc.topk_select(ref["okey"], L, k, S=S, W=W)
+    gi, gc, gk = run_fused(skv, skv.SKETCH_INT4, T.dev(q8), T.dev(sk), L, k, S, W)
+    assert np.array_equal(gc, rc)
+    for b in range(B):
+        assert np.array_equal(gi[b, :gc[b]], ri[b, :rc[b]])
+        if lengths[b] > S + W + k:
+            assert np.array_equal(gk[b, S:lengths[b] - W], ref["okey"][b, S:lengths[b] - W])
+
+
+@pytest.mark.parametrize("distinct", [1, 2, 5])
+def test_score_select_ties(skv, orc, distinct):
+    """All rows drawn from a few distinct sketches: massive exact ties, incl. the
+    case where every candidate has the same key."""
+    rng = np.random.default_rng(77 + distinct)
+    B, n_cap, width, k, S, W = 3, 30000, 256, 2048, 64, 1024
+    q8 = rng.integers(-127, 128, (B, width)).astype(np.int8)
+    proto = rng.integers(0, 256, (distinct, width // 2)).astype(np.uint8)
+    sk = proto[rng.integers(0, distinct, (B, n_cap))]
+    L = np.array([30000, 29000, 5000], np.int32)
+    ref = orc.index_score(orc.SKETCH_INT4, q8, sk, L, S=S, W=W)
+    ri, rc = orc.topk_select(ref["okey"], L, k, S=S, W=W)
+    gi, gc, _ = run_fused(skv, skv.SKETCH_INT4, T.dev(q8), T.dev(sk), L, k, S, W, want_keys=False)
+    assert np.array_equal(gc, rc)
+    for b in range(B):
+        assert np.array_equal(gi[b, :gc[b]], ri[b, :rc[b]])
+
+
+def test_score_select_float_modes_match_two_calls(skv, orc):
+    rng = np.random.default_rng(4321)
+    # pooled bf16, ratio 4
+    B, nb_cap = 3, 70000
+    qi = wl.to_bf16_bits(rng.standard_normal((B, 128)).astype(np.float32))
+    pk = wl.to_bf16_bits(rng.standard_normal((B, nb_cap, 128)).astype(np.float32))
+    L = np.array([4 * nb_cap, 4 * 30000 + 3, 2051], np.int32)
+    gi, gc, gk = run_fused(skv, skv.POOLED_BF16, T.bf16_dev(qi), T.bf16_dev(pk), L, 512, ratio=4)
+    okeys = torch.zeros((B, nb_cap), dtype=torch.int32, device="cuda")
+    skv.index_score(skv.POOLED_BF16, T.bf16_dev(qi), T.bf16_dev(pk), T.dev(L), okeys, ratio=4)
+    si, sc = run_topk(skv, T.host(okeys).view(np.uint32), L, 512, ratio=4)
+    assert np.array_equal(gc, sc)
+    for b in range(B):
+        assert np.array_equal(gi[b, :gc[b]], si[b, :sc[b]])
+    # against the oracle: selections differ only within 1e-3 of the k-th score
+    ref = orc.index_score(orc.POOLED_BF16, qi, pk, L, ratio=4)
+    ri, rc = orc.topk_select(ref["okey"], L, 512, ratio=4)
+    for b in range(2):
+        nb = L[b] // 4
+        kth = np.sort(ref["fscore"][b, :nb])[::-1][511]
+        gblk = set((gi[b, :4 * 512:4] // 4).tolist())
+        rblk = set((ri[b, :4 * 512:4] // 4).tolist())
+        for blk in gblk ^ rblk:
+            assert abs(ref["fscore"][b, blk] - kth) <= 1e-3 * abs(kth)
+    # fp32 sketch
+    B, n_cap, width = 2, 20000, 128
+    qp = rng.standard_normal((B, width)).astype(np.float32)
+    s = rng.standard_normal((B, n_cap, width)).astype(np.float32)
+    L = np.array([20000, 9000], np.int32)
+    gi, gc, _ = run_fused(skv, skv.SKETCH_F32, T.dev(qp), T.dev(s), L, 512, 64, 256, want_keys=False)
+    okeys = torch.zeros((B, n_cap), dtype=torch.int32, device="cuda")
+    skv.index_score(skv.SKETCH_F32, T.dev(qp), T.dev(s), T.dev(L), okeys, S=64, W=256)
+    si, sc = run_topk(skv, T.host(okeys).view(np.uint32), L, 512, S=64, W=256)
+    assert np.array_equal(gc, sc)
+    for b in range(B):
+        assert np.array_equal(gi[b, :gc[b]], si[b, :sc[b]])
