@@ -8,9 +8,10 @@ per-(row, head) fp16 scale, int4 rank-64 key sketch, top-2048 + 64 sinks +
 own write path.
 
 One step = one decode token for all 8 requests through all 16 layers; per
-layer: sketch + int8 encoding of the appended token (a1), folded int8 query
-(a2), int4 score scan (a3), radix top-k with sink/tail union (a4), resident
-rows (a5 is the identity), split-K int8 attention (a6).  The 16-layer step is
+layer three launches: the appended token's sketch and int8 K/V rows plus the
+folded int8 query (a1 + a2, one kernel), the int4 score scan fused with the
+radix top-k and the sink/tail union (a3 + a4), and split-K int8 attention
+over the resident rows (a5 is the identity, a6).  The 16-layer step is
 captured in one CUDA graph.  Layer-steps/s = steps/s x 16; tokens/s = steps/s
 x 8.
 
@@ -231,20 +232,20 @@ class SketchWorkloadGPU:
         self.tws = torch.zeros((skv.score_select_workspace_size(B),), dtype=torch.uint8, device=dev)
         self.aws = torch.zeros((skv.attend_workspace_size(B, W_HQ, W_HKV, W_D, MAX_ROWS),), dtype=torch.uint8,
                                device=dev)
+        self.pws = torch.zeros((skv.decode_prepare_workspace_size(B, W_HKV),), dtype=torch.uint8, device=dev)
         self.out = torch.zeros((L, B, W_HQ, W_D), dtype=torch.float32, device=dev)
         self.status = torch.zeros((1,), dtype=torch.int32, device=dev)
         torch.cuda.synchronize()
 
-    KERNELS_PER_LAYER = 6  # a1 1, int8 encodings 2, a2 1, a3+a4 fused 1, a6 1
+    KERNELS_PER_LAYER = 3  # a1 + int8 append + a2 fused, a3 + a4 fused, a6
 
     def layer(self, l, marks=None):
         skv, st = self.skv, self.status
         ev = (lambda name: marks(l, name)) if marks else (lambda name: None)
         ev("start")
-        skv.sketch_project(self.newk[l], self.U, self.c, self.sk[l].view(W_B * W_T, -1), out_rows=self.new_rows)
-        skv.quantize_int8_rows(self.newk[l], self.k8[l], self.ks[l], out_rows=self.new_rows)
-        skv.quantize_int8_rows(self.newv[l], self.v8[l], self.vs[l], out_rows=self.new_rows)
-        skv.sketch_query(self.q[l], W_HKV, self.U, self.c, self.q8, self.sigma)
+        skv.decode_prepare(self.q[l], self.newk[l], self.newv[l], self.U, self.c, self.new_rows,
+                           self.sk[l].view(W_B * W_T, -1), self.k8[l], self.ks[l], self.v8[l], self.vs[l], self.q8,
+                           self.pws, sigma=self.sigma)
         ev("scan0")
         skv.score_select(skv.SKETCH_INT4, self.q8, self.sk[l], self.lengths, W_K, self.idx, self.cnt, self.tws,
                          S=W_S, W=W_W, status=st)

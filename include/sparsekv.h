@@ -134,6 +134,33 @@ int skv_sketch_query(const uint16_t *q, int B, int Hq, int Hkv, int d, int r,
                      void *stream);
 
 /* ========================================================================== */
+/* a1 + a2 + int8 append fused: the per-layer work before the score scan.      */
+/* ========================================================================== */
+/*
+ * For every request b: appends the current token -- its int4 key sketch
+ * (skv_sketch_project with c) and its int8 K and V rows (skv_quantize_int8_rows)
+ * -- at pool row new_rows[b], and folds the query into q8 / sigma
+ * (skv_sketch_query with c), in one launch.  The folded query is computed as
+ * c[h][j] * (basis^T (sum of the group's query heads))[j], the same linear map
+ * as skv_sketch_query; codes may differ from it by one only at rounding ties.
+ *   q       bf16 [B][Hq][d]         new_k, new_v  bf16 [B][Hkv][d]
+ *   basis   fp32 [d][r]             c  fp32 [Hkv][r]
+ *   new_rows int64 [B]: pool row of the current token of request b
+ *   sketch  u8 [rows][Hkv*r/2]      k8, v8  int8 [rows][Hkv][d]
+ *   k_scale, v_scale  fp16 [rows][Hkv]
+ *   q8      int8 [B][Hkv*r]         sigma  fp32 [B] (may be NULL)
+ *   workspace  skv_decode_prepare_workspace_size(B, Hkv, r) bytes, zero-filled
+ *              before first use (its tickets return to zero).
+ * Constraints: r == 64, Hq % Hkv == 0, d <= 512.
+ */
+size_t skv_decode_prepare_workspace_size(int B, int Hkv, int r);
+int skv_decode_prepare(const uint16_t *q, const uint16_t *new_k, const uint16_t *new_v, int B,
+                       int Hq, int Hkv, int d, int r, const float *basis, const float *c,
+                       const int64_t *new_rows, uint8_t *sketch, int8_t *k8, uint16_t *k_scale,
+                       int8_t *v8, uint16_t *v_scale, int8_t *q8, float *sigma, void *workspace,
+                       size_t workspace_bytes, void *stream);
+
+/* ========================================================================== */
 /* a2': pooled indexer keys ([P3]: indexer keys compressed by ratio 4; [P4]   */
 /* "What Needs to Stay in VRAM": keys pooled per block, kept in HBM).         */
 /* ========================================================================== */

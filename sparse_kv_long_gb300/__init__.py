@@ -50,6 +50,9 @@ def _load():
                 "skv_sketch_project": ([P, i64, i32, i32, i32, P, P, P, P, P], i32),
                 "skv_sketch_query": ([P, i32, i32, i32, i32, i32, P, P, P, P, P], i32),
                 "skv_pool_keys": ([P, i32, i64, i32, i32, i64, i64, P, P], i32),
+                "skv_decode_prepare_workspace_size": ([i32, i32, i32], sz),
+                "skv_decode_prepare": ([P, P, P, i32, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P, P, P, sz, P],
+                                       i32),
                 "skv_index_score": ([i32, i32, i32, P, P, i64, P, i32, i32, i32, P, P, P, P], i32),
                 "skv_topk_workspace_size": ([i32], sz),
                 "skv_topk_select": ([i32, P, i64, P, i32, i32, i32, i32, P, i32, P, P, sz, P, P], i32),
@@ -117,6 +120,23 @@ def sketch_query(q, Hkv, basis, c, out, sigma=None, stream=None):
     _check("skv_sketch_query", _load().skv_sketch_query(
         _ptr(q), B, Hq, Hkv, d, r, _ptr(basis), _ptr(c), _ptr(out), _ptr(sigma), _stream(stream)))
     return out
+
+
+def decode_prepare_workspace_size(B, Hkv, r=64) -> int:
+    return int(_load().skv_decode_prepare_workspace_size(B, Hkv, r))
+
+
+def decode_prepare(q, new_k, new_v, basis, c, new_rows, sketch, k8, k_scale, v8, v_scale, q8, workspace,
+                   sigma=None, stream=None):
+    """Append the current token (sketch + int8 K/V rows at new_rows) and fold the query into q8."""
+    B, Hq, d = q.shape
+    Hkv = new_k.shape[1]
+    r = basis.shape[1]
+    _check("skv_decode_prepare", _load().skv_decode_prepare(
+        _ptr(q), _ptr(new_k), _ptr(new_v), B, Hq, Hkv, d, r, _ptr(basis), _ptr(c), _ptr(new_rows), _ptr(sketch),
+        _ptr(k8), _ptr(k_scale), _ptr(v8), _ptr(v_scale), _ptr(q8), _ptr(sigma), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return q8
 
 
 def pool_keys(keys, pooled, first_block, n_blocks, ratio=4, stream=None):

@@ -7,34 +7,40 @@
 // [token][kv_head][dim].
 //
 // Design.  A CTA owns one (request, KV head, group of up to 8 query heads,
-// split of the selected rows).  It first stages the split's physical row
-// numbers and (int8) scales in shared memory.  Each of its 4 warps then takes
-// 16-row tiles in turn through a private 2-stage shared-memory ring: lanes
-// 0..15 each issue two TMA bulk copies (cp.async.bulk, one K row and one V
-// row of the KV head) completing on the stage's mbarrier, so the next tile is
-// in flight while the current one is computed and no registers hold pending
-// loads.  Rows land at offsets chosen so that the fragment loads below are
-// free of shared-memory bank conflicts.
+// split of the selected rows) and runs two warp pairs.  It first stages the
+// split's physical row numbers, the int8 scales and the query heads in shared
+// memory.  Each pair takes 16-row tiles in turn through its own 2-stage
+// shared-memory ring: lanes 0..15 of the pair's first warp issue two TMA bulk
+// copies each (cp.async.bulk, one K row and one V row of the KV head)
+// completing on the stage's mbarrier, so the next tile is in flight while the
+// current one is computed.  Rows land at pitches chosen so that the fragment
+// loads below are free of shared-memory bank conflicts.
 //
-// Per tile a warp computes S = Q K^T with m16n8k16 tensor-core MMAs (query
-// heads are the M rows, padded to 16; two n8 tiles cover the 16 rows), runs
-// the online softmax on the accumulator registers, and accumulates
-// O^T += V^T P^T with the probabilities reused from the S accumulators as the
-// B operand.  The head dimension is permuted consistently on Q and K so that a
-// lane reads contiguous 16-byte pieces of a row; the V dimension is permuted
-// so that a lane reads 32 contiguous dims of 4 rows.  int8 codes convert to
-// fp16 exactly (0x6400 magic); the K scale multiplies the logits in fp32 and
-// the V scale is folded into P.  bf16 rows keep bf16 operands with P split
-// into two bf16 terms.  The warps' partials (m, l, O) merge in shared memory,
-// each CTA writes one partial, and the last CTA of a (request, head group)
-// merges the splits in split order (deterministic) and writes the output.
+// The two warps of a pair split the head dimension: warp e owns dims
+// [128e, 128e + 128) for both products.  Per tile each computes the partial
+// logits of its half with m16n8k16 tensor-core MMAs (query heads are the M
+// rows, padded to 16; two n8 tiles cover the 16 rows); the halves are
+// exchanged through shared memory and added in a fixed order, so both warps
+// run the same online softmax on bit-identical logits; each then accumulates
+// its half of O^T += V^T P^T with the probabilities reused from the
+// accumulators as the B operand.  The head dimension is permuted consistently
+// on Q and K so that a lane reads contiguous 16-byte pieces of a row; the V
+// dimension is permuted so that a lane reads 16 contiguous dims of 4 rows.
+// int8 codes convert to fp16 exactly (0x6400 magic); the K scale multiplies
+// the logits in fp32 and the V scale is folded into P.  bf16 rows keep bf16
+// operands with P split into two bf16 terms.  The pairs' partials (m, l, O)
+// merge in shared memory, each CTA writes one partial, and the last CTA of a
+// (request, head group) merges the splits in split order (deterministic) and
+// writes the output.
 #include "common.cuh"
 
 namespace skv {
 namespace {
 
 constexpr int D = 256;
-constexpr int kWarps = 4;
+constexpr int DH = D / 2;          // dims per warp of a pair
+constexpr int kPairs = 2;
+constexpr int kWarps = 2 * kPairs;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kPart = 16 + 8 * D;  // m[8], l[8], O[8][D] floats per partial
 constexpr int kMaxSplit = 64;
@@ -42,27 +48,20 @@ constexpr int kMaxRowsPerSplit = 512;
 constexpr int kStages = 2;
 constexpr int kTileRows = 16;
 constexpr long kWaitLimit = 1L << 20;  // bounded mbarrier polls (~1 s with backoff)
-// Warp partials in shared memory: float (head, dim) at head*kMH + (dim/32)*33 +
+// Pair partials in shared memory: float (head, dim) at head*kMH + (dim/32)*33 +
 // dim%32, so the fragment-order stores of a warp hit 32 different banks.
 constexpr int kMH = 8 * 33 + 4;
-constexpr int kMW = 8 * kMH;  // floats per warp
+constexpr int kMW = 8 * kMH;  // floats per pair
 __device__ __forceinline__ int mix(int head, int dim) { return head * kMH + (dim >> 5) * 33 + (dim & 31); }
 
 template <int KV>
 struct Geo {
   static constexpr int ES = KV == SKV_KV_INT8 ? 1 : 2;
-  static constexpr int RB = D * ES;                                  // bytes of one row of one head
-  static constexpr int KP = RB + 64;                                 // K row pitch in smem
-  static constexpr int VP = KV == SKV_KV_INT8 ? RB + 128 : RB + 64;  // V row pitch in smem
+  static constexpr int RB = D * ES;       // bytes of one row of one head
+  static constexpr int KP = RB + 64;      // K row pitch: 16-byte units = 4 (mod 8)
+  static constexpr int VP = RB + 16;      // V row pitch: 16-byte units = 1 (mod 8)
   static constexpr int STAGE = kTileRows * (KP + VP);
-  static constexpr int WARP_BYTES = kStages * STAGE;
-  // Row r's V slot starts 16*h(r) bytes into its pitch so that the 8 lanes of a
-  // quarter-warp read 8 different bank groups.
-  __device__ static int voff(int r) {
-    const int q = (r >> 1) & 3;
-    const int hsh = KV == SKV_KV_INT8 ? (q == 0 ? 0 : q == 1 ? 1 : q == 2 ? 4 : 5) : q;
-    return r * VP + 16 * hsh;
-  }
+  static constexpr int PAIR_BYTES = kStages * STAGE;
 };
 
 struct AttendArgs {
@@ -173,14 +172,41 @@ __device__ __forceinline__ uint32_t word(const uint4& v, int i) {
   return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
+// Barrier of the 64 threads of warp pair `pair` (named barriers 1 and 2).
+__device__ __forceinline__ void pair_sync(int pair) {
+  if (pair == 0)
+    asm volatile("bar.sync 1, 64;" ::: "memory");
+  else
+    asm volatile("bar.sync 2, 64;" ::: "memory");
+}
+
+// Pair barrier that also ANDs a predicate across the 64 threads, so both warps
+// of the pair take the same branch afterwards.
+__device__ __forceinline__ bool pair_all(int pair, bool v) {
+  uint32_t r;
+  if (pair == 0)
+    asm volatile("{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, 1, 64, p;\n selp.u32 %0, 1, 0, q;\n}"
+                 : "=r"(r)
+                 : "r"(static_cast<uint32_t>(v))
+                 : "memory");
+  else
+    asm volatile("{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, 2, 64, p;\n selp.u32 %0, 1, 0, q;\n}"
+                 : "=r"(r)
+                 : "r"(static_cast<uint32_t>(v))
+                 : "memory");
+  return r != 0;
+}
+
 template <int KV>
-__global__ __launch_bounds__(kThreads) void attend_kernel(AttendArgs a) {
+__global__ __launch_bounds__(kThreads, 4) void attend_kernel(AttendArgs a) {
   using Gm = Geo<KV>;
   extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ uint64_t bars[kWarps][kStages];
+  __shared__ uint64_t bars[kPairs][kStages];
   __shared__ int64_t s_prow[kMaxRowsPerSplit];
-  __shared__ float s_ks[kMaxRowsPerSplit], s_vs[kMaxRowsPerSplit];
-  __shared__ float sm_m[kWarps][8], sm_l[kWarps][8];
+  __shared__ float s_ks[KV == SKV_KV_INT8 ? kMaxRowsPerSplit : 1], s_vs[KV == SKV_KV_INT8 ? kMaxRowsPerSplit : 1];
+  __shared__ __align__(16) uint16_t s_q[8][D];
+  __shared__ __align__(16) float s_x[kPairs][2][32][4];  // partial logits of each warp of a pair
+  __shared__ float sm_m[kPairs][8], sm_l[kPairs][8];
   __shared__ float fin_m[8], fin_l[8];
   __shared__ float wts[8][kMaxSplit];
   __shared__ int is_last;
@@ -188,10 +214,8 @@ __global__ __launch_bounds__(kThreads) void attend_kernel(AttendArgs a) {
   const int b = blockIdx.z, hy = blockIdx.y, split = blockIdx.x;
   const int h = hy / a.hgroups, hg = hy % a.hgroups;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int pair = warp >> 1, e = warp & 1;  // e: which half of the head dimension
   const int g = lane >> 2, c = lane & 3;
-  const int head_local = hg * 8 + g;
-  const bool head_ok = head_local < a.G;
-  const int qh = h * a.G + head_local;
 
   int n = a.count[b];
   n = n < 0 ? 0 : (n > a.max_rows ? a.max_rows : n);
@@ -203,7 +227,7 @@ __global__ __launch_bounds__(kThreads) void attend_kernel(AttendArgs a) {
   const uint8_t* kbase = a.kpool + static_cast<int64_t>(h) * Gm::RB;
   const uint8_t* vbase = a.vpool + static_cast<int64_t>(h) * Gm::RB;
 
-  // ---- stage row numbers and scales of this split ----------------------------
+  // ---- stage row numbers, scales and the query heads ---------------------------
   for (int i = threadIdx.x; i < nr; i += blockDim.x) {
     const int32_t rid = a.rows[static_cast<int64_t>(b) * a.max_rows + r0 + i];
     const int64_t p = static_cast<int64_t>(b) * a.req_row_stride + rid;
@@ -218,111 +242,124 @@ __global__ __launch_bounds__(kThreads) void attend_kernel(AttendArgs a) {
       s_vs[i] = pr >= 0 ? __half2float(__ushort_as_half(a.vscale[pr * a.Hkv + h])) : 0.f;
     }
   }
-  if (lane == 0) {
-    for (int s = 0; s < kStages; s++) mbar_init(&bars[warp][s], 1);
+  for (int i = threadIdx.x; i < 8 * D / 8; i += blockDim.x) {  // 16-byte pieces of 8 query heads
+    const int hd = i / (D / 8), x8 = i % (D / 8);
+    const int hl = hg * 8 + hd;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (hl < a.G)
+      v = *reinterpret_cast<const uint4*>(a.q + (static_cast<int64_t>(b) * a.Hq + h * a.G + hl) * D + 8 * x8);
+    *reinterpret_cast<uint4*>(&s_q[hd][8 * x8]) = v;
+  }
+  if (threadIdx.x < kPairs * kStages) {
+    mbar_init(&bars[threadIdx.x / kStages][threadIdx.x % kStages], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
 
-  // ---- query fragments (A operand of S = Q K^T), permuted head dim ----------
-  uint32_t qa[16][2];
-  {
-    const uint16_t* qrow = a.q + (static_cast<int64_t>(b) * a.Hq + (head_ok ? qh : 0)) * D;
+  // ---- query fragments of this warp's half (A operand of S = Q K^T) -----------
+  // k-step ks covers 4 dims of the half: base(ks) below; slots 2c,2c+1 <- +0,+1
+  // and 2c+8,2c+9 <- +2,+3, the same permutation as the K fragments.
+  uint32_t qa[8][2];
 #pragma unroll
-    for (int ks = 0; ks < 16; ks++) {
-      const int base = KV == SKV_KV_INT8 ? 16 * (c + 4 * (ks >> 2)) + 4 * (ks & 3)
-                                         : 8 * (c + 4 * (ks >> 1)) + 4 * (ks & 1);
-      uint2 v = head_ok ? *reinterpret_cast<const uint2*>(qrow + base) : make_uint2(0u, 0u);
-      if (KV == SKV_KV_INT8) {
-        qa[ks][0] = pack_h2(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u));
-        qa[ks][1] = pack_h2(__uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
-      } else {
-        qa[ks][0] = v.x;
-        qa[ks][1] = v.y;
-      }
+  for (int ks = 0; ks < 8; ks++) {
+    const int base = KV == SKV_KV_INT8 ? DH * e + 16 * (c + 4 * (ks >> 2)) + 4 * (ks & 3)
+                                       : DH * e + 8 * (c + 4 * (ks >> 1)) + 4 * (ks & 1);
+    const uint2 v = *reinterpret_cast<const uint2*>(&s_q[g][base]);
+    if (KV == SKV_KV_INT8) {
+      qa[ks][0] = pack_h2(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u));
+      qa[ks][1] = pack_h2(__uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
+    } else {
+      qa[ks][0] = v.x;
+      qa[ks][1] = v.y;
     }
   }
 
-  float o[16][4];
+  float o[8][4];
 #pragma unroll
-  for (int mt = 0; mt < 16; mt++) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+  for (int mt = 0; mt < 8; mt++) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
   float m_run = -INFINITY, l_part = 0.f;
 
-  unsigned char* wbuf = smem + warp * Gm::WARP_BYTES;
+  unsigned char* pbuf = smem + pair * Gm::PAIR_BYTES;
   const int ntiles = (nr + kTileRows - 1) / kTileRows;
   int my_tiles = 0;
-  for (int t = warp; t < ntiles; t += kWarps) my_tiles++;
+  for (int t = pair; t < ntiles; t += kPairs) my_tiles++;
 
-  for (int it = 0; it < kStages && it < my_tiles; it++) {
-    // Lanes 0..15 copy row `lane` of the warp's tile `it` into stage `it`.
-    // Absent rows copy pool row 0 and are masked below.
-    unsigned char* kst = wbuf + it * Gm::STAGE;
+  // Lanes 0..15 of the pair's first warp copy row `lane` of the pair's tile
+  // `it` into stage it % kStages.  Absent rows copy pool row 0 and are masked.
+  auto issue = [&](int it) {
+    const int stage = it % kStages;
+    unsigned char* kst = pbuf + stage * Gm::STAGE;
     unsigned char* vst = kst + kTileRows * Gm::KP;
-    uint64_t* bar = &bars[warp][it];
+    uint64_t* bar = &bars[pair][stage];
     if (lane == 0) mbar_arrive_expect_tx(bar, kTileRows * 2 * Gm::RB);
     __syncwarp();
     if (lane < kTileRows) {
-      const int idx = (warp + kWarps * it) * kTileRows + lane;
+      const int idx = (pair + kPairs * it) * kTileRows + lane;
       int64_t pr = idx < nr ? s_prow[idx] : -1;
       if (pr < 0) pr = 0;
       bulk_g2s(kst + lane * Gm::KP, kbase + pr * pitch, Gm::RB, bar);
-      bulk_g2s(vst + Gm::voff(lane), vbase + pr * pitch, Gm::RB, bar);
+      bulk_g2s(vst + lane * Gm::VP, vbase + pr * pitch, Gm::RB, bar);
     }
-  }
+  };
+  if (e == 0)
+    for (int it = 0; it < kStages && it < my_tiles; it++) issue(it);
 
   int completed = 0;  // tiles whose copies have landed
   for (int it = 0; it < my_tiles; it++) {
     const int stage = it % kStages;
     const uint32_t parity = (it / kStages) & 1;
-    if (!mbar_wait(&bars[warp][stage], parity)) {
+    // Both warps of the pair must agree, or one would wait for the other at
+    // the pair barriers below.
+    if (!pair_all(pair, mbar_wait(&bars[pair][stage], parity))) {
       set_status(a.status, SKV_DEV_TIMEOUT);
       break;
     }
     completed = it + 1;
-    const unsigned char* kst = wbuf + stage * Gm::STAGE;
+    const unsigned char* kst = pbuf + stage * Gm::STAGE;
     const unsigned char* vst = kst + kTileRows * Gm::KP;
-    const int tbase = (warp + kWarps * it) * kTileRows;  // index of the tile's first row in the split
+    const int tbase = (pair + kPairs * it) * kTileRows;  // index of the tile's first row in the split
 
-    // ---- S = Q K^T ------------------------------------------------------------
+    // ---- partial S = Q K^T over this warp's half of the dims -------------------
     float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+    float t0[4] = {0.f, 0.f, 0.f, 0.f}, t1[4] = {0.f, 0.f, 0.f, 0.f};  // second chains (odd k-steps)
     if (KV == SKV_KV_INT8) {
-      uint4 k0[4], k1[4];
 #pragma unroll
-      for (int i = 0; i < 4; i++) {
-        k0[i] = lds128(kst + g * Gm::KP + 16 * (c + 4 * i));
-        k1[i] = lds128(kst + (g + 8) * Gm::KP + 16 * (c + 4 * i));
-      }
-      float t0[4] = {0.f, 0.f, 0.f, 0.f}, t1[4] = {0.f, 0.f, 0.f, 0.f};  // second chains (odd k-steps)
+      for (int i = 0; i < 2; i++) {
+        const uint4 ka = lds128(kst + g * Gm::KP + DH * e + 16 * (c + 4 * i));
+        const uint4 kb = lds128(kst + (g + 8) * Gm::KP + DH * e + 16 * (c + 4 * i));
 #pragma unroll
-      for (int ks = 0; ks < 16; ks++) {
-        const uint32_t w0 = word(k0[ks >> 2], ks & 3) ^ 0x80808080u;
-        const uint32_t w1 = word(k1[ks >> 2], ks & 3) ^ 0x80808080u;
-        float* d0 = (ks & 1) ? t0 : s0;
-        float* d1 = (ks & 1) ? t1 : s1;
-        mma_f16(d0, qa[ks][0], 0u, qa[ks][1], 0u, u8pair_to_h2(w0, 0x4140), u8pair_to_h2(w0, 0x4342));
-        mma_f16(d1, qa[ks][0], 0u, qa[ks][1], 0u, u8pair_to_h2(w1, 0x4140), u8pair_to_h2(w1, 0x4342));
-      }
-#pragma unroll
-      for (int j = 0; j < 4; j++) {
-        s0[j] += t0[j];
-        s1[j] += t1[j];
+        for (int ws = 0; ws < 4; ws++) {
+          const int ks = 4 * i + ws;
+          const uint32_t w0 = word(ka, ws) ^ 0x80808080u;
+          const uint32_t w1 = word(kb, ws) ^ 0x80808080u;
+          float* d0 = (ks & 1) ? t0 : s0;
+          float* d1 = (ks & 1) ? t1 : s1;
+          mma_f16(d0, qa[ks][0], 0u, qa[ks][1], 0u, u8pair_to_h2(w0, 0x4140), u8pair_to_h2(w0, 0x4342));
+          mma_f16(d1, qa[ks][0], 0u, qa[ks][1], 0u, u8pair_to_h2(w1, 0x4140), u8pair_to_h2(w1, 0x4342));
+        }
       }
     } else {
-      float t0[4] = {0.f, 0.f, 0.f, 0.f}, t1[4] = {0.f, 0.f, 0.f, 0.f};  // second chains (odd k-steps)
 #pragma unroll
-      for (int i = 0; i < 8; i++) {
-        const uint4 ka = lds128(kst + g * Gm::KP + 16 * (c + 4 * i));
-        const uint4 kb = lds128(kst + (g + 8) * Gm::KP + 16 * (c + 4 * i));
+      for (int i = 0; i < 4; i++) {
+        const uint4 ka = lds128(kst + g * Gm::KP + 2 * DH * e + 16 * (c + 4 * i));
+        const uint4 kb = lds128(kst + (g + 8) * Gm::KP + 2 * DH * e + 16 * (c + 4 * i));
         mma_bf16(s0, qa[2 * i][0], 0u, qa[2 * i][1], 0u, ka.x, ka.y);
         mma_bf16(s1, qa[2 * i][0], 0u, qa[2 * i][1], 0u, kb.x, kb.y);
         mma_bf16(t0, qa[2 * i + 1][0], 0u, qa[2 * i + 1][1], 0u, ka.z, ka.w);
         mma_bf16(t1, qa[2 * i + 1][0], 0u, qa[2 * i + 1][1], 0u, kb.z, kb.w);
       }
-#pragma unroll
-      for (int j = 0; j < 4; j++) {
-        s0[j] += t0[j];
-        s1[j] += t1[j];
-      }
+    }
+    // ---- exchange halves: full logits = half 0 + half 1 in both warps -------
+    {
+      float4 mine = make_float4(s0[0] + t0[0], s0[1] + t0[1], s1[0] + t1[0], s1[1] + t1[1]);
+      *reinterpret_cast<float4*>(s_x[pair][e][lane]) = mine;
+      pair_sync(pair);
+      const float4 other = *reinterpret_cast<const float4*>(s_x[pair][1 - e][lane]);
+      const float4 h0 = e == 0 ? mine : other, h1 = e == 0 ? other : mine;
+      s0[0] = h0.x + h1.x;
+      s0[1] = h0.y + h1.y;
+      s1[0] = h0.z + h1.z;
+      s1[1] = h0.w + h1.w;
     }
 
     // ---- online softmax on S[head g][rows 2c, 2c+1, 2c+8, 2c+9] ---------------
@@ -360,34 +397,31 @@ __global__ __launch_bounds__(kThreads) void attend_kernel(AttendArgs a) {
     const float a_e = __shfl_sync(0xffffffffu, alpha, 8 * c);
     const float a_o = __shfl_sync(0xffffffffu, alpha, 8 * c + 4);
 #pragma unroll
-    for (int mt = 0; mt < 16; mt++) {
+    for (int mt = 0; mt < 8; mt++) {
       o[mt][0] *= a_e;
       o[mt][1] *= a_o;
       o[mt][2] *= a_e;
       o[mt][3] *= a_o;
     }
 
-    // ---- O^T += V^T P^T -------------------------------------------------------
+    // ---- this half of O^T += V^T P^T -----------------------------------------
+    // M-tile mt, slot g <-> dim 128e + 16g + 2mt, slot g+8 <-> the next dim.
     if (KV == SKV_KV_INT8) {
       const uint32_t bp0 = pack_h2(p[0] * vsc[0], p[1] * vsc[1]);
       const uint32_t bp1 = pack_h2(p[2] * vsc[2], p[3] * vsc[3]);
+      uint4 v[4];
 #pragma unroll
-      for (int hh = 0; hh < 2; hh++) {
-        uint4 v[4];
+      for (int r = 0; r < 4; r++) v[r] = lds128(vst + rr[r] * Gm::VP + DH * e + 16 * g);
 #pragma unroll
-        for (int r = 0; r < 4; r++) v[r] = lds128(vst + Gm::voff(rr[r]) + 32 * g + 16 * hh);
-#pragma unroll
-        for (int ws = 0; ws < 4; ws++) {
-          const int qq = 4 * hh + ws;  // dims 32g + 4qq .. 4qq+3
-          const uint32_t t01 = prmt(word(v[0], ws), word(v[1], ws), 0x5140) ^ 0x80808080u;
-          const uint32_t t23 = prmt(word(v[0], ws), word(v[1], ws), 0x7362) ^ 0x80808080u;
-          const uint32_t u01 = prmt(word(v[2], ws), word(v[3], ws), 0x5140) ^ 0x80808080u;
-          const uint32_t u23 = prmt(word(v[2], ws), word(v[3], ws), 0x7362) ^ 0x80808080u;
-          mma_f16(o[2 * qq], u8pair_to_h2(t01, 0x4140), u8pair_to_h2(t01, 0x4342), u8pair_to_h2(u01, 0x4140),
-                  u8pair_to_h2(u01, 0x4342), bp0, bp1);
-          mma_f16(o[2 * qq + 1], u8pair_to_h2(t23, 0x4140), u8pair_to_h2(t23, 0x4342),
-                  u8pair_to_h2(u23, 0x4140), u8pair_to_h2(u23, 0x4342), bp0, bp1);
-        }
+      for (int ws = 0; ws < 4; ws++) {  // dims 16g + 4ws .. +3 of the half
+        const uint32_t t01 = prmt(word(v[0], ws), word(v[1], ws), 0x5140) ^ 0x80808080u;
+        const uint32_t t23 = prmt(word(v[0], ws), word(v[1], ws), 0x7362) ^ 0x80808080u;
+        const uint32_t u01 = prmt(word(v[2], ws), word(v[3], ws), 0x5140) ^ 0x80808080u;
+        const uint32_t u23 = prmt(word(v[2], ws), word(v[3], ws), 0x7362) ^ 0x80808080u;
+        mma_f16(o[2 * ws], u8pair_to_h2(t01, 0x4140), u8pair_to_h2(t01, 0x4342), u8pair_to_h2(u01, 0x4140),
+                u8pair_to_h2(u01, 0x4342), bp0, bp1);
+        mma_f16(o[2 * ws + 1], u8pair_to_h2(t23, 0x4140), u8pair_to_h2(t23, 0x4342), u8pair_to_h2(u23, 0x4140),
+                u8pair_to_h2(u23, 0x4342), bp0, bp1);
       }
     } else {
       const uint32_t ph0 = pack_bf2(p[0], p[1]), ph1 = pack_bf2(p[2], p[3]);
@@ -395,13 +429,13 @@ __global__ __launch_bounds__(kThreads) void attend_kernel(AttendArgs a) {
       const float e2 = p[2] - __uint_as_float(ph1 << 16), e3 = p[3] - __uint_as_float(ph1 & 0xffff0000u);
       const uint32_t pl0 = pack_bf2(e0, e1), pl1 = pack_bf2(e2, e3);
 #pragma unroll
-      for (int hh = 0; hh < 4; hh++) {  // 16-byte piece hh: dims 32g + 8hh .. +7
+      for (int hh = 0; hh < 2; hh++) {  // 16-byte piece hh: dims 16g + 8hh .. +7 of the half
         uint4 v[4];
 #pragma unroll
-        for (int r = 0; r < 4; r++) v[r] = lds128(vst + Gm::voff(rr[r]) + 64 * g + 16 * hh);
+        for (int r = 0; r < 4; r++) v[r] = lds128(vst + rr[r] * Gm::VP + 2 * DH * e + 32 * g + 16 * hh);
 #pragma unroll
         for (int ws = 0; ws < 4; ws++) {
-          const int mt = 4 * hh + ws;  // dims 32g + 2mt, 32g + 2mt + 1
+          const int mt = 4 * hh + ws;  // dims 16g + 2mt, 16g + 2mt + 1 of the half
           const uint32_t a0 = prmt(word(v[0], ws), word(v[1], ws), 0x5410);
           const uint32_t a1 = prmt(word(v[0], ws), word(v[1], ws), 0x7632);
           const uint32_t a2 = prmt(word(v[2], ws), word(v[3], ws), 0x5410);
@@ -411,44 +445,34 @@ __global__ __launch_bounds__(kThreads) void attend_kernel(AttendArgs a) {
         }
       }
     }
-    __syncwarp();
+    pair_sync(pair);  // both warps are done with this stage (and with s_x)
     const int nx = it + kStages;
-    if (nx < my_tiles) {
-      // Reads of this stage are done; refill it with the warp's tile nx.
+    if (e == 0 && nx < my_tiles) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      unsigned char* kdst = wbuf + stage * Gm::STAGE;
-      unsigned char* vdst = kdst + kTileRows * Gm::KP;
-      uint64_t* bar = &bars[warp][stage];
-      if (lane == 0) mbar_arrive_expect_tx(bar, kTileRows * 2 * Gm::RB);
-      __syncwarp();
-      if (lane < kTileRows) {
-        const int idx = (warp + kWarps * nx) * kTileRows + lane;
-        int64_t pr = idx < nr ? s_prow[idx] : -1;
-        if (pr < 0) pr = 0;
-        bulk_g2s(kdst + lane * Gm::KP, kbase + pr * pitch, Gm::RB, bar);
-        bulk_g2s(vdst + Gm::voff(lane), vbase + pr * pitch, Gm::RB, bar);
-      }
+      issue(nx);
     }
   }
   // After a timeout, give the copies still in flight a bounded chance to land
   // before the buffers are reused for the merge.
   for (int it = completed; it < my_tiles && it < completed + kStages; it++)
-    mbar_wait(&bars[warp][it % kStages], (it / kStages) & 1);
+    mbar_wait(&bars[pair][it % kStages], (it / kStages) & 1);
 
-  // ---- merge the 4 warps (partials staged in the ring buffers) -------------------
+  // ---- merge the 2 pairs (partials staged in the ring buffers) --------------------
   __syncthreads();
-  float* sm_o = reinterpret_cast<float*>(smem);  // [kWarps][kMW], see mix()
-  float l_grp = l_part;
-  l_grp += __shfl_xor_sync(0xffffffffu, l_grp, 1);
-  l_grp += __shfl_xor_sync(0xffffffffu, l_grp, 2);
-  if (c == 0) {
-    sm_m[warp][g] = m_run;
-    sm_l[warp][g] = l_grp;
+  float* sm_o = reinterpret_cast<float*>(smem);  // [kPairs][kMW], see mix()
+  if (e == 0) {
+    float l_grp = l_part;
+    l_grp += __shfl_xor_sync(0xffffffffu, l_grp, 1);
+    l_grp += __shfl_xor_sync(0xffffffffu, l_grp, 2);
+    if (c == 0) {
+      sm_m[pair][g] = m_run;
+      sm_l[pair][g] = l_grp;
+    }
   }
 #pragma unroll
-  for (int mt = 0; mt < 16; mt++) {
-    const int d0 = 32 * g + 2 * mt;
-    float* ow = sm_o + warp * kMW;
+  for (int mt = 0; mt < 8; mt++) {
+    const int d0 = DH * e + 16 * g + 2 * mt;
+    float* ow = sm_o + pair * kMW;
     ow[mix(2 * c, d0)] = o[mt][0];
     ow[mix(2 * c + 1, d0)] = o[mt][1];
     ow[mix(2 * c, d0 + 1)] = o[mt][2];
@@ -460,22 +484,30 @@ __global__ __launch_bounds__(kThreads) void attend_kernel(AttendArgs a) {
   if (threadIdx.x < 8) {
     const int hd = threadIdx.x;
     float M = -INFINITY;
-    for (int w = 0; w < kWarps; w++) M = fmaxf(M, sm_m[w][hd]);
+    for (int w = 0; w < kPairs; w++) M = fmaxf(M, sm_m[w][hd]);
     float L = 0.f;
     if (M != -INFINITY)
-      for (int w = 0; w < kWarps; w++) L += exp2f(sm_m[w][hd] - M) * sm_l[w][hd];
+      for (int w = 0; w < kPairs; w++) L += exp2f(sm_m[w][hd] - M) * sm_l[w][hd];
     fin_m[hd] = M;
     mypart[hd] = M;
     mypart[8 + hd] = L;
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < 8 * D; e += blockDim.x) {
-    const int hd = e / D;
+  for (int e4 = threadIdx.x; e4 < 8 * D / 4; e4 += blockDim.x) {
+    const int el = 4 * e4;
+    const int hd = el / D, dd = el % D;
     const float M = fin_m[hd];
-    float acc = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (M != -INFINITY)
-      for (int w = 0; w < kWarps; w++) acc += exp2f(sm_m[w][hd] - M) * sm_o[w * kMW + mix(hd, e % D)];
-    mypart[16 + e] = acc;
+      for (int w = 0; w < kPairs; w++) {
+        const float wgt = exp2f(sm_m[w][hd] - M);
+        const float* ow = sm_o + w * kMW;
+        acc.x += wgt * ow[mix(hd, dd)];
+        acc.y += wgt * ow[mix(hd, dd + 1)];
+        acc.z += wgt * ow[mix(hd, dd + 2)];
+        acc.w += wgt * ow[mix(hd, dd + 3)];
+      }
+    *reinterpret_cast<float4*>(mypart + 16 + el) = acc;
   }
   __threadfence();
   __syncthreads();
@@ -486,19 +518,32 @@ __global__ __launch_bounds__(kThreads) void attend_kernel(AttendArgs a) {
   __threadfence();
 
   // ---- last CTA: merge the splits in split order ----------------------------------
-  // Weights w[h][s] = exp2(m_s - M) / L are computed once; the O partials are
-  // then read as independent 16-byte loads so their latencies overlap.
+  // The (m, l) of every split are loaded in parallel; weights w[h][s] =
+  // exp2(m_s - M) / L are formed once; the O partials are then read as
+  // independent 16-byte loads so their latencies overlap.
   const float* parts = a.part + (static_cast<int64_t>(b) * gy + hy) * a.nsplit * kPart;
+  for (int t = threadIdx.x; t < 8 * a.nsplit; t += blockDim.x) {
+    const int hd = t / a.nsplit, s2 = t % a.nsplit;
+    wts[hd][s2] = __ldcg(parts + s2 * kPart + hd);  // m of split s2, head hd
+  }
+  __syncthreads();
   if (threadIdx.x < 8) {
     const int hd = threadIdx.x;
     float M = -INFINITY;
-    for (int s2 = 0; s2 < a.nsplit; s2++) M = fmaxf(M, __ldcg(parts + s2 * kPart + hd));
+    for (int s2 = 0; s2 < a.nsplit; s2++) M = fmaxf(M, wts[hd][s2]);
+    fin_m[hd] = M;
+  }
+  __syncthreads();
+  for (int t = threadIdx.x; t < 8 * a.nsplit; t += blockDim.x) {
+    const int hd = t / a.nsplit, s2 = t % a.nsplit;
+    const float M = fin_m[hd];
+    wts[hd][s2] = M == -INFINITY ? 0.f : exp2f(wts[hd][s2] - M);
+  }
+  __syncthreads();
+  if (threadIdx.x < 8) {
+    const int hd = threadIdx.x;
     float L = 0.f;
-    for (int s2 = 0; s2 < a.nsplit; s2++) {
-      const float wgt = M == -INFINITY ? 0.f : exp2f(__ldcg(parts + s2 * kPart + hd) - M);
-      wts[hd][s2] = wgt;
-      L += wgt * __ldcg(parts + s2 * kPart + 8 + hd);
-    }
+    for (int s2 = 0; s2 < a.nsplit; s2++) L += wts[hd][s2] * __ldcg(parts + s2 * kPart + 8 + hd);
     fin_l[hd] = L;
   }
   __syncthreads();
@@ -509,14 +554,14 @@ __global__ __launch_bounds__(kThreads) void attend_kernel(AttendArgs a) {
   }
   __syncthreads();
   for (int e4 = threadIdx.x; e4 < 8 * D / 4; e4 += blockDim.x) {
-    const int e = 4 * e4;
-    const int hd = e / D, dd = e % D;
+    const int el = 4 * e4;
+    const int hd = el / D, dd = el % D;
     const int hl = hg * 8 + hd;
     if (hl >= a.G) continue;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 8
     for (int s2 = 0; s2 < a.nsplit; s2++) {
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(parts + s2 * kPart + 16 + e));
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(parts + s2 * kPart + 16 + el));
       const float wgt = wts[hd][s2];
       acc.x += wgt * v.x;
       acc.y += wgt * v.y;
@@ -530,8 +575,8 @@ __global__ __launch_bounds__(kThreads) void attend_kernel(AttendArgs a) {
 
 template <int KV>
 size_t dyn_smem() {
-  const size_t ring = static_cast<size_t>(kWarps) * Geo<KV>::WARP_BYTES;
-  const size_t merge = static_cast<size_t>(kWarps) * kMW * sizeof(float);
+  const size_t ring = static_cast<size_t>(kPairs) * Geo<KV>::PAIR_BYTES;
+  const size_t merge = static_cast<size_t>(kPairs) * kMW * sizeof(float);
   return ring > merge ? ring : merge;
 }
 

@@ -238,3 +238,152 @@ SKV_EXPORT int skv_quantize_int8_rows(const uint16_t* x, int64_t n_rows, int Hkv
       x, items, d, out_rows, Hkv, q, reinterpret_cast<__half*>(scale));
   return launch_status();
 }
+
+// ---------------------------------------------------------------------------
+// Fused per-layer decode preparation: append the current token (key sketch
+// and int8 K/V rows) and fold the query, in one launch.
+// ---------------------------------------------------------------------------
+namespace skv {
+namespace {
+
+constexpr int kPrepThreads = 256;
+
+// CTA (h, b): the sketch of the new key and the folded query of KV head h of
+// request b share one pass over the basis (thread t: sketch dim t%64, basis
+// rows [64*(t/64), +64)), then warps 0 and 1 encode the new K and V rows of
+// head h.  The last CTA of request b (atomic ticket, no waiting) quantises the
+// request's folded query with one scale.
+__global__ __launch_bounds__(kPrepThreads) void prepare_kernel(
+    const uint16_t* __restrict__ q, const uint16_t* __restrict__ newk, const uint16_t* __restrict__ newv, int Hq,
+    int Hkv, int d, const float* __restrict__ basis, const float* __restrict__ c,
+    const int64_t* __restrict__ new_rows, uint8_t* __restrict__ sketch, int8_t* __restrict__ k8,
+    __half* __restrict__ ks, int8_t* __restrict__ v8, __half* __restrict__ vs, int8_t* __restrict__ q8,
+    float* __restrict__ sigma_out, float* __restrict__ qp_ws, unsigned* __restrict__ tickets) {
+  __shared__ float Qs[kMaxD], Ks[kMaxD];
+  __shared__ float part[4][kRank][2];
+  __shared__ int codes[kRank];
+  __shared__ int last;
+  __shared__ float red[32];
+  const int h = blockIdx.x, b = blockIdx.y;
+  const int G = Hq / Hkv;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const uint16_t* qb = q + (static_cast<int64_t>(b) * Hq + static_cast<int64_t>(h) * G) * d;
+  const uint16_t* kb = newk + (static_cast<int64_t>(b) * Hkv + h) * d;
+  for (int x = t; x < d; x += blockDim.x) {
+    float acc = 0.f;
+    for (int gg = 0; gg < G; gg++) acc = __fadd_rn(acc, bf16_bits_to_f32(qb[gg * d + x]));
+    Qs[x] = acc;
+    Ks[x] = bf16_bits_to_f32(kb[x]);
+  }
+  __syncthreads();
+  {
+    const int j = t & (kRank - 1), quarter = t >> 6;
+    const int per = (d + 3) / 4;
+    const int x0 = quarter * per, x1 = min(d, x0 + per);
+    float aq0 = 0.f, aq1 = 0.f, ak0 = 0.f, ak1 = 0.f;
+    int x = x0;
+    for (; x + 1 < x1; x += 2) {
+      const float p0 = __ldg(basis + x * kRank + j), p1 = __ldg(basis + (x + 1) * kRank + j);
+      aq0 = fmaf(p0, Qs[x], aq0);
+      ak0 = fmaf(p0, Ks[x], ak0);
+      aq1 = fmaf(p1, Qs[x + 1], aq1);
+      ak1 = fmaf(p1, Ks[x + 1], ak1);
+    }
+    if (x < x1) {
+      const float p0 = __ldg(basis + x * kRank + j);
+      aq0 = fmaf(p0, Qs[x], aq0);
+      ak0 = fmaf(p0, Ks[x], ak0);
+    }
+    part[quarter][j][0] = aq0 + aq1;
+    part[quarter][j][1] = ak0 + ak1;
+  }
+  __syncthreads();
+  const int64_t row = new_rows[b];
+  if (t < kRank) {
+    const int j = t;
+    const float qp = (part[0][j][0] + part[1][j][0]) + (part[2][j][0] + part[3][j][0]);
+    const float s = (part[0][j][1] + part[1][j][1]) + (part[2][j][1] + part[3][j][1]);
+    const float cj = c[h * kRank + j];
+    codes[j] = (cj != 0.f) ? rint_clamp(__fdiv_rn(s, cj), -8, 7) : 0;
+    qp_ws[static_cast<int64_t>(b) * Hkv * kRank + h * kRank + j] = __fmul_rn(qp, cj);
+  }
+  __syncthreads();
+  if (t < kRank / 2)
+    sketch[row * (Hkv * kRank / 2) + h * (kRank / 2) + t] =
+        static_cast<uint8_t>((codes[2 * t] & 15) | ((codes[2 * t + 1] & 15) << 4));
+  if (warp < 2) {  // int8 rows of the new K (warp 0) and V (warp 1) of head h
+    const uint16_t* src = (warp == 0 ? newk : newv) + (static_cast<int64_t>(b) * Hkv + h) * d;
+    float amax = 0.f;
+    for (int x = lane; x < d; x += 32) amax = fmaxf(amax, fabsf(bf16_bits_to_f32(src[x])));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const __half sh = __float2half_rn(__fdiv_rn(amax, 127.f));
+    const float sf = __half2float(sh);
+    const bool ok = (sf != 0.f) && isfinite(sf);
+    int8_t* dst = (warp == 0 ? k8 : v8) + (row * Hkv + h) * d;
+    for (int x = lane; x < d; x += 32)
+      dst[x] = static_cast<int8_t>(ok ? rint_clamp(__fdiv_rn(bf16_bits_to_f32(src[x]), sf), -127, 127) : 0);
+    if (lane == 0) (warp == 0 ? ks : vs)[row * Hkv + h] = sh;
+  }
+  // Folded query: the request's last CTA quantises all heads with one scale.
+  __threadfence();
+  __syncthreads();
+  if (t == 0) last = atomicAdd(&tickets[b], 1u) == static_cast<unsigned>(Hkv - 1);
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  const int width = Hkv * kRank;
+  const float* qpb = qp_ws + static_cast<int64_t>(b) * width;
+  float amax = 0.f;
+  for (int m = t; m < width; m += blockDim.x) amax = fmaxf(amax, fabsf(__ldcg(qpb + m)));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if (lane == 0) red[warp] = amax;
+  __syncthreads();
+  if (t < 32) {
+    float v = t < (blockDim.x >> 5) ? red[t] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if (t == 0) red[0] = v;
+  }
+  __syncthreads();
+  const float sigma = __fdiv_rn(red[0], 127.f);
+  if (t == 0) {
+    if (sigma_out) sigma_out[b] = sigma;
+    tickets[b] = 0u;
+  }
+  for (int m = t; m < width; m += blockDim.x) {
+    const int v = (sigma != 0.f) ? rint_clamp(__fdiv_rn(__ldcg(qpb + m), sigma), -127, 127) : 0;
+    q8[static_cast<int64_t>(b) * width + m] = static_cast<int8_t>(v);
+  }
+}
+
+}  // namespace
+}  // namespace skv
+
+SKV_EXPORT size_t skv_decode_prepare_workspace_size(int B, int Hkv, int r) {
+  if (B <= 0 || Hkv <= 0 || r != kRank) return 0;
+  return (static_cast<size_t>(B) * Hkv * kRank * sizeof(float) + 255) / 256 * 256 + (B * sizeof(unsigned) + 255) / 256 * 256;
+}
+
+SKV_EXPORT int skv_decode_prepare(const uint16_t* q, const uint16_t* new_k, const uint16_t* new_v, int B, int Hq,
+                                  int Hkv, int d, int r, const float* basis, const float* c,
+                                  const int64_t* new_rows, uint8_t* sketch, int8_t* k8, uint16_t* k_scale,
+                                  int8_t* v8, uint16_t* v_scale, int8_t* q8, float* sigma, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || r != kRank || d <= 0 || d > kMaxD || Hkv > 65535)
+    return SKV_EINVAL;
+  if (B == 0) return SKV_OK;
+  if (!q || !new_k || !new_v || !basis || !c || !new_rows || !sketch || !k8 || !k_scale || !v8 || !v_scale || !q8 ||
+      !workspace)
+    return SKV_EINVAL;
+  if (workspace_bytes < skv_decode_prepare_workspace_size(B, Hkv, r)) return SKV_ENOMEM;
+  float* qp_ws = static_cast<float*>(workspace);
+  unsigned* tickets = reinterpret_cast<unsigned*>(
+      static_cast<char*>(workspace) + (static_cast<size_t>(B) * Hkv * kRank * sizeof(float) + 255) / 256 * 256);
+  dim3 grid(Hkv, B);
+  prepare_kernel<<<grid, kPrepThreads, 0, as_stream(stream)>>>(
+      q, new_k, new_v, Hq, Hkv, d, basis, c, new_rows, sketch, k8, reinterpret_cast<__half*>(k_scale), v8,
+      reinterpret_cast<__half*>(v_scale), q8, sigma, qp_ws, tickets);
+  return launch_status();
+}

@@ -446,3 +446,46 @@ def test_score_select_float_modes_match_two_calls(skv, orc):
     assert np.array_equal(gc, sc)
     for b in range(B):
         assert np.array_equal(gi[b, :gc[b]], si[b, :sc[b]])
+
+
+# ---------------------------------------------------------------------------
+# fused per-layer preparation (a1 append + int8 append + a2)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("B,Hq,Hkv", [(8, 24, 4), (3, 16, 2), (1, 8, 8)])
+def test_decode_prepare_matches_oracle(skv, orc, B, Hq, Hkv):
+    rng = np.random.default_rng(3000 + B * Hq)
+    d, r, rows = 256, 64, 50
+    U = wl.orthonormal_basis(d, r, 11)
+    c = wl.sketch_step(Hkv, r, d)
+    q = wl.to_bf16_bits(wl.lowrank_rows(rng, B * Hq, U).reshape(B, Hq, d))
+    nk = wl.to_bf16_bits(wl.lowrank_rows(rng, B * Hkv, U).reshape(B, Hkv, d))
+    nv = wl.to_bf16_bits(rng.standard_normal((B, Hkv, d)).astype(np.float32))
+    new_rows = rng.choice(rows, size=B, replace=False).astype(np.int64)
+    sketch = torch.full((rows, Hkv * r // 2), 0x77, dtype=torch.uint8, device="cuda")
+    k8 = torch.zeros((rows, Hkv, d), dtype=torch.int8, device="cuda")
+    v8 = torch.zeros((rows, Hkv, d), dtype=torch.int8, device="cuda")
+    ks = torch.zeros((rows, Hkv), dtype=torch.float16, device="cuda")
+    vs = torch.zeros((rows, Hkv), dtype=torch.float16, device="cuda")
+    q8 = torch.zeros((B, Hkv * r), dtype=torch.int8, device="cuda")
+    sig = torch.zeros((B,), dtype=torch.float32, device="cuda")
+    ws = torch.zeros((skv.decode_prepare_workspace_size(B, Hkv),), dtype=torch.uint8, device="cuda")
+    for _ in range(2):  # tickets must return to zero
+        skv.decode_prepare(T.bf16_dev(q), T.bf16_dev(nk), T.bf16_dev(nv), T.dev(U), T.dev(c), T.dev(new_rows), sketch,
+                           k8, ks, v8, vs, q8, ws, sigma=sig)
+    torch.cuda.synchronize()
+    ref_sk = orc.sketch_project(nk, U, c)
+    ref_q = orc.sketch_query(q, Hkv, U, c)
+    rk8, rks = orc.quant_int8_rows(nk)
+    rv8, rvs = orc.quant_int8_rows(nv)
+    s_host, k8h, v8h, ksh, vsh = T.host(sketch), T.host(k8), T.host(v8), T.host(ks), T.host(vs)
+    for i in range(B):
+        row = new_rows[i]
+        T.assert_codes_match_except_ties(T.unpack_int4(s_host[row]), T.unpack_int4(ref_sk["q4"][i]),
+                                         ref_sk["x"][i].ravel())
+        assert np.array_equal(k8h[row], rk8[i]) and np.array_equal(v8h[row], rv8[i])
+        assert np.array_equal(ksh[row], rks[i]) and np.array_equal(vsh[row], rvs[i])
+    untouched = np.setdiff1d(np.arange(rows), new_rows)
+    assert np.all(s_host[untouched] == 0x77)
+    assert np.allclose(T.host(sig), ref_q["sigma"], rtol=1e-5)
+    T.assert_codes_match_except_ties(T.host(q8), ref_q["q8"], ref_q["x"])
