@@ -44,6 +44,25 @@ SEED = 2
 SCAN_BYTES_PER_CAND = W_HKV * W_R // 2          # 128 B sketch row read (keys stay on chip)
 ATTN_BYTES_PER_ROW_HEAD = 2 * W_D + 2 * 2       # int8 K + V rows and their fp16 scales
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch from one
+# ncu --set full capture of this workload (profiles/ has the summary and the
+# command), keyed by a hash of the kernel's sources: a kernel whose sources
+# changed since the capture reports null.
+MEASURED_TRAFFIC = {
+    "score_select": (("common.cuh", "score_common.cuh", "select.cu"), "fd977d44ad3ea622", 258_213_376),
+    "attend": (("common.cuh", "attend.cu"), "1f296da7a22ce8c9", 56_068_864),
+}
+
+
+def measured_traffic(kernel):
+    import hashlib
+    files, digest, nbytes = MEASURED_TRAFFIC[kernel]
+    m = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "sparse_kv_long_gb300", "csrc", f), "rb") as fh:
+            m.update(fh.read())
+    return nbytes if m.hexdigest()[:16] == digest else None
+
 
 def config_dict(l2_note, layers=W_L):
     return {"workload": f"sketch_8x250000_{layers}L_int4sketch_int8kv", "batch": W_B, "context": W_T,
@@ -397,11 +416,11 @@ def run_gpu(args):
         "parallelism": "replicas only" if world > 1 else "single GPU",
         "kernel_us": {"score_select_int4": scan_us, "sparse_attend_int8": attn_us},
         "roofline": {"bound": "hbm", "achieved": scan_gbs, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": scan_gbs / hbm_peak, "traffic": None, "kernel": "score_select_kernel (scan + top-k)",
+                     "frac": scan_gbs / hbm_peak, "traffic": measured_traffic("score_select"), "kernel": "score_select_kernel (scan + top-k)",
                      "peak_source": peak_src, "bytes_per_launch": scan_bytes,
                      "bytes_rule": f"{SCAN_BYTES_PER_CAND} B sketch row per candidate token x {W_B} x {n_cand}"},
         "roofline_attend": {"bound": "hbm", "achieved": attn_gbs, "peak": hbm_peak, "unit": "GB/s",
-                            "frac": attn_gbs / hbm_peak, "bytes_per_launch": attn_bytes,
+                            "frac": attn_gbs / hbm_peak, "traffic": measured_traffic("attend"), "bytes_per_launch": attn_bytes,
                             "bytes_rule": f"{ATTN_BYTES_PER_ROW_HEAD} B per row-head x {W_B} x {MAX_ROWS} x {W_HKV}"},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * L * SketchWorkloadGPU.KERNELS_PER_LAYER,

@@ -7,14 +7,16 @@
 // [token][kv_head][dim].
 //
 // Design.  A CTA owns one (request, KV head, group of up to 8 query heads,
-// split of the selected rows) and runs two warp pairs.  It first stages the
-// split's physical row numbers, the int8 scales and the query heads in shared
-// memory.  Each pair takes 16-row tiles in turn through its own 2-stage
-// shared-memory ring: lanes 0..15 of the pair's first warp issue two TMA bulk
-// copies each (cp.async.bulk, one K row and one V row of the KV head)
-// completing on the stage's mbarrier, so the next tile is in flight while the
-// current one is computed.  Rows land at pitches chosen so that the fragment
-// loads below are free of shared-memory bank conflicts.
+// split of the selected rows) and runs three warp pairs.  Each pair takes
+// 16-row tiles in turn through its own 3-stage shared-memory ring: the pair's
+// 64 threads copy a tile's K and V rows of the KV head with 16-byte cp.async
+// (gathering scattered 256-byte rows this way runs well above the rate of one
+// bulk copy per row) and arrive on the stage's mbarrier when their copies
+// land, so two tiles are in flight while one is computed.  The first tiles go
+// out as soon as their row numbers are read; the split's row numbers, the
+// int8 scales and the query heads are then staged in shared memory.  Rows
+// land at pitches chosen so that the fragment loads below are free of
+// shared-memory bank conflicts.
 //
 // The two warps of a pair split the head dimension: warp e owns dims
 // [128e, 128e + 128) for both products.  Per tile each computes the partial
@@ -39,13 +41,13 @@ namespace {
 
 constexpr int D = 256;
 constexpr int DH = D / 2;          // dims per warp of a pair
-constexpr int kPairs = 2;
+constexpr int kPairs = 3;
 constexpr int kWarps = 2 * kPairs;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kPart = 16 + 8 * D;  // m[8], l[8], O[8][D] floats per partial
 constexpr int kMaxSplit = 64;
 constexpr int kMaxRowsPerSplit = 512;
-constexpr int kStages = 2;
+constexpr int kStages = 3;
 constexpr int kTileRows = 16;
 constexpr long kWaitLimit = 1L << 20;  // bounded mbarrier polls (~1 s with backoff)
 // Pair partials in shared memory: float (head, dim) at head*kMH + (dim/32)*33 +
@@ -91,11 +93,6 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
 }
 
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-               : "memory");
-}
-
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -115,12 +112,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   return false;
 }
 
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
+// 16-byte asynchronous global -> shared copy (L2 only), and an arrive on `bar`
+// once all of this thread's earlier copies have landed.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 __device__ __forceinline__ uint4 lds128(const void* p) {
@@ -172,33 +170,38 @@ __device__ __forceinline__ uint32_t word(const uint4& v, int i) {
   return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
-// Barrier of the 64 threads of warp pair `pair` (named barriers 1 and 2).
+// Barrier of the 64 threads of warp pair `pair` (named barriers 1..4).
 __device__ __forceinline__ void pair_sync(int pair) {
-  if (pair == 0)
-    asm volatile("bar.sync 1, 64;" ::: "memory");
-  else
-    asm volatile("bar.sync 2, 64;" ::: "memory");
+  switch (pair) {
+    case 0: asm volatile("bar.sync 1, 64;" ::: "memory"); break;
+    case 1: asm volatile("bar.sync 2, 64;" ::: "memory"); break;
+    case 2: asm volatile("bar.sync 3, 64;" ::: "memory"); break;
+    default: asm volatile("bar.sync 4, 64;" ::: "memory"); break;
+  }
 }
 
 // Pair barrier that also ANDs a predicate across the 64 threads, so both warps
 // of the pair take the same branch afterwards.
 __device__ __forceinline__ bool pair_all(int pair, bool v) {
   uint32_t r;
-  if (pair == 0)
-    asm volatile("{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, 1, 64, p;\n selp.u32 %0, 1, 0, q;\n}"
-                 : "=r"(r)
-                 : "r"(static_cast<uint32_t>(v))
-                 : "memory");
-  else
-    asm volatile("{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, 2, 64, p;\n selp.u32 %0, 1, 0, q;\n}"
-                 : "=r"(r)
-                 : "r"(static_cast<uint32_t>(v))
-                 : "memory");
+#define SKV_PAIR_ALL(ID)                                                                              \
+  asm volatile("{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, " #ID             \
+               ", 64, p;\n selp.u32 %0, 1, 0, q;\n}"                                                   \
+               : "=r"(r)                                                                              \
+               : "r"(static_cast<uint32_t>(v))                                                        \
+               : "memory")
+  switch (pair) {
+    case 0: SKV_PAIR_ALL(1); break;
+    case 1: SKV_PAIR_ALL(2); break;
+    case 2: SKV_PAIR_ALL(3); break;
+    default: SKV_PAIR_ALL(4); break;
+  }
+#undef SKV_PAIR_ALL
   return r != 0;
 }
 
 template <int KV>
-__global__ __launch_bounds__(kThreads, 4) void attend_kernel(AttendArgs a) {
+__global__ __launch_bounds__(kThreads, 2) void attend_kernel(AttendArgs a) {
   using Gm = Geo<KV>;
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ uint64_t bars[kPairs][kStages];
@@ -227,15 +230,53 @@ __global__ __launch_bounds__(kThreads, 4) void attend_kernel(AttendArgs a) {
   const uint8_t* kbase = a.kpool + static_cast<int64_t>(h) * Gm::RB;
   const uint8_t* vbase = a.vpool + static_cast<int64_t>(h) * Gm::RB;
 
+  unsigned char* pbuf = smem + pair * Gm::PAIR_BYTES;
+  const int ntiles = (nr + kTileRows - 1) / kTileRows;
+  int my_tiles = 0;
+  for (int t = pair; t < ntiles; t += kPairs) my_tiles++;
+  // Physical row of split row idx, or -1 (absent or out of range).
+  auto phys = [&](int idx) -> int64_t {
+    const int32_t rid = a.rows[static_cast<int64_t>(b) * a.max_rows + r0 + idx];
+    const int64_t p = static_cast<int64_t>(b) * a.req_row_stride + rid;
+    return (rid >= 0 && p >= 0 && p < a.n_pool_rows) ? p : -1;
+  };
+  // The 64 threads of the pair copy tile `it` (16 K rows and 16 V rows) into
+  // stage it % kStages in 16-byte pieces: thread u of the pair takes piece
+  // u % (RB/16) of rows u / (RB/16) + 64/(RB/16) * i.  rowp(r) gives the
+  // physical row of tile row r (-1: pool row 0, masked later).  Each thread
+  // then arrives on the stage's barrier when its copies have landed.
+  constexpr int kPieces = Gm::RB / 16;                 // 16-byte pieces per row
+  constexpr int kRowsPerRound = 64 / kPieces;          // rows covered by one round of the pair
+  const int u = 32 * e + lane;
+  auto copy_tile = [&](int it, auto&& rowp) {
+    const int stage = it % kStages;
+    unsigned char* kst = pbuf + stage * Gm::STAGE;
+    unsigned char* vst = kst + kTileRows * Gm::KP;
+    const int piece = u % kPieces;
+#pragma unroll
+    for (int i = 0; i < kTileRows / kRowsPerRound; i++) {
+      const int row = u / kPieces + kRowsPerRound * i;
+      int64_t prow = rowp(row);
+      if (prow < 0) prow = 0;
+      cp_async16(kst + row * Gm::KP + 16 * piece, kbase + prow * pitch + 16 * piece);
+      cp_async16(vst + row * Gm::VP + 16 * piece, vbase + prow * pitch + 16 * piece);
+    }
+    cp_async_arrive(&bars[pair][stage]);
+  };
+
+  // ---- barriers, then the pair's first tiles go out at once ---------------------
+  if (threadIdx.x < kPairs * kStages) mbar_init(&bars[threadIdx.x / kStages][threadIdx.x % kStages], 64);
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  __syncthreads();
+  for (int it = 0; it < kStages && it < my_tiles; it++) {
+    const int tb = (pair + kPairs * it) * kTileRows;
+    copy_tile(it, [&](int row) { return tb + row < nr ? phys(tb + row) : int64_t(-1); });
+  }
+
   // ---- stage row numbers, scales and the query heads ---------------------------
   for (int i = threadIdx.x; i < nr; i += blockDim.x) {
-    const int32_t rid = a.rows[static_cast<int64_t>(b) * a.max_rows + r0 + i];
-    const int64_t p = static_cast<int64_t>(b) * a.req_row_stride + rid;
-    int64_t pr = -1;
-    if (rid >= 0 && p >= 0 && p < a.n_pool_rows)
-      pr = p;
-    else
-      set_status(a.status, SKV_DEV_RANGE);
+    const int64_t pr = phys(i);
+    if (pr < 0) set_status(a.status, SKV_DEV_RANGE);
     s_prow[i] = pr;
     if (KV == SKV_KV_INT8) {
       s_ks[i] = pr >= 0 ? __half2float(__ushort_as_half(a.kscale[pr * a.Hkv + h])) : 0.f;
@@ -249,10 +290,6 @@ __global__ __launch_bounds__(kThreads, 4) void attend_kernel(AttendArgs a) {
     if (hl < a.G)
       v = *reinterpret_cast<const uint4*>(a.q + (static_cast<int64_t>(b) * a.Hq + h * a.G + hl) * D + 8 * x8);
     *reinterpret_cast<uint4*>(&s_q[hd][8 * x8]) = v;
-  }
-  if (threadIdx.x < kPairs * kStages) {
-    mbar_init(&bars[threadIdx.x / kStages][threadIdx.x % kStages], 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
 
@@ -278,31 +315,6 @@ __global__ __launch_bounds__(kThreads, 4) void attend_kernel(AttendArgs a) {
 #pragma unroll
   for (int mt = 0; mt < 8; mt++) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
   float m_run = -INFINITY, l_part = 0.f;
-
-  unsigned char* pbuf = smem + pair * Gm::PAIR_BYTES;
-  const int ntiles = (nr + kTileRows - 1) / kTileRows;
-  int my_tiles = 0;
-  for (int t = pair; t < ntiles; t += kPairs) my_tiles++;
-
-  // Lanes 0..15 of the pair's first warp copy row `lane` of the pair's tile
-  // `it` into stage it % kStages.  Absent rows copy pool row 0 and are masked.
-  auto issue = [&](int it) {
-    const int stage = it % kStages;
-    unsigned char* kst = pbuf + stage * Gm::STAGE;
-    unsigned char* vst = kst + kTileRows * Gm::KP;
-    uint64_t* bar = &bars[pair][stage];
-    if (lane == 0) mbar_arrive_expect_tx(bar, kTileRows * 2 * Gm::RB);
-    __syncwarp();
-    if (lane < kTileRows) {
-      const int idx = (pair + kPairs * it) * kTileRows + lane;
-      int64_t pr = idx < nr ? s_prow[idx] : -1;
-      if (pr < 0) pr = 0;
-      bulk_g2s(kst + lane * Gm::KP, kbase + pr * pitch, Gm::RB, bar);
-      bulk_g2s(vst + lane * Gm::VP, vbase + pr * pitch, Gm::RB, bar);
-    }
-  };
-  if (e == 0)
-    for (int it = 0; it < kStages && it < my_tiles; it++) issue(it);
 
   int completed = 0;  // tiles whose copies have landed
   for (int it = 0; it < my_tiles; it++) {
@@ -447,9 +459,9 @@ __global__ __launch_bounds__(kThreads, 4) void attend_kernel(AttendArgs a) {
     }
     pair_sync(pair);  // both warps are done with this stage (and with s_x)
     const int nx = it + kStages;
-    if (e == 0 && nx < my_tiles) {
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      issue(nx);
+    if (nx < my_tiles) {  // both warps are past this stage (pair barrier above)
+      const int tb = (pair + kPairs * nx) * kTileRows;
+      copy_tile(nx, [&](int row) { return tb + row < nr ? s_prow[tb + row] : int64_t(-1); });
     }
   }
   // After a timeout, give the copies still in flight a bounded chance to land
