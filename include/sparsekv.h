@@ -337,6 +337,125 @@ int skv_sparse_attend_decode(int kv_kind, int B, int Hq, int Hkv, int d,
                              size_t workspace_bytes, int32_t *dev_status, void *stream);
 
 /* ========================================================================== */
+/* a5: resolve the selected tokens to pool rows.  RESIDENT is the identity    */
+/* (attention's req_row_stride addressing); the two calls below resolve       */
+/* through a hot buffer in front of a host tier.                              */
+/* ========================================================================== */
+/*
+ * skv_resolve_rows_clock -- windowed CLOCK over a host int4 tier ([P1] "What
+ * shipped": the main KV cache is int4 in host RAM -- 64-dim groups, fp16
+ * scales, 272 B per token-head -- and the GPU keeps the sketch, the sinks, the
+ * recent tail and a 2.5 % hot buffer managed by windowed CLOCK; rows fetched
+ * from the host are dequantised back to int8 rows).
+ *
+ * Per request b (one CTA each), with T = lengths[b] and the count[b] selected
+ * tokens idx[b][i] (ascending, unique, as skv_topk_select writes them):
+ *   sink  t < S          -> row t
+ *   tail  t >= T - W     -> row S + (t mod W)   (the recent-token ring)
+ *   pick  S <= t < T - W -> row S + W + slot, slot from the CLOCK:
+ *     1. a pick whose token has a slot is a hit: ref = 1, use_step = step;
+ *     2. the misses, in ascending token order, sweep the hand: a slot used
+ *        in this step is skipped; an empty slot or one with ref == 0 is taken
+ *        (its previous token loses it); a slot with ref == 1 gets ref = 0 and
+ *        the hand moves on.  A taken slot gets the token, ref = 1, use_step =
+ *        step, and the token's host row is fetched through host_rows,
+ *        requantised to int8 (x = code * group scale, exact in fp32; s8 =
+ *        fp16(max|x| / 127); q = clamp(rint(x / s8), +-127); zero s8 gives
+ *        zero codes) and written to the slot's pool rows, every head, K and V.
+ * Row ids are relative to the request: physical row = b*req_row_stride + row,
+ * as skv_sparse_attend_decode reads them.
+ *   state (device, caller-owned, per request; start: slot_token = -1, ref = 0,
+ *   use_step = -1, token_slot = -1, hand = 0):
+ *     slot_token int32 [B][Hs]   ref u8 [B][Hs]   use_step int32 [B][Hs]
+ *     token_slot int32 [B][t_cap]   hand int32 [B]
+ *   host_rows  u8 [B][t_cap][Hkv][2][d/2 + d/32] -- per token and head the K
+ *              then the V vector in skv_quantize_int4_rows layout (136 B each
+ *              for d = 256, 1088 B per token at Hkv = 4); the device alias of
+ *              registered host memory (skv_host_register) or device memory
+ *   k8, v8     int8 [B*req_row_stride][Hkv][d]; k_scale, v_scale fp16
+ *              [B*req_row_stride][Hkv]: the request's pool (sinks, tail ring,
+ *              hot slots); only hot-slot rows of misses are written
+ *   rows_out   int32 [B][max_rows]; n_miss int32 [B] (misses placed; -1 when
+ *              the request has more picks than slots)
+ *   step       the decode step, >= 0, increasing from call to call
+ * Errors: SKV_EINVAL for bad sizes, null pointers, a req_row_stride below
+ * S + W + Hs or unaligned pools; SKV_EUNSUPPORTED unless d is 256, 512, 768
+ * or 1024, Hs <= 16384, max_rows <= 8192.  On the device: a token outside
+ * [0, T) gives row -1 and SKV_DEV_RANGE; more picks than slots leave the state
+ * unchanged, give row -1 for every pick and set SKV_DEV_COUNT.
+ */
+int skv_resolve_rows_clock(int B, int64_t t_cap, const int32_t *lengths, int S, int W, int Hkv,
+                           int d, int Hs, const int32_t *idx, int max_rows, const int32_t *count,
+                           int32_t step, int32_t *slot_token, uint8_t *ref, int32_t *use_step,
+                           int32_t *token_slot, int32_t *hand, const uint8_t *host_rows,
+                           int8_t *k8, int8_t *v8, uint16_t *k_scale, uint16_t *v_scale,
+                           int64_t req_row_stride, int32_t *rows_out, int32_t *n_miss,
+                           int32_t *dev_status, void *stream);
+
+/*
+ * skv_resolve_rows_lru -- mixed residency behind a block table with an LRU
+ * hot buffer ([P2] "Three residency states, one block pool": resident tokens
+ * are read in place, hot tokens are read and refresh their LRU entry, a miss
+ * copies one row from pinned host memory into an LRU slot; "What it composes
+ * with": the hot buffer holds 2 x top-K rows).  One fused kernel, one CTA per
+ * request.
+ * Per request b and selected token t (ascending, unique):
+ *   block_table[b][t / page] = p >= 0  -> row p*page + t mod page (in place)
+ *   else a hot hit (token_slot[b][t] = s >= 0) -> row hot(b) + s, stamp = step
+ *   else a miss: the misses, in ascending token order, take the slots NOT
+ *   touched in this step with the smallest (stamp, slot index); the old token
+ *   loses the slot; row_bytes are copied from host + (b*t_cap + t)*row_bytes
+ *   to pool row hot(b) + s; stamp = step.
+ * hot(b) = hot_base + b*hot_stride.  Row ids are absolute pool rows
+ * (attention with req_row_stride = 0).
+ *   state: stamp int64 [B][n_slots] (-1 empty), slot_token int32
+ *          [B][n_slots] (-1 none), token_slot int32 [B][t_cap] (-1 none)
+ *   block_table int32 [B][n_pages]; host u8 [B][t_cap][row_bytes] (device
+ *   alias); pool u8 [n_pool_rows][row_bytes]
+ *   step   0 <= step < 2^31 - 1, increasing from call to call
+ * Errors: SKV_EINVAL for bad sizes, null or unaligned pointers, row_bytes not
+ * a multiple of 16, a hot buffer past n_pool_rows; SKV_EUNSUPPORTED for
+ * n_slots > 8192 or max_rows > 8192.  On the device: bad tokens give row -1
+ * and SKV_DEV_RANGE; fewer untouched slots than misses leave the misses
+ * unresolved (row -1), set n_miss[b] = -1 and SKV_DEV_COUNT.
+ */
+int skv_resolve_rows_lru(int B, int64_t t_cap, const int32_t *lengths, int page,
+                         const int32_t *block_table, int64_t n_pages, int64_t hot_base,
+                         int64_t hot_stride, int n_slots, int64_t step, int64_t *stamp,
+                         int32_t *slot_token, int32_t *token_slot, const uint8_t *host,
+                         uint8_t *pool, int64_t row_bytes, int64_t n_pool_rows,
+                         const int32_t *idx, int max_rows, const int32_t *count,
+                         int32_t *rows_out, int32_t *n_miss, int32_t *dev_status, void *stream);
+
+/*
+ * skv_quantize_int4_rows -- host-tier row encoding ([P1]: int4 with 64-dim
+ * groups and fp16 scales, 272 B per token-head for K and V).  Per (row, head)
+ * vector of d dims: for each 64-dim group, scale = fp16_rne(max|x| / 7) (fp32
+ * division), code = clamp(rint(x / scale), -8, 7) (zero scale: zero codes);
+ * bytes [0, d/2) hold the codes (byte i: dim 2i in the low nibble, 2i+1 in
+ * the high nibble, two's complement), then d/64 fp16 scales.  Bit-exact.
+ *   x        bf16 [n_rows][Hkv][d] (device)
+ *   out      vector (t, h) at out + orow*token_pitch + h*head_pitch, orow =
+ *            out_rows[t] (int64, device) or t when out_rows is NULL; out may
+ *            be a host alias
+ * Constraints: d in {256, 512, 768, 1024}; head_pitch >= d/2 + d/32;
+ * token_pitch >= Hkv*head_pitch; pitches and out 4-byte aligned.
+ */
+int skv_quantize_int4_rows(const uint16_t *x, int64_t n_rows, int Hkv, int d,
+                           const int64_t *out_rows, uint8_t *out, int64_t token_pitch,
+                           int64_t head_pitch, void *stream);
+
+/*
+ * skv_stream_read -- reads `bytes` at `src` (device memory or a host alias)
+ * with 16-byte loads and XORs the words into *sink: the probe that measures
+ * the bandwidth a zero-copy gather can reach.  grid = 0 picks 2 CTAs per SM.
+ * Errors: SKV_EINVAL for a null pointer, bytes not a multiple of 16 or src
+ * not 16-byte aligned.
+ */
+int skv_stream_read(const void *src, size_t bytes, unsigned long long *sink, int grid,
+                    void *stream);
+
+/* ========================================================================== */
 /* Host tier ([P4] "No Need to Rewrite the Kernel": allocate with anonymous    */
 /* mmap, cudaHostRegister(ptr, n, PORTABLE | MAPPED), use the device pointer). */
 /* ========================================================================== */

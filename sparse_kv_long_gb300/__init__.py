@@ -63,6 +63,12 @@ def _load():
                 "skv_attend_workspace_size": ([i32, i32, i32, i32, i32], sz),
                 "skv_sparse_attend_decode": ([i32, i32, i32, i32, i32, P, P, P, P, P, i64, i64, P, i32, P,
                                               f32, P, P, sz, P, P], i32),
+                "skv_resolve_rows_clock": ([i32, i64, P, i32, i32, i32, i32, i32, P, i32, P, i32, P, P, P, P, P, P,
+                                            P, P, P, P, i64, P, P, P, P], i32),
+                "skv_resolve_rows_lru": ([i32, i64, P, i32, P, i64, i64, i64, i32, i64, P, P, P, P, P, i64, i64, P,
+                                          i32, P, P, P, P, P], i32),
+                "skv_quantize_int4_rows": ([P, i64, i32, i32, P, P, i64, i64, P], i32),
+                "skv_stream_read": ([P, sz, P, i32, P], i32),
                 "skv_host_register": ([P, sz, ctypes.POINTER(ctypes.c_void_p)], i32),
                 "skv_host_unregister": ([P], i32),
             }
@@ -196,6 +202,60 @@ def quantize_int8_rows(x, q, scale, out_rows=None, stream=None):
     _check("skv_quantize_int8_rows", _load().skv_quantize_int8_rows(
         _ptr(x), n, Hkv, d, _ptr(out_rows), _ptr(q), _ptr(scale), _stream(stream)))
     return q, scale
+
+
+def quantize_int4_rows(x, out, token_pitch, head_pitch, out_rows=None, out_ptr=None, stream=None):
+    """x bf16 [n][Hkv][d] -> int4 vectors at out + orow*token_pitch + h*head_pitch.
+
+    `out` is a uint8 tensor, or None with `out_ptr` a device alias (int)."""
+    n, Hkv, d = x.shape
+    ptr = ctypes.c_void_p(out_ptr) if out is None else _ptr(out)
+    _check("skv_quantize_int4_rows", _load().skv_quantize_int4_rows(
+        _ptr(x), n, Hkv, d, _ptr(out_rows), ptr, int(token_pitch), int(head_pitch), _stream(stream)))
+    return out
+
+
+# ---- a5 -------------------------------------------------------------------------
+
+def _addr(t):
+    """A tensor's device pointer, or an int device address (host alias)."""
+    return ctypes.c_void_p(t if isinstance(t, int) else t.data_ptr())
+
+
+def resolve_rows_clock(lengths, idx, count, step, S, W, Hs, slot_token, ref, use_step, token_slot, hand,
+                       host_rows, k8, v8, k_scale, v_scale, req_row_stride, rows_out, n_miss, status=None,
+                       stream=None):
+    """Windowed CLOCK resolve (see skv_resolve_rows_clock).  host_rows: uint8 tensor or an int alias."""
+    B, max_rows = idx.shape
+    t_cap = token_slot.shape[1]
+    Hkv, d = k8.shape[-2], k8.shape[-1]
+    _check("skv_resolve_rows_clock", _load().skv_resolve_rows_clock(
+        B, t_cap, _ptr(lengths), S, W, Hkv, d, Hs, _ptr(idx), max_rows, _ptr(count), int(step),
+        _ptr(slot_token), _ptr(ref), _ptr(use_step), _ptr(token_slot), _ptr(hand), _addr(host_rows),
+        _ptr(k8), _ptr(v8), _ptr(k_scale), _ptr(v_scale), int(req_row_stride), _ptr(rows_out), _ptr(n_miss),
+        _ptr(status), _stream(stream)))
+    return rows_out, n_miss
+
+
+def resolve_rows_lru(lengths, idx, count, step, page, block_table, hot_base, hot_stride, stamp, slot_token,
+                     token_slot, host, pool, rows_out, n_miss, status=None, stream=None):
+    """Block table + LRU hot buffer resolve (see skv_resolve_rows_lru).  host: uint8 tensor or int alias."""
+    B, max_rows = idx.shape
+    t_cap = token_slot.shape[1]
+    n_slots = stamp.shape[1]
+    n_pool_rows, row_bytes = pool.shape
+    _check("skv_resolve_rows_lru", _load().skv_resolve_rows_lru(
+        B, t_cap, _ptr(lengths), page, _ptr(block_table), block_table.shape[1], int(hot_base), int(hot_stride),
+        n_slots, int(step), _ptr(stamp), _ptr(slot_token), _ptr(token_slot), _addr(host), _ptr(pool), row_bytes,
+        n_pool_rows, _ptr(idx), max_rows, _ptr(count), _ptr(rows_out), _ptr(n_miss), _ptr(status),
+        _stream(stream)))
+    return rows_out, n_miss
+
+
+def stream_read(src, nbytes, sink, grid=0, stream=None):
+    """Read nbytes at src (tensor or int address) with 16-byte loads; XOR into sink (int64 tensor)."""
+    _check("skv_stream_read", _load().skv_stream_read(_addr(src), int(nbytes), _ptr(sink), int(grid),
+                                                      _stream(stream)))
 
 
 # ---- a6 -------------------------------------------------------------------------

@@ -1,0 +1,668 @@
+// resolve.cu -- a5: map the selected tokens to pool rows (host-tier resolvers)
+// and the host-tier write path.
+//
+// [P1] "8 agents x 250K context on two 3090s ...", "What shipped": the main KV
+// cache sits in host RAM as int4 (64-dim groups, fp16 scales, 272 B per
+// token-head); the GPU keeps the sketch, the sinks, the recent tail and a 2.5%
+// hot buffer managed by windowed CLOCK, and rows fetched from the host are
+// dequantised back to int8 rows.
+// [P2] "vLLM's Hybrid HiSparse ...", "Three residency states, one block pool":
+// resident tokens are read in place, hot tokens refresh their LRU entry, and a
+// miss copies one row from pinned host memory into an LRU slot of the hot
+// buffer ("What it composes with": the hot buffer holds 2 x top-K rows).
+//
+// One CTA per request.  The resolver state of the request is staged in
+// shared memory, the hit pass runs over all threads, the sweep (CLOCK) or the
+// victim order (LRU) is computed on chip, and every warp then fetches miss
+// rows from the host alias with several rows in flight per warp.
+#include "common.cuh"
+
+namespace skv {
+namespace {
+
+constexpr int kResThreads = 1024;
+constexpr int kClockThreads = 512;
+constexpr int kFetchRows = 4;  // LRU host rows in flight per warp
+constexpr int kClockFetch = 2; // CLOCK host tokens in flight per warp
+constexpr int kMaxClockSlots = 16384;
+constexpr int kMaxLruSlots = 8192;
+constexpr int kMaxResolveRows = 8192;
+
+__host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~static_cast<size_t>(15); }
+
+// ---------------------------------------------------------------------------
+// Windowed CLOCK over the hot slots of one request.
+// ---------------------------------------------------------------------------
+struct ClockArgs {
+  int64_t t_cap;
+  const int32_t* lengths;
+  int S, W, Hkv, d, Hs;
+  const int32_t* idx;
+  int max_rows;
+  const int32_t* count;
+  int32_t step;
+  int32_t* slot_token;
+  uint8_t* ref;
+  int32_t* use_step;
+  int32_t* token_slot;
+  int32_t* hand;
+  const uint8_t* host_rows;
+  int8_t* k8;
+  int8_t* v8;
+  __half* k_scale;
+  __half* v_scale;
+  int64_t req_row_stride;
+  int32_t* rows_out;
+  int32_t* n_miss;
+  int32_t* status;
+};
+
+size_t clock_smem_bytes(int Hs, int max_rows) {
+  return align16(static_cast<size_t>(Hs) * 9) + static_cast<size_t>(max_rows) * 12 + 64 * sizeof(int);
+}
+
+// int4 vector (128 B of codes for 256 dims per 136 B, fp16 group scales after
+// the codes) -> int8 row + fp16 scale: x = code * s_g exactly in fp32,
+// s8 = fp16(max|x| / 127), q = clamp(rint(x / s8), +-127).  One lane per
+// 64-dim group; the ng lanes of a vector are consecutive.
+__device__ __forceinline__ void requant_group(const uint2 (&c)[4], uint16_t sbits, int ng, int8_t* dst,
+                                              __half* sdst, bool store) {
+  const float sg = __half2float(__ushort_as_half(sbits));
+  const uint32_t w[8] = {c[0].x, c[0].y, c[1].x, c[1].y, c[2].x, c[2].y, c[3].x, c[3].y};
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; i++) {
+#pragma unroll
+    for (int e = 0; e < 8; e++) {
+      const int code = static_cast<int>(w[i] << (28 - 4 * e)) >> 28;
+      amax = fmaxf(amax, fabsf(static_cast<float>(code) * sg));
+    }
+  }
+  for (int o = 1; o < ng; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const __half s8 = __float2half_rn(__fdiv_rn(amax, 127.f));
+  const float sf = __half2float(s8);
+  const bool ok = (sf != 0.f) && isfinite(sf);
+  if (!store) return;
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i2 = 0; i2 < 4; i2++) {
+    uint32_t out[4];
+#pragma unroll
+    for (int k = 0; k < 2; k++) {
+      const uint32_t wi = w[2 * i2 + k];
+      uint32_t lo = 0, hi = 0;
+#pragma unroll
+      for (int e = 0; e < 8; e++) {
+        const int code = static_cast<int>(wi << (28 - 4 * e)) >> 28;
+        const int q = ok ? rint_clamp(__fdiv_rn(static_cast<float>(code) * sg, sf), -127, 127) : 0;
+        const uint32_t byte = static_cast<uint32_t>(q) & 0xffu;
+        if (e < 4)
+          lo |= byte << (8 * e);
+        else
+          hi |= byte << (8 * (e - 4));
+      }
+      out[2 * k] = lo;
+      out[2 * k + 1] = hi;
+    }
+    d4[i2] = make_uint4(out[0], out[1], out[2], out[3]);
+  }
+  if (sdst) *sdst = s8;
+}
+
+__global__ __launch_bounds__(kClockThreads) void clock_kernel(ClockArgs a) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int Hs = a.Hs;
+  int32_t* s_tok = reinterpret_cast<int32_t*>(smem);
+  int32_t* s_use = s_tok + Hs;
+  uint8_t* s_ref = reinterpret_cast<uint8_t*>(s_use + Hs);
+  int32_t* m_tok = reinterpret_cast<int32_t*>(smem + align16(static_cast<size_t>(Hs) * 9));
+  int32_t* m_pos = m_tok + a.max_rows;
+  int32_t* m_slot = m_pos + a.max_rows;
+  int* scr = reinterpret_cast<int*>(m_slot + a.max_rows);
+
+  int64_t T = a.lengths[b];
+  if (T < 0 || T > a.t_cap) {
+    if (tid == 0) set_status(a.status, SKV_DEV_RANGE);
+    T = T < 0 ? 0 : a.t_cap;
+  }
+  int n = a.count[b];
+  if (n < 0 || n > a.max_rows) {
+    if (tid == 0) set_status(a.status, SKV_DEV_COUNT);
+    n = n < 0 ? 0 : a.max_rows;
+  }
+  const int32_t* idx = a.idx + static_cast<int64_t>(b) * a.max_rows;
+  int32_t* rows = a.rows_out + static_cast<int64_t>(b) * a.max_rows;
+  int32_t* tslot = a.token_slot + static_cast<int64_t>(b) * a.t_cap;
+  const int64_t sbase = static_cast<int64_t>(b) * Hs;
+  const int S = a.S, W = a.W;
+  auto is_pick = [&](int64_t t) { return t >= S && t < T - W; };
+
+  // The sweep needs at least as many slots as picks (else nothing changes).
+  int n_picks = 0;
+  for (int base = 0; base < n; base += kClockThreads) {
+    const int i = base + tid;
+    bool p = false;
+    if (i < n) {
+      const int64_t t = idx[i];
+      p = t >= 0 && t < T && is_pick(t);
+    }
+    n_picks += __syncthreads_count(p);
+  }
+  const bool fits = n_picks <= Hs;
+  if (!fits && tid == 0) set_status(a.status, SKV_DEV_COUNT);
+
+  for (int s = tid; s < Hs; s += kClockThreads) {
+    s_tok[s] = a.slot_token[sbase + s];
+    s_use[s] = a.use_step[sbase + s];
+    s_ref[s] = a.ref[sbase + s];
+  }
+  __syncthreads();
+
+  // Phase 1: sinks, tail and hits; misses listed in ascending token order.
+  int nm = 0;
+  for (int base = 0; base < n; base += kClockThreads) {
+    const int i = base + tid;
+    int miss = 0;
+    int64_t t = -1;
+    if (i < n) {
+      t = idx[i];
+      if (t < 0 || t >= T) {
+        set_status(a.status, SKV_DEV_RANGE);
+        rows[i] = -1;
+      } else if (t < S) {
+        rows[i] = static_cast<int32_t>(t);
+      } else if (t >= T - W) {
+        rows[i] = static_cast<int32_t>(S + t % W);
+      } else if (!fits) {
+        rows[i] = -1;
+      } else {
+        const int32_t s = tslot[t];
+        if (s >= 0 && s < Hs) {
+          s_ref[s] = 1;
+          s_use[s] = a.step;
+          rows[i] = S + W + s;
+        } else {
+          if (s >= Hs) set_status(a.status, SKV_DEV_RANGE);
+          rows[i] = -1;
+          miss = 1;
+        }
+      }
+    }
+    int tot;
+    const int ex = block_exclusive_scan(miss, scr, &tot);
+    if (miss) {
+      m_tok[nm + ex] = static_cast<int32_t>(t);
+      m_pos[nm + ex] = i;
+      m_slot[nm + ex] = -1;
+    }
+    nm += tot;
+  }
+  __syncthreads();
+
+  // Phase 2: one warp sweeps the hand over windows of 32 slots.  In lane order
+  // a window is exactly the sequence the one-slot-at-a-time sweep would visit:
+  // used slots are skipped, empty or ref == 0 slots are taken (up to the
+  // number of misses left), ref == 1 slots passed by the hand are cleared.
+  if (warp == 0 && nm > 0) {
+    int h = a.hand[b];
+    if (h < 0 || h >= Hs) {
+      if (lane == 0) set_status(a.status, SKV_DEV_RANGE);
+      h = 0;
+    }
+    const int w = Hs < 32 ? Hs : 32;
+    const int64_t limit = 3 * static_cast<int64_t>(Hs) + 64;  // two turns always suffice
+    int64_t moved = 0;
+    int j = 0;
+    while (j < nm) {
+      if (moved > limit) {
+        if (lane == 0) set_status(a.status, SKV_DEV_COUNT);
+        break;
+      }
+      const bool act = lane < w;
+      int s = h + lane;
+      if (s >= Hs) s -= Hs;
+      const bool used = act && s_use[s] == a.step;
+      const int32_t st = act ? s_tok[s] : 0;
+      const bool r1 = act && s_ref[s] != 0;
+      const bool cand = act && !used && (st < 0 || !r1);
+      const unsigned mask = __ballot_sync(0xffffffffu, cand);
+      const int need = nm - j;
+      int pass = w;
+      if (__popc(mask) >= need) {
+        unsigned mm = mask;
+        for (int k = 1; k < need; k++) mm &= mm - 1;
+        pass = __ffs(mm);
+      }
+      const bool in = lane < pass;
+      if (in && act && !used && !cand) s_ref[s] = 0;
+      if (in && cand) {
+        const int jj = j + __popc(mask & ((1u << lane) - 1u));
+        const int32_t tok = m_tok[jj];
+        if (st >= 0 && st < a.t_cap) tslot[st] = -1;
+        s_tok[s] = tok;
+        tslot[tok] = s;
+        s_ref[s] = 1;
+        s_use[s] = a.step;
+        m_slot[jj] = s;
+        rows[m_pos[jj]] = S + W + s;
+      }
+      const unsigned low = pass >= 32 ? 0xffffffffu : ((1u << pass) - 1u);
+      j += __popc(mask & low);
+      h += pass;
+      if (h >= Hs) h -= Hs;
+      moved += pass;
+      __syncwarp();
+    }
+    if (lane == 0) a.hand[b] = h;
+  }
+  __syncthreads();
+
+  // Phase 3: fetch each miss's host row (Hkv heads x [K | V] int4 vectors)
+  // and write its int8 requantisation into the slot's pool rows.
+  const int ng = a.d / 64;
+  const int rb = a.d / 2 + 2 * ng;
+  const int tasks = 2 * a.Hkv * ng;
+  const int64_t tok_bytes = static_cast<int64_t>(tasks / ng) * rb;
+  const int nw = kClockThreads / 32;
+  for (int j0 = warp * kClockFetch; j0 < nm; j0 += nw * kClockFetch) {
+    for (int it = 0; it * 32 < tasks; it++) {
+      const int task = it * 32 + lane;
+      const bool tv = task < tasks;
+      const int v = task / ng, g = task % ng;
+      uint2 c[kClockFetch][4];
+      uint16_t sb[kClockFetch];
+#pragma unroll
+      for (int u = 0; u < kClockFetch; u++) {
+        const int j = j0 + u;
+        if (tv && j < nm && m_slot[j] >= 0) {
+          const uint8_t* src = a.host_rows + (static_cast<int64_t>(b) * a.t_cap + m_tok[j]) * tok_bytes +
+                               static_cast<int64_t>(v) * rb;
+          const uint2* cp = reinterpret_cast<const uint2*>(src + 32 * g);
+#pragma unroll
+          for (int q = 0; q < 4; q++) c[u][q] = cp[q];
+          sb[u] = *reinterpret_cast<const uint16_t*>(src + a.d / 2 + 2 * g);
+        } else {
+#pragma unroll
+          for (int q = 0; q < 4; q++) c[u][q] = make_uint2(0u, 0u);
+          sb[u] = 0;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kClockFetch; u++) {
+        const int j = j0 + u;
+        const bool live = tv && j < nm && m_slot[j] >= 0;
+        int8_t* dst = nullptr;
+        __half* sdst = nullptr;
+        if (live) {
+          const int64_t row = static_cast<int64_t>(b) * a.req_row_stride + S + W + m_slot[j];
+          const int hh = v >> 1;
+          dst = ((v & 1) ? a.v8 : a.k8) + (row * a.Hkv + hh) * a.d + 64 * g;
+          if (g == 0) sdst = ((v & 1) ? a.v_scale : a.k_scale) + row * a.Hkv + hh;
+        }
+        requant_group(c[u], sb[u], ng, dst, sdst, live);
+      }
+    }
+  }
+
+  // Phase 4: state back to global memory.
+  for (int s = tid; s < Hs; s += kClockThreads) {
+    a.slot_token[sbase + s] = s_tok[s];
+    a.use_step[sbase + s] = s_use[s];
+    a.ref[sbase + s] = s_ref[s];
+  }
+  if (tid == 0) a.n_miss[b] = fits ? nm : -1;
+}
+
+// ---------------------------------------------------------------------------
+// LRU hot buffer behind a block table.
+// ---------------------------------------------------------------------------
+struct LruArgs {
+  int64_t t_cap;
+  const int32_t* lengths;
+  int page;
+  const int32_t* block_table;
+  int64_t n_pages;
+  int64_t hot_base, hot_stride;
+  int n_slots;
+  int64_t step;
+  int64_t* stamp;
+  int32_t* slot_token;
+  int32_t* token_slot;
+  const uint8_t* host;
+  uint8_t* pool;
+  int64_t row_bytes, n_pool_rows;
+  const int32_t* idx;
+  int max_rows;
+  const int32_t* count;
+  int32_t* rows_out;
+  int32_t* n_miss;
+  int32_t* status;
+};
+
+int pow2_at_least(int n) {
+  int p = 1;
+  while (p < n) p <<= 1;
+  return p;
+}
+
+size_t lru_smem_bytes(int n_slots, int max_rows) {
+  return static_cast<size_t>(n_slots) * 8 + static_cast<size_t>(pow2_at_least(n_slots)) * 8 +
+         static_cast<size_t>(max_rows) * 8 + 64 * sizeof(int);
+}
+
+__global__ __launch_bounds__(kResThreads) void lru_kernel(LruArgs a, int P) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int ns = a.n_slots;
+  int64_t* s_stamp = reinterpret_cast<int64_t*>(smem);
+  uint64_t* key = reinterpret_cast<uint64_t*>(s_stamp + ns);
+  int32_t* m_tok = reinterpret_cast<int32_t*>(key + P);
+  int32_t* m_pos = m_tok + a.max_rows;
+  int* scr = reinterpret_cast<int*>(m_pos + a.max_rows);
+
+  int64_t T = a.lengths[b];
+  if (T < 0 || T > a.t_cap) {
+    if (tid == 0) set_status(a.status, SKV_DEV_RANGE);
+    T = T < 0 ? 0 : a.t_cap;
+  }
+  int n = a.count[b];
+  if (n < 0 || n > a.max_rows) {
+    if (tid == 0) set_status(a.status, SKV_DEV_COUNT);
+    n = n < 0 ? 0 : a.max_rows;
+  }
+  const int32_t* idx = a.idx + static_cast<int64_t>(b) * a.max_rows;
+  int32_t* rows = a.rows_out + static_cast<int64_t>(b) * a.max_rows;
+  int32_t* tslot = a.token_slot + static_cast<int64_t>(b) * a.t_cap;
+  const int32_t* bt = a.block_table + static_cast<int64_t>(b) * a.n_pages;
+  const int64_t sbase = static_cast<int64_t>(b) * ns;
+  const int64_t hot = a.hot_base + static_cast<int64_t>(b) * a.hot_stride;
+
+  for (int s = tid; s < ns; s += kResThreads) s_stamp[s] = a.stamp[sbase + s];
+  __syncthreads();
+
+  // Phase 1: resident rows in place, hot hits refresh their stamp, misses
+  // listed in ascending token order.
+  int nm = 0;
+  for (int base = 0; base < n; base += kResThreads) {
+    const int i = base + tid;
+    int miss = 0;
+    int64_t t = -1;
+    if (i < n) {
+      t = idx[i];
+      const int64_t p = t / a.page;
+      if (t < 0 || t >= T || p >= a.n_pages) {
+        set_status(a.status, SKV_DEV_RANGE);
+        rows[i] = -1;
+      } else if (bt[p] >= 0) {
+        const int64_t row = static_cast<int64_t>(bt[p]) * a.page + t % a.page;
+        if (row >= a.n_pool_rows) set_status(a.status, SKV_DEV_RANGE);
+        rows[i] = row < a.n_pool_rows ? static_cast<int32_t>(row) : -1;
+      } else {
+        const int32_t s = tslot[t];
+        if (s >= 0 && s < ns) {
+          s_stamp[s] = a.step;
+          rows[i] = static_cast<int32_t>(hot + s);
+        } else {
+          if (s >= ns) set_status(a.status, SKV_DEV_RANGE);
+          rows[i] = -1;
+          miss = 1;
+        }
+      }
+    }
+    int tot;
+    const int ex = block_exclusive_scan(miss, scr, &tot);
+    if (miss) {
+      m_tok[nm + ex] = static_cast<int32_t>(t);
+      m_pos[nm + ex] = i;
+    }
+    nm += tot;
+  }
+  __syncthreads();
+
+  // Phase 2: victims = untouched slots by ascending (stamp, slot): bitonic
+  // sort of the P keys (stamp + 1) << 32 | slot; touched and padding slots
+  // sort last.
+  int nc = 0;
+  for (int base = 0; base < P; base += kResThreads) {
+    const int s = base + tid;
+    bool c = false;
+    if (s < P) {
+      uint64_t k = ~0ull;
+      if (s < ns && s_stamp[s] != a.step) {
+        k = (static_cast<uint64_t>(s_stamp[s] + 1) << 32) | static_cast<uint32_t>(s);
+        c = true;
+      }
+      key[s] = k;
+    }
+    nc += __syncthreads_count(c);
+  }
+  const bool ok = nc >= nm;
+  if (!ok && tid == 0) set_status(a.status, SKV_DEV_COUNT);
+  if (ok && nm > 0) {
+    for (int size = 2; size <= P; size <<= 1) {
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        for (int x = tid; x < P / 2; x += kResThreads) {
+          const int lo = 2 * x - (x & (stride - 1));
+          const int hi = lo + stride;
+          const bool up = (lo & size) == 0;
+          const uint64_t kl = key[lo], kh = key[hi];
+          if ((kl > kh) == up) {
+            key[lo] = kh;
+            key[hi] = kl;
+          }
+        }
+        __syncthreads();
+      }
+    }
+    // Phase 3: the i-th miss takes the i-th victim.
+    for (int j = tid; j < nm; j += kResThreads) {
+      const int s = static_cast<int>(key[j] & 0xffffffffu);
+      const int32_t tok = m_tok[j];
+      const int32_t old = a.slot_token[sbase + s];
+      if (old >= 0 && old < a.t_cap) tslot[old] = -1;
+      a.slot_token[sbase + s] = tok;
+      tslot[tok] = s;
+      s_stamp[s] = a.step;
+      rows[m_pos[j]] = static_cast<int32_t>(hot + s);
+    }
+    // Copy the miss rows from the host alias, kFetchRows rows per warp at once.
+    const int chunks = static_cast<int>(a.row_bytes / 16);
+    const int nw = kResThreads / 32;
+    for (int j0 = warp * kFetchRows; j0 < nm; j0 += nw * kFetchRows) {
+      for (int c0 = 0; c0 < chunks; c0 += 32) {
+        const int c = c0 + lane;
+        uint4 v[kFetchRows];
+#pragma unroll
+        for (int u = 0; u < kFetchRows; u++) {
+          const int j = j0 + u;
+          if (c < chunks && j < nm)
+            v[u] = reinterpret_cast<const uint4*>(a.host + (static_cast<int64_t>(b) * a.t_cap + m_tok[j]) *
+                                                               a.row_bytes)[c];
+        }
+#pragma unroll
+        for (int u = 0; u < kFetchRows; u++) {
+          const int j = j0 + u;
+          if (c < chunks && j < nm) {
+            const int s = static_cast<int>(key[j] & 0xffffffffu);
+            reinterpret_cast<uint4*>(a.pool + (hot + s) * a.row_bytes)[c] = v[u];
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+  for (int s = tid; s < ns; s += kResThreads) a.stamp[sbase + s] = s_stamp[s];
+  if (tid == 0) a.n_miss[b] = ok ? nm : -1;
+}
+
+// ---------------------------------------------------------------------------
+// Host-tier write path: int4 rows with 64-dim groups and fp16 group scales.
+// ---------------------------------------------------------------------------
+// One warp per (row, head) vector of d = 256*m dims: lane l encodes dims
+// [8l, 8l+8) of each 256-dim block (group g = l/8 of the block).
+__global__ __launch_bounds__(256) void quant_int4_kernel(const uint16_t* __restrict__ x, int64_t n_items,
+                                                         int Hkv, int d, const int64_t* __restrict__ out_rows,
+                                                         uint8_t* __restrict__ out, int64_t token_pitch,
+                                                         int64_t head_pitch) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  for (int64_t item = static_cast<int64_t>(blockIdx.x) * nw + warp; item < n_items;
+       item += static_cast<int64_t>(gridDim.x) * nw) {
+    const int64_t t = item / Hkv;
+    const int h = static_cast<int>(item % Hkv);
+    const int64_t orow = out_rows ? out_rows[t] : t;
+    uint8_t* o = out + orow * token_pitch + h * head_pitch;
+    const uint16_t* row = x + item * d;
+    for (int blk = 0; blk < d; blk += 256) {
+      const uint4 v = *reinterpret_cast<const uint4*>(row + blk + 8 * lane);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      float f[8];
+#pragma unroll
+      for (int e = 0; e < 4; e++) {
+        f[2 * e] = __uint_as_float(w[e] << 16);
+        f[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+      }
+      float amax = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; e++) amax = fmaxf(amax, fabsf(f[e]));
+#pragma unroll
+      for (int o2 = 1; o2 < 8; o2 <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o2));
+      const __half sh = __float2half_rn(__fdiv_rn(amax, 7.f));
+      const float sf = __half2float(sh);
+      const bool ok = (sf != 0.f) && isfinite(sf);
+      uint32_t packed = 0;
+#pragma unroll
+      for (int e = 0; e < 8; e++) {
+        const int q = ok ? rint_clamp(__fdiv_rn(f[e], sf), -8, 7) : 0;
+        packed |= (static_cast<uint32_t>(q) & 0xfu) << (4 * e);
+      }
+      *reinterpret_cast<uint32_t*>(o + blk / 2 + 4 * lane) = packed;
+      if ((lane & 7) == 0) {
+        const int g = blk / 64 + lane / 8;
+        *reinterpret_cast<__half*>(o + d / 2 + 2 * g) = sh;
+      }
+    }
+  }
+}
+
+// Streaming read of a buffer (HBM or a host alias) with 16-byte loads; the
+// XOR of every word goes to *sink so the loads cannot be dropped.
+__global__ __launch_bounds__(512) void stream_read_kernel(const uint4* __restrict__ p, int64_t n16,
+                                                          unsigned long long* sink) {
+  uint32_t acc = 0;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (; i + 3 * stride < n16; i += 4 * stride) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; u++) v[u] = ld_stream16(p + i + u * stride);
+#pragma unroll
+    for (int u = 0; u < 4; u++) acc ^= v[u].x ^ v[u].y ^ v[u].z ^ v[u].w;
+  }
+  for (; i < n16; i += stride) {
+    const uint4 v = ld_stream16(p + i);
+    acc ^= v.x ^ v.y ^ v.z ^ v.w;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc ^= __shfl_xor_sync(0xffffffffu, acc, o);
+  if ((threadIdx.x & 31) == 0 && acc) atomicXor(sink, static_cast<unsigned long long>(acc));
+}
+
+}  // namespace
+}  // namespace skv
+
+using namespace skv;
+
+SKV_EXPORT int skv_resolve_rows_clock(int B, int64_t t_cap, const int32_t* lengths, int S, int W, int Hkv, int d,
+                                      int Hs, const int32_t* idx, int max_rows, const int32_t* count,
+                                      int32_t step, int32_t* slot_token, uint8_t* ref, int32_t* use_step,
+                                      int32_t* token_slot, int32_t* hand, const uint8_t* host_rows, int8_t* k8,
+                                      int8_t* v8, uint16_t* k_scale, uint16_t* v_scale, int64_t req_row_stride,
+                                      int32_t* rows_out, int32_t* n_miss, int32_t* dev_status, void* stream) {
+  if (B < 0 || B > 65535 || t_cap < 0 || S < 0 || W < 0 || Hkv < 1 || Hs < 1 || max_rows < 1) return SKV_EINVAL;
+  if (B == 0) return SKV_OK;
+  if (d < 256 || d % 256 || d > 1024) return SKV_EUNSUPPORTED;
+  if (Hs > kMaxClockSlots || max_rows > kMaxResolveRows || t_cap > INT32_MAX) return SKV_EUNSUPPORTED;
+  if (step < 0 || req_row_stride < static_cast<int64_t>(S) + W + Hs) return SKV_EINVAL;
+  if (!lengths || !idx || !count || !slot_token || !ref || !use_step || !token_slot || !hand || !host_rows ||
+      !k8 || !v8 || !k_scale || !v_scale || !rows_out || !n_miss)
+    return SKV_EINVAL;
+  if (!aligned16(host_rows) || !aligned16(k8) || !aligned16(v8)) return SKV_EINVAL;
+  const size_t smem = clock_smem_bytes(Hs, max_rows);
+  static size_t configured = 0;
+  if (smem > 48 * 1024 && smem > configured) {
+    if (cudaFuncSetAttribute(clock_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return SKV_EUNSUPPORTED;
+    }
+    configured = smem;
+  }
+  ClockArgs a{t_cap, lengths, S, W, Hkv, d, Hs, idx, max_rows, count, step, slot_token, ref, use_step,
+              token_slot, hand, host_rows, k8, v8, reinterpret_cast<__half*>(k_scale),
+              reinterpret_cast<__half*>(v_scale), req_row_stride, rows_out, n_miss, dev_status};
+  clock_kernel<<<B, kClockThreads, smem, as_stream(stream)>>>(a);
+  return launch_status();
+}
+
+SKV_EXPORT int skv_resolve_rows_lru(int B, int64_t t_cap, const int32_t* lengths, int page,
+                                    const int32_t* block_table, int64_t n_pages, int64_t hot_base,
+                                    int64_t hot_stride, int n_slots, int64_t step, int64_t* stamp,
+                                    int32_t* slot_token, int32_t* token_slot, const uint8_t* host, uint8_t* pool,
+                                    int64_t row_bytes, int64_t n_pool_rows, const int32_t* idx, int max_rows,
+                                    const int32_t* count, int32_t* rows_out, int32_t* n_miss, int32_t* dev_status,
+                                    void* stream) {
+  if (B < 0 || B > 65535 || t_cap < 0 || page < 1 || n_pages < 0 || n_slots < 1 || max_rows < 1 ||
+      row_bytes < 16 || row_bytes % 16 || hot_base < 0 || hot_stride < 0)
+    return SKV_EINVAL;
+  if (B == 0) return SKV_OK;
+  if (n_slots > kMaxLruSlots || max_rows > kMaxResolveRows || t_cap > INT32_MAX) return SKV_EUNSUPPORTED;
+  if (step < 0 || step >= INT32_MAX) return SKV_EINVAL;
+  if (hot_base + static_cast<int64_t>(B - 1) * hot_stride + n_slots > n_pool_rows || n_pool_rows > INT32_MAX)
+    return SKV_EINVAL;
+  if (!lengths || !block_table || !stamp || !slot_token || !token_slot || !host || !pool || !idx || !count ||
+      !rows_out || !n_miss)
+    return SKV_EINVAL;
+  if (!aligned16(host) || !aligned16(pool)) return SKV_EINVAL;
+  const int P = pow2_at_least(n_slots);
+  const size_t smem = lru_smem_bytes(n_slots, max_rows);
+  static size_t configured = 0;
+  if (smem > 48 * 1024 && smem > configured) {
+    if (cudaFuncSetAttribute(lru_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return SKV_EUNSUPPORTED;
+    }
+    configured = smem;
+  }
+  LruArgs a{t_cap, lengths, page, block_table, n_pages, hot_base, hot_stride, n_slots, step, stamp, slot_token,
+            token_slot, host, pool, row_bytes, n_pool_rows, idx, max_rows, count, rows_out, n_miss, dev_status};
+  lru_kernel<<<B, kResThreads, smem, as_stream(stream)>>>(a, P);
+  return launch_status();
+}
+
+SKV_EXPORT int skv_quantize_int4_rows(const uint16_t* x, int64_t n_rows, int Hkv, int d, const int64_t* out_rows,
+                                      uint8_t* out, int64_t token_pitch, int64_t head_pitch, void* stream) {
+  if (n_rows < 0 || Hkv < 1 || d < 256 || d % 256 || d > 1024) return SKV_EINVAL;
+  if (n_rows == 0) return SKV_OK;
+  if (!x || !out || !aligned16(x)) return SKV_EINVAL;
+  const int64_t rb = d / 2 + 2 * (d / 64);
+  if (head_pitch < rb || token_pitch < Hkv * head_pitch) return SKV_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(out) | token_pitch | head_pitch) & 3) return SKV_EINVAL;
+  const int64_t items = n_rows * Hkv;
+  int64_t grid = (items + 7) / 8;
+  const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
+  if (grid > cap && cap > 0) grid = cap;
+  quant_int4_kernel<<<static_cast<int>(grid), 256, 0, as_stream(stream)>>>(x, items, Hkv, d, out_rows, out,
+                                                                            token_pitch, head_pitch);
+  return launch_status();
+}
+
+SKV_EXPORT int skv_stream_read(const void* src, size_t bytes, unsigned long long* sink, int grid, void* stream) {
+  if (!src || !sink || bytes % 16 || !aligned16(src) || grid < 0) return SKV_EINVAL;
+  if (bytes == 0) return SKV_OK;
+  if (grid == 0) grid = 2 * sm_count();
+  stream_read_kernel<<<grid, 512, 0, as_stream(stream)>>>(static_cast<const uint4*>(src),
+                                                          static_cast<int64_t>(bytes / 16), sink);
+  return launch_status();
+}

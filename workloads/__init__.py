@@ -242,6 +242,23 @@ def pooled_inputs_cpu(B: int, T: int | list, Hq: int, Hkv: int, d: int, d_idx: i
             "q_idx": to_bf16_bits(q_idx), "idx_keys": to_bf16_bits(idx_keys), "lengths": lengths}
 
 
+def pick_sequence(rng: np.random.Generator, lo: int, hi: int, k: int, n_steps: int, keep: float) -> list:
+    """Drifting selections for resolver tests: each step keeps about `keep` of
+    the previous step's tokens and draws the rest uniformly from [lo, hi).
+    Returns n_steps sorted unique int32 arrays of k tokens (k <= hi - lo)."""
+    seq = []
+    prev = np.zeros((0,), np.int64)
+    for _ in range(n_steps):
+        n_keep = min(len(prev), int(round(keep * k)))
+        kept = rng.choice(prev, size=n_keep, replace=False) if n_keep else prev[:0]
+        pool = np.setdiff1d(np.arange(lo, hi), kept)
+        new = rng.choice(pool, size=k - n_keep, replace=False)
+        cur = np.sort(np.concatenate([kept, new]))
+        seq.append(cur.astype(np.int32))
+        prev = cur
+    return seq
+
+
 # ---------------------------------------------------------------------------
 # Device (torch) generators, used by the benchmark at full size
 # ---------------------------------------------------------------------------
