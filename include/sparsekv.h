@@ -336,6 +336,37 @@ int skv_sparse_attend_decode(int kv_kind, int B, int Hq, int Hkv, int d,
                              float softmax_scale, float *out, void *workspace,
                              size_t workspace_bytes, int32_t *dev_status, void *stream);
 
+/*
+ * skv_sparse_attend_mla -- a6 over latent (MLA) rows: 128 absorbed query
+ * heads attend over fp8 e4m3 rows of d = 576 values (512 latent + 64 rope,
+ * RoPE already applied); V is the first dv = 512 values of the same row
+ * ([P2] "vLLM's Hybrid HiSparse ...", "Three residency states, one block
+ * pool": the kernel reads each selected row where the resolver placed it).
+ * For request b, head g and the count[b] rows p_i = b*req_row_stride +
+ * rows[b][i], with x_i = fp8 value times row_scale[p_i] (1 when row_scale is
+ * NULL):
+ *   logit_i = softmax_scale * sum_{j<576} q[b][g][j] * x_i[j]
+ *   out[b][g][:] = sum_i softmax(logit)_i * x_i[0:512]
+ *   q          bf16 [B][128][576] (converted to fp16 on chip: |q| <= 65504)
+ *   kv_pool    fp8 e4m3 bytes [n_pool_rows][576]
+ *   row_scale  fp32 [n_pool_rows] or NULL
+ *   out        fp32 [B][128][512]
+ *   workspace  skv_mla_workspace_size(B, max_rows) bytes (no zero-fill needed)
+ * A row outside [0, n_pool_rows) is skipped and sets SKV_DEV_RANGE.  The
+ * row splits are merged in a fixed order: the output is deterministic.
+ * Runs on the tcgen05 tensor cores with fp16 operands (fp8 -> fp16 exact),
+ * fp32 accumulation; probabilities rounded to fp16.
+ * Errors: SKV_EUNSUPPORTED unless Hq = 128, d = 576, dv = 512; SKV_EINVAL for
+ * null or unaligned (16 B) q, kv_pool, out or workspace, max_rows outside
+ * [1, 65536]; SKV_ENOMEM for a short workspace.
+ */
+size_t skv_mla_workspace_size(int B, int max_rows);
+int skv_sparse_attend_mla(int B, int Hq, int d, int dv, const uint16_t *q, const uint8_t *kv_pool,
+                          const float *row_scale, int64_t req_row_stride, int64_t n_pool_rows,
+                          const int32_t *rows, int max_rows, const int32_t *count,
+                          float softmax_scale, float *out, void *workspace, size_t workspace_bytes,
+                          int32_t *dev_status, void *stream);
+
 /* ========================================================================== */
 /* a5: resolve the selected tokens to pool rows.  RESIDENT is the identity    */
 /* (attention's req_row_stride addressing); the two calls below resolve       */

@@ -63,6 +63,9 @@ def _load():
                 "skv_attend_workspace_size": ([i32, i32, i32, i32, i32], sz),
                 "skv_sparse_attend_decode": ([i32, i32, i32, i32, i32, P, P, P, P, P, i64, i64, P, i32, P,
                                               f32, P, P, sz, P, P], i32),
+                "skv_mla_workspace_size": ([i32, i32], sz),
+                "skv_sparse_attend_mla": ([i32, i32, i32, i32, P, P, P, i64, i64, P, i32, P, f32, P, P, sz, P, P],
+                                          i32),
                 "skv_resolve_rows_clock": ([i32, i64, P, i32, i32, i32, i32, i32, P, i32, P, i32, P, P, P, P, P, P,
                                             P, P, P, P, i64, P, P, P, P], i32),
                 "skv_resolve_rows_lru": ([i32, i64, P, i32, P, i64, i64, i64, i32, i64, P, P, P, P, P, i64, i64, P,
@@ -276,6 +279,24 @@ def sparse_attend_decode(kv_kind, q, k_pool, v_pool, rows, count, softmax_scale,
         int(req_row_stride), int(n_pool_rows), _ptr(rows), rows.shape[1], _ptr(count), float(softmax_scale),
         _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(status),
         _stream(stream)))
+    return out
+
+
+def mla_workspace_size(B, max_rows) -> int:
+    return int(_load().skv_mla_workspace_size(B, max_rows))
+
+
+def sparse_attend_mla(q, kv_pool, rows, count, softmax_scale, out, workspace, row_scale=None, req_row_stride=0,
+                      n_pool_rows=None, status=None, stream=None):
+    """q bf16 [B][128][576]; kv_pool uint8 (fp8 e4m3) [n_rows][576]; rows int32 [B][max_rows] -> out fp32."""
+    B, Hq, d = q.shape
+    dv = out.shape[2]
+    if n_pool_rows is None:
+        n_pool_rows = kv_pool.shape[0]
+    _check("skv_sparse_attend_mla", _load().skv_sparse_attend_mla(
+        B, Hq, d, dv, _ptr(q), _ptr(kv_pool), _ptr(row_scale), int(req_row_stride), int(n_pool_rows), _ptr(rows),
+        rows.shape[1], _ptr(count), float(softmax_scale), _ptr(out), _ptr(workspace),
+        0 if workspace is None else workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream)))
     return out
 
 

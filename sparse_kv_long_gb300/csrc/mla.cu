@@ -1,0 +1,479 @@
+// mla.cu -- a6 over latent (MLA) rows: exact sparse attention of 128 absorbed
+// query heads over fp8 e4m3 rows of 576 values (512 latent + 64 rope, V = the
+// latent part), on the 5th-generation tensor cores.
+//
+// [P2] "vLLM's Hybrid HiSparse ...", "Three residency states, one block pool":
+// the attention kernel reads the selected rows wherever the resolver put
+// them (in place, hot buffer); the pool rows here are what that resolver
+// returns.
+//
+// Per request the work is S = Q.K^T (M = 128 heads, K = 576) and O = P.V
+// (N = 512): 570 MFLOP over 2048 rows, about 480 flop per byte read, so the
+// tensor cores set the pace.  The fp32 output O (128 x 512) alone fills a
+// whole SM's tensor memory, so a CTA pair (cluster of 2) shares every row
+// chunk:
+//   * CTA r gathers dims [256 r, 256 r + 320) of each row (fp8 -> fp16, exact)
+//     into a 128-byte-swizzled tile that serves both products;
+//   * it computes the partial logits over its share of the contraction
+//     (dims [0, 320) and [320, 576)), sends them to its peer through
+//     distributed shared memory and adds the peer's (a + b on both sides, so
+//     both hold the same logits and the same softmax);
+//   * it accumulates O for its half of the value dims ([0, 256) or
+//     [256, 512)) in tensor memory.
+// Roles in a CTA: warp 0 issues tcgen05.mma (one thread), warps 1-3 gather
+// rows, warps 4-7 own one head each (tensor-memory lane = head) for the
+// online softmax and the epilogue.  Rows are split across clusters; the splits
+// are merged in a fixed order, so the result is deterministic.
+#include "tc.cuh"
+
+namespace skv {
+namespace {
+
+constexpr int kH = 128;
+constexpr int kD = 576;
+constexpr int kDv = 512;
+constexpr int kNr = 64;                         // rows per chunk (N of the logit product)
+constexpr int kSlice = 320;                     // dims gathered per CTA
+constexpr int kAtoms = kSlice / 64;             // 64-dim swizzle atoms per tile row
+constexpr int kPieces = kSlice / 16;            // 16-byte fp8 pieces per row and CTA
+constexpr int kQBytes = kAtoms * kH * 128;      // 80 KB
+constexpr int kKVBytes = kAtoms * kNr * 128;    // 40 KB
+constexpr int kPBytes = kH * 128;               // 16 KB
+constexpr int kXBytes = kH * kNr * 4;           // 32 KB
+constexpr int kThreads = 256;
+constexpr int kProducers = 96;
+constexpr int kPerProducer = (kNr * kPieces + kProducers - 1) / kProducers;
+constexpr int kTmemCols = 512;                  // S double buffer at [0, 128), O at [256, 512)
+constexpr int kOCol = 256;
+constexpr float kRescaleLog2 = 8.f;             // rescale O only when the max grows by > 2^8
+
+struct Aux {
+  uint64_t kv_full[2], kv_empty[2], s_full[2], s_empty[2];
+  uint64_t p_full, pv_done, x_full, x_empty, mma_idle;
+  int32_t row[2][kNr];
+  float rs[2][kNr];
+  uint32_t tmem_base;
+  int abort;
+};
+
+constexpr int kSmem = 1024 + kQBytes + 2 * kKVBytes + kPBytes + kXBytes + static_cast<int>(sizeof(Aux));
+
+struct MlaArgs {
+  const uint16_t* q;
+  const uint8_t* pool;
+  const float* row_scale;
+  int64_t req_row_stride, n_pool_rows;
+  const int32_t* rows;
+  int max_rows;
+  const int32_t* count;
+  float scale_log2;
+  float* out;
+  float* ws_o;
+  float* ws_ml;
+  int nsplit;
+  int32_t* status;
+};
+
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+  const __half2 h = __floats2half2_rn(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n)); }
+
+// Named barrier over n threads that also ANDs a predicate across them.
+__device__ __forceinline__ bool named_sync_and(int id, int n, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbarrier.red.and.pred q, %2, %3, p;\nselp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_kernel(MlaArgs a) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* sm = smem_raw + ((1024u - (tc::smem_addr(smem_raw) & 1023u)) & 1023u);
+  unsigned char* sQ = sm;
+  unsigned char* sKV = sQ + kQBytes;
+  unsigned char* sP = sKV + 2 * kKVBytes;
+  float* sX = reinterpret_cast<float*>(sP + kPBytes);
+  Aux* ax = reinterpret_cast<Aux*>(sP + kPBytes + kXBytes);
+
+  const uint32_t rank = tc::cluster_rank(), peer = rank ^ 1u;
+  const int split = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  int n = a.count[b];
+  if (n < 0 || n > a.max_rows) {
+    if (tid == 0 && rank == 0 && split == 0) set_status(a.status, SKV_DEV_COUNT);
+    n = n < 0 ? 0 : a.max_rows;
+  }
+  const int per = ((n + a.nsplit - 1) / a.nsplit + kNr - 1) / kNr * kNr;
+  const int r0 = split * per;
+  const int r1 = min(n, r0 + per);
+  const int nchunks = r1 > r0 ? (r1 - r0 + kNr - 1) / kNr : 0;
+
+  if (tid == 0) {
+    for (int s = 0; s < 2; s++) {
+      tc::bar_init(&ax->kv_full[s], kProducers);
+      tc::bar_init(&ax->kv_empty[s], 1);
+      tc::bar_init(&ax->s_full[s], 1);
+      tc::bar_init(&ax->s_empty[s], kH);
+    }
+    tc::bar_init(&ax->p_full, kH);
+    tc::bar_init(&ax->pv_done, 1);
+    tc::bar_init(&ax->x_full, kH);
+    tc::bar_init(&ax->x_empty, kH);
+    tc::bar_init(&ax->mma_idle, 1);
+    ax->abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+
+  // Query slice -> fp16, 128-byte-swizzled K-major tile (one 128 B row per head
+  // and 64-dim atom).  CTA 0 holds dims [0, 320), CTA 1 dims [320, 576).
+  const int qdim0 = rank == 0 ? 0 : kSlice;
+  const int qatoms = rank == 0 ? kAtoms : kAtoms - 1;
+  for (int u = tid; u < kH * qatoms * 8; u += kThreads) {
+    const int h = u / (qatoms * 8), cc = u % (qatoms * 8);
+    const uint4 v = *reinterpret_cast<const uint4*>(a.q + (static_cast<int64_t>(b) * kH + h) * kD + qdim0 + 8 * cc);
+    const uint4 f = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z),
+                               bf16x2_to_f16x2(v.w));
+    *reinterpret_cast<uint4*>(sQ + (cc >> 3) * (kH * 128) + h * 128 + (((cc & 7) ^ (h & 7)) << 4)) = f;
+  }
+  tc::fence_async_smem();
+  if (warp == 0) tc::tmem_alloc<kTmemCols>(&ax->tmem_base);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  tc::cluster_sync();  // the peer's barriers exist before any remote access
+  const uint32_t tm = ax->tmem_base;
+  volatile int* abort = &ax->abort;
+
+  if (warp == 0) {
+    // ---------------- MMA issue (one thread) ----------------
+    if (lane == 0 && nchunks > 0) {
+      const uint32_t aQ = tc::smem_addr(sQ), aKV = tc::smem_addr(sKV), aP = tc::smem_addr(sP);
+      constexpr uint32_t id_qk = tc::idesc_f16(kH, kNr, 0);
+      constexpr uint32_t id_pv = tc::idesc_f16(kH, 256, 1);
+      auto issue_qk = [&](int i) {
+        const uint32_t kv = aKV + (i & 1) * kKVBytes;
+        const uint32_t d = tm + (i & 1) * kNr;
+        for (int qa = 0; qa < qatoms; qa++) {
+          const int ka = rank == 0 ? qa : qa + 1;  // CTA 1's tile starts at dim 256
+#pragma unroll
+          for (int kk = 0; kk < 4; kk++)
+            tc::mma_f16(d, tc::sw128_desc(aQ + qa * (kH * 128) + kk * 32, 16, 1024),
+                        tc::sw128_desc(kv + ka * (kNr * 128) + kk * 32, 16, 1024), id_qk, qa > 0 || kk > 0);
+        }
+      };
+      bool ok = tc::bar_wait(&ax->kv_full[0], 0, abort);
+      if (ok) {
+        tc::tc_fence_after();
+        issue_qk(0);
+        tc::mma_commit(&ax->s_full[0]);
+      }
+      for (int i = 0; ok && i < nchunks; i++) {
+        const int j = i + 1;
+        if (j < nchunks) {
+          ok = tc::bar_wait(&ax->kv_full[j & 1], (j >> 1) & 1, abort);
+          if (ok && j >= 2) ok = tc::bar_wait(&ax->s_empty[j & 1], ((j >> 1) - 1) & 1, abort);
+          if (!ok) break;
+          tc::tc_fence_after();
+          issue_qk(j);
+          tc::mma_commit(&ax->s_full[j & 1]);
+        }
+        ok = tc::bar_wait(&ax->p_full, i & 1, abort);
+        if (!ok) break;
+        tc::tc_fence_after();
+        const uint32_t kv = aKV + (i & 1) * kKVBytes;
+#pragma unroll
+        for (int kk = 0; kk < 4; kk++)  // 16 rows per step; value dims are the tile's first 4 atoms
+          tc::mma_f16(tm + kOCol, tc::sw128_desc(aP + kk * 32, 16, 1024),
+                      tc::sw128_desc(kv + kk * 2048, kNr * 128, 1024), id_pv, i > 0 || kk > 0);
+        tc::mma_commit(&ax->pv_done);
+        tc::mma_commit(&ax->kv_empty[i & 1]);
+      }
+      // Nothing of this thread's may still be running when the tensor memory
+      // is released (also after a wait that gave up).
+      tc::mma_commit(&ax->mma_idle);
+      if (!tc::bar_drain(&ax->mma_idle, 0, 4000000000ull)) set_status(a.status, SKV_DEV_TIMEOUT);
+    }
+  } else if (warp < 4) {
+    // ---------------- row gather: fp8 -> fp16 swizzled tiles ----------------
+    const int pt = tid - 32;
+    for (int i = 0; i < nchunks; i++) {
+      const int s = i & 1;
+      const bool free_buf = i < 2 || tc::bar_wait(&ax->kv_empty[s], ((i >> 1) - 1) & 1, abort);
+      if (!named_sync_and(1, kProducers, free_buf)) break;  // the same decision in every producer
+      if (pt < kNr) {
+        const int gi = r0 + i * kNr + pt;
+        int64_t p = -1;
+        float rsc = 0.f;
+        if (gi < r1) {
+          p = static_cast<int64_t>(b) * a.req_row_stride + a.rows[static_cast<int64_t>(b) * a.max_rows + gi];
+          if (p < 0 || p >= a.n_pool_rows) {
+            if (rank == 0) set_status(a.status, SKV_DEV_RANGE);
+            p = -1;
+          } else {
+            rsc = a.row_scale ? a.row_scale[p] : 1.f;
+          }
+        }
+        ax->row[s][pt] = static_cast<int32_t>(p);
+        ax->rs[s][pt] = rsc;
+      }
+      named_sync(1, kProducers);
+      uint4 v[kPerProducer];
+#pragma unroll
+      for (int m = 0; m < kPerProducer; m++) {
+        const int u = pt + m * kProducers;
+        v[m] = make_uint4(0u, 0u, 0u, 0u);
+        if (u < kNr * kPieces) {
+          const int jr = u / kPieces, q = u % kPieces;
+          const int32_t p = ax->row[s][jr];
+          if (p >= 0) v[m] = ld_nc16(a.pool + static_cast<int64_t>(p) * kD + rank * 256 + 16 * q);
+        }
+      }
+      unsigned char* tile = sKV + s * kKVBytes;
+#pragma unroll
+      for (int m = 0; m < kPerProducer; m++) {
+        const int u = pt + m * kProducers;
+        if (u < kNr * kPieces) {
+          const int jr = u / kPieces, q = u % kPieces;
+          const int c0 = (q & 3) * 2;
+          const uint2 e0 = tc::e4m3x4_to_f16x4(v[m].x), e1 = tc::e4m3x4_to_f16x4(v[m].y);
+          const uint2 e2 = tc::e4m3x4_to_f16x4(v[m].z), e3 = tc::e4m3x4_to_f16x4(v[m].w);
+          unsigned char* row = tile + (q >> 2) * (kNr * 128) + jr * 128;
+          *reinterpret_cast<uint4*>(row + ((c0 ^ (jr & 7)) << 4)) = make_uint4(e0.x, e0.y, e1.x, e1.y);
+          *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ (jr & 7)) << 4)) = make_uint4(e2.x, e2.y, e3.x, e3.y);
+        }
+      }
+      tc::fence_async_smem();
+      tc::bar_arrive(&ax->kv_full[s]);
+      named_sync(1, kProducers);  // row ids of buffer s are read above before the next refill
+    }
+  } else {
+    // ---------------- softmax + epilogue: thread = head ----------------
+    const int h = tid - 128;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    float* xrow = sX + h * kNr;
+    for (int i = 0; i < nchunks; i++) {
+      const int s = i & 1;
+      ok = __all_sync(0xffffffffu, tc::bar_wait(&ax->s_full[s], (i >> 1) & 1, abort));
+      if (!ok) break;
+      tc::tc_fence_after();
+      uint32_t ra[32], rb[32];
+      tc::tmem_ld32(tm + lane_base + s * kNr, ra);
+      tc::tmem_ld32(tm + lane_base + s * kNr + 32, rb);
+      tc::tmem_wait_ld();
+      tc::tc_fence_before();
+      tc::bar_arrive(&ax->s_empty[s]);
+      // partial logits to the peer, then the peer's from this CTA's buffer
+      if (i >= 1) {
+        ok = __all_sync(0xffffffffu, tc::bar_wait(&ax->x_empty, (i - 1) & 1, abort, true));
+        if (!ok) break;
+      }
+#pragma unroll
+      for (int c = 0; c < 16; c++) {
+        const uint32_t* r = c < 8 ? &ra[4 * c] : &rb[4 * (c - 8)];
+        tc::st_remote16(xrow + 4 * (c ^ (h & 7)), peer,
+                        make_float4(__uint_as_float(r[0]), __uint_as_float(r[1]), __uint_as_float(r[2]),
+                                    __uint_as_float(r[3])));
+      }
+      tc::bar_arrive_remote(&ax->x_full, peer);
+      ok = __all_sync(0xffffffffu, tc::bar_wait(&ax->x_full, i & 1, abort, true));
+      if (!ok) break;
+      float x[64];
+#pragma unroll
+      for (int c = 0; c < 16; c++) {
+        const float4 o = *reinterpret_cast<const float4*>(xrow + 4 * (c ^ (h & 7)));
+        const uint32_t* r = c < 8 ? &ra[4 * c] : &rb[4 * (c - 8)];
+        x[4 * c] = __uint_as_float(r[0]) + o.x;
+        x[4 * c + 1] = __uint_as_float(r[1]) + o.y;
+        x[4 * c + 2] = __uint_as_float(r[2]) + o.z;
+        x[4 * c + 3] = __uint_as_float(r[3]) + o.w;
+      }
+      tc::bar_arrive_remote(&ax->x_empty, peer);
+      float mc = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 64; j++) {
+        const bool valid = ax->row[s][j] >= 0;
+        const float v = valid ? x[j] * ax->rs[s][j] * a.scale_log2 : -INFINITY;
+        x[j] = v;
+        mc = fmaxf(mc, v);
+      }
+      bool rescale = false;
+      float alpha = 1.f;
+      if (mc > m_ref + kRescaleLog2) {
+        alpha = exp2f(m_ref - mc);
+        rescale = i > 0;
+        m_ref = mc;
+      }
+      if (i >= 1) {
+        ok = __all_sync(0xffffffffu, tc::bar_wait(&ax->pv_done, (i - 1) & 1, abort));
+        if (!ok) break;
+        tc::tc_fence_after();
+      }
+      if (rescale) {
+        for (int c0 = 0; c0 < 256; c0 += 32) {
+          uint32_t o[32];
+          tc::tmem_ld32(tm + lane_base + kOCol + c0, o);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 32; k++) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+          tc::tmem_st32(tm + lane_base + kOCol + c0, o);
+        }
+        tc::tmem_wait_st();
+        l *= alpha;
+      }
+      float lsum = 0.f;
+      uint32_t pk[32];
+#pragma unroll
+      for (int j = 0; j < 64; j += 2) {
+        const float p0 = x[j] == -INFINITY ? 0.f : exp2f(x[j] - m_ref);
+        const float p1 = x[j + 1] == -INFINITY ? 0.f : exp2f(x[j + 1] - m_ref);
+        lsum += p0;
+        lsum += p1;
+        pk[j >> 1] = pack_f16x2(p0 * ax->rs[s][j], p1 * ax->rs[s][j + 1]);
+      }
+      l += lsum;
+#pragma unroll
+      for (int c = 0; c < 8; c++)
+        *reinterpret_cast<uint4*>(sP + h * 128 + ((c ^ (h & 7)) << 4)) =
+            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      tc::fence_async_smem();
+      tc::tc_fence_before();
+      tc::bar_arrive(&ax->p_full);
+    }
+    // epilogue: this CTA's 256 value dims of head h
+    bool have_o = ok && nchunks > 0;
+    if (have_o) {
+      have_o = __all_sync(0xffffffffu, tc::bar_wait(&ax->pv_done, (nchunks - 1) & 1, abort));
+      tc::tc_fence_after();
+    }
+    if (!ok || (nchunks > 0 && !have_o)) set_status(a.status, SKV_DEV_TIMEOUT);
+    const bool merged = a.nsplit == 1;
+    const float inv = (merged && l > 0.f) ? 1.f / l : 0.f;
+    float* dst = merged ? a.out + (static_cast<int64_t>(b) * kH + h) * kDv + rank * 256
+                        : a.ws_o + ((static_cast<int64_t>(b) * a.nsplit + split) * kH + h) * kDv + rank * 256;
+    for (int c0 = 0; c0 < 256; c0 += 32) {
+      uint32_t o[32];
+      if (have_o) {
+        tc::tmem_ld32(tm + lane_base + kOCol + c0, o);
+        tc::tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int k = 0; k < 32; k++) o[k] = 0u;
+      }
+#pragma unroll
+      for (int k = 0; k < 32; k += 4) {
+        float4 v = make_float4(__uint_as_float(o[k]), __uint_as_float(o[k + 1]), __uint_as_float(o[k + 2]),
+                               __uint_as_float(o[k + 3]));
+        if (merged) v = make_float4(v.x * inv, v.y * inv, v.z * inv, v.w * inv);
+        *reinterpret_cast<float4*>(dst + c0 + k) = v;
+      }
+    }
+    if (!merged && rank == 0) {
+      float* ml = a.ws_ml + ((static_cast<int64_t>(b) * a.nsplit + split) * kH + h) * 2;
+      ml[0] = have_o ? m_ref : -INFINITY;
+      ml[1] = have_o ? l : 0.f;
+    }
+  }
+
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc<kTmemCols>(tm);
+  }
+  tc::cluster_sync();  // the peer's stores into this CTA's shared memory are done
+}
+
+// Splits of one (request, head) combined in split order.
+__global__ __launch_bounds__(128) void mla_merge_kernel(const float* __restrict__ ws_o,
+                                                        const float* __restrict__ ws_ml, int nsplit,
+                                                        float* __restrict__ out) {
+  const int h = blockIdx.x, b = blockIdx.y, t = threadIdx.x;
+  const float* ml = ws_ml + (static_cast<int64_t>(b) * nsplit * kH + h) * 2;
+  float m = -INFINITY;
+  for (int s = 0; s < nsplit; s++) m = fmaxf(m, ml[static_cast<int64_t>(s) * kH * 2]);
+  float den = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s = 0; s < nsplit; s++) {
+    const float ms = ml[static_cast<int64_t>(s) * kH * 2], ls = ml[static_cast<int64_t>(s) * kH * 2 + 1];
+    const float w = ms == -INFINITY ? 0.f : exp2f(ms - m);
+    den += w * ls;
+    const float4 o = *reinterpret_cast<const float4*>(
+        ws_o + ((static_cast<int64_t>(b) * nsplit + s) * kH + h) * kDv + 4 * t);
+    acc.x += w * o.x;
+    acc.y += w * o.y;
+    acc.z += w * o.z;
+    acc.w += w * o.w;
+  }
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  *reinterpret_cast<float4*>(out + (static_cast<int64_t>(b) * kH + h) * kDv + 4 * t) =
+      make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+}
+
+int mla_splits(int B, int max_rows) {
+  const int clusters = sm_count() / 2;
+  int ns = B > 0 ? clusters / B : 1;
+  const int chunks = (max_rows + kNr - 1) / kNr;
+  if (ns > chunks) ns = chunks;
+  return ns < 1 ? 1 : ns;
+}
+
+}  // namespace
+}  // namespace skv
+
+using namespace skv;
+
+SKV_EXPORT size_t skv_mla_workspace_size(int B, int max_rows) {
+  if (B < 1 || max_rows < 1) return 0;
+  const int ns = mla_splits(B, max_rows);
+  if (ns == 1) return 16;
+  return static_cast<size_t>(B) * ns * kH * (kDv + 2) * sizeof(float);
+}
+
+SKV_EXPORT int skv_sparse_attend_mla(int B, int Hq, int d, int dv, const uint16_t* q, const uint8_t* kv_pool,
+                                     const float* row_scale, int64_t req_row_stride, int64_t n_pool_rows,
+                                     const int32_t* rows, int max_rows, const int32_t* count, float softmax_scale,
+                                     float* out, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                     void* stream) {
+  if (B < 0 || B > 65535 || max_rows < 1 || max_rows > 65536 || n_pool_rows < 1 || req_row_stride < 0)
+    return SKV_EINVAL;
+  if (Hq != kH || d != kD || dv != kDv) return SKV_EUNSUPPORTED;
+  if (B == 0) return SKV_OK;
+  if (!q || !kv_pool || !rows || !count || !out) return SKV_EINVAL;
+  if (!aligned16(q) || !aligned16(kv_pool) || !aligned16(out) || n_pool_rows > INT32_MAX) return SKV_EINVAL;
+  if (static_cast<int64_t>(B - 1) * req_row_stride > INT32_MAX) return SKV_EINVAL;
+  const int ns = mla_splits(B, max_rows);
+  if (ns > 1) {
+    if (!workspace || !aligned16(workspace) || workspace_bytes < skv_mla_workspace_size(B, max_rows))
+      return SKV_ENOMEM;
+  }
+  static bool configured = false;
+  if (!configured) {
+    if (cudaFuncSetAttribute(mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess) {
+      cudaGetLastError();
+      return SKV_EUNSUPPORTED;
+    }
+    configured = true;
+  }
+  float* ws = static_cast<float*>(workspace);
+  MlaArgs a{q, kv_pool, row_scale, req_row_stride, n_pool_rows, rows, max_rows, count,
+            softmax_scale * kLog2e, out, ws, ns > 1 ? ws + static_cast<size_t>(B) * ns * kH * kDv : nullptr, ns,
+            dev_status};
+  cudaStream_t st = as_stream(stream);
+  mla_kernel<<<dim3(2, ns, B), kThreads, kSmem, st>>>(a);
+  if (ns > 1) mla_merge_kernel<<<dim3(kH, B), 128, 0, st>>>(a.ws_o, a.ws_ml, ns, out);
+  return launch_status();
+}

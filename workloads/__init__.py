@@ -242,6 +242,23 @@ def pooled_inputs_cpu(B: int, T: int | list, Hq: int, Hkv: int, d: int, d_idx: i
             "q_idx": to_bf16_bits(q_idx), "idx_keys": to_bf16_bits(idx_keys), "lengths": lengths}
 
 
+def fp8_e4m3_codes(x: np.ndarray) -> np.ndarray:
+    """float32 values -> fp8 e4m3 bytes (round to nearest even, saturating at
+    +-448), through torch's float8_e4m3fn type on the CPU."""
+    import torch
+    t = torch.from_numpy(np.clip(np.ascontiguousarray(x, np.float32), -448.0, 448.0))
+    return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def mla_inputs_cpu(B: int, n_pool_rows: int, seed: int, Hq: int = 128, d: int = 576) -> dict:
+    """Small instances of the latent-row workload: rows ~ N(0,1) as fp8 e4m3,
+    absorbed queries ~ N(0,1) bf16."""
+    rng = np.random.default_rng(seed)
+    pool = fp8_e4m3_codes(rng.standard_normal((n_pool_rows, d)).astype(np.float32))
+    q = to_bf16_bits(rng.standard_normal((B, Hq, d)).astype(np.float32))
+    return {"pool": pool, "q": q}
+
+
 def pick_sequence(rng: np.random.Generator, lo: int, hi: int, k: int, n_steps: int, keep: float) -> list:
     """Drifting selections for resolver tests: each step keeps about `keep` of
     the previous step's tokens and draws the rest uniformly from [lo, hi).
