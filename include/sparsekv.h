@@ -199,7 +199,9 @@ int skv_pool_keys(const uint16_t *keys, int B, int64_t t_cap, int D, int ratio,
  *   raw_scores  int32 (INT4) or fp32 (other modes) [B][n_cap], or NULL
  * width: Hkv*r for the sketch modes, the indexer dim for pooled mode.
  * Constraints: INT4 width in {128, 256, 512}; F32 width a multiple of 4 and
- * <= 1024; POOLED width == 128; ratio == 1 for sketch modes, 4 for pooled;
+ * <= 1024; POOLED width == 128; ratio == 1 for sketch modes; for pooled
+ * mode 1 <= ratio <= 64 (4: keys pooled by skv_pool_keys; 1: raw indexer
+ * keys, one per token, as a latent-attention indexer scores them);
  * lengths[b] <= n_cap (sketch) or n_cap*ratio (pooled) (else SKV_DEV_RANGE
  * and the request is clamped).  Keys rows must be 16-byte aligned.
  */
@@ -408,7 +410,10 @@ int skv_sparse_attend_mla(int B, int Hq, int d, int dv, const uint16_t *q, const
  *              hot slots); only hot-slot rows of misses are written
  *   rows_out   int32 [B][max_rows]; n_miss int32 [B] (misses placed; -1 when
  *              the request has more picks than slots)
- *   step       the decode step, >= 0, increasing from call to call
+ *   step       int32 [2] (device): step[0] = this call's decode step (>= 0),
+ *              read by every CTA and advanced by one when the call completes
+ *              (so a captured graph replays with a fresh step); step[1] = 0, a
+ *              ticket the call returns to zero
  * Errors: SKV_EINVAL for bad sizes, null pointers, a req_row_stride below
  * S + W + Hs or unaligned pools; SKV_EUNSUPPORTED unless d is 256, 512, 768
  * or 1024, Hs <= 16384, max_rows <= 8192.  On the device: a token outside
@@ -417,7 +422,7 @@ int skv_sparse_attend_mla(int B, int Hq, int d, int dv, const uint16_t *q, const
  */
 int skv_resolve_rows_clock(int B, int64_t t_cap, const int32_t *lengths, int S, int W, int Hkv,
                            int d, int Hs, const int32_t *idx, int max_rows, const int32_t *count,
-                           int32_t step, int32_t *slot_token, uint8_t *ref, int32_t *use_step,
+                           int32_t *step, int32_t *slot_token, uint8_t *ref, int32_t *use_step,
                            int32_t *token_slot, int32_t *hand, const uint8_t *host_rows,
                            int8_t *k8, int8_t *v8, uint16_t *k_scale, uint16_t *v_scale,
                            int64_t req_row_stride, int32_t *rows_out, int32_t *n_miss,
@@ -443,7 +448,8 @@ int skv_resolve_rows_clock(int B, int64_t t_cap, const int32_t *lengths, int S, 
  *          [B][n_slots] (-1 none), token_slot int32 [B][t_cap] (-1 none)
  *   block_table int32 [B][n_pages]; host u8 [B][t_cap][row_bytes] (device
  *   alias); pool u8 [n_pool_rows][row_bytes]
- *   step   0 <= step < 2^31 - 1, increasing from call to call
+ *   step   int32 [2] (device), as for skv_resolve_rows_clock: step[0] is the
+ *          decode step, advanced by one when the call completes; step[1] = 0
  * Errors: SKV_EINVAL for bad sizes, null or unaligned pointers, row_bytes not
  * a multiple of 16, a hot buffer past n_pool_rows; SKV_EUNSUPPORTED for
  * n_slots > 8192 or max_rows > 8192.  On the device: bad tokens give row -1
@@ -452,7 +458,7 @@ int skv_resolve_rows_clock(int B, int64_t t_cap, const int32_t *lengths, int S, 
  */
 int skv_resolve_rows_lru(int B, int64_t t_cap, const int32_t *lengths, int page,
                          const int32_t *block_table, int64_t n_pages, int64_t hot_base,
-                         int64_t hot_stride, int n_slots, int64_t step, int64_t *stamp,
+                         int64_t hot_stride, int n_slots, int32_t *step, int64_t *stamp,
                          int32_t *slot_token, int32_t *token_slot, const uint8_t *host,
                          uint8_t *pool, int64_t row_bytes, int64_t n_pool_rows,
                          const int32_t *idx, int max_rows, const int32_t *count,

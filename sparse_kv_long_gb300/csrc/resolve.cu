@@ -30,6 +30,23 @@ constexpr int kMaxResolveRows = 8192;
 
 __host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~static_cast<size_t>(15); }
 
+// The decode step lives in device memory so that a captured graph replays
+// with a new step each time: every CTA reads step[0] at its start; the last
+// CTA to finish (ticket step[1]) advances step[0] and resets the ticket.
+__device__ __forceinline__ int32_t read_step(const int32_t* step) {
+  return *reinterpret_cast<const volatile int32_t*>(step);
+}
+
+__device__ __forceinline__ void advance_step(int32_t* step) {
+  __threadfence();
+  if (atomicAdd(reinterpret_cast<unsigned*>(step + 1), 1u) == gridDim.x - 1) {
+    __threadfence();
+    step[0] = step[0] + 1;
+    step[1] = 0;
+    __threadfence();
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Windowed CLOCK over the hot slots of one request.
 // ---------------------------------------------------------------------------
@@ -40,7 +57,7 @@ struct ClockArgs {
   const int32_t* idx;
   int max_rows;
   const int32_t* count;
-  int32_t step;
+  int32_t* step;  // [0] decode step, [1] ticket
   int32_t* slot_token;
   uint8_t* ref;
   int32_t* use_step;
@@ -136,6 +153,7 @@ __global__ __launch_bounds__(kClockThreads) void clock_kernel(ClockArgs a) {
   int32_t* tslot = a.token_slot + static_cast<int64_t>(b) * a.t_cap;
   const int64_t sbase = static_cast<int64_t>(b) * Hs;
   const int S = a.S, W = a.W;
+  const int32_t step = read_step(a.step);
   auto is_pick = [&](int64_t t) { return t >= S && t < T - W; };
 
   // The sweep needs at least as many slots as picks (else nothing changes).
@@ -180,7 +198,7 @@ __global__ __launch_bounds__(kClockThreads) void clock_kernel(ClockArgs a) {
         const int32_t s = tslot[t];
         if (s >= 0 && s < Hs) {
           s_ref[s] = 1;
-          s_use[s] = a.step;
+          s_use[s] = step;
           rows[i] = S + W + s;
         } else {
           if (s >= Hs) set_status(a.status, SKV_DEV_RANGE);
@@ -222,7 +240,7 @@ __global__ __launch_bounds__(kClockThreads) void clock_kernel(ClockArgs a) {
       const bool act = lane < w;
       int s = h + lane;
       if (s >= Hs) s -= Hs;
-      const bool used = act && s_use[s] == a.step;
+      const bool used = act && s_use[s] == step;
       const int32_t st = act ? s_tok[s] : 0;
       const bool r1 = act && s_ref[s] != 0;
       const bool cand = act && !used && (st < 0 || !r1);
@@ -243,7 +261,7 @@ __global__ __launch_bounds__(kClockThreads) void clock_kernel(ClockArgs a) {
         s_tok[s] = tok;
         tslot[tok] = s;
         s_ref[s] = 1;
-        s_use[s] = a.step;
+        s_use[s] = step;
         m_slot[jj] = s;
         rows[m_pos[jj]] = S + W + s;
       }
@@ -312,6 +330,8 @@ __global__ __launch_bounds__(kClockThreads) void clock_kernel(ClockArgs a) {
     a.ref[sbase + s] = s_ref[s];
   }
   if (tid == 0) a.n_miss[b] = fits ? nm : -1;
+  __syncthreads();
+  if (tid == 0) advance_step(a.step);
 }
 
 // ---------------------------------------------------------------------------
@@ -325,7 +345,7 @@ struct LruArgs {
   int64_t n_pages;
   int64_t hot_base, hot_stride;
   int n_slots;
-  int64_t step;
+  int32_t* step;  // [0] decode step, [1] ticket
   int64_t* stamp;
   int32_t* slot_token;
   int32_t* token_slot;
@@ -377,6 +397,7 @@ __global__ __launch_bounds__(kResThreads) void lru_kernel(LruArgs a, int P) {
   const int32_t* bt = a.block_table + static_cast<int64_t>(b) * a.n_pages;
   const int64_t sbase = static_cast<int64_t>(b) * ns;
   const int64_t hot = a.hot_base + static_cast<int64_t>(b) * a.hot_stride;
+  const int64_t step = read_step(a.step);
 
   for (int s = tid; s < ns; s += kResThreads) s_stamp[s] = a.stamp[sbase + s];
   __syncthreads();
@@ -401,7 +422,7 @@ __global__ __launch_bounds__(kResThreads) void lru_kernel(LruArgs a, int P) {
       } else {
         const int32_t s = tslot[t];
         if (s >= 0 && s < ns) {
-          s_stamp[s] = a.step;
+          s_stamp[s] = step;
           rows[i] = static_cast<int32_t>(hot + s);
         } else {
           if (s >= ns) set_status(a.status, SKV_DEV_RANGE);
@@ -429,7 +450,7 @@ __global__ __launch_bounds__(kResThreads) void lru_kernel(LruArgs a, int P) {
     bool c = false;
     if (s < P) {
       uint64_t k = ~0ull;
-      if (s < ns && s_stamp[s] != a.step) {
+      if (s < ns && s_stamp[s] != step) {
         k = (static_cast<uint64_t>(s_stamp[s] + 1) << 32) | static_cast<uint32_t>(s);
         c = true;
       }
@@ -463,7 +484,7 @@ __global__ __launch_bounds__(kResThreads) void lru_kernel(LruArgs a, int P) {
       if (old >= 0 && old < a.t_cap) tslot[old] = -1;
       a.slot_token[sbase + s] = tok;
       tslot[tok] = s;
-      s_stamp[s] = a.step;
+      s_stamp[s] = step;
       rows[m_pos[j]] = static_cast<int32_t>(hot + s);
     }
     // Copy the miss rows from the host alias, kFetchRows rows per warp at once.
@@ -494,6 +515,8 @@ __global__ __launch_bounds__(kResThreads) void lru_kernel(LruArgs a, int P) {
   __syncthreads();
   for (int s = tid; s < ns; s += kResThreads) a.stamp[sbase + s] = s_stamp[s];
   if (tid == 0) a.n_miss[b] = ok ? nm : -1;
+  __syncthreads();
+  if (tid == 0) advance_step(a.step);
 }
 
 // ---------------------------------------------------------------------------
@@ -575,7 +598,7 @@ using namespace skv;
 
 SKV_EXPORT int skv_resolve_rows_clock(int B, int64_t t_cap, const int32_t* lengths, int S, int W, int Hkv, int d,
                                       int Hs, const int32_t* idx, int max_rows, const int32_t* count,
-                                      int32_t step, int32_t* slot_token, uint8_t* ref, int32_t* use_step,
+                                      int32_t* step, int32_t* slot_token, uint8_t* ref, int32_t* use_step,
                                       int32_t* token_slot, int32_t* hand, const uint8_t* host_rows, int8_t* k8,
                                       int8_t* v8, uint16_t* k_scale, uint16_t* v_scale, int64_t req_row_stride,
                                       int32_t* rows_out, int32_t* n_miss, int32_t* dev_status, void* stream) {
@@ -583,7 +606,7 @@ SKV_EXPORT int skv_resolve_rows_clock(int B, int64_t t_cap, const int32_t* lengt
   if (B == 0) return SKV_OK;
   if (d < 256 || d % 256 || d > 1024) return SKV_EUNSUPPORTED;
   if (Hs > kMaxClockSlots || max_rows > kMaxResolveRows || t_cap > INT32_MAX) return SKV_EUNSUPPORTED;
-  if (step < 0 || req_row_stride < static_cast<int64_t>(S) + W + Hs) return SKV_EINVAL;
+  if (!step || req_row_stride < static_cast<int64_t>(S) + W + Hs) return SKV_EINVAL;
   if (!lengths || !idx || !count || !slot_token || !ref || !use_step || !token_slot || !hand || !host_rows ||
       !k8 || !v8 || !k_scale || !v_scale || !rows_out || !n_miss)
     return SKV_EINVAL;
@@ -607,7 +630,7 @@ SKV_EXPORT int skv_resolve_rows_clock(int B, int64_t t_cap, const int32_t* lengt
 
 SKV_EXPORT int skv_resolve_rows_lru(int B, int64_t t_cap, const int32_t* lengths, int page,
                                     const int32_t* block_table, int64_t n_pages, int64_t hot_base,
-                                    int64_t hot_stride, int n_slots, int64_t step, int64_t* stamp,
+                                    int64_t hot_stride, int n_slots, int32_t* step, int64_t* stamp,
                                     int32_t* slot_token, int32_t* token_slot, const uint8_t* host, uint8_t* pool,
                                     int64_t row_bytes, int64_t n_pool_rows, const int32_t* idx, int max_rows,
                                     const int32_t* count, int32_t* rows_out, int32_t* n_miss, int32_t* dev_status,
@@ -617,7 +640,7 @@ SKV_EXPORT int skv_resolve_rows_lru(int B, int64_t t_cap, const int32_t* lengths
     return SKV_EINVAL;
   if (B == 0) return SKV_OK;
   if (n_slots > kMaxLruSlots || max_rows > kMaxResolveRows || t_cap > INT32_MAX) return SKV_EUNSUPPORTED;
-  if (step < 0 || step >= INT32_MAX) return SKV_EINVAL;
+  if (!step) return SKV_EINVAL;
   if (hot_base + static_cast<int64_t>(B - 1) * hot_stride + n_slots > n_pool_rows || n_pool_rows > INT32_MAX)
     return SKV_EINVAL;
   if (!lengths || !block_table || !stamp || !slot_token || !token_slot || !host || !pool || !idx || !count ||

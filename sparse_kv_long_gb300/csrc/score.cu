@@ -151,7 +151,7 @@ SKV_EXPORT int skv_index_score(int mode, int B, int width, const void* query, co
         static_cast<const float*>(query), static_cast<const float*>(keys), n_cap, width, lengths, S, W, grid.x,
         order_keys, static_cast<float*>(raw_scores), dev_status);
   } else if (mode == SKV_SCORE_POOLED_BF16) {
-    if (ratio != 4 || width != 128 || S != 0 || W != 0) return SKV_EINVAL;
+    if (ratio < 1 || ratio > 64 || width != 128 || S != 0 || W != 0) return SKV_EINVAL;
     dim3 grid(chunks_for(score_pooled_kernel, B), B);
     score_pooled_kernel<<<grid, kScanThreads, 0, st>>>(
         static_cast<const uint16_t*>(query), static_cast<const uint16_t*>(keys), n_cap, lengths, ratio, grid.x,

@@ -575,7 +575,7 @@ SKV_EXPORT int skv_score_select(int mode, int B, int width, const void* query, c
   if (!aligned16(keys) || !aligned16(query) || !aligned16(workspace)) return SKV_EINVAL;
   if (workspace_bytes < ws_bytes(B)) return SKV_ENOMEM;
   const bool pooled = mode == SKV_SCORE_POOLED_BF16;
-  if (pooled ? (ratio != 4 || width != 128 || S != 0 || W != 0) : ratio != 1) return SKV_EINVAL;
+  if (pooled ? (ratio > 64 || width != 128 || S != 0 || W != 0) : ratio != 1) return SKV_EINVAL;
   const int64_t need_rows = pooled ? static_cast<int64_t>(ratio) * k + ratio - 1 : static_cast<int64_t>(S) + k + W;
   if (max_rows < need_rows) return SKV_EINVAL;
   Args a{mode, width, query, keys, n_cap, lengths, ratio, k, S, W, idx, max_rows, count, order_keys, dev_status, B};

@@ -489,3 +489,29 @@ def test_decode_prepare_matches_oracle(skv, orc, B, Hq, Hkv):
     assert np.all(s_host[untouched] == 0x77)
     assert np.allclose(T.host(sig), ref_q["sigma"], rtol=1e-5)
     T.assert_codes_match_except_ties(T.host(q8), ref_q["q8"], ref_q["x"])
+
+
+def test_score_select_pooled_ratio1_raw_indexer_keys(skv, orc):
+    """Raw 128-dim bf16 indexer keys, one per token (ratio 1, no sinks/tail):
+    the fused select against the oracle within 1e-3 of the k-th score, and
+    identical to the two-call path."""
+    rng = np.random.default_rng(777)
+    B, n_cap, k = 3, 50000, 2048
+    qi = wl.to_bf16_bits(rng.standard_normal((B, 128)).astype(np.float32))
+    keys = wl.to_bf16_bits(rng.standard_normal((B, n_cap, 128)).astype(np.float32))
+    L = np.array([50000, 20001, 2048], np.int32)
+    gi, gc, _ = run_fused(skv, skv.POOLED_BF16, T.bf16_dev(qi), T.bf16_dev(keys), L, k, ratio=1)
+    okeys = torch.zeros((B, n_cap), dtype=torch.int32, device="cuda")
+    skv.index_score(skv.POOLED_BF16, T.bf16_dev(qi), T.bf16_dev(keys), T.dev(L), okeys, ratio=1)
+    si, sc = run_topk(skv, T.host(okeys).view(np.uint32), L, k, ratio=1)
+    assert np.array_equal(gc, sc)
+    for b in range(B):
+        assert np.array_equal(gi[b, :gc[b]], si[b, :sc[b]])
+    ref = orc.index_score(orc.POOLED_BF16, qi, keys, L, ratio=1)
+    ri, rc = orc.topk_select(ref["okey"], L, k, ratio=1)
+    assert np.array_equal(gc, rc)
+    np.testing.assert_array_equal(gi[2, :gc[2]], np.arange(2048))        # T <= k: dense
+    for b in range(2):
+        kth = np.sort(ref["fscore"][b, :L[b]])[::-1][k - 1]
+        for t in set(gi[b, :gc[b]].tolist()) ^ set(ri[b, :rc[b]].tolist()):
+            assert abs(ref["fscore"][b, t] - kth) <= 1e-3 * abs(kth)

@@ -212,6 +212,7 @@ def test_host_clock_workload_small_end_to_end(skv, orc):
         g_use = torch.full((B, Hs), -1, dtype=torch.int32, device="cuda")
         g_tslot = torch.full((B, Tcap), -1, dtype=torch.int32, device="cuda")
         g_hand = torch.zeros((B,), dtype=torch.int32, device="cuda")
+        g_step = torch.zeros((2,), dtype=torch.int32, device="cuda")
         states = [orc.ClockState(Hs, Tcap) for _ in range(B)]
         Ld, skd = T.dev(L), T.dev(sk)
         ws = torch.zeros((skv.score_select_workspace_size(B),), dtype=torch.uint8, device="cuda")
@@ -234,7 +235,7 @@ def test_host_clock_workload_small_end_to_end(skv, orc):
             skv.score_select(skv.SKETCH_INT4, T.dev(qq["q8"]), skd, Ld, k, idx, cnt, ws, S=S, W=W, status=st)
             rows = torch.zeros((B, max_rows), dtype=torch.int32, device="cuda")
             nmiss = torch.zeros((B,), dtype=torch.int32, device="cuda")
-            skv.resolve_rows_clock(Ld, idx, cnt, step, S, W, Hs, g_tok, g_ref, g_use, g_tslot, g_hand, alias,
+            skv.resolve_rows_clock(Ld, idx, cnt, g_step, S, W, Hs, g_tok, g_ref, g_use, g_tslot, g_hand, alias,
                                    g["k8"], g["v8"], g["ks"], g["vs"], R, rows, nmiss, status=st)
             out = torch.zeros((B, Hq, d), dtype=torch.float32, device="cuda")
             skv.sparse_attend_decode(skv.KV_INT8, T.bf16_dev(qb), g["k8"].view(B * R, Hkv, d),

@@ -111,6 +111,7 @@ def test_clock_resolve_matches_oracle(skv, orc, Hs, k, keep, where):
     g_use = torch.full((B, Hs), -1, dtype=torch.int32, device="cuda")
     g_tslot = torch.full((B, t_cap), -1, dtype=torch.int32, device="cuda")
     g_hand = torch.zeros((B,), dtype=torch.int32, device="cuda")
+    g_step = torch.zeros((2,), dtype=torch.int32, device="cuda")   # [step, ticket], advanced by each call
     g_len = T.dev(lengths)
     hb = None
     if where == "host":
@@ -129,10 +130,11 @@ def test_clock_resolve_matches_oracle(skv, orc, Hs, k, keep, where):
             rows = torch.full((B, max_rows), -9, dtype=torch.int32, device="cuda")
             nmiss = torch.zeros((B,), dtype=torch.int32, device="cuda")
             st = status_word()
-            skv.resolve_rows_clock(g_len, T.dev(idx), T.dev(count), step, S, W, Hs, g_tok, g_ref, g_use, g_tslot,
+            skv.resolve_rows_clock(g_len, T.dev(idx), T.dev(count), g_step, S, W, Hs, g_tok, g_ref, g_use, g_tslot,
                                    g_hand, host_arg, g_k8, g_v8, g_ks, g_vs, R, rows, nmiss, status=st)
             torch.cuda.synchronize()
             assert int(st.item()) == 0
+            assert T.host(g_step).tolist() == [step + 1, 0]
             got_rows = T.host(rows)
             for b in range(B):
                 n = int(count[b])
@@ -170,8 +172,8 @@ def test_clock_more_picks_than_slots_is_flagged(skv):
     ks = torch.zeros((R, Hkv), dtype=torch.float16, device="cuda")
     host = torch.zeros((t_cap, Hkv, 2, 136), dtype=torch.uint8, device="cuda")
     st = status_word()
-    skv.resolve_rows_clock(T.dev(np.array([200], np.int32)), T.dev(idx), T.dev(np.array([40], np.int32)), 0, S, W,
-                           Hs, tok, ref, use, tslot, hand, host, k8, k8.clone(), ks, ks.clone(), R, rows, nmiss,
+    skv.resolve_rows_clock(T.dev(np.array([200], np.int32)), T.dev(idx), T.dev(np.array([40], np.int32)),
+                           torch.zeros(2, dtype=torch.int32, device="cuda"), S, W, Hs, tok, ref, use, tslot, hand, host, k8, k8.clone(), ks, ks.clone(), R, rows, nmiss,
                            status=st)
     torch.cuda.synchronize()
     assert int(st.item()) & 8                              # SKV_DEV_COUNT
@@ -214,6 +216,7 @@ def test_lru_resolve_matches_oracle(skv, orc, n_slots, k, keep, where):
     g_tok = torch.full((B, n_slots), -1, dtype=torch.int32, device="cuda")
     g_tslot = torch.full((B, t_cap), -1, dtype=torch.int32, device="cuda")
     g_bt, g_len = T.dev(bt), T.dev(lengths)
+    g_step = torch.zeros((2,), dtype=torch.int32, device="cuda")
     hb = None
     if where == "host":
         hb = HostBuffer(skv, host)
@@ -229,10 +232,11 @@ def test_lru_resolve_matches_oracle(skv, orc, n_slots, k, keep, where):
             rows = torch.full((B, k + 2), -9, dtype=torch.int32, device="cuda")
             nmiss = torch.zeros((B,), dtype=torch.int32, device="cuda")
             st = status_word()
-            skv.resolve_rows_lru(g_len, T.dev(idx), T.dev(count), step, page, g_bt, hot_base, hot_stride, g_stamp,
+            skv.resolve_rows_lru(g_len, T.dev(idx), T.dev(count), g_step, page, g_bt, hot_base, hot_stride, g_stamp,
                                  g_tok, g_tslot, host_arg, g_pool, rows, nmiss, status=st)
             torch.cuda.synchronize()
             assert int(st.item()) == 0
+            assert T.host(g_step).tolist() == [step + 1, 0]
             got_rows = T.host(rows)
             for b in range(B):
                 ref_rows, m = states[b].resolve(idx[b, :k], page, bt[b], hot_base + b * hot_stride, step, host[b],
@@ -260,7 +264,8 @@ def test_lru_too_few_slots_is_flagged(skv):
     rows = torch.full((B, 10), -9, dtype=torch.int32, device="cuda")
     nmiss = torch.zeros((B,), dtype=torch.int32, device="cuda")
     st = status_word()
-    skv.resolve_rows_lru(T.dev(np.array([256], np.int32)), T.dev(idx), T.dev(np.array([10], np.int32)), 0, page,
+    skv.resolve_rows_lru(T.dev(np.array([256], np.int32)), T.dev(idx), T.dev(np.array([10], np.int32)),
+                         torch.zeros(2, dtype=torch.int32, device="cuda"), page,
                          T.dev(bt), 0, 0, stamp, tok, tslot, host, pool, rows, nmiss, status=st)
     torch.cuda.synchronize()
     assert int(st.item()) & 8
