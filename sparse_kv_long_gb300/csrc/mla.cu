@@ -24,6 +24,8 @@
 // rows, warps 4-7 own one head each (tensor-memory lane = head) for the
 // online softmax and the epilogue.  Rows are split across clusters; the splits
 // are merged in a fixed order, so the result is deterministic.
+#include <cstddef>
+
 #include "tc.cuh"
 
 namespace skv {
@@ -50,11 +52,18 @@ constexpr float kRescaleLog2 = 8.f;             // rescale O only when the max g
 struct Aux {
   uint64_t kv_full[2], kv_empty[2], s_full[2], s_empty[2];
   uint64_t p_full, pv_done, x_full, x_empty, mma_idle;
-  int32_t row[2][kNr];
-  float rs[2][kNr];
+  alignas(16) int32_t prow[2][kNr];  // pool rows of the chunk in buffer s (-1: none), staged by the gather warps
+  alignas(16) float kl[2][kNr];      // logit factor of each row: row scale x softmax scale x log2(e); 0 if no row
+  alignas(16) float madd[2][kNr];    // 0, or -inf for a missing row
+  alignas(16) float vsc[2][kNr];     // value factor: the row scale; 0 if no row
   uint32_t tmem_base;
   int abort;
 };
+
+// The softmax reads kl / madd / vsc as float4.
+static_assert(offsetof(Aux, kl) % 16 == 0 && offsetof(Aux, madd) % 16 == 0 && offsetof(Aux, vsc) % 16 == 0,
+              "per-row factor arrays must be 16-byte aligned");
+static_assert((kQBytes + 2 * kKVBytes + kPBytes + kXBytes) % 16 == 0, "Aux must start 16-byte aligned");
 
 constexpr int kSmem = 1024 + kQBytes + 2 * kKVBytes + kPBytes + kXBytes + static_cast<int>(sizeof(Aux));
 
@@ -129,8 +138,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_ker
     }
     tc::bar_init(&ax->p_full, kH);
     tc::bar_init(&ax->pv_done, 1);
-    tc::bar_init(&ax->x_full, kH);
-    tc::bar_init(&ax->x_empty, kH);
+    tc::bar_init(&ax->x_full, 1);   // one local arm per chunk + kXBytes of st.async data from the peer
+    tc::bar_init(&ax->x_empty, kH / 32);  // one remote arrive per peer softmax warp and chunk
     tc::bar_init(&ax->mma_idle, 1);
     ax->abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -140,12 +149,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_ker
   // and 64-dim atom).  CTA 0 holds dims [0, 320), CTA 1 dims [320, 576).
   const int qdim0 = rank == 0 ? 0 : kSlice;
   const int qatoms = rank == 0 ? kAtoms : kAtoms - 1;
-  for (int u = tid; u < kH * qatoms * 8; u += kThreads) {
-    const int h = u / (qatoms * 8), cc = u % (qatoms * 8);
-    const uint4 v = *reinterpret_cast<const uint4*>(a.q + (static_cast<int64_t>(b) * kH + h) * kD + qdim0 + 8 * cc);
-    const uint4 f = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z),
-                               bf16x2_to_f16x2(v.w));
-    *reinterpret_cast<uint4*>(sQ + (cc >> 3) * (kH * 128) + h * 128 + (((cc & 7) ^ (h & 7)) << 4)) = f;
+  {
+    constexpr int kQBatch = 10;  // loads in flight per thread
+    const int nq = kH * qatoms * 8;
+    for (int u0 = tid; u0 < nq; u0 += kThreads * kQBatch) {
+      uint4 v[kQBatch];
+#pragma unroll
+      for (int m = 0; m < kQBatch; m++) {
+        const int u = u0 + m * kThreads;
+        if (u < nq) {
+          const int h = u / (qatoms * 8), cc = u % (qatoms * 8);
+          v[m] = ld_nc16(a.q + (static_cast<int64_t>(b) * kH + h) * kD + qdim0 + 8 * cc);
+        }
+      }
+#pragma unroll
+      for (int m = 0; m < kQBatch; m++) {
+        const int u = u0 + m * kThreads;
+        if (u < nq) {
+          const int h = u / (qatoms * 8), cc = u % (qatoms * 8);
+          const uint4 f = make_uint4(bf16x2_to_f16x2(v[m].x), bf16x2_to_f16x2(v[m].y), bf16x2_to_f16x2(v[m].z),
+                                     bf16x2_to_f16x2(v[m].w));
+          *reinterpret_cast<uint4*>(sQ + (cc >> 3) * (kH * 128) + h * 128 + (((cc & 7) ^ (h & 7)) << 4)) = f;
+        }
+      }
+    }
   }
   tc::fence_async_smem();
   if (warp == 0) tc::tmem_alloc<kTmemCols>(&ax->tmem_base);
@@ -207,28 +234,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_ker
     }
   } else if (warp < 4) {
     // ---------------- row gather: fp8 -> fp16 swizzled tiles ----------------
+    // Row ids of chunk i+1 are fetched while chunk i's rows are in flight.
     const int pt = tid - 32;
+    auto row_of = [&](int i) -> int32_t {
+      const int gi = r0 + i * kNr + pt;
+      if (gi >= r1) return -1;
+      const int64_t p = static_cast<int64_t>(b) * a.req_row_stride + a.rows[static_cast<int64_t>(b) * a.max_rows + gi];
+      if (p < 0 || p >= a.n_pool_rows) {
+        if (rank == 0) set_status(a.status, SKV_DEV_RANGE);
+        return -1;
+      }
+      return static_cast<int32_t>(p);
+    };
+    if (pt < kNr && nchunks > 0) ax->prow[0][pt] = row_of(0);
+    named_sync(1, kProducers);
     for (int i = 0; i < nchunks; i++) {
       const int s = i & 1;
       const bool free_buf = i < 2 || tc::bar_wait(&ax->kv_empty[s], ((i >> 1) - 1) & 1, abort);
       if (!named_sync_and(1, kProducers, free_buf)) break;  // the same decision in every producer
-      if (pt < kNr) {
-        const int gi = r0 + i * kNr + pt;
-        int64_t p = -1;
-        float rsc = 0.f;
-        if (gi < r1) {
-          p = static_cast<int64_t>(b) * a.req_row_stride + a.rows[static_cast<int64_t>(b) * a.max_rows + gi];
-          if (p < 0 || p >= a.n_pool_rows) {
-            if (rank == 0) set_status(a.status, SKV_DEV_RANGE);
-            p = -1;
-          } else {
-            rsc = a.row_scale ? a.row_scale[p] : 1.f;
-          }
-        }
-        ax->row[s][pt] = static_cast<int32_t>(p);
-        ax->rs[s][pt] = rsc;
-      }
-      named_sync(1, kProducers);
       uint4 v[kPerProducer];
 #pragma unroll
       for (int m = 0; m < kPerProducer; m++) {
@@ -236,9 +259,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_ker
         v[m] = make_uint4(0u, 0u, 0u, 0u);
         if (u < kNr * kPieces) {
           const int jr = u / kPieces, q = u % kPieces;
-          const int32_t p = ax->row[s][jr];
+          const int32_t p = ax->prow[s][jr];
           if (p >= 0) v[m] = ld_nc16(a.pool + static_cast<int64_t>(p) * kD + rank * 256 + 16 * q);
         }
+      }
+      int32_t next = -1;
+      float rsc = 0.f;
+      bool have = false;
+      if (pt < kNr) {
+        const int32_t p = ax->prow[s][pt];
+        have = p >= 0;
+        if (have) rsc = a.row_scale ? a.row_scale[p] : 1.f;
+        if (i + 1 < nchunks) next = row_of(i + 1);
       }
       unsigned char* tile = sKV + s * kKVBytes;
 #pragma unroll
@@ -254,9 +286,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_ker
           *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ (jr & 7)) << 4)) = make_uint4(e2.x, e2.y, e3.x, e3.y);
         }
       }
+      if (pt < kNr) {
+        ax->kl[s][pt] = have ? rsc * a.scale_log2 : 0.f;
+        ax->madd[s][pt] = have ? 0.f : -INFINITY;
+        ax->vsc[s][pt] = have ? rsc : 0.f;
+        ax->prow[s ^ 1][pt] = next;  // producers only; chunk i-1's ids are no longer read
+      }
       tc::fence_async_smem();
       tc::bar_arrive(&ax->kv_full[s]);
-      named_sync(1, kProducers);  // row ids of buffer s are read above before the next refill
+      named_sync(1, kProducers);
     }
   } else {
     // ---------------- softmax + epilogue: thread = head ----------------
@@ -276,7 +314,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_ker
       tc::tmem_wait_ld();
       tc::tc_fence_before();
       tc::bar_arrive(&ax->s_empty[s]);
-      // partial logits to the peer, then the peer's from this CTA's buffer
+      // partial logits to the peer (asynchronous stores that count down the
+      // peer's receive barrier), then the peer's from this CTA's buffer
+      if (h == 0) tc::bar_arrive_expect_tx(&ax->x_full, kXBytes);
       if (i >= 1) {
         ok = __all_sync(0xffffffffu, tc::bar_wait(&ax->x_empty, (i - 1) & 1, abort, true));
         if (!ok) break;
@@ -284,12 +324,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_ker
 #pragma unroll
       for (int c = 0; c < 16; c++) {
         const uint32_t* r = c < 8 ? &ra[4 * c] : &rb[4 * (c - 8)];
-        tc::st_remote16(xrow + 4 * (c ^ (h & 7)), peer,
-                        make_float4(__uint_as_float(r[0]), __uint_as_float(r[1]), __uint_as_float(r[2]),
-                                    __uint_as_float(r[3])));
+        tc::st_async_remote16(xrow + 4 * (c ^ (h & 7)), &ax->x_full, peer,
+                              make_float4(__uint_as_float(r[0]), __uint_as_float(r[1]), __uint_as_float(r[2]),
+                                          __uint_as_float(r[3])));
       }
-      tc::bar_arrive_remote(&ax->x_full, peer);
-      ok = __all_sync(0xffffffffu, tc::bar_wait(&ax->x_full, i & 1, abort, true));
+      ok = __all_sync(0xffffffffu, tc::bar_wait(&ax->x_full, i & 1, abort));
       if (!ok) break;
       float x[64];
 #pragma unroll
@@ -301,15 +340,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_ker
         x[4 * c + 2] = __uint_as_float(r[2]) + o.z;
         x[4 * c + 3] = __uint_as_float(r[3]) + o.w;
       }
-      tc::bar_arrive_remote(&ax->x_empty, peer);
-      float mc = -INFINITY;
+      __syncwarp();  // this warp has read its part of the peer's logits
+      if (lane == 0) tc::bar_arrive_remote_relaxed(&ax->x_empty, peer);
+      // logits in log2 units; eight independent max chains
+      float mp[8];
 #pragma unroll
-      for (int j = 0; j < 64; j++) {
-        const bool valid = ax->row[s][j] >= 0;
-        const float v = valid ? x[j] * ax->rs[s][j] * a.scale_log2 : -INFINITY;
-        x[j] = v;
-        mc = fmaxf(mc, v);
+      for (int k = 0; k < 8; k++) mp[k] = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 16; c++) {
+        const float4 f = *reinterpret_cast<const float4*>(&ax->kl[s][4 * c]);
+        const float4 m = *reinterpret_cast<const float4*>(&ax->madd[s][4 * c]);
+        x[4 * c] = fmaf(x[4 * c], f.x, m.x);
+        x[4 * c + 1] = fmaf(x[4 * c + 1], f.y, m.y);
+        x[4 * c + 2] = fmaf(x[4 * c + 2], f.z, m.z);
+        x[4 * c + 3] = fmaf(x[4 * c + 3], f.w, m.w);
+        mp[(2 * c) & 7] = fmaxf(mp[(2 * c) & 7], fmaxf(x[4 * c], x[4 * c + 1]));
+        mp[(2 * c + 1) & 7] = fmaxf(mp[(2 * c + 1) & 7], fmaxf(x[4 * c + 2], x[4 * c + 3]));
       }
+      const float mc = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                             fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
       bool rescale = false;
       float alpha = 1.f;
       if (mc > m_ref + kRescaleLog2) {
@@ -334,17 +383,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_ker
         tc::tmem_wait_st();
         l *= alpha;
       }
-      float lsum = 0.f;
+      const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t pk[32];
 #pragma unroll
-      for (int j = 0; j < 64; j += 2) {
-        const float p0 = x[j] == -INFINITY ? 0.f : exp2f(x[j] - m_ref);
-        const float p1 = x[j + 1] == -INFINITY ? 0.f : exp2f(x[j + 1] - m_ref);
-        lsum += p0;
-        lsum += p1;
-        pk[j >> 1] = pack_f16x2(p0 * ax->rs[s][j], p1 * ax->rs[s][j + 1]);
+      for (int c = 0; c < 16; c++) {
+        const float4 vf = *reinterpret_cast<const float4*>(&ax->vsc[s][4 * c]);
+        const float p0 = tc::ex2_approx(x[4 * c] - m_use), p1 = tc::ex2_approx(x[4 * c + 1] - m_use);
+        const float p2 = tc::ex2_approx(x[4 * c + 2] - m_use), p3 = tc::ex2_approx(x[4 * c + 3] - m_use);
+        ls[c & 3] += (p0 + p1) + (p2 + p3);
+        pk[2 * c] = pack_f16x2(p0 * vf.x, p1 * vf.y);
+        pk[2 * c + 1] = pack_f16x2(p2 * vf.z, p3 * vf.w);
       }
-      l += lsum;
+      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
 #pragma unroll
       for (int c = 0; c < 8; c++)
         *reinterpret_cast<uint4*>(sP + h * 128 + ((c ^ (h & 7)) << 4)) =

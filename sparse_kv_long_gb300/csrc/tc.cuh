@@ -38,6 +38,16 @@ __device__ __forceinline__ void bar_arrive_remote(uint64_t* bar, uint32_t rank) 
       : "memory");
 }
 
+// Relaxed variant: only signals, orders nothing (for "buffer consumed" notes
+// whose reads have already completed).
+__device__ __forceinline__ void bar_arrive_remote_relaxed(uint64_t* bar, uint32_t rank) {
+  asm volatile(
+      "{\n.reg .b32 ra;\nmapa.shared::cluster.u32 ra, %0, %1;\n"
+      "mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [ra];\n}\n" ::"r"(smem_addr(bar)),
+      "r"(rank)
+      : "memory");
+}
+
 __device__ __forceinline__ bool bar_test(uint64_t* bar, uint32_t parity, bool cluster_scope) {
   uint32_t ok;
   if (cluster_scope)
@@ -106,6 +116,27 @@ __device__ __forceinline__ void st_remote16(const void* local, uint32_t rank, fl
       "st.shared::cluster.v4.f32 [ra], {%2, %3, %4, %5};\n}\n" ::"r"(smem_addr(local)),
       "r"(rank), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
       : "memory");
+}
+
+// Asynchronous 16-byte store into CTA `rank`'s shared memory (same offset as
+// `local`); on arrival it completes 16 bytes of transaction count on that
+// CTA's barrier at the offset of `local_bar`.  No fence is needed: the data is
+// visible to threads that observe the barrier's phase completion.
+__device__ __forceinline__ void st_async_remote16(const void* local, const uint64_t* local_bar, uint32_t rank,
+                                                  float4 v) {
+  asm volatile(
+      "{\n.reg .b32 ra, rb;\nmapa.shared::cluster.u32 ra, %0, %2;\nmapa.shared::cluster.u32 rb, %1, %2;\n"
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [ra], {%3, %4, %5, %6}, [rb];\n}\n" ::"r"(
+          smem_addr(local)),
+      "r"(smem_addr(local_bar)), "r"(rank), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+      : "memory");
+}
+
+// Arrive on a local barrier and add `bytes` to the transaction count its
+// current phase waits for.
+__device__ __forceinline__ void bar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
 }
 
 // ---- tensor memory ------------------------------------------------------------
@@ -189,6 +220,13 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    smem_addr(bar))
                : "memory");
+}
+
+// 2^x on the special-function unit (approximate, flushes subnormals; 2^-inf = 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // Two fp8 e4m3 values (a 16-bit pair) -> two fp16 values, exact.
