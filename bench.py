@@ -471,7 +471,7 @@ class MlaLruWorkloadGPU:
     host-only, hot buffer of 4096 rows per request."""
 
     B, T, H, D, DV, K, PAGE, SLOTS, DI = 32, 142_000, 128, 576, 512, 2048, 64, 4096, 128
-    KERNELS_PER_LAYER = 4  # score+select, LRU resolve, MLA attention, split merge
+    KERNELS_PER_LAYER = 5  # score+select, LRU state pass + row fetch, MLA attention + split merge
 
     def __init__(self, torch, skv, wl, dev, layers, n_steps, eta=0.25, context=None):
         self.torch, self.skv, self.L = torch, skv, layers
@@ -517,6 +517,7 @@ class MlaLruWorkloadGPU:
         self.nmiss = torch.zeros((layers, B), dtype=torch.int32, device=dev)
         self.tws = torch.zeros((skv.score_select_workspace_size(B),), dtype=torch.uint8, device=dev)
         self.mws = torch.zeros((max(16, skv.mla_workspace_size(B, self.K)),), dtype=torch.uint8, device=dev)
+        self.rws = torch.zeros((skv.resolve_workspace_size(B, self.K),), dtype=torch.uint8, device=dev)
         self.out = torch.zeros((B, self.H, self.DV), dtype=torch.float32, device=dev)
         self.status = torch.zeros((1,), dtype=torch.int32, device=dev)
         torch.cuda.synchronize()
@@ -532,7 +533,8 @@ class MlaLruWorkloadGPU:
         ev("res0")
         skv.resolve_rows_lru(self.lengths, self.idx, self.cnt, self.step_ctr[l], self.PAGE, self.bt, self.hot_base,
                              self.hot_stride, self.stamp[l], self.slot_tok[l], self.tok_slot[l],
-                             self.hosts[l].alias, self.pool[l], self.rows, self.nmiss[l], status=st)
+                             self.hosts[l].alias, self.pool[l], self.rows, self.nmiss[l], workspace=self.rws,
+                             status=st)
         ev("att0")
         skv.sparse_attend_mla(self.q[l], self.pool[l], self.rows, self.cnt, 1 / math.sqrt(self.D), self.out,
                               self.mws, status=st)
@@ -566,7 +568,7 @@ class HostClockWorkloadGPU:
     sketch, 64 sinks, the 1024-token tail and a 2.5 % hot buffer (6,250 slots)
     under windowed CLOCK; a drifting query gives the hot-buffer misses."""
 
-    KERNELS_PER_LAYER = 5  # prepare, int4 host append, score+select, CLOCK resolve, attention
+    KERNELS_PER_LAYER = 7  # prepare, int4 host append (K, V), score+select, CLOCK state + fetch, attention
 
     def __init__(self, torch, skv, wl, dev, layers, n_steps, eta):
         self.torch, self.skv, self.L = torch, skv, layers
@@ -629,6 +631,7 @@ class HostClockWorkloadGPU:
         self.aws = torch.zeros((skv.attend_workspace_size(B, W_HQ, Hkv, D, MAX_ROWS),), dtype=torch.uint8,
                                device=dev)
         self.pws = torch.zeros((skv.decode_prepare_workspace_size(B, Hkv),), dtype=torch.uint8, device=dev)
+        self.rws = torch.zeros((skv.resolve_workspace_size(B, MAX_ROWS),), dtype=torch.uint8, device=dev)
         self.out = torch.zeros((B, W_HQ, D), dtype=torch.float32, device=dev)
         self.status = torch.zeros((1,), dtype=torch.int32, device=dev)
         self.rb = rb
@@ -654,7 +657,7 @@ class HostClockWorkloadGPU:
         skv.resolve_rows_clock(self.lengths, self.idx, self.cnt, self.step_ctr[l], W_S, W_W, self.Hs, self.tok[l],
                                self.ref[l], self.use[l], self.tslot[l], self.hand[l], self.hosts[l].alias,
                                self.k8[l], self.v8[l], self.ks[l], self.vs[l], self.R, self.rows, self.nmiss[l],
-                               status=st)
+                               workspace=self.rws, status=st)
         ev("att0")
         skv.sparse_attend_decode(skv.KV_INT8, self.q[l], self.k8[l], self.v8[l], self.rows, self.cnt,
                                  1 / math.sqrt(W_D), self.out, self.aws, W_HKV, k_scale=self.ks[l],

@@ -414,19 +414,28 @@ int skv_sparse_attend_mla(int B, int Hq, int d, int dv, const uint16_t *q, const
  *              read by every CTA and advanced by one when the call completes
  *              (so a captured graph replays with a fresh step); step[1] = 0, a
  *              ticket the call returns to zero
+ *   workspace  skv_resolve_workspace_size(B, max_rows) bytes (the miss list
+ *              passed from the state pass to the fetch pass; no zero-fill)
+ * Two launches: one CTA per request runs the state machine and lists the
+ * misses, then one warp per miss fetches and requantises its host row.
  * Errors: SKV_EINVAL for bad sizes, null pointers, a req_row_stride below
  * S + W + Hs or unaligned pools; SKV_EUNSUPPORTED unless d is 256, 512, 768
- * or 1024, Hs <= 16384, max_rows <= 8192.  On the device: a token outside
+ * or 1024, Hs <= 16384, max_rows <= 8192 and a token's host row (2 Hkv
+ * vectors) is at most 5120 bytes; SKV_ENOMEM for a short workspace.  On the device: a token outside
  * [0, T) gives row -1 and SKV_DEV_RANGE; more picks than slots leave the state
  * unchanged, give row -1 for every pick and set SKV_DEV_COUNT.
  */
+/* Scratch bytes for either resolver call below. */
+size_t skv_resolve_workspace_size(int B, int max_rows);
+
 int skv_resolve_rows_clock(int B, int64_t t_cap, const int32_t *lengths, int S, int W, int Hkv,
                            int d, int Hs, const int32_t *idx, int max_rows, const int32_t *count,
                            int32_t *step, int32_t *slot_token, uint8_t *ref, int32_t *use_step,
                            int32_t *token_slot, int32_t *hand, const uint8_t *host_rows,
                            int8_t *k8, int8_t *v8, uint16_t *k_scale, uint16_t *v_scale,
                            int64_t req_row_stride, int32_t *rows_out, int32_t *n_miss,
-                           int32_t *dev_status, void *stream);
+                           void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                           void *stream);
 
 /*
  * skv_resolve_rows_lru -- mixed residency behind a block table with an LRU
@@ -450,9 +459,12 @@ int skv_resolve_rows_clock(int B, int64_t t_cap, const int32_t *lengths, int S, 
  *   alias); pool u8 [n_pool_rows][row_bytes]
  *   step   int32 [2] (device), as for skv_resolve_rows_clock: step[0] is the
  *          decode step, advanced by one when the call completes; step[1] = 0
+ *   workspace  skv_resolve_workspace_size(B, max_rows) bytes (miss list)
+ * Two launches: the state pass (one CTA per request), then one warp per miss
+ * copies the host row.
  * Errors: SKV_EINVAL for bad sizes, null or unaligned pointers, row_bytes not
  * a multiple of 16, a hot buffer past n_pool_rows; SKV_EUNSUPPORTED for
- * n_slots > 8192 or max_rows > 8192.  On the device: bad tokens give row -1
+ * n_slots > 8192 or max_rows > 8192; SKV_ENOMEM for a short workspace.  On the device: bad tokens give row -1
  * and SKV_DEV_RANGE; fewer untouched slots than misses leave the misses
  * unresolved (row -1), set n_miss[b] = -1 and SKV_DEV_COUNT.
  */
@@ -462,7 +474,8 @@ int skv_resolve_rows_lru(int B, int64_t t_cap, const int32_t *lengths, int page,
                          int32_t *slot_token, int32_t *token_slot, const uint8_t *host,
                          uint8_t *pool, int64_t row_bytes, int64_t n_pool_rows,
                          const int32_t *idx, int max_rows, const int32_t *count,
-                         int32_t *rows_out, int32_t *n_miss, int32_t *dev_status, void *stream);
+                         int32_t *rows_out, int32_t *n_miss, void *workspace,
+                         size_t workspace_bytes, int32_t *dev_status, void *stream);
 
 /*
  * skv_quantize_int4_rows -- host-tier row encoding ([P1]: int4 with 64-dim

@@ -66,10 +66,11 @@ def _load():
                 "skv_mla_workspace_size": ([i32, i32], sz),
                 "skv_sparse_attend_mla": ([i32, i32, i32, i32, P, P, P, i64, i64, P, i32, P, f32, P, P, sz, P, P],
                                           i32),
+                "skv_resolve_workspace_size": ([i32, i32], sz),
                 "skv_resolve_rows_clock": ([i32, i64, P, i32, i32, i32, i32, i32, P, i32, P, P, P, P, P, P, P, P,
-                                            P, P, P, P, i64, P, P, P, P], i32),
+                                            P, P, P, P, i64, P, P, P, sz, P, P], i32),
                 "skv_resolve_rows_lru": ([i32, i64, P, i32, P, i64, i64, i64, i32, P, P, P, P, P, P, i64, i64, P,
-                                          i32, P, P, P, P, P], i32),
+                                          i32, P, P, P, P, sz, P, P], i32),
                 "skv_quantize_int4_rows": ([P, i64, i32, i32, P, P, i64, i64, P], i32),
                 "skv_stream_read": ([P, sz, P, i32, P], i32),
                 "skv_host_register": ([P, sz, ctypes.POINTER(ctypes.c_void_p)], i32),
@@ -225,35 +226,47 @@ def _addr(t):
     return ctypes.c_void_p(t if isinstance(t, int) else t.data_ptr())
 
 
+def resolve_workspace_size(B, max_rows) -> int:
+    return int(_load().skv_resolve_workspace_size(B, max_rows))
+
+
+def _resolve_ws(workspace, B, max_rows):
+    if workspace is None:
+        workspace = torch.empty((resolve_workspace_size(B, max_rows),), dtype=torch.uint8, device="cuda")
+    return workspace
+
+
 def resolve_rows_clock(lengths, idx, count, step, S, W, Hs, slot_token, ref, use_step, token_slot, hand,
-                       host_rows, k8, v8, k_scale, v_scale, req_row_stride, rows_out, n_miss, status=None,
-                       stream=None):
+                       host_rows, k8, v8, k_scale, v_scale, req_row_stride, rows_out, n_miss, workspace=None,
+                       status=None, stream=None):
     """Windowed CLOCK resolve (see skv_resolve_rows_clock).  step: int32 device tensor [2] (advanced by
     the call); host_rows: uint8 tensor or an int alias."""
     B, max_rows = idx.shape
     t_cap = token_slot.shape[1]
     Hkv, d = k8.shape[-2], k8.shape[-1]
+    workspace = _resolve_ws(workspace, B, max_rows)
     _check("skv_resolve_rows_clock", _load().skv_resolve_rows_clock(
         B, t_cap, _ptr(lengths), S, W, Hkv, d, Hs, _ptr(idx), max_rows, _ptr(count), _ptr(step),
         _ptr(slot_token), _ptr(ref), _ptr(use_step), _ptr(token_slot), _ptr(hand), _addr(host_rows),
         _ptr(k8), _ptr(v8), _ptr(k_scale), _ptr(v_scale), int(req_row_stride), _ptr(rows_out), _ptr(n_miss),
-        _ptr(status), _stream(stream)))
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream)))
     return rows_out, n_miss
 
 
 def resolve_rows_lru(lengths, idx, count, step, page, block_table, hot_base, hot_stride, stamp, slot_token,
-                     token_slot, host, pool, rows_out, n_miss, status=None, stream=None):
+                     token_slot, host, pool, rows_out, n_miss, workspace=None, status=None, stream=None):
     """Block table + LRU hot buffer resolve (see skv_resolve_rows_lru).  step: int32 device tensor [2]
     (advanced by the call); host: uint8 tensor or int alias."""
     B, max_rows = idx.shape
     t_cap = token_slot.shape[1]
     n_slots = stamp.shape[1]
     n_pool_rows, row_bytes = pool.shape
+    workspace = _resolve_ws(workspace, B, max_rows)
     _check("skv_resolve_rows_lru", _load().skv_resolve_rows_lru(
         B, t_cap, _ptr(lengths), page, _ptr(block_table), block_table.shape[1], int(hot_base), int(hot_stride),
         n_slots, _ptr(step), _ptr(stamp), _ptr(slot_token), _ptr(token_slot), _addr(host), _ptr(pool), row_bytes,
-        n_pool_rows, _ptr(idx), max_rows, _ptr(count), _ptr(rows_out), _ptr(n_miss), _ptr(status),
-        _stream(stream)))
+        n_pool_rows, _ptr(idx), max_rows, _ptr(count), _ptr(rows_out), _ptr(n_miss), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream)))
     return rows_out, n_miss
 
 

@@ -11,10 +11,12 @@
 // miss copies one row from pinned host memory into an LRU slot of the hot
 // buffer ("What it composes with": the hot buffer holds 2 x top-K rows).
 //
-// One CTA per request.  The resolver state of the request is staged in
-// shared memory, the hit pass runs over all threads, the sweep (CLOCK) or the
-// victim order (LRU) is computed on chip, and every warp then fetches miss
-// rows from the host alias with several rows in flight per warp.
+// Two launches per call.  First one CTA per request: the resolver state of
+// the request is staged in shared memory, the hit pass runs over all threads,
+// the sweep (CLOCK) or the victim order (LRU) is computed on chip, and the
+// misses are listed.  Then a wide grid with one warp per miss reads the host
+// rows with coalesced 16-byte loads, so that many SMs keep host reads in
+// flight at once.
 #include "common.cuh"
 
 namespace skv {
@@ -22,8 +24,7 @@ namespace {
 
 constexpr int kResThreads = 1024;
 constexpr int kClockThreads = 512;
-constexpr int kFetchRows = 4;  // LRU host rows in flight per warp
-constexpr int kClockFetch = 2; // CLOCK host tokens in flight per warp
+constexpr int kMaxTokBytes = 5120;  // host bytes of one token's row (all heads, K and V), CLOCK tier
 constexpr int kMaxClockSlots = 16384;
 constexpr int kMaxLruSlots = 8192;
 constexpr int kMaxResolveRows = 8192;
@@ -71,6 +72,8 @@ struct ClockArgs {
   int64_t req_row_stride;
   int32_t* rows_out;
   int32_t* n_miss;
+  int32_t* ws_tok;  // [B][max_rows] miss tokens
+  int32_t* ws_row;  // [B][max_rows] their destination pool rows
   int32_t* status;
 };
 
@@ -276,51 +279,11 @@ __global__ __launch_bounds__(kClockThreads) void clock_kernel(ClockArgs a) {
   }
   __syncthreads();
 
-  // Phase 3: fetch each miss's host row (Hkv heads x [K | V] int4 vectors)
-  // and write its int8 requantisation into the slot's pool rows.
-  const int ng = a.d / 64;
-  const int rb = a.d / 2 + 2 * ng;
-  const int tasks = 2 * a.Hkv * ng;
-  const int64_t tok_bytes = static_cast<int64_t>(tasks / ng) * rb;
-  const int nw = kClockThreads / 32;
-  for (int j0 = warp * kClockFetch; j0 < nm; j0 += nw * kClockFetch) {
-    for (int it = 0; it * 32 < tasks; it++) {
-      const int task = it * 32 + lane;
-      const bool tv = task < tasks;
-      const int v = task / ng, g = task % ng;
-      uint2 c[kClockFetch][4];
-      uint16_t sb[kClockFetch];
-#pragma unroll
-      for (int u = 0; u < kClockFetch; u++) {
-        const int j = j0 + u;
-        if (tv && j < nm && m_slot[j] >= 0) {
-          const uint8_t* src = a.host_rows + (static_cast<int64_t>(b) * a.t_cap + m_tok[j]) * tok_bytes +
-                               static_cast<int64_t>(v) * rb;
-          const uint2* cp = reinterpret_cast<const uint2*>(src + 32 * g);
-#pragma unroll
-          for (int q = 0; q < 4; q++) c[u][q] = cp[q];
-          sb[u] = *reinterpret_cast<const uint16_t*>(src + a.d / 2 + 2 * g);
-        } else {
-#pragma unroll
-          for (int q = 0; q < 4; q++) c[u][q] = make_uint2(0u, 0u);
-          sb[u] = 0;
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < kClockFetch; u++) {
-        const int j = j0 + u;
-        const bool live = tv && j < nm && m_slot[j] >= 0;
-        int8_t* dst = nullptr;
-        __half* sdst = nullptr;
-        if (live) {
-          const int64_t row = static_cast<int64_t>(b) * a.req_row_stride + S + W + m_slot[j];
-          const int hh = v >> 1;
-          dst = ((v & 1) ? a.v8 : a.k8) + (row * a.Hkv + hh) * a.d + 64 * g;
-          if (g == 0) sdst = ((v & 1) ? a.v_scale : a.k_scale) + row * a.Hkv + hh;
-        }
-        requant_group(c[u], sb[u], ng, dst, sdst, live);
-      }
-    }
+  // Phase 3: the miss list for the fetch kernel (token, destination pool row).
+  for (int j = tid; j < nm; j += kClockThreads) {
+    a.ws_tok[static_cast<int64_t>(b) * a.max_rows + j] = m_tok[j];
+    a.ws_row[static_cast<int64_t>(b) * a.max_rows + j] =
+        m_slot[j] >= 0 ? static_cast<int32_t>(static_cast<int64_t>(b) * a.req_row_stride + S + W + m_slot[j]) : -1;
   }
 
   // Phase 4: state back to global memory.
@@ -332,6 +295,78 @@ __global__ __launch_bounds__(kClockThreads) void clock_kernel(ClockArgs a) {
   if (tid == 0) a.n_miss[b] = fits ? nm : -1;
   __syncthreads();
   if (tid == 0) advance_step(a.step);
+}
+
+// One warp per miss: the token's host row (Hkv heads x [K | V] int4 vectors,
+// contiguous) is read with coalesced 16-byte loads into shared memory, then
+// each lane requantises one 64-dim group to int8 and writes it to the pool.
+constexpr int kFetchWarps = 8;
+
+__global__ __launch_bounds__(32 * kFetchWarps) void fetch_int4_kernel(
+    const int32_t* __restrict__ ws_tok, const int32_t* __restrict__ ws_row, const int32_t* __restrict__ n_miss,
+    int max_rows, int64_t t_cap, int Hkv, int d, const uint8_t* __restrict__ host_rows, int8_t* __restrict__ k8,
+    int8_t* __restrict__ v8, __half* __restrict__ k_scale, __half* __restrict__ v_scale) {
+  extern __shared__ __align__(16) unsigned char stage_all[];
+  const int b = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int j = blockIdx.x * kFetchWarps + warp;
+  const int nm = n_miss[b];
+  if (j >= nm) return;  // also nm == -1
+  const int64_t row = ws_row[static_cast<int64_t>(b) * max_rows + j];
+  if (row < 0) return;
+  const int32_t tok = ws_tok[static_cast<int64_t>(b) * max_rows + j];
+  const int ng = d / 64, rb = d / 2 + 2 * ng, tasks = 2 * Hkv * ng;
+  const int tb = 2 * Hkv * rb;
+  unsigned char* stage = stage_all + warp * tb;
+  const uint4* src = reinterpret_cast<const uint4*>(host_rows + (static_cast<int64_t>(b) * t_cap + tok) * tb);
+  for (int c = lane; c < tb / 16; c += 32) reinterpret_cast<uint4*>(stage)[c] = ld_nc16(src + c);
+  __syncwarp();
+  for (int it = 0; it * 32 < tasks; it++) {
+    const int task = it * 32 + lane;
+    const bool live = task < tasks;
+    const int v = live ? task / ng : 0, g = live ? task % ng : 0;
+    const unsigned char* vec = stage + v * rb;
+    uint2 c[4];
+#pragma unroll
+    for (int q = 0; q < 4; q++) c[q] = reinterpret_cast<const uint2*>(vec + 32 * g)[q];
+    const uint16_t sb = *reinterpret_cast<const uint16_t*>(vec + d / 2 + 2 * g);
+    const int hh = v >> 1;
+    int8_t* dst = ((v & 1) ? v8 : k8) + (row * Hkv + hh) * d + 64 * g;
+    __half* sdst = g == 0 ? ((v & 1) ? v_scale : k_scale) + row * Hkv + hh : nullptr;
+    requant_group(c, sb, ng, dst, sdst, live);
+  }
+}
+
+// One warp per miss, kRowsPerWarp rows in flight: plain row copy host -> pool.
+constexpr int kRowsPerWarp = 2;
+
+__global__ __launch_bounds__(32 * kFetchWarps) void fetch_rows_kernel(
+    const int32_t* __restrict__ ws_tok, const int32_t* __restrict__ ws_row, const int32_t* __restrict__ n_miss,
+    int max_rows, int64_t t_cap, const uint8_t* __restrict__ host, uint8_t* __restrict__ pool, int64_t row_bytes) {
+  const int b = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int j0 = (blockIdx.x * kFetchWarps + warp) * kRowsPerWarp;
+  const int nm = n_miss[b];
+  if (j0 >= nm) return;
+  const int chunks = static_cast<int>(row_bytes / 16);
+  for (int c0 = 0; c0 < chunks; c0 += 32) {
+    const int c = c0 + lane;
+    uint4 v[kRowsPerWarp];
+#pragma unroll
+    for (int u = 0; u < kRowsPerWarp; u++) {
+      const int j = j0 + u;
+      if (c < chunks && j < nm) {
+        const int32_t tok = ws_tok[static_cast<int64_t>(b) * max_rows + j];
+        v[u] = ld_nc16(host + (static_cast<int64_t>(b) * t_cap + tok) * row_bytes + 16 * c);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kRowsPerWarp; u++) {
+      const int j = j0 + u;
+      if (c < chunks && j < nm) {
+        const int64_t row = ws_row[static_cast<int64_t>(b) * max_rows + j];
+        reinterpret_cast<uint4*>(pool + row * row_bytes)[c] = v[u];
+      }
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -357,6 +392,8 @@ struct LruArgs {
   const int32_t* count;
   int32_t* rows_out;
   int32_t* n_miss;
+  int32_t* ws_tok;
+  int32_t* ws_row;
   int32_t* status;
 };
 
@@ -487,29 +524,11 @@ __global__ __launch_bounds__(kResThreads) void lru_kernel(LruArgs a, int P) {
       s_stamp[s] = step;
       rows[m_pos[j]] = static_cast<int32_t>(hot + s);
     }
-    // Copy the miss rows from the host alias, kFetchRows rows per warp at once.
-    const int chunks = static_cast<int>(a.row_bytes / 16);
-    const int nw = kResThreads / 32;
-    for (int j0 = warp * kFetchRows; j0 < nm; j0 += nw * kFetchRows) {
-      for (int c0 = 0; c0 < chunks; c0 += 32) {
-        const int c = c0 + lane;
-        uint4 v[kFetchRows];
-#pragma unroll
-        for (int u = 0; u < kFetchRows; u++) {
-          const int j = j0 + u;
-          if (c < chunks && j < nm)
-            v[u] = reinterpret_cast<const uint4*>(a.host + (static_cast<int64_t>(b) * a.t_cap + m_tok[j]) *
-                                                               a.row_bytes)[c];
-        }
-#pragma unroll
-        for (int u = 0; u < kFetchRows; u++) {
-          const int j = j0 + u;
-          if (c < chunks && j < nm) {
-            const int s = static_cast<int>(key[j] & 0xffffffffu);
-            reinterpret_cast<uint4*>(a.pool + (hot + s) * a.row_bytes)[c] = v[u];
-          }
-        }
-      }
+    // the miss list for the fetch kernel
+    for (int j = tid; j < nm; j += kResThreads) {
+      a.ws_tok[static_cast<int64_t>(b) * a.max_rows + j] = m_tok[j];
+      a.ws_row[static_cast<int64_t>(b) * a.max_rows + j] =
+          static_cast<int32_t>(hot + static_cast<int64_t>(key[j] & 0xffffffffu));
     }
   }
   __syncthreads();
@@ -596,12 +615,18 @@ __global__ __launch_bounds__(512) void stream_read_kernel(const uint4* __restric
 
 using namespace skv;
 
+SKV_EXPORT size_t skv_resolve_workspace_size(int B, int max_rows) {
+  if (B < 1 || max_rows < 1) return 0;
+  return 2 * static_cast<size_t>(B) * max_rows * sizeof(int32_t);
+}
+
 SKV_EXPORT int skv_resolve_rows_clock(int B, int64_t t_cap, const int32_t* lengths, int S, int W, int Hkv, int d,
                                       int Hs, const int32_t* idx, int max_rows, const int32_t* count,
                                       int32_t* step, int32_t* slot_token, uint8_t* ref, int32_t* use_step,
                                       int32_t* token_slot, int32_t* hand, const uint8_t* host_rows, int8_t* k8,
                                       int8_t* v8, uint16_t* k_scale, uint16_t* v_scale, int64_t req_row_stride,
-                                      int32_t* rows_out, int32_t* n_miss, int32_t* dev_status, void* stream) {
+                                      int32_t* rows_out, int32_t* n_miss, void* workspace, size_t workspace_bytes,
+                                      int32_t* dev_status, void* stream) {
   if (B < 0 || B > 65535 || t_cap < 0 || S < 0 || W < 0 || Hkv < 1 || Hs < 1 || max_rows < 1) return SKV_EINVAL;
   if (B == 0) return SKV_OK;
   if (d < 256 || d % 256 || d > 1024) return SKV_EUNSUPPORTED;
@@ -611,6 +636,11 @@ SKV_EXPORT int skv_resolve_rows_clock(int B, int64_t t_cap, const int32_t* lengt
       !k8 || !v8 || !k_scale || !v_scale || !rows_out || !n_miss)
     return SKV_EINVAL;
   if (!aligned16(host_rows) || !aligned16(k8) || !aligned16(v8)) return SKV_EINVAL;
+  const int tb = 2 * Hkv * (d / 2 + d / 32);
+  if (tb > kMaxTokBytes) return SKV_EUNSUPPORTED;
+  if (!workspace || workspace_bytes < skv_resolve_workspace_size(B, max_rows)) return SKV_ENOMEM;
+  int32_t* ws_tok = static_cast<int32_t*>(workspace);
+  int32_t* ws_row = ws_tok + static_cast<size_t>(B) * max_rows;
   const size_t smem = clock_smem_bytes(Hs, max_rows);
   static size_t configured = 0;
   if (smem > 48 * 1024 && smem > configured) {
@@ -623,8 +653,13 @@ SKV_EXPORT int skv_resolve_rows_clock(int B, int64_t t_cap, const int32_t* lengt
   }
   ClockArgs a{t_cap, lengths, S, W, Hkv, d, Hs, idx, max_rows, count, step, slot_token, ref, use_step,
               token_slot, hand, host_rows, k8, v8, reinterpret_cast<__half*>(k_scale),
-              reinterpret_cast<__half*>(v_scale), req_row_stride, rows_out, n_miss, dev_status};
-  clock_kernel<<<B, kClockThreads, smem, as_stream(stream)>>>(a);
+              reinterpret_cast<__half*>(v_scale), req_row_stride, rows_out, n_miss, ws_tok, ws_row, dev_status};
+  cudaStream_t st = as_stream(stream);
+  clock_kernel<<<B, kClockThreads, smem, st>>>(a);
+  const dim3 fgrid((max_rows + kFetchWarps - 1) / kFetchWarps, B);
+  fetch_int4_kernel<<<fgrid, 32 * kFetchWarps, kFetchWarps * tb, st>>>(
+      ws_tok, ws_row, n_miss, max_rows, t_cap, Hkv, d, host_rows, k8, v8, reinterpret_cast<__half*>(k_scale),
+      reinterpret_cast<__half*>(v_scale));
   return launch_status();
 }
 
@@ -633,8 +668,8 @@ SKV_EXPORT int skv_resolve_rows_lru(int B, int64_t t_cap, const int32_t* lengths
                                     int64_t hot_stride, int n_slots, int32_t* step, int64_t* stamp,
                                     int32_t* slot_token, int32_t* token_slot, const uint8_t* host, uint8_t* pool,
                                     int64_t row_bytes, int64_t n_pool_rows, const int32_t* idx, int max_rows,
-                                    const int32_t* count, int32_t* rows_out, int32_t* n_miss, int32_t* dev_status,
-                                    void* stream) {
+                                    const int32_t* count, int32_t* rows_out, int32_t* n_miss, void* workspace,
+                                    size_t workspace_bytes, int32_t* dev_status, void* stream) {
   if (B < 0 || B > 65535 || t_cap < 0 || page < 1 || n_pages < 0 || n_slots < 1 || max_rows < 1 ||
       row_bytes < 16 || row_bytes % 16 || hot_base < 0 || hot_stride < 0)
     return SKV_EINVAL;
@@ -647,6 +682,9 @@ SKV_EXPORT int skv_resolve_rows_lru(int B, int64_t t_cap, const int32_t* lengths
       !rows_out || !n_miss)
     return SKV_EINVAL;
   if (!aligned16(host) || !aligned16(pool)) return SKV_EINVAL;
+  if (!workspace || workspace_bytes < skv_resolve_workspace_size(B, max_rows)) return SKV_ENOMEM;
+  int32_t* ws_tok = static_cast<int32_t*>(workspace);
+  int32_t* ws_row = ws_tok + static_cast<size_t>(B) * max_rows;
   const int P = pow2_at_least(n_slots);
   const size_t smem = lru_smem_bytes(n_slots, max_rows);
   static size_t configured = 0;
@@ -659,8 +697,13 @@ SKV_EXPORT int skv_resolve_rows_lru(int B, int64_t t_cap, const int32_t* lengths
     configured = smem;
   }
   LruArgs a{t_cap, lengths, page, block_table, n_pages, hot_base, hot_stride, n_slots, step, stamp, slot_token,
-            token_slot, host, pool, row_bytes, n_pool_rows, idx, max_rows, count, rows_out, n_miss, dev_status};
-  lru_kernel<<<B, kResThreads, smem, as_stream(stream)>>>(a, P);
+            token_slot, host, pool, row_bytes, n_pool_rows, idx, max_rows, count, rows_out, n_miss, ws_tok, ws_row,
+            dev_status};
+  cudaStream_t st = as_stream(stream);
+  lru_kernel<<<B, kResThreads, smem, st>>>(a, P);
+  const int per_cta = kFetchWarps * kRowsPerWarp;
+  fetch_rows_kernel<<<dim3((max_rows + per_cta - 1) / per_cta, B), 32 * kFetchWarps, 0, st>>>(
+      ws_tok, ws_row, n_miss, max_rows, t_cap, host, pool, row_bytes);
   return launch_status();
 }
 

@@ -1,0 +1,81 @@
+"""Full-size parity in the benchmark's launch configuration.
+
+One layer-step of the sketch workload -- 8 requests x 250,000 tokens, 24
+query / 4 KV heads, head dim 256, int8 K/V, int4 rank-64 sketch, top 2048 +
+64 sinks + 1024 tail -- built and launched by the very code the benchmark
+times (bench.SketchWorkloadGPU: fused prepare, fused score + select,
+attention), then checked against the oracle:
+
+* prepare: the folded query q8 and the appended token's sketch codes equal
+  the oracle's except +-1 at rounding ties; its int8 K/V rows are bit-exact;
+* selection: bit-exact for every request against the oracle's score + top-k
+  on the same sketch bytes and q8 (all 248,912 candidates per request);
+* attention: every output within 2e-3 of the fp64 oracle on the selected rows.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import skvtest as T
+import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def skv():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from sparse_kv_long_gb300 import _build
+    _build.build()
+    import sparse_kv_long_gb300 as m
+    return m
+
+
+def test_sketch_workload_full_size_layer_step(skv, orc):
+    import bench
+    B, Tn, Hq, Hkv, d, r = bench.W_B, bench.W_T, bench.W_HQ, bench.W_HKV, bench.W_D, bench.W_R
+    k, S, W = bench.W_K, bench.W_S, bench.W_W
+    w = bench.SketchWorkloadGPU(torch, skv, wl, torch.device("cuda", 0), layers=1)
+    w.layer(0)
+    torch.cuda.synchronize()
+    assert int(w.status.item()) == 0
+    U, c = T.host(w.U), T.host(w.c)
+    q, nk, nv = T.host(w.q[0]), T.host(w.newk[0]), T.host(w.newv[0])
+
+    # a1 + a2 + int8 append of the current token (row T-1 of every request)
+    ref_q = orc.sketch_query(q, Hkv, U, c)
+    T.assert_codes_match_except_ties(T.host(w.q8), ref_q["q8"], ref_q["x"])
+    ref_sk = orc.sketch_project(nk, U, c)
+    sk = T.host(w.sk[0])                                          # [B][T][128] int4 codes
+    rk8, rks = orc.quant_int8_rows(nk)
+    rv8, rvs = orc.quant_int8_rows(nv)
+    last = torch.arange(B, device="cuda") * Tn + (Tn - 1)
+    for b in range(B):
+        T.assert_codes_match_except_ties(T.unpack_int4(sk[b, Tn - 1]), T.unpack_int4(ref_sk["q4"][b]),
+                                         ref_sk["x"][b].ravel())
+    np.testing.assert_array_equal(T.host(w.k8[0][last]), rk8)
+    np.testing.assert_array_equal(T.host(w.v8[0][last]), rv8)
+    np.testing.assert_array_equal(T.host(w.ks[0][last]), rks)
+    np.testing.assert_array_equal(T.host(w.vs[0][last]), rvs)
+
+    # a3 + a4 on the same bytes
+    L = np.full((B,), Tn, np.int32)
+    sc = orc.index_score(orc.SKETCH_INT4, T.host(w.q8), sk, L, S=S, W=W)
+    ridx, rcnt = orc.topk_select(sc["okey"], L, k, S=S, W=W)
+    gidx, gcnt = T.host(w.idx), T.host(w.cnt)
+    np.testing.assert_array_equal(gcnt, rcnt)
+    np.testing.assert_array_equal(gidx, ridx)
+
+    # a6 on the selected rows
+    n = S + k + W
+    phys = (torch.arange(B, device="cuda")[:, None] * Tn + w.idx.long()).reshape(-1)
+    k8s, v8s = T.host(w.k8[0][phys]), T.host(w.v8[0][phys])
+    kss, vss = T.host(w.ks[0][phys]), T.host(w.vs[0][phys])
+    rows = np.tile(np.arange(n, dtype=np.int32), (B, 1))
+    ref = orc.attend(orc.KV_INT8, q, k8s.reshape(B * n, -1), v8s.reshape(B * n, -1), rows, gcnt, 1 / math.sqrt(d),
+                     Hkv, d, d, k_scale=kss, v_scale=vss, req_row_stride=n)
+    err = np.max(np.abs(T.host(w.out[0]) - ref))
+    assert err < 2e-3, err
