@@ -49,7 +49,7 @@ ATTN_BYTES_PER_ROW_HEAD = 2 * W_D + 2 * 2       # int8 K + V rows and their fp16
 # command), keyed by a hash of the kernel's sources: a kernel whose sources
 # changed since the capture reports null.
 MEASURED_TRAFFIC = {
-    "score_select": (("common.cuh", "score_common.cuh", "select.cu"), "fd977d44ad3ea622", 258_213_376),
+    "score_select": (("common.cuh", "fold.cuh", "score_common.cuh", "select.cu"), "fd977d44ad3ea622", 258_213_376),
     "attend": (("common.cuh", "attend.cu"), "1f296da7a22ce8c9", 56_068_864),
 }
 
@@ -256,18 +256,16 @@ class SketchWorkloadGPU:
         self.status = torch.zeros((1,), dtype=torch.int32, device=dev)
         torch.cuda.synchronize()
 
-    KERNELS_PER_LAYER = 3  # a1 + int8 append + a2 fused, a3 + a4 fused, a6
+    KERNELS_PER_LAYER = 2  # a1 + int8 append + a2 + a3 + a4 in one launch, a6
 
     def layer(self, l, marks=None):
         skv, st = self.skv, self.status
         ev = (lambda name: marks(l, name)) if marks else (lambda name: None)
         ev("start")
-        skv.decode_prepare(self.q[l], self.newk[l], self.newv[l], self.U, self.c, self.new_rows,
-                           self.sk[l].view(W_B * W_T, -1), self.k8[l], self.ks[l], self.v8[l], self.vs[l], self.q8,
-                           self.pws, sigma=self.sigma)
         ev("scan0")
-        skv.score_select(skv.SKETCH_INT4, self.q8, self.sk[l], self.lengths, W_K, self.idx, self.cnt, self.tws,
-                         S=W_S, W=W_W, status=st)
+        skv.decode_select(self.q[l], self.newk[l], self.newv[l], self.U, self.c, self.new_rows, self.sk[l],
+                          self.k8[l], self.ks[l], self.v8[l], self.vs[l], self.lengths, W_K, self.idx, self.cnt,
+                          self.tws, S=W_S, W=W_W, q8_out=self.q8, status=st)
         ev("scan1")
         ev("attn0")
         skv.sparse_attend_decode(skv.KV_INT8, self.q[l], self.k8[l], self.v8[l], self.idx, self.cnt,
@@ -414,9 +412,10 @@ def run_gpu(args):
                               f"{step_bytes / 1e9:.2f} GB read per step", layers=L),
         "tokens_per_s": tokens_per_s, "hbm_gbs": step_gbs,
         "parallelism": "replicas only" if world > 1 else "single GPU",
-        "kernel_us": {"score_select_int4": scan_us, "sparse_attend_int8": attn_us},
+        "kernel_us": {"decode_select_int4": scan_us, "sparse_attend_int8": attn_us},
         "roofline": {"bound": "hbm", "achieved": scan_gbs, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": scan_gbs / hbm_peak, "traffic": measured_traffic("score_select"), "kernel": "score_select_kernel (scan + top-k)",
+                     "frac": scan_gbs / hbm_peak, "traffic": measured_traffic("score_select"),
+                     "kernel": "score_select_kernel (query fold + append + scan + top-k)",
                      "peak_source": peak_src, "bytes_per_launch": scan_bytes,
                      "bytes_rule": f"{SCAN_BYTES_PER_CAND} B sketch row per candidate token x {W_B} x {n_cand}"},
         "roofline_attend": {"bound": "hbm", "achieved": attn_gbs, "peak": hbm_peak, "unit": "GB/s",

@@ -287,6 +287,31 @@ int skv_score_select(int mode, int B, int width, const void *query, const void *
                      void *workspace, size_t workspace_bytes, int32_t *dev_status,
                      void *stream);
 
+/*
+ * skv_decode_select -- skv_decode_prepare followed by skv_score_select
+ * (SKETCH_INT4) on the same sketch, in one cooperative launch: the per-layer
+ * path before attention.  Every CTA folds its request's query itself (the
+ * arithmetic of skv_decode_prepare, so the same q8 bits), and CTA h < Hkv of
+ * each request appends head h of the current token (sketch codes, int8 K and
+ * V rows at new_rows[b]).  Arguments as in those two calls; the sketch is
+ * both the append target ([rows][Hkv*r/2], rows = b*n_cap + t) and the scored
+ * keys ([B][n_cap][Hkv*r/2]).
+ *   q8_out  int8 [B][Hkv*r] copy of the folded query, or NULL
+ * The appended token must be in its request's recent tail (new_rows[b] =
+ * b*n_cap + t with t >= T_b - W), as the newest token is: tail tokens are not
+ * scored, so no CTA reads the row being written.  A row inside the scored
+ * range sets SKV_DEV_RANGE.
+ * Constraints: r == 64, W >= 1, Hkv*r in {128, 256, 512},
+ * Hkv*d + d + 5*Hkv*r + 256 <= 8192; others as skv_score_select.
+ */
+int skv_decode_select(int B, int Hq, int Hkv, int d, int r, const uint16_t *q,
+                      const uint16_t *new_k, const uint16_t *new_v, const float *basis,
+                      const float *c, const int64_t *new_rows, uint8_t *sketch, int8_t *k8,
+                      uint16_t *k_scale, int8_t *v8, uint16_t *v_scale, int64_t n_cap,
+                      const int32_t *lengths, int k, int S, int W, int32_t *idx, int max_rows,
+                      int32_t *count, int8_t *q8_out, void *workspace, size_t workspace_bytes,
+                      int32_t *dev_status, void *stream);
+
 /* ========================================================================== */
 /* KV row encoding (write path).                                               */
 /* ========================================================================== */

@@ -59,6 +59,8 @@ def _load():
                 "skv_score_select_workspace_size": ([i32], sz),
                 "skv_score_select": ([i32, i32, i32, P, P, i64, P, i32, i32, i32, i32, P, i32, P, P, P, sz, P, P],
                                      i32),
+                "skv_decode_select": ([i32, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P, P, P, i64, P, i32, i32,
+                                       i32, P, i32, P, P, P, sz, P, P], i32),
                 "skv_quantize_int8_rows": ([P, i64, i32, i32, P, P, P, P], i32),
                 "skv_attend_workspace_size": ([i32, i32, i32, i32, i32], sz),
                 "skv_sparse_attend_decode": ([i32, i32, i32, i32, i32, P, P, P, P, P, i64, i64, P, i32, P,
@@ -195,6 +197,22 @@ def score_select(mode, query, keys, lengths, k, idx, count, workspace, S=0, W=0,
         mode, B, width, _ptr(query), _ptr(keys), n_cap, _ptr(lengths), ratio, k, S, W, _ptr(idx), idx.shape[1],
         _ptr(count), _ptr(order_keys), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _ptr(status), _stream(stream)))
+    return idx, count
+
+
+def decode_select(q, new_k, new_v, basis, c, new_rows, sketch, k8, k_scale, v8, v_scale, lengths, k, idx, count,
+                  workspace, S=0, W=1, q8_out=None, status=None, stream=None):
+    """decode_prepare + score_select(SKETCH_INT4) in one launch.  sketch uint8 [B][n_cap][Hkv*r/2]
+    (also the append target); k8/v8 [B*n_cap][Hkv][d]; new_rows int64 [B] flat rows."""
+    B, Hq, d = q.shape
+    Hkv = new_k.shape[1]
+    r = basis.shape[1]
+    n_cap = sketch.shape[1]
+    _check("skv_decode_select", _load().skv_decode_select(
+        B, Hq, Hkv, d, r, _ptr(q), _ptr(new_k), _ptr(new_v), _ptr(basis), _ptr(c), _ptr(new_rows), _ptr(sketch),
+        _ptr(k8), _ptr(k_scale), _ptr(v8), _ptr(v_scale), n_cap, _ptr(lengths), k, S, W, _ptr(idx), idx.shape[1],
+        _ptr(count), _ptr(q8_out), _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(status),
+        _stream(stream)))
     return idx, count
 
 

@@ -29,6 +29,7 @@
 // leave resets it.  Polls are bounded: a wait that runs out sets
 // SKV_DEV_TIMEOUT and the kernel goes on.  The cooperative launch guarantees
 // that all CTAs are resident together.
+#include "fold.cuh"
 #include "score_common.cuh"
 
 namespace skv {
@@ -71,6 +72,27 @@ Ws ws_carve(void* base, int B) {
   return w;
 }
 
+// Optional per-step preparation done inside the launch (skv_decode_select):
+// every CTA folds its request's query into int8 itself (same arithmetic as
+// skv_decode_prepare, so the same q8 in every CTA), and CTA h < Hkv of each
+// request appends head h of the current token (sketch codes, int8 K and V
+// rows).  The appended token is in the recent tail, so no CTA scores it.
+struct Prep {
+  const uint16_t* q;  // bf16 [B][Hq][d]; NULL: q8 is read from Args::query
+  const uint16_t* newk;
+  const uint16_t* newv;
+  const float* basis;  // [d][64]
+  const float* c;      // [Hkv][64]
+  const int64_t* new_rows;
+  uint8_t* sketch;  // [rows][Hkv*32]
+  int8_t* k8;
+  __half* ks;
+  int8_t* v8;
+  __half* vs;
+  int8_t* q8_out;  // optional copy of the folded query
+  int Hq, Hkv, d;
+};
+
 struct Args {
   int mode, width;
   const void* query;
@@ -84,7 +106,106 @@ struct Args {
   uint32_t* okeys;  // optional copy of the order keys
   int32_t* status;
   int B;
+  Prep prep;
 };
+
+// The preparation step inside every CTA of a request: the group sums of the
+// query heads (Hkv vectors) and, in CTA h < Hkv, the appended key of head h
+// share one pass over the basis (one 32-dim slice of one basis column per
+// thread, the arithmetic of skv_decode_prepare); every CTA then derives the
+// request's scale and int8 query itself (the same bits everywhere, no
+// waiting), and CTA h writes head h's sketch codes and int8 K and V rows.
+// `scratch` holds (Hkv + 2)*d + (Hkv + 1)*64*ceil(d/32) + Hkv*64 floats.
+__device__ __noinline__ void prepare_in_cta(const Prep& p, int b, int c, int64_t n_cap, int64_t T, int S, int W,
+                                            float* scratch, int8_t* s_q8, float* red, int32_t* status) {
+  using fold::kRank;
+  const int Hkv = p.Hkv, d = p.d, G = p.Hq / Hkv, ns = fold::n_slices(d), width = Hkv * kRank;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nt = blockDim.x;
+  const bool app = c < Hkv;  // this CTA appends head c
+  const int nv = Hkv + (app ? 1 : 0);
+  float* X = scratch;                   // [Hkv + 1][d]: group sums, appended key of head c
+  float* part = X + (Hkv + 1) * d;      // [ns][Hkv + 1][64]
+  float* qp = part + ns * (Hkv + 1) * kRank;  // [width]
+  uint16_t* kv_rows = reinterpret_cast<uint16_t*>(qp + width);  // [2][d] bf16 rows to encode
+  int64_t row = 0;
+  if (app) {
+    row = p.new_rows[b];
+    for (int u = tid; u < 2 * (d / 8); u += nt) {
+      const int which = u / (d / 8), piece = u - which * (d / 8);
+      const uint16_t* src = (which == 0 ? p.newk : p.newv) + (static_cast<int64_t>(b) * Hkv + c) * d + 8 * piece;
+      asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(
+                       __cvta_generic_to_shared(kv_rows + which * d + 8 * piece))),
+                   "l"(src)
+                   : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
+  const bool one_task = ns * kRank <= nt;
+  float bcol[fold::kSlice];
+  if (one_task && tid < ns * kRank) fold::load_slice(p.basis, d, tid % kRank, tid / kRank, bcol);
+  for (int i = tid; i < Hkv * d; i += nt) {
+    const int h = i / d, x = i - h * d;
+    X[i] = fold::group_sum(p.q + (static_cast<int64_t>(b) * p.Hq + static_cast<int64_t>(h) * G) * d, G, d, x);
+  }
+  if (app)
+    for (int x = tid; x < d; x += nt) X[Hkv * d + x] = bf16_bits_to_f32(p.newk[(static_cast<int64_t>(b) * Hkv + c) * d + x]);
+  __syncthreads();
+  if (one_task) {
+    if (tid < ns * kRank) {
+      const int sl = tid / kRank, j = tid - sl * kRank;
+      fold::dot_slice(bcol, X, d, nv, d, sl, part + sl * (Hkv + 1) * kRank + j, kRank);
+    }
+  } else {
+    for (int task = tid; task < ns * kRank; task += nt) {
+      const int sl = task / kRank, j = task - sl * kRank;
+      fold::proj_slice(p.basis, X, d, nv, d, j, sl, part + sl * (Hkv + 1) * kRank + j, kRank);
+    }
+  }
+  __syncthreads();
+  float amax = 0.f;
+  for (int m = tid; m < width; m += nt) {
+    const float v = __fmul_rn(fold::combine_slices(part + m, (Hkv + 1) * kRank, ns), p.c[m]);
+    qp[m] = v;
+    amax = fmaxf(amax, fabsf(v));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if (lane == 0) red[warp] = amax;
+  __syncthreads();
+  amax = 0.f;
+  for (int v = 0; v < (nt >> 5); v++) amax = fmaxf(amax, red[v]);
+  const float sigma = __fdiv_rn(amax, 127.f);
+  for (int m = tid; m < width; m += nt) {
+    const int8_t qc = fold::query_code(qp[m], sigma);
+    s_q8[m] = qc;
+    if (c == 0 && p.q8_out) p.q8_out[static_cast<int64_t>(b) * width + m] = qc;
+  }
+  if (app) {
+    const float* pk = part + Hkv * kRank;  // the appended key's slices
+    if (tid < kRank / 2) {
+      const int j0 = 2 * tid;
+      const int stride = (Hkv + 1) * kRank;
+      const int c0 = fold::sketch_code(fold::combine_slices(pk + j0, stride, ns), p.c[c * kRank + j0]);
+      const int c1 = fold::sketch_code(fold::combine_slices(pk + j0 + 1, stride, ns), p.c[c * kRank + j0 + 1]);
+      p.sketch[row * (Hkv * kRank / 2) + c * (kRank / 2) + tid] = static_cast<uint8_t>((c0 & 15) | ((c1 & 15) << 4));
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncthreads();
+    if (warp < 2) {
+      float rowv[16];
+#pragma unroll
+      for (int i = 0; i < 16; i++) {
+        const int x = lane + 32 * i;
+        rowv[i] = x < d ? bf16_bits_to_f32(kv_rows[warp * d + x]) : 0.f;
+      }
+      fold::encode_row_warp(rowv, d, (warp == 0 ? p.k8 : p.v8) + (row * Hkv + c) * d,
+                            (warp == 0 ? p.ks : p.vs) + row * Hkv + c);
+    }
+    const int64_t t = row - static_cast<int64_t>(b) * n_cap;
+    if (tid == 0 && c == 0 && t >= S && t < T - W) set_status(status, SKV_DEV_RANGE);  // would race the scan
+  }
+  __syncthreads();
+}
 
 // Request-wide barrier: the n-th barrier of a launch waits until the
 // request's arrival counter reaches n * C.
@@ -164,6 +285,8 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
   __shared__ uint32_t s_digit, s_above;
   __shared__ int s_before[2];
 
+  __shared__ __align__(16) int8_t s_q8[512];
+  __shared__ float s_red[kWarpsF];
   const int b = blockIdx.y, c = blockIdx.x, C = gridDim.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const bool pooled = MODE == SKV_SCORE_POOLED_BF16;
@@ -176,6 +299,11 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
   }
   if (T < 0) T = 0;
   int32_t* out = a.idx + static_cast<int64_t>(b) * a.max_rows;
+  const bool prepared = MODE == SKV_SCORE_SKETCH_INT4 && a.prep.q != nullptr;
+  unsigned* arrive = w.bar + 2 * b;
+  unsigned nbar = 0;
+  if (prepared)  // before the dense shortcut: the append and q8 happen either way
+    prepare_in_cta(a.prep, b, c, a.n_cap, T, a.S, a.W, reinterpret_cast<float*>(hist), s_q8, s_red, a.status);
   const bool dense = pooled ? T <= static_cast<int64_t>(ratio) * a.k + ratio - 1
                             : T <= static_cast<int64_t>(a.S) + a.W + a.k;
   if (dense) {  // every token; the same decision in every CTA of the request
@@ -192,8 +320,6 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
   if (c0 > hi) c0 = hi;
   const int64_t c1 = c0 + chunk < hi ? c0 + chunk : hi;
   const int len = static_cast<int>(c1 - c0);
-  unsigned* arrive = w.bar + 2 * b;
-  unsigned nbar = 0;
 
   // ---- 1. scores of the chunk into shared memory -----------------------------------
   unsigned kmax = 0u, kinv = 0u;
@@ -206,7 +332,7 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
   };
   if (MODE == SKV_SCORE_SKETCH_INT4) {
     constexpr int width = LPT * 32;
-    const int8_t* q8 = static_cast<const int8_t*>(a.query) + static_cast<int64_t>(b) * width;
+    const int8_t* q8 = prepared ? s_q8 : static_cast<const int8_t*>(a.query) + static_cast<int64_t>(b) * width;
     const uint8_t* rows = static_cast<const uint8_t*>(a.keys) + static_cast<int64_t>(b) * a.n_cap * (width / 2);
     auto emit = [&](int64_t t, int32_t sc) { keep(t, order_key_i32(sc)); };
     if (LPT == 8)
@@ -595,4 +721,36 @@ SKV_EXPORT int skv_score_select(int mode, int B, int width, const void* query, c
     default:
       return SKV_EINVAL;
   }
+}
+
+SKV_EXPORT int skv_decode_select(int B, int Hq, int Hkv, int d, int r, const uint16_t* q, const uint16_t* new_k,
+                                 const uint16_t* new_v, const float* basis, const float* c, const int64_t* new_rows,
+                                 uint8_t* sketch, int8_t* k8, uint16_t* k_scale, int8_t* v8, uint16_t* v_scale,
+                                 int64_t n_cap, const int32_t* lengths, int k, int S, int W, int32_t* idx,
+                                 int max_rows, int32_t* count, int8_t* q8_out, void* workspace,
+                                 size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  if (B < 0 || B > 65535 || n_cap < 0 || k < 1 || S < 0 || W < 1) return SKV_EINVAL;
+  if (Hq <= 0 || Hkv <= 0 || Hq % Hkv || r != fold::kRank || d <= 0 || d % 2) return SKV_EINVAL;
+  if (B == 0) return SKV_OK;
+  const int width = Hkv * fold::kRank;
+  if (width != 128 && width != 256 && width != 512) return SKV_EUNSUPPORTED;
+  const size_t ns = (d + 31) / 32;
+  if (d > 512 || d % 8 ||
+      (Hkv + 2ull) * d + (Hkv + 1ull) * fold::kRank * ns + static_cast<size_t>(width) > kBins)
+    return SKV_EUNSUPPORTED;
+  if (!q || !new_k || !new_v || !basis || !c || !new_rows || !sketch || !k8 || !k_scale || !v8 || !v_scale ||
+      !lengths || !idx || !count || !workspace)
+    return SKV_EINVAL;
+  if (!aligned16(sketch) || !aligned16(workspace)) return SKV_EINVAL;
+  if (workspace_bytes < ws_bytes(B)) return SKV_ENOMEM;
+  if (max_rows < static_cast<int64_t>(S) + k + W) return SKV_EINVAL;
+  Args a{SKV_SCORE_SKETCH_INT4, width, nullptr, sketch, n_cap, lengths, 1, k, S, W, idx, max_rows, count,
+         nullptr, dev_status, B};
+  a.prep = Prep{q, new_k, new_v, basis, c, new_rows, sketch, k8, reinterpret_cast<__half*>(k_scale), v8,
+                reinterpret_cast<__half*>(v_scale), q8_out, Hq, Hkv, d};
+  Ws w = ws_carve(workspace, B);
+  cudaStream_t st = as_stream(stream);
+  if (width == 128) return launch<SKV_SCORE_SKETCH_INT4, 4>(a, w, st);
+  if (width == 256) return launch<SKV_SCORE_SKETCH_INT4, 8>(a, w, st);
+  return launch<SKV_SCORE_SKETCH_INT4, 16>(a, w, st);
 }

@@ -4,6 +4,7 @@
 // token is scored through a rank-64 key sketch stored int4, computed on a
 // frozen basis; one pick per layer is shared by all KV heads.
 #include "common.cuh"
+#include "fold.cuh"
 
 namespace skv {
 namespace {
@@ -259,9 +260,9 @@ __global__ __launch_bounds__(kPrepThreads) void prepare_kernel(
     const int64_t* __restrict__ new_rows, uint8_t* __restrict__ sketch, int8_t* __restrict__ k8,
     __half* __restrict__ ks, int8_t* __restrict__ v8, __half* __restrict__ vs, int8_t* __restrict__ q8,
     float* __restrict__ sigma_out, float* __restrict__ qp_ws, unsigned* __restrict__ tickets) {
-  __shared__ float Qs[kMaxD], Ks[kMaxD];
-  __shared__ float part[4][kRank][2];
-  __shared__ int codes[kRank];
+  __shared__ float QK[2][kMaxD];                          // folded query, new key (head h)
+  __shared__ float part[kMaxD / fold::kSlice][2][kRank];  // per slice: query, key
+  __shared__ __align__(16) uint16_t kv_rows[2][kMaxD];    // the new K and V rows of head h
   __shared__ int last;
   __shared__ float red[32];
   const int h = blockIdx.x, b = blockIdx.y;
@@ -269,61 +270,66 @@ __global__ __launch_bounds__(kPrepThreads) void prepare_kernel(
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const uint16_t* qb = q + (static_cast<int64_t>(b) * Hq + static_cast<int64_t>(h) * G) * d;
   const uint16_t* kb = newk + (static_cast<int64_t>(b) * Hkv + h) * d;
-  for (int x = t; x < d; x += blockDim.x) {
-    float acc = 0.f;
-    for (int gg = 0; gg < G; gg++) acc = __fadd_rn(acc, bf16_bits_to_f32(qb[gg * d + x]));
-    Qs[x] = acc;
-    Ks[x] = bf16_bits_to_f32(kb[x]);
-  }
-  __syncthreads();
-  {
-    const int j = t & (kRank - 1), quarter = t >> 6;
-    const int per = (d + 3) / 4;
-    const int x0 = quarter * per, x1 = min(d, x0 + per);
-    float aq0 = 0.f, aq1 = 0.f, ak0 = 0.f, ak1 = 0.f;
-    int x = x0;
-    for (; x + 1 < x1; x += 2) {
-      const float p0 = __ldg(basis + x * kRank + j), p1 = __ldg(basis + (x + 1) * kRank + j);
-      aq0 = fmaf(p0, Qs[x], aq0);
-      ak0 = fmaf(p0, Ks[x], ak0);
-      aq1 = fmaf(p1, Qs[x + 1], aq1);
-      ak1 = fmaf(p1, Ks[x + 1], ak1);
-    }
-    if (x < x1) {
-      const float p0 = __ldg(basis + x * kRank + j);
-      aq0 = fmaf(p0, Qs[x], aq0);
-      ak0 = fmaf(p0, Ks[x], ak0);
-    }
-    part[quarter][j][0] = aq0 + aq1;
-    part[quarter][j][1] = ak0 + ak1;
-  }
-  __syncthreads();
+  // Every load first, so that the first-touch latencies overlap.
   const int64_t row = new_rows[b];
-  if (t < kRank) {
-    const int j = t;
-    const float qp = (part[0][j][0] + part[1][j][0]) + (part[2][j][0] + part[3][j][0]);
-    const float s = (part[0][j][1] + part[1][j][1]) + (part[2][j][1] + part[3][j][1]);
-    const float cj = c[h * kRank + j];
-    codes[j] = (cj != 0.f) ? rint_clamp(__fdiv_rn(s, cj), -8, 7) : 0;
-    qp_ws[static_cast<int64_t>(b) * Hkv * kRank + h * kRank + j] = __fmul_rn(qp, cj);
+  for (int u = t; u < 2 * (d / 8); u += blockDim.x) {
+    const int which = u / (d / 8), piece = u - which * (d / 8);
+    const uint16_t* src = (which == 0 ? newk : newv) + (static_cast<int64_t>(b) * Hkv + h) * d + 8 * piece;
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(
+                     __cvta_generic_to_shared(&kv_rows[which][8 * piece]))),
+                 "l"(src)
+                 : "memory");
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  const int ns = fold::n_slices(d);
+  constexpr int kTasks = 2;  // slice tasks per thread held in registers (d <= 256)
+  float bcol[kTasks][fold::kSlice];
+  const bool held = ns * kRank <= kTasks * kPrepThreads;
+#pragma unroll
+  for (int k = 0; k < kTasks; k++) {
+    const int task = t + k * kPrepThreads;
+    if (held && task < ns * kRank) fold::load_slice(basis, d, task % kRank, task / kRank, bcol[k]);
+  }
+  for (int x = t; x < d; x += blockDim.x) {
+    QK[0][x] = fold::group_sum(qb, G, d, x);
+    QK[1][x] = bf16_bits_to_f32(kb[x]);
   }
   __syncthreads();
-  if (t < kRank / 2)
-    sketch[row * (Hkv * kRank / 2) + h * (kRank / 2) + t] =
-        static_cast<uint8_t>((codes[2 * t] & 15) | ((codes[2 * t + 1] & 15) << 4));
-  if (warp < 2) {  // int8 rows of the new K (warp 0) and V (warp 1) of head h
-    const uint16_t* src = (warp == 0 ? newk : newv) + (static_cast<int64_t>(b) * Hkv + h) * d;
-    float amax = 0.f;
-    for (int x = lane; x < d; x += 32) amax = fmaxf(amax, fabsf(bf16_bits_to_f32(src[x])));
+  if (held) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const __half sh = __float2half_rn(__fdiv_rn(amax, 127.f));
-    const float sf = __half2float(sh);
-    const bool ok = (sf != 0.f) && isfinite(sf);
-    int8_t* dst = (warp == 0 ? k8 : v8) + (row * Hkv + h) * d;
-    for (int x = lane; x < d; x += 32)
-      dst[x] = static_cast<int8_t>(ok ? rint_clamp(__fdiv_rn(bf16_bits_to_f32(src[x]), sf), -127, 127) : 0);
-    if (lane == 0) (warp == 0 ? ks : vs)[row * Hkv + h] = sh;
+    for (int k = 0; k < kTasks; k++) {
+      const int task = t + k * kPrepThreads;
+      if (task < ns * kRank)
+        fold::dot_slice(bcol[k], &QK[0][0], kMaxD, 2, d, task / kRank, &part[task / kRank][0][task % kRank], kRank);
+    }
+  } else {
+    for (int task = t; task < ns * kRank; task += blockDim.x) {
+      const int sl = task / kRank, j = task - sl * kRank;
+      fold::proj_slice(basis, &QK[0][0], kMaxD, 2, d, j, sl, &part[sl][0][j], kRank);
+    }
+  }
+  __syncthreads();
+  if (t < kRank) {
+    const float cj = c[h * kRank + t];
+    qp_ws[static_cast<int64_t>(b) * Hkv * kRank + h * kRank + t] =
+        __fmul_rn(fold::combine_slices(&part[0][0][t], 2 * kRank, ns), cj);
+  }
+  if (t < kRank / 2) {
+    const int j0 = 2 * t;
+    const int c0 = fold::sketch_code(fold::combine_slices(&part[0][1][j0], 2 * kRank, ns), c[h * kRank + j0]);
+    const int c1 = fold::sketch_code(fold::combine_slices(&part[0][1][j0 + 1], 2 * kRank, ns), c[h * kRank + j0 + 1]);
+    sketch[row * (Hkv * kRank / 2) + h * (kRank / 2) + t] = static_cast<uint8_t>((c0 & 15) | ((c1 & 15) << 4));
+  }
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  __syncthreads();
+  if (warp < 2) {  // int8 rows of the new K (warp 0) and V (warp 1) of head h
+    float rowv[16];
+#pragma unroll
+    for (int i = 0; i < 16; i++) {
+      const int x = lane + 32 * i;
+      rowv[i] = x < d ? bf16_bits_to_f32(kv_rows[warp][x]) : 0.f;
+    }
+    fold::encode_row_warp(rowv, d, (warp == 0 ? k8 : v8) + (row * Hkv + h) * d, (warp == 0 ? ks : vs) + row * Hkv + h);
   }
   // Folded query: the request's last CTA quantises all heads with one scale.
   __threadfence();
@@ -353,8 +359,7 @@ __global__ __launch_bounds__(kPrepThreads) void prepare_kernel(
     tickets[b] = 0u;
   }
   for (int m = t; m < width; m += blockDim.x) {
-    const int v = (sigma != 0.f) ? rint_clamp(__fdiv_rn(__ldcg(qpb + m), sigma), -127, 127) : 0;
-    q8[static_cast<int64_t>(b) * width + m] = static_cast<int8_t>(v);
+    q8[static_cast<int64_t>(b) * width + m] = fold::query_code(__ldcg(qpb + m), sigma);
   }
 }
 
@@ -371,7 +376,7 @@ SKV_EXPORT int skv_decode_prepare(const uint16_t* q, const uint16_t* new_k, cons
                                   const int64_t* new_rows, uint8_t* sketch, int8_t* k8, uint16_t* k_scale,
                                   int8_t* v8, uint16_t* v_scale, int8_t* q8, float* sigma, void* workspace,
                                   size_t workspace_bytes, void* stream) {
-  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || r != kRank || d <= 0 || d > kMaxD || Hkv > 65535)
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || r != kRank || d <= 0 || d % 8 || d > kMaxD || Hkv > 65535)
     return SKV_EINVAL;
   if (B == 0) return SKV_OK;
   if (!q || !new_k || !new_v || !basis || !c || !new_rows || !sketch || !k8 || !k_scale || !v8 || !v_scale || !q8 ||

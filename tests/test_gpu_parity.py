@@ -515,3 +515,61 @@ def test_score_select_pooled_ratio1_raw_indexer_keys(skv, orc):
         kth = np.sort(ref["fscore"][b, :L[b]])[::-1][k - 1]
         for t in set(gi[b, :gc[b]].tolist()) ^ set(ri[b, :rc[b]].tolist()):
             assert abs(ref["fscore"][b, t] - kth) <= 1e-3 * abs(kth)
+
+
+@pytest.mark.parametrize("lengths,Hq,Hkv", [([9000, 5000, 3136, 3137], 24, 4), ([40000, 2000], 16, 2)])
+def test_decode_select_equals_prepare_then_select(skv, orc, lengths, Hq, Hkv):
+    """The one-launch prepare + select gives the same bits as decode_prepare
+    followed by score_select: folded query, appended sketch and int8 rows,
+    selection; and the selection equals the oracle's on those bytes."""
+    B, d, r, k, S, W = len(lengths), 256, 64, 2048, 64, 1024
+    x = wl.sketch_inputs_cpu(B, lengths, Hq, Hkv, d, r, seed=71 + B)
+    Tcap = int(max(lengths))
+    L = x["lengths"]
+    sk0 = orc.sketch_project(x["K"].reshape(B * Tcap, Hkv, d), x["basis"], x["c"])["q4"].reshape(B, Tcap, -1)
+    k80, ks0 = orc.quant_int8_rows(x["K"].reshape(B * Tcap, Hkv, d))
+    v80, vs0 = orc.quant_int8_rows(x["V"].reshape(B * Tcap, Hkv, d))
+    rng = np.random.default_rng(5)
+    nk = wl.to_bf16_bits(wl.lowrank_rows(rng, B * Hkv, x["basis"]).reshape(B, Hkv, d))
+    nv = wl.to_bf16_bits(rng.standard_normal((B, Hkv, d)).astype(np.float32))
+    new_rows = (np.arange(B) * Tcap + (L - 1)).astype(np.int64)
+    U, c = T.dev(x["basis"]), T.dev(x["c"])
+    max_rows = S + k + W
+
+    def state():
+        return (T.dev(sk0.copy()), T.dev(k80), T.f16_dev(ks0), T.dev(v80), T.f16_dev(vs0))
+
+    # two launches
+    skA, k8A, ksA, v8A, vsA = state()
+    q8A = torch.zeros((B, Hkv * r), dtype=torch.int8, device="cuda")
+    pws = torch.zeros((skv.decode_prepare_workspace_size(B, Hkv),), dtype=torch.uint8, device="cuda")
+    skv.decode_prepare(T.bf16_dev(x["q"]), T.bf16_dev(nk), T.bf16_dev(nv), U, c, T.dev(new_rows),
+                       skA.view(B * Tcap, -1), k8A.view(B * Tcap, Hkv, d), ksA, v8A.view(B * Tcap, Hkv, d), vsA, q8A,
+                       pws)
+    idxA = torch.zeros((B, max_rows), dtype=torch.int32, device="cuda")
+    cntA = torch.zeros((B,), dtype=torch.int32, device="cuda")
+    tws = torch.zeros((skv.score_select_workspace_size(B),), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    skv.score_select(skv.SKETCH_INT4, q8A, skA, T.dev(L), k, idxA, cntA, tws, S=S, W=W, status=st)
+    # one launch
+    skB, k8B, ksB, v8B, vsB = state()
+    q8B = torch.zeros((B, Hkv * r), dtype=torch.int8, device="cuda")
+    idxB = torch.full((B, max_rows), -3, dtype=torch.int32, device="cuda")
+    cntB = torch.zeros((B,), dtype=torch.int32, device="cuda")
+    for _ in range(2):  # the workspace is reusable without clearing
+        skv.decode_select(T.bf16_dev(x["q"]), T.bf16_dev(nk), T.bf16_dev(nv), U, c, T.dev(new_rows), skB,
+                          k8B.view(B * Tcap, Hkv, d), ksB, v8B.view(B * Tcap, Hkv, d), vsB, T.dev(L), k, idxB, cntB,
+                          tws, S=S, W=W, q8_out=q8B, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for a_, b_ in ((q8A, q8B), (skA, skB), (k8A, k8B), (ksA, ksB), (v8A, v8B), (vsA, vsB), (cntA, cntB)):
+        np.testing.assert_array_equal(T.host(a_), T.host(b_))
+    gi, gc = T.host(idxB), T.host(cntB)
+    ai = T.host(idxA)
+    for b in range(B):
+        np.testing.assert_array_equal(gi[b, :gc[b]], ai[b, :gc[b]])
+    sc = orc.index_score(orc.SKETCH_INT4, T.host(q8B), T.host(skB), L, S=S, W=W)
+    ri, rc = orc.topk_select(sc["okey"], L, k, S=S, W=W)
+    np.testing.assert_array_equal(gc, rc)
+    for b in range(B):
+        np.testing.assert_array_equal(gi[b, :gc[b]], ri[b, :rc[b]])
