@@ -220,6 +220,11 @@ __global__ __launch_bounds__(kThreads, 2) void attend_kernel(AttendArgs a) {
   const int pair = warp >> 1, e = warp & 1;  // e: which half of the head dimension
   const int g = lane >> 2, c = lane & 3;
 
+  // The query and the barriers do not depend on the kernel before this one
+  // (the selection); everything else does.
+  if (threadIdx.x < kPairs * kStages) mbar_init(&bars[threadIdx.x / kStages][threadIdx.x % kStages], 64);
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  grid_dependency_wait();
   int n = a.count[b];
   n = n < 0 ? 0 : (n > a.max_rows ? a.max_rows : n);
   const int r0 = split * a.rows_per_split;
@@ -264,9 +269,7 @@ __global__ __launch_bounds__(kThreads, 2) void attend_kernel(AttendArgs a) {
     cp_async_arrive(&bars[pair][stage]);
   };
 
-  // ---- barriers, then the pair's first tiles go out at once ---------------------
-  if (threadIdx.x < kPairs * kStages) mbar_init(&bars[threadIdx.x / kStages][threadIdx.x % kStages], 64);
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  // ---- the pair's first tiles go out at once ------------------------------------
   __syncthreads();
   for (int it = 0; it < kStages && it < my_tiles; it++) {
     const int tb = (pair + kPairs * it) * kTileRows;
@@ -597,6 +600,7 @@ int occupancy() {
   static int cached = -1;
   if (cached < 0) {
     int per_sm = 0;
+    prefer_max_smem(attend_kernel<KV>);
     if (cudaFuncSetAttribute(attend_kernel<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(dyn_smem<KV>())) != cudaSuccess ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attend_kernel<KV>, kThreads, dyn_smem<KV>()) !=
@@ -702,10 +706,23 @@ SKV_EXPORT int skv_sparse_attend_decode(int kv_kind, int B, int Hq, int Hkv, int
   a.part = reinterpret_cast<float*>(static_cast<char*>(workspace) + p.ticket_bytes);
   a.out = out;
   a.status = dev_status;
-  dim3 grid(p.nsplit, p.gy, B);
-  if (kv_kind == SKV_KV_INT8)
-    attend_kernel<SKV_KV_INT8><<<grid, kThreads, dyn_smem<SKV_KV_INT8>(), as_stream(stream)>>>(a);
-  else
-    attend_kernel<SKV_KV_BF16><<<grid, kThreads, dyn_smem<SKV_KV_BF16>(), as_stream(stream)>>>(a);
-  return launch_status();
+  // Launched with programmatic stream serialization: the CTAs may start (and
+  // set up) while the selection that produces `rows` is still finishing.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.nsplit, p.gy, B);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kv_kind == SKV_KV_INT8 ? dyn_smem<SKV_KV_INT8>() : dyn_smem<SKV_KV_BF16>();
+  cfg.stream = as_stream(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = kv_kind == SKV_KV_INT8 ? cudaLaunchKernelEx(&cfg, attend_kernel<SKV_KV_INT8>, a)
+                                               : cudaLaunchKernelEx(&cfg, attend_kernel<SKV_KV_BF16>, a);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return SKV_ECUDA;
+  }
+  return SKV_OK;
 }

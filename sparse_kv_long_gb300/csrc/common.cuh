@@ -35,6 +35,25 @@ inline int sm_count() {
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// All per-step kernels ask for the largest shared-memory carveout, so an SM
+// does not have to re-partition L1 / shared memory between consecutive kernels.
+template <typename K>
+inline void prefer_max_smem(K kernel) {
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           static_cast<int>(cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
+    cudaGetLastError();
+}
+
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream serialization attribute may start while the previous kernel in the
+// stream runs; it must call grid_dependency_wait() before touching anything
+// that kernel writes.  The previous kernel lets it start early with
+// allow_dependent_launch().
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_dependent_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void set_status(int32_t* st, unsigned bits) {
   if (st) atomicOr(reinterpret_cast<unsigned*>(st), bits);
 }

@@ -287,6 +287,7 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
 
   __shared__ __align__(16) int8_t s_q8[512];
   __shared__ float s_red[kWarpsF];
+  allow_dependent_launch();  // the attention that follows may set up meanwhile
   const int b = blockIdx.y, c = blockIdx.x, C = gridDim.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const bool pooled = MODE == SKV_SCORE_POOLED_BF16;
@@ -640,6 +641,7 @@ int launch(const Args& a, Ws w, cudaStream_t st) {
   auto kernel = score_select_kernel<MODE, LPT>;
   static bool configured = false;
   if (!configured) {
+    prefer_max_smem(kernel);
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kKeyBudget)) !=
         cudaSuccess) {
       cudaGetLastError();
