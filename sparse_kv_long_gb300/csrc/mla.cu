@@ -14,16 +14,19 @@
 // chunk:
 //   * CTA r gathers dims [256 r, 256 r + 320) of each row (fp8 -> fp16, exact)
 //     into a 128-byte-swizzled tile that serves both products;
-//   * it computes the partial logits over its share of the contraction
-//     (dims [0, 320) and [320, 576)), sends them to its peer through
-//     distributed shared memory and adds the peer's (a + b on both sides, so
-//     both hold the same logits and the same softmax);
+//   * its share of the query (dims [0, 320) or [320, 576)) sits in tensor
+//     memory as the A operand of the logit product, so only the row tile is
+//     read from shared memory by each MMA;
+//   * it computes the partial logits over its share of the contraction, each
+//     softmax warp ships its 32 heads' partials to the peer with one bulk
+//     copy (completion counted on the peer's barrier) and adds the peer's
+//     (a + b on both sides, so both hold the same logits and softmax);
 //   * it accumulates O for its half of the value dims ([0, 256) or
 //     [256, 512)) in tensor memory.
 // Roles in a CTA: warp 0 issues tcgen05.mma (one thread), warps 1-3 gather
-// rows, warps 4-7 own one head each (tensor-memory lane = head) for the
-// online softmax and the epilogue.  Rows are split across clusters; the splits
-// are merged in a fixed order, so the result is deterministic.
+// rows into a 3-deep ring, warps 4-7 own one head each (tensor-memory lane =
+// head) for the online softmax and the epilogue.  Rows are split across
+// clusters; the splits are merged in a fixed order (deterministic).
 #include <cstddef>
 
 #include "tc.cuh"
@@ -38,24 +41,26 @@ constexpr int kNr = 64;                         // rows per chunk (N of the logi
 constexpr int kSlice = 320;                     // dims gathered per CTA
 constexpr int kAtoms = kSlice / 64;             // 64-dim swizzle atoms per tile row
 constexpr int kPieces = kSlice / 16;            // 16-byte fp8 pieces per row and CTA
-constexpr int kQBytes = kAtoms * kH * 128;      // 80 KB
-constexpr int kKVBytes = kAtoms * kNr * 128;    // 40 KB
+constexpr int kBuf = 3;                         // gather ring depth
+constexpr int kKVBytes = kAtoms * kNr * 128;    // 40 KB per ring slot
 constexpr int kPBytes = kH * 128;               // 16 KB
-constexpr int kXBytes = kH * kNr * 4;           // 32 KB
+constexpr int kXBytes = kH * kNr * 4;           // 32 KB (one direction of the exchange)
 constexpr int kThreads = 256;
 constexpr int kProducers = 96;
 constexpr int kPerProducer = (kNr * kPieces + kProducers - 1) / kProducers;
-constexpr int kTmemCols = 512;                  // S double buffer at [0, 128), O at [256, 512)
+constexpr int kTmemCols = 512;                  // S [0, 64), Q [64, 224), O [256, 512)
+constexpr int kSCol = 0;
+constexpr int kQCol = 64;
 constexpr int kOCol = 256;
 constexpr float kRescaleLog2 = 8.f;             // rescale O only when the max grows by > 2^8
 
 struct Aux {
-  uint64_t kv_full[2], kv_empty[2], s_full[2], s_empty[2];
-  uint64_t p_full, pv_done, x_full, x_empty, mma_idle;
-  alignas(16) int32_t prow[2][kNr];  // pool rows of the chunk in buffer s (-1: none), staged by the gather warps
-  alignas(16) float kl[2][kNr];      // logit factor of each row: row scale x softmax scale x log2(e); 0 if no row
-  alignas(16) float madd[2][kNr];    // 0, or -inf for a missing row
-  alignas(16) float vsc[2][kNr];     // value factor: the row scale; 0 if no row
+  uint64_t kv_full[kBuf], kv_empty[kBuf];
+  uint64_t s_full, s_empty, p_full, pv_done, x_full, x_empty, mma_idle;
+  alignas(16) int32_t prow[kBuf][kNr];  // pool rows of the chunk in slot s (-1: none), staged by the gather warps
+  alignas(16) float kl[kBuf][kNr];      // logit factor of each row: row scale x softmax scale x log2(e); 0 if no row
+  alignas(16) float madd[kBuf][kNr];    // 0, or -inf for a missing row
+  alignas(16) float vsc[kBuf][kNr];     // value factor: the row scale; 0 if no row
   uint32_t tmem_base;
   int abort;
 };
@@ -63,9 +68,9 @@ struct Aux {
 // The softmax reads kl / madd / vsc as float4.
 static_assert(offsetof(Aux, kl) % 16 == 0 && offsetof(Aux, madd) % 16 == 0 && offsetof(Aux, vsc) % 16 == 0,
               "per-row factor arrays must be 16-byte aligned");
-static_assert((kQBytes + 2 * kKVBytes + kPBytes + kXBytes) % 16 == 0, "Aux must start 16-byte aligned");
+static_assert((kBuf * kKVBytes + kPBytes + 2 * kXBytes) % 16 == 0, "Aux must start 16-byte aligned");
 
-constexpr int kSmem = 1024 + kQBytes + 2 * kKVBytes + kPBytes + kXBytes + static_cast<int>(sizeof(Aux));
+constexpr int kSmem = 1024 + kBuf * kKVBytes + kPBytes + 2 * kXBytes + static_cast<int>(sizeof(Aux));
 
 struct MlaArgs {
   const uint16_t* q;
@@ -109,11 +114,11 @@ __device__ __forceinline__ bool named_sync_and(int id, int n, bool pred) {
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_kernel(MlaArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = smem_raw + ((1024u - (tc::smem_addr(smem_raw) & 1023u)) & 1023u);
-  unsigned char* sQ = sm;
-  unsigned char* sKV = sQ + kQBytes;
-  unsigned char* sP = sKV + 2 * kKVBytes;
-  float* sX = reinterpret_cast<float*>(sP + kPBytes);
-  Aux* ax = reinterpret_cast<Aux*>(sP + kPBytes + kXBytes);
+  unsigned char* sKV = sm;
+  unsigned char* sP = sKV + kBuf * kKVBytes;
+  float* sXin = reinterpret_cast<float*>(sP + kPBytes);   // the peer's partial logits
+  float* sXout = sXin + kH * kNr;                         // this CTA's, staged for the bulk copy
+  Aux* ax = reinterpret_cast<Aux*>(sP + kPBytes + 2 * kXBytes);
 
   const uint32_t rank = tc::cluster_rank(), peer = rank ^ 1u;
   const int split = blockIdx.y, b = blockIdx.z;
@@ -128,104 +133,94 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_ker
   const int r0 = split * per;
   const int r1 = min(n, r0 + per);
   const int nchunks = r1 > r0 ? (r1 - r0 + kNr - 1) / kNr : 0;
+  const int qdim0 = rank == 0 ? 0 : kSlice;          // this CTA's share of the contraction
+  const int qsteps = rank == 0 ? kSlice / 16 : (kD - kSlice) / 16;  // 16-dim MMA steps: 20 or 16
 
   if (tid == 0) {
-    for (int s = 0; s < 2; s++) {
+    for (int s = 0; s < kBuf; s++) {
       tc::bar_init(&ax->kv_full[s], kProducers);
       tc::bar_init(&ax->kv_empty[s], 1);
-      tc::bar_init(&ax->s_full[s], 1);
-      tc::bar_init(&ax->s_empty[s], kH);
     }
+    tc::bar_init(&ax->s_full, 1);
+    tc::bar_init(&ax->s_empty, kH);
     tc::bar_init(&ax->p_full, kH);
     tc::bar_init(&ax->pv_done, 1);
-    tc::bar_init(&ax->x_full, 1);   // one local arm per chunk + kXBytes of st.async data from the peer
-    tc::bar_init(&ax->x_empty, kH / 32);  // one remote arrive per peer softmax warp and chunk
+    tc::bar_init(&ax->x_full, 1);          // one local arm per chunk + kXBytes of bulk data from the peer
+    tc::bar_init(&ax->x_empty, kH / 32);   // one remote arrive per peer softmax warp and chunk
     tc::bar_init(&ax->mma_idle, 1);
     ax->abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-
-  // Query slice -> fp16, 128-byte-swizzled K-major tile (one 128 B row per head
-  // and 64-dim atom).  CTA 0 holds dims [0, 320), CTA 1 dims [320, 576).
-  const int qdim0 = rank == 0 ? 0 : kSlice;
-  const int qatoms = rank == 0 ? kAtoms : kAtoms - 1;
-  {
-    constexpr int kQBatch = 10;  // loads in flight per thread
-    const int nq = kH * qatoms * 8;
-    for (int u0 = tid; u0 < nq; u0 += kThreads * kQBatch) {
-      uint4 v[kQBatch];
-#pragma unroll
-      for (int m = 0; m < kQBatch; m++) {
-        const int u = u0 + m * kThreads;
-        if (u < nq) {
-          const int h = u / (qatoms * 8), cc = u % (qatoms * 8);
-          v[m] = ld_nc16(a.q + (static_cast<int64_t>(b) * kH + h) * kD + qdim0 + 8 * cc);
-        }
-      }
-#pragma unroll
-      for (int m = 0; m < kQBatch; m++) {
-        const int u = u0 + m * kThreads;
-        if (u < nq) {
-          const int h = u / (qatoms * 8), cc = u % (qatoms * 8);
-          const uint4 f = make_uint4(bf16x2_to_f16x2(v[m].x), bf16x2_to_f16x2(v[m].y), bf16x2_to_f16x2(v[m].z),
-                                     bf16x2_to_f16x2(v[m].w));
-          *reinterpret_cast<uint4*>(sQ + (cc >> 3) * (kH * 128) + h * 128 + (((cc & 7) ^ (h & 7)) << 4)) = f;
-        }
-      }
-    }
-  }
-  tc::fence_async_smem();
   if (warp == 0) tc::tmem_alloc<kTmemCols>(&ax->tmem_base);
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
-  tc::cluster_sync();  // the peer's barriers exist before any remote access
   const uint32_t tm = ax->tmem_base;
+
+  // Query share -> fp16 -> tensor memory: softmax thread h writes head h's
+  // row (lane h), columns kQCol + c holding dims 2c, 2c + 1 of the share.
+  if (warp >= 4) {
+    const int h = tid - 128;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const uint16_t* qrow = a.q + (static_cast<int64_t>(b) * kH + h) * kD + qdim0;
+    for (int c0 = 0; c0 < qsteps * 8; c0 += 32) {  // 32 columns = 64 dims per store
+      uint4 v[8];
+#pragma unroll
+      for (int m = 0; m < 8; m++) v[m] = ld_nc16(qrow + 2 * c0 + 8 * m);
+      uint32_t r[32];
+#pragma unroll
+      for (int m = 0; m < 8; m++) {
+        r[4 * m] = bf16x2_to_f16x2(v[m].x);
+        r[4 * m + 1] = bf16x2_to_f16x2(v[m].y);
+        r[4 * m + 2] = bf16x2_to_f16x2(v[m].z);
+        r[4 * m + 3] = bf16x2_to_f16x2(v[m].w);
+      }
+      tc::tmem_st32(tm + lane_base + kQCol + c0, r);
+    }
+    tc::tmem_wait_st();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  tc::cluster_sync();  // the peer's barriers exist before any remote access
   volatile int* abort = &ax->abort;
 
   if (warp == 0) {
     // ---------------- MMA issue (one thread) ----------------
     if (lane == 0 && nchunks > 0) {
-      const uint32_t aQ = tc::smem_addr(sQ), aKV = tc::smem_addr(sKV), aP = tc::smem_addr(sP);
+      const uint32_t aKV = tc::smem_addr(sKV), aP = tc::smem_addr(sP);
       constexpr uint32_t id_qk = tc::idesc_f16(kH, kNr, 0);
       constexpr uint32_t id_pv = tc::idesc_f16(kH, 256, 1);
-      auto issue_qk = [&](int i) {
-        const uint32_t kv = aKV + (i & 1) * kKVBytes;
-        const uint32_t d = tm + (i & 1) * kNr;
-        for (int qa = 0; qa < qatoms; qa++) {
-          const int ka = rank == 0 ? qa : qa + 1;  // CTA 1's tile starts at dim 256
-#pragma unroll
-          for (int kk = 0; kk < 4; kk++)
-            tc::mma_f16(d, tc::sw128_desc(aQ + qa * (kH * 128) + kk * 32, 16, 1024),
-                        tc::sw128_desc(kv + ka * (kNr * 128) + kk * 32, 16, 1024), id_qk, qa > 0 || kk > 0);
-        }
-      };
-      bool ok = tc::bar_wait(&ax->kv_full[0], 0, abort);
-      if (ok) {
-        tc::tc_fence_after();
-        issue_qk(0);
-        tc::mma_commit(&ax->s_full[0]);
-      }
-      for (int i = 0; ok && i < nchunks; i++) {
-        const int j = i + 1;
-        if (j < nchunks) {
-          ok = tc::bar_wait(&ax->kv_full[j & 1], (j >> 1) & 1, abort);
-          if (ok && j >= 2) ok = tc::bar_wait(&ax->s_empty[j & 1], ((j >> 1) - 1) & 1, abort);
+      bool ok = true;
+      for (int i = 0; ok && i <= nchunks; i++) {
+        if (i < nchunks) {  // S(i) = Q . K(i)^T, once slot i%3 is full and S(i-1) was read
+          const int s = i % kBuf;
+          ok = tc::bar_wait(&ax->kv_full[s], (i / kBuf) & 1, abort);
+          if (ok && i >= 1) ok = tc::bar_wait(&ax->s_empty, (i - 1) & 1, abort);
           if (!ok) break;
           tc::tc_fence_after();
-          issue_qk(j);
-          tc::mma_commit(&ax->s_full[j & 1]);
+          const uint32_t kv = aKV + s * kKVBytes;
+          for (int ks = 0; ks < qsteps; ks++) {
+            const int dim = qdim0 + 16 * ks - rank * 256;  // dim within this CTA's tile
+            tc::mma_f16_ts(tm + kSCol, tm + kQCol + 8 * ks,
+                           tc::sw128_desc(kv + (dim >> 6) * (kNr * 128) + ((dim & 63) >> 4) * 32, 16, 1024), id_qk,
+                           ks > 0);
+          }
+          tc::mma_commit(&ax->s_full);
         }
-        ok = tc::bar_wait(&ax->p_full, i & 1, abort);
-        if (!ok) break;
-        tc::tc_fence_after();
-        const uint32_t kv = aKV + (i & 1) * kKVBytes;
+        if (i >= 1) {  // O += P(i-1) . V(i-1)
+          const int j = i - 1, s = j % kBuf;
+          ok = tc::bar_wait(&ax->p_full, j & 1, abort);
+          if (!ok) break;
+          tc::tc_fence_after();
+          const uint32_t kv = aKV + s * kKVBytes;
 #pragma unroll
-        for (int kk = 0; kk < 4; kk++)  // 16 rows per step; value dims are the tile's first 4 atoms
-          tc::mma_f16(tm + kOCol, tc::sw128_desc(aP + kk * 32, 16, 1024),
-                      tc::sw128_desc(kv + kk * 2048, kNr * 128, 1024), id_pv, i > 0 || kk > 0);
-        tc::mma_commit(&ax->pv_done);
-        tc::mma_commit(&ax->kv_empty[i & 1]);
+          for (int kk = 0; kk < 4; kk++)  // 16 rows per step; value dims are the tile's first 4 atoms
+            tc::mma_f16(tm + kOCol, tc::sw128_desc(aP + kk * 32, 16, 1024),
+                        tc::sw128_desc(kv + kk * 2048, kNr * 128, 1024), id_pv, j > 0 || kk > 0);
+          tc::mma_commit(&ax->pv_done);
+          tc::mma_commit(&ax->kv_empty[s]);
+        }
       }
       // Nothing of this thread's may still be running when the tensor memory
       // is released (also after a wait that gave up).
@@ -249,8 +244,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_ker
     if (pt < kNr && nchunks > 0) ax->prow[0][pt] = row_of(0);
     named_sync(1, kProducers);
     for (int i = 0; i < nchunks; i++) {
-      const int s = i & 1;
-      const bool free_buf = i < 2 || tc::bar_wait(&ax->kv_empty[s], ((i >> 1) - 1) & 1, abort);
+      const int s = i % kBuf;
+      const bool free_buf = i < kBuf || tc::bar_wait(&ax->kv_empty[s], ((i / kBuf) - 1) & 1, abort);
       if (!named_sync_and(1, kProducers, free_buf)) break;  // the same decision in every producer
       uint4 v[kPerProducer];
 #pragma unroll
@@ -290,7 +285,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_ker
         ax->kl[s][pt] = have ? rsc * a.scale_log2 : 0.f;
         ax->madd[s][pt] = have ? 0.f : -INFINITY;
         ax->vsc[s][pt] = have ? rsc : 0.f;
-        ax->prow[s ^ 1][pt] = next;  // producers only; chunk i-1's ids are no longer read
+        ax->prow[(i + 1) % kBuf][pt] = next;  // producers only; slot (i+1)%3 held chunk i-2, long done
       }
       tc::fence_async_smem();
       tc::bar_arrive(&ax->kv_full[s]);
@@ -299,41 +294,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_ker
   } else {
     // ---------------- softmax + epilogue: thread = head ----------------
     const int h = tid - 128;
-    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const int wq = warp & 3;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * wq) << 16;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
-    float* xrow = sX + h * kNr;
+    float* xin = sXin + h * kNr;
+    float* xout = sXout + h * kNr;
     for (int i = 0; i < nchunks; i++) {
-      const int s = i & 1;
-      ok = __all_sync(0xffffffffu, tc::bar_wait(&ax->s_full[s], (i >> 1) & 1, abort));
+      const int s = i % kBuf;
+      ok = __all_sync(0xffffffffu, tc::bar_wait(&ax->s_full, i & 1, abort));
       if (!ok) break;
       tc::tc_fence_after();
       uint32_t ra[32], rb[32];
-      tc::tmem_ld32(tm + lane_base + s * kNr, ra);
-      tc::tmem_ld32(tm + lane_base + s * kNr + 32, rb);
+      tc::tmem_ld32(tm + lane_base + kSCol, ra);
+      tc::tmem_ld32(tm + lane_base + kSCol + 32, rb);
       tc::tmem_wait_ld();
       tc::tc_fence_before();
-      tc::bar_arrive(&ax->s_empty[s]);
-      // partial logits to the peer (asynchronous stores that count down the
-      // peer's receive barrier), then the peer's from this CTA's buffer
+      tc::bar_arrive(&ax->s_empty);
+      // This warp's 32 heads of partial logits: staged in shared memory, then
+      // one bulk copy into the peer's buffer (which counts down the peer's
+      // receive barrier); the peer's come into sXin the same way.
       if (h == 0) tc::bar_arrive_expect_tx(&ax->x_full, kXBytes);
       if (i >= 1) {
+        if (lane == 0) tc::wait_bulk_read();  // the previous copy has left sXout
         ok = __all_sync(0xffffffffu, tc::bar_wait(&ax->x_empty, (i - 1) & 1, abort, true));
         if (!ok) break;
       }
 #pragma unroll
       for (int c = 0; c < 16; c++) {
         const uint32_t* r = c < 8 ? &ra[4 * c] : &rb[4 * (c - 8)];
-        tc::st_async_remote16(xrow + 4 * (c ^ (h & 7)), &ax->x_full, peer,
-                              make_float4(__uint_as_float(r[0]), __uint_as_float(r[1]), __uint_as_float(r[2]),
-                                          __uint_as_float(r[3])));
+        *reinterpret_cast<float4*>(xout + 4 * (c ^ (h & 7))) =
+            make_float4(__uint_as_float(r[0]), __uint_as_float(r[1]), __uint_as_float(r[2]), __uint_as_float(r[3]));
+      }
+      tc::fence_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        const int off = 32 * wq * kNr;  // this warp's 32 heads
+        tc::bulk_copy_to_peer(sXin + off, sXout + off, 32 * kNr * 4, &ax->x_full, peer);
+        tc::commit_bulk();
       }
       ok = __all_sync(0xffffffffu, tc::bar_wait(&ax->x_full, i & 1, abort));
       if (!ok) break;
       float x[64];
 #pragma unroll
       for (int c = 0; c < 16; c++) {
-        const float4 o = *reinterpret_cast<const float4*>(xrow + 4 * (c ^ (h & 7)));
+        const float4 o = *reinterpret_cast<const float4*>(xin + 4 * (c ^ (h & 7)));
         const uint32_t* r = c < 8 ? &ra[4 * c] : &rb[4 * (c - 8)];
         x[4 * c] = __uint_as_float(r[0]) + o.x;
         x[4 * c + 1] = __uint_as_float(r[1]) + o.y;
@@ -404,6 +409,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_ker
       tc::tc_fence_before();
       tc::bar_arrive(&ax->p_full);
     }
+    if (lane == 0) tc::wait_bulk_done();  // this warp's copies into the peer have completed
     // epilogue: this CTA's 256 value dims of head h
     bool have_o = ok && nchunks > 0;
     if (have_o) {
@@ -445,7 +451,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_ker
     tc::tc_fence_after();
     tc::tmem_dealloc<kTmemCols>(tm);
   }
-  tc::cluster_sync();  // the peer's stores into this CTA's shared memory are done
+  tc::cluster_sync();  // the peer's copies into this CTA's shared memory are done
 }
 
 // Splits of one (request, head) combined in split order.

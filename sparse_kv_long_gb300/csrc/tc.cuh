@@ -132,6 +132,24 @@ __device__ __forceinline__ void st_async_remote16(const void* local, const uint6
       : "memory");
 }
 
+// Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory at
+// `src` to the same offset as `dst_local` in CTA `rank`'s shared memory; on
+// arrival it completes `bytes` of transaction count on that CTA's barrier at
+// the offset of `bar_local`.  Issued by one thread; commit_bulk() closes the
+// group and wait_bulk_read() waits until the source may be overwritten.
+__device__ __forceinline__ void bulk_copy_to_peer(const void* dst_local, const void* src, uint32_t bytes,
+                                                  const uint64_t* bar_local, uint32_t rank) {
+  asm volatile(
+      "{\n.reg .b32 rd, rb;\nmapa.shared::cluster.u32 rd, %0, %3;\nmapa.shared::cluster.u32 rb, %2, %3;\n"
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [rd], [%1], %4, [rb];\n}\n" ::"r"(
+          smem_addr(dst_local)),
+      "r"(smem_addr(src)), "r"(smem_addr(bar_local)), "r"(rank), "r"(bytes)
+      : "memory");
+}
+__device__ __forceinline__ void commit_bulk() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void wait_bulk_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void wait_bulk_done() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // Arrive on a local barrier and add `bytes` to the transaction count its
 // current phase waits for.
 __device__ __forceinline__ void bar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
@@ -212,6 +230,17 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64
       "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1 : 0));
+}
+
+// One elected thread: D[tmem] (+)= A[tmem] . B[smem].  A in tensor memory:
+// lane i holds row i, 32-bit column c holds elements 2c (low half) and 2c + 1
+// (high half) of the K dimension.
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                           bool accumulate) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1 : 0));
 }
 
 // The barrier's phase completes when every earlier tcgen05 operation of this
