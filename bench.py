@@ -256,16 +256,18 @@ class SketchWorkloadGPU:
         self.status = torch.zeros((1,), dtype=torch.int32, device=dev)
         torch.cuda.synchronize()
 
-    KERNELS_PER_LAYER = 2  # a1 + int8 append + a2 + a3 + a4 in one launch, a6
+    KERNELS_PER_LAYER = 3  # a1 + int8 append + a2 fused, a3 + a4 fused, a6
 
     def layer(self, l, marks=None):
         skv, st = self.skv, self.status
         ev = (lambda name: marks(l, name)) if marks else (lambda name: None)
         ev("start")
+        skv.decode_prepare(self.q[l], self.newk[l], self.newv[l], self.U, self.c, self.new_rows,
+                           self.sk[l].view(W_B * W_T, -1), self.k8[l], self.ks[l], self.v8[l], self.vs[l], self.q8,
+                           self.pws, sigma=self.sigma)
         ev("scan0")
-        skv.decode_select(self.q[l], self.newk[l], self.newv[l], self.U, self.c, self.new_rows, self.sk[l],
-                          self.k8[l], self.ks[l], self.v8[l], self.vs[l], self.lengths, W_K, self.idx, self.cnt,
-                          self.tws, S=W_S, W=W_W, q8_out=self.q8, status=st)
+        skv.score_select(skv.SKETCH_INT4, self.q8, self.sk[l], self.lengths, W_K, self.idx, self.cnt, self.tws,
+                         S=W_S, W=W_W, status=st)
         ev("scan1")
         ev("attn0")
         skv.sparse_attend_decode(skv.KV_INT8, self.q[l], self.k8[l], self.v8[l], self.idx, self.cnt,
@@ -412,10 +414,10 @@ def run_gpu(args):
                               f"{step_bytes / 1e9:.2f} GB read per step", layers=L),
         "tokens_per_s": tokens_per_s, "hbm_gbs": step_gbs,
         "parallelism": "replicas only" if world > 1 else "single GPU",
-        "kernel_us": {"decode_select_int4": scan_us, "sparse_attend_int8": attn_us},
+        "kernel_us": {"score_select_int4": scan_us, "sparse_attend_int8": attn_us},
         "roofline": {"bound": "hbm", "achieved": scan_gbs, "peak": hbm_peak, "unit": "GB/s",
                      "frac": scan_gbs / hbm_peak, "traffic": measured_traffic("score_select"),
-                     "kernel": "score_select_kernel (query fold + append + scan + top-k)",
+                     "kernel": "score_select_kernel (scan + top-k)",
                      "peak_source": peak_src, "bytes_per_launch": scan_bytes,
                      "bytes_rule": f"{SCAN_BYTES_PER_CAND} B sketch row per candidate token x {W_B} x {n_cand}"},
         "roofline_attend": {"bound": "hbm", "achieved": attn_gbs, "peak": hbm_peak, "unit": "GB/s",
@@ -489,7 +491,7 @@ class MlaLruWorkloadGPU:
         self.bt = bt.to(dev)
         self.lengths = torch.full((B,), T, dtype=torch.int32, device=dev)
         self.pool, self.keys, self.hosts, self.q = [], [], [], []
-        self.stamp, self.slot_tok, self.tok_slot, self.step_ctr = [], [], [], []
+        self.stamp, self.slot_tok, self.tok_slot, self.order, self.step_ctr = [], [], [], [], []
         for l in range(layers):
             pool = torch.zeros((B * self.rpr, D), dtype=torch.uint8, device=dev)
             host = HostTier(skv, B * T * D)
@@ -506,6 +508,7 @@ class MlaLruWorkloadGPU:
             self.stamp.append(torch.full((B, self.SLOTS), -1, dtype=torch.int64, device=dev))
             self.slot_tok.append(torch.full((B, self.SLOTS), -1, dtype=torch.int32, device=dev))
             self.tok_slot.append(torch.full((B, T), -1, dtype=torch.int32, device=dev))
+            self.order.append(torch.arange(self.SLOTS, dtype=torch.int32, device=dev).repeat(B, 1).contiguous())
             self.step_ctr.append(torch.zeros((2,), dtype=torch.int32, device=dev))
         q0 = torch.randn((layers, B, self.DI), generator=gen, device=dev)
         self.qidx_seq = drift_walk(torch, gen, q0, n_steps, eta)   # [steps][L][B][128]
@@ -531,7 +534,7 @@ class MlaLruWorkloadGPU:
                          self.tws, ratio=1, status=st)
         ev("res0")
         skv.resolve_rows_lru(self.lengths, self.idx, self.cnt, self.step_ctr[l], self.PAGE, self.bt, self.hot_base,
-                             self.hot_stride, self.stamp[l], self.slot_tok[l], self.tok_slot[l],
+                             self.hot_stride, self.stamp[l], self.slot_tok[l], self.tok_slot[l], self.order[l],
                              self.hosts[l].alias, self.pool[l], self.rows, self.nmiss[l], workspace=self.rws,
                              status=st)
         ev("att0")

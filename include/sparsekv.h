@@ -479,7 +479,11 @@ int skv_resolve_rows_clock(int B, int64_t t_cap, const int32_t *lengths, int S, 
  * hot(b) = hot_base + b*hot_stride.  Row ids are absolute pool rows
  * (attention with req_row_stride = 0).
  *   state: stamp int64 [B][n_slots] (-1 empty), slot_token int32
- *          [B][n_slots] (-1 none), token_slot int32 [B][t_cap] (-1 none)
+ *          [B][n_slots] (-1 none), token_slot int32 [B][t_cap] (-1 none),
+ *          order int32 [B][n_slots]: the slots by ascending (stamp, slot),
+ *          maintained by the call (start: 0, 1, ..., n_slots - 1, since all
+ *          stamps start at -1), so the victims are read off its front instead
+ *          of sorting every step
  *   block_table int32 [B][n_pages]; host u8 [B][t_cap][row_bytes] (device
  *   alias); pool u8 [n_pool_rows][row_bytes]
  *   step   int32 [2] (device), as for skv_resolve_rows_clock: step[0] is the
@@ -496,7 +500,7 @@ int skv_resolve_rows_clock(int B, int64_t t_cap, const int32_t *lengths, int S, 
 int skv_resolve_rows_lru(int B, int64_t t_cap, const int32_t *lengths, int page,
                          const int32_t *block_table, int64_t n_pages, int64_t hot_base,
                          int64_t hot_stride, int n_slots, int32_t *step, int64_t *stamp,
-                         int32_t *slot_token, int32_t *token_slot, const uint8_t *host,
+                         int32_t *slot_token, int32_t *token_slot, int32_t *order, const uint8_t *host,
                          uint8_t *pool, int64_t row_bytes, int64_t n_pool_rows,
                          const int32_t *idx, int max_rows, const int32_t *count,
                          int32_t *rows_out, int32_t *n_miss, void *workspace,

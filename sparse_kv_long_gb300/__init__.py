@@ -71,8 +71,8 @@ def _load():
                 "skv_resolve_workspace_size": ([i32, i32], sz),
                 "skv_resolve_rows_clock": ([i32, i64, P, i32, i32, i32, i32, i32, P, i32, P, P, P, P, P, P, P, P,
                                             P, P, P, P, i64, P, P, P, sz, P, P], i32),
-                "skv_resolve_rows_lru": ([i32, i64, P, i32, P, i64, i64, i64, i32, P, P, P, P, P, P, i64, i64, P,
-                                          i32, P, P, P, P, sz, P, P], i32),
+                "skv_resolve_rows_lru": ([i32, i64, P, i32, P, i64, i64, i64, i32, P, P, P, P, P, P, P, i64, i64,
+                                          P, i32, P, P, P, P, sz, P, P], i32),
                 "skv_quantize_int4_rows": ([P, i64, i32, i32, P, P, i64, i64, P], i32),
                 "skv_stream_read": ([P, sz, P, i32, P], i32),
                 "skv_host_register": ([P, sz, ctypes.POINTER(ctypes.c_void_p)], i32),
@@ -272,7 +272,7 @@ def resolve_rows_clock(lengths, idx, count, step, S, W, Hs, slot_token, ref, use
 
 
 def resolve_rows_lru(lengths, idx, count, step, page, block_table, hot_base, hot_stride, stamp, slot_token,
-                     token_slot, host, pool, rows_out, n_miss, workspace=None, status=None, stream=None):
+                     token_slot, order, host, pool, rows_out, n_miss, workspace=None, status=None, stream=None):
     """Block table + LRU hot buffer resolve (see skv_resolve_rows_lru).  step: int32 device tensor [2]
     (advanced by the call); host: uint8 tensor or int alias."""
     B, max_rows = idx.shape
@@ -282,7 +282,8 @@ def resolve_rows_lru(lengths, idx, count, step, page, block_table, hot_base, hot
     workspace = _resolve_ws(workspace, B, max_rows)
     _check("skv_resolve_rows_lru", _load().skv_resolve_rows_lru(
         B, t_cap, _ptr(lengths), page, _ptr(block_table), block_table.shape[1], int(hot_base), int(hot_stride),
-        n_slots, _ptr(step), _ptr(stamp), _ptr(slot_token), _ptr(token_slot), _addr(host), _ptr(pool), row_bytes,
+        n_slots, _ptr(step), _ptr(stamp), _ptr(slot_token), _ptr(token_slot), _ptr(order), _addr(host), _ptr(pool),
+        row_bytes,
         n_pool_rows, _ptr(idx), max_rows, _ptr(count), _ptr(rows_out), _ptr(n_miss), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream)))
     return rows_out, n_miss

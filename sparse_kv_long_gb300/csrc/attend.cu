@@ -600,7 +600,6 @@ int occupancy() {
   static int cached = -1;
   if (cached < 0) {
     int per_sm = 0;
-    prefer_max_smem(attend_kernel<KV>);
     if (cudaFuncSetAttribute(attend_kernel<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(dyn_smem<KV>())) != cudaSuccess ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attend_kernel<KV>, kThreads, dyn_smem<KV>()) !=

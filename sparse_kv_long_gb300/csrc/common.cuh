@@ -35,15 +35,6 @@ inline int sm_count() {
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// All per-step kernels ask for the largest shared-memory carveout, so an SM
-// does not have to re-partition L1 / shared memory between consecutive kernels.
-template <typename K>
-inline void prefer_max_smem(K kernel) {
-  if (cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                           static_cast<int>(cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
-    cudaGetLastError();
-}
-
 // Programmatic dependent launch: a kernel launched with the programmatic
 // stream serialization attribute may start while the previous kernel in the
 // stream runs; it must call grid_dependency_wait() before touching anything

@@ -384,6 +384,7 @@ struct LruArgs {
   int64_t* stamp;
   int32_t* slot_token;
   int32_t* token_slot;
+  int32_t* order;  // [B][n_slots]: the slots by ascending (stamp, slot)
   const uint8_t* host;
   uint8_t* pool;
   int64_t row_bytes, n_pool_rows;
@@ -397,24 +398,19 @@ struct LruArgs {
   int32_t* status;
 };
 
-int pow2_at_least(int n) {
-  int p = 1;
-  while (p < n) p <<= 1;
-  return p;
-}
-
 size_t lru_smem_bytes(int n_slots, int max_rows) {
-  return static_cast<size_t>(n_slots) * 8 + static_cast<size_t>(pow2_at_least(n_slots)) * 8 +
-         static_cast<size_t>(max_rows) * 8 + 64 * sizeof(int);
+  return static_cast<size_t>(n_slots) * 8 + static_cast<size_t>(n_slots) * 4 * 2 + static_cast<size_t>(max_rows) * 8 +
+         64 * sizeof(int);
 }
 
-__global__ __launch_bounds__(kResThreads) void lru_kernel(LruArgs a, int P) {
+__global__ __launch_bounds__(kResThreads) void lru_kernel(LruArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int ns = a.n_slots;
   int64_t* s_stamp = reinterpret_cast<int64_t*>(smem);
-  uint64_t* key = reinterpret_cast<uint64_t*>(s_stamp + ns);
-  int32_t* m_tok = reinterpret_cast<int32_t*>(key + P);
+  int32_t* s_order = reinterpret_cast<int32_t*>(s_stamp + ns);  // LRU order on entry
+  int32_t* s_new = s_order + ns;                                // victim slots, then the new order
+  int32_t* m_tok = s_new + ns;
   int32_t* m_pos = m_tok + a.max_rows;
   int* scr = reinterpret_cast<int*>(m_pos + a.max_rows);
 
@@ -478,58 +474,85 @@ __global__ __launch_bounds__(kResThreads) void lru_kernel(LruArgs a, int P) {
   }
   __syncthreads();
 
-  // Phase 2: victims = untouched slots by ascending (stamp, slot): bitonic
-  // sort of the P keys (stamp + 1) << 32 | slot; touched and padding slots
-  // sort last.
-  int nc = 0;
-  for (int base = 0; base < P; base += kResThreads) {
-    const int s = base + tid;
-    bool c = false;
-    if (s < P) {
-      uint64_t k = ~0ull;
-      if (s < ns && s_stamp[s] != step) {
-        k = (static_cast<uint64_t>(s_stamp[s] + 1) << 32) | static_cast<uint32_t>(s);
-        c = true;
-      }
-      key[s] = k;
+  // Phase 2: the victims are the first nm untouched slots of the LRU order
+  // (ascending (stamp, slot)).  A block scan over the order ranks the
+  // untouched slots; rank j < nm is the j-th victim.
+  int32_t* order = a.order + sbase;
+  for (int pos = tid; pos < ns; pos += kResThreads) {
+    int32_t v = order[pos];
+    if (v < 0 || v >= ns) {  // not a permutation of the slots: flag it and use the identity there
+      set_status(a.status, SKV_DEV_RANGE);
+      v = pos;
     }
-    nc += __syncthreads_count(c);
+    s_order[pos] = v;
   }
-  const bool ok = nc >= nm;
+  __syncthreads();
+  constexpr int kPer = 8;  // order positions per thread (n_slots <= 8192)
+  int ucnt = 0;
+  const int p0 = tid * kPer;
+  for (int u = 0; u < kPer; u++) {
+    const int pos = p0 + u;
+    if (pos < ns && s_stamp[s_order[pos]] != step) ucnt++;
+  }
+  int n_untouched;
+  int urank = block_exclusive_scan(ucnt, scr, &n_untouched);
+  const bool ok = n_untouched >= nm;
   if (!ok && tid == 0) set_status(a.status, SKV_DEV_COUNT);
   if (ok && nm > 0) {
-    for (int size = 2; size <= P; size <<= 1) {
-      for (int stride = size >> 1; stride > 0; stride >>= 1) {
-        for (int x = tid; x < P / 2; x += kResThreads) {
-          const int lo = 2 * x - (x & (stride - 1));
-          const int hi = lo + stride;
-          const bool up = (lo & size) == 0;
-          const uint64_t kl = key[lo], kh = key[hi];
-          if ((kl > kh) == up) {
-            key[lo] = kh;
-            key[hi] = kl;
-          }
+    // victims in LRU order; the untouched rest keeps its order at the front
+    for (int u = 0; u < kPer; u++) {
+      const int pos = p0 + u;
+      if (pos < ns) {
+        const int sl = s_order[pos];
+        if (s_stamp[sl] != step) {
+          if (urank < nm)
+            s_new[urank] = sl;  // victim urank
+          urank++;
         }
-        __syncthreads();
       }
     }
+    __syncthreads();
     // Phase 3: the i-th miss takes the i-th victim.
     for (int j = tid; j < nm; j += kResThreads) {
-      const int s = static_cast<int>(key[j] & 0xffffffffu);
+      const int sl = s_new[j];
       const int32_t tok = m_tok[j];
-      const int32_t old = a.slot_token[sbase + s];
+      const int32_t old = a.slot_token[sbase + sl];
       if (old >= 0 && old < a.t_cap) tslot[old] = -1;
-      a.slot_token[sbase + s] = tok;
-      tslot[tok] = s;
-      s_stamp[s] = step;
-      rows[m_pos[j]] = static_cast<int32_t>(hot + s);
+      a.slot_token[sbase + sl] = tok;
+      tslot[tok] = sl;
+      rows[m_pos[j]] = static_cast<int32_t>(hot + sl);
+      a.ws_tok[static_cast<int64_t>(b) * a.max_rows + j] = tok;  // the miss list for the fetch kernel
+      a.ws_row[static_cast<int64_t>(b) * a.max_rows + j] = static_cast<int32_t>(hot + sl);
     }
-    // the miss list for the fetch kernel
-    for (int j = tid; j < nm; j += kResThreads) {
-      a.ws_tok[static_cast<int64_t>(b) * a.max_rows + j] = m_tok[j];
-      a.ws_row[static_cast<int64_t>(b) * a.max_rows + j] =
-          static_cast<int32_t>(hot + static_cast<int64_t>(key[j] & 0xffffffffu));
+    __syncthreads();
+    for (int j = tid; j < nm; j += kResThreads) s_stamp[s_new[j]] = step;
+  }
+  __syncthreads();
+  {
+    // New order: the untouched slots in their old order, then every slot
+    // used this step (hits and victims, all with stamp = step) by slot index.
+    int keep = 0;
+    for (int u = 0; u < kPer; u++) {
+      const int pos = p0 + u;
+      if (pos < ns && s_stamp[s_order[pos]] != step) keep++;
     }
+    int n_keep;
+    int krank = block_exclusive_scan(keep, scr, &n_keep);
+    int used = 0;
+    for (int u = 0; u < kPer; u++) {
+      const int sl = p0 + u;
+      if (sl < ns && s_stamp[sl] == step) used++;
+    }
+    int n_used;
+    int rrank = block_exclusive_scan(used, scr, &n_used);
+    for (int u = 0; u < kPer; u++) {
+      const int pos = p0 + u;
+      if (pos < ns && s_stamp[s_order[pos]] != step) s_new[krank++] = s_order[pos];
+      const int sl = p0 + u;
+      if (sl < ns && s_stamp[sl] == step) s_new[n_keep + rrank++] = sl;
+    }
+    __syncthreads();
+    for (int pos = tid; pos < ns; pos += kResThreads) order[pos] = s_new[pos];
   }
   __syncthreads();
   for (int s = tid; s < ns; s += kResThreads) a.stamp[sbase + s] = s_stamp[s];
@@ -666,7 +689,8 @@ SKV_EXPORT int skv_resolve_rows_clock(int B, int64_t t_cap, const int32_t* lengt
 SKV_EXPORT int skv_resolve_rows_lru(int B, int64_t t_cap, const int32_t* lengths, int page,
                                     const int32_t* block_table, int64_t n_pages, int64_t hot_base,
                                     int64_t hot_stride, int n_slots, int32_t* step, int64_t* stamp,
-                                    int32_t* slot_token, int32_t* token_slot, const uint8_t* host, uint8_t* pool,
+                                    int32_t* slot_token, int32_t* token_slot, int32_t* order, const uint8_t* host,
+                                    uint8_t* pool,
                                     int64_t row_bytes, int64_t n_pool_rows, const int32_t* idx, int max_rows,
                                     const int32_t* count, int32_t* rows_out, int32_t* n_miss, void* workspace,
                                     size_t workspace_bytes, int32_t* dev_status, void* stream) {
@@ -678,14 +702,13 @@ SKV_EXPORT int skv_resolve_rows_lru(int B, int64_t t_cap, const int32_t* lengths
   if (!step) return SKV_EINVAL;
   if (hot_base + static_cast<int64_t>(B - 1) * hot_stride + n_slots > n_pool_rows || n_pool_rows > INT32_MAX)
     return SKV_EINVAL;
-  if (!lengths || !block_table || !stamp || !slot_token || !token_slot || !host || !pool || !idx || !count ||
-      !rows_out || !n_miss)
+  if (!lengths || !block_table || !stamp || !slot_token || !token_slot || !order || !host || !pool || !idx ||
+      !count || !rows_out || !n_miss)
     return SKV_EINVAL;
   if (!aligned16(host) || !aligned16(pool)) return SKV_EINVAL;
   if (!workspace || workspace_bytes < skv_resolve_workspace_size(B, max_rows)) return SKV_ENOMEM;
   int32_t* ws_tok = static_cast<int32_t*>(workspace);
   int32_t* ws_row = ws_tok + static_cast<size_t>(B) * max_rows;
-  const int P = pow2_at_least(n_slots);
   const size_t smem = lru_smem_bytes(n_slots, max_rows);
   static size_t configured = 0;
   if (smem > 48 * 1024 && smem > configured) {
@@ -697,10 +720,10 @@ SKV_EXPORT int skv_resolve_rows_lru(int B, int64_t t_cap, const int32_t* lengths
     configured = smem;
   }
   LruArgs a{t_cap, lengths, page, block_table, n_pages, hot_base, hot_stride, n_slots, step, stamp, slot_token,
-            token_slot, host, pool, row_bytes, n_pool_rows, idx, max_rows, count, rows_out, n_miss, ws_tok, ws_row,
-            dev_status};
+            token_slot, order, host, pool, row_bytes, n_pool_rows, idx, max_rows, count, rows_out, n_miss, ws_tok,
+            ws_row, dev_status};
   cudaStream_t st = as_stream(stream);
-  lru_kernel<<<B, kResThreads, smem, st>>>(a, P);
+  lru_kernel<<<B, kResThreads, smem, st>>>(a);
   const int per_cta = kFetchWarps * kRowsPerWarp;
   fetch_rows_kernel<<<dim3((max_rows + per_cta - 1) / per_cta, B), 32 * kFetchWarps, 0, st>>>(
       ws_tok, ws_row, n_miss, max_rows, t_cap, host, pool, row_bytes);

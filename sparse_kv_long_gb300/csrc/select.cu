@@ -641,7 +641,6 @@ int launch(const Args& a, Ws w, cudaStream_t st) {
   auto kernel = score_select_kernel<MODE, LPT>;
   static bool configured = false;
   if (!configured) {
-    prefer_max_smem(kernel);
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kKeyBudget)) !=
         cudaSuccess) {
       cudaGetLastError();

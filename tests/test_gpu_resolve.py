@@ -215,6 +215,7 @@ def test_lru_resolve_matches_oracle(skv, orc, n_slots, k, keep, where):
     g_stamp = torch.full((B, n_slots), -1, dtype=torch.int64, device="cuda")
     g_tok = torch.full((B, n_slots), -1, dtype=torch.int32, device="cuda")
     g_tslot = torch.full((B, t_cap), -1, dtype=torch.int32, device="cuda")
+    g_order = torch.arange(n_slots, dtype=torch.int32, device="cuda").repeat(B, 1).contiguous()
     g_bt, g_len = T.dev(bt), T.dev(lengths)
     g_step = torch.zeros((2,), dtype=torch.int32, device="cuda")
     hb = None
@@ -233,7 +234,7 @@ def test_lru_resolve_matches_oracle(skv, orc, n_slots, k, keep, where):
             nmiss = torch.zeros((B,), dtype=torch.int32, device="cuda")
             st = status_word()
             skv.resolve_rows_lru(g_len, T.dev(idx), T.dev(count), g_step, page, g_bt, hot_base, hot_stride, g_stamp,
-                                 g_tok, g_tslot, host_arg, g_pool, rows, nmiss, status=st)
+                                 g_tok, g_tslot, g_order, host_arg, g_pool, rows, nmiss, status=st)
             torch.cuda.synchronize()
             assert int(st.item()) == 0
             assert T.host(g_step).tolist() == [step + 1, 0]
@@ -247,6 +248,10 @@ def test_lru_resolve_matches_oracle(skv, orc, n_slots, k, keep, where):
             np.testing.assert_array_equal(T.host(g_tok), np.stack([s.slot_token for s in states]))
             np.testing.assert_array_equal(T.host(g_tslot), np.stack([s.token_slot for s in states]))
             np.testing.assert_array_equal(T.host(g_pool), pool)
+            # the maintained LRU order is the (stamp, slot) order of the oracle's stamps
+            for b in range(B):
+                st_b = states[b].stamp
+                np.testing.assert_array_equal(T.host(g_order)[b], np.lexsort((np.arange(n_slots), st_b)))
     finally:
         if hb is not None:
             hb.close()
@@ -261,12 +266,13 @@ def test_lru_too_few_slots_is_flagged(skv):
     stamp = torch.full((B, n_slots), -1, dtype=torch.int64, device="cuda")
     tok = torch.full((B, n_slots), -1, dtype=torch.int32, device="cuda")
     tslot = torch.full((B, t_cap), -1, dtype=torch.int32, device="cuda")
+    order = torch.arange(n_slots, dtype=torch.int32, device="cuda")[None].contiguous()
     rows = torch.full((B, 10), -9, dtype=torch.int32, device="cuda")
     nmiss = torch.zeros((B,), dtype=torch.int32, device="cuda")
     st = status_word()
     skv.resolve_rows_lru(T.dev(np.array([256], np.int32)), T.dev(idx), T.dev(np.array([10], np.int32)),
                          torch.zeros(2, dtype=torch.int32, device="cuda"), page,
-                         T.dev(bt), 0, 0, stamp, tok, tslot, host, pool, rows, nmiss, status=st)
+                         T.dev(bt), 0, 0, stamp, tok, tslot, order, host, pool, rows, nmiss, status=st)
     torch.cuda.synchronize()
     assert int(st.item()) & 8
     assert int(nmiss.item()) == -1
