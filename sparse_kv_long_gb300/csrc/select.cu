@@ -46,6 +46,7 @@ constexpr int kCMax = 512;                       // CTAs per request
 constexpr long kSpinLimit = 1L << 21;            // bounded barrier polls (well under a second)
 constexpr size_t kKeyBudget = 96 * 1024;         // shared memory for the chunk's order keys
 constexpr uint32_t kInt4Base = 0x80000000u - (1u << 20);  // order key of score -2^20
+constexpr int kWin = 1024;                                 // bins read back per window (int4 first pass)
 
 struct Ws {
   unsigned* bar;   // [B][2]: arrivals (monotonic within a launch), exits
@@ -408,9 +409,61 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
     }
     __syncthreads();
     unsigned* gh = w.hist + (static_cast<size_t>(pass) * a.B + b) * kBins;
+    // int4 first pass: the request's highest occupied bin is published too, so
+    // that only a window of bins below it has to be read back.
+    const bool windowed = MODE == SKV_SCORE_SKETCH_INT4 && pass == 0;
+    unsigned top_local = 0u;
     for (int i = threadIdx.x; i < nb; i += blockDim.x)
-      if (hist[i]) atomicAdd(&gh[i], hist[i]);
+      if (hist[i]) {
+        atomicAdd(&gh[i], hist[i]);
+        top_local = max(top_local, static_cast<unsigned>(i) + 1u);
+      }
+    if (windowed) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) top_local = max(top_local, __shfl_xor_sync(0xffffffffu, top_local, o));
+      if (lane == 0 && top_local) atomicMax(&w.rng[2 * b], top_local);  // bin + 1 (0: none)
+    }
     req_barrier(arrive, ++nbar * C, a.status);
+    if (windowed) {
+      // Windows of kWin bins from the top down until `need` keys are covered.
+      const unsigned gtop = __ldcg(&w.rng[2 * b]);
+      int hi = static_cast<int>(gtop) - 1;  // highest occupied bin
+      unsigned need_rem = need, above_acc = 0u;
+      uint32_t dig = 0u, abv = 0u;
+      bool found = false;
+      while (hi >= 0) {
+        const int lo_bin = hi >= kWin - 1 ? hi - (kWin - 1) : 0;
+        const int nw = hi - lo_bin + 1;
+        for (int i = threadIdx.x; i < nw; i += blockDim.x) hist[i] = __ldcg(&gh[lo_bin + i]);
+        __syncthreads();
+        unsigned part = 0u;
+        for (int i = threadIdx.x; i < nw; i += blockDim.x) part += hist[i];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+        if (lane == 0) red_a[warp] = part;
+        __syncthreads();
+        unsigned total = 0u;
+        for (int v = 0; v < kWarpsF; v++) total += red_a[v];
+        if (total >= need_rem) {  // the same decision in every thread
+          find_digit(hist, nw, need_rem, &s_digit, &s_above, a.status);
+          dig = s_digit + static_cast<uint32_t>(lo_bin);
+          abv = s_above + above_acc;
+          found = true;
+          break;
+        }
+        __syncthreads();  // hist and red_a are rewritten by the next window
+        need_rem -= total;
+        above_acc += total;
+        hi = lo_bin - 1;
+      }
+      if (!found && threadIdx.x == 0) set_status(a.status, SKV_DEV_COUNT);  // fewer keys than k: not sparse
+      __syncthreads();
+      P = (P << wb) | dig;
+      need -= abv;
+      rem = shift;
+      pass++;
+      continue;
+    }
     {  // all loads in flight together: 16-byte pieces, unrolled
       const uint4* g4 = reinterpret_cast<const uint4*>(gh);
       uint4* h4 = reinterpret_cast<uint4*>(hist);
