@@ -56,7 +56,7 @@ constexpr float kRescaleLog2 = 8.f;             // rescale O only when the max g
 
 struct Aux {
   uint64_t kv_full[kBuf], kv_empty[kBuf];
-  uint64_t s_full, s_empty, p_full, pv_done, x_full, x_empty, mma_idle;
+  uint64_t s_full, s_empty, p_full, pv_done, x_full, x_empty, mma_idle, q_full;
   alignas(16) int32_t prow[kBuf][kNr];  // pool rows of the chunk in slot s (-1: none), staged by the gather warps
   alignas(16) float kl[kBuf][kNr];      // logit factor of each row: row scale x softmax scale x log2(e); 0 if no row
   alignas(16) float madd[kBuf][kNr];    // 0, or -inf for a missing row
@@ -70,6 +70,16 @@ static_assert(offsetof(Aux, kl) % 16 == 0 && offsetof(Aux, madd) % 16 == 0 && of
               "per-row factor arrays must be 16-byte aligned");
 static_assert((kBuf * kKVBytes + kPBytes + 2 * kXBytes) % 16 == 0, "Aux must start 16-byte aligned");
 
+// Prologue and epilogue stage rows in the (then idle) gather ring + P buffer,
+// with 16 bytes of padding per row so that thread h's row accesses fall in
+// distinct bank groups.
+constexpr int kQRowBytes = kSlice * 2;            // a CTA's query share: at most 320 dims, bf16
+constexpr int kQStride = kQRowBytes + 16;
+constexpr int kORowBytes = 256 * 4;               // a CTA's output share: 256 fp32 values
+constexpr int kOStride = kORowBytes + 16;
+static_assert(kH * kQStride <= kBuf * kKVBytes && kH * kOStride <= kBuf * kKVBytes + kPBytes,
+              "staging fits in the ring and the P buffer");
+
 constexpr int kSmem = 1024 + kBuf * kKVBytes + kPBytes + 2 * kXBytes + static_cast<int>(sizeof(Aux));
 
 struct MlaArgs {
@@ -82,8 +92,8 @@ struct MlaArgs {
   const int32_t* count;
   float scale_log2;
   float* out;
-  float* ws_o;
-  float* ws_ml;
+  float* ws_o;      // [B][nsplit][128][512] unnormalised partial outputs
+  float* ws_ml;     // [B][nsplit][128][2]: running max (log2 units), row sum
   int nsplit;
   int32_t* status;
 };
@@ -120,6 +130,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_ker
   float* sXout = sXin + kH * kNr;                         // this CTA's, staged for the bulk copy
   Aux* ax = reinterpret_cast<Aux*>(sP + kPBytes + 2 * kXBytes);
 
+  allow_dependent_launch();  // the split merge may be scheduled onto the SMs this grid leaves free
   const uint32_t rank = tc::cluster_rank(), peer = rank ^ 1u;
   const int split = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -148,8 +159,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_ker
     tc::bar_init(&ax->x_full, 1);          // one local arm per chunk + kXBytes of bulk data from the peer
     tc::bar_init(&ax->x_empty, kH / 32);   // one remote arrive per peer softmax warp and chunk
     tc::bar_init(&ax->mma_idle, 1);
+    tc::bar_init(&ax->q_full, 1);
     ax->abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    // armed for the 128 query rows copied below, before any copy is issued
+    tc::bar_arrive_expect_tx(&ax->q_full, kH * (qsteps * 32));
   }
   if (warp == 0) tc::tmem_alloc<kTmemCols>(&ax->tmem_base);
   tc::tc_fence_before();
@@ -157,25 +171,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_ker
   tc::tc_fence_after();
   const uint32_t tm = ax->tmem_base;
 
-  // Query share -> fp16 -> tensor memory: softmax thread h writes head h's
-  // row (lane h), columns kQCol + c holding dims 2c, 2c + 1 of the share.
+  // Query share -> fp16 -> tensor memory: softmax thread h copies head h's
+  // share (one bulk copy of 640 or 512 bytes) into a staging row, then
+  // writes it to lane h, columns kQCol + c holding dims 2c, 2c + 1.
   if (warp >= 4) {
     const int h = tid - 128;
     const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-    const uint16_t* qrow = a.q + (static_cast<int64_t>(b) * kH + h) * kD + qdim0;
-    for (int c0 = 0; c0 < qsteps * 8; c0 += 32) {  // 32 columns = 64 dims per store
-      uint4 v[8];
+    unsigned char* qst = sKV + h * kQStride;
+    tc::bulk_load(qst, a.q + (static_cast<int64_t>(b) * kH + h) * kD + qdim0, qsteps * 32, &ax->q_full);
+    if (!__all_sync(0xffffffffu, tc::bar_wait(&ax->q_full, 0, &ax->abort))) set_status(a.status, SKV_DEV_TIMEOUT);
 #pragma unroll
-      for (int m = 0; m < 8; m++) v[m] = ld_nc16(qrow + 2 * c0 + 8 * m);
-      uint32_t r[32];
+    for (int c0 = 0; c0 < kSlice / 2; c0 += 32) {  // 32 columns = 64 dims per store
+      if (c0 < qsteps * 8) {
+        uint32_t r[32];
 #pragma unroll
-      for (int m = 0; m < 8; m++) {
-        r[4 * m] = bf16x2_to_f16x2(v[m].x);
-        r[4 * m + 1] = bf16x2_to_f16x2(v[m].y);
-        r[4 * m + 2] = bf16x2_to_f16x2(v[m].z);
-        r[4 * m + 3] = bf16x2_to_f16x2(v[m].w);
+        for (int m = 0; m < 8; m++) {
+          const uint4 w = *reinterpret_cast<const uint4*>(qst + 4 * c0 + 16 * m);
+          r[4 * m] = bf16x2_to_f16x2(w.x);
+          r[4 * m + 1] = bf16x2_to_f16x2(w.y);
+          r[4 * m + 2] = bf16x2_to_f16x2(w.z);
+          r[4 * m + 3] = bf16x2_to_f16x2(w.w);
+        }
+        tc::tmem_st32(tm + lane_base + kQCol + c0, r);
       }
-      tc::tmem_st32(tm + lane_base + kQCol + c0, r);
     }
     tc::tmem_wait_st();
   }
@@ -245,8 +263,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_ker
     named_sync(1, kProducers);
     for (int i = 0; i < nchunks; i++) {
       const int s = i % kBuf;
-      const bool free_buf = i < kBuf || tc::bar_wait(&ax->kv_empty[s], ((i / kBuf) - 1) & 1, abort);
-      if (!named_sync_and(1, kProducers, free_buf)) break;  // the same decision in every producer
+      // The chunk's loads are issued before waiting for its slot (they only
+      // need the row ids, which the producers keep for themselves).
       uint4 v[kPerProducer];
 #pragma unroll
       for (int m = 0; m < kPerProducer; m++) {
@@ -267,6 +285,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_ker
         if (have) rsc = a.row_scale ? a.row_scale[p] : 1.f;
         if (i + 1 < nchunks) next = row_of(i + 1);
       }
+      const bool free_buf = i < kBuf || tc::bar_wait(&ax->kv_empty[s], ((i / kBuf) - 1) & 1, abort);
+      if (!named_sync_and(1, kProducers, free_buf)) break;  // the same decision in every producer
       unsigned char* tile = sKV + s * kKVBytes;
 #pragma unroll
       for (int m = 0; m < kPerProducer; m++) {
@@ -419,8 +439,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_ker
     if (!ok || (nchunks > 0 && !have_o)) set_status(a.status, SKV_DEV_TIMEOUT);
     const bool merged = a.nsplit == 1;
     const float inv = (merged && l > 0.f) ? 1.f / l : 0.f;
-    float* dst = merged ? a.out + (static_cast<int64_t>(b) * kH + h) * kDv + rank * 256
-                        : a.ws_o + ((static_cast<int64_t>(b) * a.nsplit + split) * kH + h) * kDv + rank * 256;
+    // Row h staged in shared memory (the ring and P buffer: the last value
+    // product has completed, so no tensor-core read of them is pending); the
+    // warp then writes its 32 rows out coalesced (one 1 KB row per step).
+    unsigned char* ost = sKV + h * kOStride;
     for (int c0 = 0; c0 < 256; c0 += 32) {
       uint32_t o[32];
       if (have_o) {
@@ -435,8 +457,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_ker
         float4 v = make_float4(__uint_as_float(o[k]), __uint_as_float(o[k + 1]), __uint_as_float(o[k + 2]),
                                __uint_as_float(o[k + 3]));
         if (merged) v = make_float4(v.x * inv, v.y * inv, v.z * inv, v.w * inv);
-        *reinterpret_cast<float4*>(dst + c0 + k) = v;
+        *reinterpret_cast<float4*>(ost + 4 * (c0 + k)) = v;
       }
+    }
+    __syncwarp();
+    for (int r = 0; r < 32; r++) {
+      const int hr = 32 * wq + r;
+      const unsigned char* src = sKV + hr * kOStride;
+      float* drow = merged ? a.out + (static_cast<int64_t>(b) * kH + hr) * kDv + rank * 256
+                           : a.ws_o + ((static_cast<int64_t>(b) * a.nsplit + split) * kH + hr) * kDv + rank * 256;
+#pragma unroll
+      for (int k = 0; k < 2; k++)
+        *reinterpret_cast<float4*>(drow + 4 * (lane + 32 * k)) =
+            *reinterpret_cast<const float4*>(src + 16 * (lane + 32 * k));
     }
     if (!merged && rank == 0) {
       float* ml = a.ws_ml + ((static_cast<int64_t>(b) * a.nsplit + split) * kH + h) * 2;
@@ -459,6 +492,7 @@ __global__ __launch_bounds__(128) void mla_merge_kernel(const float* __restrict_
                                                         const float* __restrict__ ws_ml, int nsplit,
                                                         float* __restrict__ out) {
   const int h = blockIdx.x, b = blockIdx.y, t = threadIdx.x;
+  grid_dependency_wait();  // launched early: the attention kernel's partials are complete from here on
   const float* ml = ws_ml + (static_cast<int64_t>(b) * nsplit * kH + h) * 2;
   float m = -INFINITY;
   for (int s = 0; s < nsplit; s++) m = fmaxf(m, ml[static_cast<int64_t>(s) * kH * 2]);
@@ -531,6 +565,26 @@ SKV_EXPORT int skv_sparse_attend_mla(int B, int Hq, int d, int dv, const uint16_
             dev_status};
   cudaStream_t st = as_stream(stream);
   mla_kernel<<<dim3(2, ns, B), kThreads, kSmem, st>>>(a);
-  if (ns > 1) mla_merge_kernel<<<dim3(kH, B), 128, 0, st>>>(a.ws_o, a.ws_ml, ns, out);
+  if (ns > 1) {
+    // Launched as a programmatic dependent of the attention kernel: its
+    // blocks take the SMs the attention grid leaves free and wait there
+    // (grid_dependency_wait) until that grid has completed.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kH, B, 1);
+    cfg.blockDim = dim3(128, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const float* wo = a.ws_o;
+    const float* wml = a.ws_ml;
+    if (cudaLaunchKernelEx(&cfg, mla_merge_kernel, wo, wml, ns, out) != cudaSuccess) {
+      cudaGetLastError();
+      return SKV_ECUDA;
+    }
+  }
   return launch_status();
 }
