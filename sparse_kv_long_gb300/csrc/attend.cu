@@ -201,6 +201,13 @@ __device__ __forceinline__ bool pair_all(int pair, bool v) {
 }
 
 template <int KV>
+__host__ __device__ constexpr size_t dyn_smem() {
+  return static_cast<size_t>(kPairs) * Geo<KV>::PAIR_BYTES > static_cast<size_t>(kPairs) * kMW * sizeof(float)
+             ? static_cast<size_t>(kPairs) * Geo<KV>::PAIR_BYTES
+             : static_cast<size_t>(kPairs) * kMW * sizeof(float);
+}
+
+template <int KV>
 __global__ __launch_bounds__(kThreads, 2) void attend_kernel(AttendArgs a) {
   using Gm = Geo<KV>;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -239,12 +246,6 @@ __global__ __launch_bounds__(kThreads, 2) void attend_kernel(AttendArgs a) {
   const int ntiles = (nr + kTileRows - 1) / kTileRows;
   int my_tiles = 0;
   for (int t = pair; t < ntiles; t += kPairs) my_tiles++;
-  // Physical row of split row idx, or -1 (absent or out of range).
-  auto phys = [&](int idx) -> int64_t {
-    const int32_t rid = a.rows[static_cast<int64_t>(b) * a.max_rows + r0 + idx];
-    const int64_t p = static_cast<int64_t>(b) * a.req_row_stride + rid;
-    return (rid >= 0 && p >= 0 && p < a.n_pool_rows) ? p : -1;
-  };
   // The 64 threads of the pair copy tile `it` (16 K rows and 16 V rows) into
   // stage it % kStages in 16-byte pieces: thread u of the pair takes piece
   // u % (RB/16) of rows u / (RB/16) + 64/(RB/16) * i.  rowp(r) gives the
@@ -269,30 +270,65 @@ __global__ __launch_bounds__(kThreads, 2) void attend_kernel(AttendArgs a) {
     cp_async_arrive(&bars[pair][stage]);
   };
 
-  // ---- the pair's first tiles go out at once ------------------------------------
-  __syncthreads();
-  for (int it = 0; it < kStages && it < my_tiles; it++) {
-    const int tb = (pair + kPairs * it) * kTileRows;
-    copy_tile(it, [&](int row) { return tb + row < nr ? phys(tb + row) : int64_t(-1); });
+  // ---- row numbers, then the first tiles, scales and query heads ---------------
+  // Each stage issues all of its loads before using any: the split's row
+  // numbers (one latency), then the pair's first tiles and the scales of
+  // every row (one more, overlapping the tiles' flight).
+  constexpr int kRowsPerThread = (kMaxRowsPerSplit + kThreads - 1) / kThreads;
+  constexpr int kQPerThread = (8 * D / 8 + kThreads - 1) / kThreads;
+  int32_t rid[kRowsPerThread];
+#pragma unroll
+  for (int j = 0; j < kRowsPerThread; j++) {
+    const int i = threadIdx.x + j * kThreads;
+    rid[j] = i < nr ? a.rows[static_cast<int64_t>(b) * a.max_rows + r0 + i] : -1;
   }
-
-  // ---- stage row numbers, scales and the query heads ---------------------------
-  for (int i = threadIdx.x; i < nr; i += blockDim.x) {
-    const int64_t pr = phys(i);
-    if (pr < 0) set_status(a.status, SKV_DEV_RANGE);
-    s_prow[i] = pr;
-    if (KV == SKV_KV_INT8) {
-      s_ks[i] = pr >= 0 ? __half2float(__ushort_as_half(a.kscale[pr * a.Hkv + h])) : 0.f;
-      s_vs[i] = pr >= 0 ? __half2float(__ushort_as_half(a.vscale[pr * a.Hkv + h])) : 0.f;
-    }
-  }
-  for (int i = threadIdx.x; i < 8 * D / 8; i += blockDim.x) {  // 16-byte pieces of 8 query heads
+  uint4 qv[kQPerThread];
+#pragma unroll
+  for (int j = 0; j < kQPerThread; j++) {  // 16-byte pieces of 8 query heads
+    const int i = threadIdx.x + j * kThreads;
     const int hd = i / (D / 8), x8 = i % (D / 8);
     const int hl = hg * 8 + hd;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (hl < a.G)
-      v = *reinterpret_cast<const uint4*>(a.q + (static_cast<int64_t>(b) * a.Hq + h * a.G + hl) * D + 8 * x8);
-    *reinterpret_cast<uint4*>(&s_q[hd][8 * x8]) = v;
+    qv[j] = make_uint4(0u, 0u, 0u, 0u);
+    if (i < 8 * D / 8 && hl < a.G)
+      qv[j] = *reinterpret_cast<const uint4*>(a.q + (static_cast<int64_t>(b) * a.Hq + h * a.G + hl) * D + 8 * x8);
+  }
+  int64_t prj[kRowsPerThread];
+#pragma unroll
+  for (int j = 0; j < kRowsPerThread; j++) {
+    const int i = threadIdx.x + j * kThreads;
+    const int64_t p = static_cast<int64_t>(b) * a.req_row_stride + rid[j];
+    prj[j] = (rid[j] >= 0 && p >= 0 && p < a.n_pool_rows) ? p : -1;  // -1: absent or out of range
+    if (i < nr) {
+      if (prj[j] < 0) set_status(a.status, SKV_DEV_RANGE);
+      s_prow[i] = prj[j];
+    }
+  }
+  __syncthreads();
+  for (int it = 0; it < kStages && it < my_tiles; it++) {  // the pair's first tiles go out at once
+    const int tb = (pair + kPairs * it) * kTileRows;
+    copy_tile(it, [&](int row) { return tb + row < nr ? s_prow[tb + row] : int64_t(-1); });
+  }
+  if (KV == SKV_KV_INT8) {
+    uint16_t ksv[kRowsPerThread], vsv[kRowsPerThread];
+#pragma unroll
+    for (int j = 0; j < kRowsPerThread; j++) {
+      const bool ok = threadIdx.x + j * kThreads < nr && prj[j] >= 0;
+      ksv[j] = ok ? a.kscale[prj[j] * a.Hkv + h] : 0;
+      vsv[j] = ok ? a.vscale[prj[j] * a.Hkv + h] : 0;
+    }
+#pragma unroll
+    for (int j = 0; j < kRowsPerThread; j++) {
+      const int i = threadIdx.x + j * kThreads;
+      if (i < nr) {
+        s_ks[i] = __half2float(__ushort_as_half(ksv[j]));
+        s_vs[i] = __half2float(__ushort_as_half(vsv[j]));
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kQPerThread; j++) {
+    const int i = threadIdx.x + j * kThreads;
+    if (i < 8 * D / 8) *reinterpret_cast<uint4*>(&s_q[i / (D / 8)][8 * (i % (D / 8))]) = qv[j];
   }
   __syncthreads();
 
@@ -533,13 +569,21 @@ __global__ __launch_bounds__(kThreads, 2) void attend_kernel(AttendArgs a) {
   __threadfence();
 
   // ---- last CTA: merge the splits in split order ----------------------------------
-  // The (m, l) of every split are loaded in parallel; weights w[h][s] =
-  // exp2(m_s - M) / L are formed once; the O partials are then read as
-  // independent 16-byte loads so their latencies overlap.
+  // When they fit in shared memory (the ring is free now), all the splits'
+  // partials are copied in at once with 16-byte cp.async (one round of
+  // latency); otherwise they are read from global memory (L2) in place.
+  // Weights w[h][s] = exp2(m_s - M) / L are formed once.
   const float* parts = a.part + (static_cast<int64_t>(b) * gy + hy) * a.nsplit * kPart;
+  if (static_cast<size_t>(a.nsplit) * kPart * sizeof(float) <= dyn_smem<KV>()) {
+    float* sp = reinterpret_cast<float*>(smem);
+    for (int i = threadIdx.x; i < a.nsplit * kPart / 4; i += blockDim.x) cp_async16(sp + 4 * i, parts + 4 * i);
+    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
+    parts = sp;
+  }
   for (int t = threadIdx.x; t < 8 * a.nsplit; t += blockDim.x) {
     const int hd = t / a.nsplit, s2 = t % a.nsplit;
-    wts[hd][s2] = __ldcg(parts + s2 * kPart + hd);  // m of split s2, head hd
+    wts[hd][s2] = parts[s2 * kPart + hd];  // m of split s2, head hd
   }
   __syncthreads();
   if (threadIdx.x < 8) {
@@ -558,7 +602,7 @@ __global__ __launch_bounds__(kThreads, 2) void attend_kernel(AttendArgs a) {
   if (threadIdx.x < 8) {
     const int hd = threadIdx.x;
     float L = 0.f;
-    for (int s2 = 0; s2 < a.nsplit; s2++) L += wts[hd][s2] * __ldcg(parts + s2 * kPart + 8 + hd);
+    for (int s2 = 0; s2 < a.nsplit; s2++) L += wts[hd][s2] * parts[s2 * kPart + 8 + hd];
     fin_l[hd] = L;
   }
   __syncthreads();
@@ -576,7 +620,7 @@ __global__ __launch_bounds__(kThreads, 2) void attend_kernel(AttendArgs a) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 8
     for (int s2 = 0; s2 < a.nsplit; s2++) {
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(parts + s2 * kPart + 16 + el));
+      const float4 v = *reinterpret_cast<const float4*>(parts + s2 * kPart + 16 + el);
       const float wgt = wts[hd][s2];
       acc.x += wgt * v.x;
       acc.y += wgt * v.y;
@@ -588,12 +632,6 @@ __global__ __launch_bounds__(kThreads, 2) void attend_kernel(AttendArgs a) {
   if (threadIdx.x == 0) a.tickets[b * gy + hy] = 0;
 }
 
-template <int KV>
-size_t dyn_smem() {
-  const size_t ring = static_cast<size_t>(kPairs) * Geo<KV>::PAIR_BYTES;
-  const size_t merge = static_cast<size_t>(kPairs) * kMW * sizeof(float);
-  return ring > merge ? ring : merge;
-}
 
 template <int KV>
 int occupancy() {
