@@ -410,6 +410,36 @@ def test_score_select_ties(skv, orc, distinct):
         assert np.array_equal(gi[b, :gc[b]], ri[b, :rc[b]])
 
 
+def test_score_select_concentrated_top_keys(skv, orc):
+    """Request 0 has its highest scores packed into one contiguous region, so
+    one chunk holds far more of the top k than any per-chunk candidate list;
+    request 1 is plain random.  Both must match the oracle bit for bit."""
+    rng = np.random.default_rng(2718)
+    B, n_cap, width, k, S, W = 2, 120_000, 256, 2048, 64, 1024
+    q8 = rng.integers(-127, 128, (B, width)).astype(np.int8)
+    sk = rng.integers(0, 256, (B, n_cap, width // 2)).astype(np.uint8)
+    # high-scoring rows: each two's-complement code near +7 where the query is
+    # positive and near -8 where it is negative (dim 2b in the low nibble,
+    # 2b+1 in the high one), jittered by one step so the keys differ
+    lo = (q8[0, 0::2] > 0).astype(np.int64)
+    hi = (q8[0, 1::2] > 0).astype(np.int64)
+    r0, nr = 50_000, 3000
+    jl = rng.integers(0, 2, (nr, width // 2))
+    jh = rng.integers(0, 2, (nr, width // 2))
+    nib_lo = np.where(lo > 0, 7 - jl, 8 + jl)
+    nib_hi = np.where(hi > 0, 7 - jh, 8 + jh)
+    sk[0, r0:r0 + nr] = (nib_lo | (nib_hi << 4)).astype(np.uint8)
+    L = np.array([n_cap, 100_000], np.int32)
+    ref = orc.index_score(orc.SKETCH_INT4, q8, sk, L, S=S, W=W)
+    ri, rc = orc.topk_select(ref["okey"], L, k, S=S, W=W)
+    picks = ri[0, S:S + k]
+    assert ((picks >= r0) & (picks < r0 + nr)).all()  # the construction did concentrate the picks
+    gi, gc, _ = run_fused(skv, skv.SKETCH_INT4, T.dev(q8), T.dev(sk), L, k, S, W, want_keys=False)
+    assert np.array_equal(gc, rc)
+    for b in range(B):
+        assert np.array_equal(gi[b, :gc[b]], ri[b, :rc[b]])
+
+
 def test_score_select_float_modes_match_two_calls(skv, orc):
     rng = np.random.default_rng(4321)
     # pooled bf16, ratio 4
