@@ -363,6 +363,110 @@ __global__ __launch_bounds__(kPrepThreads) void prepare_kernel(
   }
 }
 
+// One CTA per request, the same arithmetic as prepare_kernel: the group sums
+// of every KV head and every appended key share one pass over the basis
+// (each thread holds the basis slices it projects), so the request's scale
+// and int8 query are formed in the same CTA -- no ticket, no round trip
+// through global memory -- and the warps then encode the appended K and V
+// rows.  Dynamic shared memory: X [2 Hkv][d] floats (group sums, then new
+// keys), part [ns][2 Hkv][64] floats, qp [Hkv*64] floats, rows [2 Hkv][d] bf16.
+size_t prepare_req_smem(int Hkv, int d) {
+  const size_t nv = 2 * static_cast<size_t>(Hkv), ns = (static_cast<size_t>(d) + fold::kSlice - 1) / fold::kSlice;
+  return nv * d * 4 + ns * nv * kRank * 4 + static_cast<size_t>(Hkv) * kRank * 4 + nv * d * 2;
+}
+
+constexpr int kReqThreads = 1024;
+
+__global__ __launch_bounds__(kReqThreads, 1) void prepare_req_kernel(
+    const uint16_t* __restrict__ q, const uint16_t* __restrict__ newk, const uint16_t* __restrict__ newv, int Hq,
+    int Hkv, int d, const float* __restrict__ basis, const float* __restrict__ c,
+    const int64_t* __restrict__ new_rows, uint8_t* __restrict__ sketch, int8_t* __restrict__ k8,
+    __half* __restrict__ ks, int8_t* __restrict__ v8, __half* __restrict__ vs, int8_t* __restrict__ q8,
+    float* __restrict__ sigma_out) {
+  extern __shared__ __align__(16) float dsm[];
+  __shared__ float red[32];
+  const int b = blockIdx.x, G = Hq / Hkv, nv = 2 * Hkv, ns = fold::n_slices(d);
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  float* X = dsm;                                                  // [nv][d]
+  float* part = X + nv * d;                                        // [ns][nv][64]
+  float* qp = part + ns * nv * kRank;                              // [Hkv*64]
+  uint16_t* rows = reinterpret_cast<uint16_t*>(qp + Hkv * kRank);  // [nv][d]: K rows, then V rows
+  // Every load first, so that the first-touch latencies overlap.
+  const int64_t row = new_rows[b];
+  for (int u = t; u < nv * (d / 8); u += blockDim.x) {
+    const int r = u / (d / 8), piece = u - r * (d / 8);
+    const uint16_t* src = (r < Hkv ? newk : newv) + (static_cast<int64_t>(b) * Hkv + r % Hkv) * d + 8 * piece;
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(
+                     __cvta_generic_to_shared(rows + r * d + 8 * piece))),
+                 "l"(src)
+                 : "memory");
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  // Thread t: basis column t % 64 of slice (t / 64) % ns, projected on the
+  // group sums (first half of the threads) or on the new keys (second half).
+  const int half = kReqThreads / 2;
+  const bool held = ns * kRank <= half;
+  const int task = t % half, vh = t / half;
+  float bcol[fold::kSlice];
+  if (held && task < ns * kRank) fold::load_slice(basis, d, task % kRank, task / kRank, bcol);
+  for (int x = t; x < Hkv * d; x += blockDim.x) {
+    const int h = x / d, xi = x - h * d;
+    X[h * d + xi] = fold::group_sum(q + (static_cast<int64_t>(b) * Hq + static_cast<int64_t>(h) * G) * d, G, d, xi);
+    X[(Hkv + h) * d + xi] = bf16_bits_to_f32(newk[(static_cast<int64_t>(b) * Hkv + h) * d + xi]);
+  }
+  __syncthreads();
+  if (held) {
+    if (task < ns * kRank)
+      fold::dot_slice(bcol, X + vh * Hkv * d, d, Hkv, d, task / kRank,
+                      part + (task / kRank) * nv * kRank + vh * Hkv * kRank + task % kRank, kRank);
+  } else {
+    for (int task = t; task < ns * kRank; task += blockDim.x) {
+      const int sl = task / kRank, j = task - sl * kRank;
+      fold::proj_slice(basis, X, d, nv, d, j, sl, part + sl * nv * kRank + j, kRank);
+    }
+  }
+  __syncthreads();
+  float amax = 0.f;
+  for (int m = t; m < Hkv * kRank; m += blockDim.x) {  // folded query of head m/64, dim m%64
+    const float v = __fmul_rn(fold::combine_slices(part + m, nv * kRank, ns), c[m]);
+    qp[m] = v;
+    amax = fmaxf(amax, fabsf(v));
+  }
+  for (int m = t; m < Hkv * kRank / 2; m += blockDim.x) {  // sketch codes of the new keys, two per byte
+    const int h = m / (kRank / 2), j0 = 2 * (m % (kRank / 2));
+    const float* pk = part + (Hkv + h) * kRank;
+    const int c0 = fold::sketch_code(fold::combine_slices(pk + j0, nv * kRank, ns), c[h * kRank + j0]);
+    const int c1 = fold::sketch_code(fold::combine_slices(pk + j0 + 1, nv * kRank, ns), c[h * kRank + j0 + 1]);
+    sketch[row * (Hkv * kRank / 2) + m] = static_cast<uint8_t>((c0 & 15) | ((c1 & 15) << 4));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if (lane == 0) red[warp] = amax;
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  __syncthreads();
+  if (t < 32) {
+    float v = t < (blockDim.x >> 5) ? red[t] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if (t == 0) red[0] = v;
+  }
+  for (int r = warp; r < nv; r += blockDim.x >> 5) {  // int8 rows: K of head r, then V of head r - Hkv
+    float rowv[16];
+#pragma unroll
+    for (int i = 0; i < 16; i++) {
+      const int x = lane + 32 * i;
+      rowv[i] = x < d ? bf16_bits_to_f32(rows[r * d + x]) : 0.f;
+    }
+    const int h = r % Hkv;
+    fold::encode_row_warp(rowv, d, (r < Hkv ? k8 : v8) + (row * Hkv + h) * d, (r < Hkv ? ks : vs) + row * Hkv + h);
+  }
+  __syncthreads();
+  const float sigma = __fdiv_rn(red[0], 127.f);
+  if (t == 0 && sigma_out) sigma_out[b] = sigma;
+  for (int m = t; m < Hkv * kRank; m += blockDim.x)
+    q8[static_cast<int64_t>(b) * Hkv * kRank + m] = fold::query_code(qp[m], sigma);
+}
+
 }  // namespace
 }  // namespace skv
 
@@ -386,6 +490,13 @@ SKV_EXPORT int skv_decode_prepare(const uint16_t* q, const uint16_t* new_k, cons
   float* qp_ws = static_cast<float*>(workspace);
   unsigned* tickets = reinterpret_cast<unsigned*>(
       static_cast<char*>(workspace) + (static_cast<size_t>(B) * Hkv * kRank * sizeof(float) + 255) / 256 * 256);
+  const size_t smem = prepare_req_smem(Hkv, d);
+  if (smem <= 48 * 1024) {  // one CTA per request
+    prepare_req_kernel<<<B, kReqThreads, smem, as_stream(stream)>>>(
+        q, new_k, new_v, Hq, Hkv, d, basis, c, new_rows, sketch, k8, reinterpret_cast<__half*>(k_scale), v8,
+        reinterpret_cast<__half*>(v_scale), q8, sigma);
+    return launch_status();
+  }
   dim3 grid(Hkv, B);
   prepare_kernel<<<grid, kPrepThreads, 0, as_stream(stream)>>>(
       q, new_k, new_v, Hq, Hkv, d, basis, c, new_rows, sketch, k8, reinterpret_cast<__half*>(k_scale), v8,
