@@ -159,35 +159,46 @@ __global__ __launch_bounds__(kClockThreads) void clock_kernel(ClockArgs a) {
   const int32_t step = read_step(a.step);
   auto is_pick = [&](int64_t t) { return t >= S && t < T - W; };
 
-  // The sweep needs at least as many slots as picks (else nothing changes).
-  int n_picks = 0;
-  for (int base = 0; base < n; base += kClockThreads) {
-    const int i = base + tid;
-    bool p = false;
-    if (i < n) {
-      const int64_t t = idx[i];
-      p = t >= 0 && t < T && is_pick(t);
-    }
-    n_picks += __syncthreads_count(p);
+  // The thread's rows i = tid + 512 k: their tokens, then the slots of the
+  // picks, each round of loads issued together (rows beyond 512 * kClockPer
+  // take further rounds).
+  constexpr int kClockPer = kMaxResolveRows / kClockThreads;
+  int32_t tk[kClockPer], sk[kClockPer];
+  int picks_local = 0;
+#pragma unroll
+  for (int k = 0; k < kClockPer; k++) {
+    const int i = tid + k * kClockThreads;
+    tk[k] = i < n ? idx[i] : -1;
   }
-  const bool fits = n_picks <= Hs;
-  if (!fits && tid == 0) set_status(a.status, SKV_DEV_COUNT);
-
+#pragma unroll
+  for (int k = 0; k < kClockPer; k++) {
+    const int64_t t = tk[k];
+    const bool pk = tid + k * kClockThreads < n && t >= 0 && t < T && is_pick(t);
+    picks_local += pk;
+    sk[k] = pk ? tslot[t] : -1;
+  }
   for (int s = tid; s < Hs; s += kClockThreads) {
     s_tok[s] = a.slot_token[sbase + s];
     s_use[s] = a.use_step[sbase + s];
     s_ref[s] = a.ref[sbase + s];
   }
+  // The sweep needs at least as many slots as picks (else nothing changes).
+  int n_picks;
+  block_exclusive_scan(picks_local, scr, &n_picks);
+  const bool fits = n_picks <= Hs;
+  if (!fits && tid == 0) set_status(a.status, SKV_DEV_COUNT);
   __syncthreads();
 
   // Phase 1: sinks, tail and hits; misses listed in ascending token order.
   int nm = 0;
-  for (int base = 0; base < n; base += kClockThreads) {
-    const int i = base + tid;
+#pragma unroll
+  for (int k = 0; k < kClockPer; k++) {
+    if (k * kClockThreads >= n) break;  // the same in every thread
+    const int i = tid + k * kClockThreads;
     int miss = 0;
     int64_t t = -1;
     if (i < n) {
-      t = idx[i];
+      t = tk[k];
       if (t < 0 || t >= T) {
         set_status(a.status, SKV_DEV_RANGE);
         rows[i] = -1;
@@ -198,7 +209,7 @@ __global__ __launch_bounds__(kClockThreads) void clock_kernel(ClockArgs a) {
       } else if (!fits) {
         rows[i] = -1;
       } else {
-        const int32_t s = tslot[t];
+        const int32_t s = sk[k];
         if (s >= 0 && s < Hs) {
           s_ref[s] = 1;
           s_use[s] = step;
