@@ -380,7 +380,8 @@ int skv_sparse_attend_decode(int kv_kind, int B, int Hq, int Hkv, int d,
  *   out        fp32 [B][128][512]
  *   workspace  skv_mla_workspace_size(B, max_rows) bytes (no zero-fill needed)
  * A row outside [0, n_pool_rows) is skipped and sets SKV_DEV_RANGE.  The
- * row splits are merged in a fixed order: the output is deterministic.
+ * row splits are merged in a fixed order: the output is deterministic (two
+ * splits merge inside one thread-block cluster and need no workspace).
  * Runs on the tcgen05 tensor cores with fp16 operands (fp8 -> fp16 exact),
  * fp32 accumulation; probabilities rounded to fp16.
  * Errors: SKV_EUNSUPPORTED unless Hq = 128, d = 576, dv = 512; SKV_EINVAL for

@@ -26,7 +26,10 @@
 // Roles in a CTA: warp 0 issues tcgen05.mma (one thread), warps 1-3 gather
 // rows into a 3-deep ring, warps 4-7 own one head each (tensor-memory lane =
 // head) for the online softmax and the epilogue.  Rows are split across
-// clusters; the splits are merged in a fixed order (deterministic).
+// clusters; the splits are merged in a fixed order (deterministic): when a
+// request has two splits, its two CTA pairs form one cluster of four and merge
+// through distributed shared memory at the end, otherwise a merge kernel
+// combines the partials.
 #include <cstddef>
 
 #include "tc.cuh"
@@ -61,6 +64,7 @@ struct Aux {
   alignas(16) float kl[kBuf][kNr];      // logit factor of each row: row scale x softmax scale x log2(e); 0 if no row
   alignas(16) float madd[kBuf][kNr];    // 0, or -inf for a missing row
   alignas(16) float vsc[kBuf][kNr];     // value factor: the row scale; 0 if no row
+  float mrow[kH], lrow[kH];             // in-cluster split merge: running max and row sum per head
   uint32_t tmem_base;
   int abort;
 };
@@ -95,6 +99,7 @@ struct MlaArgs {
   float* ws_o;      // [B][nsplit][128][512] unnormalised partial outputs
   float* ws_ml;     // [B][nsplit][128][2]: running max (log2 units), row sum
   int nsplit;
+  int cmerge;       // 1: the two splits of a request are one 4-CTA cluster and merge in it
   int32_t* status;
 };
 
@@ -121,7 +126,9 @@ __device__ __forceinline__ bool named_sync_and(int id, int n, bool pred) {
   return r != 0;
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_kernel(MlaArgs a) {
+// Launched in clusters of (2, 1, 1) -- a CTA pair -- or (2, 2, 1) when the
+// request's two splits merge inside the cluster.
+__global__ void __launch_bounds__(kThreads, 1) mla_kernel(MlaArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = smem_raw + ((1024u - (tc::smem_addr(smem_raw) & 1023u)) & 1023u);
   unsigned char* sKV = sm;
@@ -131,7 +138,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_ker
   Aux* ax = reinterpret_cast<Aux*>(sP + kPBytes + 2 * kXBytes);
 
   allow_dependent_launch();  // the split merge may be scheduled onto the SMs this grid leaves free
-  const uint32_t rank = tc::cluster_rank(), peer = rank ^ 1u;
+  const uint32_t crank = tc::cluster_rank();
+  const uint32_t rank = crank & 1u, peer = crank ^ 1u;  // position in the pair, the pair partner's cluster rank
   const int split = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -460,8 +468,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_ker
         *reinterpret_cast<float4*>(ost + 4 * (c0 + k)) = v;
       }
     }
+    if (a.cmerge) {  // merged with the other split after the cluster barrier below
+      ax->mrow[h] = have_o ? m_ref : -INFINITY;
+      ax->lrow[h] = have_o ? l : 0.f;
+    }
     __syncwarp();
-    for (int r = 0; r < 32; r++) {
+    for (int r = 0; !a.cmerge && r < 32; r++) {
       const int hr = 32 * wq + r;
       const unsigned char* src = sKV + hr * kOStride;
       float* drow = merged ? a.out + (static_cast<int64_t>(b) * kH + hr) * kDv + rank * 256
@@ -471,7 +483,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_ker
         *reinterpret_cast<float4*>(drow + 4 * (lane + 32 * k)) =
             *reinterpret_cast<const float4*>(src + 16 * (lane + 32 * k));
     }
-    if (!merged && rank == 0) {
+    if (!merged && !a.cmerge && rank == 0) {
       float* ml = a.ws_ml + ((static_cast<int64_t>(b) * a.nsplit + split) * kH + h) * 2;
       ml[0] = have_o ? m_ref : -INFINITY;
       ml[1] = have_o ? l : 0.f;
@@ -484,7 +496,47 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) mla_ker
     tc::tc_fence_after();
     tc::tmem_dealloc<kTmemCols>(tm);
   }
-  tc::cluster_sync();  // the peer's copies into this CTA's shared memory are done
+  tc::cluster_sync();  // the peer's copies into this CTA's shared memory are done; partials staged
+  if (a.cmerge) {
+    // Split sc of the cluster merges heads [64 sc, 64 sc + 64) of this CTA's
+    // 256 value dims from its own staged rows and those of the CTA holding
+    // the same dims for the other split (cluster rank crank ^ 2), in split
+    // order -- the arithmetic of the merge kernel.
+    const uint32_t other = crank ^ 2u;
+    const int sc = static_cast<int>(crank >> 1);
+    const unsigned char* rows0 = sKV;  // staged rows, head h at h * kOStride
+    for (int e = tid; e < 64 * 64; e += kThreads) {
+      const int h = 64 * sc + e / 64, dd = 4 * (e % 64);
+      const unsigned char* own = rows0 + h * kOStride + 4 * dd;
+      const float4 o_own = *reinterpret_cast<const float4*>(own);
+      const float4 o_oth = tc::ld_remote16(own, other);
+      const float m_own = ax->mrow[h], l_own = ax->lrow[h];
+      const float m_oth = tc::ld_remote_f32(&ax->mrow[h], other), l_oth = tc::ld_remote_f32(&ax->lrow[h], other);
+      // split 0 first
+      const bool first = (crank >> 1) == 0;
+      const float m0 = first ? m_own : m_oth, m1 = first ? m_oth : m_own;
+      const float l0 = first ? l_own : l_oth, l1 = first ? l_oth : l_own;
+      const float4 o0 = first ? o_own : o_oth, o1 = first ? o_oth : o_own;
+      const float m = fmaxf(fmaxf(-INFINITY, m0), m1);
+      const float w0 = m0 == -INFINITY ? 0.f : exp2f(m0 - m), w1 = m1 == -INFINITY ? 0.f : exp2f(m1 - m);
+      float den = 0.f;
+      den += w0 * l0;
+      den += w1 * l1;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      acc.x += w0 * o0.x;
+      acc.y += w0 * o0.y;
+      acc.z += w0 * o0.z;
+      acc.w += w0 * o0.w;
+      acc.x += w1 * o1.x;
+      acc.y += w1 * o1.y;
+      acc.z += w1 * o1.z;
+      acc.w += w1 * o1.w;
+      const float inv = den > 0.f ? 1.f / den : 0.f;
+      *reinterpret_cast<float4*>(a.out + (static_cast<int64_t>(b) * kH + h) * kDv + rank * 256 + dd) =
+          make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    }
+    tc::cluster_sync();  // no CTA leaves while another still reads its shared memory
+  }
 }
 
 // Splits of one (request, head) combined in split order.
@@ -530,7 +582,7 @@ using namespace skv;
 SKV_EXPORT size_t skv_mla_workspace_size(int B, int max_rows) {
   if (B < 1 || max_rows < 1) return 0;
   const int ns = mla_splits(B, max_rows);
-  if (ns == 1) return 16;
+  if (ns <= 2) return 16;  // one split, or two merged inside their cluster
   return static_cast<size_t>(B) * ns * kH * (kDv + 2) * sizeof(float);
 }
 
@@ -547,7 +599,7 @@ SKV_EXPORT int skv_sparse_attend_mla(int B, int Hq, int d, int dv, const uint16_
   if (!aligned16(q) || !aligned16(kv_pool) || !aligned16(out) || n_pool_rows > INT32_MAX) return SKV_EINVAL;
   if (static_cast<int64_t>(B - 1) * req_row_stride > INT32_MAX) return SKV_EINVAL;
   const int ns = mla_splits(B, max_rows);
-  if (ns > 1) {
+  if (ns > 2) {
     if (!workspace || !aligned16(workspace) || workspace_bytes < skv_mla_workspace_size(B, max_rows))
       return SKV_ENOMEM;
   }
@@ -560,12 +612,30 @@ SKV_EXPORT int skv_sparse_attend_mla(int B, int Hq, int d, int dv, const uint16_
     configured = true;
   }
   float* ws = static_cast<float*>(workspace);
+  const bool cmerge = ns == 2;  // the two splits of a request merge inside one 4-CTA cluster
   MlaArgs a{q, kv_pool, row_scale, req_row_stride, n_pool_rows, rows, max_rows, count,
             softmax_scale * kLog2e, out, ws, ns > 1 ? ws + static_cast<size_t>(B) * ns * kH * kDv : nullptr, ns,
-            dev_status};
+            cmerge ? 1 : 0, dev_status};
   cudaStream_t st = as_stream(stream);
-  mla_kernel<<<dim3(2, ns, B), kThreads, kSmem, st>>>(a);
-  if (ns > 1) {
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, ns, B);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = cmerge ? 2 : 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, mla_kernel, a) != cudaSuccess) {
+      cudaGetLastError();
+      return SKV_ECUDA;
+    }
+  }
+  if (ns > 1 && !cmerge) {
     // Launched as a programmatic dependent of the attention kernel: its
     // blocks take the SMs the attention grid leaves free and wait there
     // (grid_dependency_wait) until that grid has completed.

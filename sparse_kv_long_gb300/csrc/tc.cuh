@@ -118,6 +118,26 @@ __device__ __forceinline__ void st_remote16(const void* local, uint32_t rank, fl
       : "memory");
 }
 
+// Loads from CTA `rank`'s shared memory at the same offset as `local`.
+__device__ __forceinline__ float4 ld_remote16(const void* local, uint32_t rank) {
+  float4 v;
+  asm volatile(
+      "{\n.reg .b32 ra;\nmapa.shared::cluster.u32 ra, %4, %5;\n"
+      "ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [ra];\n}\n"
+      : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+      : "r"(smem_addr(local)), "r"(rank)
+      : "memory");
+  return v;
+}
+__device__ __forceinline__ float ld_remote_f32(const void* local, uint32_t rank) {
+  float v;
+  asm volatile("{\n.reg .b32 ra;\nmapa.shared::cluster.u32 ra, %1, %2;\nld.shared::cluster.f32 %0, [ra];\n}\n"
+               : "=f"(v)
+               : "r"(smem_addr(local)), "r"(rank)
+               : "memory");
+  return v;
+}
+
 // Asynchronous 16-byte store into CTA `rank`'s shared memory (same offset as
 // `local`); on arrival it completes 16 bytes of transaction count on that
 // CTA's barrier at the offset of `local_bar`.  No fence is needed: the data is
