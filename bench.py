@@ -472,7 +472,7 @@ class MlaLruWorkloadGPU:
     host-only, hot buffer of 4096 rows per request."""
 
     B, T, H, D, DV, K, PAGE, SLOTS, DI = 32, 142_000, 128, 576, 512, 2048, 64, 4096, 128
-    KERNELS_PER_LAYER = 5  # score+select, LRU state pass + row fetch, MLA attention + split merge
+    KERNELS_PER_LAYER = 4  # score+select, LRU state pass + row fetch, MLA attention (splits merged in-cluster)
 
     def __init__(self, torch, skv, wl, dev, layers, n_steps, eta=0.25, context=None):
         self.torch, self.skv, self.L = torch, skv, layers
