@@ -685,6 +685,107 @@ class HostClockWorkloadGPU:
                 "l2": "inputs larger than L2: 256 MB sketch per layer"}
 
 
+class PooledWorkloadGPU:
+    """Pooled-key indexer decode: 4 requests x 1,048,576 tokens, 16 query / 2
+    KV heads, head dim 256, bf16 K/V; raw 128-dim bf16 indexer keys pooled by
+    4 (262,144 blocks per request); the top 512 blocks expand to 2048 token
+    rows.  With kv_host, K, V and the raw indexer keys sit in registered host
+    memory, read zero-copy, and only the pooled keys stay in HBM."""
+
+    KERNELS_PER_LAYER = 3  # pool the block the current token completes, score + select, attention
+
+    def __init__(self, torch, skv, wl, dev, layers, kv_host=False):
+        P = wl.POOLED
+        self.P, self.torch, self.skv, self.L, self.kv_host = P, torch, skv, layers, kv_host
+        B, Tn, Hkv, d, di = P.B, P.T, P.Hkv, P.d, P.d_idx
+        gen = wl.device_generator(SEED + 303, device=dev)
+        self.nb = Tn // P.ratio
+        self.rows = P.ratio * P.k_blocks + Tn % P.ratio     # rows attended per request
+        self.lengths = torch.full((B,), Tn, dtype=torch.int32, device=dev)
+        kv_bytes, key_bytes = B * Tn * Hkv * d * 2, B * Tn * di * 2
+        self.q, self.qidx, self.keys, self.pooled, self.K, self.V, self.hosts = [], [], [], [], [], [], []
+        for l in range(layers):
+            self.q.append(wl.randn_torch(gen, (B, P.Hq, d), device=dev))
+            qi = wl.randn_torch(gen, (B, di), device=dev)
+            self.qidx.append(qi)
+            keys = wl.pooled_index_keys_torch(gen, B, Tn, qi, P.ratio, P.clusters, P.cluster_blocks, device=dev)
+            pooled = torch.empty((B, self.nb, di), dtype=torch.bfloat16, device=dev)
+            skv.pool_keys(keys, pooled, 0, self.nb)
+            self.pooled.append(pooled)
+            if kv_host:
+                host = HostTier(skv, 2 * kv_bytes + key_bytes)
+                hv = torch.from_numpy(host.arr)
+                hk = hv[:kv_bytes].view(torch.bfloat16).view(B, Tn, Hkv, d)
+                hvv = hv[kv_bytes:2 * kv_bytes].view(torch.bfloat16).view(B, Tn, Hkv, d)
+                hv[2 * kv_bytes:].view(torch.bfloat16).view(B, Tn, di).copy_(keys)
+                for b in range(B):
+                    hk[b].copy_(wl.randn_torch(gen, (Tn, Hkv, d), device=dev))
+                    hvv[b].copy_(wl.randn_torch(gen, (Tn, Hkv, d), device=dev))
+                torch.cuda.synchronize()
+                del keys
+                self.hosts.append(host)
+                self.K.append(skv.HostView(host.alias, (B * Tn, Hkv, d), 2))
+                self.V.append(skv.HostView(host.alias + kv_bytes, (B * Tn, Hkv, d), 2))
+                self.keys.append(skv.HostView(host.alias + 2 * kv_bytes, (B, Tn, di), 2))
+            else:
+                Kl = torch.empty((B * Tn, Hkv, d), dtype=torch.bfloat16, device=dev)
+                Vl = torch.empty_like(Kl)
+                for b in range(B):
+                    Kl[b * Tn:(b + 1) * Tn].copy_(wl.randn_torch(gen, (Tn, Hkv, d), device=dev))
+                    Vl[b * Tn:(b + 1) * Tn].copy_(wl.randn_torch(gen, (Tn, Hkv, d), device=dev))
+                self.K.append(Kl)
+                self.V.append(Vl)
+                self.keys.append(keys)
+        self.max_rows = P.max_rows
+        self.idx = torch.zeros((B, self.max_rows), dtype=torch.int32, device=dev)
+        self.cnt = torch.zeros((B,), dtype=torch.int32, device=dev)
+        self.tws = torch.zeros((skv.score_select_workspace_size(B),), dtype=torch.uint8, device=dev)
+        self.aws = torch.zeros((skv.attend_workspace_size(B, P.Hq, Hkv, d, self.max_rows),), dtype=torch.uint8,
+                               device=dev)
+        self.out = torch.zeros((B, P.Hq, d), dtype=torch.float32, device=dev)
+        self.status = torch.zeros((1,), dtype=torch.int32, device=dev)
+        torch.cuda.synchronize()
+
+    def set_step(self, s):
+        pass  # stateless: no hot buffer, the same queries every step
+
+    def layer(self, l, ev=lambda name: None):
+        skv, P, st = self.skv, self.P, self.status
+        ev("pool0")
+        skv.pool_keys(self.keys[l], self.pooled[l], self.nb - 1, 1, ratio=P.ratio)
+        ev("sel0")
+        skv.score_select(skv.POOLED_BF16, self.qidx[l], self.pooled[l], self.lengths, P.k_blocks, self.idx, self.cnt,
+                         self.tws, ratio=P.ratio, status=st)
+        ev("att0")
+        skv.sparse_attend_decode(skv.KV_BF16, self.q[l], self.K[l], self.V[l], self.idx, self.cnt,
+                                 1 / math.sqrt(P.d), self.out, self.aws, P.Hkv, req_row_stride=P.T,
+                                 n_pool_rows=P.B * P.T, status=st)
+        ev("end")
+
+    def kernels(self, t):
+        P = self.P
+        row_head = 2 * P.d * 2                              # K and V bf16 per row and KV head
+        return [("pool_keys_one_block", "pool0", "sel0", "latency", None, f"{P.B} x {P.ratio} raw keys pooled"),
+                ("score_select_pooled_r4", "sel0", "att0", "hbm", P.B * self.nb * P.d_idx * 2,
+                 f"{P.d_idx * 2} B pooled key per block x {P.B} x {self.nb}"),
+                ("attend_bf16", "att0", "end", "host" if self.kv_host else "hbm",
+                 P.B * self.rows * P.Hkv * row_head,
+                 f"{row_head} B per row-head x {P.B} x {self.rows} x {P.Hkv}")]
+
+    def close(self):
+        for h in self.hosts:
+            h.close()
+
+    def config(self):
+        P = self.P
+        name = "pooled_host" if self.kv_host else "pooled"
+        return {"workload": f"{name}_{P.B}x{P.T}_{self.L}L_bf16kv", "batch": P.B, "context": P.T,
+                "layers": self.L, "q_heads": P.Hq, "kv_heads": P.Hkv, "head_dim": P.d, "indexer_dim": P.d_idx,
+                "ratio": P.ratio, "top_blocks": P.k_blocks, "rows": self.rows,
+                "kv": "registered host memory, zero-copy" if self.kv_host else "HBM",
+                "l2": "inputs larger than L2: pooled keys 268 MB per layer"}
+
+
 def run_extra(args):
     import torch
 
@@ -695,12 +796,15 @@ def run_extra(args):
     torch.cuda.set_device(0)
     _build.build()
     dev = torch.device("cuda", 0)
-    warm = max(args.warmup, 64)                    # stateful hot buffers: reach steady state first
+    stateful = args.workload in ("mla_lru", "host_clock")
+    warm = max(args.warmup, 64) if stateful else args.warmup  # hot buffers: reach steady state first
     n_steps = warm + args.steps + 20
     if args.workload == "mla_lru":
         w = MlaLruWorkloadGPU(torch, skv, wl, dev, args.layers, n_steps, context=args.context)
-    else:
+    elif args.workload == "host_clock":
         w = HostClockWorkloadGPU(torch, skv, wl, dev, args.layers, n_steps, eta=args.eta)
+    else:
+        w = PooledWorkloadGPU(torch, skv, wl, dev, args.layers, kv_host=args.workload == "pooled_host")
     stream = torch.cuda.Stream()
     nolog = lambda name: None
 
@@ -723,7 +827,6 @@ def run_extra(args):
             graph.replay()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    miss_sum = torch.zeros_like(w.nmiss, dtype=torch.int64)
     try:
         gpu_id = "GPU-" + str(torch.cuda.get_device_properties(0).uuid)
     except Exception:
@@ -740,16 +843,20 @@ def run_extra(args):
     ms_per_step = e0.elapsed_time(e1) / args.steps
     value = 1e3 / ms_per_step * w.L
     # miss statistics of the steady state (untimed replays)
-    n_stat = 16
-    with torch.cuda.stream(stream):
-        for s in range(n_stat):
-            w.set_step(warm + args.steps + s)
-            graph.replay()
-            miss_sum.add_(w.nmiss)
-    torch.cuda.synchronize()
-    misses_per_layer_step = float(miss_sum.sum().item()) / (n_stat * w.L)
-    picks = W_K * W_B if args.workload == "host_clock" else w.K * w.B
-    row_bytes = w.tok_bytes if args.workload == "host_clock" else w.D
+    n_stat = 16 if stateful else 0
+    extra = {}
+    if stateful:
+        miss_sum = torch.zeros_like(w.nmiss, dtype=torch.int64)
+        with torch.cuda.stream(stream):
+            for s in range(n_stat):
+                w.set_step(warm + args.steps + s)
+                graph.replay()
+                miss_sum.add_(w.nmiss)
+        torch.cuda.synchronize()
+        misses_per_layer_step = float(miss_sum.sum().item()) / (n_stat * w.L)
+        picks = W_K * W_B if args.workload == "host_clock" else w.K * w.B
+        row_bytes = w.tok_bytes if args.workload == "host_clock" else w.D
+        extra = {"miss_rate": misses_per_layer_step / picks, "misses_per_layer_step": misses_per_layer_step}
 
     # per-kernel durations: eager launches of one step behind a sleep, same stream
     marks = {}
@@ -773,7 +880,8 @@ def run_extra(args):
             for l in range(w.L):
                 w.layer(l, mark_for(l))
         torch.cuda.synchronize()
-        eager_misses += [float(w.nmiss[l].clamp(min=0).sum().item()) for l in range(w.L)]
+        if stateful:
+            eager_misses += [float(w.nmiss[l].clamp(min=0).sum().item()) for l in range(w.L)]
         for name, a0, a1, *_ in w.kernels(None):
             for l in range(w.L):
                 dur.setdefault(name, []).append(marks[a0][l].elapsed_time(marks[a1][l]))
@@ -782,16 +890,18 @@ def run_extra(args):
     hbm = float(peaks_d.get("hbm_gbs", 6800.0))
     tfl = float(peaks_d.get("bf16_tflops", 1900.0))
     # host link: zero-copy streaming read of layer 0's host tier
-    sink = torch.zeros((1,), dtype=torch.int64, device=dev)
-    nb = (w.hosts[0].nbytes // 16) * 16
-    skv.stream_read(w.hosts[0].alias, nb, sink)
-    torch.cuda.synchronize()
-    h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    h0.record()
-    skv.stream_read(w.hosts[0].alias, nb, sink)
-    h1.record()
-    torch.cuda.synchronize()
-    host_gbs = nb / (h0.elapsed_time(h1) * 1e-3) / 1e9
+    host_gbs = None
+    if w.hosts:
+        sink = torch.zeros((1,), dtype=torch.int64, device=dev)
+        nb = (w.hosts[0].nbytes // 16) * 16
+        skv.stream_read(w.hosts[0].alias, nb, sink)
+        torch.cuda.synchronize()
+        h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        h0.record()
+        skv.stream_read(w.hosts[0].alias, nb, sink)
+        h1.record()
+        torch.cuda.synchronize()
+        host_gbs = nb / (h0.elapsed_time(h1) * 1e-3) / 1e9
     kern = {}
     for name, a0, a1, bound, work, rule in w.kernels(None):
         # median over 3 steps x layers: a zero-copy host read now and then takes
@@ -803,17 +913,17 @@ def run_extra(args):
         elif bound == "tensor":
             blk.update(achieved=work / (us * 1e-6) / 1e12, peak=tfl, unit="TFLOP/s",
                        peak_note="bf16 dense burst (fp16 operands: same nominal rate)")
-        else:
-            hb = statistics.mean(eager_misses) * row_bytes
+        elif bound == "host":
+            hb = work if work is not None else statistics.mean(eager_misses) * row_bytes
             blk.update(achieved=hb / (us * 1e-6) / 1e9, peak=host_gbs, unit="GB/s",
                        bytes_per_launch=hb, peak_note="measured zero-copy read of the registered host tier")
-        blk["frac"] = blk["achieved"] / blk["peak"]
+        if "achieved" in blk:
+            blk["frac"] = blk["achieved"] / blk["peak"]
         kern[name] = blk
     line = {"workload": args.workload, "metric": "layer-steps/s", "value": value, "unit": "layer-steps/s",
             "n_gpus": 1, "steps": args.steps, "warmup": warm, "ms_per_step": ms_per_step,
             "higher_is_better": True, "data": "synthetic", "config": w.config(),
-            "miss_rate": misses_per_layer_step / picks, "misses_per_layer_step": misses_per_layer_step,
-            "host_read_gbs_probe": host_gbs, "kernels": kern, "clocks": clk.summary(),
+            **extra, "host_read_gbs_probe": host_gbs, "kernels": kern, "clocks": clk.summary(),
             "device_status": int(w.status.item()),
             "gpu_launches": args.steps * w.L * w.KERNELS_PER_LAYER}
     print(json.dumps(line), flush=True)
@@ -830,7 +940,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--layers", type=int, default=None, help="distinct layers (16 for the sketch workload; "
                     "fewer only for profiler captures)")
-    ap.add_argument("--workload", default="sketch", choices=["sketch", "host_clock", "mla_lru"],
+    ap.add_argument("--workload", default="sketch",
+                    choices=["sketch", "host_clock", "mla_lru", "pooled", "pooled_host"],
                     help="sketch: the headline line; the others print their own line")
     ap.add_argument("--eta", type=float, default=0.35, help="query drift per step (host_clock)")
     ap.add_argument("--context", type=int, default=None, help="mla_lru: tokens per request (default 142,000; "
@@ -839,7 +950,7 @@ def main():
     if args.warmup < 3:
         args.warmup = 3
     if args.layers is None:
-        args.layers = {"sketch": W_L, "host_clock": 4, "mla_lru": 2}[args.workload]
+        args.layers = {"sketch": W_L, "host_clock": 4, "mla_lru": 2, "pooled": 12, "pooled_host": 2}[args.workload]
     if args.impl == "reference":
         run_reference(args)
     elif args.workload == "sketch":

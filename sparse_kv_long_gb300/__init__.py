@@ -346,3 +346,27 @@ def host_register(host_ptr: int, nbytes: int) -> int:
 
 def host_unregister(host_ptr: int) -> None:
     _check("skv_host_unregister", _load().skv_host_unregister(ctypes.c_void_p(host_ptr)))
+
+
+class HostView:
+    """A shaped handle on the device alias of registered host memory.
+
+    It stands in for a tensor argument that a call reads through its pointer
+    (and, for `pool_keys`, its shape), so K/V rows or raw indexer keys can be
+    read zero-copy from the host tier.  Nothing is copied.
+    """
+
+    def __init__(self, alias: int, shape, element_size: int):
+        self.alias, self.shape, self._es = int(alias), tuple(int(s) for s in shape), int(element_size)
+
+    def data_ptr(self) -> int:
+        return self.alias
+
+    def element_size(self) -> int:
+        return self._es
+
+    def numel(self) -> int:
+        n = 1
+        for s in self.shape:
+            n *= s
+        return n

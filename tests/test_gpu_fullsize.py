@@ -79,3 +79,70 @@ def test_sketch_workload_full_size_layer_step(skv, orc):
                      Hkv, d, d, k_scale=kss, v_scale=vss, req_row_stride=n)
     err = np.max(np.abs(T.host(w.out[0]) - ref))
     assert err < 2e-3, err
+
+
+@pytest.mark.parametrize("kv_host", [False, True], ids=["hbm", "host"])
+def test_pooled_workload_full_size_layer_step(skv, orc, kv_host):
+    """One layer-step of the pooled workload -- 4 requests x 1,048,576 tokens,
+    16 query / 2 KV heads, bf16 K/V, 128-dim indexer keys pooled by 4, top 512
+    blocks -- built and launched by the benchmark's own code, K/V (and the raw
+    indexer keys) in HBM or in registered host memory read zero-copy:
+
+    * pooled keys: all 262,144 blocks per request bit-exact (the one the
+      current token completes was pooled again inside the step);
+    * selection: equal counts; block sets differ only where the oracle's fp32
+      score is within 1e-3 relative of the 512-th; each block expands to its
+      4 tokens in ascending order;
+    * attention: every output within 2e-3 of the fp64 oracle on the GPU's rows.
+    """
+    import bench
+    w = bench.PooledWorkloadGPU(torch, skv, wl, torch.device("cuda", 0), layers=1, kv_host=kv_host)
+    try:
+        P = w.P
+        B, Tn, Hkv, d, di = P.B, P.T, P.Hkv, P.d, P.d_idx
+        w.layer(0)
+        torch.cuda.synchronize()
+        assert int(w.status.item()) == 0
+        kv_bytes = B * Tn * Hkv * d * 2
+        if kv_host:
+            raw_all = w.hosts[0].arr.view(np.uint16)
+            raw = raw_all[kv_bytes:].reshape(B, Tn, di)               # after K and V, in uint16 units
+        else:
+            raw = T.host(w.keys[0])
+        pooled = T.host(w.pooled[0])
+        for b in range(B):
+            np.testing.assert_array_equal(pooled[b], orc.pool_keys(raw[b], P.ratio))
+
+        L = np.full((B,), Tn, np.int32)
+        sc = orc.index_score(orc.POOLED_BF16, T.host(w.qidx[0]), pooled, L, ratio=P.ratio)
+        ridx, rcnt = orc.topk_select(sc["okey"], L, P.k_blocks, ratio=P.ratio, max_rows=P.max_rows)
+        gidx, gcnt = T.host(w.idx), T.host(w.cnt)
+        np.testing.assert_array_equal(gcnt, rcnt)
+        n = int(gcnt[0])
+        assert n == P.ratio * P.k_blocks
+        for b in range(B):
+            g = gidx[b, :n].reshape(-1, P.ratio)
+            np.testing.assert_array_equal(g - g[:, :1], np.tile(np.arange(P.ratio), (g.shape[0], 1)))
+            assert np.all(g[:, 0] % P.ratio == 0) and np.all(np.diff(g[:, 0]) > 0)
+            kth = np.sort(sc["fscore"][b, :w.nb])[::-1][P.k_blocks - 1]
+            gb, rb = set((g[:, 0] // P.ratio).tolist()), set((ridx[b, :n:P.ratio] // P.ratio).tolist())
+            for blk in gb ^ rb:
+                assert abs(sc["fscore"][b, blk] - kth) <= 1e-3 * abs(kth)
+
+        # attention on the GPU-selected rows, gathered for the oracle
+        if kv_host:
+            hk = raw_all[:kv_bytes // 2].reshape(B, Tn, Hkv, d)
+            hv = raw_all[kv_bytes // 2:kv_bytes].reshape(B, Tn, Hkv, d)
+            ks = np.stack([hk[b, gidx[b, :n]] for b in range(B)])
+            vs = np.stack([hv[b, gidx[b, :n]] for b in range(B)])
+        else:
+            phys = (torch.arange(B, device="cuda")[:, None] * Tn + w.idx[:, :n].long()).reshape(-1)
+            ks, vs = T.host(w.K[0][phys]), T.host(w.V[0][phys])
+        rows = np.tile(np.arange(n, dtype=np.int32), (B, 1))
+        ref = orc.attend(orc.KV_BF16, T.host(w.q[0]), ks.reshape(B * n, -1), vs.reshape(B * n, -1), rows, gcnt,
+                         1 / math.sqrt(d), Hkv, d, d, req_row_stride=n)
+        err = np.max(np.abs(T.host(w.out) - ref))
+        assert err < 2e-3, err
+    finally:
+        torch.cuda.synchronize()
+        w.close()

@@ -11,6 +11,7 @@ int8 rows (identical bytes on both sides), so the index sets must be
 bit-exact.
 """
 import math
+import mmap
 
 import numpy as np
 import pytest
@@ -118,11 +119,14 @@ def test_sketch_workload_small_bit_exact_sets(skv, orc, lengths):
     assert err < 2e-3, err
 
 
-def test_pooled_workload_small_end_to_end(skv, orc):
+@pytest.mark.parametrize("kv_host", [False, True], ids=["hbm", "host"])
+def test_pooled_workload_small_end_to_end(skv, orc, kv_host):
     """Pooled indexer (ratio 4) -> fused score+select -> block expansion ->
     bf16 attention, 16 query / 2 KV heads.  Pooled keys bit-exact; selections
     may differ only within 1e-3 relative of the k-th block score; attention
-    within 2e-3 of the oracle on the GPU-selected rows."""
+    within 2e-3 of the oracle on the GPU-selected rows.  With kv_host the raw
+    indexer keys and the K/V rows are read zero-copy from registered host
+    memory (only the pooled keys live in HBM)."""
     B, Hq, Hkv, d, d_idx, kb = 2, 16, 2, 256, 128, 512
     lengths = [40003, 12000]
     x = wl.pooled_inputs_cpu(B, lengths, Hq, Hkv, d, d_idx, seed=23)
@@ -130,8 +134,36 @@ def test_pooled_workload_small_end_to_end(skv, orc):
     Tcap = x["K"].shape[1]
     Tcap4 = x["idx_keys"].shape[1]
     nb_cap = Tcap4 // 4
+    mm = None
+    if kv_host:
+        parts = [np.ascontiguousarray(x["idx_keys"]), np.ascontiguousarray(x["K"]), np.ascontiguousarray(x["V"])]
+        sizes = [a.nbytes for a in parts]
+        mm = mmap.mmap(-1, sum(sizes))
+        harr = np.frombuffer(mm, dtype=np.uint8, count=sum(sizes))
+        off = 0
+        for a in parts:
+            harr[off:off + a.nbytes] = a.view(np.uint8).reshape(-1)
+            off += a.nbytes
+        alias = skv.host_register(harr.ctypes.data, harr.nbytes)
+        keys = skv.HostView(alias, x["idx_keys"].shape, 2)
+        Kd = skv.HostView(alias + sizes[0], (B * Tcap, Hkv, d), 2)
+        Vd = skv.HostView(alias + sizes[0] + sizes[1], (B * Tcap, Hkv, d), 2)
+    else:
+        keys = T.bf16_dev(x["idx_keys"])
+        Kd = T.bf16_dev(x["K"].reshape(B * Tcap, Hkv, d))
+        Vd = T.bf16_dev(x["V"].reshape(B * Tcap, Hkv, d))
+    try:
+        _pooled_chain_check(skv, orc, x, B, Hq, Hkv, d, d_idx, kb, L, Tcap, nb_cap, keys, Kd, Vd)
+    finally:
+        if kv_host:
+            torch.cuda.synchronize()
+            skv.host_unregister(harr.ctypes.data)
+            del harr
+            mm.close()
+
+
+def _pooled_chain_check(skv, orc, x, B, Hq, Hkv, d, d_idx, kb, L, Tcap, nb_cap, keys, Kd, Vd):
     # GPU: pool, score + select, attend
-    keys = T.bf16_dev(x["idx_keys"])
     pooled = torch.zeros((B, nb_cap, d_idx), dtype=torch.bfloat16, device="cuda")
     skv.pool_keys(keys, pooled, 0, nb_cap)
     max_rows = 4 * kb + 3
@@ -143,9 +175,8 @@ def test_pooled_workload_small_end_to_end(skv, orc):
                      status=st)
     out = torch.zeros((B, Hq, d), dtype=torch.float32, device="cuda")
     aws = torch.zeros((skv.attend_workspace_size(B, Hq, Hkv, d, max_rows),), dtype=torch.uint8, device="cuda")
-    skv.sparse_attend_decode(skv.KV_BF16, T.bf16_dev(x["q"]), T.bf16_dev(x["K"].reshape(B * Tcap, Hkv, d)),
-                             T.bf16_dev(x["V"].reshape(B * Tcap, Hkv, d)), idx, cnt, 1 / math.sqrt(d), out, aws,
-                             Hkv, req_row_stride=Tcap, status=st)
+    skv.sparse_attend_decode(skv.KV_BF16, T.bf16_dev(x["q"]), Kd, Vd, idx, cnt, 1 / math.sqrt(d), out, aws,
+                             Hkv, req_row_stride=Tcap, n_pool_rows=B * Tcap, status=st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     # oracle
@@ -177,7 +208,6 @@ def test_host_clock_workload_small_end_to_end(skv, orc):
     requantised to int8) -> int8 attention over the request's HBM pool of
     sinks, tail ring and hot slots, over several decode steps with a drifting
     query.  Index sets, row ids and the pool bit-exact; attention within 2e-3."""
-    import mmap
     B, Hq, Hkv, d, r, k, S, W = 2, 24, 4, 256, 64, 512, 64, 256
     lengths = [20000, 12001]
     x = wl.sketch_inputs_cpu(B, lengths, Hq, Hkv, d, r, seed=31)

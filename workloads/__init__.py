@@ -300,3 +300,27 @@ def lowrank_rows_torch(gen, n: int, U_dev, noise: float = 0.3, out_dtype=None):
 
 def randn_torch(gen, shape, device="cuda", dtype=None):
     return torch.randn(shape, generator=gen, device=device, dtype=torch.float32).to(dtype or torch.bfloat16)
+
+
+def pooled_index_keys_torch(gen, B: int, T: int, q_idx, ratio: int = 4, clusters: int = 16,
+                            cluster_blocks: int = 32, device="cuda"):
+    """Device version of the pooled workload's raw indexer keys (torch RNG).
+
+    Keys N(0,1) bf16 [B][T][d_idx], except `clusters` runs of `cluster_blocks`
+    consecutive blocks per request at seeded random block offsets, whose keys
+    are 1.5 * sqrt(d_idx) * unit(q_idx[b]) + N(0,1).
+    """
+    d_idx = q_idx.shape[-1]
+    keys = torch.empty((B, T, d_idx), dtype=torch.bfloat16, device=device)
+    nb = T // ratio
+    for b in range(B):
+        x = torch.randn((T, d_idx), generator=gen, device=device, dtype=torch.float32)
+        if nb > cluster_blocks:
+            u = q_idx[b].float()
+            u = u / u.norm()
+            starts = torch.randperm(nb - cluster_blocks, generator=gen, device=device)[:clusters].tolist()
+            for s0 in starts:
+                x[s0 * ratio:(s0 + cluster_blocks) * ratio] += 1.5 * math.sqrt(d_idx) * u
+        keys[b].copy_(x)
+        del x
+    return keys
