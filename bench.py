@@ -20,6 +20,7 @@ x 8.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -694,8 +695,8 @@ class PooledWorkloadGPU:
 
     KERNELS_PER_LAYER = 3  # pool the block the current token completes, score + select, attention
 
-    def __init__(self, torch, skv, wl, dev, layers, kv_host=False):
-        P = wl.POOLED
+    def __init__(self, torch, skv, wl, dev, layers, kv_host=False, context=None):
+        P = wl.POOLED if not context else dataclasses.replace(wl.POOLED, T=context)
         self.P, self.torch, self.skv, self.L, self.kv_host = P, torch, skv, layers, kv_host
         B, Tn, Hkv, d, di = P.B, P.T, P.Hkv, P.d, P.d_idx
         gen = wl.device_generator(SEED + 303, device=dev)
@@ -783,7 +784,7 @@ class PooledWorkloadGPU:
                 "layers": self.L, "q_heads": P.Hq, "kv_heads": P.Hkv, "head_dim": P.d, "indexer_dim": P.d_idx,
                 "ratio": P.ratio, "top_blocks": P.k_blocks, "rows": self.rows,
                 "kv": "registered host memory, zero-copy" if self.kv_host else "HBM",
-                "l2": "inputs larger than L2: pooled keys 268 MB per layer"}
+                "l2": f"inputs larger than L2: pooled keys {P.B * self.nb * P.d_idx * 2 / 1e6:.0f} MB per layer"}
 
 
 def run_extra(args):
@@ -804,7 +805,8 @@ def run_extra(args):
     elif args.workload == "host_clock":
         w = HostClockWorkloadGPU(torch, skv, wl, dev, args.layers, n_steps, eta=args.eta)
     else:
-        w = PooledWorkloadGPU(torch, skv, wl, dev, args.layers, kv_host=args.workload == "pooled_host")
+        w = PooledWorkloadGPU(torch, skv, wl, dev, args.layers, kv_host=args.workload == "pooled_host",
+                              context=args.context)
     stream = torch.cuda.Stream()
     nolog = lambda name: None
 
@@ -944,7 +946,8 @@ def main():
                     choices=["sketch", "host_clock", "mla_lru", "pooled", "pooled_host"],
                     help="sketch: the headline line; the others print their own line")
     ap.add_argument("--eta", type=float, default=0.35, help="query drift per step (host_clock)")
-    ap.add_argument("--context", type=int, default=None, help="mla_lru: tokens per request (default 142,000; "
+    ap.add_argument("--context", type=int, default=None, help="mla_lru, pooled: tokens per request (default "
+                    "142,000 and 1,048,576; "
                     "smaller only for profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -12,19 +12,21 @@
 //   1. streams its chunk of indexer rows (the same loops, hence the same
 //      scores, as skv_index_score: coalesced 16-byte loads, eight in flight
 //      per lane) and keeps the order keys in shared memory;
-//   2. works on rel = key - base, where every candidate's rel fits in `bits`
-//      bits: int32 sketch scores are bounded (|s| < 2^20), so base is fixed;
-//      for fp32 scores the CTAs first agree on the key range (one barrier);
+//   2. works on rel = key - base: int32 sketch scores are bounded
+//      (|s| < 2^20), so rel fits 21 bits above a fixed base; fp32 order keys
+//      take all 32 bits;
 //   3. radix passes over rel, top digits first: each non-final pass (<= 13
 //      bits) histograms the keys still matching the prefix, adds the bins to
 //      the request's global histogram, and after a request-wide barrier every
-//      CTA derives the same digit;
-//   4. the final pass (<= 8 bits) publishes per-CTA bins plus the count of
-//      keys above the prefix; after one barrier every CTA knows the exact k-th
-//      key K*, how many keys equal to K* are taken, and -- from the chunks
-//      before it -- where its own picks go; it writes them in ascending index
-//      order (equal keys: lowest index first).
-// int32 scores need two barriers, fp32 scores three or four.  A barrier is a
+//      CTA derives the same digit (the first pass reads back only windows of
+//      bins below the highest occupied one);
+//   4. the final pass (8 bits) adds its bins to a request-wide histogram and
+//      publishes per-CTA suffix counts (keys above the prefix plus keys in
+//      bins >= d, for every d); after one barrier every CTA knows the exact
+//      k-th key K*, how many keys equal to K* are taken, and -- from two
+//      counts per earlier chunk -- where its own picks go; it writes them in
+//      ascending index order (equal keys: lowest index first).
+// int32 scores need two barriers, fp32 scores three.  A barrier is a
 // monotonic arrival counter (release add, acquire poll); the last CTA to
 // leave resets it.  Polls are bounded: a wait that runs out sets
 // SKV_DEV_TIMEOUT and the kernel goes on.  The cooperative launch guarantees
@@ -41,7 +43,7 @@ constexpr int kMaxDigit = 13;                    // bits of a non-final pass
 constexpr int kBins = 1 << kMaxDigit;
 constexpr int kLastBits = 8;                     // bits of the final pass
 constexpr int kLastBins = 1 << kLastBits;
-constexpr int kFin = 4 + kLastBins;              // per-CTA final record: above count, pad, bins
+constexpr int kFin = 4 + kLastBins;              // per-CTA final record: kLastBins + 1 suffix counts, pad
 constexpr int kCMax = 512;                       // CTAs per request
 constexpr long kSpinLimit = 1L << 21;            // bounded barrier polls (well under a second)
 constexpr size_t kKeyBudget = 96 * 1024;         // shared memory for the chunk's order keys
@@ -49,14 +51,16 @@ constexpr uint32_t kInt4Base = 0x80000000u - (1u << 20);  // order key of score 
 constexpr int kWin = 1024;                                 // bins read back per window (int4 first pass)
 
 struct Ws {
-  unsigned* bar;   // [B][2]: arrivals (monotonic within a launch), exits
-  unsigned* rng;   // [B][2]: largest key, largest inverted key (= ~smallest key)
-  unsigned* hist;  // [2][B][kBins]: non-final passes
-  int* fin;        // [B][kCMax][kFin]: final pass, per CTA
+  unsigned* bar;    // [B][2]: arrivals (monotonic within a launch), exits
+  unsigned* rng;    // [B][2]: highest occupied first-pass bin + 1
+  unsigned* hist;   // [2][B][kBins]: non-final passes
+  int* fin;         // [B][kCMax][kFin]: final pass, per CTA suffix counts
+  unsigned* fhist;  // [B][kLastBins]: final pass, request-wide bins
 };
 
 size_t ws_bytes(int B) {
-  const size_t words = 2ull * B + 2ull * B + 2ull * B * kBins + static_cast<size_t>(B) * kCMax * kFin;
+  const size_t words = 2ull * B + 2ull * B + 2ull * B * kBins + static_cast<size_t>(B) * kCMax * kFin +
+                       static_cast<size_t>(B) * kLastBins;
   return (words * 4 + 255) / 256 * 256;
 }
 
@@ -70,6 +74,8 @@ Ws ws_carve(void* base, int B) {
   w.hist = p;
   p += 2ull * B * kBins;
   w.fin = reinterpret_cast<int*>(p);
+  p += static_cast<size_t>(B) * kCMax * kFin;
+  w.fhist = p;
   return w;
 }
 
@@ -282,7 +288,7 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
   extern __shared__ uint32_t skey[];
   __shared__ __align__(16) uint32_t hist[kBins];
   __shared__ int wgt[kWarpsF], weq[kWarpsF];
-  __shared__ unsigned red_a[kWarpsF], red_b[kWarpsF];
+  __shared__ unsigned red_a[kWarpsF];
   __shared__ uint32_t s_digit, s_above;
   __shared__ int s_before[2];
 
@@ -324,13 +330,10 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
   const int len = static_cast<int>(c1 - c0);
 
   // ---- 1. scores of the chunk into shared memory -----------------------------------
-  unsigned kmax = 0u, kinv = 0u;
   uint32_t* gk = a.okeys ? a.okeys + static_cast<int64_t>(b) * a.n_cap : nullptr;
   auto keep = [&](int64_t t, uint32_t key) {
     skey[t - c0] = key;
     if (gk) gk[t] = key;
-    kmax = max(kmax, key);
-    kinv = max(kinv, ~key);
   };
   if (MODE == SKV_SCORE_SKETCH_INT4) {
     constexpr int width = LPT * 32;
@@ -358,38 +361,11 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
   }
 
   // ---- 2. the range of rel = key - base ----------------------------------------------
-  uint32_t base;
-  int bits;
-  if (MODE == SKV_SCORE_SKETCH_INT4) {
-    base = kInt4Base;  // |score| < 2^20 for any int8 query and int4 codes, width <= 512
-    bits = 21;
-    __syncthreads();
-  } else {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
-      kinv = max(kinv, __shfl_xor_sync(0xffffffffu, kinv, o));
-    }
-    if (lane == 0) {
-      red_a[warp] = kmax;
-      red_b[warp] = kinv;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0 && len > 0) {
-      unsigned m1 = 0u, m2 = 0u;
-      for (int i = 0; i < kWarpsF; i++) {
-        m1 = max(m1, red_a[i]);
-        m2 = max(m2, red_b[i]);
-      }
-      atomicMax(&w.rng[2 * b], m1);
-      atomicMax(&w.rng[2 * b + 1], m2);
-    }
-    req_barrier(arrive, ++nbar * C, a.status);
-    const unsigned gmax = __ldcg(&w.rng[2 * b]);
-    const unsigned gmin = ~__ldcg(&w.rng[2 * b + 1]);
-    base = gmin;
-    bits = gmax == gmin ? 0 : 32 - __clz(gmax - gmin);
-  }
+  // int4 scores fit 21 bits above a fixed base; fp32 order keys take all 32
+  // (three passes: 13 windowed, 11, 8 bits).
+  const uint32_t base = MODE == SKV_SCORE_SKETCH_INT4 ? kInt4Base : 0u;
+  const int bits = MODE == SKV_SCORE_SKETCH_INT4 ? 21 : 32;  // int4: |score| < 2^20, width <= 512
+  __syncthreads();
 
   // ---- 3. non-final radix passes ---------------------------------------------------
   uint32_t need = static_cast<uint32_t>(a.k);
@@ -409,9 +385,9 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
     }
     __syncthreads();
     unsigned* gh = w.hist + (static_cast<size_t>(pass) * a.B + b) * kBins;
-    // int4 first pass: the request's highest occupied bin is published too, so
-    // that only a window of bins below it has to be read back.
-    const bool windowed = MODE == SKV_SCORE_SKETCH_INT4 && pass == 0;
+    // First pass: the request's highest occupied bin is published too, so that
+    // only a window of bins below it has to be read back.
+    const bool windowed = pass == 0;
     unsigned top_local = 0u;
     for (int i = threadIdx.x; i < nb; i += blockDim.x)
       if (hist[i]) {
@@ -491,119 +467,81 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
   }
 
   // ---- 4. final pass: K*, ties, and this CTA's offsets ------------------------------
-  uint32_t kstar;
-  uint32_t need_eq;  // keys equal to K* that are taken (lowest index first)
-  if (wlast == 0) {  // every candidate has the same key
-    kstar = base;
-    need_eq = need;
-    if (threadIdx.x == 0) {
-      s_before[0] = 0;
-      s_before[1] = static_cast<int>(c0 - lo);
-    }
-  } else {
-    const int nbf = 1 << wlast;
-    for (int i = threadIdx.x; i < nbf; i += blockDim.x) hist[i] = 0u;
-    if (threadIdx.x == 0) s_above = 0u;
-    __syncthreads();
-    unsigned above_local = 0u;
-    for (int i = threadIdx.x; i < len; i += blockDim.x) {
-      const uint32_t rel = skey[i] - base;
-      const uint32_t t = rel >> wlast;
-      if (t == P)
-        atomicAdd(&hist[rel & static_cast<uint32_t>(nbf - 1)], 1u);
-      else if (t > P)
-        above_local++;
-    }
+  // The request-wide bins of the last digit go to global memory by atomics.
+  // Each CTA also publishes suffix counts rec[d] = (its keys above the prefix)
+  // + (its keys in bins >= d), d = 0..nbf, so that a later CTA gets the keys
+  // above K* and equal to K* of every earlier chunk from two words each.
+  constexpr int nbf = kLastBins;  // wlast == kLastBits: bits >= 21 in every mode
+  for (int i = threadIdx.x; i < nbf; i += blockDim.x) hist[i] = 0u;
+  if (threadIdx.x == 0) s_above = 0u;
+  __syncthreads();
+  unsigned above_local = 0u;
+  for (int i = threadIdx.x; i < len; i += blockDim.x) {
+    const uint32_t rel = skey[i] - base;
+    const uint32_t t = rel >> wlast;
+    if (t == P)
+      atomicAdd(&hist[rel & static_cast<uint32_t>(nbf - 1)], 1u);
+    else if (t > P)
+      above_local++;
+  }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) above_local += __shfl_xor_sync(0xffffffffu, above_local, o);
-    if (lane == 0 && above_local) atomicAdd(&s_above, above_local);
-    __syncthreads();
-    // Record: [0] keys above the prefix, [1..3] unused, [4 + d] bin d.
-    int* myfin = w.fin + (static_cast<size_t>(b) * kCMax + c) * kFin;
-    if (threadIdx.x < 4) myfin[threadIdx.x] = threadIdx.x == 0 ? static_cast<int>(s_above) : 0;
-    for (int i = threadIdx.x; i < kLastBins; i += blockDim.x) myfin[4 + i] = i < nbf ? static_cast<int>(hist[i]) : 0;
-    req_barrier(arrive, ++nbar * C, a.status);
-    // Every record of the request, read once (16-byte loads, all in flight):
-    // the request-wide bins, and the records of the chunks before this one.
-    for (int i = threadIdx.x; i < nbf; i += blockDim.x) hist[i] = 0u;
-    __syncthreads();
-    const int4* rf4 = reinterpret_cast<const int4*>(w.fin + static_cast<size_t>(b) * kCMax * kFin);
-    constexpr int kQ = kFin / 4;  // 16-byte pieces per record
-    const int nq = C * kQ;
-    constexpr int kPerF = 8;
-    int4 rv[kPerF];
-    // pieces beyond the unrolled window are read in a second loop
+  for (int o = 16; o > 0; o >>= 1) above_local += __shfl_xor_sync(0xffffffffu, above_local, o);
+  if (lane == 0 && above_local) atomicAdd(&s_above, above_local);
+  __syncthreads();
+  unsigned* gf = w.fhist + static_cast<size_t>(b) * kLastBins;
+  int* myfin = w.fin + (static_cast<size_t>(b) * kCMax + c) * kFin;
+  for (int i = threadIdx.x; i < nbf; i += blockDim.x)
+    if (hist[i]) atomicAdd(&gf[i], hist[i]);
+  if (warp == 0) {  // lane l owns bins [8l, 8l + 8); suffix sums from the top
+    constexpr int kPerLane = nbf / 32;
+    unsigned v[kPerLane], own = 0u;
 #pragma unroll
-    for (int j = 0; j < kPerF; j++) {
-      const int e = threadIdx.x + j * kThreads;
-      rv[j] = e < nq ? __ldcg(&rf4[e]) : make_int4(0, 0, 0, 0);
+    for (int j = 0; j < kPerLane; j++) {
+      v[j] = hist[kPerLane * lane + j];
+      own += v[j];
     }
+    unsigned suf = own;  // sum over lanes >= l
 #pragma unroll
-    for (int j = 0; j < kPerF; j++) {
-      const int e = threadIdx.x + j * kThreads;
-      const int q = e % kQ;
-      if (e < nq && q > 0) {
-        const int d = 4 * (q - 1);
-        const int vv[4] = {rv[j].x, rv[j].y, rv[j].z, rv[j].w};
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned y = __shfl_down_sync(0xffffffffu, suf, o);
+      if (lane + o < 32) suf += y;
+    }
+    unsigned acc = s_above + suf - own;
 #pragma unroll
-        for (int u = 0; u < 4; u++)
-          if (vv[u] && d + u < nbf) atomicAdd(&hist[d + u], static_cast<unsigned>(vv[u]));
-      }
+    for (int j = kPerLane - 1; j >= 0; j--) {
+      acc += v[j];
+      myfin[kPerLane * lane + j] = static_cast<int>(acc);
     }
-    for (int e = threadIdx.x + kPerF * kThreads; e < nq; e += blockDim.x) {
-      const int q = e % kQ;
-      if (q > 0) {
-        const int4 x = __ldcg(&rf4[e]);
-        const int d = 4 * (q - 1);
-        const int vv[4] = {x.x, x.y, x.z, x.w};
-        for (int u = 0; u < 4; u++)
-          if (vv[u] && d + u < nbf) atomicAdd(&hist[d + u], static_cast<unsigned>(vv[u]));
-      }
-    }
-    __syncthreads();
-    find_digit(hist, nbf, need, &s_digit, &s_above, a.status);
-    const uint32_t dstar = s_digit;
-    need_eq = need - s_above;
-    kstar = base + ((P << wlast) | dstar);
-    // keys of the chunks before this one: above K*, and equal to K*
-    int gb = 0, eb = 0;
-    auto tally = [&](int e, const int4& x) {
-      const int cc = e / kQ, q = e % kQ;
-      if (cc >= c) return;
-      if (q == 0) {
-        gb += x.x;
-        return;
-      }
-      const int d = 4 * (q - 1);
-      const int vv[4] = {x.x, x.y, x.z, x.w};
+    if (lane == 0) myfin[nbf] = static_cast<int>(s_above);
+  }
+  req_barrier(arrive, ++nbar * C, a.status);
+  for (int i = threadIdx.x; i < nbf; i += blockDim.x) hist[i] = __ldcg(&gf[i]);
+  __syncthreads();
+  find_digit(hist, nbf, need, &s_digit, &s_above, a.status);
+  const uint32_t dstar = s_digit;
+  const uint32_t need_eq = need - s_above;  // keys equal to K* that are taken (lowest index first)
+  const uint32_t kstar = base + ((P << wlast) | dstar);
+  // keys of the chunks before this one: above K*, and equal to K*
+  int gb = 0, eb = 0;
+  for (int cc = threadIdx.x; cc < c; cc += blockDim.x) {
+    const int* rf = w.fin + (static_cast<size_t>(b) * kCMax + cc) * kFin;
+    const int above_d = __ldcg(&rf[dstar + 1]);
+    gb += above_d;
+    eb += __ldcg(&rf[dstar]) - above_d;
+  }
 #pragma unroll
-      for (int u = 0; u < 4; u++) {
-        if (d + u > static_cast<int>(dstar))
-          gb += vv[u];
-        else if (d + u == static_cast<int>(dstar))
-          eb += vv[u];
-      }
-    };
-#pragma unroll
-    for (int j = 0; j < kPerF; j++) {
-      const int e = threadIdx.x + j * kThreads;
-      if (e < nq) tally(e, rv[j]);
-    }
-    for (int e = threadIdx.x + kPerF * kThreads; e < nq; e += blockDim.x) tally(e, __ldcg(&rf4[e]));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      gb += __shfl_xor_sync(0xffffffffu, gb, o);
-      eb += __shfl_xor_sync(0xffffffffu, eb, o);
-    }
-    if (threadIdx.x == 0) s_before[0] = s_before[1] = 0;
-    __syncthreads();
-    if (lane == 0) {
-      atomicAdd(&s_before[0], gb);
-      atomicAdd(&s_before[1], eb);
-    }
+  for (int o = 16; o > 0; o >>= 1) {
+    gb += __shfl_xor_sync(0xffffffffu, gb, o);
+    eb += __shfl_xor_sync(0xffffffffu, eb, o);
+  }
+  if (threadIdx.x == 0) s_before[0] = s_before[1] = 0;
+  __syncthreads();
+  if (lane == 0 && (gb || eb)) {
+    atomicAdd(&s_before[0], gb);
+    atomicAdd(&s_before[1], eb);
   }
   // This CTA is done with everything the request's CTAs published.  The last
-  // CTA to get here clears the range cells, the non-final histograms and the
+  // CTA to get here clears the window cells, the histograms and the
   // counters, so the workspace is ready for the next launch.
   __shared__ int s_last;
   __syncthreads();
@@ -616,6 +554,7 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
     __threadfence();
     for (int p = 0; p < pass; p++)
       for (int i = threadIdx.x; i < kBins; i += blockDim.x) w.hist[(static_cast<size_t>(p) * a.B + b) * kBins + i] = 0u;
+    for (int i = threadIdx.x; i < kLastBins; i += blockDim.x) w.fhist[static_cast<size_t>(b) * kLastBins + i] = 0u;
     if (threadIdx.x == 0) {
       w.rng[2 * b] = 0u;
       w.rng[2 * b + 1] = 0u;
