@@ -289,7 +289,7 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
   __shared__ __align__(16) uint32_t hist[kBins];
   __shared__ int wgt[kWarpsF], weq[kWarpsF];
   __shared__ unsigned red_a[kWarpsF];
-  __shared__ uint32_t s_digit, s_above;
+  __shared__ uint32_t s_digit, s_above, s_top;
   __shared__ int s_before[2];
 
   __shared__ __align__(16) int8_t s_q8[512];
@@ -330,10 +330,23 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
   const int len = static_cast<int>(c1 - c0);
 
   // ---- 1. scores of the chunk into shared memory -----------------------------------
+  // rel = key - base fits `bits` bits: int32 sketch scores are bounded
+  // (|s| < 2^20), so 21 bits above a fixed base; fp32 order keys take all 32.
+  // int32 keys: the first radix pass (the top kMaxDigit bits) is counted
+  // during the scan.  (fp32 keys crowd into a few bins of that pass, and the
+  // contended atomics would slow the scan; they are counted after it.)
+  const uint32_t base = MODE == SKV_SCORE_SKETCH_INT4 ? kInt4Base : 0u;
+  const int bits = MODE == SKV_SCORE_SKETCH_INT4 ? 21 : 32;
+  constexpr bool count0 = MODE == SKV_SCORE_SKETCH_INT4;
+  const int shift0 = bits - kMaxDigit;  // bits - kLastBits >= kMaxDigit in every mode
+  for (int i = threadIdx.x; i < kBins; i += blockDim.x) hist[i] = 0u;
+  if (threadIdx.x == 0) s_top = 0u;
+  __syncthreads();
   uint32_t* gk = a.okeys ? a.okeys + static_cast<int64_t>(b) * a.n_cap : nullptr;
   auto keep = [&](int64_t t, uint32_t key) {
     skey[t - c0] = key;
     if (gk) gk[t] = key;
+    if (count0) atomicAdd(&hist[(key - base) >> shift0], 1u);
   };
   if (MODE == SKV_SCORE_SKETCH_INT4) {
     constexpr int width = LPT * 32;
@@ -359,15 +372,10 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
                keep(t, order_key_f32(sc));
              });
   }
-
-  // ---- 2. the range of rel = key - base ----------------------------------------------
-  // int4 scores fit 21 bits above a fixed base; fp32 order keys take all 32
-  // (three passes: 13 windowed, 11, 8 bits).
-  const uint32_t base = MODE == SKV_SCORE_SKETCH_INT4 ? kInt4Base : 0u;
-  const int bits = MODE == SKV_SCORE_SKETCH_INT4 ? 21 : 32;  // int4: |score| < 2^20, width <= 512
   __syncthreads();
 
-  // ---- 3. non-final radix passes ---------------------------------------------------
+  // ---- 2. non-final radix passes ---------------------------------------------------
+  // int32 keys: one (13 bits, windowed); fp32 keys: two (13 windowed, 11).
   uint32_t need = static_cast<uint32_t>(a.k);
   uint32_t P = 0;  // rel >> rem of the keys still in play
   int rem = bits;
@@ -377,13 +385,17 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
     const int wb = rem - wlast < kMaxDigit ? rem - wlast : kMaxDigit;
     const int shift = rem - wb;
     const int nb = 1 << wb;
-    for (int i = threadIdx.x; i < nb; i += blockDim.x) hist[i] = 0u;
-    __syncthreads();
-    for (int i = threadIdx.x; i < len; i += blockDim.x) {
-      const uint32_t rel = skey[i] - base;
-      if (top_bits(rel, rem) == P) atomicAdd(&hist[(rel >> shift) & static_cast<uint32_t>(nb - 1)], 1u);
+    if (pass > 0 || !count0) {
+      if (pass > 0) {
+        for (int i = threadIdx.x; i < nb; i += blockDim.x) hist[i] = 0u;
+        __syncthreads();
+      }
+      for (int i = threadIdx.x; i < len; i += blockDim.x) {
+        const uint32_t rel = skey[i] - base;
+        if (top_bits(rel, rem) == P) atomicAdd(&hist[(rel >> shift) & static_cast<uint32_t>(nb - 1)], 1u);
+      }
+      __syncthreads();
     }
-    __syncthreads();
     unsigned* gh = w.hist + (static_cast<size_t>(pass) * a.B + b) * kBins;
     // First pass: the request's highest occupied bin is published too, so that
     // only a window of bins below it has to be read back.
@@ -394,10 +406,12 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
         atomicAdd(&gh[i], hist[i]);
         top_local = max(top_local, static_cast<unsigned>(i) + 1u);
       }
-    if (windowed) {
+    if (windowed) {  // one global atomic per CTA
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) top_local = max(top_local, __shfl_xor_sync(0xffffffffu, top_local, o));
-      if (lane == 0 && top_local) atomicMax(&w.rng[2 * b], top_local);  // bin + 1 (0: none)
+      if (lane == 0 && top_local) atomicMax(&s_top, top_local);
+      __syncthreads();
+      if (threadIdx.x == 0 && s_top) atomicMax(&w.rng[2 * b], s_top);  // bin + 1 (0: none)
     }
     req_barrier(arrive, ++nbar * C, a.status);
     if (windowed) {
@@ -466,7 +480,7 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
     pass++;
   }
 
-  // ---- 4. final pass: K*, ties, and this CTA's offsets ------------------------------
+  // ---- 3. final pass: K*, ties, and this CTA's offsets ------------------------------
   // The request-wide bins of the last digit go to global memory by atomics.
   // Each CTA also publishes suffix counts rec[d] = (its keys above the prefix)
   // + (its keys in bins >= d), d = 0..nbf, so that a later CTA gets the keys
@@ -563,7 +577,7 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
     }
   }
 
-  // ---- 5. this CTA's picks, in ascending index order ---------------------------------
+  // ---- 4. this CTA's picks, in ascending index order ---------------------------------
   // Warp v owns the contiguous piece [v*sub, (v+1)*sub) of the chunk.
   const int sub = ((len + kWarpsF - 1) / kWarpsF + 31) / 32 * 32;
   const int p0 = warp * sub, p1 = min(len, p0 + sub);
