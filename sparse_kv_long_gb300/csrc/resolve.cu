@@ -131,6 +131,7 @@ __device__ __forceinline__ void requant_group(const uint2 (&c)[4], uint16_t sbit
 
 __global__ __launch_bounds__(kClockThreads) void clock_kernel(ClockArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
+  allow_dependent_launch();  // the row fetch may be scheduled now; it waits for this grid to finish
   const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int Hs = a.Hs;
   int32_t* s_tok = reinterpret_cast<int32_t*>(smem);
@@ -311,13 +312,17 @@ __global__ __launch_bounds__(kClockThreads) void clock_kernel(ClockArgs a) {
 // One warp per miss: the token's host row (Hkv heads x [K | V] int4 vectors,
 // contiguous) is read with coalesced 16-byte loads into shared memory, then
 // each lane requantises one 64-dim group to int8 and writes it to the pool.
+// A lane issues all its loads of the row before it stores any (a host read
+// takes microseconds, so the round trips must overlap, not follow each other).
 constexpr int kFetchWarps = 8;
+constexpr int kFetchPieces = 8;  // 16-byte pieces per lane and row held in registers (rows up to 4 KB)
 
-__global__ __launch_bounds__(32 * kFetchWarps) void fetch_int4_kernel(
+__global__ __launch_bounds__(32 * kFetchWarps, 3) void fetch_int4_kernel(
     const int32_t* __restrict__ ws_tok, const int32_t* __restrict__ ws_row, const int32_t* __restrict__ n_miss,
     int max_rows, int64_t t_cap, int Hkv, int d, const uint8_t* __restrict__ host_rows, int8_t* __restrict__ k8,
     int8_t* __restrict__ v8, __half* __restrict__ k_scale, __half* __restrict__ v_scale) {
   extern __shared__ __align__(16) unsigned char stage_all[];
+  grid_dependency_wait();  // launched early: the state pass's miss list is complete from here on
   const int b = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int j = blockIdx.x * kFetchWarps + warp;
   const int nm = n_miss[b];
@@ -329,7 +334,15 @@ __global__ __launch_bounds__(32 * kFetchWarps) void fetch_int4_kernel(
   const int tb = 2 * Hkv * rb;
   unsigned char* stage = stage_all + warp * tb;
   const uint4* src = reinterpret_cast<const uint4*>(host_rows + (static_cast<int64_t>(b) * t_cap + tok) * tb);
-  for (int c = lane; c < tb / 16; c += 32) reinterpret_cast<uint4*>(stage)[c] = ld_nc16(src + c);
+  const int np = tb / 16;  // 17 d / 16 bytes per vector: a whole number of pieces for d % 256 == 0
+  uint4 v[kFetchPieces];
+#pragma unroll
+  for (int u = 0; u < kFetchPieces; u++)
+    if (lane + 32 * u < np) v[u] = ld_nc16(src + lane + 32 * u);
+#pragma unroll
+  for (int u = 0; u < kFetchPieces; u++)
+    if (lane + 32 * u < np) reinterpret_cast<uint4*>(stage)[lane + 32 * u] = v[u];
+  for (int c = lane + 32 * kFetchPieces; c < np; c += 32) reinterpret_cast<uint4*>(stage)[c] = ld_nc16(src + c);
   __syncwarp();
   for (int it = 0; it * 32 < tasks; it++) {
     const int task = it * 32 + lane;
@@ -347,37 +360,45 @@ __global__ __launch_bounds__(32 * kFetchWarps) void fetch_int4_kernel(
   }
 }
 
-// One warp per miss, kRowsPerWarp rows in flight: plain row copy host -> pool.
+// One warp per kRowsPerWarp misses: plain row copy host -> pool, every load
+// of the warp's rows (up to kFetchPieces / kRowsPerWarp pieces per lane and
+// row) issued before the first store.
 constexpr int kRowsPerWarp = 2;
 
 __global__ __launch_bounds__(32 * kFetchWarps) void fetch_rows_kernel(
     const int32_t* __restrict__ ws_tok, const int32_t* __restrict__ ws_row, const int32_t* __restrict__ n_miss,
     int max_rows, int64_t t_cap, const uint8_t* __restrict__ host, uint8_t* __restrict__ pool, int64_t row_bytes) {
+  grid_dependency_wait();  // launched early: the state pass's miss list is complete from here on
   const int b = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int j0 = (blockIdx.x * kFetchWarps + warp) * kRowsPerWarp;
   const int nm = n_miss[b];
   if (j0 >= nm) return;
   const int chunks = static_cast<int>(row_bytes / 16);
-  for (int c0 = 0; c0 < chunks; c0 += 32) {
-    const int c = c0 + lane;
-    uint4 v[kRowsPerWarp];
+  constexpr int kPer = kFetchPieces / kRowsPerWarp;
+  const uint8_t* src[kRowsPerWarp];
+  uint4* dst[kRowsPerWarp];
 #pragma unroll
-    for (int u = 0; u < kRowsPerWarp; u++) {
-      const int j = j0 + u;
-      if (c < chunks && j < nm) {
-        const int32_t tok = ws_tok[static_cast<int64_t>(b) * max_rows + j];
-        v[u] = ld_nc16(host + (static_cast<int64_t>(b) * t_cap + tok) * row_bytes + 16 * c);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kRowsPerWarp; u++) {
-      const int j = j0 + u;
-      if (c < chunks && j < nm) {
-        const int64_t row = ws_row[static_cast<int64_t>(b) * max_rows + j];
-        reinterpret_cast<uint4*>(pool + row * row_bytes)[c] = v[u];
-      }
-    }
+  for (int u = 0; u < kRowsPerWarp; u++) {
+    const int j = j0 + u < nm ? j0 + u : j0;  // j0 < nm
+    const int32_t tok = ws_tok[static_cast<int64_t>(b) * max_rows + j];
+    const int64_t row = ws_row[static_cast<int64_t>(b) * max_rows + j];
+    src[u] = host + (static_cast<int64_t>(b) * t_cap + tok) * row_bytes;
+    dst[u] = reinterpret_cast<uint4*>(pool + row * row_bytes);
   }
+  uint4 v[kRowsPerWarp][kPer];
+#pragma unroll
+  for (int u = 0; u < kRowsPerWarp; u++)
+#pragma unroll
+    for (int q = 0; q < kPer; q++)
+      if (j0 + u < nm && lane + 32 * q < chunks) v[u][q] = ld_nc16(src[u] + 16 * (lane + 32 * q));
+#pragma unroll
+  for (int u = 0; u < kRowsPerWarp; u++)
+#pragma unroll
+    for (int q = 0; q < kPer; q++)
+      if (j0 + u < nm && lane + 32 * q < chunks) dst[u][lane + 32 * q] = v[u][q];
+  for (int c = lane + 32 * kPer; c < chunks; c += 32)  // rows above kPer * 512 bytes
+    for (int u = 0; u < kRowsPerWarp; u++)
+      if (j0 + u < nm) dst[u][c] = ld_nc16(src[u] + 16 * c);
 }
 
 // ---------------------------------------------------------------------------
@@ -416,7 +437,8 @@ size_t lru_smem_bytes(int n_slots, int max_rows) {
 
 __global__ __launch_bounds__(kResThreads) void lru_kernel(LruArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
-  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  allow_dependent_launch();  // the row fetch may be scheduled now; it waits for this grid to finish
+  const int b = blockIdx.x, tid = threadIdx.x;
   const int ns = a.n_slots;
   int64_t* s_stamp = reinterpret_cast<int64_t*>(smem);
   int32_t* s_order = reinterpret_cast<int32_t*>(s_stamp + ns);  // LRU order on entry
@@ -647,6 +669,29 @@ __global__ __launch_bounds__(512) void stream_read_kernel(const uint4* __restric
 }  // namespace
 }  // namespace skv
 
+namespace skv {
+namespace {
+// A launch that may start while the previous kernel in the stream is still
+// running (programmatic dependent launch); the kernel waits for that kernel
+// with grid_dependency_wait() before it reads anything the kernel produced.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(dim3 grid, int threads, size_t smem, cudaStream_t st, void (*kernel)(KArgs...),
+                             Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+}  // namespace
+}  // namespace skv
+
 using namespace skv;
 
 SKV_EXPORT size_t skv_resolve_workspace_size(int B, int max_rows) {
@@ -691,9 +736,12 @@ SKV_EXPORT int skv_resolve_rows_clock(int B, int64_t t_cap, const int32_t* lengt
   cudaStream_t st = as_stream(stream);
   clock_kernel<<<B, kClockThreads, smem, st>>>(a);
   const dim3 fgrid((max_rows + kFetchWarps - 1) / kFetchWarps, B);
-  fetch_int4_kernel<<<fgrid, 32 * kFetchWarps, kFetchWarps * tb, st>>>(
-      ws_tok, ws_row, n_miss, max_rows, t_cap, Hkv, d, host_rows, k8, v8, reinterpret_cast<__half*>(k_scale),
-      reinterpret_cast<__half*>(v_scale));
+  if (launch_dependent(fgrid, 32 * kFetchWarps, kFetchWarps * tb, st, fetch_int4_kernel, ws_tok, ws_row, n_miss,
+                       max_rows, t_cap, Hkv, d, host_rows, k8, v8, reinterpret_cast<__half*>(k_scale),
+                       reinterpret_cast<__half*>(v_scale)) != cudaSuccess) {
+    cudaGetLastError();
+    return SKV_ECUDA;
+  }
   return launch_status();
 }
 
@@ -736,8 +784,11 @@ SKV_EXPORT int skv_resolve_rows_lru(int B, int64_t t_cap, const int32_t* lengths
   cudaStream_t st = as_stream(stream);
   lru_kernel<<<B, kResThreads, smem, st>>>(a);
   const int per_cta = kFetchWarps * kRowsPerWarp;
-  fetch_rows_kernel<<<dim3((max_rows + per_cta - 1) / per_cta, B), 32 * kFetchWarps, 0, st>>>(
-      ws_tok, ws_row, n_miss, max_rows, t_cap, host, pool, row_bytes);
+  if (launch_dependent(dim3((max_rows + per_cta - 1) / per_cta, B), 32 * kFetchWarps, 0, st, fetch_rows_kernel,
+                       ws_tok, ws_row, n_miss, max_rows, t_cap, host, pool, row_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return SKV_ECUDA;
+  }
   return launch_status();
 }
 
