@@ -536,6 +536,63 @@ int skv_stream_read(const void *src, size_t bytes, unsigned long long *sink, int
                     void *stream);
 
 /* ========================================================================== */
+/* Chunked sparse prefill ([P4] "3.14M Context on 3x 3090 ...", "The Downside */
+/* to Keep in Mind": every prefill token picks its own top blocks, so the     */
+/* loops are swapped -- the history is staged chunk by chunk into a small HBM */
+/* buffer once, every query of the prefill chunk attends to its own picks     */
+/* inside it, and the partial softmax states are merged).                     */
+/* ========================================================================== */
+/*
+ * skv_prefill_index_scores -- pooled indexer scores of a chunk of prefill
+ * queries that share one request's pooled keys:
+ *   order_keys[i][blk] = order key of sum_x q_idx[i][x] * pooled[blk][x]
+ * (fp32 accumulate of bf16 products, the POOLED_BF16 key map of
+ * skv_index_score) for every query i < nq and block blk < n_blocks; entries
+ * blk >= n_blocks are not written.  skv_topk_select with B = nq, lengths[i] =
+ * (position of query i) + 1 and ratio 4 then gives every query its causal
+ * selection.  The products are summed in tensor-core tiles, so a score agrees
+ * with skv_index_score's to fp32 rounding.  A NaN score sets SKV_DEV_NAN.
+ *   q_idx       bf16 [nq][128]           pooled  bf16 [n_blocks][128]
+ *   order_keys  u32 [nq][key_stride]
+ * Constraints: key_stride >= n_blocks and even; q_idx, pooled 16-byte
+ * aligned, order_keys 8-byte aligned.  Errors: SKV_EINVAL otherwise.
+ */
+int skv_prefill_index_scores(int nq, const uint16_t *q_idx, const uint16_t *pooled,
+                             int64_t n_blocks, uint32_t *order_keys, int64_t key_stride,
+                             int32_t *dev_status, void *stream);
+
+/*
+ * skv_prefill_attend -- exact attention of each query of a prefill chunk over
+ * its own selected tokens, loops swapped: for every history chunk [c0, c0 +
+ * chunk_tokens) below n_tokens, the chunk's K and V rows are copied once
+ * (cudaMemcpyAsync on `stream`) from k_src / v_src into the staging buffers;
+ * one launch then attends every query head to the query's selected tokens
+ * inside the chunk and merges the partial softmax state (running max m, sum
+ * l, accumulator acc) into `state`; a last launch writes out = acc / l.  For
+ * query i and query head g (KV head g / (Hq / Hkv)) the result is
+ *   out[i][g] = sum_{t in S_i} softmax_t(scale * q[i][g] . k[t]) v[t],
+ * S_i = idx[i][0 .. count[i]), which is what skv_sparse_attend_decode gives
+ * for one request with those rows, to fp32 rounding.  Host-link bytes per call:
+ * n_tokens * Hkv * d * 4 when the sources are host memory, independent of nq.
+ *   q              bf16 [nq][Hq][d]
+ *   k_src, v_src   bf16 [n_tokens][Hkv][d]: host memory registered with
+ *                  skv_host_register (HOST pointer), or device memory
+ *   k_stage, v_stage  bf16 [chunk_tokens][Hkv][d], device, caller-owned
+ *   idx            int32 [nq][max_rows], each row ascending
+ *   count          int32 [nq]
+ *   state          fp32 [nq][Hq][d + 4] scratch (no initial contents needed)
+ *   out            fp32 [nq][Hq][d]; a query with count 0 gets zeros
+ * A selected token >= n_tokens sets SKV_DEV_RANGE and is skipped.
+ * Constraints: d == 256, Hq % Hkv == 0, Hq / Hkv <= 32, chunk_tokens >= 1;
+ * q, stages 16-byte aligned.
+ */
+int skv_prefill_attend(int nq, int Hq, int Hkv, int d, const uint16_t *q, const uint16_t *k_src,
+                       const uint16_t *v_src, int64_t n_tokens, uint16_t *k_stage,
+                       uint16_t *v_stage, int64_t chunk_tokens, const int32_t *idx, int max_rows,
+                       const int32_t *count, float softmax_scale, float *state, float *out,
+                       int32_t *dev_status, void *stream);
+
+/* ========================================================================== */
 /* Host tier ([P4] "No Need to Rewrite the Kernel": allocate with anonymous    */
 /* mmap, cudaHostRegister(ptr, n, PORTABLE | MAPPED), use the device pointer). */
 /* ========================================================================== */

@@ -75,6 +75,9 @@ def _load():
                                           P, i32, P, P, P, P, sz, P, P], i32),
                 "skv_quantize_int4_rows": ([P, i64, i32, i32, P, P, i64, i64, P], i32),
                 "skv_stream_read": ([P, sz, P, i32, P], i32),
+                "skv_prefill_index_scores": ([i32, P, P, i64, P, i64, P, P], i32),
+                "skv_prefill_attend": ([i32, i32, i32, i32, P, P, P, i64, P, P, i64, P, i32, P, f32, P, P, P, P],
+                                       i32),
                 "skv_host_register": ([P, sz, ctypes.POINTER(ctypes.c_void_p)], i32),
                 "skv_host_unregister": ([P], i32),
             }
@@ -240,7 +243,7 @@ def quantize_int4_rows(x, out, token_pitch, head_pitch, out_rows=None, out_ptr=N
 # ---- a5 -------------------------------------------------------------------------
 
 def _addr(t):
-    """A tensor's device pointer, or an int device address (host alias)."""
+    """A tensor's data pointer, or an int address (a host alias or a registered host pointer)."""
     return ctypes.c_void_p(t if isinstance(t, int) else t.data_ptr())
 
 
@@ -331,6 +334,33 @@ def sparse_attend_mla(q, kv_pool, rows, count, softmax_scale, out, workspace, ro
         B, Hq, d, dv, _ptr(q), _ptr(kv_pool), _ptr(row_scale), int(req_row_stride), int(n_pool_rows), _ptr(rows),
         rows.shape[1], _ptr(count), float(softmax_scale), _ptr(out), _ptr(workspace),
         0 if workspace is None else workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream)))
+    return out
+
+
+# ---- chunked sparse prefill -------------------------------------------------------
+
+def prefill_index_scores(q_idx, pooled, order_keys, n_blocks=None, status=None, stream=None):
+    """q_idx bf16 [nq][128], pooled bf16 [n_blocks][128] -> order_keys u32 [nq][stride]."""
+    nq = q_idx.shape[0]
+    if n_blocks is None:
+        n_blocks = pooled.shape[0]
+    _check("skv_prefill_index_scores", _load().skv_prefill_index_scores(
+        nq, _ptr(q_idx), _ptr(pooled), int(n_blocks), _ptr(order_keys), order_keys.shape[1], _ptr(status),
+        _stream(stream)))
+    return order_keys
+
+
+def prefill_attend(q, k_src, v_src, n_tokens, k_stage, v_stage, idx, count, softmax_scale, state, out, Hkv,
+                   status=None, stream=None):
+    """q bf16 [nq][Hq][d]; k_src / v_src: a tensor or an int address (a registered
+    HOST pointer, or device memory) of bf16 [n_tokens][Hkv][d]; stages bf16
+    [chunk][Hkv][d]; idx int32 [nq][max_rows] ascending; state fp32 [nq][Hq][d+4]."""
+    nq, Hq, d = q.shape
+    chunk = k_stage.shape[0]
+    _check("skv_prefill_attend", _load().skv_prefill_attend(
+        nq, Hq, Hkv, d, _ptr(q), _addr(k_src), _addr(v_src), int(n_tokens), _ptr(k_stage), _ptr(v_stage),
+        int(chunk), _ptr(idx), idx.shape[1], _ptr(count), float(softmax_scale), _ptr(state), _ptr(out),
+        _ptr(status), _stream(stream)))
     return out
 
 

@@ -57,3 +57,20 @@ def test_host_side_argument_checks(lib):
     assert lib.skv_pool_keys(P(16), 0, 64, 128, 4, 0, 4, P(16), None) == 0
     assert lib.skv_pool_keys(P(16), 1, 64, 128, 4, 10, 8, P(16), None) == 1  # past capacity
     assert lib.skv_topk_workspace_size(8) > 0
+
+
+def test_prefill_argument_checks(lib):
+    P = ctypes.c_void_p
+    # scores: odd key stride, stride below n_blocks, negative nq; empty is a no-op
+    assert lib.skv_prefill_index_scores(4, P(16), P(16), 10, P(16), 11, None, None) == 1
+    assert lib.skv_prefill_index_scores(4, P(16), P(16), 10, P(16), 8, None, None) == 1
+    assert lib.skv_prefill_index_scores(-1, P(16), P(16), 10, P(16), 10, None, None) == 1
+    assert lib.skv_prefill_index_scores(0, P(16), P(16), 10, P(16), 10, None, None) == 0
+    assert lib.skv_prefill_index_scores(4, P(16), P(16), 10, P(12), 10, None, None) == 1  # keys not 8-aligned
+    # attention: head dim 256 only, Hq % Hkv, chunk >= 1; nq == 0 is a no-op
+    args = lambda nq, Hq, Hkv, d, chunk: (nq, Hq, Hkv, d, P(16), P(16), P(16), 100, P(16), P(16), chunk,
+                                          P(16), 8, P(16), 1.0, P(16), P(16), None, None)
+    assert lib.skv_prefill_attend(*args(2, 16, 2, 128, 64)) == 1
+    assert lib.skv_prefill_attend(*args(2, 16, 3, 256, 64)) == 1
+    assert lib.skv_prefill_attend(*args(2, 16, 2, 256, 0)) == 1
+    assert lib.skv_prefill_attend(*args(0, 16, 2, 256, 64)) == 0
