@@ -787,6 +787,154 @@ class PooledWorkloadGPU:
                 "l2": f"inputs larger than L2: pooled keys {P.B * self.nb * P.d_idx * 2 / 1e6:.0f} MB per layer"}
 
 
+class PrefillWorkloadGPU:
+    """Chunked sparse prefill of one attention layer: one request whose history
+    K/V (bf16, 2 KV heads x 256) sit in registered host memory, a prompt chunk
+    of 4,096 queries ending at `context` tokens, each query selecting its own
+    top 512 pooled blocks (causal), attention with the loops swapped through a
+    32 MiB staging buffer (16,384 tokens of K and V)."""
+
+    NQ, HQ, HKV, D, DI, KB, STAGE = 4096, 16, 2, 256, 128, 512, 16_384
+
+    def __init__(self, torch, skv, wl, dev, context=None):
+        self.torch, self.skv = torch, skv
+        T = self.T = context or wl.POOLED.T
+        nq, Hq, Hkv, D, DI = self.NQ, self.HQ, self.HKV, self.D, self.DI
+        gen = wl.device_generator(SEED + 606, device=dev)
+        self.nb = T // 4
+        # queries: indexer queries around one direction (their picks overlap), random attention queries
+        q0 = torch.randn((DI,), generator=gen, device=dev)
+        qi = q0 + 0.5 * torch.randn((nq, DI), generator=gen, device=dev)
+        self.q_idx = (qi / qi.norm(dim=1, keepdim=True) * q0.norm()).to(torch.bfloat16).contiguous()
+        self.q = wl.randn_torch(gen, (nq, Hq, D), device=dev)
+        keys = wl.pooled_index_keys_torch(gen, 1, T, q0[None].to(torch.bfloat16), 4, 16, 32, device=dev)
+        self.pooled = torch.empty((1, self.nb, DI), dtype=torch.bfloat16, device=dev)
+        skv.pool_keys(keys, self.pooled, 0, self.nb)
+        del keys
+        kv_bytes = T * Hkv * D * 2
+        self.host = HostTier(skv, 2 * kv_bytes)
+        hv = torch.from_numpy(self.host.arr)
+        step = 1 << 18
+        for half in range(2):
+            dst = hv[half * kv_bytes:(half + 1) * kv_bytes].view(torch.bfloat16).view(T, Hkv, D)
+            for t0 in range(0, T, step):
+                dst[t0:t0 + step].copy_(wl.randn_torch(gen, (min(step, T - t0), Hkv, D), device=dev))
+        torch.cuda.synchronize()
+        self.k_src, self.v_src = self.host.addr, self.host.addr + kv_bytes
+        self.kv_bytes = kv_bytes
+        self.pos = torch.arange(T - nq, T, dtype=torch.int32, device=dev)
+        self.lengths = (self.pos + 1).contiguous()
+        self.stride = self.nb + (self.nb & 1)
+        self.keys = torch.empty((nq, self.stride), dtype=torch.int32, device=dev)
+        self.max_rows = 4 * self.KB + 3
+        self.idx = torch.zeros((nq, self.max_rows), dtype=torch.int32, device=dev)
+        self.cnt = torch.zeros((nq,), dtype=torch.int32, device=dev)
+        self.tws = torch.zeros((skv.topk_workspace_size(nq),), dtype=torch.uint8, device=dev)
+        self.kst = torch.empty((self.STAGE, Hkv, D), dtype=torch.bfloat16, device=dev)
+        self.vst = torch.empty_like(self.kst)
+        self.state = torch.empty((nq, Hq, D + 4), dtype=torch.float32, device=dev)
+        self.out = torch.empty((nq, Hq, D), dtype=torch.float32, device=dev)
+        self.status = torch.zeros((1,), dtype=torch.int32, device=dev)
+        torch.cuda.synchronize()
+
+    def step(self, ev=lambda name: None):
+        skv, st = self.skv, self.status
+        ev("sc0")
+        skv.prefill_index_scores(self.q_idx, self.pooled[0], self.keys, n_blocks=self.nb, status=st)
+        ev("tk0")
+        skv.topk_select(self.keys, self.lengths, self.KB, self.idx, self.cnt, self.tws, ratio=4, status=st)
+        ev("at0")
+        skv.prefill_attend(self.q, self.k_src, self.v_src, self.T, self.kst, self.vst, self.idx, self.cnt,
+                           1 / math.sqrt(self.D), self.state, self.out, self.HKV, status=st)
+        ev("end")
+
+    def close(self):
+        self.host.close()
+
+
+def run_prefill(args):
+    import torch
+
+    import sparse_kv_long_gb300 as skv
+    import workloads as wl
+    from sparse_kv_long_gb300 import _build
+
+    torch.cuda.set_device(0)
+    _build.build()
+    dev = torch.device("cuda", 0)
+    w = PrefillWorkloadGPU(torch, skv, wl, dev, context=args.context)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            w.step()
+    torch.cuda.synchronize()
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(0).uuid)
+    except Exception:
+        gpu_id = "0"
+    marks = {}
+
+    def ev(name):
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(stream)
+        marks.setdefault(name, []).append(e)
+
+    with ClockSampler(gpu_id) as clk:
+        time.sleep(0.3)
+        with torch.cuda.stream(stream):
+            for _ in range(args.steps):
+                w.step(ev)
+        torch.cuda.synchronize()
+    ms = marks["sc0"][0].elapsed_time(marks["end"][-1]) / args.steps
+    per = {n: statistics.median(marks[a][s].elapsed_time(marks[b][s]) for s in range(args.steps))
+           for n, a, b in (("scores", "sc0", "tk0"), ("topk", "tk0", "at0"), ("attend", "at0", "end"))}
+    # host-link probe over the history's K half
+    sink = torch.zeros((1,), dtype=torch.int64, device=dev)
+    nbytes = (w.kv_bytes // 16) * 16
+    alias = w.host.alias
+    skv.stream_read(alias, nbytes, sink)
+    h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    h0.record()
+    skv.stream_read(alias, nbytes, sink)
+    h1.record()
+    torch.cuda.synchronize()
+    host_gbs = nbytes / (h0.elapsed_time(h1) * 1e-3) / 1e9
+    peaks_d = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+        os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    hbm = float(peaks_d.get("hbm_gbs", 6800.0))
+    link_bytes = 2 * w.kv_bytes
+    naive_bytes = float(w.cnt.sum().item()) * w.HKV * w.D * 2 * 2
+    flops = 2.0 * w.NQ * w.nb * w.DI
+    key_bytes = 4.0 * w.NQ * w.nb
+    kern = {
+        "prefill_scores": {"us": 1e3 * per["scores"], "bound": "hbm", "work_bytes": key_bytes + w.nb * w.DI * 2,
+                           "rule": f"4 B order key per (query, block) written + pooled keys read once: "
+                                   f"{w.NQ} x {w.nb}", "tflops": flops / (per["scores"] * 1e-3) / 1e12},
+        "topk_select": {"us": 1e3 * per["topk"], "bound": "hbm", "work_bytes": key_bytes,
+                        "rule": "order keys read (one pass) per query"},
+        "prefill_attend": {"us": 1e3 * per["attend"], "bound": "host", "work_bytes": link_bytes,
+                           "rule": "history K and V staged once over the host link"},
+    }
+    for k, blk in kern.items():
+        ach = blk["work_bytes"] / (blk["us"] * 1e-6) / 1e9
+        peak = host_gbs if blk["bound"] == "host" else hbm
+        blk.update(achieved=ach, peak=peak, unit="GB/s", frac=ach / peak)
+    line = {"workload": "prefill", "metric": "prefill tokens/s (one attention layer)",
+            "value": w.NQ / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "data": "synthetic",
+            "config": {"workload": f"prefill_{w.NQ}q_at_{w.T}_bf16kv_host", "prompt_chunk": w.NQ,
+                       "context": w.T, "q_heads": w.HQ, "kv_heads": w.HKV, "head_dim": w.D,
+                       "top_blocks": w.KB, "staging_tokens": w.STAGE,
+                       "staging_mib": 2 * w.STAGE * w.HKV * w.D * 2 / 2 ** 20,
+                       "l2": "inputs larger than L2: 4.3 GB of order keys, 2 GiB host history per step"},
+            "host_bytes_per_step": link_bytes, "naive_host_bytes_per_step": naive_bytes,
+            "host_bytes_reduction": naive_bytes / link_bytes, "host_read_gbs_probe": host_gbs,
+            "kernels": kern, "clocks": clk.summary(), "device_status": int(w.status.item()),
+            "gpu_launches": args.steps * (1 + 5 + (w.T + w.STAGE - 1) // w.STAGE + 1)}
+    print(json.dumps(line), flush=True)
+    w.close()
+
+
 def run_extra(args):
     import torch
 
@@ -943,7 +1091,7 @@ def main():
     ap.add_argument("--layers", type=int, default=None, help="distinct layers (16 for the sketch workload; "
                     "fewer only for profiler captures)")
     ap.add_argument("--workload", default="sketch",
-                    choices=["sketch", "host_clock", "mla_lru", "pooled", "pooled_host"],
+                    choices=["sketch", "host_clock", "mla_lru", "pooled", "pooled_host", "prefill"],
                     help="sketch: the headline line; the others print their own line")
     ap.add_argument("--eta", type=float, default=0.35, help="query drift per step (host_clock)")
     ap.add_argument("--context", type=int, default=None, help="mla_lru, pooled: tokens per request (default "
@@ -953,11 +1101,14 @@ def main():
     if args.warmup < 3:
         args.warmup = 3
     if args.layers is None:
-        args.layers = {"sketch": W_L, "host_clock": 4, "mla_lru": 2, "pooled": 12, "pooled_host": 2}[args.workload]
+        args.layers = {"sketch": W_L, "host_clock": 4, "mla_lru": 2, "pooled": 12, "pooled_host": 2,
+                       "prefill": 1}[args.workload]
     if args.impl == "reference":
         run_reference(args)
     elif args.workload == "sketch":
         run_gpu(args)
+    elif args.workload == "prefill":
+        run_prefill(args)
     else:
         run_extra(args)
 

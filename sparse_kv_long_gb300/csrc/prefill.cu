@@ -23,7 +23,8 @@
 // Attention.  One CTA per (query, KV head); warp w handles query heads
 // w, w + 8, ... of the group; a lane holds 8 of the 256 dims.  The query's
 // picks inside the staged chunk are a contiguous run of its ascending index
-// list (two binary searches); rows are taken eight at a time, all sixteen
+// list, starting where the previous chunk's run ended (a cursor kept in the
+// state; one binary search in the first chunk); rows are taken eight at a time, all sixteen
 // 16-byte K/V loads of a lane in flight before the first use.  The chunk's
 // partial (m, l, acc) is merged into the running state in global memory.
 #include "common.cuh"
@@ -158,7 +159,7 @@ __global__ __launch_bounds__(kScoreThreads, 2) void prefill_scores_kernel(const 
 constexpr int kD = 256;
 constexpr int kAttThreads = 256;  // 8 warps
 constexpr int kRowBatch = 8;      // rows whose K/V loads are in flight together
-constexpr int kStatePitch = kD + 4;  // floats per query head: acc, m, l, pad (16-byte rows for float4)
+constexpr int kStatePitch = kD + 4;  // floats per query head: acc, m, l, cursor, pad (16-byte rows)
 
 struct ChunkArgs {
   int nq, Hq, Hkv, G;
@@ -170,12 +171,13 @@ struct ChunkArgs {
   int max_rows;
   const int32_t* count;
   float scale_log2;  // softmax scale * log2(e)
-  float* state;      // [nq][Hq][kStatePitch]: acc[kD], m (log2 units), l, 2 pad
+  float* state;      // [nq][Hq][kStatePitch]: acc[kD], m (log2 units), l, cursor, pad
   int first;         // the first chunk: the state has no contents yet
   int32_t* status;
 };
 
-// First index in idx[0, n) whose value is >= v (idx ascending).
+// First index in idx[0, n) whose value is >= v (idx ascending).  Only the
+// first chunk searches; later chunks start where the previous one stopped.
 __device__ __forceinline__ int lower_bound(const int32_t* idx, int n, int64_t v) {
   int lo = 0, hi = n;
   while (lo < hi) {
@@ -200,19 +202,30 @@ __device__ __forceinline__ void unpack8(const uint4& v, float* f) {
 __global__ __launch_bounds__(kAttThreads) void prefill_chunk_kernel(ChunkArgs a) {
   const int i = blockIdx.x, h = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __shared__ int s_range[2];
+  __shared__ int s_j0;
   const int cnt = min(max(a.count[i], 0), a.max_rows);
   const int32_t* row = a.idx + static_cast<int64_t>(i) * a.max_rows;
+  // The query's picks are ascending, so the chunks take consecutive runs of
+  // them: each (query, KV head) keeps the index where its next chunk starts in
+  // the pad word after l of its group's first head.
+  float* cur = a.state + (static_cast<int64_t>(i) * a.Hq + h * a.G) * kStatePitch + kD + 2;
   if (threadIdx.x == 0) {
-    s_range[0] = lower_bound(row, cnt, a.c0);
-    s_range[1] = lower_bound(row, cnt, a.c1);
-    // picks below 0 precede the first chunk; picks at or past n_tokens follow the last
-    if ((a.c0 == 0 && s_range[0] > 0) || (a.c1 == a.n_tokens && s_range[1] < cnt))
-      set_status(a.status, SKV_DEV_RANGE);
+    int j0;
+    if (a.first) {
+      j0 = lower_bound(row, cnt, a.c0);
+      if (j0 > 0) set_status(a.status, SKV_DEV_RANGE);  // picks below 0 precede the first chunk
+    } else {
+      j0 = __float_as_int(*cur);
+    }
+    s_j0 = j0;
   }
   __syncthreads();
-  const int j0 = s_range[0], j1 = s_range[1];
-  if (j0 == j1 && !a.first) return;  // no pick of this query in the chunk: the state stays
+  const int j0 = s_j0;
+  if (!a.first && (j0 >= cnt || __ldg(row + j0) >= a.c1)) {
+    if (a.c1 == a.n_tokens && j0 < cnt && threadIdx.x == 0) set_status(a.status, SKV_DEV_RANGE);
+    return;  // no pick of this query in the chunk: the state stays
+  }
+  int j1 = j0;  // end of the run inside [c0, c1), found by the row loop
   for (int gi = warp; gi < a.G; gi += kAttThreads / 32) {
     const int g = h * a.G + gi;
     float qv[8], acc[8];
@@ -223,18 +236,24 @@ __global__ __launch_bounds__(kAttThreads) void prefill_chunk_kernel(ChunkArgs a)
 #pragma unroll
     for (int u = 0; u < 8; u++) acc[u] = 0.f;
     float m = -INFINITY, l = 0.f;
-    for (int jb = j0; jb < j1; jb += kRowBatch) {
+    bool more = true;
+    for (int jb = j0; more && jb < cnt; jb += kRowBatch) {
       uint4 kr[kRowBatch], vr[kRowBatch];
       bool ok[kRowBatch];
 #pragma unroll
       for (int r = 0; r < kRowBatch; r++) {
         const int j = jb + r;
-        const int64_t t = j < j1 ? static_cast<int64_t>(__ldg(row + j)) : a.c0;
-        ok[r] = j < j1 && t >= a.c0 && t < a.c1;  // false only for a list that is not ascending
+        const int64_t t = j < cnt ? static_cast<int64_t>(__ldg(row + j)) : a.c1;
+        more = more && t < a.c1;  // ascending: the run stops at the first pick past the chunk
+        ok[r] = more;
+        if (more) j1 = j + 1;
+        if (ok[r] && t < a.c0) {  // a list that is not ascending
+          ok[r] = false;
+          if (lane == 0) set_status(a.status, SKV_DEV_RANGE);
+        }
         const int64_t off = ((ok[r] ? t - a.c0 : 0) * a.Hkv + h) * kD + 8 * lane;
         kr[r] = ok[r] ? ld_nc16(a.k_stage + off) : make_uint4(0u, 0u, 0u, 0u);
         vr[r] = ok[r] ? ld_nc16(a.v_stage + off) : make_uint4(0u, 0u, 0u, 0u);
-        if (j < j1 && !ok[r] && lane == 0) set_status(a.status, SKV_DEV_RANGE);
       }
       float s[kRowBatch];
 #pragma unroll
@@ -295,6 +314,200 @@ __global__ __launch_bounds__(kAttThreads) void prefill_chunk_kernel(ChunkArgs a)
       st[kD] = M;
       st[kD + 1] = L;
     }
+  }
+  __syncthreads();  // every warp has read the cursor (s_j0) and found the same run
+  if (threadIdx.x == 0) {
+    *cur = __int_as_float(j1);
+    if (a.c1 == a.n_tokens && j1 < cnt) set_status(a.status, SKV_DEV_RANGE);  // picks past the history
+  }
+}
+
+// ---- the same on tensor cores (query groups of at most 8 heads) ---------------------
+// One warp per (query, KV head).  A 16-row tile of the query's run:
+//   S = Q . K^T   (m16n8k16, M = the group's heads padded to 16, N = rows,
+//                  K = dims): lane (g, c) holds the 8-byte groups at dims
+//                  64c + 4ks of row g -- one permutation of the 256 dims used
+//                  for Q and K alike, so a lane reads a contiguous 128 B of a
+//                  K row;
+//   O^T += V^T . P^T  (M = dims, N = heads, K = rows): lane g owns dims
+//                  [32g, 32g + 32) of the output; the probabilities come from
+//                  the S accumulators (their layout is the B operand's), split
+//                  into bf16 hi + lo parts so that they keep ~16 bits.
+constexpr int kTcMaxG = 8;
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void bf16x2_to_f32(uint32_t w, float& lo, float& hi) {
+  lo = __uint_as_float(w << 16);
+  hi = __uint_as_float(w & 0xffff0000u);
+}
+
+__global__ __launch_bounds__(32) void prefill_chunk_tc_kernel(ChunkArgs a) {
+  const int i = blockIdx.x, h = blockIdx.y, lane = threadIdx.x;
+  const int g = lane >> 2, c = lane & 3;
+  const int cnt = min(max(a.count[i], 0), a.max_rows);
+  const int32_t* row = a.idx + static_cast<int64_t>(i) * a.max_rows;
+  float* cur = a.state + (static_cast<int64_t>(i) * a.Hq + h * a.G) * kStatePitch + kD + 2;
+  int j0;
+  if (a.first) {
+    j0 = lower_bound(row, cnt, a.c0);
+    if (j0 > 0 && lane == 0) set_status(a.status, SKV_DEV_RANGE);  // picks below 0 precede the first chunk
+  } else {
+    j0 = __float_as_int(*cur);
+    if (j0 >= cnt || __ldg(row + j0) >= a.c1) {
+      if (a.c1 == a.n_tokens && j0 < cnt && lane == 0) set_status(a.status, SKV_DEV_RANGE);
+      return;  // no pick of this query in the chunk: the state stays
+    }
+  }
+  // Q fragments (a0, a2) of head g, k-step ks: dims 64c + 4ks .. +3; padded heads are zero
+  uint32_t qa[16][2];
+  {
+    const bool live = g < a.G;
+    const uint16_t* qg = a.q + (static_cast<int64_t>(i) * a.Hq + h * a.G + (live ? g : 0)) * kD + 64 * c;
+#pragma unroll
+    for (int p = 0; p < 8; p++) {
+      const uint4 v = live ? *reinterpret_cast<const uint4*>(qg + 8 * p) : make_uint4(0u, 0u, 0u, 0u);
+      qa[2 * p][0] = v.x;
+      qa[2 * p][1] = v.y;
+      qa[2 * p + 1][0] = v.z;
+      qa[2 * p + 1][1] = v.w;
+    }
+  }
+  float o[16][4];  // O^T tile mt: (dim 32g + 2mt, heads 2c, 2c+1), (dim 32g + 2mt + 1, ...)
+#pragma unroll
+  for (int mt = 0; mt < 16; mt++) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+  float m = -INFINITY, l = 0.f;  // running max (log2 units) and sum of head g
+  int j1 = j0;
+  bool more = true;
+  for (int jt = j0; more && jt < cnt; jt += 16) {
+    // the tile's token ids: lane r < 16 loads row jt + r; a row counts while the run is ascending in the chunk
+    const int jr = jt + (lane & 15);
+    const int64_t tr = jr < cnt ? static_cast<int64_t>(__ldg(row + jr)) : a.c1;
+    const bool in_chunk = tr < a.c1;
+    const unsigned inb = __ballot_sync(0xffffffffu, in_chunk) & 0xffffu;
+    const int nvalid = __popc(~inb & 0xffffu) ? __ffs(~inb & 0xffffu) - 1 : 16;  // leading rows in the chunk
+    if (nvalid < 16) more = false;
+    j1 = jt + nvalid;
+    const bool low = in_chunk && tr < a.c0 && (lane & 15) < nvalid;  // a list that is not ascending
+    if (__any_sync(0xffffffffu, low) && lane == 0) set_status(a.status, SKV_DEV_RANGE);
+    auto tok = [&](int r) -> int64_t { return __shfl_sync(0xffffffffu, tr, r); };
+    auto valid = [&](int r, int64_t t) { return r < nvalid && t >= a.c0; };
+    // S = Q K^T for rows g (n-tile 0) and 8 + g (n-tile 1)
+    float sacc[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; nt++) {
+      sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+      const int r = 8 * nt + g;
+      const int64_t t = tok(r);
+      const bool ok = valid(r, t);
+      const uint16_t* kp = a.k_stage + ((ok ? t - a.c0 : 0) * a.Hkv + h) * kD + 64 * c;
+      uint4 kv[8];
+#pragma unroll
+      for (int p = 0; p < 8; p++) kv[p] = ok ? ld_nc16(kp + 8 * p) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int p = 0; p < 8; p++) {
+        const uint32_t a0[4] = {qa[2 * p][0], 0u, qa[2 * p][1], 0u};
+        const uint32_t a1[4] = {qa[2 * p + 1][0], 0u, qa[2 * p + 1][1], 0u};
+        mma_bf16_16816(sacc[nt], a0, kv[p].x, kv[p].y);
+        mma_bf16_16816(sacc[nt], a1, kv[p].z, kv[p].w);
+      }
+    }
+    // online softmax of head g over the tile's rows 2c, 2c+1 (n-tile 0) and 8 + 2c, 9 + 2c (n-tile 1)
+    float sv[4];
+#pragma unroll
+    for (int nt = 0; nt < 2; nt++)
+#pragma unroll
+      for (int e = 0; e < 2; e++) {
+        const int r = 8 * nt + 2 * c + e;
+        const int64_t t = tok(r);  // every lane shuffles: the source lane varies with c
+        const bool ok = r < nvalid && t >= a.c0;
+        sv[2 * nt + e] = ok ? sacc[nt][e] * a.scale_log2 : -INFINITY;
+      }
+    float tmax = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
+    tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
+    tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
+    const float mn = fmaxf(m, tmax);
+    const float alpha = mn == -INFINITY ? 1.f : exp2f(m - mn);
+    float pv[4], psum = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; e++) {
+      pv[e] = mn == -INFINITY ? 0.f : exp2f(sv[e] - mn);
+      psum += pv[e];
+    }
+    psum += __shfl_xor_sync(0xffffffffu, psum, 1);
+    psum += __shfl_xor_sync(0xffffffffu, psum, 2);
+    l = l * alpha + psum;
+    m = mn;
+    // rescale O: lane (g, c) holds heads 2c, 2c+1, whose alpha lives in lanes 4(2c), 4(2c+1)
+    const float al0 = __shfl_sync(0xffffffffu, alpha, 8 * c), al1 = __shfl_sync(0xffffffffu, alpha, 8 * c + 4);
+#pragma unroll
+    for (int mt = 0; mt < 16; mt++) {
+      o[mt][0] *= al0;
+      o[mt][1] *= al1;
+      o[mt][2] *= al0;
+      o[mt][3] *= al1;
+    }
+    // P^T as the B operand (rows 2c, 2c+1 | 8 + 2c, 9 + 2c; head g), hi and lo bf16 parts
+    const uint32_t bh0 = pack_bf16x2(pv[0], pv[1]), bh1 = pack_bf16x2(pv[2], pv[3]);
+    float h0, h1, h2, h3;
+    bf16x2_to_f32(bh0, h0, h1);
+    bf16x2_to_f32(bh1, h2, h3);
+    const uint32_t bl0 = pack_bf16x2(pv[0] - h0, pv[1] - h1), bl1 = pack_bf16x2(pv[2] - h2, pv[3] - h3);
+    // V rows 2c, 2c+1, 8 + 2c, 9 + 2c; dims [32g, 32g + 32) in four 16-byte pieces
+    const uint16_t* vp[4];
+    bool vok[4];
+#pragma unroll
+    for (int e = 0; e < 4; e++) {
+      const int r = (e & 1) + 2 * c + 8 * (e >> 1);
+      const int64_t t = tok(r);
+      vok[e] = valid(r, t);
+      vp[e] = a.v_stage + ((vok[e] ? t - a.c0 : 0) * a.Hkv + h) * kD + 32 * g;
+    }
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+      uint4 vv[4];
+#pragma unroll
+      for (int e = 0; e < 4; e++) vv[e] = vok[e] ? ld_nc16(vp[e] + 8 * q) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int w = 0; w < 4; w++) {  // m-tile 4q + w: dims 32g + 8q + 2w (a0, a2) and + 1 (a1, a3)
+        const uint32_t r0 = (&vv[0].x)[w], r1 = (&vv[1].x)[w], r2 = (&vv[2].x)[w], r3 = (&vv[3].x)[w];
+        const uint32_t av[4] = {__byte_perm(r0, r1, 0x5410), __byte_perm(r0, r1, 0x7632),
+                                __byte_perm(r2, r3, 0x5410), __byte_perm(r2, r3, 0x7632)};
+        mma_bf16_16816(o[4 * q + w], av, bh0, bh1);
+        mma_bf16_16816(o[4 * q + w], av, bl0, bl1);
+      }
+    }
+  }
+  // merge into the running state: heads 2c, 2c+1 (when < G), dims [32g, 32g + 32)
+  const float mh0 = __shfl_sync(0xffffffffu, m, 8 * c), mh1 = __shfl_sync(0xffffffffu, m, 8 * c + 4);
+  const float lh0 = __shfl_sync(0xffffffffu, l, 8 * c), lh1 = __shfl_sync(0xffffffffu, l, 8 * c + 4);
+#pragma unroll
+  for (int e = 0; e < 2; e++) {
+    const int hd = 2 * c + e;
+    if (hd >= a.G) continue;
+    float* st = a.state + (static_cast<int64_t>(i) * a.Hq + h * a.G + hd) * kStatePitch;
+    const float mp = e ? mh1 : mh0, lp = e ? lh1 : lh0;
+    const float M = a.first ? -INFINITY : st[kD], L = a.first ? 0.f : st[kD + 1];
+    const float Mn = fmaxf(M, mp);
+    const float wa = Mn == -INFINITY ? 0.f : exp2f(M - Mn), wb = Mn == -INFINITY ? 0.f : exp2f(mp - Mn);
+#pragma unroll
+    for (int mt = 0; mt < 16; mt++) {
+      float2* sp = reinterpret_cast<float2*>(st + 32 * g + 2 * mt);
+      const float2 old = a.first ? make_float2(0.f, 0.f) : *sp;
+      *sp = make_float2(old.x * wa + o[mt][e] * wb, old.y * wa + o[mt][2 + e] * wb);
+    }
+    if (g == 0) {
+      st[kD] = Mn;
+      st[kD + 1] = L * wa + lp * wb;
+    }
+  }
+  __syncwarp();
+  if (lane == 0) {
+    *cur = __int_as_float(j1);
+    if (a.c1 == a.n_tokens && j1 < cnt) set_status(a.status, SKV_DEV_RANGE);  // picks past the history
   }
 }
 
@@ -379,7 +592,10 @@ SKV_EXPORT int skv_prefill_attend(int nq, int Hq, int Hkv, int d, const uint16_t
     a.c0 = c0;
     a.c1 = c1;
     a.first = c0 == 0;
-    prefill_chunk_kernel<<<dim3(static_cast<unsigned>(nq), static_cast<unsigned>(Hkv)), kAttThreads, 0, st>>>(a);
+    if (a.G <= kTcMaxG)
+      prefill_chunk_tc_kernel<<<dim3(static_cast<unsigned>(nq), static_cast<unsigned>(Hkv)), 32, 0, st>>>(a);
+    else
+      prefill_chunk_kernel<<<dim3(static_cast<unsigned>(nq), static_cast<unsigned>(Hkv)), kAttThreads, 0, st>>>(a);
     const int rc = launch_status();
     if (rc != SKV_OK) return rc;
   }

@@ -23,8 +23,11 @@ namespace skv {
 namespace {
 
 constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 2048;
 constexpr int kCTMax = 64;
+constexpr int kUnroll = 8;         // keys per thread whose loads are in flight together
+constexpr int kFlagWords = 1024;   // write pass: bits marking 32-key groups that hold a pick candidate
 
 struct Ws {
   uint32_t* hist;   // [3][B][kBins]
@@ -117,15 +120,24 @@ __global__ __launch_bounds__(kThreads) void topk_hist_kernel(Sel s, Ws w, int pa
   chunk_of(lo, hi, s.CT, c, &c0, &c1);
   const uint32_t* ok = s.okeys + static_cast<int64_t>(b) * s.n_cap;
   const int lane = threadIdx.x & 31;
-  for (int64_t base = c0; base < c1; base += blockDim.x) {
-    const int64_t i = base + threadIdx.x;
-    uint32_t digit = 0xffffffffu;
-    if (i < c1) {
-      const uint32_t key = ok[i];
-      if ((key & mask) == prefix) digit = (key >> shift) & static_cast<uint32_t>(nbins - 1);
+  for (int64_t base = c0; base < c1; base += static_cast<int64_t>(blockDim.x) * kUnroll) {
+    uint32_t key[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; u++) {
+      const int64_t i = base + threadIdx.x + u * blockDim.x;
+      key[u] = i < c1 ? ok[i] : 0u;
     }
-    const unsigned peers = __match_any_sync(0xffffffffu, digit);
-    if (digit != 0xffffffffu && lane == __ffs(peers) - 1) atomicAdd(&h[digit], __popc(peers));
+#pragma unroll
+    for (int u = 0; u < kUnroll; u++) {
+      const int64_t i = base + threadIdx.x + u * blockDim.x;
+      uint32_t digit = 0xffffffffu;
+      if (i < c1 && (key[u] & mask) == prefix) digit = (key[u] >> shift) & static_cast<uint32_t>(nbins - 1);
+      // later passes: most keys left the prefix already, and a warp with none
+      // of them skips the (costly) match
+      if (pass > 0 && !__any_sync(0xffffffffu, digit != 0xffffffffu)) continue;
+      const unsigned peers = __match_any_sync(0xffffffffu, digit);
+      if (digit != 0xffffffffu && lane == __ffs(peers) - 1) atomicAdd(&h[digit], __popc(peers));
+    }
   }
   __syncthreads();
   uint32_t* gh = w.hist + (static_cast<size_t>(pass) * s.B + b) * kBins;
@@ -174,10 +186,19 @@ __global__ __launch_bounds__(kThreads) void topk_count_kernel(Sel s, Ws w) {
   chunk_of(lo, hi, s.CT, c, &c0, &c1);
   const uint32_t* ok = s.okeys + static_cast<int64_t>(b) * s.n_cap;
   int gt = 0, eq = 0;
-  for (int64_t i = c0 + threadIdx.x; i < c1; i += blockDim.x) {
-    const uint32_t key = ok[i];
-    gt += key > kstar;
-    eq += key == kstar;
+  for (int64_t base = c0; base < c1; base += static_cast<int64_t>(blockDim.x) * kUnroll) {
+    uint32_t key[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; u++) {
+      const int64_t i = base + threadIdx.x + u * blockDim.x;
+      key[u] = i < c1 ? ok[i] : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; u++) {
+      const bool valid = base + threadIdx.x + u * blockDim.x < c1;
+      gt += valid && key[u] > kstar;
+      eq += valid && key[u] == kstar;
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -201,10 +222,18 @@ __global__ __launch_bounds__(kThreads) void topk_count_kernel(Sel s, Ws w) {
   }
 }
 
+// Ordered write of this CTA's picks.  Warp v owns the contiguous piece
+// [p0, p1) of the CTA's chunk.  A first pass counts each warp's keys above
+// K* and equal to K* and marks the 32-key groups that hold any of them; the
+// warps' output offsets follow from those counts (ties: lowest index first,
+// up to the quota); a second pass revisits only the marked groups and writes
+// the picks with warp ballots, so no block-wide scan runs per key.
 __global__ __launch_bounds__(kThreads) void topk_write_kernel(Sel s, Ws w) {
-  __shared__ int scan[33];
   __shared__ int base_s[2];
+  __shared__ int wgt[kWarps], weq[kWarps];
+  __shared__ unsigned flags[kFlagWords];
   const int b = blockIdx.y, c = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int64_t T, lo, hi;
   const bool dense = request_range(s, b, &T, &lo, &hi);
   int32_t* out = s.idx + static_cast<int64_t>(b) * s.max_rows;
@@ -233,39 +262,88 @@ __global__ __launch_bounds__(kThreads) void topk_write_kernel(Sel s, Ws w) {
       base_s[1] = e;
     }
   }
-  __syncthreads();
-  const int ties_before = base_s[1] < need ? base_s[1] : need;
-  const int quota = need - ties_before;
-  int out_pos = base_s[0] + ties_before;
-  int eq_seen = 0;
   int64_t c0, c1;
   chunk_of(lo, hi, s.CT, c, &c0, &c1);
   const uint32_t* ok = s.okeys + static_cast<int64_t>(b) * s.n_cap;
+  const int64_t sub = ((c1 - c0 + kWarps - 1) / kWarps + 31) / 32 * 32;  // whole 32-key groups per warp
+  const int64_t p0 = c0 + warp * sub < c1 ? c0 + warp * sub : c1;
+  const int64_t p1 = p0 + sub < c1 ? p0 + sub : c1;
+  const int64_t n_groups = (p1 - p0 + 31) / 32;
+  constexpr int kWordsPerWarp = kFlagWords / kWarps;
+  const bool marked = n_groups <= 32 * kWordsPerWarp;  // larger pieces revisit every group
+  unsigned* myflags = flags + warp * kWordsPerWarp;
+  // pass 1: counts and group marks, kUnroll groups' loads in flight per lane
+  int ngt = 0, neq = 0;
+  for (int64_t g0 = 0; g0 < n_groups; g0 += 32) {
+    unsigned word = 0u;
+    for (int q = 0; q < 32 && g0 + q < n_groups; q += kUnroll) {
+      uint32_t key[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; u++) {
+        const int64_t i = p0 + (g0 + q + u) * 32 + lane;
+        key[u] = i < p1 ? ok[i] : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; u++) {
+        const bool valid = p0 + (g0 + q + u) * 32 + lane < p1;
+        const bool gt = valid && key[u] > kstar, eq = valid && key[u] == kstar;
+        ngt += gt;
+        neq += eq;
+        if (__ballot_sync(0xffffffffu, gt || eq)) word |= 1u << (q + u);
+      }
+    }
+    if (marked && lane == 0) myflags[g0 / 32] = word;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    ngt += __shfl_xor_sync(0xffffffffu, ngt, o);
+    neq += __shfl_xor_sync(0xffffffffu, neq, o);
+  }
+  if (lane == 0) {
+    wgt[warp] = ngt;
+    weq[warp] = neq;
+  }
+  __syncthreads();
+  const int ties_before = base_s[1] < need ? base_s[1] : need;
+  const int quota = need - ties_before;
+  int pos = base_s[0] + ties_before;
+  int eq_run = 0;  // keys equal to K* in this CTA before this warp's piece
+  for (int v = 0; v < warp; v++) {
+    pos += wgt[v] + max(0, min(weq[v], quota - eq_run));
+    eq_run += weq[v];
+  }
+  if (c == s.CT - 1 && threadIdx.x == 0) {  // the request's last chunk: every pick placed
+    int end = base_s[0] + ties_before, er = 0;
+    for (int v = 0; v < kWarps; v++) {
+      end += wgt[v] + max(0, min(weq[v], quota - er));
+      er += weq[v];
+    }
+    if (end != s.k) set_status(s.status, SKV_DEV_COUNT);
+  }
+  // pass 2: the marked groups again, picks written in ascending index order
   const int ratio = s.ratio > 1 ? s.ratio : 1;
   const int head = s.ratio > 1 ? 0 : s.S;
-  for (int64_t base = c0; base < c1; base += blockDim.x) {
-    const int64_t i = base + threadIdx.x;
-    uint32_t key = 0;
-    const bool valid = i < c1;
-    if (valid) key = ok[i];
-    const int gt = valid && key > kstar;
-    const int eq = valid && key == kstar;
-    int eq_tot, sel_tot;
-    const int eq_rank = block_exclusive_scan(eq, scan, &eq_tot) + eq_seen;
-    const int sel = gt || (eq && eq_rank < quota);
-    const int pos = block_exclusive_scan(sel, scan, &sel_tot);
+  const unsigned lt = (1u << lane) - 1u;
+  for (int64_t gi = 0; gi < n_groups; gi++) {
+    if (marked && !((myflags[gi / 32] >> (gi % 32)) & 1u)) continue;
+    const int64_t i = p0 + gi * 32 + lane;
+    const uint32_t key = i < p1 ? ok[i] : 0u;
+    const bool gt = i < p1 && key > kstar;
+    const bool eq = i < p1 && key == kstar;
+    const unsigned eqb = __ballot_sync(0xffffffffu, eq);
+    const bool sel = gt || (eq && eq_run + __popc(eqb & lt) < quota);
+    const unsigned selb = __ballot_sync(0xffffffffu, sel);
     if (sel) {
-      const int j = out_pos + pos;
+      const int j = pos + __popc(selb & lt);
       if (j < s.k) {
         for (int u = 0; u < ratio; u++) out[head + ratio * j + u] = static_cast<int32_t>(ratio * i + u);
       } else {
         set_status(s.status, SKV_DEV_COUNT);
       }
     }
-    out_pos += sel_tot;
-    eq_seen += eq_tot;
+    pos += __popc(selb);
+    eq_run += __popc(eqb);
   }
-  if (c == s.CT - 1 && threadIdx.x == 0 && out_pos != s.k) set_status(s.status, SKV_DEV_COUNT);
   if (c == 0) {
     if (s.ratio <= 1) {
       for (int i = threadIdx.x; i < s.S; i += blockDim.x) out[i] = i;

@@ -246,6 +246,23 @@ def test_topk_bit_exact(skv, orc, case):
         assert np.array_equal(gi[b, :gc[b]], ri[b, :rc[b]])
 
 
+def test_topk_many_requests_bit_exact(skv, orc):
+    """More requests than SMs (one CTA each): ragged lengths, dense and sparse
+    requests side by side, heavy ties, sinks and tail."""
+    rng = np.random.default_rng(901)
+    B, k, S, W = 600, 300, 4, 16
+    L = rng.integers(100, 20000, B).astype(np.int32)
+    L[:5] = [S + W + k, S + W + k + 1, 1, 0, 19999]
+    n_cap = int(L.max())
+    okey = (0x80000000 + rng.integers(0, 40, (B, n_cap))).astype(np.uint32)   # few distinct keys
+    okey[::2] = rng.integers(0, 2 ** 32, (B // 2, n_cap), dtype=np.uint64).astype(np.uint32)
+    gi, gc = run_topk(skv, okey, L, k, S, W)
+    ri, rc = orc.topk_select(okey, L, k, S=S, W=W)
+    assert np.array_equal(gc, rc)
+    for b in range(B):
+        assert np.array_equal(gi[b, :gc[b]], ri[b, :rc[b]]), b
+
+
 @pytest.mark.parametrize("lengths", [[2051], [2052, 2055, 4 * 262_144], [9, 2048 * 4 + 3]])
 def test_topk_pooled_bit_exact(skv, orc, lengths):
     rng = np.random.default_rng(800 + len(lengths))

@@ -145,8 +145,11 @@ def _attend_case(seed, nq, Hq, Hkv, d, n_tok, max_rows):
 
 @pytest.mark.parametrize("chunk", [1000, 4096, 8192, 37])
 @pytest.mark.parametrize("where", ["device", "host"])
-def test_prefill_attend_loop_swapped(skv, orc, chunk, where):
-    nq, Hq, Hkv, d, n_tok, max_rows = 29, 16, 2, 256, 5000, 700
+@pytest.mark.parametrize("Hq,Hkv", [(16, 2), (6, 1), (16, 1)], ids=["G8", "G6", "G16"])
+def test_prefill_attend_loop_swapped(skv, orc, chunk, where, Hq, Hkv):
+    """G <= 8 runs the tensor-core chunk kernel (G = 6 with padded heads),
+    G = 16 the CUDA-core one."""
+    nq, d, n_tok, max_rows = 29, 256, 5000, 700
     K, V, q, idx, cnt = _attend_case(3 + chunk, nq, Hq, Hkv, d, n_tok, max_rows)
     scale = 1 / math.sqrt(d)
     kst = torch.zeros((chunk, Hkv, d), dtype=torch.bfloat16, device="cuda")
