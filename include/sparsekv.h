@@ -593,6 +593,87 @@ int skv_prefill_attend(int nq, int Hq, int Hkv, int d, const uint16_t *q, const 
                        int32_t *dev_status, void *stream);
 
 /* ========================================================================== */
+/* Pressure-driven residency ([P2] "vLLM's Hybrid HiSparse ...", "Three       */
+/* residency states, one block pool": KV stays on the GPU while there is room */
+/* and gives up residency page by page as the pool runs short; completed      */
+/* prefix pages are copied to host memory ahead of need).                     */
+/* ========================================================================== */
+/*
+ * The residency manager is host state (not thread-safe; one per block pool):
+ * the pool's free blocks and, per request slot, one entry per page of `page`
+ * tokens -- a pool block, or -1, a placeholder whose rows live only in host
+ * memory.  That table is the `block_table` of skv_resolve_rows_lru (copy it
+ * to the device with skv_residency_block_table + cudaMemcpyAsync).  Rules:
+ *  - a page may be released only after its host copy was issued: completed
+ *    resident pages are listed by skv_residency_pending, copied with
+ *    skv_materialize_pages and then marked with skv_residency_mark_copied;
+ *  - release picks, among the releasable pages (resident, copied, neither the
+ *    request's newest page nor among its last `tail_pages` pages), the oldest
+ *    page of the request that holds the most resident pages (ties: the lowest
+ *    slot);
+ *  - taking a block when none is free releases one page that way; the call
+ *    fails with SKV_ENOMEM when nothing is releasable;
+ *  - a request added with host_prefix = 1 (a prefix that exists only in host
+ *    memory) starts with placeholders for its complete pages; a partial last
+ *    page gets a block whose first rows must be brought in (listed by
+ *    skv_residency_fills, copied by skv_fill_pages, then marked with
+ *    skv_residency_mark_filled) before anything is appended into that page:
+ *    the fill copies the whole page.
+ * Every call returns SKV_OK or SKV_EINVAL (bad slot, page or size) /
+ * SKV_ENOMEM (out array or pool too small).
+ */
+typedef struct skv_residency skv_residency;
+#define SKV_RESIDENCY_FULL 0   /* every page of the request is resident          */
+#define SKV_RESIDENCY_MIXED 1  /* some pages are placeholders                     */
+#define SKV_RESIDENCY_NONE 2   /* no page is resident                             */
+int skv_residency_create(int n_blocks, int page, int max_requests, int64_t max_pages, int tail_pages,
+                         skv_residency **out);
+void skv_residency_destroy(skv_residency *r);
+/* Starts slot b with n_tokens tokens: every page resident (host_prefix = 0) or
+ * placeholders (host_prefix = 1). */
+int skv_residency_add(skv_residency *r, int b, int64_t n_tokens, int host_prefix);
+/* Ends slot b; its blocks return to the pool. */
+int skv_residency_remove(skv_residency *r, int b);
+/* Appends n tokens to slot b; a token that opens a page takes a block. */
+int skv_residency_append(skv_residency *r, int b, int64_t n);
+/* Complete resident pages of slot b without a host copy (ascending). */
+int skv_residency_pending(const skv_residency *r, int b, int32_t *pages, int max_out, int *n_out);
+int skv_residency_mark_copied(skv_residency *r, int b, const int32_t *pages, int n);
+/* Resident pages of slot b whose first rows must come from host memory. */
+int skv_residency_fills(const skv_residency *r, int b, int32_t *pages, int max_out, int *n_out);
+int skv_residency_mark_filled(skv_residency *r, int b, const int32_t *pages, int n);
+/* Releases up to n_wanted pages under the rule above; released[2i], [2i+1] =
+ * (slot, page); *n_out of them. */
+int skv_residency_reclaim(skv_residency *r, int n_wanted, int32_t *released, int *n_out);
+/* The block table, int32 HOST array [max_requests][max_pages] (-1: placeholder
+ * or unused). */
+int skv_residency_block_table(const skv_residency *r, int32_t *table);
+/* SKV_RESIDENCY_* of slot b, or -1 for a free slot. */
+int skv_residency_state(const skv_residency *r, int b);
+int skv_residency_free_blocks(const skv_residency *r);
+
+/*
+ * skv_materialize_pages / skv_fill_pages -- whole-page copies between the
+ * pool and the host tier, one CTA per listed page: materialize writes the
+ * rows of a resident page to the host (the copy ahead of need), fill brings
+ * a page's host rows into its block.  Page (b, p) = pages[2j], pages[2j+1]:
+ * pool rows block_table[b][p] * page + r, host rows b * t_cap + p * page + r,
+ * r < page.  A page out of range, or not resident, sets SKV_DEV_RANGE and is
+ * skipped.
+ *   pages        int32 [n][2] (device)   block_table int32 [B][n_pages]
+ *   pool         u8 [n_pool_rows][row_bytes]
+ *   host         u8 [B][t_cap][row_bytes] (the host tier's device alias)
+ * Constraints: row_bytes a multiple of 16; pool and host 16-byte aligned.
+ */
+int skv_materialize_pages(int n, const int32_t *pages, int B, int page, const int32_t *block_table,
+                          int64_t n_pages, const uint8_t *pool, int64_t row_bytes,
+                          int64_t n_pool_rows, uint8_t *host, int64_t t_cap, int32_t *dev_status,
+                          void *stream);
+int skv_fill_pages(int n, const int32_t *pages, int B, int page, const int32_t *block_table,
+                   int64_t n_pages, uint8_t *pool, int64_t row_bytes, int64_t n_pool_rows,
+                   const uint8_t *host, int64_t t_cap, int32_t *dev_status, void *stream);
+
+/* ========================================================================== */
 /* Host tier ([P4] "No Need to Rewrite the Kernel": allocate with anonymous    */
 /* mmap, cudaHostRegister(ptr, n, PORTABLE | MAPPED), use the device pointer). */
 /* ========================================================================== */

@@ -78,6 +78,21 @@ def _load():
                 "skv_prefill_index_scores": ([i32, P, P, i64, P, i64, P, P], i32),
                 "skv_prefill_attend": ([i32, i32, i32, i32, P, P, P, i64, P, P, i64, P, i32, P, f32, P, P, P, P],
                                        i32),
+                "skv_residency_create": ([i32, i32, i32, i64, i32, ctypes.POINTER(ctypes.c_void_p)], i32),
+                "skv_residency_destroy": ([P], None),
+                "skv_residency_add": ([P, i32, i64, i32], i32),
+                "skv_residency_remove": ([P, i32], i32),
+                "skv_residency_append": ([P, i32, i64], i32),
+                "skv_residency_pending": ([P, i32, P, i32, ctypes.POINTER(i32)], i32),
+                "skv_residency_mark_copied": ([P, i32, P, i32], i32),
+                "skv_residency_fills": ([P, i32, P, i32, ctypes.POINTER(i32)], i32),
+                "skv_residency_mark_filled": ([P, i32, P, i32], i32),
+                "skv_residency_reclaim": ([P, i32, P, ctypes.POINTER(i32)], i32),
+                "skv_residency_block_table": ([P, P], i32),
+                "skv_residency_state": ([P, i32], i32),
+                "skv_residency_free_blocks": ([P], i32),
+                "skv_materialize_pages": ([i32, P, i32, i32, P, i64, P, i64, i64, P, i64, P, P], i32),
+                "skv_fill_pages": ([i32, P, i32, i32, P, i64, P, i64, i64, P, i64, P, P], i32),
                 "skv_host_register": ([P, sz, ctypes.POINTER(ctypes.c_void_p)], i32),
                 "skv_host_unregister": ([P], i32),
             }
@@ -362,6 +377,107 @@ def prefill_attend(q, k_src, v_src, n_tokens, k_stage, v_stage, idx, count, soft
         int(chunk), _ptr(idx), idx.shape[1], _ptr(count), float(softmax_scale), _ptr(state), _ptr(out),
         _ptr(status), _stream(stream)))
     return out
+
+
+# ---- pressure-driven residency -----------------------------------------------------
+
+RESIDENCY_FULL, RESIDENCY_MIXED, RESIDENCY_NONE = 0, 1, 2
+
+
+class Residency:
+    """Handle on a native residency manager (see skv_residency_*); the methods
+    marshal arguments only.  Page lists are numpy int32 arrays."""
+
+    def __init__(self, n_blocks, page, max_requests, max_pages, tail_pages=1):
+        self.page, self.max_requests, self.max_pages = page, max_requests, max_pages
+        h = ctypes.c_void_p()
+        _check("skv_residency_create", _load().skv_residency_create(n_blocks, page, max_requests, max_pages,
+                                                                   tail_pages, ctypes.byref(h)))
+        self._h = h
+
+    def close(self):
+        if self._h:
+            _load().skv_residency_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def add(self, b, n_tokens, host_prefix=False):
+        _check("skv_residency_add", _load().skv_residency_add(self._h, b, int(n_tokens), int(bool(host_prefix))))
+
+    def remove(self, b):
+        _check("skv_residency_remove", _load().skv_residency_remove(self._h, b))
+
+    def append(self, b, n=1):
+        _check("skv_residency_append", _load().skv_residency_append(self._h, b, int(n)))
+
+    def _list(self, name, b):
+        import numpy as np
+        out = np.zeros((self.max_pages,), np.int32)
+        n = ctypes.c_int(0)
+        _check(name, getattr(_load(), name)(self._h, b, out.ctypes.data_as(ctypes.c_void_p), self.max_pages,
+                                            ctypes.byref(n)))
+        return out[:n.value].copy()
+
+    def pending(self, b):
+        return self._list("skv_residency_pending", b)
+
+    def fills(self, b):
+        return self._list("skv_residency_fills", b)
+
+    def mark_copied(self, b, pages):
+        import numpy as np
+        p = np.ascontiguousarray(pages, np.int32)
+        _check("skv_residency_mark_copied", _load().skv_residency_mark_copied(
+            self._h, b, p.ctypes.data_as(ctypes.c_void_p), p.size))
+
+    def mark_filled(self, b, pages):
+        import numpy as np
+        p = np.ascontiguousarray(pages, np.int32)
+        _check("skv_residency_mark_filled", _load().skv_residency_mark_filled(
+            self._h, b, p.ctypes.data_as(ctypes.c_void_p), p.size))
+
+    def reclaim(self, n):
+        import numpy as np
+        out = np.zeros((max(n, 1), 2), np.int32)
+        k = ctypes.c_int(0)
+        _check("skv_residency_reclaim", _load().skv_residency_reclaim(
+            self._h, int(n), out.ctypes.data_as(ctypes.c_void_p), ctypes.byref(k)))
+        return out[:k.value].copy()
+
+    def block_table(self):
+        import numpy as np
+        out = np.zeros((self.max_requests, self.max_pages), np.int32)
+        _check("skv_residency_block_table", _load().skv_residency_block_table(
+            self._h, out.ctypes.data_as(ctypes.c_void_p)))
+        return out
+
+    def state(self, b):
+        return int(_load().skv_residency_state(self._h, b))
+
+    def free_blocks(self):
+        return int(_load().skv_residency_free_blocks(self._h))
+
+
+def _page_copy(name, pages, page, block_table, pool, host, t_cap, status, stream):
+    n_pool_rows, row_bytes = pool.shape
+    B, n_pages = block_table.shape
+    _check(name, getattr(_load(), name)(
+        pages.shape[0], _ptr(pages), B, page, _ptr(block_table), n_pages, _ptr(pool), row_bytes, n_pool_rows,
+        _addr(host), int(t_cap), _ptr(status), _stream(stream)))
+
+
+def materialize_pages(pages, page, block_table, pool, host, t_cap, status=None, stream=None):
+    """pages int32 [n][2] (slot, page), device; pool u8 [rows][row_bytes]; host: tensor or alias (int)."""
+    _page_copy("skv_materialize_pages", pages, page, block_table, pool, host, t_cap, status, stream)
+
+
+def fill_pages(pages, page, block_table, pool, host, t_cap, status=None, stream=None):
+    _page_copy("skv_fill_pages", pages, page, block_table, pool, host, t_cap, status, stream)
 
 
 # ---- host tier -------------------------------------------------------------------
