@@ -935,6 +935,95 @@ def run_prefill(args):
     w.close()
 
 
+def run_residency(args):
+    """Pressure-driven residency on the latent-row shapes: 32 requests x 142,000
+    tokens of 576 B rows in pages of 64 tokens, a pool holding 40 % of the
+    pages.  Times the whole-page copies (pool -> host ahead of need, host ->
+    pool) against a plain cudaMemcpyAsync of the same bytes, and the manager's
+    host-side work per decode step (append one token to every request, list
+    and copy completed pages, export the block table)."""
+    import ctypes
+
+    import torch
+
+    import sparse_kv_long_gb300 as skv
+    from sparse_kv_long_gb300 import _build
+
+    torch.cuda.set_device(0)
+    _build.build()
+    dev = torch.device("cuda", 0)
+    B, T, page, row_bytes = 32, 142_000, 64, 576
+    n_pages = -(-T // page)
+    n_blocks = int(0.4 * B * n_pages)
+    t_cap = n_pages * page
+    r = skv.Residency(n_blocks, page, B, n_pages, tail_pages=2)
+    full = n_blocks // B
+    for b in range(B):                               # each request resident on its newest pages
+        r.add(b, full * page)
+    pool = torch.randint(0, 256, (n_blocks * page, row_bytes), dtype=torch.uint8, device=dev)
+    host = HostTier(skv, B * t_cap * row_bytes)
+    bt = torch.from_numpy(r.block_table()).to(dev)
+    pairs = np.concatenate([np.stack([np.full(len(p), b, np.int32), p], 1) for b in range(B)
+                            for p in [r.pending(b)]]).astype(np.int32)
+    g_pairs = torch.from_numpy(pairs).to(dev)
+    n_copy = pairs.shape[0]
+    nbytes = n_copy * page * row_bytes
+    st = torch.zeros((1,), dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream()
+
+    def timed(fn, reps):
+        with torch.cuda.stream(stream):
+            fn()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                fn()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    reps = max(3, args.steps // 20)
+    ms_mat = timed(lambda: skv.materialize_pages(g_pairs, page, bt, pool, host.alias, t_cap, status=st,
+                                                 stream=stream), reps)
+    ms_fill = timed(lambda: skv.fill_pages(g_pairs, page, bt, pool, host.alias, t_cap, status=st, stream=stream),
+                    reps)
+    hview = torch.from_numpy(host.arr[:nbytes]).view(n_copy * page, row_bytes)
+    ms_d2h = timed(lambda: hview.copy_(pool[:n_copy * page], non_blocking=True), reps)
+    ms_h2d = timed(lambda: pool[:n_copy * page].copy_(hview, non_blocking=True), reps)
+    for b in range(B):
+        r.mark_copied(b, r.pending(b))
+    # manager work per decode step (one token per request), with the copies it asks for
+    n_steps = args.steps
+    t0 = time.perf_counter()
+    copied = 0
+    table = np.zeros((B, n_pages), np.int32)
+    for s in range(n_steps):
+        for b in range(B):
+            r.append(b, 1)
+        for b in range(B):
+            p = r.pending(b)
+            if p.size:
+                pr = torch.from_numpy(np.stack([np.full(p.size, b, np.int32), p], 1).astype(np.int32)).to(dev)
+                skv.materialize_pages(pr, page, bt, pool, host.alias, t_cap, status=st, stream=stream)
+                r.mark_copied(b, p)
+                copied += p.size
+        table[:] = r.block_table()
+        bt.copy_(torch.from_numpy(table), non_blocking=True)
+    torch.cuda.synchronize()
+    us_step = (time.perf_counter() - t0) * 1e6 / n_steps
+    line = {"workload": "residency", "metric": "page copy GB/s and residency-manager us per decode step",
+            "value": nbytes / (ms_mat * 1e-3) / 1e9, "unit": "GB/s", "n_gpus": 1, "steps": n_steps,
+            "higher_is_better": True, "data": "synthetic",
+            "config": {"workload": f"residency_{B}x{T}_page{page}_576B_pool40pct", "requests": B, "context": T,
+                       "page": page, "row_bytes": row_bytes, "pool_blocks": n_blocks, "pages_copied": n_copy},
+            "materialize_gbs": nbytes / (ms_mat * 1e-3) / 1e9, "fill_gbs": nbytes / (ms_fill * 1e-3) / 1e9,
+            "memcpy_d2h_gbs": nbytes / (ms_d2h * 1e-3) / 1e9, "memcpy_h2d_gbs": nbytes / (ms_h2d * 1e-3) / 1e9,
+            "bytes_per_copy": nbytes, "manager_us_per_step": us_step, "pages_copied_in_steps": copied,
+            "free_blocks_after": r.free_blocks(), "device_status": int(st.item())}
+    print(json.dumps(line), flush=True)
+    host.close()
+
+
 def run_extra(args):
     import torch
 
@@ -1091,7 +1180,7 @@ def main():
     ap.add_argument("--layers", type=int, default=None, help="distinct layers (16 for the sketch workload; "
                     "fewer only for profiler captures)")
     ap.add_argument("--workload", default="sketch",
-                    choices=["sketch", "host_clock", "mla_lru", "pooled", "pooled_host", "prefill"],
+                    choices=["sketch", "host_clock", "mla_lru", "pooled", "pooled_host", "prefill", "residency"],
                     help="sketch: the headline line; the others print their own line")
     ap.add_argument("--eta", type=float, default=0.35, help="query drift per step (host_clock)")
     ap.add_argument("--context", type=int, default=None, help="mla_lru, pooled: tokens per request (default "
@@ -1102,13 +1191,15 @@ def main():
         args.warmup = 3
     if args.layers is None:
         args.layers = {"sketch": W_L, "host_clock": 4, "mla_lru": 2, "pooled": 12, "pooled_host": 2,
-                       "prefill": 1}[args.workload]
+                       "prefill": 1, "residency": 1}[args.workload]
     if args.impl == "reference":
         run_reference(args)
     elif args.workload == "sketch":
         run_gpu(args)
     elif args.workload == "prefill":
         run_prefill(args)
+    elif args.workload == "residency":
+        run_residency(args)
     else:
         run_extra(args)
 

@@ -81,6 +81,9 @@ struct skv_residency {
     std::vector<int32_t> block;      // per page: pool block, or -1 (placeholder: host only)
     std::vector<uint8_t> host_copy;  // per page: its host rows are written (the copy was issued)
     std::vector<uint8_t> need_fill;  // per page: resident, earlier rows still only in host memory
+    int64_t resident = 0;            // resident pages
+    int64_t first_pending = 0;       // pages below: copied, placeholders or awaiting a fill
+    int64_t first_release = 0;       // pages below: placeholders
   };
   int n_blocks = 0, page = 0, tail_pages = 0;
   int64_t max_pages = 0;
@@ -93,23 +96,28 @@ struct skv_residency {
   // issued, neither the newest page nor among the last tail_pages pages), the
   // oldest page of the request holding the most resident pages (ties: the
   // lowest request number).
+  // Oldest releasable page of a request, or -1.  Placeholders at the front
+  // are skipped for good (a released page never comes back), so with pages
+  // copied in order the search stops at its first step.
+  int64_t oldest_releasable(Req& r) const {
+    const int64_t keep = tail_pages > 1 ? tail_pages : 1;
+    const int64_t used = pages_of(r.n_tokens);
+    while (r.first_release < used && r.block[r.first_release] < 0) r.first_release++;
+    for (int64_t p = r.first_release; p < used - keep; p++)
+      if (r.block[p] >= 0 && r.host_copy[p] && !r.need_fill[p]) return p;
+    return -1;
+  }
+
   bool release_one(int32_t* out_b, int32_t* out_p) {
     int best = -1;
     int64_t best_res = 0, best_page = -1;
-    const int64_t keep = tail_pages > 1 ? tail_pages : 1;
     for (size_t b = 0; b < req.size(); b++) {
-      const Req& r = req[b];
-      if (!r.live) continue;
-      const int64_t used = pages_of(r.n_tokens);
-      int64_t res = 0, first = -1;
-      for (int64_t p = 0; p < used; p++) {
-        if (r.block[p] < 0) continue;
-        res++;
-        if (first < 0 && p < used - keep && r.host_copy[p] && !r.need_fill[p]) first = p;
-      }
-      if (first >= 0 && res > best_res) {
+      Req& r = req[b];
+      if (!r.live || r.resident <= best_res) continue;
+      const int64_t first = oldest_releasable(r);
+      if (first >= 0) {
         best = static_cast<int>(b);
-        best_res = res;
+        best_res = r.resident;
         best_page = first;
       }
     }
@@ -117,6 +125,7 @@ struct skv_residency {
     Req& r = req[best];
     free_list.push_back(r.block[best_page]);
     r.block[best_page] = -1;
+    r.resident--;
     if (out_b) *out_b = best;
     if (out_p) *out_p = static_cast<int32_t>(best_page);
     return true;
@@ -179,6 +188,7 @@ SKV_EXPORT int skv_residency_add(skv_residency* r, int b, int64_t n_tokens, int 
     }
     taken.push_back(blk);
     q.block[p] = blk;
+    q.resident++;
     if (host_prefix) q.need_fill[p] = 1;  // the partial tail page: its first rows come from host memory
   }
   r->req[b] = q;
@@ -207,6 +217,7 @@ SKV_EXPORT int skv_residency_append(skv_residency* r, int b, int64_t n) {
       return SKV_ENOMEM;
     }
     q.block[p] = blk;
+    q.resident++;
     q.host_copy[p] = 0;
     q.need_fill[p] = t % r->page != 0;  // earlier rows of the page are in host memory only
     q.n_tokens = t + 1;
@@ -217,10 +228,13 @@ SKV_EXPORT int skv_residency_append(skv_residency* r, int b, int64_t n) {
 
 SKV_EXPORT int skv_residency_pending(const skv_residency* r, int b, int32_t* pages, int max_out, int* n_out) {
   if (!r || !n_out || !r->valid(b) || max_out < 0) return SKV_EINVAL;
-  const skv_residency::Req& q = r->req[b];
+  skv_residency::Req& q = const_cast<skv_residency*>(r)->req[b];  // the scan start is a cache
   const int64_t complete = q.n_tokens / r->page;
+  while (q.first_pending < complete &&
+         (q.block[q.first_pending] < 0 || q.host_copy[q.first_pending]) && !q.need_fill[q.first_pending])
+    q.first_pending++;
   int n = 0;
-  for (int64_t p = 0; p < complete; p++)
+  for (int64_t p = q.first_pending; p < complete; p++)
     if (q.block[p] >= 0 && !q.host_copy[p] && !q.need_fill[p]) {
       if (n >= max_out) return SKV_ENOMEM;
       if (pages) pages[n] = static_cast<int32_t>(p);
