@@ -35,10 +35,12 @@ struct Ws {
   uint32_t* state;  // [B][4]: prefix, mask, need, pad
   int32_t* cgt;     // [B][kCTMax]
   int32_t* ceq;     // [B][kCTMax]
+  int32_t* todo;    // [B]: the request still needs the radix passes (many-request path)
 };
 
 __host__ __device__ inline size_t ws_bytes(int B) {
-  return sizeof(uint32_t) * (3ull * B * kBins + 3ull * B + 4ull * B) + sizeof(int32_t) * 2ull * B * kCTMax;
+  return sizeof(uint32_t) * (3ull * B * kBins + 3ull * B + 4ull * B) + sizeof(int32_t) * 2ull * B * kCTMax +
+         sizeof(int32_t) * static_cast<size_t>(B);
 }
 
 inline Ws ws_carve(void* base, int B) {
@@ -52,6 +54,7 @@ inline Ws ws_carve(void* base, int B) {
   p += 4ull * B;
   w.cgt = reinterpret_cast<int32_t*>(p);
   w.ceq = w.cgt + static_cast<size_t>(B) * kCTMax;
+  w.todo = w.ceq + static_cast<size_t>(B) * kCTMax;
   return w;
 }
 
@@ -64,6 +67,7 @@ struct Sel {
   int max_rows;
   int32_t* count;
   int32_t* status;
+  const int32_t* todo;  // NULL: every request; else only those with todo[b] != 0
 };
 
 // Candidate range [lo, hi) of request b and whether it takes the dense path.
@@ -104,6 +108,7 @@ __global__ __launch_bounds__(kThreads) void topk_hist_kernel(Sel s, Ws w, int pa
   __shared__ int scan[33];
   __shared__ int last;
   const int b = blockIdx.y, c = blockIdx.x;
+  if (s.todo && !s.todo[b]) return;
   int64_t T, lo, hi;
   if (request_range(s, b, &T, &lo, &hi)) return;  // dense: nothing to select
   int shift, nbins;
@@ -179,6 +184,7 @@ __global__ __launch_bounds__(kThreads) void topk_hist_kernel(Sel s, Ws w, int pa
 __global__ __launch_bounds__(kThreads) void topk_count_kernel(Sel s, Ws w) {
   __shared__ int red[2][32];
   const int b = blockIdx.y, c = blockIdx.x;
+  if (s.todo && !s.todo[b]) return;
   int64_t T, lo, hi;
   if (request_range(s, b, &T, &lo, &hi)) return;
   const uint32_t kstar = w.state[4 * b];
@@ -234,6 +240,7 @@ __global__ __launch_bounds__(kThreads) void topk_write_kernel(Sel s, Ws w) {
   __shared__ unsigned flags[kFlagWords];
   const int b = blockIdx.y, c = blockIdx.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (s.todo && !s.todo[b]) return;
   int64_t T, lo, hi;
   const bool dense = request_range(s, b, &T, &lo, &hi);
   int32_t* out = s.idx + static_cast<int64_t>(b) * s.max_rows;
@@ -360,6 +367,142 @@ __global__ __launch_bounds__(kThreads) void topk_write_kernel(Sel s, Ws w) {
   }
 }
 
+// ---- many requests: one CTA each, threshold filter -----------------------------------
+// With at least two requests per SM every request has a single CTA, and the
+// radix passes would stream its keys five times.  Instead the CTA takes an
+// evenly spaced sample of the keys, sorts it, and picks a threshold tau below
+// the sample's ~2k/n quantile; every key >= tau (with its index) goes to
+// shared memory -- at least k of them hold the k best, ties at K* included,
+// since all keys equal to K* >= tau are kept -- and a bitonic sort by (key
+// descending, index ascending) of those candidates gives the selection, which
+// a second sort puts in index order.  A request whose candidates overflow the
+// buffer, or number fewer than k, is marked for the radix passes.
+constexpr int kCand = 8192;       // candidates held in shared memory (64-bit: key, inverted index)
+constexpr int kSamp = 4096;       // sampled keys
+constexpr int kMaxFilterK = 2048;
+
+__device__ void bitonic_desc_u64(unsigned long long* a, int n) {
+  for (int size = 2; size <= n; size <<= 1)
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int t = threadIdx.x; t < n / 2; t += blockDim.x) {
+        const int i = 2 * t - (t & (stride - 1)), j = i + stride;
+        const bool up = (i & size) == 0;  // this run ends descending
+        const unsigned long long x = a[i], y = a[j];
+        if ((x < y) == up) {
+          a[i] = y;
+          a[j] = x;
+        }
+      }
+      __syncthreads();
+    }
+}
+
+template <typename V>
+__device__ void bitonic_asc(V* a, int n) {
+  for (int size = 2; size <= n; size <<= 1)
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int t = threadIdx.x; t < n / 2; t += blockDim.x) {
+        const int i = 2 * t - (t & (stride - 1)), j = i + stride;
+        const bool up = (i & size) == 0;
+        const V x = a[i], y = a[j];
+        if ((x > y) == up) {
+          a[i] = y;
+          a[j] = x;
+        }
+      }
+      __syncthreads();
+    }
+}
+
+__global__ __launch_bounds__(kThreads) void topk_filter_kernel(Sel s, Ws w) {
+  extern __shared__ __align__(16) unsigned long long cand[];  // [kCand]; the sample aliases its front
+  __shared__ int32_t picks[kMaxFilterK];
+  __shared__ unsigned s_cnt;
+  const int b = blockIdx.x, lane = threadIdx.x & 31;
+  int64_t T, lo, hi;
+  const bool dense = request_range(s, b, &T, &lo, &hi);
+  int32_t* out = s.idx + static_cast<int64_t>(b) * s.max_rows;
+  if (dense) {
+    for (int64_t i = threadIdx.x; i < T; i += blockDim.x) out[i] = static_cast<int32_t>(i);
+    if (threadIdx.x == 0) {
+      s.count[b] = static_cast<int32_t>(T);
+      w.todo[b] = 0;
+    }
+    return;
+  }
+  const int64_t n = hi - lo;
+  const uint32_t* ok = s.okeys + static_cast<int64_t>(b) * s.n_cap + lo;
+  uint32_t tau = 0u;
+  if (n > kCand) {
+    uint32_t* samp = reinterpret_cast<uint32_t*>(cand);
+    for (int j = threadIdx.x; j < kSamp; j += blockDim.x) samp[j] = ok[static_cast<int64_t>(j) * n / kSamp];
+    __syncthreads();
+    bitonic_asc(samp, kSamp);
+    const int64_t r = (2ll * s.k * kSamp + n - 1) / n + 16;  // from the top
+    tau = samp[kSamp - 1 - (r < kSamp ? r : kSamp - 1)];
+    __syncthreads();  // the candidates overwrite the sample
+  }
+  if (threadIdx.x == 0) s_cnt = 0u;
+  __syncthreads();
+  const unsigned lt = (1u << lane) - 1u;
+  for (int64_t base = 0; base < n; base += static_cast<int64_t>(blockDim.x) * kUnroll) {
+    uint32_t key[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; u++) {
+      const int64_t i = base + threadIdx.x + u * blockDim.x;
+      key[u] = i < n ? ok[i] : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; u++) {
+      const int64_t i = base + threadIdx.x + u * blockDim.x;
+      const bool keep = i < n && key[u] >= tau;
+      const unsigned m = __ballot_sync(0xffffffffu, keep);
+      unsigned at = 0u;
+      if (lane == 0 && m) at = atomicAdd(&s_cnt, static_cast<unsigned>(__popc(m)));
+      at = __shfl_sync(0xffffffffu, at, 0);
+      if (keep) {
+        const unsigned slot = at + __popc(m & lt);
+        if (slot < kCand)
+          cand[slot] = (static_cast<unsigned long long>(key[u]) << 32) | (0xffffffffu - static_cast<uint32_t>(i));
+      }
+    }
+  }
+  __syncthreads();
+  const unsigned total = s_cnt;
+  if (total < static_cast<unsigned>(s.k) || total > static_cast<unsigned>(kCand)) {  // the same in every thread
+    if (threadIdx.x == 0) w.todo[b] = 1;
+    return;
+  }
+  int N = 1;
+  while (N < static_cast<int>(total)) N <<= 1;
+  for (int j = static_cast<int>(total) + threadIdx.x; j < N; j += blockDim.x) cand[j] = 0ull;  // sorts last
+  __syncthreads();
+  bitonic_desc_u64(cand, N);
+  int K = 1;
+  while (K < s.k) K <<= 1;
+  for (int j = threadIdx.x; j < K; j += blockDim.x)
+    picks[j] = j < s.k ? static_cast<int32_t>(0xffffffffu - static_cast<uint32_t>(cand[j])) : INT32_MAX;
+  __syncthreads();
+  bitonic_asc(picks, K);
+  const int ratio = s.ratio > 1 ? s.ratio : 1;
+  const int head = s.ratio > 1 ? 0 : s.S;
+  for (int j = threadIdx.x; j < s.k; j += blockDim.x) {
+    const int64_t i = lo + picks[j];
+    for (int u = 0; u < ratio; u++) out[head + ratio * j + u] = static_cast<int32_t>(ratio * i + u);
+  }
+  if (s.ratio <= 1) {
+    for (int i = threadIdx.x; i < s.S; i += blockDim.x) out[i] = i;
+    for (int i = threadIdx.x; i < s.W; i += blockDim.x) out[s.S + s.k + i] = static_cast<int32_t>(T - s.W + i);
+    if (threadIdx.x == 0) s.count[b] = s.S + s.k + s.W;
+  } else {
+    const int64_t nb = T / s.ratio;
+    const int rem = static_cast<int>(T - nb * s.ratio);
+    for (int i = threadIdx.x; i < rem; i += blockDim.x) out[s.ratio * s.k + i] = static_cast<int32_t>(nb * s.ratio + i);
+    if (threadIdx.x == 0) s.count[b] = s.ratio * s.k + rem;
+  }
+  if (threadIdx.x == 0) w.todo[b] = 0;
+}
+
 }  // namespace
 }  // namespace skv
 
@@ -382,10 +525,24 @@ SKV_EXPORT int skv_topk_select(int B, const uint32_t* order_keys, int64_t n_cap,
   if (reinterpret_cast<uintptr_t>(workspace) & 15) return SKV_EINVAL;
   int CT = (2 * sm_count() + B - 1) / B;
   CT = CT < 1 ? 1 : (CT > kCTMax ? kCTMax : CT);
-  Sel s{order_keys, n_cap, lengths, k, S, W, ratio, CT, B, idx, max_rows, count, dev_status};
+  Sel s{order_keys, n_cap, lengths, k, S, W, ratio, CT, B, idx, max_rows, count, dev_status, nullptr};
   Ws w = ws_carve(workspace, B);
   cudaStream_t st = as_stream(stream);
   dim3 grid(CT, B);
+  if (CT == 1 && k <= kMaxFilterK) {  // one CTA per request: threshold filter, radix passes for the rest
+    constexpr size_t smem = kCand * sizeof(unsigned long long);
+    static bool configured = false;
+    if (!configured) {
+      if (cudaFuncSetAttribute(topk_filter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(smem)) != cudaSuccess) {
+        cudaGetLastError();
+        return SKV_ECUDA;
+      }
+      configured = true;
+    }
+    topk_filter_kernel<<<B, kThreads, smem, st>>>(s, w);
+    s.todo = w.todo;
+  }
   for (int pass = 0; pass < 3; pass++) topk_hist_kernel<<<grid, kThreads, 0, st>>>(s, w, pass);
   topk_count_kernel<<<grid, kThreads, 0, st>>>(s, w);
   topk_write_kernel<<<grid, kThreads, 0, st>>>(s, w);
@@ -410,7 +567,7 @@ namespace {
 constexpr int kNoAllocMaxB = 32;
 constexpr size_t kNoAllocBytes = sizeof(uint32_t) * (3ull * kNoAllocMaxB * kBins + 3ull * kNoAllocMaxB +
                                                      4ull * kNoAllocMaxB) +
-                                 sizeof(int32_t) * 2ull * kNoAllocMaxB * kCTMax;
+                                 sizeof(int32_t) * 2ull * kNoAllocMaxB * kCTMax + sizeof(int32_t) * kNoAllocMaxB;
 
 static __device__ __align__(256) unsigned char g_topk_scratch[kNoAllocBytes];
 
@@ -470,7 +627,7 @@ SKV_EXPORT int skv_topk_select_noalloc(int B, const uint32_t* order_keys, int64_
   }
   int CT = (2 * sm_count() + B - 1) / B;
   CT = CT < 1 ? 1 : (CT > kCTMax ? kCTMax : CT);
-  Sel s{order_keys, n_cap, lengths, k, S, W, ratio, CT, B, idx, max_rows, count, dev_status};
+  Sel s{order_keys, n_cap, lengths, k, S, W, ratio, CT, B, idx, max_rows, count, dev_status, nullptr};
   Ws w = ws_carve(scratch, B);
   dim3 grid(CT, B);
   for (int pass = 0; pass < 3; pass++) topk_hist_kernel<<<grid, kThreads, 0, st>>>(s, w, pass);

@@ -263,6 +263,30 @@ def test_topk_many_requests_bit_exact(skv, orc):
         assert np.array_equal(gi[b, :gc[b]], ri[b, :rc[b]]), b
 
 
+def test_topk_many_requests_filter_and_fallbacks(skv, orc):
+    """One CTA per request (more requests than twice the SMs): the threshold
+    filter for ordinary keys, and the radix passes for the two ways the
+    filter gives up -- too many candidates (every key equal) and too few
+    (the sampled positions hold the largest keys, so the threshold lands
+    above the k-th key)."""
+    rng = np.random.default_rng(905)
+    B, k, n = 400, 2000, 10_000
+    L = np.full(B, n, np.int32)
+    okey = rng.integers(0, 2 ** 32, (B, n), dtype=np.uint64).astype(np.uint32)
+    okey[1::3] = 0x80000000                                        # all equal
+    samp = (np.arange(4096, dtype=np.int64) * n) // 4096           # the filter's sample positions
+    low = rng.integers(0, 2 ** 20, (B, n), dtype=np.uint64).astype(np.uint32)
+    high = (0xF0000000 + rng.integers(0, 2 ** 20, (B, 4096), dtype=np.uint64)).astype(np.uint32)
+    for b in range(2, B, 3):
+        okey[b] = low[b]
+        okey[b, samp] = high[b]
+    gi, gc = run_topk(skv, okey, L, k)
+    ri, rc = orc.topk_select(okey, L, k)
+    assert np.array_equal(gc, rc)
+    for b in range(B):
+        assert np.array_equal(gi[b, :gc[b]], ri[b, :rc[b]]), b
+
+
 @pytest.mark.parametrize("lengths", [[2051], [2052, 2055, 4 * 262_144], [9, 2048 * 4 + 3]])
 def test_topk_pooled_bit_exact(skv, orc, lengths):
     rng = np.random.default_rng(800 + len(lengths))
@@ -274,6 +298,22 @@ def test_topk_pooled_bit_exact(skv, orc, lengths):
     assert np.array_equal(gc, rc)
     for b in range(len(L)):
         assert np.array_equal(gi[b, :gc[b]], ri[b, :rc[b]])
+
+
+def test_topk_pooled_many_requests_bit_exact(skv, orc):
+    """Block selection with expansion, one CTA per request, ragged lengths
+    (dense fallback, incomplete last blocks)."""
+    rng = np.random.default_rng(906)
+    B = 350
+    L = rng.integers(1000, 60_000, B).astype(np.int32)
+    L[:3] = [4 * 512 + 3, 4 * 512 + 4, 4 * 512 + 7]
+    n_cap = int(L.max()) // 4 + 1
+    okey = rng.integers(0x7fff0000, 0x80010000, (B, n_cap), dtype=np.uint64).astype(np.uint32)
+    gi, gc = run_topk(skv, okey, L, 512, ratio=4)
+    ri, rc = orc.topk_select(okey, L, 512, ratio=4)
+    assert np.array_equal(gc, rc)
+    for b in range(B):
+        assert np.array_equal(gi[b, :gc[b]], ri[b, :rc[b]]), b
 
 
 # ---------------------------------------------------------------------------
