@@ -174,7 +174,49 @@ struct ChunkArgs {
   float* state;      // [nq][Hq][kStatePitch]: acc[kD], m (log2 units), l, cursor, pad
   int first;         // the first chunk: the state has no contents yet
   int32_t* status;
+  // Staging of the next chunk by the first CTAs of the same launch (blockIdx.x
+  // < ncx; they start first): next_rows rows of K and V from device-readable
+  // sources into the other half of the buffers.
+  const uint16_t* k_next_src;
+  const uint16_t* v_next_src;
+  uint16_t* k_next;
+  uint16_t* v_next;
+  int64_t next_rows;
+  int ncx;     // copy columns of the grid (0: no staging in this launch)
+  int n_copy;  // copy CTAs = ncx * gridDim.y
 };
+
+// Copy CTA `cid` of n_copy: its share of the next chunk's K and V bytes, 16-byte
+// pieces, several loads in flight per thread.
+__device__ __forceinline__ void stage_next(const ChunkArgs& a, int cid) {
+  const int64_t n16 = a.next_rows * a.Hkv * kD / 8;  // pieces per tensor
+  const int64_t per = (n16 + a.n_copy - 1) / a.n_copy;
+  const int64_t p0 = cid * per, p1 = p0 + per < n16 ? p0 + per : n16;
+  const uint4* ks = reinterpret_cast<const uint4*>(a.k_next_src);
+  const uint4* vs = reinterpret_cast<const uint4*>(a.v_next_src);
+  uint4* kd = reinterpret_cast<uint4*>(a.k_next);
+  uint4* vd = reinterpret_cast<uint4*>(a.v_next);
+  constexpr int kU = 4;
+  for (int64_t i0 = p0 + threadIdx.x; i0 < p1; i0 += static_cast<int64_t>(blockDim.x) * kU) {
+    uint4 kv[kU], vv[kU];
+#pragma unroll
+    for (int u = 0; u < kU; u++) {
+      const int64_t i = i0 + u * blockDim.x;
+      if (i < p1) {
+        kv[u] = ld_nc16(ks + i);
+        vv[u] = ld_nc16(vs + i);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kU; u++) {
+      const int64_t i = i0 + u * blockDim.x;
+      if (i < p1) {
+        kd[i] = kv[u];
+        vd[i] = vv[u];
+      }
+    }
+  }
+}
 
 // First index in idx[0, n) whose value is >= v (idx ascending).  Only the
 // first chunk searches; later chunks start where the previous one stopped.
@@ -200,7 +242,11 @@ __device__ __forceinline__ void unpack8(const uint4& v, float* f) {
 }
 
 __global__ __launch_bounds__(kAttThreads) void prefill_chunk_kernel(ChunkArgs a) {
-  const int i = blockIdx.x, h = blockIdx.y;
+  if (static_cast<int>(blockIdx.x) < a.ncx) {
+    stage_next(a, blockIdx.x * gridDim.y + blockIdx.y);
+    return;
+  }
+  const int i = blockIdx.x - a.ncx, h = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   __shared__ int s_j0;
   const int cnt = min(max(a.count[i], 0), a.max_rows);
@@ -346,7 +392,11 @@ __device__ __forceinline__ void bf16x2_to_f32(uint32_t w, float& lo, float& hi) 
 }
 
 __global__ __launch_bounds__(32) void prefill_chunk_tc_kernel(ChunkArgs a) {
-  const int i = blockIdx.x, h = blockIdx.y, lane = threadIdx.x;
+  if (static_cast<int>(blockIdx.x) < a.ncx) {
+    stage_next(a, blockIdx.x * gridDim.y + blockIdx.y);
+    return;
+  }
+  const int i = blockIdx.x - a.ncx, h = blockIdx.y, lane = threadIdx.x;
   const int g = lane >> 2, c = lane & 3;
   const int cnt = min(max(a.count[i], 0), a.max_rows);
   const int32_t* row = a.idx + static_cast<int64_t>(i) * a.max_rows;
@@ -527,6 +577,22 @@ __global__ __launch_bounds__(kAttThreads) void prefill_finish_kernel(const float
   *reinterpret_cast<float4*>(o + 4) = make_float4(x1.x * inv, x1.y * inv, x1.z * inv, x1.w * inv);
 }
 
+// A device-readable view of a source pointer: device or managed memory as
+// is, a registered host buffer through its device alias; false for anything
+// else (pageable host memory is copied with cudaMemcpyAsync only).
+bool device_view(const void* p, const uint16_t** out) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if ((at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged && at.type != cudaMemoryTypeHost) ||
+      !at.devicePointer)
+    return false;
+  *out = static_cast<const uint16_t*>(at.devicePointer);
+  return true;
+}
+
 }  // namespace
 }  // namespace skv
 
@@ -575,29 +641,55 @@ SKV_EXPORT int skv_prefill_attend(int nq, int Hq, int Hkv, int d, const uint16_t
     return SKV_EINVAL;
   cudaStream_t st = as_stream(stream);
   const size_t row_bytes = static_cast<size_t>(Hkv) * kD * sizeof(uint16_t);
+  const int64_t row_elems = static_cast<int64_t>(Hkv) * kD;
+  // With device-readable sources (device memory, or a registered host buffer
+  // through its alias) the launch that attends chunk j also stages chunk j + 1
+  // into the other half of the buffers, so the copies overlap the attention.
+  const uint16_t* kd = nullptr;
+  const uint16_t* vd = nullptr;
+  const bool overlap = chunk_tokens >= 2 && n_tokens > chunk_tokens / 2 && device_view(k_src, &kd) &&
+                       device_view(v_src, &vd) && aligned16(kd) && aligned16(vd);
+  const int64_t chunk = overlap ? chunk_tokens / 2 : chunk_tokens;
+  const bool tc = Hq / Hkv <= kTcMaxG;
+  const int ncx = overlap ? ((tc ? 4 : 1) * (sm_count() > 0 ? sm_count() : 1) + Hkv - 1) / Hkv : 0;
   ChunkArgs a{nq, Hq, Hkv, Hq / Hkv, q, k_stage, v_stage, 0, 0, n_tokens, idx, max_rows, count,
-              softmax_scale * kLog2e, state, 1, dev_status};
+              softmax_scale * kLog2e, state, 1, dev_status, nullptr, nullptr, nullptr, nullptr, 0, 0, 0};
   // Chunk 0 also initialises the state, so one chunk pass runs even when
   // n_tokens == 0 (every query then attends to nothing).
-  for (int64_t c0 = 0; c0 == 0 || c0 < n_tokens; c0 += chunk_tokens) {
-    const int64_t c1 = c0 + chunk_tokens < n_tokens ? c0 + chunk_tokens : n_tokens;
-    if (c1 > c0) {
+  int buf = 0;
+  for (int64_t c0 = 0; c0 == 0 || c0 < n_tokens; c0 += chunk) {
+    const int64_t c1 = c0 + chunk < n_tokens ? c0 + chunk : n_tokens;
+    uint16_t* kb = k_stage + buf * chunk * row_elems;
+    uint16_t* vb = v_stage + buf * chunk * row_elems;
+    if (c1 > c0 && (!overlap || c0 == 0)) {  // staged by the previous launch otherwise
       const size_t bytes = static_cast<size_t>(c1 - c0) * row_bytes;
-      if (cudaMemcpyAsync(k_stage, k_src + c0 * Hkv * kD, bytes, cudaMemcpyDefault, st) != cudaSuccess ||
-          cudaMemcpyAsync(v_stage, v_src + c0 * Hkv * kD, bytes, cudaMemcpyDefault, st) != cudaSuccess) {
+      if (cudaMemcpyAsync(kb, k_src + c0 * row_elems, bytes, cudaMemcpyDefault, st) != cudaSuccess ||
+          cudaMemcpyAsync(vb, v_src + c0 * row_elems, bytes, cudaMemcpyDefault, st) != cudaSuccess) {
         cudaGetLastError();
         return SKV_ECUDA;
       }
     }
+    a.k_stage = kb;
+    a.v_stage = vb;
     a.c0 = c0;
     a.c1 = c1;
     a.first = c0 == 0;
-    if (a.G <= kTcMaxG)
-      prefill_chunk_tc_kernel<<<dim3(static_cast<unsigned>(nq), static_cast<unsigned>(Hkv)), 32, 0, st>>>(a);
+    const int64_t n1 = c1 + chunk < n_tokens ? c1 + chunk : n_tokens;
+    a.ncx = overlap && n1 > c1 ? ncx : 0;
+    a.n_copy = a.ncx * Hkv;
+    a.next_rows = n1 - c1;
+    a.k_next_src = kd ? kd + c1 * row_elems : nullptr;
+    a.v_next_src = vd ? vd + c1 * row_elems : nullptr;
+    a.k_next = k_stage + (buf ^ 1) * chunk * row_elems;
+    a.v_next = v_stage + (buf ^ 1) * chunk * row_elems;
+    const dim3 grid(static_cast<unsigned>(nq + a.ncx), static_cast<unsigned>(Hkv));
+    if (tc)
+      prefill_chunk_tc_kernel<<<grid, 32, 0, st>>>(a);
     else
-      prefill_chunk_kernel<<<dim3(static_cast<unsigned>(nq), static_cast<unsigned>(Hkv)), kAttThreads, 0, st>>>(a);
+      prefill_chunk_kernel<<<grid, kAttThreads, 0, st>>>(a);
     const int rc = launch_status();
     if (rc != SKV_OK) return rc;
+    if (overlap) buf ^= 1;
   }
   const int64_t n_heads = static_cast<int64_t>(nq) * Hq;
   prefill_finish_kernel<<<static_cast<unsigned>((n_heads + 7) / 8), kAttThreads, 0, st>>>(state, n_heads, out);
