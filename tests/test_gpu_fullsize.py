@@ -146,3 +146,113 @@ def test_pooled_workload_full_size_layer_step(skv, orc, kv_host):
     finally:
         torch.cuda.synchronize()
         w.close()
+
+
+def test_host_clock_workload_full_size_layer_step(skv, orc):
+    """One layer-step of the host-tier workload -- 8 requests x 250,000 tokens,
+    int4 K/V rows in registered host memory, HBM holding the sketch, 64 sinks,
+    the 1,024-token tail ring and 6,250 CLOCK hot slots per request -- built
+    and launched by the benchmark's own code, from a cold hot buffer:
+
+    * selection bit-exact against the oracle on the same sketch bytes and q8;
+    * resolver: row ids, misses and every CLOCK state word equal the oracle's
+      state machine, and the hot slots it filled (host int4 rows requantised
+      to int8) are bit-exact;
+    * attention within 2e-3 of the fp64 oracle on the resolved rows.
+    """
+    import bench
+    B, Tn, Hkv, d = bench.W_B, bench.W_T, bench.W_HKV, bench.W_D
+    k, S, W = bench.W_K, bench.W_S, bench.W_W
+    w = bench.HostClockWorkloadGPU(torch, skv, wl, torch.device("cuda", 0), layers=1, n_steps=2, eta=0.35)
+    try:
+        R, Hs = w.R, w.Hs
+        k8c = T.host(w.k8[0]).reshape(B, R, Hkv, d).copy()
+        v8c = T.host(w.v8[0]).reshape(B, R, Hkv, d).copy()
+        ksc = T.host(w.ks[0]).reshape(B, R, Hkv).copy()
+        vsc = T.host(w.vs[0]).reshape(B, R, Hkv).copy()
+        w.set_step(0)
+        w.layer(0, lambda name: None)
+        torch.cuda.synchronize()
+        assert int(w.status.item()) == 0
+        L = np.full((B,), Tn, np.int32)
+        sc = orc.index_score(orc.SKETCH_INT4, T.host(w.q8), T.host(w.sk[0]), L, S=S, W=W)
+        ridx, rcnt = orc.topk_select(sc["okey"], L, k, S=S, W=W)
+        gidx, gcnt, grows = T.host(w.idx), T.host(w.cnt), T.host(w.rows)
+        np.testing.assert_array_equal(gcnt, rcnt)
+        np.testing.assert_array_equal(gidx, ridx)
+        host = w.hosts[0].arr.reshape(B, Tn, w.tok_bytes)
+        tok, ref, use, tslot, hand = (T.host(w.tok[0]), T.host(w.ref[0]), T.host(w.use[0]), T.host(w.tslot[0]),
+                                      T.host(w.hand[0]))
+        k8g, v8g = T.host(w.k8[0]).reshape(B, R, Hkv, d), T.host(w.v8[0]).reshape(B, R, Hkv, d)
+        for b in range(B):
+            n = int(rcnt[b])
+            st = orc.ClockState(Hs, Tn)
+            rr, m = st.resolve(Tn, S, W, ridx[b, :n], 0, host[b], k8c[b], v8c[b], ksc[b], vsc[b], Hkv, d)
+            np.testing.assert_array_equal(grows[b, :n], rr, err_msg=f"rows b={b}")
+            assert int(w.nmiss[0, b].item()) == m
+            np.testing.assert_array_equal(tok[b], st.slot_token)
+            np.testing.assert_array_equal(ref[b], st.ref)
+            np.testing.assert_array_equal(use[b], st.use_step)
+            np.testing.assert_array_equal(tslot[b], st.token_slot)
+            assert int(hand[b]) == int(st.hand[0])
+            np.testing.assert_array_equal(k8g[b, S + W:], k8c[b, S + W:])     # the hot slots
+            np.testing.assert_array_equal(v8g[b, S + W:], v8c[b, S + W:])
+        ks_g, vs_g = T.host(w.ks[0]), T.host(w.vs[0])
+        ref_out = orc.attend(orc.KV_INT8, T.host(w.q[0]), k8g.reshape(B * R, -1), v8g.reshape(B * R, -1), grows,
+                             gcnt, 1 / math.sqrt(d), Hkv, d, d, k_scale=ks_g, v_scale=vs_g, req_row_stride=R)
+        err = np.max(np.abs(T.host(w.out) - ref_out))
+        assert err < 2e-3, err
+    finally:
+        torch.cuda.synchronize()
+        w.close()
+
+
+def test_mla_lru_workload_full_size_layer_step(skv, orc):
+    """One layer-step of the latent-row workload -- 32 requests x 142,000
+    tokens, fp8 rows of 576, 128 absorbed heads, indexer over raw 128-dim
+    bf16 keys, pages of 64 with the oldest 70 % host-only, 4,096 LRU hot
+    slots -- built and launched by the benchmark's own code:
+
+    * selection: counts equal; sets differ only within 1e-3 relative of the
+      oracle's 2,048-th score;
+    * resolver: row ids, misses and the pool bytes it wrote equal the
+      oracle's LRU state machine on the GPU's picks;
+    * attention of four requests (all 128 heads) within 2e-3 of the fp64
+      oracle on the resolved rows.
+    """
+    import bench
+    w = bench.MlaLruWorkloadGPU(torch, skv, wl, torch.device("cuda", 0), layers=1, n_steps=2)
+    try:
+        B, Tn, K, P, D, DV = w.B, w.T, w.K, w.PAGE, w.D, w.DV
+        pool0 = T.host(w.pool[0]).copy()
+        w.set_step(0)
+        w.layer(0, lambda name: None)
+        torch.cuda.synchronize()
+        assert int(w.status.item()) == 0
+        L = np.full((B,), Tn, np.int32)
+        sc = orc.index_score(orc.POOLED_BF16, T.host(w.qidx[0]), T.host(w.keys[0]), L, ratio=1)
+        ridx, rcnt = orc.topk_select(sc["okey"], L, K, ratio=1)
+        gidx, gcnt, grows = T.host(w.idx), T.host(w.cnt), T.host(w.rows)
+        np.testing.assert_array_equal(gcnt, rcnt)
+        for b in range(B):
+            kth = np.sort(sc["fscore"][b, :Tn])[::-1][K - 1]
+            for t in set(gidx[b].tolist()) ^ set(ridx[b].tolist()):
+                assert abs(sc["fscore"][b, t] - kth) <= 1e-3 * abs(kth), (b, t)
+        bt = T.host(w.bt)
+        host = w.hosts[0].arr.reshape(B, Tn, D)
+        for b in range(B):
+            st = orc.LruState(w.SLOTS, Tn)
+            rr, m = st.resolve(gidx[b], P, bt[b], w.hot_base + b * w.hot_stride, 0, host[b], pool0, D)
+            np.testing.assert_array_equal(grows[b], rr, err_msg=f"rows b={b}")
+            assert int(w.nmiss[0, b].item()) == m
+        pool1 = T.host(w.pool[0])
+        np.testing.assert_array_equal(pool1, pool0)
+        q = T.host(w.q[0])
+        for b in (0, 7, 19, 31):
+            ref_out = orc.attend(orc.KV_FP8, q[b:b + 1], pool1, pool1, grows[b:b + 1], gcnt[b:b + 1],
+                                 1 / math.sqrt(D), 1, D, DV, k_pitch=D, v_pitch=D)
+            err = np.max(np.abs(T.host(w.out[b:b + 1]) - ref_out))
+            assert err < 2e-3, (b, err)
+    finally:
+        torch.cuda.synchronize()
+        w.close()
