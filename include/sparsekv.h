@@ -506,6 +506,23 @@ int skv_resolve_rows_lru(int B, int64_t t_cap, const int32_t *lengths, int page,
                          const int32_t *idx, int max_rows, const int32_t *count,
                          int32_t *rows_out, int32_t *n_miss, void *workspace,
                          size_t workspace_bytes, int32_t *dev_status, void *stream);
+/*
+ * skv_resolve_rows_lru_leased -- the same, with the hot buffer made of blocks
+ * leased from the pool ([P2] "Three residency states, one block pool": a hot
+ * buffer page is an ordinary KV-cache block, leased from the same pool as the
+ * resident pages): slot s of request b is pool row
+ *   hot_blocks[b][s / page] * page + s mod page,
+ * hot_blocks int32 [B][ceil(n_slots / page)] (see skv_residency_lease_hot).  A
+ * slot whose block is negative or past n_pool_rows gives row -1 and
+ * SKV_DEV_RANGE (its miss is not copied).
+ */
+int skv_resolve_rows_lru_leased(int B, int64_t t_cap, const int32_t *lengths, int page,
+                                const int32_t *block_table, int64_t n_pages, const int32_t *hot_blocks,
+                                int n_slots, int32_t *step, int64_t *stamp, int32_t *slot_token,
+                                int32_t *token_slot, int32_t *order, const uint8_t *host, uint8_t *pool,
+                                int64_t row_bytes, int64_t n_pool_rows, const int32_t *idx, int max_rows,
+                                const int32_t *count, int32_t *rows_out, int32_t *n_miss, void *workspace,
+                                size_t workspace_bytes, int32_t *dev_status, void *stream);
 
 /*
  * skv_quantize_int4_rows -- host-tier row encoding ([P1]: int4 with 64-dim
@@ -613,6 +630,8 @@ int skv_prefill_attend(int nq, int Hq, int Hkv, int d, const uint16_t *q, const 
  *    slot);
  *  - taking a block when none is free releases one page that way; the call
  *    fails with SKV_ENOMEM when nothing is releasable;
+ *  - hot buffers are leased from the same pool (skv_residency_lease_hot): a
+ *    block freed by one request can become another request's hot capacity;
  *  - a request added with host_prefix = 1 (a prefix that exists only in host
  *    memory) starts with placeholders for its complete pages; a partial last
  *    page gets a block whose first rows must be brought in (listed by
@@ -642,6 +661,11 @@ int skv_residency_mark_copied(skv_residency *r, int b, const int32_t *pages, int
 /* Resident pages of slot b whose first rows must come from host memory. */
 int skv_residency_fills(const skv_residency *r, int b, int32_t *pages, int max_out, int *n_out);
 int skv_residency_mark_filled(skv_residency *r, int b, const int32_t *pages, int n);
+/* Leases n_pages blocks as slot b's hot buffer (releasing pages under the rule
+ * above when none is free) and writes their numbers to blocks[0 .. n_pages);
+ * they stay leased until skv_residency_remove.  A second lease for the same
+ * slot is SKV_EINVAL. */
+int skv_residency_lease_hot(skv_residency *r, int b, int n_pages, int32_t *blocks);
 /* Releases up to n_wanted pages under the rule above; released[2i], [2i+1] =
  * (slot, page); *n_out of them. */
 int skv_residency_reclaim(skv_residency *r, int n_wanted, int32_t *released, int *n_out);

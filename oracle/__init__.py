@@ -79,7 +79,7 @@ def _load():
                 "orc_clock_step": ([i32, P, P, P, P, P, ctypes.c_int32, P, i32, P, P], i32),
                 "orc_resolve_clock": ([i64, i32, i32, i32, i32, i32, P, i32, ctypes.c_int32,
                                        P, P, P, P, P, P, P, P, P, P, P], i32),
-                "orc_resolve_lru": ([P, i32, i32, P, i64, i32, i64, P, P, P, P, P, i64, P], i32),
+                "orc_resolve_lru": ([P, i32, i32, P, i64, P, i32, i64, P, P, P, P, P, i64, P], i32),
             }
             for name, (args, res) in sig.items():
                 fn = getattr(lib, name)
@@ -359,12 +359,14 @@ class LruState:
         self.slot_token = np.full((n_slots,), -1, np.int32)
         self.token_slot = np.full((n_tok,), -1, np.int32)
 
-    def resolve(self, idx, page, block_table, hot_base, step, host, pool, row_bytes):
+    def resolve(self, idx, page, block_table, hot_base, step, host, pool, row_bytes, hot_rows=None):
+        """hot_rows: int32 [n_slots] pool row of each hot slot (leased blocks), or None for hot_base + s."""
         lib = _load()
         idx = _c(idx, np.int32)
         bt = _c(block_table, np.int32)
+        hr = None if hot_rows is None else _c(hot_rows, np.int32)
         rows = np.zeros((idx.shape[0],), np.int32)
-        m = lib.orc_resolve_lru(_p(idx), idx.shape[0], page, _p(bt), int(hot_base), self.n_slots,
+        m = lib.orc_resolve_lru(_p(idx), idx.shape[0], page, _p(bt), int(hot_base), _p(hr), self.n_slots,
                                 int(step), _p(self.stamp), _p(self.slot_token), _p(self.token_slot),
                                 _p(host), _p(pool), int(row_bytes), _p(rows))
         if m < 0:

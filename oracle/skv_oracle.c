@@ -752,7 +752,9 @@ static int cmp_lru(const void *a, const void *b) {
  * into an LRU slot; the tail is never evicted; [P2] "What it composes with":
  * the hot buffer holds 2 x top-K rows).  Readings: pages of `page` tokens;
  * block_table[p] >= 0 is the pool page holding resident page p, -1 a null
- * placeholder (host-only page).  Hot slot s is pool row hot_base + s.
+ * placeholder (host-only page).  Hot slot s is pool row hot_rows[s] when
+ * hot_rows is given (a hot-buffer page is an ordinary block leased from the
+ * pool: "Three residency states, one block pool"), else hot_base + s.
  * State: stamp[n_slots] (-1 empty), slot_token[n_slots] (-1 none),
  * token_slot[n_tok] (-1 none).
  *   1. resident token: row = block_table[t/page]*page + t%page;
@@ -765,7 +767,7 @@ static int cmp_lru(const void *a, const void *b) {
  * untouched slots are fewer than the misses.
  */
 ORC_API int orc_resolve_lru(const int32_t *idx, int n, int page, const int32_t *block_table,
-                            int64_t hot_base, int n_slots, int64_t step, int64_t *stamp,
+                            int64_t hot_base, const int32_t *hot_rows, int n_slots, int64_t step, int64_t *stamp,
                             int32_t *slot_token, int32_t *token_slot,
                             const uint8_t *host, uint8_t *pool, int64_t row_bytes,
                             int32_t *row_out) {
@@ -780,7 +782,7 @@ ORC_API int orc_resolve_lru(const int32_t *idx, int n, int page, const int32_t *
     } else if (token_slot[t] >= 0) {
       int32_t s = token_slot[t];
       stamp[s] = step;
-      row_out[i] = (int32_t)(hot_base + s);
+      row_out[i] = hot_rows ? hot_rows[s] : (int32_t)(hot_base + s);
     } else {
       mtok[nm] = (int32_t)t;
       mpos[nm] = i;
@@ -806,7 +808,7 @@ ORC_API int orc_resolve_lru(const int32_t *idx, int n, int page, const int32_t *
     slot_token[s] = mtok[i];
     token_slot[mtok[i]] = s;
     stamp[s] = step;
-    int64_t row = hot_base + s;
+    int64_t row = hot_rows ? (int64_t)hot_rows[s] : hot_base + s;
     memcpy(pool + row * row_bytes, host + (int64_t)mtok[i] * row_bytes, (size_t)row_bytes);
     row_out[mpos[i]] = (int32_t)row;
   }

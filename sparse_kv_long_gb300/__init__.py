@@ -73,6 +73,9 @@ def _load():
                                             P, P, P, P, i64, P, P, P, sz, P, P], i32),
                 "skv_resolve_rows_lru": ([i32, i64, P, i32, P, i64, i64, i64, i32, P, P, P, P, P, P, P, i64, i64,
                                           P, i32, P, P, P, P, sz, P, P], i32),
+                "skv_resolve_rows_lru_leased": ([i32, i64, P, i32, P, i64, P, i32, P, P, P, P, P, P, P, i64, i64,
+                                                 P, i32, P, P, P, P, sz, P, P], i32),
+                "skv_residency_lease_hot": ([P, i32, i32, P], i32),
                 "skv_quantize_int4_rows": ([P, i64, i32, i32, P, P, i64, i64, P], i32),
                 "skv_stream_read": ([P, sz, P, i32, P], i32),
                 "skv_prefill_index_scores": ([i32, P, P, i64, P, i64, P, P], i32),
@@ -290,14 +293,23 @@ def resolve_rows_clock(lengths, idx, count, step, S, W, Hs, slot_token, ref, use
 
 
 def resolve_rows_lru(lengths, idx, count, step, page, block_table, hot_base, hot_stride, stamp, slot_token,
-                     token_slot, order, host, pool, rows_out, n_miss, workspace=None, status=None, stream=None):
+                     token_slot, order, host, pool, rows_out, n_miss, workspace=None, status=None, stream=None,
+                     hot_blocks=None):
     """Block table + LRU hot buffer resolve (see skv_resolve_rows_lru).  step: int32 device tensor [2]
-    (advanced by the call); host: uint8 tensor or int alias."""
+    (advanced by the call); host: uint8 tensor or int alias.  hot_blocks: int32 device tensor
+    [B][ceil(n_slots / page)] of leased blocks (skv_resolve_rows_lru_leased; hot_base, hot_stride unused)."""
     B, max_rows = idx.shape
     t_cap = token_slot.shape[1]
     n_slots = stamp.shape[1]
     n_pool_rows, row_bytes = pool.shape
     workspace = _resolve_ws(workspace, B, max_rows)
+    if hot_blocks is not None:
+        _check("skv_resolve_rows_lru_leased", _load().skv_resolve_rows_lru_leased(
+            B, t_cap, _ptr(lengths), page, _ptr(block_table), block_table.shape[1], _ptr(hot_blocks), n_slots,
+            _ptr(step), _ptr(stamp), _ptr(slot_token), _ptr(token_slot), _ptr(order), _addr(host), _ptr(pool),
+            row_bytes, n_pool_rows, _ptr(idx), max_rows, _ptr(count), _ptr(rows_out), _ptr(n_miss),
+            _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream)))
+        return rows_out, n_miss
     _check("skv_resolve_rows_lru", _load().skv_resolve_rows_lru(
         B, t_cap, _ptr(lengths), page, _ptr(block_table), block_table.shape[1], int(hot_base), int(hot_stride),
         n_slots, _ptr(step), _ptr(stamp), _ptr(slot_token), _ptr(token_slot), _ptr(order), _addr(host), _ptr(pool),
@@ -440,6 +452,14 @@ class Residency:
         p = np.ascontiguousarray(pages, np.int32)
         _check("skv_residency_mark_filled", _load().skv_residency_mark_filled(
             self._h, b, p.ctypes.data_as(ctypes.c_void_p), p.size))
+
+    def lease_hot(self, b, n_pages):
+        """Leases n_pages pool blocks as slot b's hot buffer; returns their numbers."""
+        import numpy as np
+        out = np.zeros((n_pages,), np.int32)
+        _check("skv_residency_lease_hot", _load().skv_residency_lease_hot(
+            self._h, b, int(n_pages), out.ctypes.data_as(ctypes.c_void_p)))
+        return out
 
     def reclaim(self, n):
         import numpy as np

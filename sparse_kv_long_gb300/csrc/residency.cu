@@ -84,6 +84,7 @@ struct skv_residency {
     int64_t resident = 0;            // resident pages
     int64_t first_pending = 0;       // pages below: copied, placeholders or awaiting a fill
     int64_t first_release = 0;       // pages below: placeholders
+    std::vector<int32_t> hot;        // blocks leased as the request's hot buffer
   };
   int n_blocks = 0, page = 0, tail_pages = 0;
   int64_t max_pages = 0;
@@ -199,6 +200,7 @@ SKV_EXPORT int skv_residency_remove(skv_residency* r, int b) {
   if (!r || !r->valid(b)) return SKV_EINVAL;
   for (int32_t blk : r->req[b].block)
     if (blk >= 0) r->free_list.push_back(blk);
+  for (int32_t blk : r->req[b].hot) r->free_list.push_back(blk);
   r->req[b] = skv_residency::Req();
   return SKV_OK;
 }
@@ -278,6 +280,22 @@ SKV_EXPORT int skv_residency_mark_filled(skv_residency* r, int b, const int32_t*
     q.need_fill[pages[i]] = 0;
     q.host_copy[pages[i]] = 0;
   }
+  return SKV_OK;
+}
+
+SKV_EXPORT int skv_residency_lease_hot(skv_residency* r, int b, int n_pages, int32_t* blocks) {
+  if (!r || !r->valid(b) || n_pages < 1 || !blocks || !r->req[b].hot.empty()) return SKV_EINVAL;
+  std::vector<int32_t> got;
+  for (int i = 0; i < n_pages; i++) {
+    const int32_t blk = r->take_block();  // may release pages of any request, this one's included
+    if (blk < 0) {
+      for (int32_t t : got) r->free_list.push_back(t);
+      return SKV_ENOMEM;
+    }
+    got.push_back(blk);
+  }
+  r->req[b].hot = got;
+  for (int i = 0; i < n_pages; i++) blocks[i] = got[i];
   return SKV_OK;
 }
 

@@ -377,28 +377,30 @@ __global__ __launch_bounds__(32 * kFetchWarps) void fetch_rows_kernel(
   constexpr int kPer = kFetchPieces / kRowsPerWarp;
   const uint8_t* src[kRowsPerWarp];
   uint4* dst[kRowsPerWarp];
+  bool live[kRowsPerWarp];  // a miss whose destination row is known (-1: nothing to write)
 #pragma unroll
   for (int u = 0; u < kRowsPerWarp; u++) {
     const int j = j0 + u < nm ? j0 + u : j0;  // j0 < nm
     const int32_t tok = ws_tok[static_cast<int64_t>(b) * max_rows + j];
     const int64_t row = ws_row[static_cast<int64_t>(b) * max_rows + j];
+    live[u] = j0 + u < nm && row >= 0;
     src[u] = host + (static_cast<int64_t>(b) * t_cap + tok) * row_bytes;
-    dst[u] = reinterpret_cast<uint4*>(pool + row * row_bytes);
+    dst[u] = reinterpret_cast<uint4*>(pool + (row >= 0 ? row : 0) * row_bytes);
   }
   uint4 v[kRowsPerWarp][kPer];
 #pragma unroll
   for (int u = 0; u < kRowsPerWarp; u++)
 #pragma unroll
     for (int q = 0; q < kPer; q++)
-      if (j0 + u < nm && lane + 32 * q < chunks) v[u][q] = ld_nc16(src[u] + 16 * (lane + 32 * q));
+      if (live[u] && lane + 32 * q < chunks) v[u][q] = ld_nc16(src[u] + 16 * (lane + 32 * q));
 #pragma unroll
   for (int u = 0; u < kRowsPerWarp; u++)
 #pragma unroll
     for (int q = 0; q < kPer; q++)
-      if (j0 + u < nm && lane + 32 * q < chunks) dst[u][lane + 32 * q] = v[u][q];
+      if (live[u] && lane + 32 * q < chunks) dst[u][lane + 32 * q] = v[u][q];
   for (int c = lane + 32 * kPer; c < chunks; c += 32)  // rows above kPer * 512 bytes
     for (int u = 0; u < kRowsPerWarp; u++)
-      if (j0 + u < nm) dst[u][c] = ld_nc16(src[u] + 16 * c);
+      if (live[u]) dst[u][c] = ld_nc16(src[u] + 16 * c);
 }
 
 // ---------------------------------------------------------------------------
@@ -428,6 +430,11 @@ struct LruArgs {
   int32_t* ws_tok;
   int32_t* ws_row;
   int32_t* status;
+  // Leased hot pages ([P2]: a hot-buffer page is an ordinary block of the
+  // pool): slot s of request b is row hot_blocks[b][s / page] * page + s % page.
+  // NULL: the reserved region hot_base + b * hot_stride + s.
+  const int32_t* hot_blocks;
+  int n_hot_pages;
 };
 
 size_t lru_smem_bytes(int n_slots, int max_rows) {
@@ -463,6 +470,13 @@ __global__ __launch_bounds__(kResThreads) void lru_kernel(LruArgs a) {
   const int32_t* bt = a.block_table + static_cast<int64_t>(b) * a.n_pages;
   const int64_t sbase = static_cast<int64_t>(b) * ns;
   const int64_t hot = a.hot_base + static_cast<int64_t>(b) * a.hot_stride;
+  const int32_t* hb = a.hot_blocks ? a.hot_blocks + static_cast<int64_t>(b) * a.n_hot_pages : nullptr;
+  auto hot_row = [&](int s) -> int64_t {  // -1 when the leased page is missing or out of the pool
+    if (!hb) return hot + s;
+    const int64_t blk = hb[s / a.page];
+    const int64_t row = blk * a.page + s % a.page;
+    return blk < 0 || row >= a.n_pool_rows ? -1 : row;
+  };
   const int64_t step = read_step(a.step);
 
   for (int s = tid; s < ns; s += kResThreads) s_stamp[s] = a.stamp[sbase + s];
@@ -489,7 +503,9 @@ __global__ __launch_bounds__(kResThreads) void lru_kernel(LruArgs a) {
         const int32_t s = tslot[t];
         if (s >= 0 && s < ns) {
           s_stamp[s] = step;
-          rows[i] = static_cast<int32_t>(hot + s);
+          const int64_t row = hot_row(s);
+          if (row < 0) set_status(a.status, SKV_DEV_RANGE);
+          rows[i] = static_cast<int32_t>(row);
         } else {
           if (s >= ns) set_status(a.status, SKV_DEV_RANGE);
           rows[i] = -1;
@@ -553,9 +569,11 @@ __global__ __launch_bounds__(kResThreads) void lru_kernel(LruArgs a) {
       if (old >= 0 && old < a.t_cap) tslot[old] = -1;
       a.slot_token[sbase + sl] = tok;
       tslot[tok] = sl;
-      rows[m_pos[j]] = static_cast<int32_t>(hot + sl);
+      const int64_t row = hot_row(sl);  // -1: the fetch skips it
+      if (row < 0) set_status(a.status, SKV_DEV_RANGE);
+      rows[m_pos[j]] = static_cast<int32_t>(row);
       a.ws_tok[static_cast<int64_t>(b) * a.max_rows + j] = tok;  // the miss list for the fetch kernel
-      a.ws_row[static_cast<int64_t>(b) * a.max_rows + j] = static_cast<int32_t>(hot + sl);
+      a.ws_row[static_cast<int64_t>(b) * a.max_rows + j] = static_cast<int32_t>(row);
     }
     __syncthreads();
     for (int j = tid; j < nm; j += kResThreads) s_stamp[s_new[j]] = step;
@@ -745,22 +763,21 @@ SKV_EXPORT int skv_resolve_rows_clock(int B, int64_t t_cap, const int32_t* lengt
   return launch_status();
 }
 
-SKV_EXPORT int skv_resolve_rows_lru(int B, int64_t t_cap, const int32_t* lengths, int page,
-                                    const int32_t* block_table, int64_t n_pages, int64_t hot_base,
-                                    int64_t hot_stride, int n_slots, int32_t* step, int64_t* stamp,
-                                    int32_t* slot_token, int32_t* token_slot, int32_t* order, const uint8_t* host,
-                                    uint8_t* pool,
-                                    int64_t row_bytes, int64_t n_pool_rows, const int32_t* idx, int max_rows,
-                                    const int32_t* count, int32_t* rows_out, int32_t* n_miss, void* workspace,
-                                    size_t workspace_bytes, int32_t* dev_status, void* stream) {
+namespace {
+int lru_resolve(int B, int64_t t_cap, const int32_t* lengths, int page, const int32_t* block_table, int64_t n_pages,
+                int64_t hot_base, int64_t hot_stride, const int32_t* hot_blocks, int n_slots, int32_t* step,
+                int64_t* stamp, int32_t* slot_token, int32_t* token_slot, int32_t* order, const uint8_t* host,
+                uint8_t* pool, int64_t row_bytes, int64_t n_pool_rows, const int32_t* idx, int max_rows,
+                const int32_t* count, int32_t* rows_out, int32_t* n_miss, void* workspace, size_t workspace_bytes,
+                int32_t* dev_status, void* stream) {
   if (B < 0 || B > 65535 || t_cap < 0 || page < 1 || n_pages < 0 || n_slots < 1 || max_rows < 1 ||
       row_bytes < 16 || row_bytes % 16 || hot_base < 0 || hot_stride < 0)
     return SKV_EINVAL;
   if (B == 0) return SKV_OK;
   if (n_slots > kMaxLruSlots || max_rows > kMaxResolveRows || t_cap > INT32_MAX) return SKV_EUNSUPPORTED;
   if (!step) return SKV_EINVAL;
-  if (hot_base + static_cast<int64_t>(B - 1) * hot_stride + n_slots > n_pool_rows || n_pool_rows > INT32_MAX)
-    return SKV_EINVAL;
+  if (n_pool_rows > INT32_MAX) return SKV_EINVAL;
+  if (!hot_blocks && hot_base + static_cast<int64_t>(B - 1) * hot_stride + n_slots > n_pool_rows) return SKV_EINVAL;
   if (!lengths || !block_table || !stamp || !slot_token || !token_slot || !order || !host || !pool || !idx ||
       !count || !rows_out || !n_miss)
     return SKV_EINVAL;
@@ -780,7 +797,7 @@ SKV_EXPORT int skv_resolve_rows_lru(int B, int64_t t_cap, const int32_t* lengths
   }
   LruArgs a{t_cap, lengths, page, block_table, n_pages, hot_base, hot_stride, n_slots, step, stamp, slot_token,
             token_slot, order, host, pool, row_bytes, n_pool_rows, idx, max_rows, count, rows_out, n_miss, ws_tok,
-            ws_row, dev_status};
+            ws_row, dev_status, hot_blocks, (n_slots + page - 1) / page};
   cudaStream_t st = as_stream(stream);
   lru_kernel<<<B, kResThreads, smem, st>>>(a);
   const int per_cta = kFetchWarps * kRowsPerWarp;
@@ -790,6 +807,34 @@ SKV_EXPORT int skv_resolve_rows_lru(int B, int64_t t_cap, const int32_t* lengths
     return SKV_ECUDA;
   }
   return launch_status();
+}
+}  // namespace
+
+SKV_EXPORT int skv_resolve_rows_lru(int B, int64_t t_cap, const int32_t* lengths, int page,
+                                    const int32_t* block_table, int64_t n_pages, int64_t hot_base,
+                                    int64_t hot_stride, int n_slots, int32_t* step, int64_t* stamp,
+                                    int32_t* slot_token, int32_t* token_slot, int32_t* order, const uint8_t* host,
+                                    uint8_t* pool,
+                                    int64_t row_bytes, int64_t n_pool_rows, const int32_t* idx, int max_rows,
+                                    const int32_t* count, int32_t* rows_out, int32_t* n_miss, void* workspace,
+                                    size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  return lru_resolve(B, t_cap, lengths, page, block_table, n_pages, hot_base, hot_stride, nullptr, n_slots, step,
+                     stamp, slot_token, token_slot, order, host, pool, row_bytes, n_pool_rows, idx, max_rows, count,
+                     rows_out, n_miss, workspace, workspace_bytes, dev_status, stream);
+}
+
+SKV_EXPORT int skv_resolve_rows_lru_leased(int B, int64_t t_cap, const int32_t* lengths, int page,
+                                           const int32_t* block_table, int64_t n_pages, const int32_t* hot_blocks,
+                                           int n_slots, int32_t* step, int64_t* stamp, int32_t* slot_token,
+                                           int32_t* token_slot, int32_t* order, const uint8_t* host, uint8_t* pool,
+                                           int64_t row_bytes, int64_t n_pool_rows, const int32_t* idx, int max_rows,
+                                           const int32_t* count, int32_t* rows_out, int32_t* n_miss,
+                                           void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                           void* stream) {
+  if (!hot_blocks) return SKV_EINVAL;
+  return lru_resolve(B, t_cap, lengths, page, block_table, n_pages, 0, 0, hot_blocks, n_slots, step, stamp,
+                     slot_token, token_slot, order, host, pool, row_bytes, n_pool_rows, idx, max_rows, count,
+                     rows_out, n_miss, workspace, workspace_bytes, dev_status, stream);
 }
 
 SKV_EXPORT int skv_quantize_int4_rows(const uint16_t* x, int64_t n_rows, int Hkv, int d, const int64_t* out_rows,

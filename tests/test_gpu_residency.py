@@ -39,21 +39,36 @@ def skv():
     return m
 
 
-def test_pressure_driven_transitions_under_decode(skv, orc):
+@pytest.mark.parametrize("leased", [False, True], ids=["reserved_hot", "leased_hot"])
+def test_pressure_driven_transitions_under_decode(skv, orc, leased):
+    """leased: every request's hot buffer is made of blocks leased from the
+    same pool as the resident pages (skv_residency_lease_hot and the leased
+    resolver); otherwise a reserved region after the pool's blocks."""
     B, page, t_cap, row_bytes = 3, 16, 1024, 576
     max_pages = t_cap // page
-    n_blocks, n_slots, k, n_steps = 60, 40, 24, 48
+    n_slots, k, n_steps = 40, 24, 48
+    n_hp = -(-n_slots // page)                  # hot pages per request
+    n_blocks = 60 + (B * n_hp if leased else 0)
     start = [500, 400, 300]                     # requests 0, 1 resident; 2 from a host prefix
     rng = np.random.default_rng(77)
     truth = rng.integers(0, 256, (B, t_cap, row_bytes), dtype=np.uint8)
     hot_base, hot_stride = n_blocks * page, n_slots
-    n_pool_rows = hot_base + B * hot_stride
+    n_pool_rows = n_blocks * page if leased else hot_base + B * hot_stride
 
     r = skv.Residency(n_blocks, page, B, max_pages, tail_pages=1)
     r.add(0, start[0])
     r.add(1, start[1])
     r.add(2, start[2], host_prefix=True)
     assert r.state(2) == skv.RESIDENCY_MIXED   # placeholders plus the resident partial last page
+    hot_rows = [None] * B
+    g_hot = None
+    if leased:
+        hb = np.stack([r.lease_hot(b, n_hp) for b in range(B)])
+        assert r.free_blocks() == n_blocks - 58 - B * n_hp
+        hot_rows = [(hb[b][np.arange(n_slots) // page] * page + np.arange(n_slots) % page).astype(np.int32)
+                    for b in range(B)]
+        assert len(set(np.concatenate(hot_rows).tolist())) == B * n_slots
+        g_hot = T.dev(hb.astype(np.int32))
 
     # host tier (registered host memory): only request 2's prefix is there at first
     nbytes = B * t_cap * row_bytes
@@ -132,14 +147,14 @@ def test_pressure_driven_transitions_under_decode(skv, orc):
             nmiss = torch.zeros((B,), dtype=torch.int32, device="cuda")
             skv.resolve_rows_lru(T.dev(np.array(n_tok, np.int32)), T.dev(idx), T.dev(np.full(B, k, np.int32)), g_step,
                                  page, g_bt, hot_base, hot_stride, g_stamp, g_tok, g_tslot, g_order, alias, g_pool,
-                                 rows, nmiss, status=st)
+                                 rows, nmiss, status=st, hot_blocks=g_hot)
             torch.cuda.synchronize()
             assert int(st.item()) == 0
             got = T.host(rows)
             pool_now = T.host(g_pool)
             for b in range(B):
                 ref_rows, m = states[b].resolve(idx[b], page, bt[b], hot_base + b * hot_stride, step, host_cpu[b],
-                                                pool_cpu, row_bytes)
+                                                pool_cpu, row_bytes, hot_rows=hot_rows[b])
                 np.testing.assert_array_equal(got[b], ref_rows, err_msg=f"rows b={b} step={step}")
                 assert int(nmiss[b].item()) == m
                 np.testing.assert_array_equal(pool_now[got[b]], truth[b, idx[b]], err_msg=f"bytes b={b} step={step}")

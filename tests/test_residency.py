@@ -136,3 +136,24 @@ def test_argument_errors():
         r.add(0, 4)                                     # slot in use
     with pytest.raises(SkvError):
         r.append(0, 100)                                # past max_pages
+
+
+def test_hot_buffers_are_leased_from_the_pool():
+    page = 4
+    r = skv.Residency(n_blocks=12, page=page, max_requests=2, max_pages=16, tail_pages=1)
+    r.add(0, 8 * page)                                  # 8 blocks
+    hb0 = r.lease_hot(0, 2)                             # 2 more: 10 used, 2 free
+    assert r.free_blocks() == 2 and len(set(hb0.tolist()) | set(r.block_table()[0, :8].tolist())) == 10
+    with pytest.raises(SkvError):
+        r.lease_hot(0, 1)                               # one lease per request
+    r.add(1, 0)
+    with pytest.raises(SkvError):
+        r.lease_hot(1, 3)                               # 2 free and nothing copied: cannot lease 3
+    assert r.free_blocks() == 2                         # a failed lease takes nothing
+    r.mark_copied(0, r.pending(0))
+    hb1 = r.lease_hot(1, 3)                             # request 0 gives its oldest copied page
+    t = r.block_table()
+    assert t[0, 0] == -1 and r.free_blocks() == 0
+    assert not (set(hb1.tolist()) & set(hb0.tolist())) and not (set(hb1.tolist()) & set(t[t >= 0].tolist()))
+    r.remove(0)                                         # its pages and its hot blocks return
+    assert r.free_blocks() == 7 + 2
