@@ -580,12 +580,17 @@ int skv_prefill_index_scores(int nq, const uint16_t *q_idx, const uint16_t *pool
 
 /*
  * skv_prefill_attend -- exact attention of each query of a prefill chunk over
- * its own selected tokens, loops swapped: for every history chunk [c0, c0 +
- * chunk_tokens) below n_tokens, the chunk's K and V rows are copied once
- * (cudaMemcpyAsync on `stream`) from k_src / v_src into the staging buffers;
- * one launch then attends every query head to the query's selected tokens
- * inside the chunk and merges the partial softmax state (running max m, sum
- * l, accumulator acc) into `state`; a last launch writes out = acc / l.  For
+ * its own selected tokens, loops swapped: the history below n_tokens is taken
+ * chunk by chunk, each chunk's K and V rows copied once into the staging
+ * buffers; one launch attends every query head to the query's selected
+ * tokens inside the chunk and merges the partial softmax state (running max
+ * m, sum l, accumulator acc) into `state`; a last launch writes out = acc / l.
+ * When the sources are device-readable (device memory, or host memory
+ * registered with skv_host_register) the buffers are used as two halves of
+ * chunk_tokens / 2 rows and the launch that attends one half also copies the
+ * next chunk into the other, overlapping the copies with the attention;
+ * otherwise each chunk of chunk_tokens rows goes in with cudaMemcpyAsync on
+ * `stream` before its launch.  For
  * query i and query head g (KV head g / (Hq / Hkv)) the result is
  *   out[i][g] = sum_{t in S_i} softmax_t(scale * q[i][g] . k[t]) v[t],
  * S_i = idx[i][0 .. count[i]), which is what skv_sparse_attend_decode gives
