@@ -449,6 +449,29 @@ def test_score_select_int4_bit_exact(skv, orc, lengths, width, k, S, W):
             assert np.array_equal(gk[b, S:lengths[b] - W], ref["okey"][b, S:lengths[b] - W])
 
 
+@pytest.mark.parametrize("k,S,W", [(512, 64, 256), (7, 0, 0), (1, 4, 4)])
+def test_score_select_and_topk_edge_lengths(skv, orc, k, S, W):
+    """The lengths around every boundary at once (1, 3-5, 63-65 tokens, the
+    dense threshold S + W + k and its neighbours, 2051/2052, 8192), the fused
+    launch and the standalone selection both bit-exact against the oracle."""
+    rng = np.random.default_rng(1200 + k)
+    edge = S + W + k
+    lengths = sorted({1, 3, 4, 5, 63, 64, 65, 831, 832, 833, 2051, 2052, 8192, edge - 1, edge, edge + 1})
+    lengths = [t for t in lengths if t >= 1]
+    B, n_cap, width = len(lengths), max(lengths), 256
+    q8 = rng.integers(-127, 128, (B, width)).astype(np.int8)
+    sk = rng.integers(0, 256, (B, n_cap, width // 2)).astype(np.uint8)
+    L = np.array(lengths, np.int32)
+    ref = orc.index_score(orc.SKETCH_INT4, q8, sk, L, S=S, W=W)
+    ri, rc = orc.topk_select(ref["okey"], L, k, S=S, W=W)
+    gi, gc, _ = run_fused(skv, skv.SKETCH_INT4, T.dev(q8), T.dev(sk), L, k, S, W, want_keys=False)
+    ti, tc = run_topk(skv, ref["okey"], L, k, S, W)
+    assert np.array_equal(gc, rc) and np.array_equal(tc, rc)
+    for b in range(B):
+        assert np.array_equal(gi[b, :gc[b]], ri[b, :rc[b]]), lengths[b]
+        assert np.array_equal(ti[b, :tc[b]], ri[b, :rc[b]]), lengths[b]
+
+
 @pytest.mark.parametrize("distinct", [1, 2, 5])
 def test_score_select_ties(skv, orc, distinct):
     """All rows drawn from a few distinct sketches: massive exact ties, incl. the
