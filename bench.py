@@ -80,6 +80,26 @@ def peaks():
     return 6800.0, "fallback"
 
 
+def max_over_ranks(x, world, device=None):
+    """The largest x over the replicas; every rank calls it.  A replica
+    decodes its own requests and shares nothing with the others, so this is
+    the only collective, outside the timed region: the job's time is its
+    slowest replica's."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank, seconds, world):
+    """Whole-job throughput: the units all replicas processed over the
+    (slowest replica's) time."""
+    return units_per_rank * world / seconds
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle sample (cpu_baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
@@ -336,15 +356,10 @@ def run_gpu(args):
             e1.record(stream)
         torch.cuda.synchronize()
     barrier()
-    ms_total = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(e0.elapsed_time(e1), world, dev)
     ms_per_step = ms_total / args.steps
-    steps_per_s = 1e3 / ms_per_step
-    value = steps_per_s * L * world              # layer-steps/s over all replicas
-    tokens_per_s = steps_per_s * W_B * world
+    value = job_rate(args.steps * L, ms_total * 1e-3, world)         # layer-steps/s over all replicas
+    tokens_per_s = job_rate(args.steps * W_B, ms_total * 1e-3, world)
     status = int(w.status.item())
 
     # ---- per-kernel durations: eager launches queued behind a sleep -------------------
@@ -402,7 +417,8 @@ def run_gpu(args):
         stream.synchronize()
     e2e_s = (time.perf_counter() - t0) / args.steps
     barrier()
-    e2e_value = L * world / e2e_s
+    e2e_s = max_over_ranks(e2e_s, world, dev)
+    e2e_value = job_rate(L, e2e_s, world)
 
     if rank != 0:
         return
