@@ -155,12 +155,22 @@ class OracleSample:
 
 def cpu_baseline_block(budget_s=15.0):
     s = OracleSample()
+    cores = s.orc.max_threads()
     times = s.time_steps(budget_s=budget_s)
     per_req_layer = statistics.median(times)
     value = 1.0 / (per_req_layer * W_B)  # layer-steps/s (a layer-step covers all 8 requests)
-    return {"value": value, "unit": UNIT, "cores": s.orc.max_threads(), "kind": "oracle",
+    # the same sample on one thread (a few runs, within a fifth of the budget)
+    s.orc.set_threads(1)
+    try:
+        t1 = s.time_steps(n=5, budget_s=budget_s / 5)
+    finally:
+        s.orc.set_threads(cores)
+    per_1 = statistics.median(t1)
+    return {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"1 request x 1 layer at 250,000 tokens (a1..a6), {len(times)} runs, median "
-                      f"{per_req_layer:.3f} s, scaled x8 requests per layer-step"}
+                      f"{per_req_layer:.3f} s, scaled x8 requests per layer-step",
+            "one_thread": {"value": 1.0 / (per_1 * W_B), "unit": UNIT, "cores": 1,
+                           "sample": f"the same sample, {len(t1)} runs on one thread, median {per_1:.3f} s"}}
 
 
 def run_reference(args):
