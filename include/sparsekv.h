@@ -227,7 +227,10 @@ int skv_index_score(int mode, int B, int width, const void *query, const void *k
  *    count[b] = ratio*k + T % ratio.
  *   order_keys u32 [B][n_cap] (skv_index_score output; n_cap in candidates)
  *   idx        int32 [B][max_rows]   count int32 [B]
- *   workspace  skv_topk_workspace_size(B) bytes (zero-filled before first use)
+ *   workspace  skv_topk_workspace_size(B) bytes, zero-filled before first use.
+ *              Each request's scratch sits at a fixed stride whatever B is and
+ *              every call returns its counters to zero, so a workspace sized
+ *              for B_max serves later calls with any B <= B_max, in any order.
  * Constraints: k >= 1; max_rows >= S + k + W (sketch) or ratio*k + ratio - 1
  * (pooled); B <= 4096.  The result is unique and bit-exact.
  */
@@ -272,7 +275,9 @@ int skv_topk_select_noalloc(int B, const uint32_t *order_keys, int64_t n_cap,
  * digit passes skip the bits all keys share.  `order_keys` ([B][n_cap], may be
  * NULL) receives a copy of the keys of the candidates.
  *   workspace  skv_score_select_workspace_size(B) bytes, zero-filled before
- *              first use; each call returns its counters to zero.
+ *              first use; each call returns its counters to zero.  Per-request
+ *              scratch sits at a fixed stride, so a workspace sized for B_max
+ *              serves later calls with any B <= B_max, in any order.
  * Errors: as skv_index_score and skv_topk_select; SKV_EUNSUPPORTED when B is
  * larger than the GPU can hold one resident CTA per request for, or when a
  * request's chunk of keys does not fit on chip (more than about 24K rows per
@@ -381,7 +386,11 @@ int skv_sparse_attend_decode(int kv_kind, int B, int Hq, int Hkv, int d,
  *   workspace  skv_mla_workspace_size(B, max_rows) bytes (no zero-fill needed)
  * A row outside [0, n_pool_rows) is skipped and sets SKV_DEV_RANGE.  The
  * row splits are merged in a fixed order: the output is deterministic (two
- * splits merge inside one thread-block cluster and need no workspace).
+ * splits merge inside one thread-block cluster and need no workspace).  A
+ * request of more than 64 rows always runs as at least two splits (with more
+ * than half as many requests as SMs, two per request in 4-CTA clusters, in
+ * more than one wave); one CTA pair never streams several 64-row chunks on
+ * its own.
  * Runs on the tcgen05 tensor cores with fp16 operands (fp8 -> fp16 exact),
  * fp32 accumulation; probabilities rounded to fp16.
  * Errors: SKV_EUNSUPPORTED unless Hq = 128, d = 576, dv = 512; SKV_EINVAL for

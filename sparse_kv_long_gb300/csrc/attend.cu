@@ -633,10 +633,12 @@ __global__ __launch_bounds__(kThreads, 2) void attend_kernel(AttendArgs a) {
 }
 
 
+// CTAs per SM on the current device; also raises the kernel's dynamic
+// shared-memory limit there (once per device).
 template <int KV>
 int occupancy() {
-  static int cached = -1;
-  if (cached < 0) {
+  static std::atomic<int> cached[kMaxDevices];
+  return once_per_device(cached, []() -> int {
     int per_sm = 0;
     if (cudaFuncSetAttribute(attend_kernel<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(dyn_smem<KV>())) != cudaSuccess ||
@@ -644,11 +646,10 @@ int occupancy() {
             cudaSuccess ||
         per_sm < 1) {
       cudaGetLastError();
-      per_sm = 1;
+      return -1;
     }
-    cached = per_sm;
-  }
-  return cached;
+    return per_sm;
+  });
 }
 
 struct Plan {

@@ -6,6 +6,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "../../include/sparsekv.h"
 
 #define SKV_EXPORT extern "C" __attribute__((visibility("default")))
@@ -31,6 +34,65 @@ inline int sm_count() {
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
   return n;
+}
+
+// Host-side set-up that belongs to a device (a kernel's shared-memory limit,
+// an occupancy figure) is done once per device and cached here: `slot` is a
+// call site's own zero-initialised table holding value + 1 (0: not yet
+// computed).  `compute` returns the value (>= 0), or -1 on failure, which is
+// not cached.  Safe to call from several host threads: two of them may both
+// compute the value the first time, which the set-up calls used here allow.
+constexpr int kMaxDevices = 64;
+template <typename F>
+inline int once_per_device(std::atomic<int> (&slot)[kMaxDevices], F&& compute) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return compute();
+  }
+  const int v = slot[dev].load(std::memory_order_acquire);
+  if (v > 0) return v - 1;
+  const int r = compute();
+  if (r >= 0) slot[dev].store(r + 1, std::memory_order_release);
+  return r;
+}
+
+// Raises `kernel`'s dynamic shared-memory limit to `bytes` on the current
+// device, once per device and call site; SKV_OK or SKV_ECUDA.
+template <typename K>
+inline int smem_limit_once(std::atomic<int> (&slot)[kMaxDevices], K kernel, size_t bytes) {
+  const int r = once_per_device(slot, [&]() -> int {
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes)) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return -1;
+    }
+    return 0;
+  });
+  return r < 0 ? SKV_ECUDA : SKV_OK;
+}
+
+// Raises `kernel`'s dynamic shared-memory limit on the current device to at
+// least `bytes` (the limit only grows; per device and call site, under a
+// lock so that a concurrent call never lowers it).  SKV_OK or SKV_ECUDA.
+template <typename K>
+inline int smem_limit_at_least(std::atomic<int> (&slot)[kMaxDevices], std::mutex& mu, K kernel, size_t bytes) {
+  if (bytes <= 48 * 1024) return SKV_OK;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return SKV_ECUDA;
+  }
+  if (static_cast<size_t>(slot[dev].load(std::memory_order_acquire)) >= bytes) return SKV_OK;
+  std::lock_guard<std::mutex> lock(mu);
+  if (static_cast<size_t>(slot[dev].load(std::memory_order_relaxed)) >= bytes) return SKV_OK;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes)) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return SKV_ECUDA;
+  }
+  slot[dev].store(static_cast<int>(bytes), std::memory_order_release);
+  return SKV_OK;
 }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

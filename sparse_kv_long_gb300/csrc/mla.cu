@@ -566,12 +566,22 @@ __global__ __launch_bounds__(128) void mla_merge_kernel(const float* __restrict_
       make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
 }
 
+// Row splits per request: as many CTA pairs per request as one wave holds.
+// A request of more than one 64-row chunk always gets at least two splits,
+// merged inside one 4-CTA cluster when there are exactly two: a single split
+// streaming several chunks through one CTA pair (and writing the normalised
+// output itself) is never launched.  That shape has never been run on a GPU,
+// and a variant of this kernel with two softmax threads per head stalled on
+// it; with 39 or more requests on 152 SMs the two-split clusters simply take
+// more than one wave.
 int mla_splits(int B, int max_rows) {
   const int clusters = sm_count() / 2;
   int ns = B > 0 ? clusters / B : 1;
   const int chunks = (max_rows + kNr - 1) / kNr;
   if (ns > chunks) ns = chunks;
-  return ns < 1 ? 1 : ns;
+  if (ns < 1) ns = 1;
+  if (ns == 1 && chunks > 1) ns = 2;
+  return ns;
 }
 
 }  // namespace
@@ -603,14 +613,8 @@ SKV_EXPORT int skv_sparse_attend_mla(int B, int Hq, int d, int dv, const uint16_
     if (!workspace || !aligned16(workspace) || workspace_bytes < skv_mla_workspace_size(B, max_rows))
       return SKV_ENOMEM;
   }
-  static bool configured = false;
-  if (!configured) {
-    if (cudaFuncSetAttribute(mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess) {
-      cudaGetLastError();
-      return SKV_EUNSUPPORTED;
-    }
-    configured = true;
-  }
+  static std::atomic<int> configured[kMaxDevices];
+  if (smem_limit_once(configured, mla_kernel, kSmem) != SKV_OK) return SKV_EUNSUPPORTED;
   float* ws = static_cast<float*>(workspace);
   const bool cmerge = ns == 2;  // the two splits of a request merge inside one 4-CTA cluster
   MlaArgs a{q, kv_pool, row_scale, req_row_stride, n_pool_rows, rows, max_rows, count,

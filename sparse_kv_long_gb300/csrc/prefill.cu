@@ -611,15 +611,8 @@ SKV_EXPORT int skv_prefill_index_scores(int nq, const uint16_t* q_idx, const uin
   const int64_t gx = (nq + kQT - 1) / kQT;
   if (gy > 65535 || gx > 2147483647) return SKV_EUNSUPPORTED;
   constexpr size_t smem = (static_cast<size_t>(kQT) + 2 * kBT) * kPitch * sizeof(uint16_t);
-  static bool configured = false;
-  if (!configured) {
-    if (cudaFuncSetAttribute(prefill_scores_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess) {
-      cudaGetLastError();
-      return SKV_ECUDA;
-    }
-    configured = true;
-  }
+  static std::atomic<int> configured[kMaxDevices];
+  if (smem_limit_once(configured, prefill_scores_kernel, smem) != SKV_OK) return SKV_ECUDA;
   prefill_scores_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), kScoreThreads, smem,
                           as_stream(stream)>>>(q_idx, nq, pooled, n_blocks, order_keys, key_stride, dev_status);
   return launch_status();

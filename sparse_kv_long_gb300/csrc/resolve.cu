@@ -739,15 +739,9 @@ SKV_EXPORT int skv_resolve_rows_clock(int B, int64_t t_cap, const int32_t* lengt
   int32_t* ws_tok = static_cast<int32_t*>(workspace);
   int32_t* ws_row = ws_tok + static_cast<size_t>(B) * max_rows;
   const size_t smem = clock_smem_bytes(Hs, max_rows);
-  static size_t configured = 0;
-  if (smem > 48 * 1024 && smem > configured) {
-    if (cudaFuncSetAttribute(clock_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
-        cudaSuccess) {
-      cudaGetLastError();
-      return SKV_EUNSUPPORTED;
-    }
-    configured = smem;
-  }
+  static std::atomic<int> configured[kMaxDevices];
+  static std::mutex configured_mu;
+  if (smem_limit_at_least(configured, configured_mu, clock_kernel, smem) != SKV_OK) return SKV_EUNSUPPORTED;
   ClockArgs a{t_cap, lengths, S, W, Hkv, d, Hs, idx, max_rows, count, step, slot_token, ref, use_step,
               token_slot, hand, host_rows, k8, v8, reinterpret_cast<__half*>(k_scale),
               reinterpret_cast<__half*>(v_scale), req_row_stride, rows_out, n_miss, ws_tok, ws_row, dev_status};
@@ -786,15 +780,9 @@ int lru_resolve(int B, int64_t t_cap, const int32_t* lengths, int page, const in
   int32_t* ws_tok = static_cast<int32_t*>(workspace);
   int32_t* ws_row = ws_tok + static_cast<size_t>(B) * max_rows;
   const size_t smem = lru_smem_bytes(n_slots, max_rows);
-  static size_t configured = 0;
-  if (smem > 48 * 1024 && smem > configured) {
-    if (cudaFuncSetAttribute(lru_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
-        cudaSuccess) {
-      cudaGetLastError();
-      return SKV_EUNSUPPORTED;
-    }
-    configured = smem;
-  }
+  static std::atomic<int> configured[kMaxDevices];
+  static std::mutex configured_mu;
+  if (smem_limit_at_least(configured, configured_mu, lru_kernel, smem) != SKV_OK) return SKV_EUNSUPPORTED;
   LruArgs a{t_cap, lengths, page, block_table, n_pages, hot_base, hot_stride, n_slots, step, stamp, slot_token,
             token_slot, order, host, pool, row_bytes, n_pool_rows, idx, max_rows, count, rows_out, n_miss, ws_tok,
             ws_row, dev_status, hot_blocks, (n_slots + page - 1) / page};

@@ -50,34 +50,34 @@ constexpr size_t kKeyBudget = 96 * 1024;         // shared memory for the chunk'
 constexpr uint32_t kInt4Base = 0x80000000u - (1u << 20);  // order key of score -2^20
 constexpr int kWin = 1024;                                 // bins read back per window (int4 first pass)
 
+// Scratch of one request, at a fixed stride whatever B is, so that one
+// zero-filled workspace serves calls with any number of requests: the words
+// that must start at zero (barrier counters, the range word, histograms) are
+// returned to zero by the request's last CTA, and the per-CTA records are
+// written before they are read.
+//   bar   [2]              arrivals (monotonic within a launch), exits
+//   rng   [2]              highest occupied first-pass bin + 1, pad
+//   hist  [2][kBins]       non-final passes
+//   fhist [kLastBins]      final pass, request-wide bins
+//   fin   [kCMax][kFin]    final pass, per-CTA suffix counts
+constexpr size_t kReqWords = 4 + 2ull * kBins + kLastBins + static_cast<size_t>(kCMax) * kFin;
+static_assert(kReqWords % 4 == 0, "request blocks stay 16-byte aligned");
+
 struct Ws {
-  unsigned* bar;    // [B][2]: arrivals (monotonic within a launch), exits
-  unsigned* rng;    // [B][2]: highest occupied first-pass bin + 1
-  unsigned* hist;   // [2][B][kBins]: non-final passes
-  int* fin;         // [B][kCMax][kFin]: final pass, per CTA suffix counts
-  unsigned* fhist;  // [B][kLastBins]: final pass, request-wide bins
+  unsigned* base;
+  __device__ __forceinline__ unsigned* req(int b) const { return base + static_cast<size_t>(b) * kReqWords; }
+  __device__ __forceinline__ unsigned* bar(int b) const { return req(b); }
+  __device__ __forceinline__ unsigned* rng(int b) const { return req(b) + 2; }
+  __device__ __forceinline__ unsigned* hist(int pass, int b) const { return req(b) + 4 + static_cast<size_t>(pass) * kBins; }
+  __device__ __forceinline__ unsigned* fhist(int b) const { return req(b) + 4 + 2 * kBins; }
+  __device__ __forceinline__ int* fin(int b, int c) const {
+    return reinterpret_cast<int*>(req(b) + 4 + 2 * kBins + kLastBins) + static_cast<size_t>(c) * kFin;
+  }
 };
 
-size_t ws_bytes(int B) {
-  const size_t words = 2ull * B + 2ull * B + 2ull * B * kBins + static_cast<size_t>(B) * kCMax * kFin +
-                       static_cast<size_t>(B) * kLastBins;
-  return (words * 4 + 255) / 256 * 256;
-}
+size_t ws_bytes(int B) { return (kReqWords * 4 * static_cast<size_t>(B) + 255) / 256 * 256; }
 
-Ws ws_carve(void* base, int B) {
-  Ws w;
-  unsigned* p = static_cast<unsigned*>(base);
-  w.bar = p;
-  p += 2ull * B;
-  w.rng = p;
-  p += 2ull * B;
-  w.hist = p;
-  p += 2ull * B * kBins;
-  w.fin = reinterpret_cast<int*>(p);
-  p += static_cast<size_t>(B) * kCMax * kFin;
-  w.fhist = p;
-  return w;
-}
+Ws ws_carve(void* base, int) { return Ws{static_cast<unsigned*>(base)}; }
 
 // Optional per-step preparation done inside the launch (skv_decode_select):
 // every CTA folds its request's query into int8 itself (same arithmetic as
@@ -308,7 +308,7 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
   if (T < 0) T = 0;
   int32_t* out = a.idx + static_cast<int64_t>(b) * a.max_rows;
   const bool prepared = MODE == SKV_SCORE_SKETCH_INT4 && a.prep.q != nullptr;
-  unsigned* arrive = w.bar + 2 * b;
+  unsigned* arrive = w.bar(b);
   unsigned nbar = 0;
   if (prepared)  // before the dense shortcut: the append and q8 happen either way
     prepare_in_cta(a.prep, b, c, a.n_cap, T, a.S, a.W, reinterpret_cast<float*>(hist), s_q8, s_red, a.status);
@@ -396,7 +396,7 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
       }
       __syncthreads();
     }
-    unsigned* gh = w.hist + (static_cast<size_t>(pass) * a.B + b) * kBins;
+    unsigned* gh = w.hist(pass, b);
     // First pass: the request's highest occupied bin is published too, so that
     // only a window of bins below it has to be read back.
     const bool windowed = pass == 0;
@@ -411,12 +411,12 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
       for (int o = 16; o > 0; o >>= 1) top_local = max(top_local, __shfl_xor_sync(0xffffffffu, top_local, o));
       if (lane == 0 && top_local) atomicMax(&s_top, top_local);
       __syncthreads();
-      if (threadIdx.x == 0 && s_top) atomicMax(&w.rng[2 * b], s_top);  // bin + 1 (0: none)
+      if (threadIdx.x == 0 && s_top) atomicMax(w.rng(b), s_top);  // bin + 1 (0: none)
     }
     req_barrier(arrive, ++nbar * C, a.status);
     if (windowed) {
       // Windows of kWin bins from the top down until `need` keys are covered.
-      const unsigned gtop = __ldcg(&w.rng[2 * b]);
+      const unsigned gtop = __ldcg(w.rng(b));
       int hi = static_cast<int>(gtop) - 1;  // highest occupied bin
       unsigned need_rem = need, above_acc = 0u;
       uint32_t dig = 0u, abv = 0u;
@@ -502,8 +502,8 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
   for (int o = 16; o > 0; o >>= 1) above_local += __shfl_xor_sync(0xffffffffu, above_local, o);
   if (lane == 0 && above_local) atomicAdd(&s_above, above_local);
   __syncthreads();
-  unsigned* gf = w.fhist + static_cast<size_t>(b) * kLastBins;
-  int* myfin = w.fin + (static_cast<size_t>(b) * kCMax + c) * kFin;
+  unsigned* gf = w.fhist(b);
+  int* myfin = w.fin(b, c);
   for (int i = threadIdx.x; i < nbf; i += blockDim.x)
     if (hist[i]) atomicAdd(&gf[i], hist[i]);
   if (warp == 0) {  // lane l owns bins [8l, 8l + 8); suffix sums from the top
@@ -538,7 +538,7 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
   // keys of the chunks before this one: above K*, and equal to K*
   int gb = 0, eb = 0;
   for (int cc = threadIdx.x; cc < c; cc += blockDim.x) {
-    const int* rf = w.fin + (static_cast<size_t>(b) * kCMax + cc) * kFin;
+    const int* rf = w.fin(b, cc);
     const int above_d = __ldcg(&rf[dstar + 1]);
     gb += above_d;
     eb += __ldcg(&rf[dstar]) - above_d;
@@ -561,19 +561,19 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
-    s_last = atomicAdd(&w.bar[2 * b + 1], 1u) == static_cast<unsigned>(C - 1);
+    s_last = atomicAdd(w.bar(b) + 1, 1u) == static_cast<unsigned>(C - 1);
   }
   __syncthreads();
   if (s_last) {
     __threadfence();
     for (int p = 0; p < pass; p++)
-      for (int i = threadIdx.x; i < kBins; i += blockDim.x) w.hist[(static_cast<size_t>(p) * a.B + b) * kBins + i] = 0u;
-    for (int i = threadIdx.x; i < kLastBins; i += blockDim.x) w.fhist[static_cast<size_t>(b) * kLastBins + i] = 0u;
+      for (int i = threadIdx.x; i < kBins; i += blockDim.x) w.hist(p, b)[i] = 0u;
+    for (int i = threadIdx.x; i < kLastBins; i += blockDim.x) w.fhist(b)[i] = 0u;
     if (threadIdx.x == 0) {
-      w.rng[2 * b] = 0u;
-      w.rng[2 * b + 1] = 0u;
-      w.bar[2 * b] = 0u;
-      w.bar[2 * b + 1] = 0u;
+      w.rng(b)[0] = 0u;
+      w.rng(b)[1] = 0u;
+      w.bar(b)[0] = 0u;
+      w.bar(b)[1] = 0u;
     }
   }
 
@@ -645,15 +645,8 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
 template <int MODE, int LPT>
 int launch(const Args& a, Ws w, cudaStream_t st) {
   auto kernel = score_select_kernel<MODE, LPT>;
-  static bool configured = false;
-  if (!configured) {
-    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kKeyBudget)) !=
-        cudaSuccess) {
-      cudaGetLastError();
-      return SKV_ECUDA;
-    }
-    configured = true;
-  }
+  static std::atomic<int> configured[kMaxDevices];
+  if (smem_limit_once(configured, kernel, kKeyBudget) != SKV_OK) return SKV_ECUDA;
   // Largest grid whose CTAs are all resident at once (two per SM if they fit).
   int C = 0;
   size_t smem = 0;

@@ -29,34 +29,31 @@ constexpr int kCTMax = 64;
 constexpr int kUnroll = 8;         // keys per thread whose loads are in flight together
 constexpr int kFlagWords = 1024;   // write pass: bits marking 32-key groups that hold a pick candidate
 
+// Scratch of one request, at a fixed stride whatever B is, so that one
+// zero-filled workspace serves calls with any number of requests: the words
+// that must start at zero (histograms, tickets, todo) are returned to zero by
+// every call, and the rest is written before it is read.
+//   hist   [3][kBins]  digit histograms of the three passes
+//   done   [3]         per-pass tickets
+//   todo   [1]         the request still needs the radix passes (many-request path)
+//   state  [4]         prefix, mask, need, pad
+//   cgt, ceq [kCTMax]  per-chunk counts of keys above / equal to K*
+constexpr size_t kReqWords = 3ull * kBins + 4 + 4 + 2ull * kCTMax;
+
 struct Ws {
-  uint32_t* hist;   // [3][B][kBins]
-  uint32_t* done;   // [3][B]
-  uint32_t* state;  // [B][4]: prefix, mask, need, pad
-  int32_t* cgt;     // [B][kCTMax]
-  int32_t* ceq;     // [B][kCTMax]
-  int32_t* todo;    // [B]: the request still needs the radix passes (many-request path)
+  uint32_t* base;
+  __device__ __forceinline__ uint32_t* req(int b) const { return base + static_cast<size_t>(b) * kReqWords; }
+  __device__ __forceinline__ uint32_t* hist(int pass, int b) const { return req(b) + static_cast<size_t>(pass) * kBins; }
+  __device__ __forceinline__ uint32_t* done(int pass, int b) const { return req(b) + 3 * kBins + pass; }
+  __device__ __forceinline__ int32_t* todo(int b) const { return reinterpret_cast<int32_t*>(req(b) + 3 * kBins + 3); }
+  __device__ __forceinline__ uint32_t* state(int b) const { return req(b) + 3 * kBins + 4; }
+  __device__ __forceinline__ int32_t* cgt(int b) const { return reinterpret_cast<int32_t*>(req(b) + 3 * kBins + 8); }
+  __device__ __forceinline__ int32_t* ceq(int b) const { return cgt(b) + kCTMax; }
 };
 
-__host__ __device__ inline size_t ws_bytes(int B) {
-  return sizeof(uint32_t) * (3ull * B * kBins + 3ull * B + 4ull * B) + sizeof(int32_t) * 2ull * B * kCTMax +
-         sizeof(int32_t) * static_cast<size_t>(B);
-}
+__host__ __device__ inline size_t ws_bytes(int B) { return sizeof(uint32_t) * kReqWords * static_cast<size_t>(B); }
 
-inline Ws ws_carve(void* base, int B) {
-  Ws w;
-  uint32_t* p = static_cast<uint32_t*>(base);
-  w.hist = p;
-  p += 3ull * B * kBins;
-  w.done = p;
-  p += 3ull * B;
-  w.state = p;
-  p += 4ull * B;
-  w.cgt = reinterpret_cast<int32_t*>(p);
-  w.ceq = w.cgt + static_cast<size_t>(B) * kCTMax;
-  w.todo = w.ceq + static_cast<size_t>(B) * kCTMax;
-  return w;
-}
+inline Ws ws_carve(void* base, int) { return Ws{static_cast<uint32_t*>(base)}; }
 
 struct Sel {
   const uint32_t* okeys;
@@ -67,7 +64,7 @@ struct Sel {
   int max_rows;
   int32_t* count;
   int32_t* status;
-  const int32_t* todo;  // NULL: every request; else only those with todo[b] != 0
+  int only_todo;  // 0: every request; else only those whose workspace todo word is set
 };
 
 // Candidate range [lo, hi) of request b and whether it takes the dense path.
@@ -108,16 +105,16 @@ __global__ __launch_bounds__(kThreads) void topk_hist_kernel(Sel s, Ws w, int pa
   __shared__ int scan[33];
   __shared__ int last;
   const int b = blockIdx.y, c = blockIdx.x;
-  if (s.todo && !s.todo[b]) return;
+  if (s.only_todo && !*w.todo(b)) return;
   int64_t T, lo, hi;
   if (request_range(s, b, &T, &lo, &hi)) return;  // dense: nothing to select
   int shift, nbins;
   pass_digits(pass, &shift, &nbins);
   uint32_t prefix = 0, mask = 0, need = static_cast<uint32_t>(s.k);
   if (pass > 0) {
-    prefix = w.state[4 * b];
-    mask = w.state[4 * b + 1];
-    need = w.state[4 * b + 2];
+    prefix = w.state(b)[0];
+    mask = w.state(b)[1];
+    need = w.state(b)[2];
   }
   for (int i = threadIdx.x; i < nbins; i += blockDim.x) h[i] = 0;
   __syncthreads();
@@ -145,12 +142,12 @@ __global__ __launch_bounds__(kThreads) void topk_hist_kernel(Sel s, Ws w, int pa
     }
   }
   __syncthreads();
-  uint32_t* gh = w.hist + (static_cast<size_t>(pass) * s.B + b) * kBins;
+  uint32_t* gh = w.hist(pass, b);
   for (int i = threadIdx.x; i < nbins; i += blockDim.x)
     if (h[i]) atomicAdd(&gh[i], h[i]);
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) last = (atomicAdd(&w.done[pass * s.B + b], 1u) == static_cast<unsigned>(s.CT - 1));
+  if (threadIdx.x == 0) last = (atomicAdd(w.done(pass, b), 1u) == static_cast<unsigned>(s.CT - 1));
   __syncthreads();
   if (!last) return;
   __threadfence();
@@ -172,22 +169,22 @@ __global__ __launch_bounds__(kThreads) void topk_hist_kernel(Sel s, Ws w, int pa
     const int bin = top - j;
     const int cnt = static_cast<int>(h[bin]);
     if (static_cast<uint32_t>(above) < need && static_cast<uint32_t>(above + cnt) >= need) {
-      w.state[4 * b] = prefix | (static_cast<uint32_t>(bin) << shift);
-      w.state[4 * b + 1] = mask | (static_cast<uint32_t>(nbins - 1) << shift);
-      w.state[4 * b + 2] = need - static_cast<uint32_t>(above);
+      w.state(b)[0] = prefix | (static_cast<uint32_t>(bin) << shift);
+      w.state(b)[1] = mask | (static_cast<uint32_t>(nbins - 1) << shift);
+      w.state(b)[2] = need - static_cast<uint32_t>(above);
     }
     above += cnt;
   }
-  if (threadIdx.x == 0) w.done[pass * s.B + b] = 0;
+  if (threadIdx.x == 0) *w.done(pass, b) = 0;
 }
 
 __global__ __launch_bounds__(kThreads) void topk_count_kernel(Sel s, Ws w) {
   __shared__ int red[2][32];
   const int b = blockIdx.y, c = blockIdx.x;
-  if (s.todo && !s.todo[b]) return;
+  if (s.only_todo && !*w.todo(b)) return;
   int64_t T, lo, hi;
   if (request_range(s, b, &T, &lo, &hi)) return;
-  const uint32_t kstar = w.state[4 * b];
+  const uint32_t kstar = w.state(b)[0];
   int64_t c0, c1;
   chunk_of(lo, hi, s.CT, c, &c0, &c1);
   const uint32_t* ok = s.okeys + static_cast<int64_t>(b) * s.n_cap;
@@ -223,8 +220,8 @@ __global__ __launch_bounds__(kThreads) void topk_count_kernel(Sel s, Ws w) {
       g += red[0][i];
       e += red[1][i];
     }
-    w.cgt[b * kCTMax + c] = g;
-    w.ceq[b * kCTMax + c] = e;
+    w.cgt(b)[c] = g;
+    w.ceq(b)[c] = e;
   }
 }
 
@@ -240,7 +237,7 @@ __global__ __launch_bounds__(kThreads) void topk_write_kernel(Sel s, Ws w) {
   __shared__ unsigned flags[kFlagWords];
   const int b = blockIdx.y, c = blockIdx.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (s.todo && !s.todo[b]) return;
+  if (s.only_todo && !*w.todo(b)) return;
   int64_t T, lo, hi;
   const bool dense = request_range(s, b, &T, &lo, &hi);
   int32_t* out = s.idx + static_cast<int64_t>(b) * s.max_rows;
@@ -251,13 +248,13 @@ __global__ __launch_bounds__(kThreads) void topk_write_kernel(Sel s, Ws w) {
     if (c == 0 && threadIdx.x == 0) s.count[b] = static_cast<int32_t>(T);
     return;
   }
-  const uint32_t kstar = w.state[4 * b];
-  const int need = static_cast<int>(w.state[4 * b + 2]);
+  const uint32_t kstar = w.state(b)[0];
+  const int need = static_cast<int>(w.state(b)[2]);
   if (threadIdx.x < 32) {
     int g = 0, e = 0;
     for (int i = threadIdx.x; i < c; i += 32) {
-      g += w.cgt[b * kCTMax + i];
-      e += w.ceq[b * kCTMax + i];
+      g += w.cgt(b)[i];
+      e += w.ceq(b)[i];
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -426,7 +423,7 @@ __global__ __launch_bounds__(kThreads) void topk_filter_kernel(Sel s, Ws w) {
     for (int64_t i = threadIdx.x; i < T; i += blockDim.x) out[i] = static_cast<int32_t>(i);
     if (threadIdx.x == 0) {
       s.count[b] = static_cast<int32_t>(T);
-      w.todo[b] = 0;
+      *w.todo(b) = 0;
     }
     return;
   }
@@ -470,7 +467,7 @@ __global__ __launch_bounds__(kThreads) void topk_filter_kernel(Sel s, Ws w) {
   __syncthreads();
   const unsigned total = s_cnt;
   if (total < static_cast<unsigned>(s.k) || total > static_cast<unsigned>(kCand)) {  // the same in every thread
-    if (threadIdx.x == 0) w.todo[b] = 1;
+    if (threadIdx.x == 0) *w.todo(b) = 1;
     return;
   }
   int N = 1;
@@ -500,7 +497,7 @@ __global__ __launch_bounds__(kThreads) void topk_filter_kernel(Sel s, Ws w) {
     for (int i = threadIdx.x; i < rem; i += blockDim.x) out[s.ratio * s.k + i] = static_cast<int32_t>(nb * s.ratio + i);
     if (threadIdx.x == 0) s.count[b] = s.ratio * s.k + rem;
   }
-  if (threadIdx.x == 0) w.todo[b] = 0;
+  if (threadIdx.x == 0) *w.todo(b) = 0;
 }
 
 }  // namespace
@@ -525,23 +522,16 @@ SKV_EXPORT int skv_topk_select(int B, const uint32_t* order_keys, int64_t n_cap,
   if (reinterpret_cast<uintptr_t>(workspace) & 15) return SKV_EINVAL;
   int CT = (2 * sm_count() + B - 1) / B;
   CT = CT < 1 ? 1 : (CT > kCTMax ? kCTMax : CT);
-  Sel s{order_keys, n_cap, lengths, k, S, W, ratio, CT, B, idx, max_rows, count, dev_status, nullptr};
+  Sel s{order_keys, n_cap, lengths, k, S, W, ratio, CT, B, idx, max_rows, count, dev_status, 0};
   Ws w = ws_carve(workspace, B);
   cudaStream_t st = as_stream(stream);
   dim3 grid(CT, B);
   if (CT == 1 && k <= kMaxFilterK) {  // one CTA per request: threshold filter, radix passes for the rest
     constexpr size_t smem = kCand * sizeof(unsigned long long);
-    static bool configured = false;
-    if (!configured) {
-      if (cudaFuncSetAttribute(topk_filter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(smem)) != cudaSuccess) {
-        cudaGetLastError();
-        return SKV_ECUDA;
-      }
-      configured = true;
-    }
+    static std::atomic<int> configured[kMaxDevices];
+    if (smem_limit_once(configured, topk_filter_kernel, smem) != SKV_OK) return SKV_ECUDA;
     topk_filter_kernel<<<B, kThreads, smem, st>>>(s, w);
-    s.todo = w.todo;
+    s.only_todo = 1;
   }
   for (int pass = 0; pass < 3; pass++) topk_hist_kernel<<<grid, kThreads, 0, st>>>(s, w, pass);
   topk_count_kernel<<<grid, kThreads, 0, st>>>(s, w);
@@ -565,13 +555,10 @@ namespace skv {
 namespace {
 
 constexpr int kNoAllocMaxB = 32;
-constexpr size_t kNoAllocBytes = sizeof(uint32_t) * (3ull * kNoAllocMaxB * kBins + 3ull * kNoAllocMaxB +
-                                                     4ull * kNoAllocMaxB) +
-                                 sizeof(int32_t) * 2ull * kNoAllocMaxB * kCTMax + sizeof(int32_t) * kNoAllocMaxB;
+constexpr size_t kNoAllocBytes = sizeof(uint32_t) * kReqWords * kNoAllocMaxB;
 
 static __device__ __align__(256) unsigned char g_topk_scratch[kNoAllocBytes];
 
-constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
 
@@ -618,16 +605,17 @@ SKV_EXPORT int skv_topk_select_noalloc(int B, const uint32_t* order_keys, int64_
   const int rc = scratch_address(&scratch);
   if (rc != SKV_OK) return rc;
   cudaStream_t st = as_stream(stream);
-  // The array keeps whatever the previous call left; the histograms and
-  // tickets must start at zero, so clear them (no allocation involved).
-  const size_t zero_bytes = sizeof(uint32_t) * (3ull * B * kBins + 3ull * B);
+  // The array keeps whatever the previous call left; the histograms, tickets
+  // and todo words must start at zero, so the call's per-request blocks are
+  // cleared (no allocation involved).
+  const size_t zero_bytes = ws_bytes(B);
   if (cudaMemsetAsync(scratch, 0, zero_bytes, st) != cudaSuccess) {
     cudaGetLastError();
     return SKV_ECUDA;
   }
   int CT = (2 * sm_count() + B - 1) / B;
   CT = CT < 1 ? 1 : (CT > kCTMax ? kCTMax : CT);
-  Sel s{order_keys, n_cap, lengths, k, S, W, ratio, CT, B, idx, max_rows, count, dev_status, nullptr};
+  Sel s{order_keys, n_cap, lengths, k, S, W, ratio, CT, B, idx, max_rows, count, dev_status, 0};
   Ws w = ws_carve(scratch, B);
   dim3 grid(CT, B);
   for (int pass = 0; pass < 3; pass++) topk_hist_kernel<<<grid, kThreads, 0, st>>>(s, w, pass);

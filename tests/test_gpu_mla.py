@@ -68,6 +68,29 @@ def test_mla_matches_oracle(skv, orc, B, counts, max_rows, scaled):
             assert (got[b] == 0).all()
 
 
+def test_mla_many_requests_take_two_split_clusters(skv, orc):
+    """40 requests of up to 256 rows on 152 SMs: one CTA pair per request
+    would fit in a wave, but a request of more than one 64-row chunk is never
+    run as a single split; it takes two splits merged inside a 4-CTA cluster,
+    and the 40 clusters run in more than one wave."""
+    B, max_rows, n_pool = 40, 256, 6000
+    counts = [256] * 36 + [65, 130, 0, 200]
+    x = wl.mla_inputs_cpu(B, n_pool, seed=40)
+    rng = np.random.default_rng(4040)
+    rows = np.full((B, max_rows), -1, np.int32)
+    for b, c in enumerate(counts):
+        rows[b, :c] = np.sort(rng.choice(n_pool, size=c, replace=False))
+    count = np.array(counts, np.int32)
+    scale = 1.0 / math.sqrt(D)
+    assert skv.mla_workspace_size(B, max_rows) <= 16  # two splits: merged in the cluster, no partials
+    got, st = run_mla(skv, x["q"], x["pool"], rows, count, scale)
+    assert st == 0
+    ref = orc.attend(orc.KV_FP8, x["q"], x["pool"], x["pool"], rows, count, scale, 1, D, DV, k_pitch=D, v_pitch=D)
+    assert np.isfinite(got).all()
+    assert np.max(np.abs(got - ref)) < ATOL
+    assert (got[38] == 0).all()
+
+
 def test_mla_single_row_gives_v(skv, orc):
     x = wl.mla_inputs_cpu(1, 64, seed=5)
     rows = np.array([[37]], np.int32)

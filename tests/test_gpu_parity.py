@@ -216,8 +216,11 @@ def run_topk(skv, okey, L, k, S=0, W=0, ratio=1):
     st = status_word()
     skv.topk_select(T.dev(okey.view(np.int32)), T.dev(L), k, idx, cnt, ws, S=S, W=W, ratio=ratio, status=st)
     check_status(st)
-    # histograms and tickets (the parts that must start at zero) are left zero-filled
-    assert int(ws[:4 * (3 * B * 2048 + 3 * B)].count_nonzero().item()) == 0
+    # histograms and tickets (the parts that must start at zero) are left
+    # zero-filled: per request, a block of 3 x 2048 bins and 3 tickets at the
+    # start of a fixed 6280-word stride
+    blocks = ws.view(torch.int32).view(B, -1)
+    assert int(blocks[:, :3 * 2048 + 3].count_nonzero().item()) == 0
     return T.host(idx), T.host(cnt)
 
 

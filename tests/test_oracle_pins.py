@@ -564,6 +564,120 @@ def test_clock_capacity_covers_all_tokens(orc):
         assert m == 0
 
 
+def _int4_vector(codes, scale_bits=0x3C00):
+    """One int4 vector in the host-row encoding: codes of dims 2i (low nibble)
+    and 2i+1 (high nibble) in byte i, two's complement, then one fp16 scale
+    per 64-dim group (all groups get `scale_bits`; 0x3C00 is 1.0)."""
+    codes = np.asarray(codes, np.int64)
+    nib = (codes & 15).astype(np.uint8)
+    body = (nib[0::2] | (nib[1::2] << 4)).astype(np.uint8)
+    scales = np.full((codes.size // 64,), scale_bits, np.uint16).view(np.uint8)
+    return np.concatenate([body, scales])
+
+
+def test_clock_resolve_hand_worked(orc):
+    """The CLOCK resolve composed with the host tier, worked by hand.
+    S = 2 sinks, W = 3 tail tokens, Hs = 3 hot slots, Hkv = 2 heads, D = 64.
+    HBM rows of the request: sink t -> t; tail t -> S + t mod W (the ring);
+    pick -> S + W + slot.  Host row of token t: for head h, the K vector then
+    the V vector, 34 bytes each (32 of codes, one fp16 group scale).
+    Vector (t, h, kv) holds code c on even dims and -c on odd dims, scale 1,
+    c = (4t + 2h + kv) mod 15 - 7, so every (head, K/V) of a token differs.
+    Requantised to int8: s8 = fp16(|c| / 127) and the codes are
+    +-127 * sign(c) (|c| / s8 lies within half a step of 127).
+      step 0, T = 10, picks {3, 5}: both miss, take empty slots 0, 1.
+      step 1, T = 11, picks {5, 6}: 5 hits slot 1; 6 takes empty slot 2.
+      step 2, T = 12, picks {2, 4}: the hand clears the ref bits of slots 0,
+        1, 2, then takes slot 0 (token 3 out) for 2 and slot 1 (token 5 out)
+        for 4.
+      step 3, T = 12, picks {3, 6}: 6 hits slot 2 (used this step, skipped by
+        the hand); 3 clears slot 0, slot 1 and takes slot 0 (token 2 out)."""
+    S, W, Hs, Hkv, D = 2, 3, 3, 2, 64
+    rb = orc.int4_row_bytes(D)
+    assert rb == 34
+    n_tok = 12
+
+    def code(t, h, kv):
+        return (4 * t + 2 * h + kv) % 15 - 7
+
+    host = np.zeros((n_tok, Hkv, 2, rb), np.uint8)
+    for t in range(n_tok):
+        for h in range(Hkv):
+            for kv in range(2):
+                c = code(t, h, kv)
+                host[t, h, kv] = _int4_vector(np.tile([c, -c], D // 2))
+
+    def expect_int8(c):
+        s8 = np.float16(np.float32(abs(c)) / np.float32(127))
+        if c:
+            assert 126.5 < abs(c) / float(s8) < 127.5
+        q = np.tile(np.array([127, -127], np.int64) * int(np.sign(c)), D // 2).astype(np.int8)
+        return q, int(s8.view(np.uint16))
+
+    n_rows = S + W + Hs
+    k8 = np.full((n_rows, Hkv, D), 0x11, np.int8)
+    v8 = np.full((n_rows, Hkv, D), 0x22, np.int8)
+    ks = np.full((n_rows, Hkv), 0x1111, np.uint16)
+    vs = np.full((n_rows, Hkv), 0x2222, np.uint16)
+    st = orc.ClockState(Hs, n_tok)
+    steps = [  # T, selection, expected rows, expected misses, slot -> token after the step
+        (10, [0, 1, 3, 5, 7, 8, 9], [0, 1, 5, 6, 3, 4, 2], 2, [3, 5, -1]),
+        (11, [0, 1, 5, 6, 8, 9, 10], [0, 1, 6, 7, 4, 2, 3], 1, [3, 5, 6]),
+        (12, [0, 1, 2, 4, 9, 10, 11], [0, 1, 5, 6, 2, 3, 4], 2, [2, 4, 6]),
+        (12, [0, 1, 3, 6, 9, 10, 11], [0, 1, 5, 7, 2, 3, 4], 1, [3, 4, 6]),
+    ]
+    for step, (T, sel, want_rows, want_m, want_slots) in enumerate(steps):
+        rows, m = st.resolve(T, S, W, np.array(sel, np.int32), step, host, k8, v8, ks, vs, Hkv, D)
+        assert list(rows) == want_rows, step
+        assert m == want_m, step
+        assert list(st.slot_token) == want_slots, step
+        for slot, t in enumerate(want_slots):
+            if t < 0:
+                continue
+            r = S + W + slot
+            for h in range(Hkv):
+                qk, sk = expect_int8(code(t, h, 0))
+                qv, sv = expect_int8(code(t, h, 1))
+                assert np.array_equal(k8[r, h], qk) and ks[r, h] == sk, (step, slot, h)
+                assert np.array_equal(v8[r, h], qv) and vs[r, h] == sv, (step, slot, h)
+        # sink and tail rows are HBM-resident: never written by the resolve
+        assert np.all(k8[:S + W] == 0x11) and np.all(v8[:S + W] == 0x22)
+        assert np.all(ks[:S + W] == 0x1111) and np.all(vs[:S + W] == 0x2222)
+    assert list(st.ref) == [1, 0, 1] and int(st.hand[0]) == 1
+    assert list(st.token_slot[[2, 3, 4, 5, 6]]) == [-1, 0, 1, -1, 2]
+
+
+def test_lru_hand_worked_with_leased_hot_rows(orc):
+    """The LRU resolve with the hot buffer made of rows leased from the pool:
+    hot slot s is pool row hot_rows[s] (here 40, 17, 33), never hot_base + s.
+    Pages of 2 tokens; page 2 (tokens 4, 5) is resident at pool page 9 (rows
+    18, 19), the rest host-only.  Host row of token t: 4 bytes, all t + 100.
+      step 1, picks {0, 3, 5}: 5 resident -> row 19; 0, 3 miss -> slots 0, 1.
+      step 2, picks {3, 6, 7}: 3 hits slot 1 -> row 17; 6 takes slot 2 (empty);
+        7 needs an untouched slot: slot 0 (stamp 1) -> row 40, token 0 out.
+      step 3, picks {0, 4, 7}: 4 resident -> row 18; 7 hits slot 0 -> row 40
+        (stamp 3); 0 misses: the untouched slots, by (stamp, slot), are slot 1
+        (stamp 2) and slot 2 (stamp 2) -> slot 1, token 3 out -> row 17."""
+    st = orc.LruState(3, 8)
+    bt = np.array([-1, -1, 9, -1], np.int32)
+    hot_rows = np.array([40, 17, 33], np.int32)
+    host = np.repeat((np.arange(8) + 100).astype(np.uint8)[:, None], 4, axis=1)
+    pool = np.zeros((64, 4), np.uint8)
+    rows, m = st.resolve([0, 3, 5], 2, bt, 1000, 1, host, pool, 4, hot_rows=hot_rows)
+    assert list(rows) == [40, 17, 19] and m == 2
+    assert np.all(pool[40] == 100) and np.all(pool[17] == 103)
+    rows, m = st.resolve([3, 6, 7], 2, bt, 1000, 2, host, pool, 4, hot_rows=hot_rows)
+    assert list(rows) == [17, 33, 40] and m == 2
+    assert np.all(pool[33] == 106) and np.all(pool[40] == 107) and st.token_slot[0] == -1
+    rows, m = st.resolve([0, 4, 7], 2, bt, 1000, 3, host, pool, 4, hot_rows=hot_rows)
+    assert list(rows) == [17, 18, 40] and m == 1
+    assert np.all(pool[17] == 100) and st.token_slot[3] == -1
+    assert list(st.slot_token) == [7, 0, 6] and list(st.stamp) == [3, 3, 2]
+    # nothing outside the leased rows was written
+    touched = {17, 33, 40}
+    assert all(np.all(pool[r] == 0) for r in range(64) if r not in touched)
+
+
 def test_lru_hand_worked(orc):
     """Pages of 2 tokens, 3 pages; page 0 host-only, pages 1,2 resident at pool
     pages 5,6.  2 hot slots at pool rows 100,101.  Host row of token t is the

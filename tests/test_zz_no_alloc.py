@@ -4,7 +4,8 @@ skv_topk_select_noalloc exists for callers that cannot hand the library any
 scratch memory (an engine that has reserved all device memory for its own KV
 pools, or a decode loop that must not call cudaMalloc).  It keeps its scratch
 in a fixed device array inside the library.  This test calls it through the C
-ABI twice in a row, on different inputs, and checks that each result equals
+ABI several times in a row (4, 3, then the full 32 requests, then 3 again), on
+different inputs, and checks that each result equals
 what skv_topk_select returns with a caller-provided workspace (selections are
 integer results, so equality is exact).  It also checks that a batch larger
 than the fixed capacity is refused before any launch.
@@ -46,6 +47,10 @@ def test_noalloc_matches_workspace_version_on_two_calls(skv):
     cases = [
         dict(lengths=[250_000, 9000, 3136, 40_000], k=2048, S=64, W=1024, ratio=1, alphabet=None),
         dict(lengths=[70_001, 3137, 12_345], k=512, S=0, W=0, ratio=4, alphabet=5),  # heavy ties
+        # the capacity of the fixed array (32 requests), then a smaller call
+        # again: what a larger call left in the array must not leak into it
+        dict(lengths=list(rng.integers(3137, 30_000, 32)), k=1024, S=32, W=256, ratio=1, alphabet=None),
+        dict(lengths=[20_000, 5000, 8191], k=300, S=4, W=8, ratio=1, alphabet=7),
     ]
     for case in cases:
         L = np.array(case["lengths"], np.int32)
