@@ -11,9 +11,11 @@ One step = one decode token for all 8 requests through all 16 layers; per
 layer three launches: the appended token's sketch and int8 K/V rows plus the
 folded int8 query (a1 + a2, one kernel), the int4 score scan fused with the
 radix top-k and the sink/tail union (a3 + a4), and split-K int8 attention
-over the resident rows (a5 is the identity, a6).  The 16-layer step is
-captured in one CUDA graph.  Layer-steps/s = steps/s x 16; tokens/s = steps/s
-x 8.
+over the resident rows (a5 is the identity, a6), all three issued by one
+skv_decode_layer_step call.  The 16 calls of a step are captured in one CUDA
+graph; the end-to-end figure makes the same calls eagerly, with the step's
+inputs and outputs copied between pinned host memory and the device inside
+the timed region.  Layer-steps/s = steps/s x 16; tokens/s = steps/s x 8.
 
 `--impl reference` times the CPU oracle on the machine's host cores instead.
 """
@@ -65,10 +67,22 @@ def measured_traffic(kernel):
     return nbytes if m.hexdigest()[:16] == digest else None
 
 
-def config_dict(l2_note, layers=W_L):
+def step_bytes(layers=W_L):
+    """Algorithmic HBM bytes of one decode step: per layer the sketch rows of
+    every candidate and the selected int8 K/V rows with their scales."""
+    scan = W_B * (W_T - W_S - W_W) * SCAN_BYTES_PER_CAND
+    attn = W_B * MAX_ROWS * W_HKV * ATTN_BYTES_PER_ROW_HEAD
+    return layers * (scan + attn)
+
+
+def config_dict(layers=W_L):
+    """The workload's description; the GPU arm and the reference arm print the same one."""
+    resident = W_B * W_T * (2 * W_HKV * W_D + 4 * W_HKV + W_HKV * W_R // 2) / 1e9
+    l2 = (f"inputs larger than L2: {layers} layers x {resident:.1f} GB resident, "
+          f"{step_bytes(layers) / 1e9:.2f} GB read per step")
     return {"workload": f"sketch_8x250000_{layers}L_int4sketch_int8kv", "batch": W_B, "context": W_T,
             "layers": layers, "q_heads": W_HQ, "kv_heads": W_HKV, "head_dim": W_D, "sketch_rank": W_R,
-            "top_k": W_K, "sinks": W_S, "tail": W_W, "rows_per_request": MAX_ROWS, "l2": l2_note}
+            "top_k": W_K, "sinks": W_S, "tail": W_W, "rows_per_request": MAX_ROWS, "l2": l2}
 
 
 def peaks():
@@ -181,14 +195,16 @@ def run_reference(args):
     s.time_steps(n=args.warmup)
     times = s.time_steps(n=args.steps)
     per = float(np.mean(times))
-    value = 1.0 / (per * W_B)
+    value = 1.0 / (per * W_B)  # a layer-step covers the 8 requests
+    sample = (f"each timed step is one sample: 1 request x 1 layer of the workload at 250,000 tokens "
+              f"(a1..a6 on the CPU oracle), {per * 1e3:.1f} ms on average; layer-steps/s = 1 / "
+              f"(8 x that time), i.e. the sample scaled to the 8 requests of a layer-step")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": per * W_B * W_L * 1e3,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": per * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32+f64",
-            "data": "synthetic", "config": config_dict("cpu"),
+            "data": "synthetic", "config": config_dict(W_L),
             "cpu_baseline": {"kind": "oracle", "cores": s.orc.max_threads(), "value": value, "unit": UNIT,
-                             "sample": "each step: 1 request x 1 layer at 250,000 tokens (a1..a6), "
-                                       "scaled x8 requests per layer-step"},
+                             "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -285,9 +301,22 @@ class SketchWorkloadGPU:
         self.pws = torch.zeros((skv.decode_prepare_workspace_size(B, W_HKV),), dtype=torch.uint8, device=dev)
         self.out = torch.zeros((L, B, W_HQ, W_D), dtype=torch.float32, device=dev)
         self.status = torch.zeros((1,), dtype=torch.int32, device=dev)
+        # one skv_layer_step per layer (the public layer-step call); the
+        # layers run one after the other, so they share one workspace
+        self.args = [skv.layer_step_args(q=self.q[l], new_k=self.newk[l], new_v=self.newv[l], lengths=self.lengths,
+                                         basis=self.U, c=self.c, sketch=self.sk[l], k8=self.k8[l],
+                                         k_scale=self.ks[l], v8=self.v8[l], v_scale=self.vs[l], idx=self.idx,
+                                         count=self.cnt, out=self.out[l], k=W_K, S=W_S, W=W_W,
+                                         softmax_scale=1 / math.sqrt(W_D)) for l in range(L)]
+        self.lws = torch.zeros((skv.decode_layer_step_workspace_size(self.args[0]),), dtype=torch.uint8,
+                               device=dev)
         torch.cuda.synchronize()
 
     KERNELS_PER_LAYER = 3  # a1 + int8 append + a2 fused, a3 + a4 fused, a6
+
+    def layer_step(self, l, stream=None):
+        """One layer through the public C-ABI layer step."""
+        self.skv.decode_layer_step(self.args[l], self.lws, status=self.status, stream=stream)
 
     def layer(self, l, marks=None):
         skv, st = self.skv, self.status
@@ -306,9 +335,9 @@ class SketchWorkloadGPU:
                                  v_scale=self.vs[l], req_row_stride=W_T, status=st)
         ev("attn1")
 
-    def step(self):
+    def step(self, stream=None):
         for l in range(self.L):
-            self.layer(l)
+            self.layer_step(l, stream)
 
 
 def run_gpu(args):
@@ -340,6 +369,8 @@ def run_gpu(args):
     # ---- capture the 16-layer step in one CUDA graph -------------------------------
     with torch.cuda.stream(stream):
         w.step()  # eager warm-up (also sets kernel attributes)
+        for l in range(L):  # the separate calls used for the per-kernel timing below
+            w.layer(l)
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream, capture_error_mode="relaxed"):
@@ -401,10 +432,12 @@ def run_gpu(args):
     hbm_peak, peak_src = peaks()
     scan_gbs = scan_bytes / (scan_us * 1e-6) / 1e9
     attn_gbs = attn_bytes / (attn_us * 1e-6) / 1e9
-    step_bytes = L * (scan_bytes + attn_bytes)
-    step_gbs = step_bytes / (ms_per_step * 1e-3) / 1e9
+    step_gbs = step_bytes(L) / (ms_per_step * 1e-3) / 1e9
 
-    # ---- end to end through the API with host buffers -----------------------------------
+    # ---- end to end through the public API with host buffers ------------------------------
+    # Every step: the step's inputs (queries and the appended token's K/V of
+    # every layer) copied from pinned host memory, one skv_decode_layer_step
+    # call per layer (eager, no graph), the outputs copied back.
     q_host = torch.empty(w.q.shape, dtype=w.q.dtype, pin_memory=True)
     k_host = torch.empty(w.newk.shape, dtype=w.newk.dtype, pin_memory=True)
     v_host = torch.empty(w.newv.shape, dtype=w.newv.dtype, pin_memory=True)
@@ -422,7 +455,7 @@ def run_gpu(args):
             w.q.copy_(q_host, non_blocking=True)
             w.newk.copy_(k_host, non_blocking=True)
             w.newv.copy_(v_host, non_blocking=True)
-            graph.replay()
+            w.step(stream)
             o_host.copy_(w.out, non_blocking=True)
         stream.synchronize()
     e2e_s = (time.perf_counter() - t0) / args.steps
@@ -432,13 +465,11 @@ def run_gpu(args):
 
     if rank != 0:
         return
-    gb = world * (L * (W_B * W_T * (2 * W_HKV * W_D + 4 * W_HKV + W_HKV * W_R // 2))) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int8/int4 storage, int32 scores, fp32 accumulate", "data": "synthetic",
-        "config": config_dict(f"inputs larger than L2: {L} layers x {gb / world / L:.1f} GB resident, "
-                              f"{step_bytes / 1e9:.2f} GB read per step", layers=L),
+        "config": config_dict(L),
         "tokens_per_s": tokens_per_s, "hbm_gbs": step_gbs,
         "parallelism": "replicas only" if world > 1 else "single GPU",
         "kernel_us": {"score_select_int4": scan_us, "sparse_attend_int8": attn_us},
@@ -450,7 +481,9 @@ def run_gpu(args):
         "roofline_attend": {"bound": "hbm", "achieved": attn_gbs, "peak": hbm_peak, "unit": "GB/s",
                             "frac": attn_gbs / hbm_peak, "traffic": measured_traffic("attend"), "bytes_per_launch": attn_bytes,
                             "bytes_rule": f"{ATTN_BYTES_PER_ROW_HEAD} B per row-head x {W_B} x {MAX_ROWS} x {W_HKV}"},
-        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "path": "per step: pinned host -> device copies of the queries and appended K/V, one eager "
+                        "skv_decode_layer_step C-ABI call per layer, device -> host copy of the outputs"},
         "gpu_launches": args.steps * L * SketchWorkloadGPU.KERNELS_PER_LAYER,
         "clocks": clk.summary(), "device_status": status,
     }
@@ -478,6 +511,12 @@ class HostTier:
 
     def close(self):
         self.skv.host_unregister(self.addr)
+
+
+def torch_seed(gen):
+    """A deterministic seed drawn from a torch generator."""
+    import torch
+    return int(torch.randint(0, 2 ** 31 - 1, (1,), generator=gen, device=gen.device).item())
 
 
 def drift_walk(torch, gen, q0, n_steps, eta):
@@ -597,7 +636,11 @@ class HostClockWorkloadGPU:
     sketch, 64 sinks, the 1024-token tail and a 2.5 % hot buffer (6,250 slots)
     under windowed CLOCK; a drifting query gives the hot-buffer misses."""
 
-    KERNELS_PER_LAYER = 7  # prepare, int4 host append (K, V), score+select, CLOCK state + fetch, attention
+    # one skv_decode_layer_step per layer: prepare (with the int4 host append),
+    # score + select, CLOCK state pass + fetch, attention
+    KERNELS_PER_LAYER = 5
+    MISS_BAND = (0.14, 0.16)   # steady-state hot-buffer miss rate the drift is tuned to
+    CAL_WARM, CAL_MEASURE = 64, 16
 
     def __init__(self, torch, skv, wl, dev, layers, n_steps, eta):
         self.torch, self.skv, self.L = torch, skv, layers
@@ -643,13 +686,16 @@ class HostClockWorkloadGPU:
             self.hand.append(torch.zeros((B,), dtype=torch.int32, device=dev))
             self.step_ctr.append(torch.zeros((2,), dtype=torch.int32, device=dev))
         q0 = wl.lowrank_rows_torch(gen, layers * B * W_HQ, self.U).view(layers, B, W_HQ, D)
-        self.q_seq = drift_walk(torch, gen, q0, n_steps, eta)       # [steps][L][B][Hq][D]
-        self.q = torch.empty_like(self.q_seq[0])
+        self.q = torch.empty((layers, B, W_HQ, D), dtype=torch.bfloat16, device=dev)
         self.newk = wl.lowrank_rows_torch(gen, layers * B * Hkv, self.U).view(layers, B, Hkv, D).contiguous()
         self.newv = wl.randn_torch(gen, (layers, B, Hkv, D), device=dev).contiguous()
         # the current token T-1 lives in the tail ring row S + (T-1) mod W and in the host tier
         self.new_rows = (torch.arange(B, device=dev, dtype=torch.int64) * self.R + W_S + (T - 1) % W_W)
         self.new_host = (torch.arange(B, device=dev, dtype=torch.int64) * T + (T - 1))
+        # the separate-call path (per-kernel timing) folds the query with
+        # skv_decode_prepare, whose sketch row is the int8 row: that copy goes
+        # to a scratch buffer and skv_sketch_project writes the real sketch row
+        self.sk_scratch = torch.empty((B * self.R, Hkv * R // 2), dtype=torch.uint8, device=dev)
         self.q8 = torch.empty((B, Hkv * R), dtype=torch.int8, device=dev)
         self.sigma = torch.empty((B,), dtype=torch.float32, device=dev)
         self.idx = torch.zeros((B, MAX_ROWS), dtype=torch.int32, device=dev)
@@ -664,17 +710,81 @@ class HostClockWorkloadGPU:
         self.out = torch.zeros((B, W_HQ, D), dtype=torch.float32, device=dev)
         self.status = torch.zeros((1,), dtype=torch.int32, device=dev)
         self.rb = rb
+        self.args = [skv.layer_step_args(
+            q=self.q[l], new_k=self.newk[l], new_v=self.newv[l], lengths=self.lengths, basis=self.U, c=self.c,
+            sketch=self.sk[l], k8=self.k8[l], k_scale=self.ks[l], v8=self.v8[l], v_scale=self.vs[l], idx=self.idx,
+            count=self.cnt, out=self.out, k=W_K, S=W_S, W=W_W, softmax_scale=1 / math.sqrt(W_D),
+            policy=skv.HOST_CLOCK, Hs=self.Hs, host_rows=self.hosts[l].alias, step=self.step_ctr[l],
+            slot_token=self.tok[l], ref=self.ref[l], use_step=self.use[l], token_slot=self.tslot[l],
+            hand=self.hand[l], n_miss=self.nmiss[l]) for l in range(layers)]
+        self.lws = torch.zeros((skv.decode_layer_step_workspace_size(self.args[0]),), dtype=torch.uint8, device=dev)
         torch.cuda.synchronize()
+        self.eta_calibrated = eta is None
+        if eta is None:
+            eta, self.calibration = self.calibrate_eta(q0[:1].contiguous(), gen)
+        self.eta = eta
+        self.q_seq = drift_walk(torch, gen, q0, n_steps, eta)       # [steps][L][B][Hq][D]
+        torch.cuda.synchronize()
+
+    def _reset_state(self, l):
+        self.tok[l].fill_(-1)
+        self.ref[l].zero_()
+        self.use[l].fill_(-1)
+        self.tslot[l].fill_(-1)
+        self.hand[l].zero_()
+        self.step_ctr[l].zero_()
+
+    def miss_rate(self, q0_l0, eta, seed):
+        """Steady-state miss rate of layer 0 under drift eta: CAL_WARM steps
+        from a cold hot buffer, then the misses of CAL_MEASURE steps."""
+        torch = self.torch
+        g = torch.Generator(device=q0_l0.device)
+        g.manual_seed(seed)
+        seq = drift_walk(torch, g, q0_l0, self.CAL_WARM + self.CAL_MEASURE, eta)  # [steps][1][B][Hq][D]
+        self._reset_state(0)
+        total = torch.zeros((), dtype=torch.int64, device=q0_l0.device)
+        for s in range(self.CAL_WARM + self.CAL_MEASURE):
+            self.q[0].copy_(seq[s][0])
+            self.graph_layer(0)
+            if s >= self.CAL_WARM:
+                total += self.nmiss[0].clamp(min=0).sum()
+        rate = float(total.item()) / (self.CAL_MEASURE * W_K * W_B)
+        self._reset_state(0)
+        return rate
+
+    def calibrate_eta(self, q0_l0, gen, lo=0.0, hi=1.0, iters=14):
+        """Bisection on the query drift eta (the miss rate grows with it) until
+        layer 0's steady-state miss rate lies in MISS_BAND; the same seed for
+        every trial.  Returns eta and the trials (eta, miss rate)."""
+        seed = int(torch_seed(gen))
+        trials = []
+        eta = 0.5 * (lo + hi)
+        for _ in range(iters):
+            eta = 0.5 * (lo + hi)
+            rate = self.miss_rate(q0_l0, eta, seed)
+            trials.append((eta, rate))
+            if rate < self.MISS_BAND[0]:
+                lo = eta
+            elif rate > self.MISS_BAND[1]:
+                hi = eta
+            else:
+                break
+        return eta, trials
 
     def set_step(self, s):
         self.q.copy_(self.q_seq[s % self.q_seq.shape[0]], non_blocking=True)
 
+    def graph_layer(self, l):
+        """One layer through the public C-ABI layer step."""
+        self.skv.decode_layer_step(self.args[l], self.lws, status=self.status)
+
     def layer(self, l, ev):
+        """The same layer as separate calls, for per-kernel timing."""
         skv, st = self.skv, self.status
         ev("prep0")
-        skv.decode_prepare(self.q[l], self.newk[l], self.newv[l], self.U, self.c, self.new_rows,
-                           self.sk[l].view(W_B * W_T, -1), self.k8[l], self.ks[l], self.v8[l], self.vs[l], self.q8,
-                           self.pws, sigma=self.sigma)
+        skv.decode_prepare(self.q[l], self.newk[l], self.newv[l], self.U, self.c, self.new_rows, self.sk_scratch,
+                           self.k8[l], self.ks[l], self.v8[l], self.vs[l], self.q8, self.pws, sigma=self.sigma)
+        skv.sketch_project(self.newk[l], self.U, self.c, self.sk[l].view(W_B * W_T, -1), out_rows=self.new_host)
         skv.quantize_int4_rows(self.newk[l], None, self.tok_bytes, 2 * self.rb, out_rows=self.new_host,
                                out_ptr=self.hosts[l].alias)
         skv.quantize_int4_rows(self.newv[l], None, self.tok_bytes, 2 * self.rb, out_rows=self.new_host,
@@ -706,9 +816,14 @@ class HostClockWorkloadGPU:
             h.close()
 
     def config(self):
+        cal = ({"drift_eta": self.eta, "eta_from": "seeded bisection on layer 0's steady-state miss rate "
+                f"({self.CAL_WARM} warm-up steps, {self.CAL_MEASURE} measured) into "
+                f"[{self.MISS_BAND[0]}, {self.MISS_BAND[1]}]",
+                "eta_trials": [[round(e, 6), round(r, 5)] for e, r in self.calibration]}
+               if self.eta_calibrated else {"drift_eta": self.eta, "eta_from": "--eta"})
         return {"workload": f"host_clock_8x250000_{self.L}L_int4host", "batch": W_B, "context": W_T,
                 "layers": self.L, "q_heads": W_HQ, "kv_heads": W_HKV, "head_dim": W_D, "top_k": W_K, "sinks": W_S,
-                "tail": W_W, "hot_slots": self.Hs, "host_bytes_per_token_layer": self.tok_bytes,
+                "tail": W_W, "hot_slots": self.Hs, "host_bytes_per_token_layer": self.tok_bytes, **cal,
                 "l2": "inputs larger than L2: 256 MB sketch per layer"}
 
 
@@ -1075,7 +1190,10 @@ def run_extra(args):
 
     def step():
         for l in range(w.L):
-            w.layer(l, nolog)
+            if hasattr(w, "graph_layer"):
+                w.graph_layer(l)  # the public layer-step call
+            else:
+                w.layer(l, nolog)
 
     with torch.cuda.stream(stream):
         w.set_step(0)
@@ -1208,7 +1326,8 @@ def main():
     ap.add_argument("--workload", default="sketch",
                     choices=["sketch", "host_clock", "mla_lru", "pooled", "pooled_host", "prefill", "residency"],
                     help="sketch: the headline line; the others print their own line")
-    ap.add_argument("--eta", type=float, default=0.35, help="query drift per step (host_clock)")
+    ap.add_argument("--eta", type=float, default=None, help="query drift per step (host_clock; default: "
+                    "found by bisection so that the steady-state miss rate is 14-16 %%)")
     ap.add_argument("--context", type=int, default=None, help="mla_lru, pooled: tokens per request (default "
                     "142,000 and 1,048,576; "
                     "smaller only for profiler captures)")
@@ -1216,7 +1335,7 @@ def main():
     if args.warmup < 3:
         args.warmup = 3
     if args.layers is None:
-        args.layers = {"sketch": W_L, "host_clock": 4, "mla_lru": 2, "pooled": 12, "pooled_host": 2,
+        args.layers = {"sketch": W_L, "host_clock": W_L, "mla_lru": 2, "pooled": 12, "pooled_host": 2,
                        "prefill": 1, "residency": 1}[args.workload]
     if args.impl == "reference":
         run_reference(args)

@@ -318,6 +318,87 @@ int skv_decode_select(int B, int Hq, int Hkv, int d, int r, const uint16_t *q,
                       int32_t *dev_status, void *stream);
 
 /* ========================================================================== */
+/* One decode step of one attention layer, every step of the path chained on   */
+/* one stream: append the current token, fold the query, score and select,    */
+/* resolve the rows, attend ([P1] "8 agents x 250K context on two 3090s ...",  */
+/* "What shipped": the sparse step is captured as one CUDA-graph family;      */
+/* [P2] "vLLM's Hybrid HiSparse ...", "Three residency states, one block      */
+/* pool": nothing in the step waits on a decision made on the CPU).           */
+/* ========================================================================== */
+/* Residency of the layer's int8 K/V rows (skv_layer_step.policy). */
+#define SKV_RESIDENT 0    /* every token's rows in HBM: request b, token t at row b*n_cap + t */
+#define SKV_HOST_CLOCK 1  /* int4 rows in a host tier; HBM holds per request S sink rows,    */
+                          /* a ring of the last W tokens and Hs hot slots (windowed CLOCK)   */
+
+/*
+ * Arguments of skv_decode_layer_step (all pointers are device pointers;
+ * host_rows is the device alias of the registered host tier).
+ * Shapes: d == 256, r == 64, Hq % Hkv == 0, Hkv*r in {128, 256, 512}, k >= 1,
+ * S >= 0, W >= 1, 1 <= lengths[b] <= n_cap.
+ */
+typedef struct skv_layer_step {
+  int B, Hq, Hkv, d, r;
+  int64_t n_cap;        /* token capacity per request (sketch and host-tier rows)      */
+  int k, S, W;          /* top-k, sinks, recent tail                                   */
+  float softmax_scale;
+  int policy;           /* SKV_RESIDENT or SKV_HOST_CLOCK                              */
+  int Hs;               /* hot slots per request (SKV_HOST_CLOCK; else unused)         */
+  /* frozen per-layer artifacts */
+  const float *basis;   /* fp32 [d][r]                                                 */
+  const float *c;       /* fp32 [Hkv][r] sketch quantiser step                         */
+  /* the layer's caches */
+  uint8_t *sketch;      /* u8 [B][n_cap][Hkv*r/2] int4 key sketch                      */
+  int8_t *k8, *v8;      /* int8 [B*R][Hkv][d], R = n_cap (SKV_RESIDENT) or S + W + Hs  */
+  uint16_t *k_scale, *v_scale;  /* fp16 [B*R][Hkv]                                     */
+  uint8_t *host_rows;   /* SKV_HOST_CLOCK: int4 host tier [B][n_cap][Hkv][2][d/2+d/32] */
+  /* windowed-CLOCK state (SKV_HOST_CLOCK), as skv_resolve_rows_clock */
+  int32_t *step;        /* int32 [2]: decode step, advanced by every call; ticket      */
+  int32_t *slot_token;  /* int32 [B][Hs]  */
+  uint8_t *ref;         /* u8 [B][Hs]     */
+  int32_t *use_step;    /* int32 [B][Hs]  */
+  int32_t *token_slot;  /* int32 [B][n_cap] */
+  int32_t *hand;        /* int32 [B]      */
+  /* per-step inputs */
+  const uint16_t *q;                /* bf16 [B][Hq][d]                                 */
+  const uint16_t *new_k, *new_v;    /* bf16 [B][Hkv][d]: the current token, T - 1       */
+  const int32_t *lengths;           /* int32 [B]: T, the current token included         */
+  /* outputs */
+  int32_t *idx;         /* int32 [B][S+k+W]: the selection, ascending                  */
+  int32_t *count;       /* int32 [B]                                                   */
+  int32_t *n_miss;      /* int32 [B] hot-buffer misses (SKV_HOST_CLOCK), or NULL       */
+  int8_t *q8_out;       /* int8 [B][Hkv*r] copy of the folded query, or NULL           */
+  float *out;           /* fp32 [B][Hq][d] attention output                             */
+} skv_layer_step;
+
+/*
+ * skv_decode_layer_step -- for every request b with T = lengths[b]:
+ *  1. append the current token T - 1: its int4 sketch at sketch row
+ *     b*n_cap + T - 1, its int8 K and V rows (skv_quantize_int8_rows
+ *     encoding) at pool row b*n_cap + T - 1 (SKV_RESIDENT) or at the ring row
+ *     b*(S+W+Hs) + S + (T-1) mod W (SKV_HOST_CLOCK, which also writes the
+ *     token's int4 host row, skv_quantize_int4_rows encoding, at host row
+ *     b*n_cap + T - 1); fold the query into int8 (skv_decode_prepare);
+ *  2. score the candidates through the sketch and select the top k, with the
+ *     sinks and the tail (skv_score_select, SKETCH_INT4; when that does not
+ *     fit one launch, skv_index_score then skv_topk_select);
+ *  3. SKV_HOST_CLOCK: resolve the selection through the hot buffer, fetching
+ *     misses from the host tier (skv_resolve_rows_clock);
+ *  4. attend over the selected int8 rows (skv_sparse_attend_decode).
+ * The result is that of those calls made one after the other.  Every launch
+ * goes to `stream`; the call has no host-side decision that depends on
+ * device data, so a sequence of layer steps can be captured in a CUDA graph.
+ *   workspace  skv_decode_layer_step_workspace_size(a) bytes, zero-filled
+ *              before first use; every call leaves it ready for the next call
+ *              with the same shapes (B, Hq, Hkv, n_cap, k, S, W, policy, Hs).
+ *              Zero-fill it again before using it for other shapes.
+ * Errors: SKV_EINVAL for null pointers, shapes outside the constraints, or a
+ * short workspace (SKV_ENOMEM); the device status bits of the chained calls.
+ */
+size_t skv_decode_layer_step_workspace_size(const skv_layer_step *a);
+int skv_decode_layer_step(const skv_layer_step *a, void *workspace, size_t workspace_bytes,
+                          int32_t *dev_status, void *stream);
+
+/* ========================================================================== */
 /* KV row encoding (write path).                                               */
 /* ========================================================================== */
 /*

@@ -21,10 +21,28 @@ LIB_PATH = os.path.join(_HERE, "libsparsekv.so")
 
 SKETCH_INT4, SKETCH_F32, POOLED_BF16 = 0, 1, 2
 KV_BF16, KV_INT8 = 0, 1
+RESIDENT, HOST_CLOCK = 0, 1
 DEV_NAN, DEV_RANGE, DEV_TIMEOUT, DEV_COUNT = 1, 2, 4, 8
 
 _lock = threading.Lock()
 _lib = None
+
+
+class LayerStep(ctypes.Structure):
+    """The C struct skv_layer_step (include/sparsekv.h), field for field."""
+    _fields_ = [
+        ("B", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int), ("d", ctypes.c_int), ("r", ctypes.c_int),
+        ("n_cap", ctypes.c_int64), ("k", ctypes.c_int), ("S", ctypes.c_int), ("W", ctypes.c_int),
+        ("softmax_scale", ctypes.c_float), ("policy", ctypes.c_int), ("Hs", ctypes.c_int),
+        ("basis", ctypes.c_void_p), ("c", ctypes.c_void_p),
+        ("sketch", ctypes.c_void_p), ("k8", ctypes.c_void_p), ("v8", ctypes.c_void_p),
+        ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p), ("host_rows", ctypes.c_void_p),
+        ("step", ctypes.c_void_p), ("slot_token", ctypes.c_void_p), ("ref", ctypes.c_void_p),
+        ("use_step", ctypes.c_void_p), ("token_slot", ctypes.c_void_p), ("hand", ctypes.c_void_p),
+        ("q", ctypes.c_void_p), ("new_k", ctypes.c_void_p), ("new_v", ctypes.c_void_p), ("lengths", ctypes.c_void_p),
+        ("idx", ctypes.c_void_p), ("count", ctypes.c_void_p), ("n_miss", ctypes.c_void_p), ("q8_out", ctypes.c_void_p),
+        ("out", ctypes.c_void_p),
+    ]
 
 
 class SkvError(RuntimeError):
@@ -62,6 +80,8 @@ def _load():
                 "skv_decode_select": ([i32, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P, P, P, i64, P, i32, i32,
                                        i32, P, i32, P, P, P, sz, P, P], i32),
                 "skv_quantize_int8_rows": ([P, i64, i32, i32, P, P, P, P], i32),
+                "skv_decode_layer_step_workspace_size": ([ctypes.POINTER(LayerStep)], sz),
+                "skv_decode_layer_step": ([ctypes.POINTER(LayerStep), P, sz, P, P], i32),
                 "skv_attend_workspace_size": ([i32, i32, i32, i32, i32], sz),
                 "skv_sparse_attend_decode": ([i32, i32, i32, i32, i32, P, P, P, P, P, i64, i64, P, i32, P,
                                               f32, P, P, sz, P, P], i32),
@@ -170,6 +190,39 @@ def decode_prepare(q, new_k, new_v, basis, c, new_rows, sketch, k8, k_scale, v8,
         _ptr(k8), _ptr(k_scale), _ptr(v8), _ptr(v_scale), _ptr(q8), _ptr(sigma), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
     return q8
+
+
+def layer_step_args(*, q, new_k, new_v, lengths, basis, c, sketch, k8, k_scale, v8, v_scale, idx, count, out, k, S,
+                    W, softmax_scale, policy=RESIDENT, Hs=0, host_rows=None, step=None, slot_token=None, ref=None,
+                    use_step=None, token_slot=None, hand=None, n_miss=None, q8_out=None) -> LayerStep:
+    """Fills the skv_layer_step struct from tensors (host_rows: a device
+    alias, as an int address or anything with data_ptr())."""
+    B, Hq, d = q.shape
+    Hkv, r = new_k.shape[1], basis.shape[1]
+    n_cap = sketch.shape[1]
+
+    def addr(t):
+        if t is None:
+            return None
+        return int(t) if isinstance(t, int) else t.data_ptr()
+
+    return LayerStep(B, Hq, Hkv, d, r, n_cap, k, S, W, float(softmax_scale), policy, Hs, addr(basis), addr(c),
+                     addr(sketch), addr(k8), addr(v8), addr(k_scale), addr(v_scale), addr(host_rows), addr(step),
+                     addr(slot_token), addr(ref), addr(use_step), addr(token_slot), addr(hand), addr(q), addr(new_k),
+                     addr(new_v), addr(lengths), addr(idx), addr(count), addr(n_miss), addr(q8_out), addr(out))
+
+
+def decode_layer_step_workspace_size(args: LayerStep) -> int:
+    return int(_load().skv_decode_layer_step_workspace_size(ctypes.byref(args)))
+
+
+def decode_layer_step(args: LayerStep, workspace, status=None, stream=None):
+    """One decode step of one layer, every step of the path chained on one
+    stream (append, fold, score + select, resolve, attend)."""
+    _check("skv_decode_layer_step", _load().skv_decode_layer_step(
+        ctypes.byref(args), _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(status),
+        _stream(stream)))
+    return args
 
 
 def pool_keys(keys, pooled, first_block, n_blocks, ratio=4, stream=None):

@@ -119,6 +119,71 @@ __device__ __forceinline__ void encode_int8_row_warp(const uint16_t* src, int d,
   encode_row_warp(v, d, dst, scale);
 }
 
+// One warp encodes a row of d (a multiple of 64, <= 512) dims held as in
+// encode_row_warp (lane l: dims l + 32 i) as an int4 host row: per 64-dim
+// group g (values i = 2g, 2g + 1 of every lane) scale = fp16(max|x| / 7),
+// code = clamp(rint(x / scale), -8, 7) (zero or non-finite scale: code 0);
+// bytes [0, d/2): dim 2j in the low nibble of byte j, 2j + 1 in the high
+// nibble; then the d/64 fp16 scales.  dst must be 4-byte aligned.
+__device__ __forceinline__ void encode_int4_row_warp(const float (&v)[16], int d, uint8_t* dst) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int g = 0; g < 8; g++) {
+    if (64 * g >= d) break;  // the same in every lane
+    float m = fmaxf(fabsf(v[2 * g]), fabsf(v[2 * g + 1]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const __half sh = __float2half_rn(__fdiv_rn(m, 7.f));
+    const float sf = __half2float(sh);
+    const bool ok = (sf != 0.f) && isfinite(sf);
+#pragma unroll
+    for (int u = 0; u < 2; u++) {
+      const int i = 2 * g + u;
+      const uint32_t nib = static_cast<uint32_t>(ok ? rint_clamp(__fdiv_rn(v[i], sf), -8, 7) : 0) & 15u;
+      // even lanes form the byte of dims (32 i + lane, + 1), lanes 8j the
+      // word of dims [32 i + 8 j, + 8)
+      const uint32_t byte = nib | (__shfl_down_sync(0xffffffffu, nib, 1) << 4);
+      const uint32_t w = byte | (__shfl_down_sync(0xffffffffu, byte, 2) << 8) |
+                         (__shfl_down_sync(0xffffffffu, byte, 4) << 16) |
+                         (__shfl_down_sync(0xffffffffu, byte, 6) << 24);
+      if ((lane & 7) == 0) *reinterpret_cast<uint32_t*>(dst + 16 * i + lane / 2) = w;
+    }
+    if (lane == 0) *reinterpret_cast<__half*>(dst + d / 2 + 2 * g) = sh;
+  }
+}
+
+// Where the token a decode step appends goes, for request b.  Either explicit
+// rows (`rows`: the int8 row, and the sketch row unless `sketch_rows` is
+// given), or rows derived from the request's length T = lengths[b] (the
+// appended token is T - 1): sketch (and int4 host) row b*n_cap + T - 1, int8
+// row b*kv_stride + T - 1, or b*kv_stride + S + (T - 1) mod W when `ring` is
+// set (HBM keeps S sinks and a ring of the last W tokens in front of the hot
+// slots).  `host4`, when set, receives the token's int4 host row at
+// host4 + (b*n_cap + T - 1) * Hkv*2*rb (head h: K at 2h*rb, V at (2h+1)*rb).
+struct Append {
+  const int64_t* rows;
+  const int64_t* sketch_rows;
+  const int32_t* lengths;
+  int64_t n_cap, kv_stride;
+  int S, W, ring;
+  uint8_t* host4;
+};
+
+// False when the request has no token to append (length <= 0 or beyond the
+// capacity): nothing is written for it.
+__device__ __forceinline__ bool append_rows(const Append& a, int b, int64_t* kv_row, int64_t* sk_row) {
+  if (a.rows) {
+    *kv_row = a.rows[b];
+    *sk_row = a.sketch_rows ? a.sketch_rows[b] : *kv_row;
+    return true;
+  }
+  const int64_t T = a.lengths[b];
+  if (T < 1 || T > a.n_cap) return false;
+  *sk_row = static_cast<int64_t>(b) * a.n_cap + (T - 1);
+  *kv_row = static_cast<int64_t>(b) * a.kv_stride + (a.ring ? a.S + (T - 1) % a.W : T - 1);
+  return true;
+}
+
 // int8 code of a folded query coordinate with the request's scale sigma.
 __device__ __forceinline__ int8_t query_code(float qp, float sigma) {
   return static_cast<int8_t>(sigma != 0.f ? rint_clamp(__fdiv_rn(qp, sigma), -127, 127) : 0);

@@ -642,19 +642,20 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
   }
 }
 
+// CTAs per request of the largest grid whose CTAs are all resident at once
+// (two per SM if they fit), with the shared memory each needs; 0 when B
+// requests do not fit (too many requests, or a chunk too large for on-chip
+// keys).
 template <int MODE, int LPT>
-int launch(const Args& a, Ws w, cudaStream_t st) {
+int plan_grid(int B, int64_t n_cap, size_t* smem) {
   auto kernel = score_select_kernel<MODE, LPT>;
   static std::atomic<int> configured[kMaxDevices];
-  if (smem_limit_once(configured, kernel, kKeyBudget) != SKV_OK) return SKV_ECUDA;
-  // Largest grid whose CTAs are all resident at once (two per SM if they fit).
-  int C = 0;
-  size_t smem = 0;
-  for (int per_sm_try = 2; per_sm_try >= 1 && C == 0; per_sm_try--) {
-    const int c_try = per_sm_try * sm_count() / a.B;
+  if (smem_limit_once(configured, kernel, kKeyBudget) != SKV_OK) return 0;
+  for (int per_sm_try = 2; per_sm_try >= 1; per_sm_try--) {
+    const int c_try = per_sm_try * sm_count() / B;
     if (c_try < 1) continue;
     const int c_use = c_try > kCMax ? kCMax : c_try;
-    const size_t need = static_cast<size_t>((a.n_cap + c_use - 1) / c_use) * sizeof(uint32_t);
+    const size_t need = static_cast<size_t>((n_cap + c_use - 1) / c_use) * sizeof(uint32_t);
     int fit = 0;
     if (need > kKeyBudget ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, kernel, kThreads, need) != cudaSuccess) {
@@ -662,10 +663,18 @@ int launch(const Args& a, Ws w, cudaStream_t st) {
       continue;
     }
     if (fit >= per_sm_try) {
-      C = c_use;
-      smem = need;
+      *smem = need;
+      return c_use;
     }
   }
+  return 0;
+}
+
+template <int MODE, int LPT>
+int launch(const Args& a, Ws w, cudaStream_t st) {
+  auto kernel = score_select_kernel<MODE, LPT>;
+  size_t smem = 0;
+  const int C = plan_grid<MODE, LPT>(a.B, a.n_cap, &smem);
   if (C < 1) return SKV_EUNSUPPORTED;  // too many requests, or a chunk too large for on-chip keys
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(C, a.B, 1);
@@ -685,6 +694,18 @@ int launch(const Args& a, Ws w, cudaStream_t st) {
 }
 
 }  // namespace
+
+// Whether skv_score_select runs as one launch for these shapes (int4 sketch
+// scores of the given width); otherwise it returns SKV_EUNSUPPORTED.
+bool score_select_fits_int4(int width, int B, int64_t n_cap) {
+  size_t smem = 0;
+  if (B < 1) return false;
+  if (width == 128) return plan_grid<SKV_SCORE_SKETCH_INT4, 4>(B, n_cap, &smem) > 0;
+  if (width == 256) return plan_grid<SKV_SCORE_SKETCH_INT4, 8>(B, n_cap, &smem) > 0;
+  if (width == 512) return plan_grid<SKV_SCORE_SKETCH_INT4, 16>(B, n_cap, &smem) > 0;
+  return false;
+}
+
 }  // namespace skv
 
 using namespace skv;

@@ -256,8 +256,8 @@ constexpr int kPrepThreads = 256;
 // request's folded query with one scale.
 __global__ __launch_bounds__(kPrepThreads) void prepare_kernel(
     const uint16_t* __restrict__ q, const uint16_t* __restrict__ newk, const uint16_t* __restrict__ newv, int Hq,
-    int Hkv, int d, const float* __restrict__ basis, const float* __restrict__ c,
-    const int64_t* __restrict__ new_rows, uint8_t* __restrict__ sketch, int8_t* __restrict__ k8,
+    int Hkv, int d, const float* __restrict__ basis, const float* __restrict__ c, const fold::Append ap,
+    uint8_t* __restrict__ sketch, int8_t* __restrict__ k8,
     __half* __restrict__ ks, int8_t* __restrict__ v8, __half* __restrict__ vs, int8_t* __restrict__ q8,
     float* __restrict__ sigma_out, float* __restrict__ qp_ws, unsigned* __restrict__ tickets) {
   __shared__ float QK[2][kMaxD];                          // folded query, new key (head h)
@@ -271,7 +271,8 @@ __global__ __launch_bounds__(kPrepThreads) void prepare_kernel(
   const uint16_t* qb = q + (static_cast<int64_t>(b) * Hq + static_cast<int64_t>(h) * G) * d;
   const uint16_t* kb = newk + (static_cast<int64_t>(b) * Hkv + h) * d;
   // Every load first, so that the first-touch latencies overlap.
-  const int64_t row = new_rows[b];
+  int64_t row = 0, sk_row = 0;
+  const bool app = fold::append_rows(ap, b, &row, &sk_row);
   for (int u = t; u < 2 * (d / 8); u += blockDim.x) {
     const int which = u / (d / 8), piece = u - which * (d / 8);
     const uint16_t* src = (which == 0 ? newk : newv) + (static_cast<int64_t>(b) * Hkv + h) * d + 8 * piece;
@@ -314,15 +315,15 @@ __global__ __launch_bounds__(kPrepThreads) void prepare_kernel(
     qp_ws[static_cast<int64_t>(b) * Hkv * kRank + h * kRank + t] =
         __fmul_rn(fold::combine_slices(&part[0][0][t], 2 * kRank, ns), cj);
   }
-  if (t < kRank / 2) {
+  if (app && t < kRank / 2) {
     const int j0 = 2 * t;
     const int c0 = fold::sketch_code(fold::combine_slices(&part[0][1][j0], 2 * kRank, ns), c[h * kRank + j0]);
     const int c1 = fold::sketch_code(fold::combine_slices(&part[0][1][j0 + 1], 2 * kRank, ns), c[h * kRank + j0 + 1]);
-    sketch[row * (Hkv * kRank / 2) + h * (kRank / 2) + t] = static_cast<uint8_t>((c0 & 15) | ((c1 & 15) << 4));
+    sketch[sk_row * (Hkv * kRank / 2) + h * (kRank / 2) + t] = static_cast<uint8_t>((c0 & 15) | ((c1 & 15) << 4));
   }
   asm volatile("cp.async.wait_all;" ::: "memory");
   __syncthreads();
-  if (warp < 2) {  // int8 rows of the new K (warp 0) and V (warp 1) of head h
+  if (app && warp < 2) {  // int8 rows of the new K (warp 0) and V (warp 1) of head h
     float rowv[16];
 #pragma unroll
     for (int i = 0; i < 16; i++) {
@@ -330,6 +331,10 @@ __global__ __launch_bounds__(kPrepThreads) void prepare_kernel(
       rowv[i] = x < d ? bf16_bits_to_f32(kv_rows[warp][x]) : 0.f;
     }
     fold::encode_row_warp(rowv, d, (warp == 0 ? k8 : v8) + (row * Hkv + h) * d, (warp == 0 ? ks : vs) + row * Hkv + h);
+    if (ap.host4) {
+      const int64_t rb = d / 2 + d / 32;
+      fold::encode_int4_row_warp(rowv, d, ap.host4 + (sk_row * Hkv * 2 + 2 * h + warp) * rb);
+    }
   }
   // Folded query: the request's last CTA quantises all heads with one scale.
   __threadfence();
@@ -379,8 +384,8 @@ constexpr int kReqThreads = 1024;
 
 __global__ __launch_bounds__(kReqThreads, 1) void prepare_req_kernel(
     const uint16_t* __restrict__ q, const uint16_t* __restrict__ newk, const uint16_t* __restrict__ newv, int Hq,
-    int Hkv, int d, const float* __restrict__ basis, const float* __restrict__ c,
-    const int64_t* __restrict__ new_rows, uint8_t* __restrict__ sketch, int8_t* __restrict__ k8,
+    int Hkv, int d, const float* __restrict__ basis, const float* __restrict__ c, const fold::Append ap,
+    uint8_t* __restrict__ sketch, int8_t* __restrict__ k8,
     __half* __restrict__ ks, int8_t* __restrict__ v8, __half* __restrict__ vs, int8_t* __restrict__ q8,
     float* __restrict__ sigma_out) {
   extern __shared__ __align__(16) float dsm[];
@@ -392,7 +397,8 @@ __global__ __launch_bounds__(kReqThreads, 1) void prepare_req_kernel(
   float* qp = part + ns * nv * kRank;                              // [Hkv*64]
   uint16_t* rows = reinterpret_cast<uint16_t*>(qp + Hkv * kRank);  // [nv][d]: K rows, then V rows
   // Every load first, so that the first-touch latencies overlap.
-  const int64_t row = new_rows[b];
+  int64_t row = 0, sk_row = 0;
+  const bool app = fold::append_rows(ap, b, &row, &sk_row);
   for (int u = t; u < nv * (d / 8); u += blockDim.x) {
     const int r = u / (d / 8), piece = u - r * (d / 8);
     const uint16_t* src = (r < Hkv ? newk : newv) + (static_cast<int64_t>(b) * Hkv + r % Hkv) * d + 8 * piece;
@@ -432,12 +438,12 @@ __global__ __launch_bounds__(kReqThreads, 1) void prepare_req_kernel(
     qp[m] = v;
     amax = fmaxf(amax, fabsf(v));
   }
-  for (int m = t; m < Hkv * kRank / 2; m += blockDim.x) {  // sketch codes of the new keys, two per byte
+  for (int m = t; app && m < Hkv * kRank / 2; m += blockDim.x) {  // sketch codes of the new keys, two per byte
     const int h = m / (kRank / 2), j0 = 2 * (m % (kRank / 2));
     const float* pk = part + (Hkv + h) * kRank;
     const int c0 = fold::sketch_code(fold::combine_slices(pk + j0, nv * kRank, ns), c[h * kRank + j0]);
     const int c1 = fold::sketch_code(fold::combine_slices(pk + j0 + 1, nv * kRank, ns), c[h * kRank + j0 + 1]);
-    sketch[row * (Hkv * kRank / 2) + m] = static_cast<uint8_t>((c0 & 15) | ((c1 & 15) << 4));
+    sketch[sk_row * (Hkv * kRank / 2) + m] = static_cast<uint8_t>((c0 & 15) | ((c1 & 15) << 4));
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
@@ -450,7 +456,7 @@ __global__ __launch_bounds__(kReqThreads, 1) void prepare_req_kernel(
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
     if (t == 0) red[0] = v;
   }
-  for (int r = warp; r < nv; r += blockDim.x >> 5) {  // int8 rows: K of head r, then V of head r - Hkv
+  for (int r = warp; app && r < nv; r += blockDim.x >> 5) {  // int8 rows: K of head r, then V of head r - Hkv
     float rowv[16];
 #pragma unroll
     for (int i = 0; i < 16; i++) {
@@ -459,6 +465,10 @@ __global__ __launch_bounds__(kReqThreads, 1) void prepare_req_kernel(
     }
     const int h = r % Hkv;
     fold::encode_row_warp(rowv, d, (r < Hkv ? k8 : v8) + (row * Hkv + h) * d, (r < Hkv ? ks : vs) + row * Hkv + h);
+    if (ap.host4) {  // the token's int4 host row: head h, K then V
+      const int64_t rb = d / 2 + d / 32;
+      fold::encode_int4_row_warp(rowv, d, ap.host4 + (sk_row * Hkv * 2 + 2 * h + (r < Hkv ? 0 : 1)) * rb);
+    }
   }
   __syncthreads();
   const float sigma = __fdiv_rn(red[0], 127.f);
@@ -475,6 +485,34 @@ SKV_EXPORT size_t skv_decode_prepare_workspace_size(int B, int Hkv, int r) {
   return (static_cast<size_t>(B) * Hkv * kRank * sizeof(float) + 255) / 256 * 256 + (B * sizeof(unsigned) + 255) / 256 * 256;
 }
 
+namespace skv {
+
+// Launches the per-step preparation (a1 + a2 + the int8 / int4 append) with
+// the appended rows given by `ap`; used by skv_decode_prepare and by the
+// chained layer step.
+int launch_prepare(const uint16_t* q, const uint16_t* new_k, const uint16_t* new_v, int B, int Hq, int Hkv, int d,
+                   const float* basis, const float* c, const fold::Append& ap, uint8_t* sketch, int8_t* k8,
+                   uint16_t* k_scale, int8_t* v8, uint16_t* v_scale, int8_t* q8, float* sigma, void* workspace,
+                   cudaStream_t st) {
+  float* qp_ws = static_cast<float*>(workspace);
+  unsigned* tickets = reinterpret_cast<unsigned*>(
+      static_cast<char*>(workspace) + (static_cast<size_t>(B) * Hkv * kRank * sizeof(float) + 255) / 256 * 256);
+  const size_t smem = prepare_req_smem(Hkv, d);
+  if (smem <= 48 * 1024) {  // one CTA per request
+    prepare_req_kernel<<<B, kReqThreads, smem, st>>>(q, new_k, new_v, Hq, Hkv, d, basis, c, ap, sketch, k8,
+                                                     reinterpret_cast<__half*>(k_scale), v8,
+                                                     reinterpret_cast<__half*>(v_scale), q8, sigma);
+    return launch_status();
+  }
+  dim3 grid(Hkv, B);
+  prepare_kernel<<<grid, kPrepThreads, 0, st>>>(q, new_k, new_v, Hq, Hkv, d, basis, c, ap, sketch, k8,
+                                                reinterpret_cast<__half*>(k_scale), v8,
+                                                reinterpret_cast<__half*>(v_scale), q8, sigma, qp_ws, tickets);
+  return launch_status();
+}
+
+}  // namespace skv
+
 SKV_EXPORT int skv_decode_prepare(const uint16_t* q, const uint16_t* new_k, const uint16_t* new_v, int B, int Hq,
                                   int Hkv, int d, int r, const float* basis, const float* c,
                                   const int64_t* new_rows, uint8_t* sketch, int8_t* k8, uint16_t* k_scale,
@@ -487,19 +525,8 @@ SKV_EXPORT int skv_decode_prepare(const uint16_t* q, const uint16_t* new_k, cons
       !workspace)
     return SKV_EINVAL;
   if (workspace_bytes < skv_decode_prepare_workspace_size(B, Hkv, r)) return SKV_ENOMEM;
-  float* qp_ws = static_cast<float*>(workspace);
-  unsigned* tickets = reinterpret_cast<unsigned*>(
-      static_cast<char*>(workspace) + (static_cast<size_t>(B) * Hkv * kRank * sizeof(float) + 255) / 256 * 256);
-  const size_t smem = prepare_req_smem(Hkv, d);
-  if (smem <= 48 * 1024) {  // one CTA per request
-    prepare_req_kernel<<<B, kReqThreads, smem, as_stream(stream)>>>(
-        q, new_k, new_v, Hq, Hkv, d, basis, c, new_rows, sketch, k8, reinterpret_cast<__half*>(k_scale), v8,
-        reinterpret_cast<__half*>(v_scale), q8, sigma);
-    return launch_status();
-  }
-  dim3 grid(Hkv, B);
-  prepare_kernel<<<grid, kPrepThreads, 0, as_stream(stream)>>>(
-      q, new_k, new_v, Hq, Hkv, d, basis, c, new_rows, sketch, k8, reinterpret_cast<__half*>(k_scale), v8,
-      reinterpret_cast<__half*>(v_scale), q8, sigma, qp_ws, tickets);
-  return launch_status();
+  fold::Append ap{};
+  ap.rows = new_rows;
+  return launch_prepare(q, new_k, new_v, B, Hq, Hkv, d, basis, c, ap, sketch, k8, k_scale, v8, v_scale, q8, sigma,
+                        workspace, as_stream(stream));
 }

@@ -74,3 +74,42 @@ def test_prefill_argument_checks(lib):
     assert lib.skv_prefill_attend(*args(2, 16, 3, 256, 64)) == 1
     assert lib.skv_prefill_attend(*args(2, 16, 2, 256, 0)) == 1
     assert lib.skv_prefill_attend(*args(0, 16, 2, 256, 64)) == 0
+
+
+def test_layer_step_struct_matches_the_header(lib, tmp_path):
+    """The binding's LayerStep has the size and field offsets that a C
+    compiler gives skv_layer_step (include/sparsekv.h)."""
+    import shutil
+    import subprocess
+
+    import sparse_kv_long_gb300 as skv
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    names = [f[0] for f in skv.LayerStep._fields_]
+    src = tmp_path / "layout.c"
+    body = "".join(f'  printf("{n} %zu\\n", offsetof(skv_layer_step, {n}));\n' for n in names)
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "sparsekv.h"\nint main(void) {\n'
+                   '  printf("size %zu\\n", sizeof(skv_layer_step));\n' + body + "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-I", str(skvtest.ROOT) + "/include", str(src), "-o", str(exe)], check=True)
+    got = dict(line.split() for line in subprocess.run([str(exe)], capture_output=True, text=True,
+                                                       check=True).stdout.splitlines())
+    assert int(got["size"]) == ctypes.sizeof(skv.LayerStep)
+    for n in names:
+        assert int(got[n]) == getattr(skv.LayerStep, n).offset, n
+
+
+def test_layer_step_argument_checks(lib):
+    import sparse_kv_long_gb300 as skv
+    a = skv.LayerStep()
+    a.B, a.Hq, a.Hkv, a.d, a.r, a.n_cap, a.k, a.S, a.W = 2, 24, 4, 256, 64, 1000, 64, 4, 16
+    ws = ctypes.c_void_p(256)
+    assert lib.skv_decode_layer_step(ctypes.byref(a), ws, 1 << 30, None, None) == 1  # null pointers
+    a.r = 32
+    assert lib.skv_decode_layer_step_workspace_size(ctypes.byref(a)) == 0             # rank must be 64
+    a.r, a.W = 64, 0
+    assert lib.skv_decode_layer_step_workspace_size(ctypes.byref(a)) == 0             # the tail holds the new token
+    a.W, a.policy, a.Hs = 16, 1, 10
+    assert lib.skv_decode_layer_step_workspace_size(ctypes.byref(a)) == 0             # fewer hot slots than picks
+    assert lib.skv_decode_layer_step(None, ws, 1 << 30, None, None) == 1

@@ -81,7 +81,7 @@ def test_score_select_workspace_serves_growing_and_shrinking_batches(skv, orc, m
             k, ratio = 128, 4
             nb = rng.integers(600, 9000, B)
             L = (nb * ratio + rng.integers(0, ratio, B)).astype(np.int32)
-            n_cap = int(nb.max())
+            n_cap = int(nb.max()) + 1  # room for the incomplete last block
             qi = rng.integers(-3, 4, (B, 128)).astype(np.float32)
             pk = rng.integers(-3, 4, (B, n_cap, 128)).astype(np.float32)
             q_bits = (qi.view(np.uint32) >> 16).astype(np.uint16)
