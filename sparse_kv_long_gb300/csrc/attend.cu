@@ -37,6 +37,16 @@
 #include "common.cuh"
 
 namespace skv {
+
+// The rows every selection holds besides its picks (known-rows mode of the
+// attention): request b's first S tokens and last W tokens, with k picks in
+// between (all T = lengths[b] tokens when T <= S + W + k), as skv_score_select
+// writes them; physical row b*req_row_stride + token.
+struct KnownRows {
+  const int32_t* lengths;
+  int S, W, k;
+};
+
 namespace {
 
 constexpr int D = 256;
@@ -78,6 +88,12 @@ struct AttendArgs {
   int max_rows;
   const int32_t* count;
   int B, Hq, Hkv, G, hgroups, nsplit, rows_per_split;
+  // known-rows mode (lengths != NULL): the selection of request b holds its
+  // first kS tokens and last kW tokens besides kK picks (all T tokens when
+  // T <= kS + kW + kK); split s takes known_per_split of the former and
+  // picks_per_split of the picks
+  const int32_t* lengths;
+  int kS, kW, kK, known_per_split, picks_per_split;
   float scale_log2;
   float* part;
   unsigned* tickets;
@@ -227,61 +243,104 @@ __global__ __launch_bounds__(kThreads, 2) void attend_kernel(AttendArgs a) {
   const int pair = warp >> 1, e = warp & 1;  // e: which half of the head dimension
   const int g = lane >> 2, c = lane & 3;
 
-  // The query and the barriers do not depend on the kernel before this one
-  // (the selection); everything else does.
+  // Rows of the split.  In known-rows mode (a.lengths set) the split takes a
+  // slice of the rows every selection contains -- the sinks and the recent
+  // tail, found from the request's length -- and a slice of the picks; the
+  // first are staged and attended before waiting for the kernel that writes
+  // the selection (a programmatic dependency), the picks after.  s_prow[i]:
+  // physical row of split row i (-1: none); known rows take [0, npad), picks
+  // start at npad (a whole number of tiles).
   if (threadIdx.x < kPairs * kStages) mbar_init(&bars[threadIdx.x / kStages][threadIdx.x % kStages], 64);
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  grid_dependency_wait();
-  int n = a.count[b];
-  n = n < 0 ? 0 : (n > a.max_rows ? a.max_rows : n);
-  const int r0 = split * a.rows_per_split;
-  const int r1 = r0 + a.rows_per_split < n ? r0 + a.rows_per_split : n;
-  const int nr = r1 > r0 ? r1 - r0 : 0;
 
   const int64_t pitch = static_cast<int64_t>(a.Hkv) * Gm::RB;  // bytes per pool row
   const uint8_t* kbase = a.kpool + static_cast<int64_t>(h) * Gm::RB;
   const uint8_t* vbase = a.vpool + static_cast<int64_t>(h) * Gm::RB;
 
   unsigned char* pbuf = smem + pair * Gm::PAIR_BYTES;
-  const int ntiles = (nr + kTileRows - 1) / kTileRows;
-  int my_tiles = 0;
-  for (int t = pair; t < ntiles; t += kPairs) my_tiles++;
   // The 64 threads of the pair copy tile `it` (16 K rows and 16 V rows) into
   // stage it % kStages in 16-byte pieces: thread u of the pair takes piece
-  // u % (RB/16) of rows u / (RB/16) + 64/(RB/16) * i.  rowp(r) gives the
-  // physical row of tile row r (-1: pool row 0, masked later).  Each thread
-  // then arrives on the stage's barrier when its copies have landed.
+  // u % (RB/16) of rows u / (RB/16) + 64/(RB/16) * i.  Rows without a
+  // physical row read pool row 0 (masked later).  Each thread then arrives on
+  // the stage's barrier when its copies have landed.
   constexpr int kPieces = Gm::RB / 16;                 // 16-byte pieces per row
   constexpr int kRowsPerRound = 64 / kPieces;          // rows covered by one round of the pair
   const int u = 32 * e + lane;
-  auto copy_tile = [&](int it, auto&& rowp) {
+  int nr = 0;  // split rows whose physical rows are staged so far
+  auto copy_tile = [&](int it) {
     const int stage = it % kStages;
+    const int tb = (pair + kPairs * it) * kTileRows;
     unsigned char* kst = pbuf + stage * Gm::STAGE;
     unsigned char* vst = kst + kTileRows * Gm::KP;
     const int piece = u % kPieces;
 #pragma unroll
     for (int i = 0; i < kTileRows / kRowsPerRound; i++) {
       const int row = u / kPieces + kRowsPerRound * i;
-      int64_t prow = rowp(row);
+      int64_t prow = tb + row < nr ? s_prow[tb + row] : int64_t(-1);
       if (prow < 0) prow = 0;
       cp_async16(kst + row * Gm::KP + 16 * piece, kbase + prow * pitch + 16 * piece);
       cp_async16(vst + row * Gm::VP + 16 * piece, vbase + prow * pitch + 16 * piece);
     }
     cp_async_arrive(&bars[pair][stage]);
   };
-
-  // ---- row numbers, then the first tiles, scales and query heads ---------------
-  // Each stage issues all of its loads before using any: the split's row
-  // numbers (one latency), then the pair's first tiles and the scales of
-  // every row (one more, overlapping the tiles' flight).
+  // Physical row of split row i from a token / row id p (-1: none).
+  auto stage_row = [&](int i, int64_t p) {
+    const bool ok = p >= 0 && p < a.n_pool_rows;
+    if (!ok) set_status(a.status, SKV_DEV_RANGE);
+    s_prow[i] = ok ? p : -1;
+  };
+  // The int8 scales of split rows [i0, i1), every load in flight before any
+  // is stored (called once the rows' tiles are on their way).
   constexpr int kRowsPerThread = (kMaxRowsPerSplit + kThreads - 1) / kThreads;
-  constexpr int kQPerThread = (8 * D / 8 + kThreads - 1) / kThreads;
-  int32_t rid[kRowsPerThread];
+  auto stage_scales = [&](int i0, int i1) {
+    if (KV != SKV_KV_INT8) return;
+    uint16_t ksv[kRowsPerThread], vsv[kRowsPerThread];
 #pragma unroll
-  for (int j = 0; j < kRowsPerThread; j++) {
-    const int i = threadIdx.x + j * kThreads;
-    rid[j] = i < nr ? a.rows[static_cast<int64_t>(b) * a.max_rows + r0 + i] : -1;
+    for (int j = 0; j < kRowsPerThread; j++) {
+      const int i = i0 + threadIdx.x + j * kThreads;
+      const int64_t p = i < i1 ? s_prow[i] : int64_t(-1);
+      ksv[j] = p >= 0 ? a.kscale[p * a.Hkv + h] : 0;
+      vsv[j] = p >= 0 ? a.vscale[p * a.Hkv + h] : 0;
+    }
+#pragma unroll
+    for (int j = 0; j < kRowsPerThread; j++) {
+      const int i = i0 + threadIdx.x + j * kThreads;
+      if (i < i1) {
+        s_ks[i] = __half2float(__ushort_as_half(ksv[j]));
+        s_vs[i] = __half2float(__ushort_as_half(vsv[j]));
+      }
+    }
+  };
+
+  int64_t T = 0;
+  int head = 0, tailn = 0, npick = 0, kk0 = 0, nk = 0;
+  if (a.lengths) {  // sinks [0, head) and the tail [T - tailn, T) of every selection
+    T = a.lengths[b];
+    if (T < 0) T = 0;
+    if (a.req_row_stride > 0 && T > a.req_row_stride) {  // the selection clamps it the same way
+      if (split == 0 && threadIdx.x == 0) set_status(a.status, SKV_DEV_RANGE);
+      T = a.req_row_stride;
+    }
+    const bool dense = T <= static_cast<int64_t>(a.kS) + a.kW + a.kK;
+    head = static_cast<int>(T < a.kS ? T : a.kS);
+    tailn = static_cast<int>(T - head < a.kW ? T - head : a.kW);
+    const int64_t npos = dense ? T : static_cast<int64_t>(a.kS) + a.kK + a.kW;
+    npick = static_cast<int>(npos - head - tailn);
+    kk0 = split * a.known_per_split;
+    const int kk1 = kk0 + a.known_per_split < head + tailn ? kk0 + a.known_per_split : head + tailn;
+    nk = kk1 > kk0 ? kk1 - kk0 : 0;
   }
+  const int npad = (nk + kTileRows - 1) / kTileRows * kTileRows;
+  for (int i = threadIdx.x; i < npad; i += blockDim.x) {
+    if (i < nk) {
+      const int pos = kk0 + i;
+      const int64_t tok = pos < head ? pos : T - tailn + (pos - head);
+      stage_row(i, static_cast<int64_t>(b) * a.req_row_stride + tok);
+    } else {
+      s_prow[i] = -1;
+    }
+  }
+  constexpr int kQPerThread = (8 * D / 8 + kThreads - 1) / kThreads;
   uint4 qv[kQPerThread];
 #pragma unroll
   for (int j = 0; j < kQPerThread; j++) {  // 16-byte pieces of 8 query heads
@@ -292,39 +351,14 @@ __global__ __launch_bounds__(kThreads, 2) void attend_kernel(AttendArgs a) {
     if (i < 8 * D / 8 && hl < a.G)
       qv[j] = *reinterpret_cast<const uint4*>(a.q + (static_cast<int64_t>(b) * a.Hq + h * a.G + hl) * D + 8 * x8);
   }
-  int64_t prj[kRowsPerThread];
-#pragma unroll
-  for (int j = 0; j < kRowsPerThread; j++) {
-    const int i = threadIdx.x + j * kThreads;
-    const int64_t p = static_cast<int64_t>(b) * a.req_row_stride + rid[j];
-    prj[j] = (rid[j] >= 0 && p >= 0 && p < a.n_pool_rows) ? p : -1;  // -1: absent or out of range
-    if (i < nr) {
-      if (prj[j] < 0) set_status(a.status, SKV_DEV_RANGE);
-      s_prow[i] = prj[j];
-    }
-  }
   __syncthreads();
-  for (int it = 0; it < kStages && it < my_tiles; it++) {  // the pair's first tiles go out at once
-    const int tb = (pair + kPairs * it) * kTileRows;
-    copy_tile(it, [&](int row) { return tb + row < nr ? s_prow[tb + row] : int64_t(-1); });
-  }
-  if (KV == SKV_KV_INT8) {
-    uint16_t ksv[kRowsPerThread], vsv[kRowsPerThread];
-#pragma unroll
-    for (int j = 0; j < kRowsPerThread; j++) {
-      const bool ok = threadIdx.x + j * kThreads < nr && prj[j] >= 0;
-      ksv[j] = ok ? a.kscale[prj[j] * a.Hkv + h] : 0;
-      vsv[j] = ok ? a.vscale[prj[j] * a.Hkv + h] : 0;
-    }
-#pragma unroll
-    for (int j = 0; j < kRowsPerThread; j++) {
-      const int i = threadIdx.x + j * kThreads;
-      if (i < nr) {
-        s_ks[i] = __half2float(__ushort_as_half(ksv[j]));
-        s_vs[i] = __half2float(__ushort_as_half(vsv[j]));
-      }
-    }
-  }
+  nr = npad;
+  const int ntk = npad / kTileRows;  // tiles of known rows
+  int my_known = 0;
+  for (int t = pair; t < ntk; t += kPairs) my_known++;
+  int issued = 0;
+  while (issued < my_known && issued < kStages) copy_tile(issued++);  // the pair's first known tiles go out at once
+  stage_scales(0, npad);
 #pragma unroll
   for (int j = 0; j < kQPerThread; j++) {
     const int i = threadIdx.x + j * kThreads;
@@ -355,15 +389,17 @@ __global__ __launch_bounds__(kThreads, 2) void attend_kernel(AttendArgs a) {
   for (int mt = 0; mt < 8; mt++) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
   float m_run = -INFINITY, l_part = 0.f;
 
-  int completed = 0;  // tiles whose copies have landed
-  for (int it = 0; it < my_tiles; it++) {
+  int completed = 0;  // tiles whose copies have landed and were attended
+  // Attends tile `it` of the pair (its copies were issued); false when the
+  // wait for its copies gave up.
+  auto attend_tile = [&](int it) -> bool {
     const int stage = it % kStages;
     const uint32_t parity = (it / kStages) & 1;
     // Both warps of the pair must agree, or one would wait for the other at
     // the pair barriers below.
     if (!pair_all(pair, mbar_wait(&bars[pair][stage], parity))) {
       set_status(a.status, SKV_DEV_TIMEOUT);
-      break;
+      return false;
     }
     completed = it + 1;
     const unsigned char* kst = pbuf + stage * Gm::STAGE;
@@ -497,16 +533,60 @@ __global__ __launch_bounds__(kThreads, 2) void attend_kernel(AttendArgs a) {
       }
     }
     pair_sync(pair);  // both warps are done with this stage (and with s_x)
-    const int nx = it + kStages;
-    if (nx < my_tiles) {  // both warps are past this stage (pair barrier above)
-      const int tb = (pair + kPairs * nx) * kTileRows;
-      copy_tile(nx, [&](int row) { return tb + row < nr ? s_prow[tb + row] : int64_t(-1); });
+    return true;
+  };
+  bool live = true;
+  // ---- phase A: the known rows, before the selection is complete --------------------
+  for (int it = 0; live && it < my_known; it++) {
+    live = attend_tile(it);
+    if (live && issued < my_known && issued < it + 1 + kStages) copy_tile(issued++);
+  }
+  // ---- the picks: after the kernel that wrote the selection -------------------------
+  grid_dependency_wait();
+  int np = 0, pos0 = 0;
+  if (a.lengths) {
+    const int pp0 = split * a.picks_per_split;
+    const int pp1 = pp0 + a.picks_per_split < npick ? pp0 + a.picks_per_split : npick;
+    np = pp1 > pp0 ? pp1 - pp0 : 0;
+    pos0 = head + pp0;
+  } else {
+    int n = a.count[b];
+    n = n < 0 ? 0 : (n > a.max_rows ? a.max_rows : n);
+    const int r0 = split * a.rows_per_split;
+    const int r1 = r0 + a.rows_per_split < n ? r0 + a.rows_per_split : n;
+    np = r1 > r0 ? r1 - r0 : 0;
+    pos0 = r0;
+  }
+  {  // every row id load in flight before any is used
+    int32_t rid[kRowsPerThread];
+#pragma unroll
+    for (int j = 0; j < kRowsPerThread; j++) {
+      const int i = threadIdx.x + j * kThreads;
+      rid[j] = i < np ? a.rows[static_cast<int64_t>(b) * a.max_rows + pos0 + i] : -1;
     }
+#pragma unroll
+    for (int j = 0; j < kRowsPerThread; j++) {
+      const int i = threadIdx.x + j * kThreads;
+      if (i < np) stage_row(npad + i, rid[j] >= 0 ? static_cast<int64_t>(b) * a.req_row_stride + rid[j] : -1);
+    }
+  }
+  __syncthreads();
+  nr = npad + np;
+  const int ntiles = (nr + kTileRows - 1) / kTileRows;
+  int my_tiles = 0;
+  for (int t = pair; t < ntiles; t += kPairs) my_tiles++;
+  // ---- phase B: the picks ------------------------------------------------------------
+  if (live)
+    while (issued < my_tiles && issued < my_known + kStages) copy_tile(issued++);
+  stage_scales(npad, nr);
+  __syncthreads();
+  for (int it = my_known; live && it < my_tiles; it++) {
+    live = attend_tile(it);
+    if (live && issued < my_tiles && issued < it + 1 + kStages) copy_tile(issued++);
   }
   // After a timeout, give the copies still in flight a bounded chance to land
   // before the buffers are reused for the merge.
-  for (int it = completed; it < my_tiles && it < completed + kStages; it++)
-    mbar_wait(&bars[pair][it % kStages], (it / kStages) & 1);
+  for (int it = completed; it < issued; it++) mbar_wait(&bars[pair][it % kStages], (it / kStages) & 1);
 
   // ---- merge the 2 pairs (partials staged in the ring buffers) --------------------
   __syncthreads();
@@ -653,18 +733,18 @@ int occupancy() {
 }
 
 struct Plan {
-  int hgroups, gy, nsplit, rows_per_split;
+  int hgroups, gy, nsplit, rows_per_split, known_per_split, picks_per_split;
   size_t part_bytes, ticket_bytes;
 };
 
-Plan make_plan(int kv_kind, int B, int Hq, int Hkv, int max_rows) {
+Plan make_plan(int kv_kind, int B, int Hq, int Hkv, int max_rows, const KnownRows* known) {
   Plan p;
   const int G = Hq / Hkv;
   p.hgroups = (G + 7) / 8;
   p.gy = Hkv * p.hgroups;
   const int pairs = B * p.gy;
   const int per_sm = kv_kind == SKV_KV_INT8 ? occupancy<SKV_KV_INT8>() : occupancy<SKV_KV_BF16>();
-  const int target = per_sm * (sm_count() > 0 ? sm_count() : 1);
+  const int target = (per_sm > 0 ? per_sm : 1) * (sm_count() > 0 ? sm_count() : 1);
   int ns = target / pairs;  // at most one wave ...
   const int min_ns = (max_rows + kMaxRowsPerSplit - 1) / kMaxRowsPerSplit;  // ... unless splits get long
   const int max_ns = (max_rows + 63) / 64;
@@ -676,6 +756,16 @@ Plan make_plan(int kv_kind, int B, int Hq, int Hkv, int max_rows) {
   rps = (rps + 15) / 16 * 16;
   if (rps > kMaxRowsPerSplit) rps = kMaxRowsPerSplit;
   ns = (max_rows + rps - 1) / rps;
+  p.known_per_split = p.picks_per_split = 0;
+  if (known) {  // a slice of the sinks + tail and a slice of the picks per split, each whole tiles
+    const int nknown = known->S + known->W, npicks = max_rows - nknown;
+    for (;; ns++) {
+      p.known_per_split = ((nknown + ns - 1) / ns + 15) / 16 * 16;
+      p.picks_per_split = ((npicks + ns - 1) / ns + 15) / 16 * 16;
+      if (p.known_per_split + p.picks_per_split <= kMaxRowsPerSplit || ns >= kMaxSplit) break;
+    }
+    rps = p.known_per_split + p.picks_per_split;
+  }
   p.nsplit = ns;
   p.rows_per_split = rps;
   p.part_bytes = static_cast<size_t>(B) * p.gy * ns * kPart * sizeof(float);
@@ -684,6 +774,72 @@ Plan make_plan(int kv_kind, int B, int Hq, int Hkv, int max_rows) {
 }
 
 }  // namespace
+
+size_t attend_workspace_bytes(int kv_kind, int B, int Hq, int Hkv, int max_rows, const KnownRows* known) {
+  const Plan p = make_plan(kv_kind, B, Hq, Hkv, max_rows, known);
+  return p.ticket_bytes + p.part_bytes;
+}
+
+int launch_attend(int kv_kind, int B, int Hq, int Hkv, const uint16_t* q, const void* k_pool, const void* v_pool,
+                  const uint16_t* k_scale, const uint16_t* v_scale, int64_t req_row_stride, int64_t n_pool_rows,
+                  const int32_t* rows, int max_rows, const int32_t* count, float softmax_scale, float* out,
+                  void* workspace, size_t workspace_bytes, int32_t* dev_status, const KnownRows* known,
+                  cudaStream_t st) {
+  Plan p = make_plan(kv_kind, B, Hq, Hkv, max_rows, known);
+  if (workspace_bytes < p.ticket_bytes + p.part_bytes) return SKV_ENOMEM;
+  if (p.gy > 65535) return SKV_EUNSUPPORTED;
+  if (known && p.known_per_split + p.picks_per_split > kMaxRowsPerSplit) return SKV_EUNSUPPORTED;
+  AttendArgs a;
+  a.q = q;
+  a.kpool = static_cast<const uint8_t*>(k_pool);
+  a.vpool = static_cast<const uint8_t*>(v_pool);
+  a.kscale = k_scale;
+  a.vscale = v_scale;
+  a.req_row_stride = req_row_stride;
+  a.n_pool_rows = n_pool_rows;
+  a.rows = rows;
+  a.max_rows = max_rows;
+  a.count = count;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.G = Hq / Hkv;
+  a.hgroups = p.hgroups;
+  a.nsplit = p.nsplit;
+  a.rows_per_split = p.rows_per_split;
+  a.lengths = known ? known->lengths : nullptr;
+  a.kS = known ? known->S : 0;
+  a.kW = known ? known->W : 0;
+  a.kK = known ? known->k : 0;
+  a.known_per_split = p.known_per_split;
+  a.picks_per_split = p.picks_per_split;
+  a.scale_log2 = softmax_scale * kLog2e;
+  a.tickets = static_cast<unsigned*>(workspace);
+  a.part = reinterpret_cast<float*>(static_cast<char*>(workspace) + p.ticket_bytes);
+  a.out = out;
+  a.status = dev_status;
+  // Launched with programmatic stream serialization: the CTAs may start (and
+  // set up, and in known-rows mode attend the sinks and the tail) while the
+  // selection that produces `rows` is still finishing.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.nsplit, p.gy, B);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kv_kind == SKV_KV_INT8 ? dyn_smem<SKV_KV_INT8>() : dyn_smem<SKV_KV_BF16>();
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = kv_kind == SKV_KV_INT8 ? cudaLaunchKernelEx(&cfg, attend_kernel<SKV_KV_INT8>, a)
+                                               : cudaLaunchKernelEx(&cfg, attend_kernel<SKV_KV_BF16>, a);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return SKV_ECUDA;
+  }
+  return SKV_OK;
+}
+
 }  // namespace skv
 
 using namespace skv;
@@ -693,9 +849,8 @@ SKV_EXPORT size_t skv_attend_workspace_size(int B, int Hq, int Hkv, int d, int m
       max_rows > kMaxSplit * kMaxRowsPerSplit)
     return 0;
   // Sized for the larger of the two row encodings' plans.
-  Plan p8 = make_plan(SKV_KV_INT8, B, Hq, Hkv, max_rows);
-  Plan p16 = make_plan(SKV_KV_BF16, B, Hq, Hkv, max_rows);
-  const size_t s8 = p8.ticket_bytes + p8.part_bytes, s16 = p16.ticket_bytes + p16.part_bytes;
+  const size_t s8 = attend_workspace_bytes(SKV_KV_INT8, B, Hq, Hkv, max_rows, nullptr);
+  const size_t s16 = attend_workspace_bytes(SKV_KV_BF16, B, Hq, Hkv, max_rows, nullptr);
   return s8 > s16 ? s8 : s16;
 }
 
@@ -718,49 +873,7 @@ SKV_EXPORT int skv_sparse_attend_decode(int kv_kind, int B, int Hq, int Hkv, int
   if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out) || !aligned16(workspace) ||
       (reinterpret_cast<uintptr_t>(q) & 7))
     return SKV_EINVAL;
-  Plan p = make_plan(kv_kind, B, Hq, Hkv, max_rows);
-  if (workspace_bytes < p.ticket_bytes + p.part_bytes) return SKV_ENOMEM;
-  if (p.gy > 65535) return SKV_EUNSUPPORTED;
-  AttendArgs a;
-  a.q = q;
-  a.kpool = static_cast<const uint8_t*>(k_pool);
-  a.vpool = static_cast<const uint8_t*>(v_pool);
-  a.kscale = k_scale;
-  a.vscale = v_scale;
-  a.req_row_stride = req_row_stride;
-  a.n_pool_rows = n_pool_rows;
-  a.rows = rows;
-  a.max_rows = max_rows;
-  a.count = count;
-  a.B = B;
-  a.Hq = Hq;
-  a.Hkv = Hkv;
-  a.G = Hq / Hkv;
-  a.hgroups = p.hgroups;
-  a.nsplit = p.nsplit;
-  a.rows_per_split = p.rows_per_split;
-  a.scale_log2 = softmax_scale * kLog2e;
-  a.tickets = static_cast<unsigned*>(workspace);
-  a.part = reinterpret_cast<float*>(static_cast<char*>(workspace) + p.ticket_bytes);
-  a.out = out;
-  a.status = dev_status;
-  // Launched with programmatic stream serialization: the CTAs may start (and
-  // set up) while the selection that produces `rows` is still finishing.
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.nsplit, p.gy, B);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kv_kind == SKV_KV_INT8 ? dyn_smem<SKV_KV_INT8>() : dyn_smem<SKV_KV_BF16>();
-  cfg.stream = as_stream(stream);
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  const cudaError_t e = kv_kind == SKV_KV_INT8 ? cudaLaunchKernelEx(&cfg, attend_kernel<SKV_KV_INT8>, a)
-                                               : cudaLaunchKernelEx(&cfg, attend_kernel<SKV_KV_BF16>, a);
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    return SKV_ECUDA;
-  }
-  return SKV_OK;
+  return launch_attend(kv_kind, B, Hq, Hkv, q, k_pool, v_pool, k_scale, v_scale, req_row_stride, n_pool_rows, rows,
+                       max_rows, count, softmax_scale, out, workspace, workspace_bytes, dev_status, nullptr,
+                       as_stream(stream));
 }

@@ -23,6 +23,16 @@ int launch_prepare(const uint16_t* q, const uint16_t* new_k, const uint16_t* new
                    uint16_t* k_scale, int8_t* v8, uint16_t* v_scale, int8_t* q8, float* sigma, void* workspace,
                    cudaStream_t st);
 bool score_select_fits_int4(int width, int B, int64_t n_cap);
+struct KnownRows {
+  const int32_t* lengths;
+  int S, W, k;
+};
+size_t attend_workspace_bytes(int kv_kind, int B, int Hq, int Hkv, int max_rows, const KnownRows* known);
+int launch_attend(int kv_kind, int B, int Hq, int Hkv, const uint16_t* q, const void* k_pool, const void* v_pool,
+                  const uint16_t* k_scale, const uint16_t* v_scale, int64_t req_row_stride, int64_t n_pool_rows,
+                  const int32_t* rows, int max_rows, const int32_t* count, float softmax_scale, float* out,
+                  void* workspace, size_t workspace_bytes, int32_t* dev_status, const KnownRows* known,
+                  cudaStream_t st);
 
 namespace {
 
@@ -68,7 +78,11 @@ StepWs plan(const skv_layer_step& a) {
     off += up256(static_cast<size_t>(a.B) * sizeof(int32_t));
   }
   w.att = off;
-  off += up256(skv_attend_workspace_size(a.B, a.Hq, a.Hkv, a.d, max_rows));
+  // resident rows: the attention takes the sinks and the tail before the
+  // selection is complete (its known-rows plan)
+  const KnownRows known{a.lengths, a.S, a.W, a.k};
+  off += up256(attend_workspace_bytes(SKV_KV_INT8, a.B, a.Hq, a.Hkv, max_rows,
+                                      a.policy == SKV_RESIDENT ? &known : nullptr));
   w.total = off;
   return w;
 }
@@ -150,9 +164,12 @@ SKV_EXPORT int skv_decode_layer_step(const skv_layer_step* ap, void* workspace, 
     rows = r;
   }
 
-  // 4. attention over the selected rows
-  return skv_sparse_attend_decode(SKV_KV_INT8, a.B, a.Hq, a.Hkv, a.d, a.q, a.k8, a.v8, a.k_scale, a.v_scale, R,
-                                  static_cast<int64_t>(a.B) * R, rows, max_rows, a.count, a.softmax_scale, a.out,
-                                  ws + w.att, skv_attend_workspace_size(a.B, a.Hq, a.Hkv, a.d, max_rows),
-                                  dev_status, stream);
+  // 4. attention over the selected rows; with resident rows the sinks and
+  // the tail (known from the lengths) are attended while the selection is
+  // still finishing
+  const KnownRows known{a.lengths, a.S, a.W, a.k};
+  const KnownRows* kr = host ? nullptr : &known;
+  return launch_attend(SKV_KV_INT8, a.B, a.Hq, a.Hkv, a.q, a.k8, a.v8, a.k_scale, a.v_scale, R,
+                       static_cast<int64_t>(a.B) * R, rows, max_rows, a.count, a.softmax_scale, a.out, ws + w.att,
+                       attend_workspace_bytes(SKV_KV_INT8, a.B, a.Hq, a.Hkv, max_rows, kr), dev_status, kr, st);
 }

@@ -55,7 +55,8 @@ def _check_fold_and_selection(orc, x, qb, q8_gpu, sk, L, k, S, W, gidx, gcnt, Hk
     return ridx, rcnt
 
 
-@pytest.mark.parametrize("lengths", [[9000, 5000, 3137], [2500, 40_000]], ids=["ragged", "dense_and_sparse"])
+@pytest.mark.parametrize("lengths", [[9000, 5000, 3137], [2500, 40_000], [500, 1090, 70_001]],
+                         ids=["ragged", "dense_and_sparse", "shorter_than_sinks_and_tail"])
 def test_layer_step_resident_matches_oracle_chain(skv, orc, lengths):
     B, Hq, Hkv, d, r, k, S, W = len(lengths), 24, 4, 256, 64, 2048, 64, 1024
     n_steps = 3
