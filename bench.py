@@ -1285,6 +1285,26 @@ def run_extra(args):
         h1.record()
         torch.cuda.synchronize()
         host_gbs = nb / (h0.elapsed_time(h1) * 1e-3) / 1e9
+    # scattered rows, the fetches' access pattern: as many rows per launch as
+    # the resolver's misses per layer-step, random over each layer's tier in
+    # turn (every tier registered, as in the timed steps)
+    gather_gbs = None
+    if w.hosts and stateful:
+        row_b = row_bytes
+        n_rows_tier = (w.hosts[0].nbytes // row_b)
+        per = max(1, int(round(misses_per_layer_step)))
+        grng = np.random.default_rng(SEED + 99)
+        rates = []
+        for rep in range(3):
+            for l in range(len(w.hosts)):
+                rows = torch.from_numpy(grng.choice(n_rows_tier, size=per, replace=False).astype(np.int64)).to(dev)
+                g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                g0.record()
+                skv.gather_read(w.hosts[l].alias, rows, row_b, sink)
+                g1.record()
+                torch.cuda.synchronize()
+                rates.append(per * row_b / (g0.elapsed_time(g1) * 1e-3) / 1e9)
+        gather_gbs = statistics.median(rates)
     kern = {}
     for name, a0, a1, bound, work, rule in w.kernels(None):
         # median over 3 steps x layers: a zero-copy host read now and then takes
@@ -1298,15 +1318,20 @@ def run_extra(args):
                        peak_note="bf16 dense burst (fp16 operands: same nominal rate)")
         elif bound == "host":
             hb = work if work is not None else statistics.mean(eager_misses) * row_bytes
-            blk.update(achieved=hb / (us * 1e-6) / 1e9, peak=host_gbs, unit="GB/s",
-                       bytes_per_launch=hb, peak_note="measured zero-copy read of the registered host tier")
+            ach = hb / (us * 1e-6) / 1e9
+            blk.update(achieved=ach, peak=gather_gbs if gather_gbs else host_gbs, unit="GB/s", bytes_per_launch=hb,
+                       peak_note=("measured zero-copy read of scattered rows: the same number of rows per launch, "
+                                  "the same row size, random over every layer's registered tier")
+                       if gather_gbs else "measured zero-copy streaming read of the registered host tier",
+                       stream_peak=host_gbs, frac_vs_stream=ach / host_gbs if host_gbs else None)
         if "achieved" in blk:
             blk["frac"] = blk["achieved"] / blk["peak"]
         kern[name] = blk
     line = {"workload": args.workload, "metric": "layer-steps/s", "value": value, "unit": "layer-steps/s",
             "n_gpus": 1, "steps": args.steps, "warmup": warm, "ms_per_step": ms_per_step,
             "higher_is_better": True, "data": "synthetic", "config": w.config(),
-            **extra, "host_read_gbs_probe": host_gbs, "kernels": kern, "clocks": clk.summary(),
+            **extra, "host_read_gbs_probe": host_gbs, "host_gather_gbs_probe": gather_gbs, "kernels": kern,
+            "clocks": clk.summary(),
             "device_status": int(w.status.item()),
             "gpu_launches": args.steps * w.L * w.KERNELS_PER_LAYER}
     print(json.dumps(line), flush=True)

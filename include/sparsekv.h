@@ -642,6 +642,20 @@ int skv_quantize_int4_rows(const uint16_t *x, int64_t n_rows, int Hkv, int d,
 int skv_stream_read(const void *src, size_t bytes, unsigned long long *sink, int grid,
                     void *stream);
 
+/*
+ * skv_gather_read -- reads the n rows rows[i] (int64, device) of row_bytes
+ * each at base + rows[i] * row_bytes (device memory or a host alias), one
+ * warp per row with every load of the row in flight at once, and XORs the
+ * words into *sink: the probe for the access pattern of the host-tier
+ * fetches (scattered rows of about a kilobyte), whose rate on registered
+ * host memory depends on how many rows are read at once and on how much
+ * host memory is registered, unlike a streaming read.
+ * Errors: SKV_EINVAL for null pointers, n < 0, row_bytes not a multiple of
+ * 16, or base not 16-byte aligned.
+ */
+int skv_gather_read(const void *base, const int64_t *rows, int n, int64_t row_bytes,
+                    unsigned long long *sink, void *stream);
+
 /* ========================================================================== */
 /* Chunked sparse prefill ([P4] "3.14M Context on 3x 3090 ...", "The Downside */
 /* to Keep in Mind": every prefill token picks its own top blocks, so the     */

@@ -98,6 +98,7 @@ def _load():
                 "skv_residency_lease_hot": ([P, i32, i32, P], i32),
                 "skv_quantize_int4_rows": ([P, i64, i32, i32, P, P, i64, i64, P], i32),
                 "skv_stream_read": ([P, sz, P, i32, P], i32),
+                "skv_gather_read": ([P, P, i32, i64, P, P], i32),
                 "skv_prefill_index_scores": ([i32, P, P, i64, P, i64, P, P], i32),
                 "skv_prefill_attend": ([i32, i32, i32, i32, P, P, P, i64, P, P, i64, P, i32, P, f32, P, P, P, P],
                                        i32),
@@ -370,6 +371,12 @@ def resolve_rows_lru(lengths, idx, count, step, page, block_table, hot_base, hot
         n_pool_rows, _ptr(idx), max_rows, _ptr(count), _ptr(rows_out), _ptr(n_miss), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream)))
     return rows_out, n_miss
+
+
+def gather_read(base, rows, row_bytes, sink, stream=None):
+    """Read rows[i] * row_bytes from base (tensor or int address), one warp per row; XOR into sink."""
+    _check("skv_gather_read", _load().skv_gather_read(_addr(base), _ptr(rows), rows.numel(), int(row_bytes),
+                                                      _ptr(sink), _stream(stream)))
 
 
 def stream_read(src, nbytes, sink, grid=0, stream=None):

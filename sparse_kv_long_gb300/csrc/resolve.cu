@@ -85,44 +85,59 @@ size_t clock_smem_bytes(int Hs, int max_rows) {
 // the codes) -> int8 row + fp16 scale: x = code * s_g exactly in fp32,
 // s8 = fp16(max|x| / 127), q = clamp(rint(x / s8), +-127).  One lane per
 // 64-dim group; the ng lanes of a vector are consecutive.
+// A code takes one of 16 values, so q is computed once per value and the
+// codes are mapped through that table: max|x| = max|code| * s_g (exact),
+// q(-c) = -q(c) (IEEE division, rounding to even and the clamp are
+// symmetric), q(0) = 0, and q(-8) = -q(8).
 __device__ __forceinline__ void requant_group(const uint2 (&c)[4], uint16_t sbits, int ng, int8_t* dst,
                                               __half* sdst, bool store) {
   const float sg = __half2float(__ushort_as_half(sbits));
   const uint32_t w[8] = {c[0].x, c[0].y, c[1].x, c[1].y, c[2].x, c[2].y, c[3].x, c[3].y};
-  float amax = 0.f;
+  // largest |code|: per nibble, 8 - n for n >= 8 (code n - 16), else n
+  int cmax = 0;
 #pragma unroll
   for (int i = 0; i < 8; i++) {
 #pragma unroll
     for (int e = 0; e < 8; e++) {
       const int code = static_cast<int>(w[i] << (28 - 4 * e)) >> 28;
-      amax = fmaxf(amax, fabsf(static_cast<float>(code) * sg));
+      cmax = max(cmax, code < 0 ? -code : code);
     }
   }
+  // max_e |code_e * s_g| (a NaN product counts as 0, as fmaxf over the elements would have it)
+  float amax = fmaxf(0.f, static_cast<float>(cmax) * fabsf(sg));
   for (int o = 1; o < ng; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
   const __half s8 = __float2half_rn(__fdiv_rn(amax, 127.f));
   const float sf = __half2float(s8);
   const bool ok = (sf != 0.f) && isfinite(sf);
   if (!store) return;
+  // table bytes by nibble n: q(n) for n < 8, q(n - 16) = -q(16 - n) for n >= 8
+  int qp[9];
+  qp[0] = 0;
+#pragma unroll
+  for (int m = 1; m <= 8; m++)
+    qp[m] = ok ? rint_clamp(__fdiv_rn(static_cast<float>(m) * sg, sf), -127, 127) : 0;
+  auto byte_of = [](int v) { return static_cast<uint32_t>(v) & 0xffu; };
+  const uint32_t t0 = byte_of(qp[0]) | (byte_of(qp[1]) << 8) | (byte_of(qp[2]) << 16) | (byte_of(qp[3]) << 24);
+  const uint32_t t1 = byte_of(qp[4]) | (byte_of(qp[5]) << 8) | (byte_of(qp[6]) << 16) | (byte_of(qp[7]) << 24);
+  const uint32_t t2 = byte_of(-qp[8]) | (byte_of(-qp[7]) << 8) | (byte_of(-qp[6]) << 16) | (byte_of(-qp[5]) << 24);
+  const uint32_t t3 = byte_of(-qp[4]) | (byte_of(-qp[3]) << 8) | (byte_of(-qp[2]) << 16) | (byte_of(-qp[1]) << 24);
+  // four nibbles held one per byte -> their four table bytes
+  auto lookup = [&](uint32_t x) {
+    const uint32_t sel = (x & 0x7u) | ((x >> 4) & 0x70u) | ((x >> 8) & 0x700u) | ((x >> 12) & 0x7000u);
+    const uint32_t lo = prmt(t0, t1, sel), hi = prmt(t2, t3, sel);
+    const uint32_t m = ((x & 0x08080808u) >> 3) * 0xffu;  // 0xff in the bytes whose nibble is >= 8
+    return (lo & ~m) | (hi & m);
+  };
   uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
   for (int i2 = 0; i2 < 4; i2++) {
     uint32_t out[4];
 #pragma unroll
     for (int k = 0; k < 2; k++) {
-      const uint32_t wi = w[2 * i2 + k];
-      uint32_t lo = 0, hi = 0;
-#pragma unroll
-      for (int e = 0; e < 8; e++) {
-        const int code = static_cast<int>(wi << (28 - 4 * e)) >> 28;
-        const int q = ok ? rint_clamp(__fdiv_rn(static_cast<float>(code) * sg, sf), -127, 127) : 0;
-        const uint32_t byte = static_cast<uint32_t>(q) & 0xffu;
-        if (e < 4)
-          lo |= byte << (8 * e);
-        else
-          hi |= byte << (8 * (e - 4));
-      }
-      out[2 * k] = lo;
-      out[2 * k + 1] = hi;
+      const uint32_t wi = w[2 * i2 + k];  // nibble e = dim 8 (2 i2 + k) + e
+      const uint32_t ev = wi & 0x0f0f0f0fu, od = (wi >> 4) & 0x0f0f0f0fu;  // nibbles 0,2,4,6 and 1,3,5,7
+      out[2 * k] = lookup(prmt(ev, od, 0x5140u));      // dims 0..3 of the word
+      out[2 * k + 1] = lookup(prmt(ev, od, 0x7362u));  // dims 4..7
     }
     d4[i2] = make_uint4(out[0], out[1], out[2], out[3]);
   }
@@ -132,7 +147,7 @@ __device__ __forceinline__ void requant_group(const uint2 (&c)[4], uint16_t sbit
 __global__ __launch_bounds__(kClockThreads) void clock_kernel(ClockArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   allow_dependent_launch();  // the row fetch may be scheduled now; it waits for this grid to finish
-  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b = blockIdx.x, tid = threadIdx.x;
   const int Hs = a.Hs;
   int32_t* s_tok = reinterpret_cast<int32_t*>(smem);
   int32_t* s_use = s_tok + Hs;
@@ -160,21 +175,23 @@ __global__ __launch_bounds__(kClockThreads) void clock_kernel(ClockArgs a) {
   const int32_t step = read_step(a.step);
   auto is_pick = [&](int64_t t) { return t >= S && t < T - W; };
 
-  // The thread's rows i = tid + 512 k: their tokens, then the slots of the
-  // picks, each round of loads issued together (rows beyond 512 * kClockPer
-  // take further rounds).
-  constexpr int kClockPer = kMaxResolveRows / kClockThreads;
-  int32_t tk[kClockPer], sk[kClockPer];
+  // Thread tid owns the contiguous run of rows [tid*run, tid*run + run): its
+  // tokens, then the slots of its picks, each round of loads issued together,
+  // so that one block-wide scan orders the misses.
+  constexpr int kRun = kMaxResolveRows / kClockThreads;
+  const int run = (n + kClockThreads - 1) / kClockThreads;
+  const int i0 = tid * run;
+  int32_t tk[kRun], sk[kRun];
   int picks_local = 0;
 #pragma unroll
-  for (int k = 0; k < kClockPer; k++) {
-    const int i = tid + k * kClockThreads;
-    tk[k] = i < n ? idx[i] : -1;
+  for (int k = 0; k < kRun; k++) {
+    const int i = i0 + k;
+    tk[k] = k < run && i < n ? idx[i] : -1;
   }
 #pragma unroll
-  for (int k = 0; k < kClockPer; k++) {
+  for (int k = 0; k < kRun; k++) {
     const int64_t t = tk[k];
-    const bool pk = tid + k * kClockThreads < n && t >= 0 && t < T && is_pick(t);
+    const bool pk = k < run && i0 + k < n && t >= 0 && t < T && is_pick(t);
     picks_local += pk;
     sk[k] = pk ? tslot[t] : -1;
   }
@@ -191,103 +208,112 @@ __global__ __launch_bounds__(kClockThreads) void clock_kernel(ClockArgs a) {
   __syncthreads();
 
   // Phase 1: sinks, tail and hits; misses listed in ascending token order.
-  int nm = 0;
+  int miss_local = 0;
+  uint32_t miss_bits = 0u;
 #pragma unroll
-  for (int k = 0; k < kClockPer; k++) {
-    if (k * kClockThreads >= n) break;  // the same in every thread
-    const int i = tid + k * kClockThreads;
-    int miss = 0;
-    int64_t t = -1;
-    if (i < n) {
-      t = tk[k];
-      if (t < 0 || t >= T) {
-        set_status(a.status, SKV_DEV_RANGE);
-        rows[i] = -1;
-      } else if (t < S) {
-        rows[i] = static_cast<int32_t>(t);
-      } else if (t >= T - W) {
-        rows[i] = static_cast<int32_t>(S + t % W);
-      } else if (!fits) {
-        rows[i] = -1;
+  for (int k = 0; k < kRun; k++) {
+    const int i = i0 + k;
+    if (k >= run || i >= n) continue;
+    const int64_t t = tk[k];
+    if (t < 0 || t >= T) {
+      set_status(a.status, SKV_DEV_RANGE);
+      rows[i] = -1;
+    } else if (t < S) {
+      rows[i] = static_cast<int32_t>(t);
+    } else if (t >= T - W) {
+      rows[i] = static_cast<int32_t>(S + t % W);
+    } else if (!fits) {
+      rows[i] = -1;
+    } else {
+      const int32_t s = sk[k];
+      if (s >= 0 && s < Hs) {
+        s_ref[s] = 1;
+        s_use[s] = step;
+        rows[i] = S + W + s;
       } else {
-        const int32_t s = sk[k];
-        if (s >= 0 && s < Hs) {
-          s_ref[s] = 1;
-          s_use[s] = step;
-          rows[i] = S + W + s;
-        } else {
-          if (s >= Hs) set_status(a.status, SKV_DEV_RANGE);
-          rows[i] = -1;
-          miss = 1;
-        }
+        if (s >= Hs) set_status(a.status, SKV_DEV_RANGE);
+        rows[i] = -1;
+        miss_bits |= 1u << k;
+        miss_local++;
       }
     }
-    int tot;
-    const int ex = block_exclusive_scan(miss, scr, &tot);
-    if (miss) {
-      m_tok[nm + ex] = static_cast<int32_t>(t);
-      m_pos[nm + ex] = i;
-      m_slot[nm + ex] = -1;
+  }
+  int nm;
+  int mo = block_exclusive_scan(miss_local, scr, &nm);
+#pragma unroll
+  for (int k = 0; k < kRun; k++) {
+    if (miss_bits & (1u << k)) {
+      m_tok[mo] = tk[k];
+      m_pos[mo] = i0 + k;
+      m_slot[mo] = -1;
+      mo++;
     }
-    nm += tot;
   }
   __syncthreads();
 
-  // Phase 2: one warp sweeps the hand over windows of 32 slots.  In lane order
-  // a window is exactly the sequence the one-slot-at-a-time sweep would visit:
-  // used slots are skipped, empty or ref == 0 slots are taken (up to the
-  // number of misses left), ref == 1 slots passed by the hand are cleared.
-  if (warp == 0 && nm > 0) {
+  // Phase 2: the hand sweeps windows of up to 512 slots, all threads at once.
+  // Visiting slots in order from the hand, the one-slot-at-a-time CLOCK skips
+  // slots used in this step, takes slots that are empty or have ref == 0 (one
+  // per remaining miss), and clears the ref bit of the others; so within a
+  // window the first m candidates are taken (m = misses left), the ref bits
+  // of the non-candidates before the last taken slot are cleared, and the
+  // hand stops after it.  A window without enough candidates takes all of
+  // them, clears every ref bit it passes and hands over to the next window.
+  if (nm > 0) {
+    __shared__ int s_hand, s_last;
     int h = a.hand[b];
     if (h < 0 || h >= Hs) {
-      if (lane == 0) set_status(a.status, SKV_DEV_RANGE);
+      if (tid == 0) set_status(a.status, SKV_DEV_RANGE);
       h = 0;
     }
-    const int w = Hs < 32 ? Hs : 32;
-    const int64_t limit = 3 * static_cast<int64_t>(Hs) + 64;  // two turns always suffice
+    const int win = Hs < kClockThreads ? Hs : kClockThreads;
+    const int64_t limit = 3 * static_cast<int64_t>(Hs) + 2 * kClockThreads;  // two turns always suffice
     int64_t moved = 0;
-    int j = 0;
+    int j = 0;  // misses placed so far (the same in every thread)
     while (j < nm) {
       if (moved > limit) {
-        if (lane == 0) set_status(a.status, SKV_DEV_COUNT);
+        if (tid == 0) set_status(a.status, SKV_DEV_COUNT);
         break;
       }
-      const bool act = lane < w;
-      int s = h + lane;
+      const bool act = tid < win;
+      int s = h + tid;
       if (s >= Hs) s -= Hs;
       const bool used = act && s_use[s] == step;
       const int32_t st = act ? s_tok[s] : 0;
-      const bool r1 = act && s_ref[s] != 0;
-      const bool cand = act && !used && (st < 0 || !r1);
-      const unsigned mask = __ballot_sync(0xffffffffu, cand);
+      const bool cand = act && !used && (st < 0 || s_ref[s] == 0);
+      int total;
+      const int rank = block_exclusive_scan(cand ? 1 : 0, scr, &total);
       const int need = nm - j;
-      int pass = w;
-      if (__popc(mask) >= need) {
-        unsigned mm = mask;
-        for (int k = 1; k < need; k++) mm &= mm - 1;
-        pass = __ffs(mm);
+      // position of the last slot the hand visits in this window
+      if (tid == 0) s_last = win - 1;
+      __syncthreads();
+      if (total >= need && cand && rank == need - 1) s_last = tid;
+      __syncthreads();
+      const int last = s_last;
+      if (act && tid <= last) {
+        if (cand && rank < need) {
+          const int jj = j + rank;
+          const int32_t tok = m_tok[jj];
+          if (st >= 0 && st < a.t_cap) tslot[st] = -1;
+          s_tok[s] = tok;
+          tslot[tok] = s;
+          s_ref[s] = 1;
+          s_use[s] = step;
+          m_slot[jj] = s;
+          rows[m_pos[jj]] = S + W + s;
+        } else if (!used && !cand) {
+          s_ref[s] = 0;
+        }
       }
-      const bool in = lane < pass;
-      if (in && act && !used && !cand) s_ref[s] = 0;
-      if (in && cand) {
-        const int jj = j + __popc(mask & ((1u << lane) - 1u));
-        const int32_t tok = m_tok[jj];
-        if (st >= 0 && st < a.t_cap) tslot[st] = -1;
-        s_tok[s] = tok;
-        tslot[tok] = s;
-        s_ref[s] = 1;
-        s_use[s] = step;
-        m_slot[jj] = s;
-        rows[m_pos[jj]] = S + W + s;
-      }
-      const unsigned low = pass >= 32 ? 0xffffffffu : ((1u << pass) - 1u);
-      j += __popc(mask & low);
-      h += pass;
+      j += total < need ? total : need;
+      h += last + 1;
       if (h >= Hs) h -= Hs;
-      moved += pass;
-      __syncwarp();
+      moved += last + 1;
+      __syncthreads();  // the window's state changes are visible to the next window
     }
-    if (lane == 0) a.hand[b] = h;
+    if (tid == 0) s_hand = h;
+    __syncthreads();
+    if (tid == 0) a.hand[b] = s_hand;
   }
   __syncthreads();
 
@@ -661,6 +687,34 @@ __global__ __launch_bounds__(256) void quant_int4_kernel(const uint16_t* __restr
   }
 }
 
+// Gather read: one warp per listed row (rows[i] * row_bytes from `base`,
+// HBM or a host alias), every 16-byte load of the row issued before any is
+// used; the XOR of the words goes to *sink.  The probe for reads of
+// scattered rows, the access pattern of the host-tier fetches.
+__global__ __launch_bounds__(256) void gather_read_kernel(const uint8_t* __restrict__ base,
+                                                          const int64_t* __restrict__ rows, int n, int64_t row_bytes,
+                                                          unsigned long long* sink) {
+  const int64_t wid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (wid >= n) return;
+  const uint4* src = reinterpret_cast<const uint4*>(base + rows[wid] * row_bytes);
+  const int chunks = static_cast<int>(row_bytes / 16);
+  uint32_t acc = 0;
+  uint4 v[kFetchPieces];
+#pragma unroll
+  for (int u = 0; u < kFetchPieces; u++)
+    v[u] = lane + 32 * u < chunks ? ld_stream16(src + lane + 32 * u) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+  for (int u = 0; u < kFetchPieces; u++) acc ^= v[u].x ^ v[u].y ^ v[u].z ^ v[u].w;
+  for (int c = lane + 32 * kFetchPieces; c < chunks; c += 32) {
+    const uint4 x = ld_stream16(src + c);
+    acc ^= x.x ^ x.y ^ x.z ^ x.w;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc ^= __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0 && acc == 0x9e3779b9u) atomicAdd(sink, 1ull);  // keeps the loads; almost never taken
+}
+
 // Streaming read of a buffer (HBM or a host alias) with 16-byte loads; the
 // XOR of every word goes to *sink so the loads cannot be dropped.
 __global__ __launch_bounds__(512) void stream_read_kernel(const uint4* __restrict__ p, int64_t n16,
@@ -839,6 +893,17 @@ SKV_EXPORT int skv_quantize_int4_rows(const uint16_t* x, int64_t n_rows, int Hkv
   if (grid > cap && cap > 0) grid = cap;
   quant_int4_kernel<<<static_cast<int>(grid), 256, 0, as_stream(stream)>>>(x, items, Hkv, d, out_rows, out,
                                                                             token_pitch, head_pitch);
+  return launch_status();
+}
+
+SKV_EXPORT int skv_gather_read(const void* base, const int64_t* rows, int n, int64_t row_bytes,
+                               unsigned long long* sink, void* stream) {
+  if (!base || !rows || !sink || n < 0 || row_bytes < 16 || row_bytes % 16 || !aligned16(base)) return SKV_EINVAL;
+  if (n == 0) return SKV_OK;
+  const int64_t blocks = (static_cast<int64_t>(n) * 32 + 255) / 256;
+  if (blocks > INT32_MAX) return SKV_EINVAL;
+  gather_read_kernel<<<static_cast<int>(blocks), 256, 0, as_stream(stream)>>>(static_cast<const uint8_t*>(base), rows,
+                                                                             n, row_bytes, sink);
   return launch_status();
 }
 

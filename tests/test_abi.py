@@ -57,6 +57,11 @@ def test_host_side_argument_checks(lib):
     assert lib.skv_pool_keys(P(16), 0, 64, 128, 4, 0, 4, P(16), None) == 0
     assert lib.skv_pool_keys(P(16), 1, 64, 128, 4, 10, 8, P(16), None) == 1  # past capacity
     assert lib.skv_topk_workspace_size(8) > 0
+    # gather probe: rows of a multiple of 16 bytes from an aligned base; none is a no-op
+    assert lib.skv_gather_read(P(16), P(16), 4, 24, P(16), None) == 1
+    assert lib.skv_gather_read(P(8), P(16), 4, 32, P(16), None) == 1
+    assert lib.skv_gather_read(P(16), P(16), -1, 32, P(16), None) == 1
+    assert lib.skv_gather_read(P(16), P(16), 0, 32, P(16), None) == 0
 
 
 def test_prefill_argument_checks(lib):

@@ -278,3 +278,23 @@ def test_lru_too_few_slots_is_flagged(skv):
     assert int(nmiss.item()) == -1
     assert (T.host(rows) == -1).all()
     assert (T.host(pool) == 0).all()
+
+
+def test_gather_read_probe_runs_on_device_and_host_memory(skv):
+    """The scattered-row read probe runs over device memory and over a
+    registered host tier and leaves the status clean."""
+    import mmap
+    rows = torch.tensor([5, 0, 99, 37, 12], dtype=torch.int64, device="cuda")
+    sink = torch.zeros((1,), dtype=torch.int64, device="cuda")
+    dev_buf = torch.zeros((100 * 1088,), dtype=torch.uint8, device="cuda")
+    skv.gather_read(dev_buf, rows, 1088, sink)
+    nbytes = 100 * 1088
+    mm = mmap.mmap(-1, nbytes)
+    harr = np.frombuffer(mm, dtype=np.uint8, count=nbytes)
+    harr[:] = 7
+    alias = skv.host_register(harr.ctypes.data, nbytes)
+    try:
+        skv.gather_read(alias, rows, 1088, sink)
+        torch.cuda.synchronize()
+    finally:
+        skv.host_unregister(harr.ctypes.data)
