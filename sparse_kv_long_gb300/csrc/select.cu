@@ -485,22 +485,42 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
   // Each CTA also publishes suffix counts rec[d] = (its keys above the prefix)
   // + (its keys in bins >= d), d = 0..nbf, so that a later CTA gets the keys
   // above K* and equal to K* of every earlier chunk from two words each.
+  // Each warp histograms its own contiguous piece of the chunk (the piece it
+  // writes the picks of in step 4), so that once K* is known its counts of
+  // keys above and equal to K* come from its bins, without another pass over
+  // the keys; the CTA's bins are the warps' summed.
   constexpr int nbf = kLastBins;  // wlast == kLastBits: bits >= 21 in every mode
-  for (int i = threadIdx.x; i < nbf; i += blockDim.x) hist[i] = 0u;
-  if (threadIdx.x == 0) s_above = 0u;
+  uint32_t* whist = hist + nbf;   // [kWarpsF][nbf]
+  static_assert(nbf * (kWarpsF + 1) <= kBins, "per-warp bins fit in the histogram buffer");
+  for (int i = threadIdx.x; i < nbf * (kWarpsF + 1); i += blockDim.x) hist[i] = 0u;
   __syncthreads();
+  const int sub = ((len + kWarpsF - 1) / kWarpsF + 31) / 32 * 32;  // warp v owns [v*sub, (v+1)*sub)
+  const int p0 = min(len, warp * sub), p1 = min(len, p0 + sub);
+  uint32_t* myh = whist + warp * nbf;
   unsigned above_local = 0u;
-  for (int i = threadIdx.x; i < len; i += blockDim.x) {
+  for (int i = p0 + lane; i < p1; i += 32) {
     const uint32_t rel = skey[i] - base;
     const uint32_t t = rel >> wlast;
     if (t == P)
-      atomicAdd(&hist[rel & static_cast<uint32_t>(nbf - 1)], 1u);
+      atomicAdd(&myh[rel & static_cast<uint32_t>(nbf - 1)], 1u);
     else if (t > P)
       above_local++;
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) above_local += __shfl_xor_sync(0xffffffffu, above_local, o);
-  if (lane == 0 && above_local) atomicAdd(&s_above, above_local);
+  if (lane == 0) wgt[warp] = static_cast<int>(above_local);
+  __syncthreads();
+  for (int d = threadIdx.x; d < nbf; d += blockDim.x) {
+    unsigned sum = 0u;
+#pragma unroll
+    for (int v = 0; v < kWarpsF; v++) sum += whist[v * nbf + d];
+    hist[d] = sum;
+  }
+  if (threadIdx.x == 0) {
+    unsigned tot = 0u;
+    for (int v = 0; v < kWarpsF; v++) tot += static_cast<unsigned>(wgt[v]);
+    s_above = tot;
+  }
   __syncthreads();
   unsigned* gf = w.fhist(b);
   int* myfin = w.fin(b, c);
@@ -578,23 +598,24 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
   }
 
   // ---- 4. this CTA's picks, in ascending index order ---------------------------------
-  // Warp v owns the contiguous piece [v*sub, (v+1)*sub) of the chunk.
-  const int sub = ((len + kWarpsF - 1) / kWarpsF + 31) / 32 * 32;
-  const int p0 = warp * sub, p1 = min(len, p0 + sub);
-  int ngt = 0, neq = 0;
-  for (int i = p0 + lane; i < p1; i += 32) {
-    const uint32_t key = skey[i];
-    ngt += key > kstar;
-    neq += key == kstar;
-  }
+  // Warp v owns the contiguous piece [v*sub, (v+1)*sub) of the chunk; its
+  // keys above K* are those above the prefix plus those in its bins above
+  // d*, its keys equal to K* those in bin d*.
+  {
+    int ngt = 0;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    ngt += __shfl_xor_sync(0xffffffffu, ngt, o);
-    neq += __shfl_xor_sync(0xffffffffu, neq, o);
-  }
-  if (lane == 0) {
-    wgt[warp] = ngt;
-    weq[warp] = neq;
+    for (int j = 0; j < nbf / 32; j++) {
+      const int d = lane * (nbf / 32) + j;
+      if (d > static_cast<int>(dstar)) ngt += static_cast<int>(myh[d]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ngt += __shfl_xor_sync(0xffffffffu, ngt, o);
+    const int neq = static_cast<int>(myh[dstar]);
+    __syncwarp();
+    if (lane == 0) {
+      wgt[warp] += ngt;  // keys above the prefix were counted in the final pass
+      weq[warp] = neq;
+    }
   }
   __syncthreads();
   const int needi = static_cast<int>(need_eq);
