@@ -19,10 +19,14 @@
 //      bits) histograms the keys still matching the prefix, adds the bins to
 //      the request's global histogram, and after a request-wide barrier every
 //      CTA derives the same digit (the first pass reads back only windows of
-//      bins below the highest occupied one);
+//      bins below the highest occupied one, the first of them guessed from
+//      the CTA's own top bin and read in the same round trip as the
+//      request's);
 //   4. the final pass (8 bits) adds its bins to a request-wide histogram and
 //      publishes per-CTA suffix counts (keys above the prefix plus keys in
-//      bins >= d, for every d); after one barrier every CTA knows the exact
+//      bins >= d, for every d); once every CTA has arrived -- the poll reads
+//      the request's bins with the arrival count, and they are complete when
+//      they sum to the keys matching the prefix -- every CTA knows the exact
 //      k-th key K*, how many keys equal to K* are taken, and -- from two
 //      counts per earlier chunk -- where its own picks go; it writes them in
 //      ascending index order (equal keys: lowest index first).
@@ -49,6 +53,8 @@ constexpr long kSpinLimit = 1L << 21;            // bounded barrier polls (well 
 constexpr size_t kKeyBudget = 96 * 1024;         // shared memory for the chunk's order keys
 constexpr uint32_t kInt4Base = 0x80000000u - (1u << 20);  // order key of score -2^20
 constexpr int kWin = 1024;                                 // bins read back per window (int4 first pass)
+constexpr int kAhead = 256;                                // first window: bins above the CTA's own top
+constexpr uint32_t kUnknown = 0xffffffffu;                 // keys matching the prefix: not counted
 
 // Scratch of one request, at a fixed stride whatever B is, so that one
 // zero-filled workspace serves calls with any number of requests: the words
@@ -235,6 +241,15 @@ __device__ void req_barrier(unsigned* arrive, unsigned target, int32_t* status) 
   __syncthreads();
 }
 
+__device__ __forceinline__ uint4 ld_relaxed_v4(const unsigned* p) {
+  uint4 v;
+  asm volatile("ld.relaxed.gpu.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
+
 // rel >> sh, with a shift of 32 giving 0.
 __device__ __forceinline__ uint32_t top_bits(uint32_t rel, int sh) { return sh >= 32 ? 0u : rel >> sh; }
 
@@ -377,7 +392,8 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
   // ---- 2. non-final radix passes ---------------------------------------------------
   // int32 keys: one (13 bits, windowed); fp32 keys: two (13 windowed, 11).
   uint32_t need = static_cast<uint32_t>(a.k);
-  uint32_t P = 0;  // rel >> rem of the keys still in play
+  uint32_t P = 0;         // rel >> rem of the keys still in play
+  uint32_t n_match = kUnknown;  // the request's keys matching P
   int rem = bits;
   const int wlast = bits < kLastBits ? bits : kLastBits;
   int pass = 0;
@@ -413,14 +429,50 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
       __syncthreads();
       if (threadIdx.x == 0 && s_top) atomicMax(w.rng(b), s_top);  // bin + 1 (0: none)
     }
+    // The request's highest bin is rarely far above this CTA's own: the first
+    // window is read around the local top, in the same round trip as the
+    // request's top, and kept when it covers that top and `need` keys.
+    const int guess_hi = windowed && s_top ? min(nb - 1, static_cast<int>(s_top) - 1 + kAhead) : -1;
     req_barrier(arrive, ++nbar * C, a.status);
     if (windowed) {
-      // Windows of kWin bins from the top down until `need` keys are covered.
-      const unsigned gtop = __ldcg(w.rng(b));
-      int hi = static_cast<int>(gtop) - 1;  // highest occupied bin
       unsigned need_rem = need, above_acc = 0u;
       uint32_t dig = 0u, abv = 0u;
       bool found = false;
+      const int g_lo = guess_hi >= kWin - 1 ? guess_hi - (kWin - 1) : 0;
+      const int g_n = guess_hi - g_lo + 1;  // 0 without a guess
+      const unsigned gtop = __ldcg(w.rng(b));
+      {
+        unsigned v[kWin / kThreads];
+#pragma unroll
+        for (int j = 0; j < kWin / kThreads; j++) {
+          const int i = threadIdx.x + j * kThreads;
+          v[j] = i < g_n ? __ldcg(&gh[g_lo + i]) : 0u;
+        }
+        unsigned part = 0u;
+#pragma unroll
+        for (int j = 0; j < kWin / kThreads; j++) {
+          const int i = threadIdx.x + j * kThreads;
+          if (i < g_n) hist[i] = v[j];
+          part += v[j];
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+        if (lane == 0) red_a[warp] = part;
+        __syncthreads();
+        unsigned total = 0u;
+        for (int v2 = 0; v2 < kWarpsF; v2++) total += red_a[v2];
+        if (g_n > 0 && static_cast<int>(gtop) - 1 <= guess_hi && total >= need_rem) {  // the same in every thread
+          find_digit(hist, g_n, need_rem, &s_digit, &s_above, a.status);
+          dig = s_digit + static_cast<uint32_t>(g_lo);
+          abv = s_above;
+          n_match = hist[s_digit];
+          found = true;
+        }
+        __syncthreads();  // hist and red_a are rewritten below
+      }
+      // Otherwise windows of kWin bins from the request's top down until
+      // `need` keys are covered.
+      int hi = found ? -1 : static_cast<int>(gtop) - 1;  // highest occupied bin
       while (hi >= 0) {
         const int lo_bin = hi >= kWin - 1 ? hi - (kWin - 1) : 0;
         const int nw = hi - lo_bin + 1;
@@ -438,6 +490,7 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
           find_digit(hist, nw, need_rem, &s_digit, &s_above, a.status);
           dig = s_digit + static_cast<uint32_t>(lo_bin);
           abv = s_above + above_acc;
+          n_match = hist[s_digit];
           found = true;
           break;
         }
@@ -474,6 +527,7 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
     }
     __syncthreads();
     find_digit(hist, nb, need, &s_digit, &s_above, a.status);
+    n_match = hist[s_digit];
     P = (P << wb) | s_digit;
     need -= s_above;
     rem = shift;
@@ -548,8 +602,39 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
     }
     if (lane == 0) myfin[nbf] = static_cast<int>(s_above);
   }
-  req_barrier(arrive, ++nbar * C, a.status);
-  for (int i = threadIdx.x; i < nbf; i += blockDim.x) hist[i] = __ldcg(&gf[i]);
+  // Arrive, then poll the request's final bins with the arrival count: the
+  // bins are complete once they sum to the request's keys matching P (they
+  // only grow), and every CTA's record is visible once all have arrived.
+  __syncthreads();
+  if (warp == 0) {
+    const unsigned target = ++nbar * C;
+    if (lane == 0) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(arrive) : "memory");
+    uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
+    bool ok = false;
+    for (long it = 0; it < kSpinLimit; it++) {
+      unsigned arr = 0u;
+      if (lane == 0) asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(arr) : "l"(arrive) : "memory");
+      v0 = ld_relaxed_v4(gf + 8 * lane);
+      v1 = ld_relaxed_v4(gf + 8 * lane + 4);
+      unsigned sum = v0.x + v0.y + v0.z + v0.w + v1.x + v1.y + v1.z + v1.w;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      arr = __shfl_sync(0xffffffffu, arr, 0);
+      if (arr >= target && (n_match == kUnknown || sum == n_match)) {
+        ok = true;
+        break;
+      }
+      if (it > 64) __nanosleep(32);
+    }
+    __threadfence();  // acquire: the records of every CTA
+    if (n_match == kUnknown) {
+      v0 = ld_relaxed_v4(gf + 8 * lane);
+      v1 = ld_relaxed_v4(gf + 8 * lane + 4);
+    }
+    reinterpret_cast<uint4*>(hist)[2 * lane] = v0;
+    reinterpret_cast<uint4*>(hist)[2 * lane + 1] = v1;
+    if (!ok && lane == 0) set_status(a.status, SKV_DEV_TIMEOUT);
+  }
   __syncthreads();
   find_digit(hist, nbf, need, &s_digit, &s_above, a.status);
   const uint32_t dstar = s_digit;
@@ -574,27 +659,15 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
     atomicAdd(&s_before[0], gb);
     atomicAdd(&s_before[1], eb);
   }
-  // This CTA is done with everything the request's CTAs published.  The last
-  // CTA to get here clears the window cells, the histograms and the
-  // counters, so the workspace is ready for the next launch.
-  __shared__ int s_last;
+  // This CTA is done with everything the request's CTAs published: it takes
+  // an exit ticket now and reads it at the end, where the last CTA clears
+  // the window cells, the histograms and the counters, so the workspace is
+  // ready for the next launch.
+  unsigned ticket = 0u;
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
-    s_last = atomicAdd(w.bar(b) + 1, 1u) == static_cast<unsigned>(C - 1);
-  }
-  __syncthreads();
-  if (s_last) {
-    __threadfence();
-    for (int p = 0; p < pass; p++)
-      for (int i = threadIdx.x; i < kBins; i += blockDim.x) w.hist(p, b)[i] = 0u;
-    for (int i = threadIdx.x; i < kLastBins; i += blockDim.x) w.fhist(b)[i] = 0u;
-    if (threadIdx.x == 0) {
-      w.rng(b)[0] = 0u;
-      w.rng(b)[1] = 0u;
-      w.bar(b)[0] = 0u;
-      w.bar(b)[1] = 0u;
-    }
+    ticket = atomicAdd(w.bar(b) + 1, 1u);
   }
 
   // ---- 4. this CTA's picks, in ascending index order ---------------------------------
@@ -659,6 +732,21 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
       for (int i = threadIdx.x; i < rem_tok; i += blockDim.x)
         out[ratio * a.k + i] = static_cast<int32_t>(nbk * ratio + i);
       if (threadIdx.x == 0) a.count[b] = ratio * a.k + rem_tok;
+    }
+  }
+  __shared__ int s_last;
+  if (threadIdx.x == 0) s_last = ticket == static_cast<unsigned>(C - 1);
+  __syncthreads();
+  if (s_last) {
+    __threadfence();
+    for (int p = 0; p < pass; p++)
+      for (int i = threadIdx.x; i < kBins; i += blockDim.x) w.hist(p, b)[i] = 0u;
+    for (int i = threadIdx.x; i < kLastBins; i += blockDim.x) w.fhist(b)[i] = 0u;
+    if (threadIdx.x == 0) {
+      w.rng(b)[0] = 0u;
+      w.rng(b)[1] = 0u;
+      w.bar(b)[0] = 0u;
+      w.bar(b)[1] = 0u;
     }
   }
 }
