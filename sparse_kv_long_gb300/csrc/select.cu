@@ -306,6 +306,7 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
   __shared__ unsigned red_a[kWarpsF];
   __shared__ uint32_t s_digit, s_above, s_top;
   __shared__ int s_before[2];
+  __shared__ int s_ok;
 
   __shared__ __align__(16) int8_t s_q8[512];
   __shared__ float s_red[kWarpsF];
@@ -633,9 +634,20 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
     }
     reinterpret_cast<uint4*>(hist)[2 * lane] = v0;
     reinterpret_cast<uint4*>(hist)[2 * lane + 1] = v1;
-    if (!ok && lane == 0) set_status(a.status, SKV_DEV_TIMEOUT);
+    if (lane == 0) {
+      s_ok = ok;
+      if (!ok) set_status(a.status, SKV_DEV_TIMEOUT);
+    }
   }
   __syncthreads();
+  // Every CTA has read the non-final bins by now (each did before it
+  // arrived): each clears its share of them.
+  if (s_ok) {
+    const int share = (kBins + C - 1) / C;
+    const int i0 = c * share, i1 = min(kBins, i0 + share);
+    for (int p = 0; p < pass; p++)
+      for (int i = i0 + threadIdx.x; i < i1; i += blockDim.x) w.hist(p, b)[i] = 0u;
+  }
   find_digit(hist, nbf, need, &s_digit, &s_above, a.status);
   const uint32_t dstar = s_digit;
   const uint32_t need_eq = need - s_above;  // keys equal to K* that are taken (lowest index first)
@@ -661,7 +673,7 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
   }
   // This CTA is done with everything the request's CTAs published: it takes
   // an exit ticket now and reads it at the end, where the last CTA clears
-  // the window cells, the histograms and the counters, so the workspace is
+  // the window cells, the final bins and the counters, so the workspace is
   // ready for the next launch.
   unsigned ticket = 0u;
   __syncthreads();
@@ -739,8 +751,10 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
   __syncthreads();
   if (s_last) {
     __threadfence();
-    for (int p = 0; p < pass; p++)
-      for (int i = threadIdx.x; i < kBins; i += blockDim.x) w.hist(p, b)[i] = 0u;
+    // after a timed-out wait the shares above may have been cleared too early
+    if (a.status && __ldcg(a.status) != 0)
+      for (int p = 0; p < pass; p++)
+        for (int i = threadIdx.x; i < kBins; i += blockDim.x) w.hist(p, b)[i] = 0u;
     for (int i = threadIdx.x; i < kLastBins; i += blockDim.x) w.fhist(b)[i] = 0u;
     if (threadIdx.x == 0) {
       w.rng(b)[0] = 0u;
