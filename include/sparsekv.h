@@ -275,9 +275,11 @@ int skv_topk_select_noalloc(int B, const uint32_t *order_keys, int64_t n_cap,
  * digit passes skip the bits all keys share.  `order_keys` ([B][n_cap], may be
  * NULL) receives a copy of the keys of the candidates.
  *   workspace  skv_score_select_workspace_size(B) bytes, zero-filled before
- *              first use; each call returns its counters to zero.  Per-request
- *              scratch sits at a fixed stride, so a workspace sized for B_max
- *              serves later calls with any B <= B_max, in any order.
+ *              first use; each call returns its counters to zero and advances
+ *              a per-request launch counter (the tag of the per-CTA records it
+ *              writes).  Per-request scratch sits at a fixed stride, so a
+ *              workspace sized for B_max serves later calls with any B <=
+ *              B_max, in any order.
  * Errors: as skv_index_score and skv_topk_select; SKV_EUNSUPPORTED when B is
  * larger than the GPU can hold one resident CTA per request for, or when a
  * request's chunk of keys does not fit on chip (more than about 24K rows per

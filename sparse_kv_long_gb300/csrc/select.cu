@@ -59,15 +59,18 @@ constexpr uint32_t kUnknown = 0xffffffffu;                 // keys matching the 
 // Scratch of one request, at a fixed stride whatever B is, so that one
 // zero-filled workspace serves calls with any number of requests: the words
 // that must start at zero (barrier counters, the range word, histograms) are
-// returned to zero by the request's last CTA, and the per-CTA records are
-// written before they are read.
+// returned to zero by the request's CTAs before the launch ends, the epoch
+// only grows (its tag never takes the value 0 of a fresh workspace), and a
+// per-CTA record word is read only once it carries this launch's tag.
 //   bar   [2]              arrivals (monotonic within a launch), exits
-//   rng   [2]              highest occupied first-pass bin + 1, pad
+//   rng   [2]              highest occupied first-pass bin + 1, launch epoch
 //   hist  [2][kBins]       non-final passes
 //   fhist [kLastBins]      final pass, request-wide bins
-//   fin   [kCMax][kFin]    final pass, per-CTA suffix counts
+//   fin   [kCMax][kFin]    final pass, per-CTA suffix counts, each word tagged
+//                          with the launch epoch (high 16 bits)
 constexpr size_t kReqWords = 4 + 2ull * kBins + kLastBins + static_cast<size_t>(kCMax) * kFin;
 static_assert(kReqWords % 4 == 0, "request blocks stay 16-byte aligned");
+static_assert(kKeyBudget / 4 < 65536, "a CTA's counts fit the 16 low bits of a tagged record word");
 
 struct Ws {
   unsigned* base;
@@ -241,6 +244,12 @@ __device__ void req_barrier(unsigned* arrive, unsigned target, int32_t* status) 
   __syncthreads();
 }
 
+__device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ uint4 ld_relaxed_v4(const unsigned* p) {
   uint4 v;
   asm volatile("ld.relaxed.gpu.global.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -300,7 +309,7 @@ __device__ void find_digit(const uint32_t* h, int nb, uint32_t need, uint32_t* d
 
 template <int MODE, int LPT>
 __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w) {
-  extern __shared__ uint32_t skey[];
+  extern __shared__ __align__(16) uint32_t skey[];
   __shared__ __align__(16) uint32_t hist[kBins];
   __shared__ int wgt[kWarpsF], weq[kWarpsF];
   __shared__ unsigned red_a[kWarpsF];
@@ -337,6 +346,11 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
     if (c == 0 && threadIdx.x == 0) a.count[b] = static_cast<int32_t>(T);
     return;
   }
+  // The request's launch epoch: bumped by the last CTA of each launch, so
+  // every CTA of this launch reads the same value.  Its tag marks the words
+  // of this launch's final records.
+  const unsigned epoch = __ldcg(w.rng(b) + 1);
+  const unsigned tag = (epoch % 65535u + 1u) << 16;
   const int64_t lo = pooled ? 0 : a.S;
   const int64_t hi = pooled ? T / ratio : T - a.W;
   const int64_t chunk = (hi - lo + C - 1) / C;
@@ -552,14 +566,31 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
   const int sub = ((len + kWarpsF - 1) / kWarpsF + 31) / 32 * 32;  // warp v owns [v*sub, (v+1)*sub)
   const int p0 = min(len, warp * sub), p1 = min(len, p0 + sub);
   uint32_t* myh = whist + warp * nbf;
+  // Four keys per lane per step: the tail of the launch runs every warp of
+  // the SM at once, so instructions per key count.
   unsigned above_local = 0u;
-  for (int i = p0 + lane; i < p1; i += 32) {
-    const uint32_t rel = skey[i] - base;
-    const uint32_t t = rel >> wlast;
-    if (t == P)
-      atomicAdd(&myh[rel & static_cast<uint32_t>(nbf - 1)], 1u);
-    else if (t > P)
-      above_local++;
+  for (int i0 = p0; i0 < p1; i0 += 128) {
+    const int i = i0 + 4 * lane;
+    uint32_t k4[4];
+    if (i + 3 < p1) {
+      const uint4 v = *reinterpret_cast<const uint4*>(&skey[i]);
+      k4[0] = v.x;
+      k4[1] = v.y;
+      k4[2] = v.z;
+      k4[3] = v.w;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; j++) k4[j] = i + j < p1 ? skey[i + j] : base;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+      const uint32_t rel = k4[j] - base;
+      const uint32_t t = rel >> wlast;
+      if (t == P && i + j < p1)
+        atomicAdd(&myh[rel & static_cast<uint32_t>(nbf - 1)], 1u);
+      else if (t > P)
+        above_local++;
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) above_local += __shfl_xor_sync(0xffffffffu, above_local, o);
@@ -599,17 +630,18 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
 #pragma unroll
     for (int j = kPerLane - 1; j >= 0; j--) {
       acc += v[j];
-      myfin[kPerLane * lane + j] = static_cast<int>(acc);
+      myfin[kPerLane * lane + j] = static_cast<int>(tag | acc);
     }
-    if (lane == 0) myfin[nbf] = static_cast<int>(s_above);
+    if (lane == 0) myfin[nbf] = static_cast<int>(tag | s_above);
   }
   // Arrive, then poll the request's final bins with the arrival count: the
   // bins are complete once they sum to the request's keys matching P (they
-  // only grow), and every CTA's record is visible once all have arrived.
+  // only grow).  No release fence: the records the CTAs read next carry the
+  // epoch tag in every word and are checked word by word.
   __syncthreads();
   if (warp == 0) {
     const unsigned target = ++nbar * C;
-    if (lane == 0) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(arrive) : "memory");
+    if (lane == 0) asm volatile("red.relaxed.gpu.global.add.u32 [%0], 1;" ::"l"(arrive) : "memory");
     uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
     bool ok = false;
     for (long it = 0; it < kSpinLimit; it++) {
@@ -627,7 +659,6 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
       }
       if (it > 64) __nanosleep(32);
     }
-    __threadfence();  // acquire: the records of every CTA
     if (n_match == kUnknown) {
       v0 = ld_relaxed_v4(gf + 8 * lane);
       v1 = ld_relaxed_v4(gf + 8 * lane + 4);
@@ -655,10 +686,21 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
   // keys of the chunks before this one: above K*, and equal to K*
   int gb = 0, eb = 0;
   for (int cc = threadIdx.x; cc < c; cc += blockDim.x) {
-    const int* rf = w.fin(b, cc);
-    const int above_d = __ldcg(&rf[dstar + 1]);
+    const unsigned* rf = reinterpret_cast<const unsigned*>(w.fin(b, cc));
+    unsigned x1 = 0u, x0 = 0u;
+    for (long it = 0;; it++) {  // both words from this launch (bounded poll)
+      x1 = ld_relaxed_u32(&rf[dstar + 1]);
+      x0 = ld_relaxed_u32(&rf[dstar]);
+      if ((x1 & 0xffff0000u) == tag && (x0 & 0xffff0000u) == tag) break;
+      if (it >= kSpinLimit) {
+        set_status(a.status, SKV_DEV_TIMEOUT);
+        break;
+      }
+      if (it > 64) __nanosleep(32);
+    }
+    const int above_d = static_cast<int>(x1 & 0xffffu);
     gb += above_d;
-    eb += __ldcg(&rf[dstar]) - above_d;
+    eb += static_cast<int>(x0 & 0xffffu) - above_d;
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -677,9 +719,9 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
   // ready for the next launch.
   unsigned ticket = 0u;
   __syncthreads();
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0) {  // the high half counts CTAs whose final poll ran out
     __threadfence();
-    ticket = atomicAdd(w.bar(b) + 1, 1u);
+    ticket = atomicAdd(w.bar(b) + 1, s_ok ? 1u : 0x10001u);
   }
 
   // ---- 4. this CTA's picks, in ascending index order ---------------------------------
@@ -715,6 +757,8 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
   for (int bb = p0; bb < p1; bb += 32) {
     const int i = bb + lane;
     const uint32_t key = i < p1 ? skey[i] : 0u;
+    // most blocks of 32 keys hold no key >= K*: one vote skips them
+    if (!__any_sync(0xffffffffu, i < p1 && key >= kstar)) continue;
     const bool gt = i < p1 && key > kstar;
     const bool eq = i < p1 && key == kstar;
     const unsigned eqb = __ballot_sync(0xffffffffu, eq);
@@ -747,18 +791,19 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
     }
   }
   __shared__ int s_last;
-  if (threadIdx.x == 0) s_last = ticket == static_cast<unsigned>(C - 1);
+  if (threadIdx.x == 0)
+    s_last = (ticket & 0xffffu) != static_cast<unsigned>(C - 1) ? 0 : (ticket >> 16) == 0u && s_ok ? 1 : 2;
   __syncthreads();
   if (s_last) {
     __threadfence();
-    // after a timed-out wait the shares above may have been cleared too early
-    if (a.status && __ldcg(a.status) != 0)
+    // after a poll that ran out the shares above may have been cleared early
+    if (s_last == 2)
       for (int p = 0; p < pass; p++)
         for (int i = threadIdx.x; i < kBins; i += blockDim.x) w.hist(p, b)[i] = 0u;
     for (int i = threadIdx.x; i < kLastBins; i += blockDim.x) w.fhist(b)[i] = 0u;
     if (threadIdx.x == 0) {
       w.rng(b)[0] = 0u;
-      w.rng(b)[1] = 0u;
+      w.rng(b)[1] = epoch + 1u;
       w.bar(b)[0] = 0u;
       w.bar(b)[1] = 0u;
     }
