@@ -23,7 +23,10 @@
 // logits of its half with m16n8k16 tensor-core MMAs (query heads are the M
 // rows, padded to 16; two n8 tiles cover the 16 rows); the halves are
 // exchanged through shared memory and added in a fixed order, so both warps
-// run the same online softmax on bit-identical logits; each then accumulates
+// run the same online softmax on bit-identical logits (its reference max
+// moves only when a tile's logits pass it by more than 2^4 in probability,
+// so most tiles rescale nothing; the rows' factors are read before the
+// tile's copies land); each then accumulates
 // its half of O^T += V^T P^T with the probabilities reused from the
 // accumulators as the B operand.  The head dimension is permuted consistently
 // on Q and K so that a lane reads contiguous 16-byte pieces of a row; the V
@@ -60,6 +63,10 @@ constexpr int kMaxRowsPerSplit = 512;
 constexpr int kStages = 3;
 constexpr int kTileRows = 16;
 constexpr long kWaitLimit = 1L << 20;  // bounded mbarrier polls (~1 s with backoff)
+// Lazy softmax rescaling: probabilities of a tile may reach 2^kLazy before
+// the reference max moves (int8 rows fold the V scale into them in fp16, so
+// this bounds p * v_scale by 16 * v_scale).
+constexpr float kLazy = 4.f;
 // Pair partials in shared memory: float (head, dim) at head*kMH + (dim/32)*33 +
 // dim%32, so the fragment-order stores of a warp hit 32 different banks.
 constexpr int kMH = 8 * 33 + 4;
@@ -395,6 +402,19 @@ __global__ __launch_bounds__(kThreads, 2) void attend_kernel(AttendArgs a) {
   auto attend_tile = [&](int it) -> bool {
     const int stage = it % kStages;
     const uint32_t parity = (it / kStages) & 1;
+    const int tbase = (pair + kPairs * it) * kTileRows;  // index of the tile's first row in the split
+    // This lane's rows' logit factors and V scales (0: no row), read while
+    // the tile's copies are still landing.
+    const int rr[4] = {2 * c, 2 * c + 1, 2 * c + 8, 2 * c + 9};
+    float fx[4], vsc[4];
+    bool okr[4];
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+      const int idx = tbase + rr[i];
+      okr[i] = idx < nr && s_prow[idx] >= 0;
+      fx[i] = okr[i] ? (KV == SKV_KV_INT8 ? a.scale_log2 * s_ks[idx] : a.scale_log2) : 0.f;
+      vsc[i] = okr[i] ? (KV == SKV_KV_INT8 ? s_vs[idx] : 1.f) : 0.f;
+    }
     // Both warps of the pair must agree, or one would wait for the other at
     // the pair barriers below.
     if (!pair_all(pair, mbar_wait(&bars[pair][stage], parity))) {
@@ -404,7 +424,6 @@ __global__ __launch_bounds__(kThreads, 2) void attend_kernel(AttendArgs a) {
     completed = it + 1;
     const unsigned char* kst = pbuf + stage * Gm::STAGE;
     const unsigned char* vst = kst + kTileRows * Gm::KP;
-    const int tbase = (pair + kPairs * it) * kTileRows;  // index of the tile's first row in the split
 
     // ---- partial S = Q K^T over this warp's half of the dims -------------------
     float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
@@ -450,46 +469,37 @@ __global__ __launch_bounds__(kThreads, 2) void attend_kernel(AttendArgs a) {
     }
 
     // ---- online softmax on S[head g][rows 2c, 2c+1, 2c+8, 2c+9] ---------------
-    const int rr[4] = {2 * c, 2 * c + 1, 2 * c + 8, 2 * c + 9};
+    // The reference max m_run of a head moves only when a tile's logits pass
+    // it by more than kLazy (log2 units); then every head takes its exact
+    // running max and the accumulators are rescaled.  Otherwise the tile's
+    // probabilities are exp2(x - m_run) <= 2^kLazy and nothing is rescaled.
+    // Both warps of the pair see bit-identical logits, so they decide alike.
     float x[4] = {s0[0], s0[1], s1[0], s1[1]};
-    float vsc[4];
 #pragma unroll
-    for (int i = 0; i < 4; i++) {
-      const int idx = tbase + rr[i];
-      const bool ok = idx < nr && s_prow[idx] >= 0;
-      if (ok) {
-        float f = a.scale_log2;
-        vsc[i] = 1.f;
-        if (KV == SKV_KV_INT8) {
-          f *= s_ks[idx];
-          vsc[i] = s_vs[idx];
-        }
-        x[i] *= f;
-      } else {
-        x[i] = -INFINITY;
-        vsc[i] = 0.f;
+    for (int i = 0; i < 4; i++) x[i] = okr[i] ? x[i] * fx[i] : -INFINITY;
+    const float lmax = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+    if (__any_sync(0xffffffffu, lmax > m_run + kLazy)) {
+      float tmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, 1));
+      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
+      const float m_new = fmaxf(m_run, tmax);
+      const float alpha = exp2f(m_run - (m_new == -INFINITY ? 0.f : m_new));
+      l_part *= alpha;
+      m_run = m_new;
+      const float a_e = __shfl_sync(0xffffffffu, alpha, 8 * c);
+      const float a_o = __shfl_sync(0xffffffffu, alpha, 8 * c + 4);
+#pragma unroll
+      for (int mt = 0; mt < 8; mt++) {
+        o[mt][0] *= a_e;
+        o[mt][1] *= a_o;
+        o[mt][2] *= a_e;
+        o[mt][3] *= a_o;
       }
     }
-    float tmax = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-    tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
-    tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
-    const float m_new = fmaxf(m_run, tmax);
-    const float m_use = m_new == -INFINITY ? 0.f : m_new;
-    const float alpha = exp2f(m_run - m_use);
+    const float m_use = m_run == -INFINITY ? 0.f : m_run;
     float p[4];
 #pragma unroll
     for (int i = 0; i < 4; i++) p[i] = exp2f(x[i] - m_use);
-    l_part = l_part * alpha + ((p[0] + p[1]) + (p[2] + p[3]));
-    m_run = m_new;
-    const float a_e = __shfl_sync(0xffffffffu, alpha, 8 * c);
-    const float a_o = __shfl_sync(0xffffffffu, alpha, 8 * c + 4);
-#pragma unroll
-    for (int mt = 0; mt < 8; mt++) {
-      o[mt][0] *= a_e;
-      o[mt][1] *= a_o;
-      o[mt][2] *= a_e;
-      o[mt][3] *= a_o;
-    }
+    l_part += (p[0] + p[1]) + (p[2] + p[3]);
 
     // ---- this half of O^T += V^T P^T -----------------------------------------
     // M-tile mt, slot g <-> dim 128e + 16g + 2mt, slot g+8 <-> the next dim.
