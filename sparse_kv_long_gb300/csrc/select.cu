@@ -30,11 +30,11 @@
 //      k-th key K*, how many keys equal to K* are taken, and -- from two
 //      counts per earlier chunk -- where its own picks go; it writes them in
 //      ascending index order (equal keys: lowest index first).
-// int32 scores need two barriers, fp32 scores three.  A barrier is a
-// monotonic arrival counter (release add, acquire poll); the last CTA to
-// leave resets it.  Polls are bounded: a wait that runs out sets
-// SKV_DEV_TIMEOUT and the kernel goes on.  The cooperative launch guarantees
-// that all CTAs are resident together.
+// int32 scores need one barrier and the final poll, fp32 scores two barriers
+// and the poll.  A barrier is a monotonic arrival counter (release add,
+// acquire poll); the last CTA to leave resets it.  Polls are bounded: a wait
+// that runs out sets SKV_DEV_TIMEOUT and the kernel goes on.  The
+// cooperative launch guarantees that all CTAs are resident together.
 #include "fold.cuh"
 #include "score_common.cuh"
 
