@@ -543,6 +543,7 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
     __syncthreads();
     find_digit(hist, nb, need, &s_digit, &s_above, a.status);
     n_match = hist[s_digit];
+    __syncthreads();  // every thread has read the bin before the next pass clears hist
     P = (P << wb) | s_digit;
     need -= s_above;
     rem = shift;

@@ -256,3 +256,67 @@ def test_mla_lru_workload_full_size_layer_step(skv, orc):
     finally:
         torch.cuda.synchronize()
         w.close()
+
+
+def _repeat_selection(launch, idx, cnt, status, reps, check_every=50):
+    """Run launch() reps times; the status word stays 0 and every result
+    equals the first (a selection is deterministic, so any difference is a
+    race between the request's CTAs)."""
+    launch()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    idx0, cnt0 = idx.clone(), cnt.clone()
+    for r in range(reps):
+        launch()
+        if r % check_every == check_every - 1:
+            torch.cuda.synchronize()
+            assert int(status.item()) == 0, f"status {int(status.item())} after {r + 2} launches"
+            assert torch.equal(cnt, cnt0) and torch.equal(idx, idx0), f"result changed after {r + 2} launches"
+
+
+def test_pooled_selection_repeated_launches(skv):
+    """The pooled workload's fused selection (4 x 1,048,576 tokens, 32-bit
+    keys: two barriers and the final poll) launched 600 times on one
+    workspace: no wait runs out and the picks never change.  A missing
+    barrier between the last non-final pass's read of its bin count and the
+    final pass's clearing of the shared histogram made this fail within a
+    few hundred launches."""
+    import bench
+    w = bench.PooledWorkloadGPU(torch, skv, wl, torch.device("cuda", 0), layers=1)
+    try:
+        P = w.P
+
+        def launch():
+            skv.score_select(skv.POOLED_BF16, w.qidx[0], w.pooled[0], w.lengths, P.k_blocks, w.idx, w.cnt, w.tws,
+                             ratio=P.ratio, status=w.status)
+
+        _repeat_selection(launch, w.idx, w.cnt, w.status, 600)
+    finally:
+        torch.cuda.synchronize()
+        w.close()
+
+
+@pytest.mark.parametrize("mode", ["f32", "int4"])
+def test_sketch_selection_repeated_launches(skv, mode):
+    """fp32 sketch keys (three radix passes) and int4 sketch keys (two) over
+    8 requests x 120,000 candidates, 600 launches on one workspace."""
+    B, Tn, width, k = 8, 120_000, 64 if mode == "f32" else 256, 2048
+    g = torch.Generator(device="cuda").manual_seed(11)
+    L = torch.full((B,), Tn, dtype=torch.int32, device="cuda")
+    if mode == "f32":
+        q = torch.randn((B, width), generator=g, device="cuda")
+        keys = torch.randn((B, Tn, width), generator=g, device="cuda")
+        m = skv.SKETCH_F32
+    else:
+        q = torch.randint(-127, 128, (B, width), generator=g, device="cuda", dtype=torch.int32).to(torch.int8)
+        keys = torch.randint(0, 256, (B, Tn, width // 2), generator=g, device="cuda", dtype=torch.int32).to(torch.uint8)
+        m = skv.SKETCH_INT4
+    idx = torch.zeros((B, 64 + k + 1024), dtype=torch.int32, device="cuda")
+    cnt = torch.zeros((B,), dtype=torch.int32, device="cuda")
+    ws = torch.zeros((skv.score_select_workspace_size(B),), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def launch():
+        skv.score_select(m, q, keys, L, k, idx, cnt, ws, S=64, W=1024, status=st)
+
+    _repeat_selection(launch, idx, cnt, st, 600)
