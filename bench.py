@@ -339,6 +339,23 @@ class SketchWorkloadGPU:
         for l in range(self.L):
             self.layer_step(l, stream)
 
+    def io_set(self):
+        """A second set of per-step inputs and outputs (queries, appended
+        K/V, attention outputs) with its own layer-step arguments; everything
+        else (caches, selection, workspaces) is shared."""
+        torch, skv = self.torch, self.skv
+        q, newk, newv = torch.empty_like(self.q), torch.empty_like(self.newk), torch.empty_like(self.newv)
+        out = torch.empty_like(self.out)
+        args = [skv.layer_step_args(q=q[l], new_k=newk[l], new_v=newv[l], lengths=self.lengths, basis=self.U,
+                                    c=self.c, sketch=self.sk[l], k8=self.k8[l], k_scale=self.ks[l], v8=self.v8[l],
+                                    v_scale=self.vs[l], idx=self.idx, count=self.cnt, out=out[l], k=W_K, S=W_S,
+                                    W=W_W, softmax_scale=1 / math.sqrt(W_D)) for l in range(self.L)]
+        return q, newk, newv, out, args
+
+    def step_args(self, args, stream=None):
+        for l in range(self.L):
+            self.skv.decode_layer_step(args[l], self.lws, status=self.status, stream=stream)
+
 
 def run_gpu(args):
     import torch
@@ -437,7 +454,10 @@ def run_gpu(args):
     # ---- end to end through the public API with host buffers ------------------------------
     # Every step: the step's inputs (queries and the appended token's K/V of
     # every layer) copied from pinned host memory, one skv_decode_layer_step
-    # call per layer (eager, no graph), the outputs copied back.
+    # call per layer (eager, no graph), the outputs copied back.  Two sets of
+    # device inputs and outputs alternate, the copies on streams of their
+    # own, so that step s+1's inputs and step s-1's outputs travel while step
+    # s computes; the clock stops after the last step's outputs landed.
     q_host = torch.empty(w.q.shape, dtype=w.q.dtype, pin_memory=True)
     k_host = torch.empty(w.newk.shape, dtype=w.newk.dtype, pin_memory=True)
     v_host = torch.empty(w.newv.shape, dtype=w.newv.dtype, pin_memory=True)
@@ -448,17 +468,36 @@ def run_gpu(args):
     torch.cuda.synchronize()
     h2d = q_host.numel() * 2 + k_host.numel() * 2 + v_host.numel() * 2
     d2h = o_host.numel() * 4
+    sets = [(w.q, w.newk, w.newv, w.out, w.args), w.io_set()]
+    h2d_st, d2h_st = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    inputs_in = [torch.cuda.Event() for _ in sets]   # a set's inputs copied in
+    computed = [torch.cuda.Event() for _ in sets]    # a set's step done (inputs free, outputs written)
+    outputs_out = [torch.cuda.Event() for _ in sets]  # a set's outputs copied out (outputs free)
+    torch.cuda.synchronize()
     barrier()
     t0 = time.perf_counter()
-    for _ in range(args.steps):
-        with torch.cuda.stream(stream):
-            w.q.copy_(q_host, non_blocking=True)
-            w.newk.copy_(k_host, non_blocking=True)
-            w.newv.copy_(v_host, non_blocking=True)
-            w.step(stream)
-            o_host.copy_(w.out, non_blocking=True)
-        stream.synchronize()
+    for s_ in range(args.steps):
+        i = s_ % 2
+        q_d, k_d, v_d, o_d, a_d = sets[i]
+        with torch.cuda.stream(h2d_st):
+            if s_ >= 2:
+                h2d_st.wait_event(computed[i])
+            q_d.copy_(q_host, non_blocking=True)
+            k_d.copy_(k_host, non_blocking=True)
+            v_d.copy_(v_host, non_blocking=True)
+            inputs_in[i].record(h2d_st)
+        stream.wait_event(inputs_in[i])
+        if s_ >= 2:
+            stream.wait_event(outputs_out[i])
+        w.step_args(a_d, stream)
+        computed[i].record(stream)
+        with torch.cuda.stream(d2h_st):
+            d2h_st.wait_event(computed[i])
+            o_host.copy_(o_d, non_blocking=True)
+            outputs_out[i].record(d2h_st)
+    d2h_st.synchronize()
     e2e_s = (time.perf_counter() - t0) / args.steps
+    status |= int(w.status.item())
     barrier()
     e2e_s = max_over_ranks(e2e_s, world, dev)
     e2e_value = job_rate(L, e2e_s, world)
@@ -483,7 +522,9 @@ def run_gpu(args):
                             "bytes_rule": f"{ATTN_BYTES_PER_ROW_HEAD} B per row-head x {W_B} x {MAX_ROWS} x {W_HKV}"},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "path": "per step: pinned host -> device copies of the queries and appended K/V, one eager "
-                        "skv_decode_layer_step C-ABI call per layer, device -> host copy of the outputs"},
+                        "skv_decode_layer_step C-ABI call per layer, device -> host copy of the outputs; two "
+                        "device input/output sets alternate, the copies on their own streams overlapping the "
+                        "neighbouring steps"},
         "gpu_launches": args.steps * L * SketchWorkloadGPU.KERNELS_PER_LAYER,
         "clocks": clk.summary(), "device_status": status,
     }
