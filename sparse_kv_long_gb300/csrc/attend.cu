@@ -253,8 +253,9 @@ __global__ __launch_bounds__(kThreads, 2) void attend_kernel(AttendArgs a) {
   // Rows of the split.  In known-rows mode (a.lengths set) the split takes a
   // slice of the rows every selection contains -- the sinks and the recent
   // tail, found from the request's length -- and a slice of the picks; the
-  // first are staged and attended before waiting for the kernel that writes
-  // the selection (a programmatic dependency), the picks after.  s_prow[i]:
+  // first are staged and their first tiles copied before waiting for the
+  // kernel that writes the selection (a programmatic dependency), the picks
+  // after; then every tile is attended in turn.  s_prow[i]:
   // physical row of split row i (-1: none); known rows take [0, npad), picks
   // start at npad (a whole number of tiles).
   if (threadIdx.x < kPairs * kStages) mbar_init(&bars[threadIdx.x / kStages][threadIdx.x % kStages], 64);
@@ -546,12 +547,10 @@ __global__ __launch_bounds__(kThreads, 2) void attend_kernel(AttendArgs a) {
     return true;
   };
   bool live = true;
-  // ---- phase A: the known rows, before the selection is complete --------------------
-  for (int it = 0; live && it < my_known; it++) {
-    live = attend_tile(it);
-    if (live && issued < my_known && issued < it + 1 + kStages) copy_tile(issued++);
-  }
   // ---- the picks: after the kernel that wrote the selection -------------------------
+  // The known rows' first tiles are already on their way; the picks are
+  // staged before any tile is attended, so that their tiles follow the known
+  // ones through the ring without a drain between the two.
   grid_dependency_wait();
   int np = 0, pos0 = 0;
   if (a.lengths) {
@@ -585,12 +584,11 @@ __global__ __launch_bounds__(kThreads, 2) void attend_kernel(AttendArgs a) {
   const int ntiles = (nr + kTileRows - 1) / kTileRows;
   int my_tiles = 0;
   for (int t = pair; t < ntiles; t += kPairs) my_tiles++;
-  // ---- phase B: the picks ------------------------------------------------------------
-  if (live)
-    while (issued < my_tiles && issued < my_known + kStages) copy_tile(issued++);
+  while (issued < my_tiles && issued < kStages) copy_tile(issued++);
   stage_scales(npad, nr);
   __syncthreads();
-  for (int it = my_known; live && it < my_tiles; it++) {
+  // ---- every tile of the pair: the known rows', then the picks' ----------------------
+  for (int it = 0; live && it < my_tiles; it++) {
     live = attend_tile(it);
     if (live && issued < my_tiles && issued < it + 1 + kStages) copy_tile(issued++);
   }
