@@ -240,7 +240,7 @@ __global__ __launch_bounds__(kThreads, 2) void attend_kernel(AttendArgs a) {
   __shared__ __align__(16) uint16_t s_q[8][D];
   __shared__ __align__(16) float s_x[kPairs][2][32][4];  // partial logits of each warp of a pair
   __shared__ float sm_m[kPairs][8], sm_l[kPairs][8];
-  __shared__ float fin_m[8], fin_l[8];
+  __shared__ float fin_m[8];
   __shared__ float wts[8][kMaxSplit];
   __shared__ int is_last;
 
@@ -660,7 +660,7 @@ __global__ __launch_bounds__(kThreads, 2) void attend_kernel(AttendArgs a) {
   // When they fit in shared memory (the ring is free now), all the splits'
   // partials are copied in at once with 16-byte cp.async (one round of
   // latency); otherwise they are read from global memory (L2) in place.
-  // Weights w[h][s] = exp2(m_s - M) / L are formed once.
+  // Weights w[h][s] = exp2(m_s - M) / L are formed once per head.
   const float* parts = a.part + (static_cast<int64_t>(b) * gy + hy) * a.nsplit * kPart;
   if (static_cast<size_t>(a.nsplit) * kPart * sizeof(float) <= dyn_smem<KV>()) {
     float* sp = reinterpret_cast<float*>(smem);
@@ -669,35 +669,24 @@ __global__ __launch_bounds__(kThreads, 2) void attend_kernel(AttendArgs a) {
     __syncthreads();
     parts = sp;
   }
-  for (int t = threadIdx.x; t < 8 * a.nsplit; t += blockDim.x) {
-    const int hd = t / a.nsplit, s2 = t % a.nsplit;
-    wts[hd][s2] = parts[s2 * kPart + hd];  // m of split s2, head hd
-  }
-  __syncthreads();
-  if (threadIdx.x < 8) {
-    const int hd = threadIdx.x;
-    float M = -INFINITY;
-    for (int s2 = 0; s2 < a.nsplit; s2++) M = fmaxf(M, wts[hd][s2]);
-    fin_m[hd] = M;
-  }
-  __syncthreads();
-  for (int t = threadIdx.x; t < 8 * a.nsplit; t += blockDim.x) {
-    const int hd = t / a.nsplit, s2 = t % a.nsplit;
-    const float M = fin_m[hd];
-    wts[hd][s2] = M == -INFINITY ? 0.f : exp2f(wts[hd][s2] - M);
-  }
-  __syncthreads();
-  if (threadIdx.x < 8) {
-    const int hd = threadIdx.x;
+  // One warp per head (heads hd = warp, warp + kWarps, ...; only the group's
+  // real heads): the splits' maxima and weighted sums reduce across lanes in
+  // a fixed order, and the weights go to shared memory once.
+  for (int hd = warp; hd < 8; hd += kWarps) {
+    if (hg * 8 + hd >= a.G) continue;  // padding head: no output
+    float mx = -INFINITY;
+    for (int s2 = lane; s2 < a.nsplit; s2 += 32) mx = fmaxf(mx, parts[s2 * kPart + hd]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     float L = 0.f;
-    for (int s2 = 0; s2 < a.nsplit; s2++) L += wts[hd][s2] * parts[s2 * kPart + 8 + hd];
-    fin_l[hd] = L;
-  }
-  __syncthreads();
-  for (int t = threadIdx.x; t < 8 * a.nsplit; t += blockDim.x) {
-    const int hd = t / a.nsplit, s2 = t % a.nsplit;
-    const float L = fin_l[hd];
-    wts[hd][s2] = L > 0.f ? wts[hd][s2] / L : 0.f;
+    for (int s2 = lane; s2 < a.nsplit; s2 += 32) {
+      const float w = mx == -INFINITY ? 0.f : exp2f(parts[s2 * kPart + hd] - mx);
+      wts[hd][s2] = w;
+      L += w * parts[s2 * kPart + 8 + hd];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    for (int s2 = lane; s2 < a.nsplit; s2 += 32) wts[hd][s2] = L > 0.f ? wts[hd][s2] / L : 0.f;
   }
   __syncthreads();
   for (int e4 = threadIdx.x; e4 < 8 * D / 4; e4 += blockDim.x) {
