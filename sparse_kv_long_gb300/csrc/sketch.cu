@@ -396,10 +396,34 @@ __global__ __launch_bounds__(kReqThreads, 1) void prepare_req_kernel(
   float* part = X + nv * d;                                        // [ns][nv][64]
   float* qp = part + ns * nv * kRank;                              // [Hkv*64]
   uint16_t* rows = reinterpret_cast<uint16_t*>(qp + Hkv * kRank);  // [nv][d]: K rows, then V rows
-  // Every load first, so that the first-touch latencies overlap.
   int64_t row = 0, sk_row = 0;
+  // One warp encodes appended row r: int8 (K of head r, then V of head
+  // r - Hkv), and with the host tier the token's int4 host row.
+  auto encode_appended = [&](int r) {
+    float rowv[16];
+#pragma unroll
+    for (int i = 0; i < 16; i++) {
+      const int x = lane + 32 * i;
+      rowv[i] = x < d ? bf16_bits_to_f32(rows[r * d + x]) : 0.f;
+    }
+    const int h = r % Hkv;
+    fold::encode_row_warp(rowv, d, (r < Hkv ? k8 : v8) + (row * Hkv + h) * d, (r < Hkv ? ks : vs) + row * Hkv + h);
+    if (ap.host4) {  // the token's int4 host row: head h, K then V
+      const int64_t rb = d / 2 + d / 32;
+      fold::encode_int4_row_warp(rowv, d, ap.host4 + (sk_row * Hkv * 2 + 2 * h + (r < Hkv ? 0 : 1)) * rb);
+    }
+  };
+  // Every load first, so that the first-touch latencies overlap.
   const bool app = fold::append_rows(ap, b, &row, &sk_row);
-  for (int u = t; u < nv * (d / 8); u += blockDim.x) {
+  // When there are enough warps, warp enc_w0 + r copies and later encodes
+  // appended row r while the warps before it combine the folded query.
+  const int enc_w0 = (Hkv * kRank + 31) / 32;
+  const bool overlap = enc_w0 + nv <= static_cast<int>(blockDim.x >> 5);
+  const bool encoder = overlap && warp >= enc_w0 && warp < enc_w0 + nv;
+  const int u0 = overlap ? (encoder ? (warp - enc_w0) * (d / 8) + lane : nv * (d / 8)) : t;
+  const int u1 = overlap ? (encoder ? (warp - enc_w0 + 1) * (d / 8) : 0) : nv * (d / 8);
+  const int ustep = overlap ? 32 : static_cast<int>(blockDim.x);
+  for (int u = u0; u < u1; u += ustep) {
     const int r = u / (d / 8), piece = u - r * (d / 8);
     const uint16_t* src = (r < Hkv ? newk : newv) + (static_cast<int64_t>(b) * Hkv + r % Hkv) * d + 8 * piece;
     asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(
@@ -433,6 +457,11 @@ __global__ __launch_bounds__(kReqThreads, 1) void prepare_req_kernel(
   }
   __syncthreads();
   float amax = 0.f;
+  if (encoder) {  // int8 row r (K of head r, then V of head r - Hkv), beside the query's combination
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncwarp();
+    if (app) encode_appended(warp - enc_w0);
+  }
   for (int m = t; m < Hkv * kRank; m += blockDim.x) {  // folded query of head m/64, dim m%64
     const float v = __fmul_rn(fold::combine_slices(part + m, nv * kRank, ns), c[m]);
     qp[m] = v;
@@ -456,20 +485,7 @@ __global__ __launch_bounds__(kReqThreads, 1) void prepare_req_kernel(
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
     if (t == 0) red[0] = v;
   }
-  for (int r = warp; app && r < nv; r += blockDim.x >> 5) {  // int8 rows: K of head r, then V of head r - Hkv
-    float rowv[16];
-#pragma unroll
-    for (int i = 0; i < 16; i++) {
-      const int x = lane + 32 * i;
-      rowv[i] = x < d ? bf16_bits_to_f32(rows[r * d + x]) : 0.f;
-    }
-    const int h = r % Hkv;
-    fold::encode_row_warp(rowv, d, (r < Hkv ? k8 : v8) + (row * Hkv + h) * d, (r < Hkv ? ks : vs) + row * Hkv + h);
-    if (ap.host4) {  // the token's int4 host row: head h, K then V
-      const int64_t rb = d / 2 + d / 32;
-      fold::encode_int4_row_warp(rowv, d, ap.host4 + (sk_row * Hkv * 2 + 2 * h + (r < Hkv ? 0 : 1)) * rb);
-    }
-  }
+  for (int r = warp; !overlap && app && r < nv; r += blockDim.x >> 5) encode_appended(r);
   __syncthreads();
   const float sigma = __fdiv_rn(red[0], 127.f);
   if (t == 0 && sigma_out) sigma_out[b] = sigma;
