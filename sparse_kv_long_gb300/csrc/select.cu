@@ -802,6 +802,12 @@ __global__ __launch_bounds__(kThreads, 2) void score_select_kernel(Args a, Ws w)
       for (int p = 0; p < pass; p++)
         for (int i = threadIdx.x; i < kBins; i += blockDim.x) w.hist(p, b)[i] = 0u;
     for (int i = threadIdx.x; i < kLastBins; i += blockDim.x) w.fhist(b)[i] = 0u;
+    // Tags repeat every 65,535 launches: when the next launch starts a new
+    // cycle, every record of the request is cleared, so that a record last
+    // written a whole cycle ago (a slot a smaller grid left unused) cannot
+    // pass for one of the next launch.
+    if ((epoch + 1u) % 65535u == 0u)
+      for (int i = threadIdx.x; i < kCMax * kFin; i += blockDim.x) w.fin(b, 0)[i] = 0;
     if (threadIdx.x == 0) {
       w.rng(b)[0] = 0u;
       w.rng(b)[1] = epoch + 1u;

@@ -95,3 +95,47 @@ def test_score_select_workspace_serves_growing_and_shrinking_batches(skv, orc, m
             torch.cuda.synchronize()
             assert int(st.item()) == 0
             _check(T.host(idx), T.host(cnt), ri, rc)
+
+
+# Layout of one request's score + select scratch (words): barrier counters
+# [0, 2), the range word and the launch counter [2, 4), two 8,192-bin
+# histograms, the 256-bin final histogram, then 512 per-CTA records of 260
+# words whose high 16 bits carry the launch's tag (launch counter mod 65,535,
+# plus one).
+_REQ_WORDS = 4 + 2 * 8192 + 256 + 512 * 260
+_EPOCH, _FIN, _FIN_WORDS, _SLOTS = 3, 4 + 2 * 8192 + 256, 260, 512
+
+
+def test_score_select_launch_counter_wrap(skv, orc):
+    """Across the wrap of the records' tag: the launch counter is preset to
+    the last launch of a tag cycle and every record slot holds a stale record
+    carrying the next cycle's first tag.  The launch at the end of the cycle
+    clears the request's records, so the next launch (whose tag equals the
+    stale one) reads only its own; both selections equal the oracle's."""
+    rng = np.random.default_rng(77)
+    B, Tn, k, S, W, width = 4, 30_000, 500, 16, 64, 256
+    q8 = rng.integers(-127, 128, (B, width), dtype=np.int8)
+    sk = rng.integers(0, 256, (B, Tn, width // 2), dtype=np.uint8)
+    L = np.full((B,), Tn, np.int32)
+    sc = orc.index_score(orc.SKETCH_INT4, q8, sk, L, S=S, W=W)
+    ridx, rcnt = orc.topk_select(sc["okey"], L, k, S=S, W=W)
+    ws = torch.zeros((skv.score_select_workspace_size(B),), dtype=torch.uint8, device="cuda")
+    w32 = ws.view(torch.int32)
+    assert w32.numel() >= B * _REQ_WORDS
+    for b in range(B):
+        base = b * _REQ_WORDS
+        w32[base + _EPOCH] = 65533                    # the next launch has the cycle's last tag
+        stale = (1 << 16) | 0x1234                    # the first tag of the next cycle, a bogus count
+        w32[base + _FIN: base + _FIN + _SLOTS * _FIN_WORDS] = stale
+    idx = torch.zeros((B, S + k + W), dtype=torch.int32, device="cuda")
+    cnt = torch.zeros((B,), dtype=torch.int32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    q8d, skd, Ld = T.dev(q8), T.dev(sk), T.dev(L)
+    for launch in range(3):
+        idx.zero_()
+        cnt.zero_()
+        skv.score_select(skv.SKETCH_INT4, q8d, skd, Ld, k, idx, cnt, ws, S=S, W=W, status=st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0, (launch, int(st.item()))
+        _check(T.host(idx), T.host(cnt), ridx, rcnt)
+    assert int(w32[_EPOCH].item()) == 65536
