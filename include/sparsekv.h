@@ -386,7 +386,10 @@ typedef struct skv_layer_step {
  *  3. SKV_HOST_CLOCK: resolve the selection through the hot buffer, fetching
  *     misses from the host tier (skv_resolve_rows_clock);
  *  4. attend over the selected int8 rows (skv_sparse_attend_decode).
- * The result is that of those calls made one after the other.  Every launch
+ * The appended rows and the selection are those of the separate calls made
+ * one after the other; with SKV_RESIDENT the attention takes each split's
+ * share of the sinks and the tail before its share of the picks, so its
+ * output equals theirs up to the order of the floating-point sums.  Every launch
  * goes to `stream`; the call has no host-side decision that depends on
  * device data, so a sequence of layer steps can be captured in a CUDA graph.
  *   workspace  skv_decode_layer_step_workspace_size(a) bytes, zero-filled
